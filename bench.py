@@ -1,0 +1,564 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one pass of the path over one batch: build the slot mapping of
+the step's new tokens, append them to the paged cache (kv_append), then run
+paged_decode over every sequence.  The default workload is the GQA bf16
+decode step (batch 64, 32 q / 8 kv heads, head_dim 128, block 16, contexts
+U{512..4096}); the long-context fp8, 3-bit MHA and mixed prefill+decode
+append workloads are measured in the same run and reported under
+"workloads".
+
+value = algorithmic bytes of the step / device time of the step (GB/s), with
+the inputs resident in HBM and L2 flushed between steps (a 256 MiB write
+outside the timed events).  e2e = the same metric through the public API
+with the step's inputs in pinned host memory, copied in and the output
+copied out inside the timed region.  The CPU oracle is timed on a bounded
+sample of the same workload (cpu_baseline); ``--impl reference`` times the
+oracle alone as the reference arm.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the path has no exchange step); value = total bytes of all ranks /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_tag, src_hash):
+    """dram bytes per launch recorded by an ncu capture (profiles/), if the
+    kernel source has not changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        parts = dict(kv.split("=", 1) for kv in line.strip().split() if "=" in kv)
+        if parts.get("kernel") == kernel_tag and parts.get("src") == src_hash:
+            try:
+                return float(parts["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.15)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.lines = [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def algorithmic_bytes(w, decode=True, append=True):
+    """Bytes the method must move (not the dense pool):
+    decode: sum_b ctx_b * Hkv * (K row + V row + 3-bit metadata) + q + out +
+            block-table entries read + context_lens;
+    append: per real new token Hkv * (2 source rows + 2 cache rows + metadata)
+            + its slot (8 B) and (request, position) (8 B)."""
+    D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
+    row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "u3": 3 * D // 8}[w.cache_kind]
+    meta = 3 if w.cache_kind == "u3" else 0
+    total = 0
+    if decode and w.q is not None:
+        ctx = w.context_lens.to(torch.int64).cpu()
+        total += int(ctx.sum()) * Hkv * 2 * (row + meta)
+        total += 2 * w.q.numel() * 2                       # q in, out
+        total += int(((ctx + BS - 1) // BS).sum()) * 4 + w.batch * 4
+    if append:
+        n_real = int((w.new_pos >= 0).sum())
+        total += n_real * Hkv * 2 * (2 * D + row + meta) + n_real * 16
+    return total
+
+
+def make_workload(name, device):
+    if name == "gqa_bf16":
+        return W.gqa_bf16(device=device)
+    if name == "fp8_long":
+        return W.fp8_long(device=device)
+    if name == "u3_mha":
+        return W.u3_mha(device=device)
+    if name == "mixed_append":
+        return W.mixed_append(device=device)
+    if name == "tiny_fp16":
+        return W.tiny(device=device)
+    raise ValueError(name)
+
+
+class Step:
+    """Device-resident state of one workload and its step."""
+
+    def __init__(self, w, pkv):
+        self.w, self.pkv = w, pkv
+        dev = w.new_req.device
+        self.cache = pkv.KVCache.allocate(
+            w.cache_kind, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, device=dev,
+            k_scale=w.k_scale, v_scale=w.v_scale, fill=0)
+        if w.k_cache0 is not None:
+            self.cache.k_cache.copy_(w.k_cache0)
+            self.cache.v_cache.copy_(w.v_cache0)
+            w.k_cache0 = w.v_cache0 = None      # release the staging copies
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.fill_req is not None:            # context fill (setup, not timed)
+            ch = 1 << 18
+            for i in range(0, w.fill_req.shape[0], ch):
+                sm = pkv.slot_mapping(w.block_tables, w.fill_req[i:i + ch], w.fill_pos[i:i + ch],
+                                      w.block_size, err_flag=self.err)
+                pkv.kv_append(w.k_fill[i:i + ch], w.v_fill[i:i + ch], sm, self.cache,
+                              err_flag=self.err)
+            w.k_fill = w.v_fill = w.fill_req = w.fill_pos = None
+        self.slots = torch.empty(w.new_req.shape[0], dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(w.q) if w.q is not None else None
+        self.ws = None
+        self.launches = 2
+        if w.q is not None:
+            n = pkv.decode_workspace_bytes(w.q, self.cache, w.block_tables)
+            self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+            self.launches += 2 if n > 0 else 1
+        torch.cuda.synchronize()
+
+    def append(self, req=None, pos=None, k=None, v=None):
+        w, pkv = self.w, self.pkv
+        pkv.slot_mapping(w.block_tables, w.new_req if req is None else req,
+                         w.new_pos if pos is None else pos, w.block_size, out=self.slots,
+                         err_flag=self.err)
+        pkv.kv_append(w.k_new if k is None else k, w.v_new if v is None else v, self.slots,
+                      self.cache, err_flag=self.err)
+
+    def decode(self, q=None):
+        w = self.w
+        if w.q is None:
+            return
+        self.pkv.paged_decode(w.q if q is None else q, self.cache, w.block_tables,
+                              w.context_lens, sm_scale=w.sm_scale, out=self.out,
+                              workspace=self.ws, err_flag=self.err)
+
+    def run(self):
+        self.append()
+        self.decode()
+
+
+def time_steps(step, steps, warmup, flush, sub=False):
+    """Per-step CUDA-event times (ms) of `steps` steps after `warmup`, L2
+    flushed before each; with sub=True also the decode call alone."""
+    for _ in range(warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, m, b in ev:
+        flush.zero_()
+        a.record()
+        step.append()
+        m.record()
+        step.decode()
+        b.record()
+    torch.cuda.synchronize()
+    tot = [a.elapsed_time(b) for a, m, b in ev]
+    dec = [m.elapsed_time(b) for a, m, b in ev]
+    app = [a.elapsed_time(m) for a, m, b in ev]
+    return tot, app, dec
+
+
+# ---------------------------------------------------------------- oracle arms
+
+class OracleArm:
+    """The CPU oracle on a bounded sample of a workload: the first sequences
+    whose decode fits in about ``budget_s`` seconds on the host cores.  The
+    sample's caches are built once (untimed); a timed step is the oracle's
+    append of the step's new tokens for those sequences plus their decode
+    (all heads)."""
+
+    def __init__(self, w_host, orc, budget_s=15.0, nthreads=None):
+        from tests import pipeline as PL
+        self.PL, self.w, self.orc = PL, w_host, orc
+        self.nthreads = orc.max_threads() if nthreads is None else nthreads
+        w = w_host
+        if w.q is None:                     # append-only workload
+            self.seqs = list(range(w.batch))
+        else:
+            # rate probe: one sequence, 16-bit reading of its cost
+            ctx = w.context_lens.to(torch.int64).numpy()
+            probe = [int(np.argmin(ctx))]
+            c = PL.oracle_caches(w, orc, seqs=probe)
+            pairs = np.arange(probe[0] * w.num_heads, (probe[0] + 1) * w.num_heads,
+                              dtype=np.int32)
+            t0 = time.perf_counter()
+            PL.oracle_decode(w, orc, c, pairs=pairs, nthreads=self.nthreads)
+            rate = ctx[probe[0]] / max(1e-6, time.perf_counter() - t0)   # tokens/s, all heads
+            budget_tokens = rate * budget_s
+            self.seqs, acc = [], 0
+            for b in range(w.batch):
+                if self.seqs and acc + ctx[b] > budget_tokens:
+                    break
+                self.seqs.append(b)
+                acc += int(ctx[b])
+        self.cache = PL.oracle_caches(w, orc, seqs=self.seqs)
+        self.pairs = None
+        if w.q is not None:
+            self.pairs = np.concatenate([np.arange(b * w.num_heads, (b + 1) * w.num_heads)
+                                         for b in self.seqs]).astype(np.int32)
+        self.bytes = self._bytes()
+
+    def _bytes(self):
+        w = self.w
+        D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
+        row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "u3": 3 * D // 8}[w.cache_kind]
+        meta = 3 if w.cache_kind == "u3" else 0
+        req = w.new_req.numpy()
+        sel = np.isin(req, self.seqs) & (w.new_pos.numpy() >= 0)
+        n = int(sel.sum())
+        total = n * Hkv * 2 * (2 * D + row + meta) + 16 * n
+        if w.q is not None:
+            for b in self.seqs:
+                ctx = int(w.context_lens[b])
+                total += ctx * Hkv * 2 * (row + meta) + 4 * w.num_heads * D
+                total += (ctx + BS - 1) // BS * 4 + 4
+        return total
+
+    def step(self):
+        w, PL, orc = self.w, self.PL, self.orc
+        t0 = time.perf_counter()
+        req = w.new_req.numpy()
+        idx = np.nonzero(np.isin(req, self.seqs) & (w.new_pos.numpy() >= 0))[0]
+        slots = orc.build_slot_mapping(w.block_tables.numpy(), req[idx], w.new_pos.numpy()[idx],
+                                       w.block_size)
+        c = self.cache
+        ti = torch.from_numpy(idx)
+        orc.kv_append(PL.KIND_CODE_ORACLE[w.cache_kind], PL.src_code(w),
+                      W.bits16(w.k_new[ti]), W.bits16(w.v_new[ti]), slots, c["k_cache"],
+                      c["v_cache"], None if w.k_scale is None else w.k_scale.numpy(),
+                      None if w.v_scale is None else w.v_scale.numpy(), c.get("k_qscale"),
+                      c.get("k_qzero"), c.get("v_qscale"), c.get("v_qzero"))
+        if w.q is not None:
+            PL.oracle_decode(w, orc, c, pairs=self.pairs, nthreads=self.nthreads)
+        return self.bytes, time.perf_counter() - t0
+
+    def describe(self, seconds):
+        w = self.w
+        what = ("append of the step's tokens + decode (all heads) of %d/%d sequences"
+                % (len(self.seqs), w.batch)) if w.q is not None else (
+            "append of all %d tokens" % w.new_req.shape[0])
+        return "%s, %d threads, %.2f s per sample" % (what, self.nthreads, seconds)
+
+
+# ---------------------------------------------------------------- main
+
+def run_reference(args, ws, rank):
+    """The reference arm: the CPU oracle, timed as it stands."""
+    if rank != 0:
+        return 0
+    import oracle as orc
+    orc.build()
+    w = make_workload(args.workload, "cpu")
+    per_step = max(1.0, min(15.0, 120.0 / max(1, args.steps + args.warmup)))
+    arm = OracleArm(w, orc, budget_s=per_step)
+    times, nbytes_all = [], []
+    for i in range(args.warmup + args.steps):
+        nb, sec = arm.step()
+        if i >= args.warmup:
+            times.append(sec)
+            nbytes_all.append(nb)
+    threads, desc = arm.nthreads, arm.describe(float(np.mean(times)))
+    value = sum(nbytes_all) / sum(times) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "device": "host cores"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "paged-decode effective HBM GB/s (% of GB300 peak); KV append tokens/s"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa_bf16")
+    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append",
+                    help="other workloads measured in the same run ('' for none)")
+    ap.add_argument("--extra-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import paged_kv_cache_num_gb300 as pkv
+    pkv.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    peak, peak_src = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # ---------------- main workload, device-timed
+    w = make_workload(args.workload, dev)
+    step_bytes = algorithmic_bytes(w)
+    dec_bytes = algorithmic_bytes(w, append=False)
+    app_bytes = algorithmic_bytes(w, decode=False)
+    n_real = int((w.new_pos >= 0).sum())
+    st = Step(w, pkv)
+    for _ in range(args.warmup):
+        flush.zero_()
+        st.run()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        tot, app, dec = time_steps(st, args.steps, 0, flush)
+        wall = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = float(np.mean(tot))
+    ms_t = torch.tensor([ms], device=dev)
+    if pg:
+        pg.all_reduce(ms_t, op=pg.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = ws * step_bytes / (ms_max * 1e-3) / 1e9
+    dec_ms = float(np.mean(dec))
+    app_ms = float(np.mean(app))
+    assert int(st.err.item()) == 0, "device error flag %d" % int(st.err.item())
+
+    # ---------------- e2e through the public API with host buffers
+    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "new_req",
+                                                          "new_pos", "block_tables",
+                                                          "context_lens")}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_t = []
+    s = torch.cuda.current_stream()
+    for i in range(args.e2e_steps + 3):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        pkv.slot_mapping(dbuf["block_tables"], dbuf["new_req"], dbuf["new_pos"], w.block_size,
+                         out=st.slots, err_flag=st.err)
+        pkv.kv_append(dbuf["k_new"], dbuf["v_new"], st.slots, st.cache, err_flag=st.err)
+        pkv.paged_decode(dbuf["q"], st.cache, dbuf["block_tables"], dbuf["context_lens"],
+                         sm_scale=w.sm_scale, out=st.out, workspace=st.ws, err_flag=st.err)
+        out_host.copy_(st.out, non_blocking=True)
+        s.synchronize()
+        if i >= 3:
+            e2e_t.append(time.perf_counter() - t0)
+    e2e_ms = 1e3 * float(np.mean(e2e_t))
+    e2e_val = step_bytes / (e2e_ms * 1e-3) / 1e9
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_val = ws * step_bytes / (float(t.item()) * 1e-3) / 1e9
+
+    # ---------------- roofline of the dominant operation (paged_decode)
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    src = source_hash("paged_kv_cache_num_gb300/csrc/decode.cu")
+    traffic = profile_traffic("paged_decode:" + args.workload, src)
+    roofline = {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
+                "measured" else "fallback 6.8 TB/s",
+                "kernel": "paged_decode (decode kernel + split-K merge, one C-ABI call)",
+                "algorithmic_bytes_per_launch": dec_bytes}
+
+    # copy-kernel yardstick (1 GiB each way)
+    a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        pkv.copy_peak(a, b)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        pkv.copy_peak(a, b)
+    e1.record()
+    torch.cuda.synchronize()
+    copy_gbs = 2 * a.numel() * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del a, b
+
+    # ---------------- other workloads (device-timed, same protocol)
+    extra = {}
+    launches_per_step = st.launches
+    del st
+    torch.cuda.empty_cache()
+    for name in [x for x in args.extra.split(",") if x]:
+        wx = make_workload(name, dev)
+        sb = algorithmic_bytes(wx)
+        db = algorithmic_bytes(wx, append=False)
+        ab = algorithmic_bytes(wx, decode=False)
+        nr = int((wx.new_pos >= 0).sum())
+        sx = Step(wx, pkv)
+        tt, aa, dd = time_steps(sx, args.extra_steps, max(3, args.warmup // 4), flush)
+        assert int(sx.err.item()) == 0, name
+        e = {"step_ms": round(float(np.mean(tt)), 4),
+             "append_tokens_per_s": round(nr / (float(np.mean(aa)) * 1e-3), 1),
+             "append_gbs": round(ab / (float(np.mean(aa)) * 1e-3) / 1e9, 1)}
+        if wx.q is not None:
+            g = db / (float(np.mean(dd)) * 1e-3) / 1e9
+            e.update({"decode_ms": round(float(np.mean(dd)), 4), "decode_gbs": round(g, 1),
+                      "decode_frac_of_peak": round(g / peak, 4),
+                      "decode_algorithmic_bytes": db})
+        extra[name] = e
+        del sx, wx
+        torch.cuda.empty_cache()
+
+    # ---------------- CPU oracle on a bounded sample
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        wh = make_workload(args.workload, "cpu")
+        arm = OracleArm(wh, orc, budget_s=15.0)
+        nb, sec = arm.step()
+        cpu = {"value": round(nb / sec / 1e9, 4), "unit": "GB/s", "cores": arm.nthreads,
+               "kind": "oracle", "sample": arm.describe(sec)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3", "u3": "u3"}[w.cache_kind],
+            "data": "synthetic (seeded torch CUDA generator; N(0,1) K/V/q)",
+            "config": {"workload": args.workload, "batch": w.batch, "num_heads": w.num_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "block_size": w.block_size, "context": "U{512..4096}",
+                       "new_tokens": n_real, "parallelism": "replicas" if ws > 1 else "single",
+                       "l2": "flushed between steps (256 MiB write outside the timed events)"},
+            "pct_of_peak": round(100 * value / peak, 2),
+            "decode_gbs": round(dec_gbs, 1), "decode_ms": round(dec_ms, 5),
+            "append_tokens_per_s": round(n_real / (app_ms * 1e-3), 1),
+            "append_ms": round(app_ms, 5),
+            "step_algorithmic_bytes": step_bytes,
+            "roofline": roofline,
+            "copy_kernel_gbs": round(copy_gbs, 1),
+            "clocks": clk.summary(),
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "cpu_baseline": cpu,
+            "workloads": extra,
+            "timed_wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,433 @@
+// pkv_api.cu -- the extern "C" entry points declared in include/pkv.h:
+// argument validation, plan selection and dispatch to the kernel launchers.
+// Nothing here touches tensor data; every step of the path runs in kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok()
+{
+    g_err[0] = '\0';
+    return PKV_OK;
+}
+
+int elem_size(int dtype)
+{
+    switch (dtype) {
+    case PKV_DTYPE_F16:
+    case PKV_DTYPE_BF16: return 2;
+    case PKV_DTYPE_E4M3:
+    case PKV_DTYPE_U3:
+    case PKV_DTYPE_U8: return 1;
+    case PKV_DTYPE_I32:
+    case PKV_DTYPE_F32: return 4;
+    case PKV_DTYPE_I64: return 8;
+    default: return 0;
+    }
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2i(int64_t x)
+{
+    int s = 0;
+    while ((int64_t(1) << s) < x) ++s;
+    return s;
+}
+
+int check_tensor(const pkv_tensor *t, const char *name, int ndim)
+{
+    if (!t) return fail(PKV_ERR_NULL, "%s: descriptor is NULL", name);
+    if (t->ndim != ndim) return fail(PKV_ERR_SHAPE, "%s: expected %d dims, got %d", name, ndim, t->ndim);
+    if (elem_size(t->dtype) == 0) return fail(PKV_ERR_DTYPE, "%s: unknown dtype %d", name, t->dtype);
+    int64_t numel = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (t->shape[i] < 0) return fail(PKV_ERR_SHAPE, "%s: negative extent", name);
+        numel *= t->shape[i];
+    }
+    if (numel > 0 && !t->data) return fail(PKV_ERR_NULL, "%s: data pointer is NULL", name);
+    return PKV_OK;
+}
+
+#define TRY(x)                  \
+    do {                        \
+        int _rc = (x);          \
+        if (_rc != PKV_OK) return _rc; \
+    } while (0)
+
+struct CacheInfo {
+    int kind;
+    int64_t num_blocks, block_size, num_kv_heads, head_dim;
+};
+
+// Validate a pkv_cache; head_dim comes from the row length and the dtype.
+int check_cache(const pkv_cache *c, CacheInfo &ci)
+{
+    if (!c) return fail(PKV_ERR_NULL, "cache: descriptor is NULL");
+    TRY(check_tensor(&c->k_cache, "k_cache", 4));
+    TRY(check_tensor(&c->v_cache, "v_cache", 4));
+    const pkv_tensor &k = c->k_cache, &v = c->v_cache;
+    if (k.dtype != v.dtype) return fail(PKV_ERR_DTYPE, "k_cache and v_cache dtypes differ");
+    const int kind = k.dtype;
+    if (kind != PKV_DTYPE_F16 && kind != PKV_DTYPE_BF16 && kind != PKV_DTYPE_E4M3 && kind != PKV_DTYPE_U3)
+        return fail(PKV_ERR_DTYPE, "cache dtype %d is not F16, BF16, E4M3 or U3", kind);
+    for (int i = 0; i < 4; ++i) {
+        if (k.shape[i] != v.shape[i]) return fail(PKV_ERR_SHAPE, "k_cache and v_cache shapes differ");
+        if (k.stride[i] != v.stride[i]) return fail(PKV_ERR_LAYOUT, "k_cache and v_cache strides differ");
+    }
+    if (k.stride[3] != 1) return fail(PKV_ERR_LAYOUT, "cache rows must be contiguous (last stride 1)");
+    const int es = elem_size(kind);
+    // 16-bit and e4m3 rows are whole 16-byte units; packed 3-bit rows
+    // (3*head_dim/8 bytes) only need 16-byte aligned blocks
+    for (int i = 0; i < (kind == PKV_DTYPE_U3 ? 1 : 3); ++i)
+        if ((k.stride[i] * es) % 16 != 0)
+            return fail(PKV_ERR_LAYOUT, "cache stride %d is not a multiple of 16 bytes", i);
+    if (!aligned(k.data, 16) || !aligned(v.data, 16))
+        return fail(PKV_ERR_LAYOUT, "cache base pointers must be 16-byte aligned");
+    ci.kind = kind;
+    ci.num_blocks = k.shape[0];
+    ci.block_size = k.shape[1];
+    ci.num_kv_heads = k.shape[2];
+    ci.head_dim = kind == PKV_DTYPE_U3 ? k.shape[3] * 8 / 3 : k.shape[3];
+    if (kind == PKV_DTYPE_U3 && k.shape[3] * 8 != ci.head_dim * 3)
+        return fail(PKV_ERR_SHAPE, "U3 cache row of %lld bytes is not 3*head_dim/8", (long long)k.shape[3]);
+    if (!is_pow2(ci.block_size) || ci.block_size > 256)
+        return fail(PKV_ERR_UNSUPPORTED, "block_size %lld must be a power of two <= 256",
+                    (long long)ci.block_size);
+    if (ci.num_blocks * ci.block_size > (int64_t(1) << 31))
+        return fail(PKV_ERR_UNSUPPORTED, "pool of more than 2^31 slots");
+    if (kind == PKV_DTYPE_E4M3 && (!c->k_scale || !c->v_scale))
+        return fail(PKV_ERR_NULL, "E4M3 cache needs k_scale and v_scale");
+    if (kind == PKV_DTYPE_U3) {
+        TRY(check_tensor(&c->k_qscale, "k_qscale", 3));
+        TRY(check_tensor(&c->k_qzero, "k_qzero", 3));
+        TRY(check_tensor(&c->v_qscale, "v_qscale", 3));
+        TRY(check_tensor(&c->v_qzero, "v_qzero", 3));
+        if (c->k_qscale.dtype != PKV_DTYPE_F16 || c->v_qscale.dtype != PKV_DTYPE_F16)
+            return fail(PKV_ERR_DTYPE, "U3 scales must be F16");
+        if (c->k_qzero.dtype != PKV_DTYPE_U8 || c->v_qzero.dtype != PKV_DTYPE_U8)
+            return fail(PKV_ERR_DTYPE, "U3 zeros must be U8");
+        for (int i = 0; i < 3; ++i) {
+            const int64_t want = k.shape[i];
+            if (c->k_qscale.shape[i] != want || c->v_qscale.shape[i] != want ||
+                c->k_qzero.shape[i] != want || c->v_qzero.shape[i] != want)
+                return fail(PKV_ERR_SHAPE, "U3 metadata must be [num_blocks, block_size, num_kv_heads]");
+            if (c->k_qscale.stride[i] != c->v_qscale.stride[i] || c->k_qzero.stride[i] != c->v_qzero.stride[i])
+                return fail(PKV_ERR_LAYOUT, "K and V metadata strides differ");
+        }
+    }
+    return PKV_OK;
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int launch_status(cudaError_t e, const char *what)
+{
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+
+namespace pkv {
+int sm_count_current_device()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+}  // namespace pkv
+
+extern "C" {
+
+const char *pkv_version(void) { return "pkv 0.1.0 (sm_103a)"; }
+int pkv_abi_version(void) { return PKV_ABI_VERSION; }
+const char *pkv_last_error(void) { return g_err; }
+
+int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, const pkv_tensor *pos,
+                     int block_size, const pkv_tensor *slot_mapping, int32_t *err_flag, void *stream)
+{
+    TRY(check_tensor(block_tables, "block_tables", 2));
+    TRY(check_tensor(req, "req", 1));
+    TRY(check_tensor(pos, "pos", 1));
+    TRY(check_tensor(slot_mapping, "slot_mapping", 1));
+    if (block_tables->dtype != PKV_DTYPE_I32 || req->dtype != PKV_DTYPE_I32 || pos->dtype != PKV_DTYPE_I32)
+        return fail(PKV_ERR_DTYPE, "block_tables, req and pos must be I32");
+    if (slot_mapping->dtype != PKV_DTYPE_I64) return fail(PKV_ERR_DTYPE, "slot_mapping must be I64");
+    const int64_t n = req->shape[0];
+    if (pos->shape[0] != n || slot_mapping->shape[0] != n)
+        return fail(PKV_ERR_SHAPE, "req, pos and slot_mapping lengths differ");
+    if (slot_mapping->stride[0] != 1 && n > 1) return fail(PKV_ERR_LAYOUT, "slot_mapping must be contiguous");
+    if (!is_pow2(block_size)) return fail(PKV_ERR_VALUE, "block_size must be a power of two");
+    pkv::SlotMapParams p{};
+    p.bt = static_cast<const int32_t *>(block_tables->data);
+    p.bt_b = block_tables->stride[0];
+    p.bt_j = block_tables->stride[1];
+    p.batch = int(block_tables->shape[0]);
+    p.max_blocks = int(block_tables->shape[1]);
+    p.req = static_cast<const int32_t *>(req->data);
+    p.req_stride = req->stride[0];
+    p.pos = static_cast<const int32_t *>(pos->data);
+    p.pos_stride = pos->stride[0];
+    p.n = n;
+    p.block_shift = log2i(block_size);
+    p.slot_mapping = static_cast<int64_t *>(slot_mapping->data);
+    p.err_flag = err_flag;
+    return launch_status(pkv::launch_slot_mapping(p, as_stream(stream)), "slot_mapping kernel");
+}
+
+int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *slot_mapping,
+                  const pkv_cache *cache, int32_t *err_flag, void *stream)
+{
+    TRY(check_tensor(k_new, "k_new", 3));
+    TRY(check_tensor(v_new, "v_new", 3));
+    TRY(check_tensor(slot_mapping, "slot_mapping", 1));
+    CacheInfo ci{};
+    TRY(check_cache(cache, ci));
+    if (k_new->dtype != v_new->dtype) return fail(PKV_ERR_DTYPE, "k_new and v_new dtypes differ");
+    const int src = k_new->dtype;
+    if (src != PKV_DTYPE_F16 && src != PKV_DTYPE_BF16) return fail(PKV_ERR_DTYPE, "k_new must be F16 or BF16");
+    if (slot_mapping->dtype != PKV_DTYPE_I64) return fail(PKV_ERR_DTYPE, "slot_mapping must be I64");
+    for (int i = 0; i < 3; ++i)
+        if (k_new->shape[i] != v_new->shape[i]) return fail(PKV_ERR_SHAPE, "k_new and v_new shapes differ");
+    const int64_t T = k_new->shape[0];
+    if (slot_mapping->shape[0] != T) return fail(PKV_ERR_SHAPE, "slot_mapping has %lld entries, k_new %lld tokens",
+                                                 (long long)slot_mapping->shape[0], (long long)T);
+    if (k_new->shape[1] != ci.num_kv_heads) return fail(PKV_ERR_SHAPE, "k_new has %lld heads, cache %lld",
+                                                        (long long)k_new->shape[1], (long long)ci.num_kv_heads);
+    if (k_new->shape[2] != ci.head_dim) return fail(PKV_ERR_SHAPE, "k_new head_dim %lld, cache %lld",
+                                                    (long long)k_new->shape[2], (long long)ci.head_dim);
+    if (k_new->stride[2] != 1 || v_new->stride[2] != 1) return fail(PKV_ERR_LAYOUT, "head_dim of k_new/v_new must be contiguous");
+    if ((ci.kind == PKV_DTYPE_F16 || ci.kind == PKV_DTYPE_BF16) && ci.kind != src)
+        return fail(PKV_ERR_DTYPE, "16-bit cache dtype must equal the source dtype");
+    if (ci.kind == PKV_DTYPE_E4M3 && ci.head_dim % 8 != 0) return fail(PKV_ERR_UNSUPPORTED, "E4M3 append needs head_dim % 8 == 0");
+    if (ci.kind == PKV_DTYPE_U3 && ci.head_dim != 64 && ci.head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "U3 append supports head_dim 64 and 128");
+    const int64_t es = 2;
+    const bool vec16 = aligned(k_new->data, 16) && aligned(v_new->data, 16) &&
+                       (k_new->stride[0] * es) % 16 == 0 && (k_new->stride[1] * es) % 16 == 0 &&
+                       (v_new->stride[0] * es) % 16 == 0 && (v_new->stride[1] * es) % 16 == 0 &&
+                       (ci.head_dim * 2) % 16 == 0;
+    pkv::AppendParams p{};
+    p.k_new = static_cast<const char *>(k_new->data);
+    p.v_new = static_cast<const char *>(v_new->data);
+    p.k_src_tok = k_new->stride[0] * es;
+    p.k_src_head = k_new->stride[1] * es;
+    p.v_src_tok = v_new->stride[0] * es;
+    p.v_src_head = v_new->stride[1] * es;
+    p.slot_mapping = static_cast<const int64_t *>(slot_mapping->data);
+    p.slot_stride = slot_mapping->stride[0];
+    p.k_cache = static_cast<char *>(cache->k_cache.data);
+    p.v_cache = static_cast<char *>(cache->v_cache.data);
+    const int ces = elem_size(ci.kind);
+    p.c_blk = cache->k_cache.stride[0] * ces;
+    p.c_slot = cache->k_cache.stride[1] * ces;
+    p.c_head = cache->k_cache.stride[2] * ces;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
+    if (ci.kind == PKV_DTYPE_U3) {
+        p.k_qs = static_cast<uint16_t *>(cache->k_qscale.data);
+        p.v_qs = static_cast<uint16_t *>(cache->v_qscale.data);
+        p.k_qz = static_cast<uint8_t *>(cache->k_qzero.data);
+        p.v_qz = static_cast<uint8_t *>(cache->v_qzero.data);
+        p.m_blk = cache->k_qscale.stride[0];
+        p.m_slot = cache->k_qscale.stride[1];
+        p.m_head = cache->k_qscale.stride[2];
+        p.z_blk = cache->k_qzero.stride[0];
+        p.z_slot = cache->k_qzero.stride[1];
+        p.z_head = cache->k_qzero.stride[2];
+    }
+    p.num_tokens = T;
+    p.num_kv_heads = int(ci.num_kv_heads);
+    p.head_dim = int(ci.head_dim);
+    p.block_shift = log2i(ci.block_size);
+    p.num_slots = ci.num_blocks * ci.block_size;
+    p.src_kind = src;
+    p.err_flag = err_flag;
+    return launch_status(pkv::launch_append(p, ci.kind, vec16, as_stream(stream)), "kv_append kernel");
+}
+
+namespace {
+
+struct DecodeCheck {
+    CacheInfo ci;
+    int64_t batch, num_heads, max_blocks;
+    pkv::DecodePlan plan;
+};
+
+int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
+                        int num_splits, DecodeCheck &dc)
+{
+    TRY(check_tensor(q, "q", 3));
+    TRY(check_cache(cache, dc.ci));
+    TRY(check_tensor(block_tables, "block_tables", 2));
+    if (q->dtype != PKV_DTYPE_F16 && q->dtype != PKV_DTYPE_BF16) return fail(PKV_ERR_DTYPE, "q must be F16 or BF16");
+    if ((dc.ci.kind == PKV_DTYPE_F16 || dc.ci.kind == PKV_DTYPE_BF16) && dc.ci.kind != q->dtype)
+        return fail(PKV_ERR_DTYPE, "16-bit cache dtype must equal q's dtype");
+    if (block_tables->dtype != PKV_DTYPE_I32) return fail(PKV_ERR_DTYPE, "block_tables must be I32");
+    dc.batch = q->shape[0];
+    dc.num_heads = q->shape[1];
+    if (q->shape[2] != dc.ci.head_dim) return fail(PKV_ERR_SHAPE, "q head_dim %lld, cache %lld",
+                                                   (long long)q->shape[2], (long long)dc.ci.head_dim);
+    if (dc.ci.head_dim != 64 && dc.ci.head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (q->stride[2] != 1) return fail(PKV_ERR_LAYOUT, "q head_dim must be contiguous");
+    if (dc.ci.num_kv_heads <= 0 || dc.num_heads % dc.ci.num_kv_heads != 0)
+        return fail(PKV_ERR_SHAPE, "num_heads %lld not a multiple of num_kv_heads %lld",
+                    (long long)dc.num_heads, (long long)dc.ci.num_kv_heads);
+    if (dc.num_heads / dc.ci.num_kv_heads > 16) return fail(PKV_ERR_UNSUPPORTED, "group of more than 16 q heads");
+    if (block_tables->shape[0] != dc.batch) return fail(PKV_ERR_SHAPE, "block_tables has %lld rows, batch %lld",
+                                                        (long long)block_tables->shape[0], (long long)dc.batch);
+    dc.max_blocks = block_tables->shape[1];
+    if (num_splits < 0) return fail(PKV_ERR_VALUE, "num_splits must be >= 0");
+    dc.plan = pkv::plan_decode(int(dc.batch), int(dc.num_heads), int(dc.ci.num_kv_heads), int(dc.ci.head_dim),
+                               int(dc.ci.block_size), int(dc.max_blocks), dc.ci.kind, num_splits,
+                               pkv::sm_count_current_device());
+    return PKV_OK;
+}
+
+}  // namespace
+
+int pkv_paged_decode_workspace(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
+                               int num_splits, size_t *bytes)
+{
+    if (!bytes) return fail(PKV_ERR_NULL, "bytes is NULL");
+    DecodeCheck dc{};
+    TRY(check_decode_common(q, cache, block_tables, num_splits, dc));
+    *bytes = dc.plan.workspace_bytes;
+    return ok();
+}
+
+int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
+                     const pkv_tensor *context_lens, float sm_scale, const pkv_tensor *out, int num_splits,
+                     void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream)
+{
+    DecodeCheck dc{};
+    TRY(check_decode_common(q, cache, block_tables, num_splits, dc));
+    TRY(check_tensor(context_lens, "context_lens", 1));
+    TRY(check_tensor(out, "out", 3));
+    if (context_lens->dtype != PKV_DTYPE_I32) return fail(PKV_ERR_DTYPE, "context_lens must be I32");
+    if (context_lens->shape[0] != dc.batch) return fail(PKV_ERR_SHAPE, "context_lens length differs from batch");
+    if (out->dtype != q->dtype) return fail(PKV_ERR_DTYPE, "out dtype must equal q dtype");
+    for (int i = 0; i < 3; ++i)
+        if (out->shape[i] != q->shape[i]) return fail(PKV_ERR_SHAPE, "out shape must equal q shape");
+    if (out->stride[2] != 1) return fail(PKV_ERR_LAYOUT, "out head_dim must be contiguous");
+    if (!std::isfinite(sm_scale)) return fail(PKV_ERR_VALUE, "sm_scale must be finite");
+    const pkv::DecodePlan &pl = dc.plan;
+    if (pl.workspace_bytes > 0) {
+        if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", pl.workspace_bytes);
+        if (workspace_bytes < pl.workspace_bytes)
+            return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes given, %zu required", workspace_bytes,
+                        pl.workspace_bytes);
+        if (!aligned(workspace, 16)) return fail(PKV_ERR_LAYOUT, "workspace must be 16-byte aligned");
+    }
+    const CacheInfo &ci = dc.ci;
+    pkv::DecodeParams p{};
+    p.q = static_cast<const char *>(q->data);
+    p.q_b = q->stride[0] * 2;
+    p.q_h = q->stride[1] * 2;
+    p.k_cache = static_cast<const char *>(cache->k_cache.data);
+    p.v_cache = static_cast<const char *>(cache->v_cache.data);
+    const int ces = elem_size(ci.kind);
+    p.c_blk = cache->k_cache.stride[0] * ces;
+    p.c_slot = cache->k_cache.stride[1] * ces;
+    p.c_head = cache->k_cache.stride[2] * ces;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
+    if (ci.kind == PKV_DTYPE_U3) {
+        p.k_qs = static_cast<const uint16_t *>(cache->k_qscale.data);
+        p.v_qs = static_cast<const uint16_t *>(cache->v_qscale.data);
+        p.k_qz = static_cast<const uint8_t *>(cache->k_qzero.data);
+        p.v_qz = static_cast<const uint8_t *>(cache->v_qzero.data);
+        p.m_blk = cache->k_qscale.stride[0];
+        p.m_slot = cache->k_qscale.stride[1];
+        p.m_head = cache->k_qscale.stride[2];
+        p.z_blk = cache->k_qzero.stride[0];
+        p.z_slot = cache->k_qzero.stride[1];
+        p.z_head = cache->k_qzero.stride[2];
+    }
+    p.block_tables = static_cast<const int32_t *>(block_tables->data);
+    p.bt_b = block_tables->stride[0];
+    p.bt_j = block_tables->stride[1];
+    p.context_lens = static_cast<const int32_t *>(context_lens->data);
+    p.cl_stride = context_lens->stride[0];
+    p.out = static_cast<char *>(out->data);
+    p.o_b = out->stride[0] * 2;
+    p.o_h = out->stride[1] * 2;
+    p.batch = int(dc.batch);
+    p.num_heads = int(dc.num_heads);
+    p.num_kv_heads = int(ci.num_kv_heads);
+    p.group = int(dc.num_heads / ci.num_kv_heads);
+    p.head_dim = int(ci.head_dim);
+    p.block_size = int(ci.block_size);
+    p.block_shift = log2i(ci.block_size);
+    p.max_blocks = int(dc.max_blocks);
+    p.num_blocks = int(ci.num_blocks);
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.num_splits = pl.num_splits;
+    p.chunk_tokens = pl.chunk_tokens;
+    if (pl.num_splits > 1) {
+        p.part_acc = static_cast<float *>(workspace);
+        p.part_ml = p.part_acc + size_t(dc.batch) * dc.num_heads * pl.num_splits * ci.head_dim;
+    }
+    p.err_flag = err_flag;
+    return launch_status(pkv::launch_decode(p, ci.kind, q->dtype, as_stream(stream)), "paged_decode kernels");
+}
+
+int pkv_pack3(const uint8_t *values, uint8_t *packed, int64_t n_octets, void *stream)
+{
+    if (n_octets < 0) return fail(PKV_ERR_VALUE, "n_octets < 0");
+    if (n_octets > 0 && (!values || !packed)) return fail(PKV_ERR_NULL, "NULL pointer");
+    if (!aligned(values, 16) || !aligned(packed, 4)) return fail(PKV_ERR_LAYOUT, "values must be 16-byte and packed 4-byte aligned");
+    return launch_status(pkv::launch_pack3(values, packed, n_octets, as_stream(stream)), "pack3 kernel");
+}
+
+int pkv_unpack3(const uint8_t *packed, uint8_t *values, int64_t n_octets, void *stream)
+{
+    if (n_octets < 0) return fail(PKV_ERR_VALUE, "n_octets < 0");
+    if (n_octets > 0 && (!values || !packed)) return fail(PKV_ERR_NULL, "NULL pointer");
+    if (!aligned(values, 16) || !aligned(packed, 4)) return fail(PKV_ERR_LAYOUT, "values must be 16-byte and packed 4-byte aligned");
+    return launch_status(pkv::launch_unpack3(packed, values, n_octets, as_stream(stream)), "unpack3 kernel");
+}
+
+int pkv_unpack3_words(const uint32_t *words, uint8_t *values, int64_t n_groups, void *stream)
+{
+    if (n_groups < 0) return fail(PKV_ERR_VALUE, "n_groups < 0");
+    if (n_groups > 0 && (!values || !words)) return fail(PKV_ERR_NULL, "NULL pointer");
+    if (!aligned(values, 16) || !aligned(words, 4)) return fail(PKV_ERR_LAYOUT, "values must be 16-byte and words 4-byte aligned");
+    return launch_status(pkv::launch_unpack3_words(words, values, n_groups, as_stream(stream)), "unpack3_words kernel");
+}
+
+int pkv_copy_peak(const void *src, void *dst, size_t bytes, void *stream)
+{
+    if (bytes % 16 != 0) return fail(PKV_ERR_VALUE, "bytes must be a multiple of 16");
+    if (bytes > 0 && (!src || !dst)) return fail(PKV_ERR_NULL, "NULL pointer");
+    if (!aligned(src, 16) || !aligned(dst, 16)) return fail(PKV_ERR_LAYOUT, "pointers must be 16-byte aligned");
+    return launch_status(pkv::launch_copy_peak(src, dst, bytes, as_stream(stream)), "copy kernel");
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// pkv_internal.h -- launch parameters shared by the C-ABI layer and the
+// kernel translation units (host + device visible, no torch types).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+enum CacheKind : int { kF16 = 1, kBF16 = 2, kE4M3 = 3, kU3 = 4 };
+
+// ---------------------------------------------------------------- append
+struct AppendParams {
+    const char *k_new;          // source rows (bytes)
+    const char *v_new;
+    int64_t k_src_tok, k_src_head;  // byte strides
+    int64_t v_src_tok, v_src_head;
+    const int64_t *slot_mapping;
+    int64_t slot_stride;        // elements
+    char *k_cache;
+    char *v_cache;
+    int64_t c_blk, c_slot, c_head;  // byte strides of K and V caches (equal)
+    // fp8
+    const float *k_scale;
+    const float *v_scale;
+    // 3-bit metadata (element strides, same for the four arrays)
+    uint16_t *k_qs;
+    uint8_t *k_qz;
+    uint16_t *v_qs;
+    uint8_t *v_qz;
+    int64_t m_blk, m_slot, m_head;      // strides of the fp16 scale arrays (elements)
+    int64_t z_blk, z_slot, z_head;      // strides of the zero arrays (bytes)
+    int64_t num_tokens;
+    int num_kv_heads;
+    int head_dim;
+    int block_shift;            // log2(block_size)
+    int64_t num_slots;          // num_blocks * block_size
+    int src_kind;               // kF16 / kBF16
+    int32_t *err_flag;
+};
+
+cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cudaStream_t s);
+
+struct SlotMapParams {
+    const int32_t *bt;
+    int64_t bt_b, bt_j;
+    int batch, max_blocks;
+    const int32_t *req;
+    int64_t req_stride;
+    const int32_t *pos;
+    int64_t pos_stride;
+    int64_t n;
+    int block_shift;
+    int64_t *slot_mapping;
+    int32_t *err_flag;
+};
+cudaError_t launch_slot_mapping(const SlotMapParams &p, cudaStream_t s);
+
+// ---------------------------------------------------------------- decode
+struct DecodeParams {
+    const char *q;              // [B, Hq, D] 16-bit
+    int64_t q_b, q_h;           // byte strides
+    const char *k_cache;
+    const char *v_cache;
+    int64_t c_blk, c_slot, c_head;  // byte strides (K and V equal)
+    const float *k_scale;
+    const float *v_scale;
+    const uint16_t *k_qs;
+    const uint8_t *k_qz;
+    const uint16_t *v_qs;
+    const uint8_t *v_qz;
+    int64_t m_blk, m_slot, m_head;  // fp16 scale strides (elements)
+    int64_t z_blk, z_slot, z_head;  // zero strides (bytes)
+    const int32_t *block_tables;
+    int64_t bt_b, bt_j;         // element strides
+    const int32_t *context_lens;
+    int64_t cl_stride;
+    char *out;                  // [B, Hq, D] 16-bit
+    int64_t o_b, o_h;           // byte strides
+    int batch, num_heads, num_kv_heads, group, head_dim, block_size, block_shift;
+    int max_blocks;
+    int num_blocks;
+    float scale_log2;           // sm_scale * log2(e)
+    int num_splits;             // chunks per sequence (1 = write out directly)
+    int chunk_tokens;           // tokens per chunk (multiple of block_size)
+    float *part_acc;            // [B, Hq, num_splits, D]   (num_splits > 1)
+    float *part_ml;             // [B, Hq, num_splits, 2]  (max in log2 units, sum)
+    int32_t *err_flag;
+};
+
+struct DecodePlan {
+    int num_splits;
+    int chunk_tokens;
+    size_t workspace_bytes;
+};
+
+DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       int max_blocks, int cache_kind, int num_splits, int sm_count);
+
+cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cudaStream_t s);
+
+// ---------------------------------------------------------------- pack3 / copy
+cudaError_t launch_pack3(const uint8_t *values, uint8_t *packed, int64_t n, cudaStream_t s);
+cudaError_t launch_unpack3(const uint8_t *packed, uint8_t *values, int64_t n, cudaStream_t s);
+cudaError_t launch_unpack3_words(const uint32_t *words, uint8_t *values, int64_t n,
+                                 cudaStream_t s);
+cudaError_t launch_copy_peak(const void *src, void *dst, size_t bytes, cudaStream_t s);
+
+int sm_count_current_device();
+
+}  // namespace pkv

@@ -1,0 +1,297 @@
+"""Python binding of the C ABI in include/pkv.h (ctypes; argument marshalling
+only).  Every operation runs in the CUDA kernels of libpkv.so; there is no
+fallback: if the library is not built or a call fails, an exception is
+raised.  PyTorch provides the device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+# dtype codes (pkv.h)
+F16, BF16, E4M3, U3, U8, I32, I64, F32 = 1, 2, 3, 4, 5, 6, 7, 8
+# device error bits
+DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE, DEVERR_POS_RANGE, DEVERR_TIMEOUT = (
+    1, 2, 4, 8, 16)
+
+_TORCH_CODES = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3,
+                torch.uint8: U8, torch.int32: I32, torch.int64: I64, torch.float32: F32}
+
+
+class PkvError(RuntimeError):
+    """A non-OK status from the library (message from pkv_last_error)."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__("pkv error %d: %s" % (code, msg))
+        self.code = code
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("k_cache", _Tensor), ("v_cache", _Tensor), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("k_qscale", _Tensor), ("k_qzero", _Tensor),
+                ("v_qscale", _Tensor), ("v_qzero", _Tensor)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded libpkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError("libpkv.so is not built (%s); run "
+                                  "paged_kv_cache_num_gb300.build.build()" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.c_void_p
+            TP = ctypes.POINTER(_Tensor)
+            CP = ctypes.POINTER(_Cache)
+            L.pkv_version.restype = ctypes.c_char_p
+            L.pkv_last_error.restype = ctypes.c_char_p
+            L.pkv_abi_version.restype = ctypes.c_int
+            L.pkv_slot_mapping.argtypes = [TP, TP, TP, ctypes.c_int, TP, P, P]
+            L.pkv_kv_append.argtypes = [TP, TP, TP, CP, P, P]
+            L.pkv_paged_decode_workspace.argtypes = [TP, CP, TP, ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+            L.pkv_paged_decode.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP, ctypes.c_int, P,
+                                           ctypes.c_size_t, P, P]
+            L.pkv_pack3.argtypes = [P, P, ctypes.c_int64, P]
+            L.pkv_unpack3.argtypes = [P, P, ctypes.c_int64, P]
+            L.pkv_unpack3_words.argtypes = [P, P, ctypes.c_int64, P]
+            L.pkv_copy_peak.argtypes = [P, P, ctypes.c_size_t, P]
+            for fn in ("pkv_slot_mapping", "pkv_kv_append", "pkv_paged_decode_workspace",
+                       "pkv_paged_decode", "pkv_pack3", "pkv_unpack3", "pkv_unpack3_words",
+                       "pkv_copy_peak"):
+                getattr(L, fn).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise PkvError(rc, lib().pkv_last_error().decode())
+
+
+def _desc(t: Optional[torch.Tensor], code: Optional[int] = None) -> _Tensor:
+    d = _Tensor()
+    if t is None:
+        return d
+    if t.dim() > 4:
+        raise ValueError("at most 4 dims")
+    d.data = t.data_ptr() if t.numel() > 0 else 0
+    d.dtype = _TORCH_CODES[t.dtype] if code is None else code
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+
+
+@dataclass
+class KVCache:
+    """A paged KV cache [num_blocks, block_size, num_kv_heads, row] in device
+    memory.  kind: "f16", "bf16", "e4m3" (+ per-kv-head fp32 scales) or "u3"
+    (3-bit codes, row = 3*head_dim/8 bytes, + fp16 scale / uint8 zero per
+    (slot, head))."""
+    kind: str
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+    k_qscale: Optional[torch.Tensor] = None
+    k_qzero: Optional[torch.Tensor] = None
+    v_qscale: Optional[torch.Tensor] = None
+    v_qzero: Optional[torch.Tensor] = None
+
+    @property
+    def num_blocks(self):
+        return self.k_cache.shape[0]
+
+    @property
+    def block_size(self):
+        return self.k_cache.shape[1]
+
+    @property
+    def num_kv_heads(self):
+        return self.k_cache.shape[2]
+
+    @property
+    def head_dim(self):
+        r = self.k_cache.shape[3]
+        return r * 8 // 3 if self.kind == "u3" else r
+
+    @staticmethod
+    def allocate(kind: str, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                 device="cuda", k_scale=None, v_scale=None, fill=None) -> "KVCache":
+        shape = (num_blocks, block_size, num_kv_heads)
+        if kind in ("f16", "bf16"):
+            dt = torch.float16 if kind == "f16" else torch.bfloat16
+            k = torch.empty(shape + (head_dim,), dtype=dt, device=device)
+            v = torch.empty_like(k)
+            c = KVCache(kind, k, v)
+        elif kind == "e4m3":
+            k = torch.empty(shape + (head_dim,), dtype=torch.uint8, device=device)
+            v = torch.empty_like(k)
+            c = KVCache(kind, k, v, k_scale=k_scale, v_scale=v_scale)
+        elif kind == "u3":
+            k = torch.empty(shape + (3 * head_dim // 8,), dtype=torch.uint8, device=device)
+            v = torch.empty_like(k)
+            c = KVCache(kind, k, v,
+                        k_qscale=torch.empty(shape, dtype=torch.float16, device=device),
+                        k_qzero=torch.empty(shape, dtype=torch.uint8, device=device),
+                        v_qscale=torch.empty(shape, dtype=torch.float16, device=device),
+                        v_qzero=torch.empty(shape, dtype=torch.uint8, device=device))
+        else:
+            raise ValueError(kind)
+        if fill is not None:
+            for t in (c.k_cache, c.v_cache, c.k_qscale, c.k_qzero, c.v_qscale, c.v_qzero):
+                if t is not None:
+                    t.view(torch.uint8).fill_(fill)
+        return c
+
+    def _struct(self) -> _Cache:
+        s = _Cache()
+        code = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "u3": U3}[self.kind]
+        s.k_cache = _desc(self.k_cache, code)
+        s.v_cache = _desc(self.v_cache, code)
+        if self.kind == "e4m3":
+            if self.k_scale is None or self.v_scale is None:
+                raise ValueError("e4m3 cache needs k_scale / v_scale")
+            s.k_scale = self.k_scale.data_ptr()
+            s.v_scale = self.v_scale.data_ptr()
+        if self.kind == "u3":
+            s.k_qscale = _desc(self.k_qscale, F16)
+            s.k_qzero = _desc(self.k_qzero, U8)
+            s.v_qscale = _desc(self.v_qscale, F16)
+            s.v_qzero = _desc(self.v_qzero, U8)
+        return s
+
+    def tensors(self):
+        return [t for t in (self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.k_qscale,
+                            self.k_qzero, self.v_qscale, self.v_qzero) if t is not None]
+
+
+def version() -> str:
+    return lib().pkv_version().decode()
+
+
+def slot_mapping(block_tables, req, pos, block_size: int, out=None, err_flag=None, stream=None):
+    """slot = block_tables[req][pos // bs] * bs + pos % bs (pos < 0 -> -1), on the GPU."""
+    _need_cuda(block_tables, req, pos)
+    if out is None:
+        out = torch.empty(req.shape[0], dtype=torch.int64, device=req.device)
+    _check(lib().pkv_slot_mapping(ctypes.byref(_desc(block_tables)), ctypes.byref(_desc(req)),
+                                  ctypes.byref(_desc(pos)), int(block_size),
+                                  ctypes.byref(_desc(out)), _ptr(err_flag), _stream(stream)))
+    return out
+
+
+def kv_append(k_new, v_new, slot_mapping, cache: KVCache, err_flag=None, stream=None):
+    """Scatter new K/V rows [T, Hkv, D] into the cache through slot_mapping."""
+    _need_cuda(k_new, v_new, slot_mapping, *cache.tensors())
+    cs = cache._struct()
+    _check(lib().pkv_kv_append(ctypes.byref(_desc(k_new)), ctypes.byref(_desc(v_new)),
+                               ctypes.byref(_desc(slot_mapping)), ctypes.byref(cs),
+                               _ptr(err_flag), _stream(stream)))
+
+
+def decode_workspace_bytes(q, cache: KVCache, block_tables, num_splits: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    cs = cache._struct()
+    _check(lib().pkv_paged_decode_workspace(ctypes.byref(_desc(q)), ctypes.byref(cs),
+                                            ctypes.byref(_desc(block_tables)), int(num_splits),
+                                            ctypes.byref(n)))
+    return int(n.value)
+
+
+def paged_decode(q, cache: KVCache, block_tables, context_lens, sm_scale: Optional[float] = None,
+                 out=None, num_splits: int = 0, workspace=None, err_flag=None, stream=None):
+    """softmax(sm_scale * q . K^T) V over each sequence's paged context."""
+    _need_cuda(q, block_tables, context_lens, *cache.tensors())
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+    if out is None:
+        out = torch.empty_like(q)
+    cs = cache._struct()
+    need = decode_workspace_bytes(q, cache, block_tables, num_splits)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
+    ws_n = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_decode(ctypes.byref(_desc(q)), ctypes.byref(cs),
+                                  ctypes.byref(_desc(block_tables)),
+                                  ctypes.byref(_desc(context_lens)), float(sm_scale),
+                                  ctypes.byref(_desc(out)), int(num_splits), ws_ptr, ws_n,
+                                  _ptr(err_flag), _stream(stream)))
+    return out
+
+
+def pack3(values, packed=None, stream=None):
+    """uint8 [n*8] codes -> uint8 [n*3] packed bytes."""
+    _need_cuda(values)
+    n = values.numel() // 8
+    if packed is None:
+        packed = torch.empty(n * 3, dtype=torch.uint8, device=values.device)
+    _check(lib().pkv_pack3(_ptr(values), _ptr(packed), n, _stream(stream)))
+    return packed
+
+
+def unpack3(packed, values=None, stream=None):
+    """uint8 [n*3] packed bytes -> uint8 [n*8] codes."""
+    _need_cuda(packed)
+    n = packed.numel() // 3
+    if values is None:
+        values = torch.empty(n * 8, dtype=torch.uint8, device=packed.device)
+    _check(lib().pkv_unpack3(_ptr(packed), _ptr(values), n, _stream(stream)))
+    return values
+
+
+def unpack3_words(words, values=None, stream=None):
+    """int32/uint32 words [m*3] (same bytes as packed octets) -> uint8 [m*32]."""
+    _need_cuda(words)
+    m = words.numel() // 3
+    if values is None:
+        values = torch.empty(m * 32, dtype=torch.uint8, device=words.device)
+    _check(lib().pkv_unpack3_words(_ptr(words), _ptr(values), m, _stream(stream)))
+    return values
+
+
+def copy_peak(src, dst, stream=None):
+    """16-byte vectorised copy of src's bytes into dst (bandwidth yardstick)."""
+    _need_cuda(src, dst)
+    nbytes = src.numel() * src.element_size()
+    _check(lib().pkv_copy_peak(_ptr(src), _ptr(dst), nbytes, _stream(stream)))

@@ -1,0 +1,172 @@
+"""GPU parity of kv_append (16-bit copy, fp8 e4m3, 3-bit) and of the device
+slot_mapping builder with the oracle: bit exact over the whole pool,
+including the untouched blocks and the -1 padding tokens."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import pipeline as PL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_cache_num_gb300 as P
+    P.lib()
+    return P
+
+
+def _assert_pools_equal(gpu, orc_c):
+    for name, arr in orc_c.items():
+        assert np.array_equal(gpu[name], arr), name
+
+
+def test_slot_mapping_kernel(pkv, orc):
+    w = W.mixed_append(n_prefill=4, n_decode=20, prefill_lo=10, prefill_hi=300, ctx_lo=5,
+                       ctx_hi=700, pad_to=256)
+    bt = w.block_tables
+    got = pkv.slot_mapping(bt.cuda(), w.new_req.cuda(), w.new_pos.cuda(), w.block_size)
+    torch.cuda.synchronize()
+    exp = orc.build_slot_mapping(bt.numpy(), w.new_req.numpy(), w.new_pos.numpy(), w.block_size)
+    assert np.array_equal(got.cpu().numpy(), exp)
+
+
+def test_slot_mapping_out_of_table_flags(pkv):
+    bt = torch.zeros((2, 3), dtype=torch.int32, device="cuda")
+    req = torch.tensor([0, 1, 5, 0], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([3, 48, 0, -1], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pkv.slot_mapping(bt, req, pos, 16, err_flag=err)
+    torch.cuda.synchronize()
+    assert got.tolist() == [3, -1, -1, -1]
+    assert int(err.item()) & pkv.pkv.DEVERR_POS_RANGE
+
+
+@pytest.mark.parametrize("literal", [False, True])
+def test_tiny_append(pkv, orc, literal):
+    w = W.tiny(literal=literal)
+    cache, _ = PL.gpu_run(w, pkv, decode=False)
+    _assert_pools_equal(PL.gpu_cache_host(cache), PL.oracle_caches(w, orc))
+
+
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_mixed_prefill_decode_append(pkv, orc, size):
+    if size == "small":
+        w = W.mixed_append(n_prefill=3, n_decode=10, prefill_lo=20, prefill_hi=200, ctx_lo=30,
+                           ctx_hi=400)
+    else:
+        w = W.mixed_append()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache, _ = PL.gpu_run(w, pkv, decode=False, err_flag=err)
+    assert int(err.item()) == 0
+    _assert_pools_equal(PL.gpu_cache_host(cache), PL.oracle_caches(w, orc))
+    assert w.new_pos.numpy()[-1] == -1          # padding present
+
+
+def test_strided_source_rows(pkv, orc):
+    """K and V sliced out of a fused [T, 3, Hkv, D] projection output."""
+    w = W.gqa_bf16(batch=5, ctx_lo=3, ctx_hi=100, seed=21)
+    T, H, D = w.k_new.shape
+    fused = torch.randn((T, 3, H, D), dtype=w.dtype)
+    fused[:, 1] = w.k_new
+    fused[:, 2] = w.v_new
+    cache = pkv.KVCache.allocate("bf16", w.num_blocks, w.block_size, H, D)
+    cache.k_cache.copy_(w.k_cache0.cuda())
+    cache.v_cache.copy_(w.v_cache0.cuda())
+    fd = fused.cuda()
+    sm = pkv.slot_mapping(w.block_tables.cuda(), w.new_req.cuda(), w.new_pos.cuda(), w.block_size)
+    pkv.kv_append(fd[:, 1], fd[:, 2], sm, cache)
+    torch.cuda.synchronize()
+    _assert_pools_equal(PL.gpu_cache_host(cache), PL.oracle_caches(w, orc))
+
+
+def test_unaligned_source_uses_scalar_path(pkv, orc):
+    w = W.tiny()
+    T, H, D = w.k_new.shape
+    buf = torch.empty(T * H * D + 1, dtype=w.dtype, device="cuda")
+    k = buf[1:].view(T, H, D)
+    k.copy_(w.k_new.cuda())
+    cache = pkv.KVCache.allocate("f16", w.num_blocks, w.block_size, H, D)
+    cache.k_cache.copy_(w.k_cache0.cuda())
+    cache.v_cache.copy_(w.v_cache0.cuda())
+    sm = pkv.slot_mapping(w.block_tables.cuda(), w.new_req.cuda(), w.new_pos.cuda(), w.block_size)
+    pkv.kv_append(k, w.v_new.cuda(), sm, cache)
+    torch.cuda.synchronize()
+    _assert_pools_equal(PL.gpu_cache_host(cache), PL.oracle_caches(w, orc))
+
+
+def test_out_of_range_slot_is_skipped_and_flagged(pkv):
+    H, D, P, BS = 2, 64, 4, 16
+    cache = pkv.KVCache.allocate("f16", P, BS, H, D, fill=0)
+    kn = torch.ones((3, H, D), dtype=torch.float16, device="cuda")
+    sm = torch.tensor([5, P * BS, -1], dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.kv_append(kn, kn, sm, cache, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.pkv.DEVERR_SLOT_RANGE
+    flat = cache.k_cache.view(P * BS, H, D)
+    assert torch.all(flat[5] == 1) and int((flat != 0).sum()) == H * D
+
+
+def test_idempotent_append(pkv):
+    w = W.tiny()
+    cache, _ = PL.gpu_run(w, pkv, decode=False)
+    before = PL.gpu_cache_host(cache)
+    sm = pkv.slot_mapping(w.block_tables.cuda(), w.new_req.cuda(), w.new_pos.cuda(), w.block_size)
+    pkv.kv_append(w.k_new.cuda(), w.v_new.cuda(), sm, cache)
+    torch.cuda.synchronize()
+    after = PL.gpu_cache_host(cache)
+    for k in before:
+        assert np.array_equal(before[k], after[k])
+
+
+@pytest.mark.parametrize("src", [torch.bfloat16, torch.float16])
+def test_e4m3_every_source_pattern(pkv, orc, src):
+    """All 2^16 source bit patterns (NaN, inf, subnormal, overflow included)
+    through the fp8 append for several scales: bit exact with the oracle."""
+    H, D, BS = 4, 128, 16
+    pats = torch.arange(1 << 16, dtype=torch.int32).to(torch.int16).view(src)
+    T = (1 << 16) // D                        # 512 tokens, one head row each x 4 heads
+    kn = pats.reshape(T, 1, D).repeat(1, H, 1)
+    vn = pats.flip(0).reshape(T, 1, D).repeat(1, H, 1)
+    P = T // BS
+    k_scale = torch.tensor([1.0, 1e-3, 37.5, 2.0 ** -20], dtype=torch.float32)
+    v_scale = torch.tensor([0.5, 3e4, 1.0 / 3.0, 448.0], dtype=torch.float32)
+    cache = pkv.KVCache.allocate("e4m3", P, BS, H, D, k_scale=k_scale.cuda(),
+                                 v_scale=v_scale.cuda(), fill=0)
+    slots = torch.randperm(P * BS, generator=torch.Generator().manual_seed(3))[:T]
+    pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache)
+    torch.cuda.synchronize()
+    kc = np.zeros((P, BS, H, D), np.uint8)
+    vc = np.zeros((P, BS, H, D), np.uint8)
+    code = 1 if src == torch.float16 else 2
+    orc.kv_append(3, code, W.bits16(kn), W.bits16(vn), slots.numpy(), kc, vc, k_scale.numpy(),
+                  v_scale.numpy())
+    assert np.array_equal(cache.k_cache.cpu().numpy(), kc)
+    assert np.array_equal(cache.v_cache.cpu().numpy(), vc)
+
+
+@pytest.mark.parametrize("D,src", [(128, torch.float16), (64, torch.float16),
+                                   (128, torch.bfloat16)])
+def test_u3_append_bit_exact(pkv, orc, D, src):
+    H, BS, P, T = 3, 16, 40, 500
+    g = torch.Generator().manual_seed(D)
+    kn = torch.randn((T, H, D), generator=g).to(src)
+    vn = (torch.randn((T, H, D), generator=g) * 50).to(src)
+    kn[7] = 1.25                                   # constant rows: scale 0
+    kn[8, 1, :5] = -2.0                            # ties / repeated extremes
+    slots = torch.randperm(P * BS, generator=g)[:T]
+    slots[[0, 99]] = -1
+    cache = pkv.KVCache.allocate("u3", P, BS, H, D, fill=0)
+    pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache)
+    torch.cuda.synchronize()
+    RB = 3 * D // 8
+    c = {"k_cache": np.zeros((P, BS, H, RB), np.uint8), "v_cache": np.zeros((P, BS, H, RB), np.uint8),
+         "k_qscale": np.zeros((P, BS, H), np.uint16), "v_qscale": np.zeros((P, BS, H), np.uint16),
+         "k_qzero": np.zeros((P, BS, H), np.uint8), "v_qzero": np.zeros((P, BS, H), np.uint8)}
+    code = 1 if src == torch.float16 else 2
+    orc.kv_append(4, code, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
+                  None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
+    _assert_pools_equal(PL.gpu_cache_host(cache), c)

@@ -1,0 +1,211 @@
+"""GPU parity of paged_decode with the fp64 oracle (max-abs 4e-3 for fp16
+outputs, 2e-2 for bf16 outputs), for 16-bit, fp8 and 3-bit caches, with and
+without the split-K merge, on small cases that span several blocks and a
+ragged tail, on the full-size workloads (sampled rows), and on the edge
+cases: empty and one-token contexts, poisoned slots beyond the context,
+permuted blocks, out-of-range table data."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import pipeline as PL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_cache_num_gb300 as P
+    P.lib()
+    return P
+
+
+def _check(w, got, ref, pairs=None):
+    g = PL.out_f64(got)
+    if pairs is not None:
+        g = g.reshape(-1, w.head_dim)[pairs]
+        ref = ref.reshape(-1, w.head_dim)[pairs]
+    assert np.isfinite(g).all()
+    err = np.max(np.abs(g - ref))
+    assert err <= PL.tolerance(w), err
+    return err
+
+
+@pytest.mark.parametrize("literal", [False, True])
+def test_tiny_fp16(pkv, orc, literal):
+    w = W.tiny(literal=literal)
+    _, out = PL.gpu_run(w, pkv)
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    _check(w, out, ref)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3, 8])
+def test_gqa_bf16_small(pkv, orc, splits):
+    w = W.gqa_bf16(batch=6, ctx_lo=1, ctx_hi=700, seed=31)
+    _, out = PL.gpu_run(w, pkv, num_splits=splits)
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    _check(w, out, ref)
+
+
+@pytest.mark.parametrize("G,BS,D", [(1, 16, 128), (2, 32, 64), (8, 16, 128), (16, 8, 64),
+                                    (4, 64, 128), (3, 16, 64)])
+def test_group_block_dim_matrix(pkv, orc, G, BS, D):
+    w = W.gqa_bf16(batch=3, ctx_lo=1, ctx_hi=9 * BS + 5, num_heads=2 * G, num_kv_heads=2,
+                   head_dim=D, block_size=BS, seed=40 + G * BS + D)
+    for splits in (1, 4):
+        _, out = PL.gpu_run(w, pkv, num_splits=splits)
+        ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+        _check(w, out, ref)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 5])
+def test_fp8_small(pkv, orc, splits):
+    w = W.fp8_long(batch=4, ctx_lo=100, ctx_hi=2000, calib_tokens=256, seed=32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache, out = PL.gpu_run(w, pkv, num_splits=splits, err_flag=err)
+    assert int(err.item()) == 0
+    oc = PL.oracle_caches(w, orc)
+    gc = PL.gpu_cache_host(cache)
+    for k in oc:
+        assert np.array_equal(gc[k], oc[k]), k
+    _check(w, out, PL.oracle_decode(w, orc, oc))
+
+
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_u3_small(pkv, orc, splits):
+    w = W.u3_mha(batch=4, ctx_lo=20, ctx_hi=900, num_heads=8, seed=33)
+    cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+    oc = PL.oracle_caches(w, orc)
+    gc = PL.gpu_cache_host(cache)
+    for k in oc:
+        assert np.array_equal(gc[k], oc[k]), k
+    _check(w, out, PL.oracle_decode(w, orc, oc))
+
+
+def test_u3_head_dim_64(pkv, orc):
+    w = W.u3_mha(batch=3, ctx_lo=5, ctx_hi=300, num_heads=4, head_dim=64, seed=34)
+    cache, out = PL.gpu_run(w, pkv)
+    oc = PL.oracle_caches(w, orc)
+    _check(w, out, PL.oracle_decode(w, orc, oc))
+
+
+def test_split_count_invariance(pkv):
+    w = W.gqa_bf16(batch=4, ctx_lo=50, ctx_hi=3000, seed=35)
+    outs = [PL.out_f64(PL.gpu_run(w, pkv, num_splits=s)[1]) for s in (1, 2, 7, 16)]
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) <= 2e-2
+
+
+def test_empty_and_single_token_contexts(pkv, orc):
+    w = W.gqa_bf16(batch=4, ctx_lo=1, ctx_hi=300, seed=36)
+    w.context_lens[0] = 0
+    w.context_lens[1] = 1
+    # keep the appended token inside the context of every sequence
+    w.new_pos[:] = torch.clamp(w.context_lens - 1, min=0)
+    w.new_pos[0] = -1
+    for splits in (1, 3):
+        _, out = PL.gpu_run(w, pkv, num_splits=splits)
+        ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+        _check(w, out, ref)
+        assert torch.all(out[0] == 0)
+
+
+def test_poison_beyond_context(pkv, orc):
+    """NaN in every slot outside the live contexts (the tail of the last block
+    included) leaves the output finite and equal to the clean run."""
+    w = W.gqa_bf16(batch=5, ctx_lo=17, ctx_hi=500, seed=37)
+    live = torch.zeros((w.num_blocks, w.block_size), dtype=torch.bool)
+    for b in range(w.batch):
+        for t in range(int(w.context_lens[b])):
+            live[int(w.block_tables[b, t // w.block_size]), t % w.block_size] = True
+    dead = (~live).cuda()
+
+    def poison(cache):
+        cache.k_cache[dead] = float("nan")
+        cache.v_cache[dead] = float("nan")
+
+    for splits in (1, 4):
+        _, clean = PL.gpu_run(w, pkv, num_splits=splits)
+        _, dirty = PL.gpu_run(w, pkv, num_splits=splits, poison=poison)
+        assert torch.isfinite(dirty.float()).all()
+        assert torch.equal(clean, dirty)
+
+
+def test_block_permutation_invariance(pkv):
+    w = W.gqa_bf16(batch=3, ctx_lo=30, ctx_hi=400, seed=38)
+    _, base = PL.gpu_run(w, pkv)
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1))
+    k2 = torch.empty_like(w.k_cache0)
+    v2 = torch.empty_like(w.v_cache0)
+    k2[perm] = w.k_cache0
+    v2[perm] = w.v_cache0
+    w.k_cache0, w.v_cache0 = k2, v2
+    w.block_tables = perm.to(torch.int32)[w.block_tables.long()]
+    _, moved = PL.gpu_run(w, pkv)
+    assert torch.equal(base, moved)
+
+
+def test_bad_table_data_is_flagged_not_faulting(pkv):
+    w = W.gqa_bf16(batch=3, ctx_lo=30, ctx_hi=60, seed=39)
+    w.block_tables[1, 0] = w.num_blocks + 7
+    w.block_tables[2, 1] = -3
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w.new_pos[1:] = -1          # no appends through the broken rows
+    PL.gpu_run(w, pkv, err_flag=err)
+    assert int(err.item()) & pkv.pkv.DEVERR_BLOCK_RANGE
+    w2 = W.gqa_bf16(batch=2, ctx_lo=30, ctx_hi=60, seed=39)
+    w2.context_lens[0] = 10 ** 6
+    w2.new_pos[:] = -1
+    err.zero_()
+    PL.gpu_run(w2, pkv, err_flag=err)
+    assert int(err.item()) & pkv.pkv.DEVERR_CONTEXT_RANGE
+
+
+# ---------------------------------------------------------------- full-size
+
+def _sample_pairs(w, seqs, heads_per_seq=None):
+    pairs = []
+    for b in seqs:
+        hs = range(w.num_heads) if heads_per_seq is None else heads_per_seq
+        pairs += [b * w.num_heads + h for h in hs]
+    return np.array(pairs, np.int32)
+
+
+def test_full_gqa_bf16(pkv, orc):
+    """Full-size GQA bf16 workload (batch 64, contexts 512..4096): every
+    output row against the oracle."""
+    w = W.gqa_bf16()
+    _, out = PL.gpu_run(w, pkv)
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    _check(w, out, ref)
+
+
+def test_full_fp8_long_sampled(pkv, orc):
+    """Full-size long-context fp8 workload: sampled sequences, all their
+    heads; the oracle fills only those sequences' rows."""
+    w = W.fp8_long()
+    cache, out = PL.gpu_run(w, pkv)
+    seqs = [0, 7, 15]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    gc = PL.gpu_cache_host(cache)
+    for b in seqs:
+        n = int(w.context_lens[b])
+        blocks = w.block_tables[b, :(n + w.block_size - 1) // w.block_size].long().numpy()
+        for k in ("k_cache", "v_cache"):
+            flat_g = gc[k][blocks].reshape(-1, w.num_kv_heads, w.head_dim)[:n]
+            flat_o = oc[k][blocks].reshape(-1, w.num_kv_heads, w.head_dim)[:n]
+            assert np.array_equal(flat_g, flat_o)
+    pairs = _sample_pairs(w, seqs)
+    ref = PL.oracle_decode(w, orc, oc, pairs=pairs)
+    _check(w, out, ref, pairs)
+
+
+def test_full_u3_mha_sampled(pkv, orc):
+    w = W.u3_mha()
+    cache, out = PL.gpu_run(w, pkv)
+    seqs = [0, 13, 31]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    pairs = _sample_pairs(w, seqs)
+    ref = PL.oracle_decode(w, orc, oc, pairs=pairs)
+    _check(w, out, ref, pairs)
