@@ -229,6 +229,36 @@ int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tens
                      void *stream);
 
 /*
+ * pkv_paged_decode_noalloc -- pkv_paged_decode for callers that cannot
+ * allocate device memory at call time: code being captured into a CUDA
+ * graph, plugin or custom-op hooks of inference engines that may not
+ * allocate while enqueueing, and serving loops that cannot afford the
+ * device-wide synchronisation of cudaMalloc.  The pages have no
+ * counterpart; it is an addition of this library.
+ *
+ * Same arguments and result as pkv_paged_decode without the workspace: the
+ * split-K scratch is a fixed array inside the library
+ * (pkv_noalloc_scratch_bytes(), 8 MiB), reserved on every GPU that loads
+ * the library until the process exits.  Nothing is allocated, by the call
+ * or by anything it calls.
+ *   - A problem whose scratch need (pkv_paged_decode_workspace) exceeds the
+ *     array is rejected with PKV_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks the array's device address up with
+ *     cudaGetSymbolAddress (once per device, with that device current);
+ *     make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose kernels overlap
+ *     on the GPU (different streams, or concurrent host threads) race on
+ *     it: serialise them, e.g. on one stream.
+ */
+size_t pkv_noalloc_scratch_bytes(void);
+
+int pkv_paged_decode_noalloc(const pkv_tensor *q, const pkv_cache *cache,
+                             const pkv_tensor *block_tables, const pkv_tensor *context_lens,
+                             float sm_scale, const pkv_tensor *out, int num_splits,
+                             int32_t *err_flag, void *stream);
+
+/*
  * pkv_pack3 / pkv_unpack3 -- 8 x uint3 <-> 3 bytes per octet
  * ("triton-3bit-kv-cache-kernel" README, section 1.A, packing and
  * explicit unpacking formulas).

@@ -161,6 +161,8 @@ int sm_count_current_device()
     }
     return cache[dev];
 }
+
+int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace pkv
 
 extern "C" {

@@ -110,4 +110,7 @@ cudaError_t launch_copy_peak(const void *src, void *dst, size_t bytes, cudaStrea
 
 int sm_count_current_device();
 
+// Record `msg` as this host thread's pkv_last_error() text; returns `code`.
+int set_last_error(int code, const char *msg);
+
 }  // namespace pkv

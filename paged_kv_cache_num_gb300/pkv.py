@@ -73,12 +73,15 @@ def lib():
                                                      ctypes.POINTER(ctypes.c_size_t)]
             L.pkv_paged_decode.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP, ctypes.c_int, P,
                                            ctypes.c_size_t, P, P]
+            L.pkv_paged_decode_noalloc.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP,
+                                                   ctypes.c_int, P, P]
+            L.pkv_noalloc_scratch_bytes.restype = ctypes.c_size_t
             L.pkv_pack3.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_unpack3.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_unpack3_words.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_copy_peak.argtypes = [P, P, ctypes.c_size_t, P]
             for fn in ("pkv_slot_mapping", "pkv_kv_append", "pkv_paged_decode_workspace",
-                       "pkv_paged_decode", "pkv_pack3", "pkv_unpack3", "pkv_unpack3_words",
+                       "pkv_paged_decode", "pkv_paged_decode_noalloc", "pkv_pack3", "pkv_unpack3", "pkv_unpack3_words",
                        "pkv_copy_peak"):
                 getattr(L, fn).restype = ctypes.c_int
             _lib = L
@@ -257,6 +260,25 @@ def paged_decode(q, cache: KVCache, block_tables, context_lens, sm_scale: Option
                                   ctypes.byref(_desc(context_lens)), float(sm_scale),
                                   ctypes.byref(_desc(out)), int(num_splits), ws_ptr, ws_n,
                                   _ptr(err_flag), _stream(stream)))
+    return out
+
+
+def paged_decode_noalloc(q, cache: KVCache, block_tables, context_lens,
+                         sm_scale: Optional[float] = None, out=None, num_splits: int = 0,
+                         err_flag=None, stream=None):
+    """paged_decode without a caller workspace: the split-K scratch is the
+    library's fixed device array (see pkv_paged_decode_noalloc in pkv.h)."""
+    _need_cuda(q, block_tables, context_lens, *cache.tensors())
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+    if out is None:
+        out = torch.empty_like(q)
+    cs = cache._struct()
+    _check(lib().pkv_paged_decode_noalloc(ctypes.byref(_desc(q)), ctypes.byref(cs),
+                                          ctypes.byref(_desc(block_tables)),
+                                          ctypes.byref(_desc(context_lens)), float(sm_scale),
+                                          ctypes.byref(_desc(out)), int(num_splits),
+                                          _ptr(err_flag), _stream(stream)))
     return out
 
 
