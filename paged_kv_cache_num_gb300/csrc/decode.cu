@@ -248,11 +248,11 @@ cudaError_t launch_by_dim(const DecodeParams &p, cudaStream_t s)
 
 }  // namespace
 
-DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                       int max_blocks, int cache_kind, int num_splits, int sm_count)
+DecodePlan plan_decode_general(int batch, int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int max_blocks, int num_splits, int sm_count)
 {
-    (void)cache_kind;
     DecodePlan pl{};
+    pl.kernel = 0;
     const int64_t max_ctx = int64_t(max_blocks) * block_size;
     int64_t chunk;
     if (num_splits > 0) {

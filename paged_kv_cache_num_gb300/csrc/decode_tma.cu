@@ -1,0 +1,823 @@
+// decode_tma.cu -- the fast paged-decode path for 16-bit and fp8 caches:
+// a persistent, load-balanced kernel that streams whole physical blocks into
+// shared memory with TMA and runs both products of each block on tensor
+// cores, plus the merge kernel for sequences split across CTAs.
+//
+// What it computes is "10. Triton KV Cache and PagedAttention", reference
+// code TODO 1-5 (block-table lookup, masked K/V tile, scores, online softmax,
+// V accumulation, final normalisation), with grouped-query heads
+// ("Write Triton Kv Cache Append Kernel", design rules) and a split of long
+// contexts whose partial (m, l, acc) triples are merged by log-sum-exp
+// rescaling.
+//
+// Work decomposition.  The unit of work is one physical block of one group
+// of `nh` kv heads.  All (head group, sequence, logical block) units are laid
+// out in one flat index space (head group major, then sequence, then block)
+// and CTA i of the persistent grid takes the contiguous range
+// [i*N/S, (i+1)*N/S): every CTA streams the same number of blocks, whatever
+// the mix of context lengths.  A CTA's range crosses sequence boundaries; each
+// maximal run of one (head group, sequence) inside it is a segment.  A segment
+// that covers its whole sequence writes the output directly; otherwise it
+// writes an fp32 partial in slot (CTA index + unit index), which is unique
+// because both grow along the flat order, and the merge kernel combines the
+// partials of the CTAs that cover the unit.
+//
+// CTA layout.  nh consumer warps (one per kv head of the group) and one
+// producer warp.  The producer resolves 32 block-table entries at a time
+// (one per lane) and issues, per block, TMA tensor copies of the K and V
+// tiles [nh heads][block_size tokens][head_dim] (128-byte swizzled rows) into
+// a ring of `stages` shared-memory stages guarded by full/empty mbarriers.
+// Each consumer warp computes, for its kv head and the G query heads that
+// share it (the M dimension of m16n8k16 mma.sync, rows >= G are zero):
+//   S = Q K^T (K from shared memory by ldmatrix, or fp8 bytes converted to
+//   f16 in registers), masking of tokens >= context_len, online softmax in
+//   log2 units, O = O * alpha + P V (P reused from the S accumulators as the
+//   A operand, V by ldmatrix.trans or fp8 -> f16 conversion).
+// Every wait is bounded (about 2 s of wall time) and raises
+// PKV_DEVERR_TIMEOUT instead of hanging.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+#define NEG_INF (-__int_as_float(0x7f800000))
+
+struct SmemLayout {
+    int tile_bytes, stage_bytes, bars_off, ok_off, prefix_off, nblk_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
+                                                  int batch)
+{
+    SmemLayout L;
+    L.tile_bytes = nh * bs * row_bytes;
+    L.stage_bytes = 2 * L.tile_bytes;
+    L.bars_off = stages * L.stage_bytes;
+    L.ok_off = L.bars_off + 2 * stages * 8;
+    L.prefix_off = L.ok_off + stages * 4;
+    L.nblk_off = L.prefix_off + (batch + 1) * 4;
+    L.total = L.nblk_off + batch * 4 + 1024;   // + alignment slack
+    return L;
+}
+
+// largest b in [0, B) with prefix[b] <= r, for 0 <= r < prefix[B]
+__device__ __forceinline__ int find_seq(const int *prefix, int B, int r)
+{
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= r) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &rlo, float &rhi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    const float2 r = __bfloat1622float2(v);
+    rlo = r.x;
+    rhi = r.y;
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float &rlo, float &rhi)
+{
+    const __half2 v = __floats2half2_rn(lo, hi);
+    const float2 r = __half22float2(v);
+    rlo = r.x;
+    rhi = r.y;
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu),
+                                                     __NV_E4M3);
+    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_shared_u64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+// CK: cache kind (kF16 / kBF16 / kE4M3); D head_dim; BS block size.
+// MMA operand type: bf16 for bf16 caches, f16 otherwise (fp8 codes convert
+// exactly to f16).
+template <int CK, int D, int BS>
+struct Tile {
+    static constexpr bool kFp8 = CK == kE4M3;
+    static constexpr bool kBF = CK == kBF16;
+    static constexpr int ES = kFp8 ? 1 : 2;
+    static constexpr int ROW = D * ES;              // bytes per token row
+    static constexpr int HALVES = ROW / 128;        // 128-byte swizzled sub-rows
+    static constexpr int NT = BS / 8;               // score n-tiles
+    static constexpr int KT = BS / 16;              // PV k-steps
+    static constexpr int DT = D / 8;                // output n-tiles
+    static constexpr int QK = D / 16;               // QK k-steps
+};
+
+template <int CK, int D, int BS>
+__global__ void __launch_bounds__(288, 1)
+decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  DecodeParams p, FastParams f)
+{
+    using T = Tile<CK, D, BS>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nh = f.nh, B = p.batch, G = p.group, stages = f.stages;
+    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
+    volatile int *stage_ok = reinterpret_cast<volatile int *>(smem + L.ok_off);
+    int *prefix = reinterpret_cast<int *>(smem + L.prefix_off);
+    int *nblk = reinterpret_cast<int *>(smem + L.nblk_off);
+
+    // ---- per-sequence block counts and their prefix sums
+    const int cap = p.max_blocks << p.block_shift;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        int ctx = p.context_lens[b * p.cl_stride];
+        if (ctx < 0 || ctx > cap) {
+            if (blockIdx.x == 0) raise_err(p.err_flag, PKV_DEVERR_CONTEXT_RANGE);
+            ctx = ctx < 0 ? 0 : cap;
+        }
+        nblk[b] = (ctx + BS - 1) / BS;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, nh);
+        }
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {               // exclusive scan, 32 sequences per step
+        int carry = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int v = (b0 + lane < B) ? nblk[b0 + lane] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (b0 + lane < B) prefix[b0 + lane] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) prefix[B] = carry;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b <= B; b += blockDim.x) f.prefix[b] = prefix[b];
+
+    const int64_t NBT = prefix[B];                  // blocks per head group
+    const int64_t N = NBT * f.n_hg;
+    const int64_t lo = int64_t(blockIdx.x) * N / gridDim.x;
+    const int64_t hi = int64_t(blockIdx.x + 1) * N / gridDim.x;
+    if (lo >= hi) return;
+
+    // ======================================================== producer warp
+    if (warp == nh) {
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tmk);
+            ptx::prefetch_tmap(&tmv);
+        }
+        bool aborted = false;
+        int64_t issued = 0;
+        for (int64_t base = lo; base < hi && !aborted; base += 32) {
+            const int64_t x = base + lane;
+            int pb = -1, hg = 0;
+            if (x < hi) {
+                hg = int(x / NBT);
+                const int r = int(x - int64_t(hg) * NBT);
+                const int b = find_seq(prefix, B, r);
+                const int j = r - prefix[b];
+                pb = p.block_tables[b * p.bt_b + j * p.bt_j];
+                if (pb < 0 || pb >= p.num_blocks) {
+                    raise_err(p.err_flag, PKV_DEVERR_BLOCK_RANGE);
+                    pb = -1;
+                }
+            }
+            const int n = int(hi - base < 32 ? hi - base : 32);
+            for (int k = 0; k < n; ++k) {
+                const int pbk = __shfl_sync(0xffffffffu, pb, k);
+                const int hgk = __shfl_sync(0xffffffffu, hg, k);
+                if (lane == 0 && !aborted) {
+                    const int64_t it = base - lo + k;
+                    const int s = int(it % stages);
+                    const int64_t round = it / stages;
+                    if (round > 0 &&
+                        !ptx::mbar_wait_bounded(bar_empty + 8 * s, uint32_t((round - 1) & 1), kTimeoutNs)) {
+                        raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
+                        aborted = true;
+                    } else {
+                        const uint32_t fb = bar_full + 8 * s;
+                        const uint32_t kdst = sbase + s * L.stage_bytes;
+                        const uint32_t vdst = kdst + L.tile_bytes;
+                        if (pbk >= 0) {
+                            stage_ok[s] = 1;
+                            ptx::mbar_arrive_expect_tx(fb, uint32_t(L.stage_bytes));
+#pragma unroll
+                            for (int h = 0; h < T::HALVES; ++h) {
+                                const int half_bytes = L.tile_bytes / T::HALVES;
+                                ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * (128 / T::ES), 0,
+                                                 hgk * nh, pbk);
+                                ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * (128 / T::ES), 0,
+                                                 hgk * nh, pbk);
+                            }
+                        } else {
+                            stage_ok[s] = 0;
+                            ptx::mbar_arrive(fb);
+                        }
+                        ++issued;
+                    }
+                }
+                aborted = __shfl_sync(0xffffffffu, aborted, 0);
+            }
+        }
+        // let the copies in flight land before this warp retires
+        if (lane == 0) {
+            for (int64_t it = issued > stages ? issued - stages : 0; it < issued; ++it)
+                ptx::mbar_wait_bounded(bar_full + 8 * int(it % stages), uint32_t((it / stages) & 1),
+                                       kTimeoutNs);
+        }
+        return;
+    }
+
+    // ======================================================== consumer warps
+    const int gid = lane >> 2, tig = lane & 3;
+    const float log2e_scale = p.scale_log2;
+    // walk state
+    int64_t x = lo;
+    int hg = int(x / NBT);
+    int b, j;
+    {
+        const int r = int(x - int64_t(hg) * NBT);
+        b = find_seq(prefix, B, r);
+        j = r - prefix[b];
+    }
+    int64_t seg_start = lo;
+
+    uint32_t qa[T::QK][4];
+    float o[T::DT][4];
+    float m[2], l[2];
+    float mult = 1.0f, vmul = 1.0f;
+    int ctx_b = 0;
+
+    auto start_segment = [&]() {
+        const int kvh = hg * nh + warp;
+        {
+            const int cb = p.context_lens[b * p.cl_stride];
+            ctx_b = cb < 0 ? 0 : (cb > cap ? cap : cb);
+        }
+        const bool r0 = gid < G, r1 = gid + 8 < G;
+        const uint16_t *q0 = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
+        const uint16_t *q1 = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid + 8) * p.q_h);
+        if constexpr (!T::kFp8) {
+#pragma unroll
+            for (int kk = 0; kk < T::QK; ++kk) {
+                const int d = 16 * kk + 2 * tig;
+                qa[kk][0] = r0 ? *reinterpret_cast<const uint32_t *>(q0 + d) : 0u;
+                qa[kk][1] = r1 ? *reinterpret_cast<const uint32_t *>(q1 + d) : 0u;
+                qa[kk][2] = r0 ? *reinterpret_cast<const uint32_t *>(q0 + d + 8) : 0u;
+                qa[kk][3] = r1 ? *reinterpret_cast<const uint32_t *>(q1 + d + 8) : 0u;
+            }
+            mult = log2e_scale;
+            vmul = 1.0f;
+        } else {
+            // q (16-bit) -> f16 operands, with the element order matching the
+            // fp8 K fragments: k-step 2kp+s, thread tig holds d = 32kp + 8tig
+            // + 4s + {0,1} (k = 2tig, 2tig+1) and + {2,3} (k = 2tig+8, +9).
+            float qf[2][D / 4];
+            float amax = 0.0f;
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {
+                const int d = 32 * kp + 8 * tig;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const bool ok = rr ? r1 : r0;
+                    uint4 u = make_uint4(0, 0, 0, 0);
+                    if (ok) u = *reinterpret_cast<const uint4 *>((rr ? q1 : q0) + d);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float a, c;
+                        if (p.q_is_bf16) {
+                            a = __uint_as_float(w[e] << 16);
+                            c = __uint_as_float(w[e] & 0xffff0000u);
+                        } else {
+                            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                            a = t.x;
+                            c = t.y;
+                        }
+                        qf[rr][8 * kp + 2 * e] = a;
+                        qf[rr][8 * kp + 2 * e + 1] = c;
+                        amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c)));
+                    }
+                }
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+            // power-of-two pre-scale that keeps every q element inside f16 range
+            float qs = 1.0f;
+            while (amax * qs > 16384.0f) qs *= 0.5f;
+            float dummy0, dummy1;
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    const int e = 8 * kp + 4 * s2;
+                    qa[2 * kp + s2][0] = pack_f16(qf[0][e] * qs, qf[0][e + 1] * qs, dummy0, dummy1);
+                    qa[2 * kp + s2][1] = pack_f16(qf[1][e] * qs, qf[1][e + 1] * qs, dummy0, dummy1);
+                    qa[2 * kp + s2][2] = pack_f16(qf[0][e + 2] * qs, qf[0][e + 3] * qs, dummy0, dummy1);
+                    qa[2 * kp + s2][3] = pack_f16(qf[1][e + 2] * qs, qf[1][e + 3] * qs, dummy0, dummy1);
+                }
+            }
+            mult = log2e_scale * p.k_scale[kvh] / qs;
+            vmul = p.v_scale[kvh];
+        }
+#pragma unroll
+        for (int t = 0; t < T::DT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
+        m[0] = m[1] = NEG_INF;
+        l[0] = l[1] = 0.0f;
+    };
+
+    auto finish_segment = [&](int64_t seg_end) {
+        const int kvh = hg * nh + warp;
+        const int64_t unit_first = int64_t(hg) * NBT + prefix[b];
+        const int64_t unit_last = unit_first + nblk[b] - 1;
+        float lt[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            lt[r] = l[r] + __shfl_xor_sync(0xffffffffu, l[r], 1);
+            lt[r] += __shfl_xor_sync(0xffffffffu, lt[r], 2);
+        }
+        const bool whole = seg_start == unit_first && seg_end == unit_last;
+        const int64_t key = int64_t(blockIdx.x) + int64_t(hg) * B + b;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int g = gid + 8 * r;
+            if (g >= G) continue;
+            const int h = kvh * G + g;
+            if (whole) {
+                const float inv = lt[r] > 0.0f ? vmul / lt[r] : 0.0f;
+                uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
+                if constexpr (!T::kFp8) {
+#pragma unroll
+                    for (int t = 0; t < T::DT; ++t) {
+                        const float v0 = o[t][2 * r] * inv, v1 = o[t][2 * r + 1] * inv;
+                        uint32_t w;
+                        if (p.q_is_bf16) {
+                            const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
+                            w = *reinterpret_cast<const uint32_t *>(&hv);
+                        } else {
+                            const __half2 hv = __floats2half2_rn(v0, v1);
+                            w = *reinterpret_cast<const uint32_t *>(&hv);
+                        }
+                        if (p.out_vec_ok) {
+                            *reinterpret_cast<uint32_t *>(orow + 8 * t + 2 * tig) = w;
+                        } else {
+                            orow[8 * t + 2 * tig] = uint16_t(w);
+                            orow[8 * t + 2 * tig + 1] = uint16_t(w >> 16);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // elements 2e, 2e+1 of d = 32q4 + 8tig + {0..7}
+                            const int e0 = 2 * e, e1 = 2 * e + 1;
+                            const float v0 = o[4 * q4 + (e0 & 3)][2 * r + (e0 >> 2)] * inv;
+                            const float v1 = o[4 * q4 + (e1 & 3)][2 * r + (e1 >> 2)] * inv;
+                            if (p.q_is_bf16) {
+                                const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
+                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                            } else {
+                                const __half2 hv = __floats2half2_rn(v0, v1);
+                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                            }
+                        }
+                        if (p.out_vec_ok) {
+                            *reinterpret_cast<uint4 *>(orow + 32 * q4 + 8 * tig) = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                orow[32 * q4 + 8 * tig + e] = uint16_t(w[e >> 1] >> (16 * (e & 1)));
+                        }
+                    }
+                }
+            } else {
+                const int64_t row = key * (int64_t(nh) * G) + int64_t(warp) * G + g;
+                float *acc = f.part_acc + row * D;
+                if (tig == 0) {
+                    f.part_ml[2 * row] = m[r];
+                    f.part_ml[2 * row + 1] = lt[r];
+                }
+                if constexpr (!T::kFp8) {
+#pragma unroll
+                    for (int t = 0; t < T::DT; ++t)
+                        *reinterpret_cast<float2 *>(acc + 8 * t + 2 * tig) =
+                            make_float2(o[t][2 * r] * vmul, o[t][2 * r + 1] * vmul);
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = o[4 * q4 + (e & 3)][2 * r + (e >> 2)] * vmul;
+                        *reinterpret_cast<float4 *>(acc + 32 * q4 + 8 * tig) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4 *>(acc + 32 * q4 + 8 * tig + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                    }
+                }
+            }
+        }
+    };
+
+    start_segment();
+    for (int64_t it = 0; x < hi; ++x, ++it) {
+        const int s = int(it % stages);
+        if (!ptx::mbar_wait_bounded(bar_full + 8 * s, uint32_t((it / stages) & 1), kTimeoutNs)) {
+            raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
+            return;
+        }
+        // valid tokens of this block (only the last block of a sequence is partial)
+        const int valid = min(BS, ctx_b - j * BS);
+        if (stage_ok[s]) {
+            const uint32_t ktile = sbase + s * L.stage_bytes;
+            const uint32_t vtile = ktile + L.tile_bytes;
+            const int half_bytes = L.tile_bytes / T::HALVES;
+            // ---------------- S = Q K^T
+            float sc[T::NT][4];
+#pragma unroll
+            for (int t = 0; t < T::NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.0f;
+            if constexpr (!T::kFp8) {
+#pragma unroll
+                for (int kk = 0; kk < T::QK; ++kk) {
+#pragma unroll
+                    for (int ntp = 0; ntp < T::NT / 2; ++ntp) {
+                        const int tok = 16 * ntp + 8 * (lane >> 4) + (lane & 7);
+                        const int chunk = 2 * kk + ((lane >> 3) & 1);
+                        const uint32_t addr = ktile + (chunk >> 3) * half_bytes + (warp * BS + tok) * 128 +
+                                              (((chunk & 7) ^ (tok & 7)) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
+                        ptx::mma16816<T::kBF>(sc[2 * ntp], qa[kk], b0, b1);
+                        ptx::mma16816<T::kBF>(sc[2 * ntp + 1], qa[kk], b2, b3);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kp = 0; kp < D / 32; ++kp) {
+#pragma unroll
+                    for (int nt = 0; nt < T::NT; ++nt) {
+                        const int tok = 8 * nt + gid;
+                        const int chunk = 2 * kp + (tig >> 1);
+                        const uint32_t addr = ktile + (warp * BS + tok) * 128 + (((chunk & 7) ^ (tok & 7)) << 4) +
+                                              (tig & 1) * 8;
+                        const uint2 w = ld_shared_u64(addr);
+                        ptx::mma16816<false>(sc[nt], qa[2 * kp], f16x2_from_e4m3x2(w.x), f16x2_from_e4m3x2(w.x >> 16));
+                        ptx::mma16816<false>(sc[nt], qa[2 * kp + 1], f16x2_from_e4m3x2(w.y),
+                                             f16x2_from_e4m3x2(w.y >> 16));
+                    }
+                }
+            }
+            // ---------------- online softmax (log2 units)
+            float mx[2] = {NEG_INF, NEG_INF};
+#pragma unroll
+            for (int t = 0; t < T::NT; ++t) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = 8 * t + 2 * tig + (e & 1);
+                    float v = sc[t][e] * mult;
+                    v = tok < valid ? v : NEG_INF;
+                    sc[t][e] = v;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
+                }
+            }
+            float alpha[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                const float mn = fmaxf(m[r], mx[r]);
+                alpha[r] = mn == NEG_INF ? 1.0f : exp2_approx(m[r] - mn);
+                m[r] = mn;
+            }
+            uint32_t pa[T::KT][4];
+            float ls[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int t = 0; t < T::NT; ++t) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float p0 = exp2_approx(sc[t][2 * r] - m[r]);
+                    const float p1 = exp2_approx(sc[t][2 * r + 1] - m[r]);
+                    float q0, q1;
+                    const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0, p1, q0, q1);
+                    ls[r] += q0 + q1;
+                    // A fragment of the PV product: k-step t/2, register (t&1)*2 + r
+                    pa[t >> 1][(t & 1) * 2 + r] = w;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + ls[r];
+#pragma unroll
+            for (int t = 0; t < T::DT; ++t) {
+                o[t][0] *= alpha[0];
+                o[t][1] *= alpha[0];
+                o[t][2] *= alpha[1];
+                o[t][3] *= alpha[1];
+            }
+            // ---------------- O += P V
+            const bool partial = valid < BS;
+            if constexpr (!T::kFp8) {
+#pragma unroll
+                for (int kt = 0; kt < T::KT; ++kt) {
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                    if (partial) {
+                        const int t0 = 16 * kt + 2 * tig;
+                        mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+                        mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+                    }
+#pragma unroll
+                    for (int ndp = 0; ndp < T::DT / 2; ++ndp) {
+                        const int tok = 16 * kt + 8 * ((lane >> 3) & 1) + (lane & 7);
+                        const int chunk = 2 * ndp + (lane >> 4);
+                        const uint32_t addr = vtile + (chunk >> 3) * half_bytes + (warp * BS + tok) * 128 +
+                                              (((chunk & 7) ^ (tok & 7)) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                        b0 &= mlo;
+                        b2 &= mlo;
+                        b1 &= mhi;
+                        b3 &= mhi;
+                        ptx::mma16816<T::kBF>(o[2 * ndp], pa[kt], b0, b1);
+                        ptx::mma16816<T::kBF>(o[2 * ndp + 1], pa[kt], b2, b3);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kt = 0; kt < T::KT; ++kt) {
+                    const int t0 = 16 * kt + 2 * tig;
+                    const int rows[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
+#pragma unroll
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                        const int chunk = 2 * q4 + (gid >> 2);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int tok = rows[i];
+                            w[i] = ld_shared_u32(vtile + (warp * BS + tok) * 128 + (((chunk & 7) ^ (tok & 7)) << 4) +
+                                                 (gid & 3) * 4);
+                            if (partial && tok >= valid) w[i] = 0u;
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj += 2) {
+                            // bytes jj, jj+1 of (w0, w1) and of (w2, w3), paired by token
+                            const uint32_t sel = jj | ((jj + 4) << 4) | ((jj + 1) << 8) | ((jj + 5) << 12);
+                            const uint32_t a01 = ptx::prmt(w[0], w[1], sel);
+                            const uint32_t a23 = ptx::prmt(w[2], w[3], sel);
+                            ptx::mma16816<false>(o[4 * q4 + jj], pa[kt], f16x2_from_e4m3x2(a01),
+                                                 f16x2_from_e4m3x2(a23));
+                            ptx::mma16816<false>(o[4 * q4 + jj + 1], pa[kt], f16x2_from_e4m3x2(a01 >> 16),
+                                                 f16x2_from_e4m3x2(a23 >> 16));
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
+        // advance the walk; close the segment at a unit boundary
+        if (x + 1 < hi) {
+            if (++j == nblk[b]) {
+                finish_segment(x);
+                j = 0;
+                do {
+                    if (++b == B) {
+                        b = 0;
+                        ++hg;
+                    }
+                } while (nblk[b] == 0);
+                seg_start = x + 1;
+                start_segment();
+            }
+        } else {
+            finish_segment(x);
+        }
+    }
+}
+
+// Merge the partials of units split across CTAs (one warp per (sequence,
+// q head)); units held whole by one CTA were written by it, units with an
+// empty context get zeros.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f)
+{
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= p.batch * p.num_heads) return;
+    const int b = w / p.num_heads, h = w % p.num_heads;
+    const int G = p.group, nh = f.nh;
+    const int kvh = h / G, hg = kvh / nh;
+    const int local = h - hg * nh * G;
+    const int64_t NBT = f.prefix[p.batch];
+    const int64_t N = NBT * f.n_hg;
+    const int n = f.prefix[b + 1] - f.prefix[b];
+    constexpr int EPL = D / 32;
+    uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+    if (n > 0) {
+        const int64_t S = f.grid;
+        const int64_t first = int64_t(hg) * NBT + f.prefix[b];
+        const int64_t i0 = ((first + 1) * S - 1) / N;
+        const int64_t i1 = ((first + n) * S - 1) / N;
+        if (i0 == i1) return;                         // written whole by CTA i0
+        const int64_t unit = int64_t(hg) * p.batch + b;
+        // CTAs with an empty range (more CTAs than blocks) wrote nothing
+        auto empty_range = [&](int64_t i) { return (i * N) / S == ((i + 1) * N) / S; };
+        float M = NEG_INF;
+        for (int64_t i = i0; i <= i1; ++i)
+            if (!empty_range(i)) M = fmaxf(M, f.part_ml[2 * ((i + unit) * nh * G + local)]);
+        float Lsum = 0.0f;
+        if (M != NEG_INF) {
+            for (int64_t i = i0; i <= i1; ++i) {
+                if (empty_range(i)) continue;
+                const int64_t row = (i + unit) * nh * G + local;
+                const float mi = f.part_ml[2 * row];
+                const float wgt = mi == NEG_INF ? 0.0f : exp2_approx(mi - M);
+                Lsum += f.part_ml[2 * row + 1] * wgt;
+                const float *pa = f.part_acc + row * D + EPL * lane;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] += pa[e] * wgt;
+            }
+        }
+        const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= inv;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+        orow[EPL * lane + e] = p.q_is_bf16 ? f2h<kBF16>(acc[e]) : f2h<kF16>(acc[e]);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 4-D map over one cache: (row element, slot, kv head, block) with the
+// caller's strides; box = one 128-byte sub-row x block_size slots x nh heads.
+bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, int P, int64_t c_slot,
+              int64_t c_head, int64_t c_blk, int nh)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int es = ck == kE4M3 ? 1 : 2;
+    const CUtensorMapDataType dt = ck == kE4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : ck == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(BS), cuuint64_t(Hkv), cuuint64_t(P)};
+    cuuint64_t strides[3] = {cuuint64_t(c_slot), cuuint64_t(c_head), cuuint64_t(c_blk)};
+    cuuint32_t box[4] = {cuuint32_t(128 / es), cuuint32_t(BS), cuuint32_t(nh), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int CK, int D, int BS>
+cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
+                          const CUtensorMap &mv, cudaStream_t s)
+{
+    auto kern = decode_tma_kernel<CK, D, BS>;
+    static int configured = 0;
+    if (configured < f.smem_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem_bytes);
+        if (e != cudaSuccess) return e;
+        configured = f.smem_bytes;
+    }
+    kern<<<f.grid, (f.nh + 1) * 32, f.smem_bytes, s>>>(mk, mv, p, f);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int rows = p.batch * p.num_heads;
+    merge_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(p, f);
+    return cudaGetLastError();
+}
+
+template <int CK, int D>
+cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
+                           const CUtensorMap &mv, cudaStream_t s)
+{
+    switch (p.block_size) {
+    case 16: return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
+    case 32: return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
+    case 64: return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch)
+{
+    if (block_size != 16 && block_size != 32 && block_size != 64) return false;
+    if (group > 16 || batch > 4096) return false;
+    if (cache_kind == kE4M3) return head_dim == 128;
+    return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
+}
+
+// Choose heads per CTA, stages and grid for the fast kernel.
+bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
+               int cache_kind, int sm_count, FastParams &f, size_t &workspace)
+{
+    const int es = cache_kind == kE4M3 ? 1 : 2;
+    const int row = head_dim * es;
+    int nh = 8;
+    while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
+    if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
+    const int budget = 227 * 1024;
+    int stages = 4;
+    while (stages > 2 && smem_layout(nh, block_size, row, stages, batch).total > budget) --stages;
+    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch);
+    if (L.total > budget) return false;
+    const int n_hg = num_kv_heads / nh;
+    const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
+    f.nh = nh;
+    f.n_hg = n_hg;
+    f.stages = stages;
+    f.grid = int(max_units < sm_count ? (max_units > 0 ? max_units : 1) : sm_count);
+    f.smem_bytes = L.total;
+    const int group = num_heads / num_kv_heads;
+    const int64_t rows = (int64_t(f.grid) + int64_t(n_hg) * batch) * nh * group;
+    const size_t prefix_bytes = (size_t(batch + 1) * 4 + 255) / 256 * 256;
+    const size_t ml_bytes = (size_t(rows) * 2 * 4 + 255) / 256 * 256;
+    workspace = prefix_bytes + ml_bytes + size_t(rows) * head_dim * 4;
+    return true;
+}
+
+bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh)
+{
+    CUtensorMap mk, mv;
+    return make_map(&mk, p.k_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
+                    p.c_head, p.c_blk, nh) &&
+           make_map(&mv, p.v_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
+                    p.c_head, p.c_blk, nh);
+}
+
+cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_kind, void *ws, size_t ws_bytes,
+                               cudaStream_t s)
+{
+    const int64_t rows = (int64_t(f.grid) + int64_t(f.n_hg) * p.batch) * f.nh * p.group;
+    char *c = static_cast<char *>(ws);
+    const size_t prefix_bytes = (size_t(p.batch + 1) * 4 + 255) / 256 * 256;
+    const size_t ml_bytes = (size_t(rows) * 2 * 4 + 255) / 256 * 256;
+    (void)ws_bytes;
+    f.prefix = reinterpret_cast<int32_t *>(c);
+    f.part_ml = reinterpret_cast<float *>(c + prefix_bytes);
+    f.part_acc = reinterpret_cast<float *>(c + prefix_bytes + ml_bytes);
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, p.k_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
+                  p.c_head, p.c_blk, f.nh) ||
+        !make_map(&mv, p.v_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
+                  p.c_head, p.c_blk, f.nh))
+        return cudaErrorInvalidValue;
+    if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
+    if (cache_kind == kBF16)
+        return p.head_dim == 128 ? launch_fast_bs<kBF16, 128>(p, f, mk, mv, s) : launch_fast_bs<kBF16, 64>(p, f, mk, mv, s);
+    return p.head_dim == 128 ? launch_fast_bs<kF16, 128>(p, f, mk, mv, s) : launch_fast_bs<kF16, 64>(p, f, mk, mv, s);
+}
+
+}  // namespace pkv

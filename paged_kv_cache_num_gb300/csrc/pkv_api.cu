@@ -279,9 +279,14 @@ namespace {
 struct DecodeCheck {
     CacheInfo ci;
     int64_t batch, num_heads, max_blocks;
+    pkv::DecodeParams p;   // every field known before context_lens / out / workspace
     pkv::DecodePlan plan;
 };
 
+// Validate what the workspace query and the decode share, fill the launch
+// parameters that follow from it, and choose the kernel: the persistent TMA
+// kernel when num_splits == 0 and the shape, dtypes and layout are covered,
+// else the general kernel with the requested (or a heuristic) split count.
 int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
                         int num_splits, DecodeCheck &dc)
 {
@@ -306,9 +311,67 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
                                                         (long long)block_tables->shape[0], (long long)dc.batch);
     dc.max_blocks = block_tables->shape[1];
     if (num_splits < 0) return fail(PKV_ERR_VALUE, "num_splits must be >= 0");
-    dc.plan = pkv::plan_decode(int(dc.batch), int(dc.num_heads), int(dc.ci.num_kv_heads), int(dc.ci.head_dim),
-                               int(dc.ci.block_size), int(dc.max_blocks), dc.ci.kind, num_splits,
-                               pkv::sm_count_current_device());
+
+    const CacheInfo &ci = dc.ci;
+    pkv::DecodeParams &p = dc.p;
+    p = pkv::DecodeParams{};
+    p.q = static_cast<const char *>(q->data);
+    p.q_b = q->stride[0] * 2;
+    p.q_h = q->stride[1] * 2;
+    p.k_cache = static_cast<const char *>(cache->k_cache.data);
+    p.v_cache = static_cast<const char *>(cache->v_cache.data);
+    const int ces = elem_size(ci.kind);
+    p.c_blk = cache->k_cache.stride[0] * ces;
+    p.c_slot = cache->k_cache.stride[1] * ces;
+    p.c_head = cache->k_cache.stride[2] * ces;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
+    if (ci.kind == PKV_DTYPE_U3) {
+        p.k_qs = static_cast<const uint16_t *>(cache->k_qscale.data);
+        p.v_qs = static_cast<const uint16_t *>(cache->v_qscale.data);
+        p.k_qz = static_cast<const uint8_t *>(cache->k_qzero.data);
+        p.v_qz = static_cast<const uint8_t *>(cache->v_qzero.data);
+        p.m_blk = cache->k_qscale.stride[0];
+        p.m_slot = cache->k_qscale.stride[1];
+        p.m_head = cache->k_qscale.stride[2];
+        p.z_blk = cache->k_qzero.stride[0];
+        p.z_slot = cache->k_qzero.stride[1];
+        p.z_head = cache->k_qzero.stride[2];
+    }
+    p.block_tables = static_cast<const int32_t *>(block_tables->data);
+    p.bt_b = block_tables->stride[0];
+    p.bt_j = block_tables->stride[1];
+    p.batch = int(dc.batch);
+    p.num_heads = int(dc.num_heads);
+    p.num_kv_heads = int(ci.num_kv_heads);
+    p.group = int(dc.num_heads / ci.num_kv_heads);
+    p.head_dim = int(ci.head_dim);
+    p.block_size = int(ci.block_size);
+    p.block_shift = log2i(ci.block_size);
+    p.max_blocks = int(dc.max_blocks);
+    p.num_blocks = int(ci.num_blocks);
+    p.q_is_bf16 = q->dtype == PKV_DTYPE_BF16;
+
+    const int sm = pkv::sm_count_current_device();
+    dc.plan = pkv::DecodePlan{};
+    if (num_splits == 0 && pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
+        // the fp8 path reads q rows 16 bytes at a time, the 16-bit path 4
+        const size_t qa = ci.kind == PKV_DTYPE_E4M3 ? 16 : 4;
+        const bool q_ok = aligned(q->data, qa) && (p.q_b % qa) == 0 && (p.q_h % qa) == 0;
+        pkv::FastParams f{};
+        size_t ws = 0;
+        if (q_ok && pkv::plan_fast(p.batch, p.num_heads, p.num_kv_heads, p.head_dim, p.block_size, p.max_blocks,
+                                   ci.kind, sm, f, ws) &&
+            pkv::fast_maps_encodable(p, ci.kind, f.nh)) {
+            dc.plan.kernel = 1;
+            dc.plan.fast = f;
+            dc.plan.workspace_bytes = ws;
+            dc.plan.num_splits = 0;
+            return PKV_OK;
+        }
+    }
+    dc.plan = pkv::plan_decode_general(p.batch, p.num_heads, p.num_kv_heads, p.head_dim, p.block_size,
+                                       p.max_blocks, num_splits, sm);
     return PKV_OK;
 }
 
@@ -347,57 +410,26 @@ int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tens
                         pl.workspace_bytes);
         if (!aligned(workspace, 16)) return fail(PKV_ERR_LAYOUT, "workspace must be 16-byte aligned");
     }
-    const CacheInfo &ci = dc.ci;
-    pkv::DecodeParams p{};
-    p.q = static_cast<const char *>(q->data);
-    p.q_b = q->stride[0] * 2;
-    p.q_h = q->stride[1] * 2;
-    p.k_cache = static_cast<const char *>(cache->k_cache.data);
-    p.v_cache = static_cast<const char *>(cache->v_cache.data);
-    const int ces = elem_size(ci.kind);
-    p.c_blk = cache->k_cache.stride[0] * ces;
-    p.c_slot = cache->k_cache.stride[1] * ces;
-    p.c_head = cache->k_cache.stride[2] * ces;
-    p.k_scale = cache->k_scale;
-    p.v_scale = cache->v_scale;
-    if (ci.kind == PKV_DTYPE_U3) {
-        p.k_qs = static_cast<const uint16_t *>(cache->k_qscale.data);
-        p.v_qs = static_cast<const uint16_t *>(cache->v_qscale.data);
-        p.k_qz = static_cast<const uint8_t *>(cache->k_qzero.data);
-        p.v_qz = static_cast<const uint8_t *>(cache->v_qzero.data);
-        p.m_blk = cache->k_qscale.stride[0];
-        p.m_slot = cache->k_qscale.stride[1];
-        p.m_head = cache->k_qscale.stride[2];
-        p.z_blk = cache->k_qzero.stride[0];
-        p.z_slot = cache->k_qzero.stride[1];
-        p.z_head = cache->k_qzero.stride[2];
-    }
-    p.block_tables = static_cast<const int32_t *>(block_tables->data);
-    p.bt_b = block_tables->stride[0];
-    p.bt_j = block_tables->stride[1];
+    pkv::DecodeParams p = dc.p;
     p.context_lens = static_cast<const int32_t *>(context_lens->data);
     p.cl_stride = context_lens->stride[0];
     p.out = static_cast<char *>(out->data);
     p.o_b = out->stride[0] * 2;
     p.o_h = out->stride[1] * 2;
-    p.batch = int(dc.batch);
-    p.num_heads = int(dc.num_heads);
-    p.num_kv_heads = int(ci.num_kv_heads);
-    p.group = int(dc.num_heads / ci.num_kv_heads);
-    p.head_dim = int(ci.head_dim);
-    p.block_size = int(ci.block_size);
-    p.block_shift = log2i(ci.block_size);
-    p.max_blocks = int(dc.max_blocks);
-    p.num_blocks = int(ci.num_blocks);
+    p.out_vec_ok = aligned(out->data, 16) && (p.o_b % 16) == 0 && (p.o_h % 16) == 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.err_flag = err_flag;
+    if (pl.kernel == 1)
+        return launch_status(pkv::launch_decode_fast(p, pl.fast, dc.ci.kind, workspace, workspace_bytes,
+                                                     as_stream(stream)),
+                             "paged_decode kernels");
     p.num_splits = pl.num_splits;
     p.chunk_tokens = pl.chunk_tokens;
     if (pl.num_splits > 1) {
         p.part_acc = static_cast<float *>(workspace);
-        p.part_ml = p.part_acc + size_t(dc.batch) * dc.num_heads * pl.num_splits * ci.head_dim;
+        p.part_ml = p.part_acc + size_t(dc.batch) * dc.num_heads * pl.num_splits * dc.ci.head_dim;
     }
-    p.err_flag = err_flag;
-    return launch_status(pkv::launch_decode(p, ci.kind, q->dtype, as_stream(stream)), "paged_decode kernels");
+    return launch_status(pkv::launch_decode(p, dc.ci.kind, q->dtype, as_stream(stream)), "paged_decode kernels");
 }
 
 int pkv_pack3(const uint8_t *values, uint8_t *packed, int64_t n_octets, void *stream)

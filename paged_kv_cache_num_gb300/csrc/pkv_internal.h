@@ -87,19 +87,42 @@ struct DecodeParams {
     int chunk_tokens;           // tokens per chunk (multiple of block_size)
     float *part_acc;            // [B, Hq, num_splits, D]   (num_splits > 1)
     float *part_ml;             // [B, Hq, num_splits, 2]  (max in log2 units, sum)
+    int q_is_bf16;
+    int out_vec_ok;             // out rows 16-byte aligned (vector stores allowed)
     int32_t *err_flag;
 };
 
+// Persistent TMA kernel (16-bit and fp8 caches).
+struct FastParams {
+    int nh;                     // kv heads per CTA (consumer warps)
+    int n_hg;                   // head groups = num_kv_heads / nh
+    int stages;                 // shared-memory ring depth
+    int grid;                   // persistent CTAs
+    int smem_bytes;
+    int32_t *prefix;            // [B+1] blocks-per-sequence prefix sums (workspace)
+    float *part_ml;             // [(grid + n_hg*B) * nh * G, 2]
+    float *part_acc;            // [(grid + n_hg*B) * nh * G, D]
+};
+
 struct DecodePlan {
+    int kernel;                 // 0 = general (split-K by chunks), 1 = persistent TMA
     int num_splits;
     int chunk_tokens;
+    FastParams fast;
     size_t workspace_bytes;
 };
 
-DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                       int max_blocks, int cache_kind, int num_splits, int sm_count);
+DecodePlan plan_decode_general(int batch, int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int max_blocks, int num_splits, int sm_count);
+
+bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch);
+bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
+               int max_blocks, int cache_kind, int sm_count, FastParams &f, size_t &workspace);
+bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh);
 
 cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cudaStream_t s);
+cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_kind, void *ws,
+                               size_t ws_bytes, cudaStream_t s);
 
 // ---------------------------------------------------------------- pack3 / copy
 cudaError_t launch_pack3(const uint8_t *values, uint8_t *packed, int64_t n, cudaStream_t s);

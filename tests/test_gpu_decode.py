@@ -53,7 +53,7 @@ def test_gqa_bf16_small(pkv, orc, splits):
 def test_group_block_dim_matrix(pkv, orc, G, BS, D):
     w = W.gqa_bf16(batch=3, ctx_lo=1, ctx_hi=9 * BS + 5, num_heads=2 * G, num_kv_heads=2,
                    head_dim=D, block_size=BS, seed=40 + G * BS + D)
-    for splits in (1, 4):
+    for splits in (0, 1, 4):
         _, out = PL.gpu_run(w, pkv, num_splits=splits)
         ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
         _check(w, out, ref)
@@ -90,9 +90,39 @@ def test_u3_head_dim_64(pkv, orc):
     _check(w, out, PL.oracle_decode(w, orc, oc))
 
 
+@pytest.mark.parametrize("batch,ctx_hi", [(1, 5), (2, 40), (3, 17), (200, 64), (7, 5000)])
+def test_fast_path_grid_shapes(pkv, orc, batch, ctx_hi):
+    """Fewer blocks than CTAs (idle CTAs between the owners of one sequence),
+    single-block sequences, many short sequences, one long sequence split
+    over many CTAs."""
+    w = W.gqa_bf16(batch=batch, ctx_lo=1, ctx_hi=ctx_hi, seed=60 + batch)
+    _, out = PL.gpu_run(w, pkv, num_splits=0)
+    _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
+
+
+def test_fast_path_fp16_and_strided_q(pkv, orc):
+    """fp16 cache with head_dim 64 (the tiny shape scaled up) and q / out
+    views with padded row strides."""
+    w = W.gqa_bf16(batch=5, ctx_lo=1, ctx_hi=900, num_heads=8, num_kv_heads=4, head_dim=64, seed=66)
+    w.dtype = torch.float16
+    w.cache_kind = "f16"
+    for name in ("q", "k_cache0", "v_cache0", "k_new", "v_new"):
+        setattr(w, name, getattr(w, name).to(torch.float16))
+    cache, out = PL.gpu_run(w, pkv, num_splits=0)
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    _check(w, out, ref)
+    qpad = torch.zeros((w.batch, w.num_heads, w.head_dim + 8), dtype=w.dtype, device="cuda")
+    qpad[..., :w.head_dim] = w.q.cuda()
+    opad = torch.zeros_like(qpad)
+    pkv.paged_decode(qpad[..., :w.head_dim], cache, w.block_tables.cuda(), w.context_lens.cuda(),
+                     sm_scale=w.sm_scale, out=opad[..., :w.head_dim])
+    torch.cuda.synchronize()
+    _check(w, opad[..., :w.head_dim], ref)
+
+
 def test_split_count_invariance(pkv):
     w = W.gqa_bf16(batch=4, ctx_lo=50, ctx_hi=3000, seed=35)
-    outs = [PL.out_f64(PL.gpu_run(w, pkv, num_splits=s)[1]) for s in (1, 2, 7, 16)]
+    outs = [PL.out_f64(PL.gpu_run(w, pkv, num_splits=s)[1]) for s in (1, 0, 2, 7, 16)]
     for o in outs[1:]:
         assert np.max(np.abs(o - outs[0])) <= 2e-2
 
@@ -104,7 +134,7 @@ def test_empty_and_single_token_contexts(pkv, orc):
     # keep the appended token inside the context of every sequence
     w.new_pos[:] = torch.clamp(w.context_lens - 1, min=0)
     w.new_pos[0] = -1
-    for splits in (1, 3):
+    for splits in (0, 1, 3):
         _, out = PL.gpu_run(w, pkv, num_splits=splits)
         ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
         _check(w, out, ref)
@@ -125,7 +155,7 @@ def test_poison_beyond_context(pkv, orc):
         cache.k_cache[dead] = float("nan")
         cache.v_cache[dead] = float("nan")
 
-    for splits in (1, 4):
+    for splits in (0, 1, 4):
         _, clean = PL.gpu_run(w, pkv, num_splits=splits)
         _, dirty = PL.gpu_run(w, pkv, num_splits=splits, poison=poison)
         assert torch.isfinite(dirty.float()).all()
