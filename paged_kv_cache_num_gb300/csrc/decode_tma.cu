@@ -27,12 +27,13 @@
 // (one per lane) and issues, per block, TMA tensor copies of the K and V
 // tiles [nh heads][block_size tokens][head_dim] (128-byte swizzled rows) into
 // a ring of `stages` shared-memory stages guarded by full/empty mbarriers.
-// Each consumer warp computes, for its kv head and the G query heads that
-// share it (the M dimension of m16n8k16 mma.sync, rows >= G are zero):
-//   S = Q K^T (K from shared memory by ldmatrix, or fp8 bytes converted to
-//   f16 in registers), masking of tokens >= context_len, online softmax in
-//   log2 units, O = O * alpha + P V (P reused from the S accumulators as the
-//   A operand, V by ldmatrix.trans or fp8 -> f16 conversion).
+// Each consumer warp computes, for its kv head and the G <= 8 query heads
+// that share it, with m16n8k16 mma.sync (block tokens on M, q heads on N):
+//   S^T = K Q^T (K from shared memory by ldmatrix, or fp8 bytes converted to
+//   f16 in registers), masking of tokens >= context_len, online softmax per
+//   q head in log2 units, O^T = O^T * alpha + V^T P^T (P^T moved from the
+//   score accumulators into operand layout by movmatrix; V^T by
+//   ldmatrix.trans or fp8 byte pairing + conversion).
 // Every wait is bounded (about 2 s of wall time) and raises
 // PKV_DEVERR_TIMEOUT instead of hanging.
 #include <cudaTypedefs.h>
@@ -106,13 +107,6 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
 {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
-__device__ __forceinline__ uint2 ld_shared_u64(uint32_t a)
-{
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
     return v;
 }
 
@@ -201,6 +195,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         bool aborted = false;
         int64_t issued = 0;
+        int ps = 0;              // next stage to fill
+        uint32_t pphase = 0;     // completed-round parity of that stage
         for (int64_t base = lo; base < hi && !aborted; base += 32) {
             const int64_t x = base + lane;
             int pb = -1, hg = 0;
@@ -220,11 +216,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int pbk = __shfl_sync(0xffffffffu, pb, k);
                 const int hgk = __shfl_sync(0xffffffffu, hg, k);
                 if (lane == 0 && !aborted) {
-                    const int64_t it = base - lo + k;
-                    const int s = int(it % stages);
-                    const int64_t round = it / stages;
-                    if (round > 0 &&
-                        !ptx::mbar_wait_bounded(bar_empty + 8 * s, uint32_t((round - 1) & 1), kTimeoutNs)) {
+                    const int s = ps;
+                    const bool reuse = issued >= stages;     // stage held a block before
+                    const uint32_t par = pphase ^ 1u;
+                    if (++ps == stages) {
+                        ps = 0;
+                        pphase ^= 1u;
+                    }
+                    if (reuse && !ptx::mbar_wait_bounded(bar_empty + 8 * s, par, kTimeoutNs)) {
                         raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
                         aborted = true;
                     } else {
@@ -256,12 +255,17 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (lane == 0) {
             for (int64_t it = issued > stages ? issued - stages : 0; it < issued; ++it)
                 ptx::mbar_wait_bounded(bar_full + 8 * int(it % stages), uint32_t((it / stages) & 1),
-                                       kTimeoutNs);
+                                       kTimeoutNs);   // once per CTA, off the hot loop
         }
         return;
     }
 
     // ======================================================== consumer warps
+    // Tokens on the MMA's M dimension, the group's q heads on N (G <= 8):
+    //   S^T[tok][head] = K[tok][:] . Q[head][:]        (A = K, B = Q^T)
+    //   O^T[d][head]  += V^T[d][tok] P^T[tok][head]     (A = V^T, B = P^T)
+    // A thread of the C fragments holds heads 2tig, 2tig+1 for tokens
+    // (or d) gid and gid+8 of each 16-row tile.
     const int gid = lane >> 2, tig = lane & 3;
     const float log2e_scale = p.scale_log2;
     // walk state
@@ -275,9 +279,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     int64_t seg_start = lo;
 
-    uint32_t qa[T::QK][4];
-    float o[T::DT][4];
-    float m[2], l[2];
+    uint32_t qb[T::QK][2];        // B fragments of Q^T per k-step
+    float o[T::DT / 2][4];        // O^T accumulators: 16-d tiles x (heads 2tig, 2tig+1)
+    float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
     float mult = 1.0f, vmul = 1.0f;
     int ctx_b = 0;
 
@@ -287,76 +291,65 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const int cb = p.context_lens[b * p.cl_stride];
             ctx_b = cb < 0 ? 0 : (cb > cap ? cap : cb);
         }
-        const bool r0 = gid < G, r1 = gid + 8 < G;
-        const uint16_t *q0 = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
-        const uint16_t *q1 = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid + 8) * p.q_h);
+        const bool hv = gid < G;  // this lane's B column (q head gid) exists
+        const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
         if constexpr (!T::kFp8) {
 #pragma unroll
             for (int kk = 0; kk < T::QK; ++kk) {
                 const int d = 16 * kk + 2 * tig;
-                qa[kk][0] = r0 ? *reinterpret_cast<const uint32_t *>(q0 + d) : 0u;
-                qa[kk][1] = r1 ? *reinterpret_cast<const uint32_t *>(q1 + d) : 0u;
-                qa[kk][2] = r0 ? *reinterpret_cast<const uint32_t *>(q0 + d + 8) : 0u;
-                qa[kk][3] = r1 ? *reinterpret_cast<const uint32_t *>(q1 + d + 8) : 0u;
+                qb[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qr + d) : 0u;
+                qb[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qr + d + 8) : 0u;
             }
             mult = log2e_scale;
             vmul = 1.0f;
         } else {
-            // q (16-bit) -> f16 operands, with the element order matching the
-            // fp8 K fragments: k-step 2kp+s, thread tig holds d = 32kp + 8tig
-            // + 4s + {0,1} (k = 2tig, 2tig+1) and + {2,3} (k = 2tig+8, +9).
-            float qf[2][D / 4];
+            // q (16-bit) -> f16 operands in the element order of the fp8 K
+            // fragments: k-step kk, lane tig holds d = 16kk + 4tig + {0,1}
+            // (k = 2tig, 2tig+1) and + {2,3} (k = 2tig+8, 2tig+9).  A
+            // power-of-two pre-scale keeps every element inside f16 range.
+            float f[T::QK][4];
             float amax = 0.0f;
 #pragma unroll
-            for (int kp = 0; kp < D / 32; ++kp) {
-                const int d = 32 * kp + 8 * tig;
+            for (int kk = 0; kk < T::QK; ++kk) {
+                uint2 u = make_uint2(0, 0);
+                if (hv) u = *reinterpret_cast<const uint2 *>(qr + 16 * kk + 4 * tig);
+                const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const bool ok = rr ? r1 : r0;
-                    uint4 u = make_uint4(0, 0, 0, 0);
-                    if (ok) u = *reinterpret_cast<const uint4 *>((rr ? q1 : q0) + d);
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float a, c;
-                        if (p.q_is_bf16) {
-                            a = __uint_as_float(w[e] << 16);
-                            c = __uint_as_float(w[e] & 0xffff0000u);
-                        } else {
-                            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-                            a = t.x;
-                            c = t.y;
-                        }
-                        qf[rr][8 * kp + 2 * e] = a;
-                        qf[rr][8 * kp + 2 * e + 1] = c;
-                        amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c)));
+                for (int e = 0; e < 2; ++e) {
+                    if (p.q_is_bf16) {
+                        f[kk][2 * e] = __uint_as_float(w[e] << 16);
+                        f[kk][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+                    } else {
+                        const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                        f[kk][2 * e] = t.x;
+                        f[kk][2 * e + 1] = t.y;
                     }
+                    amax = fmaxf(amax, fmaxf(fabsf(f[kk][2 * e]), fabsf(f[kk][2 * e + 1])));
                 }
             }
 #pragma unroll
             for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
-            // power-of-two pre-scale that keeps every q element inside f16 range
             float qs = 1.0f;
             while (amax * qs > 16384.0f) qs *= 0.5f;
-            float dummy0, dummy1;
+            float d0, d1;
 #pragma unroll
-            for (int kp = 0; kp < D / 32; ++kp) {
-#pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                    const int e = 8 * kp + 4 * s2;
-                    qa[2 * kp + s2][0] = pack_f16(qf[0][e] * qs, qf[0][e + 1] * qs, dummy0, dummy1);
-                    qa[2 * kp + s2][1] = pack_f16(qf[1][e] * qs, qf[1][e + 1] * qs, dummy0, dummy1);
-                    qa[2 * kp + s2][2] = pack_f16(qf[0][e + 2] * qs, qf[0][e + 3] * qs, dummy0, dummy1);
-                    qa[2 * kp + s2][3] = pack_f16(qf[1][e + 2] * qs, qf[1][e + 3] * qs, dummy0, dummy1);
-                }
+            for (int kk = 0; kk < T::QK; ++kk) {
+                qb[kk][0] = pack_f16(f[kk][0] * qs, f[kk][1] * qs, d0, d1);
+                qb[kk][1] = pack_f16(f[kk][2] * qs, f[kk][3] * qs, d0, d1);
             }
             mult = log2e_scale * p.k_scale[kvh] / qs;
             vmul = p.v_scale[kvh];
         }
 #pragma unroll
-        for (int t = 0; t < T::DT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
+        for (int t = 0; t < T::DT / 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
         m[0] = m[1] = NEG_INF;
         l[0] = l[1] = 0.0f;
+    };
+
+    // d held by this lane for accumulator tile t, row half r (0: gid, 1: gid+8)
+    auto d_of = [&](int t, int r) -> int {
+        if constexpr (!T::kFp8) return 16 * t + 8 * r + gid;
+        else return 32 * (t >> 1) + 4 * gid + 2 * (t & 1) + r;
     };
 
     auto finish_segment = [&](int64_t seg_end) {
@@ -365,239 +358,197 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const int64_t unit_last = unit_first + nblk[b] - 1;
         float lt[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            lt[r] = l[r] + __shfl_xor_sync(0xffffffffu, l[r], 1);
-            lt[r] += __shfl_xor_sync(0xffffffffu, lt[r], 2);
+        for (int c = 0; c < 2; ++c) {       // sum the partial sums over the 8 token rows (gid)
+            float v = l[c];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            lt[c] = v;
         }
         const bool whole = seg_start == unit_first && seg_end == unit_last;
         const int64_t key = int64_t(blockIdx.x) + int64_t(hg) * B + b;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int g = gid + 8 * r;
+        for (int c = 0; c < 2; ++c) {
+            const int g = 2 * tig + c;
             if (g >= G) continue;
             const int h = kvh * G + g;
             if (whole) {
-                const float inv = lt[r] > 0.0f ? vmul / lt[r] : 0.0f;
+                const float inv = lt[c] > 0.0f ? vmul / lt[c] : 0.0f;
                 uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
-                if constexpr (!T::kFp8) {
 #pragma unroll
-                    for (int t = 0; t < T::DT; ++t) {
-                        const float v0 = o[t][2 * r] * inv, v1 = o[t][2 * r + 1] * inv;
-                        uint32_t w;
-                        if (p.q_is_bf16) {
-                            const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
-                            w = *reinterpret_cast<const uint32_t *>(&hv);
-                        } else {
-                            const __half2 hv = __floats2half2_rn(v0, v1);
-                            w = *reinterpret_cast<const uint32_t *>(&hv);
-                        }
-                        if (p.out_vec_ok) {
-                            *reinterpret_cast<uint32_t *>(orow + 8 * t + 2 * tig) = w;
-                        } else {
-                            orow[8 * t + 2 * tig] = uint16_t(w);
-                            orow[8 * t + 2 * tig + 1] = uint16_t(w >> 16);
-                        }
+                for (int t = 0; t < T::DT / 2; ++t)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float v = o[t][2 * r + c] * inv;
+                        orow[d_of(t, r)] = p.q_is_bf16 ? f2h<kBF16>(v) : f2h<kF16>(v);
                     }
-                } else {
-#pragma unroll
-                    for (int q4 = 0; q4 < D / 32; ++q4) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            // elements 2e, 2e+1 of d = 32q4 + 8tig + {0..7}
-                            const int e0 = 2 * e, e1 = 2 * e + 1;
-                            const float v0 = o[4 * q4 + (e0 & 3)][2 * r + (e0 >> 2)] * inv;
-                            const float v1 = o[4 * q4 + (e1 & 3)][2 * r + (e1 >> 2)] * inv;
-                            if (p.q_is_bf16) {
-                                const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
-                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
-                            } else {
-                                const __half2 hv = __floats2half2_rn(v0, v1);
-                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
-                            }
-                        }
-                        if (p.out_vec_ok) {
-                            *reinterpret_cast<uint4 *>(orow + 32 * q4 + 8 * tig) = make_uint4(w[0], w[1], w[2], w[3]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                orow[32 * q4 + 8 * tig + e] = uint16_t(w[e >> 1] >> (16 * (e & 1)));
-                        }
-                    }
-                }
             } else {
                 const int64_t row = key * (int64_t(nh) * G) + int64_t(warp) * G + g;
                 float *acc = f.part_acc + row * D;
-                if (tig == 0) {
-                    f.part_ml[2 * row] = m[r];
-                    f.part_ml[2 * row + 1] = lt[r];
+                if (gid == 0) {
+                    f.part_ml[2 * row] = m[c];
+                    f.part_ml[2 * row + 1] = lt[c];
                 }
-                if constexpr (!T::kFp8) {
 #pragma unroll
-                    for (int t = 0; t < T::DT; ++t)
-                        *reinterpret_cast<float2 *>(acc + 8 * t + 2 * tig) =
-                            make_float2(o[t][2 * r] * vmul, o[t][2 * r + 1] * vmul);
-                } else {
+                for (int t = 0; t < T::DT / 2; ++t)
 #pragma unroll
-                    for (int q4 = 0; q4 < D / 32; ++q4) {
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = o[4 * q4 + (e & 3)][2 * r + (e >> 2)] * vmul;
-                        *reinterpret_cast<float4 *>(acc + 32 * q4 + 8 * tig) = make_float4(v[0], v[1], v[2], v[3]);
-                        *reinterpret_cast<float4 *>(acc + 32 * q4 + 8 * tig + 4) = make_float4(v[4], v[5], v[6], v[7]);
-                    }
-                }
+                    for (int r = 0; r < 2; ++r) acc[d_of(t, r)] = o[t][2 * r + c] * vmul;
             }
         }
     };
 
     start_segment();
-    for (int64_t it = 0; x < hi; ++x, ++it) {
-        const int s = int(it % stages);
-        if (!ptx::mbar_wait_bounded(bar_full + 8 * s, uint32_t((it / stages) & 1), kTimeoutNs)) {
+    int cs = 0;                  // stage of the current block
+    uint32_t cphase = 0;         // parity of its fill round
+    for (; x < hi; ++x) {
+        const int s = cs;
+        if (!ptx::mbar_wait_bounded(bar_full + 8 * s, cphase, kTimeoutNs)) {
             raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
             return;
+        }
+        if (++cs == stages) {
+            cs = 0;
+            cphase ^= 1u;
         }
         // valid tokens of this block (only the last block of a sequence is partial)
         const int valid = min(BS, ctx_b - j * BS);
         if (stage_ok[s]) {
-            const uint32_t ktile = sbase + s * L.stage_bytes;
+            const uint32_t ktile = sbase + s * L.stage_bytes + warp * BS * 128;
             const uint32_t vtile = ktile + L.tile_bytes;
             const int half_bytes = L.tile_bytes / T::HALVES;
-            // ---------------- S = Q K^T
-            float sc[T::NT][4];
+            const int mi = lane >> 3;    // ldmatrix: which 8x8 matrix this lane addresses
+            // ---------------- S^T = K Q^T
+            float sc[T::KT][4];
 #pragma unroll
-            for (int t = 0; t < T::NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.0f;
-            if constexpr (!T::kFp8) {
+            for (int t = 0; t < T::KT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.0f;
 #pragma unroll
-                for (int kk = 0; kk < T::QK; ++kk) {
+            for (int kk = 0; kk < T::QK; ++kk) {
 #pragma unroll
-                    for (int ntp = 0; ntp < T::NT / 2; ++ntp) {
-                        const int tok = 16 * ntp + 8 * (lane >> 4) + (lane & 7);
-                        const int chunk = 2 * kk + ((lane >> 3) & 1);
-                        const uint32_t addr = ktile + (chunk >> 3) * half_bytes + (warp * BS + tok) * 128 +
-                                              (((chunk & 7) ^ (tok & 7)) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
-                        ptx::mma16816<T::kBF>(sc[2 * ntp], qa[kk], b0, b1);
-                        ptx::mma16816<T::kBF>(sc[2 * ntp + 1], qa[kk], b2, b3);
+                for (int mt = 0; mt < T::KT; ++mt) {
+                    uint32_t a[4];
+                    if constexpr (!T::kFp8) {
+                        // matrices: (tok 0-7 | 8-15) x (d chunk 2kk | 2kk+1)
+                        const int tok = 16 * mt + 8 * (mi & 1) + (lane & 7);
+                        const int chunk = 2 * kk + (mi >> 1);
+                        ptx::ldmatrix_x4(ktile + (chunk >> 3) * half_bytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4),
+                                         a[0], a[1], a[2], a[3]);
+                    } else {
+                        const int t0 = 16 * mt + gid, t1 = t0 + 8;
+                        const uint32_t w0 = ld_shared_u32(ktile + t0 * 128 + (((kk & 7) ^ (t0 & 7)) << 4) + 4 * tig);
+                        const uint32_t w1 = ld_shared_u32(ktile + t1 * 128 + (((kk & 7) ^ (t1 & 7)) << 4) + 4 * tig);
+                        a[0] = f16x2_from_e4m3x2(w0);
+                        a[1] = f16x2_from_e4m3x2(w1);
+                        a[2] = f16x2_from_e4m3x2(w0 >> 16);
+                        a[3] = f16x2_from_e4m3x2(w1 >> 16);
                     }
-                }
-            } else {
-#pragma unroll
-                for (int kp = 0; kp < D / 32; ++kp) {
-#pragma unroll
-                    for (int nt = 0; nt < T::NT; ++nt) {
-                        const int tok = 8 * nt + gid;
-                        const int chunk = 2 * kp + (tig >> 1);
-                        const uint32_t addr = ktile + (warp * BS + tok) * 128 + (((chunk & 7) ^ (tok & 7)) << 4) +
-                                              (tig & 1) * 8;
-                        const uint2 w = ld_shared_u64(addr);
-                        ptx::mma16816<false>(sc[nt], qa[2 * kp], f16x2_from_e4m3x2(w.x), f16x2_from_e4m3x2(w.x >> 16));
-                        ptx::mma16816<false>(sc[nt], qa[2 * kp + 1], f16x2_from_e4m3x2(w.y),
-                                             f16x2_from_e4m3x2(w.y >> 16));
-                    }
+                    ptx::mma16816<T::kBF>(sc[mt], a, qb[kk][0], qb[kk][1]);
                 }
             }
-            // ---------------- online softmax (log2 units)
+            // ---------------- online softmax per q head (columns), log2 units
+            const bool partial = valid < BS;   // only a sequence's last block
             float mx[2] = {NEG_INF, NEG_INF};
 #pragma unroll
-            for (int t = 0; t < T::NT; ++t) {
+            for (int t = 0; t < T::KT; ++t) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int tok = 8 * t + 2 * tig + (e & 1);
                     float v = sc[t][e] * mult;
-                    v = tok < valid ? v : NEG_INF;
+                    if (partial) {
+                        const int tok = 16 * t + gid + 8 * (e >> 1);
+                        v = tok < valid ? v : NEG_INF;
+                    }
                     sc[t][e] = v;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
+                    mx[e & 1] = fmaxf(mx[e & 1], v);
                 }
             }
             float alpha[2];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float mn = fmaxf(m[r], mx[r]);
-                alpha[r] = mn == NEG_INF ? 1.0f : exp2_approx(m[r] - mn);
-                m[r] = mn;
+            for (int c = 0; c < 2; ++c) {
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+                const float mn = fmaxf(m[c], mx[c]);
+                alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
+                m[c] = mn;
+                l[c] *= alpha[c];
             }
-            uint32_t pa[T::KT][4];
-            float ls[2] = {0.0f, 0.0f};
+            // P^T as the B operand of the PV product: pack each 8-token half
+            // of a tile (rows = tokens, cols = heads) and transpose it in
+            // registers, giving lane (gid, tig) tokens 2tig, 2tig+1 of head gid.
+            uint32_t pb[T::KT][2];
 #pragma unroll
-            for (int t = 0; t < T::NT; ++t) {
+            for (int t = 0; t < T::KT; ++t) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float p0 = exp2_approx(sc[t][2 * r] - m[r]);
-                    const float p1 = exp2_approx(sc[t][2 * r + 1] - m[r]);
+                    const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
+                    const float p1 = exp2_approx(sc[t][2 * r + 1] - m[1]);
+                    l[0] += p0;
+                    l[1] += p1;
                     float q0, q1;
                     const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0, p1, q0, q1);
-                    ls[r] += q0 + q1;
-                    // A fragment of the PV product: k-step t/2, register (t&1)*2 + r
-                    pa[t >> 1][(t & 1) * 2 + r] = w;
+                    pb[t][r] = ptx::movmatrix_trans(w);
                 }
             }
+            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + ls[r];
-#pragma unroll
-            for (int t = 0; t < T::DT; ++t) {
-                o[t][0] *= alpha[0];
-                o[t][1] *= alpha[0];
-                o[t][2] *= alpha[1];
-                o[t][3] *= alpha[1];
+                for (int t = 0; t < T::DT / 2; ++t) {
+                    o[t][0] *= alpha[0];
+                    o[t][1] *= alpha[1];
+                    o[t][2] *= alpha[0];
+                    o[t][3] *= alpha[1];
+                }
             }
-            // ---------------- O += P V
-            const bool partial = valid < BS;
-            if constexpr (!T::kFp8) {
+            // ---------------- O^T += V^T P^T
 #pragma unroll
-                for (int kt = 0; kt < T::KT; ++kt) {
+            for (int kt = 0; kt < T::KT; ++kt) {
+                if constexpr (!T::kFp8) {
                     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (partial) {
+                    if (partial) {  // zero V of masked tokens (0 * NaN would poison O)
                         const int t0 = 16 * kt + 2 * tig;
                         mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
                         mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
                     }
 #pragma unroll
-                    for (int ndp = 0; ndp < T::DT / 2; ++ndp) {
-                        const int tok = 16 * kt + 8 * ((lane >> 3) & 1) + (lane & 7);
-                        const int chunk = 2 * ndp + (lane >> 4);
-                        const uint32_t addr = vtile + (chunk >> 3) * half_bytes + (warp * BS + tok) * 128 +
-                                              (((chunk & 7) ^ (tok & 7)) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-                        b0 &= mlo;
-                        b2 &= mlo;
-                        b1 &= mhi;
-                        b3 &= mhi;
-                        ptx::mma16816<T::kBF>(o[2 * ndp], pa[kt], b0, b1);
-                        ptx::mma16816<T::kBF>(o[2 * ndp + 1], pa[kt], b2, b3);
+                    for (int md = 0; md < T::DT / 2; ++md) {
+                        // matrices: (tok 0-7 | 8-15) x (d chunk 2md | 2md+1), transposed
+                        const int tok = 16 * kt + 8 * (mi >> 1) + (lane & 7);
+                        const int chunk = 2 * md + (mi & 1);
+                        uint32_t a[4];
+                        ptx::ldmatrix_x4_trans(vtile + (chunk >> 3) * half_bytes + tok * 128 +
+                                                   (((chunk & 7) ^ (tok & 7)) << 4),
+                                               a[0], a[1], a[2], a[3]);
+                        a[0] &= mlo;
+                        a[1] &= mlo;
+                        a[2] &= mhi;
+                        a[3] &= mhi;
+                        ptx::mma16816<T::kBF>(o[md], a, pb[kt][0], pb[kt][1]);
                     }
-                }
-            } else {
-#pragma unroll
-                for (int kt = 0; kt < T::KT; ++kt) {
+                } else {
                     const int t0 = 16 * kt + 2 * tig;
                     const int rows[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
 #pragma unroll
                     for (int q4 = 0; q4 < D / 32; ++q4) {
+                        // bytes d = 32q4 + 4gid .. +3 of the four token rows;
+                        // tile 2q4 takes bytes 0 (rows gid) and 1 (rows gid+8),
+                        // tile 2q4+1 bytes 2 and 3
                         const int chunk = 2 * q4 + (gid >> 2);
                         uint32_t w[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int tok = rows[i];
-                            w[i] = ld_shared_u32(vtile + (warp * BS + tok) * 128 + (((chunk & 7) ^ (tok & 7)) << 4) +
-                                                 (gid & 3) * 4);
+                            w[i] = ld_shared_u32(vtile + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4) + (gid & 3) * 4);
                             if (partial && tok >= valid) w[i] = 0u;
                         }
 #pragma unroll
-                        for (int jj = 0; jj < 4; jj += 2) {
-                            // bytes jj, jj+1 of (w0, w1) and of (w2, w3), paired by token
-                            const uint32_t sel = jj | ((jj + 4) << 4) | ((jj + 1) << 8) | ((jj + 5) << 12);
-                            const uint32_t a01 = ptx::prmt(w[0], w[1], sel);
-                            const uint32_t a23 = ptx::prmt(w[2], w[3], sel);
-                            ptx::mma16816<false>(o[4 * q4 + jj], pa[kt], f16x2_from_e4m3x2(a01),
-                                                 f16x2_from_e4m3x2(a23));
-                            ptx::mma16816<false>(o[4 * q4 + jj + 1], pa[kt], f16x2_from_e4m3x2(a01 >> 16),
-                                                 f16x2_from_e4m3x2(a23 >> 16));
+                        for (int hb = 0; hb < 2; ++hb) {
+                            const uint32_t sel = (2 * hb) | ((2 * hb + 4) << 4) | ((2 * hb + 1) << 8) | ((2 * hb + 5) << 12);
+                            const uint32_t x01 = ptx::prmt(w[0], w[1], sel);
+                            const uint32_t x23 = ptx::prmt(w[2], w[3], sel);
+                            uint32_t a[4];
+                            a[0] = f16x2_from_e4m3x2(x01);
+                            a[1] = f16x2_from_e4m3x2(x01 >> 16);
+                            a[2] = f16x2_from_e4m3x2(x23);
+                            a[3] = f16x2_from_e4m3x2(x23 >> 16);
+                            ptx::mma16816<false>(o[2 * q4 + hb], a, pb[kt][0], pb[kt][1]);
                         }
                     }
                 }
@@ -754,7 +705,7 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
 bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch)
 {
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
-    if (group > 16 || batch > 4096) return false;
+    if (group > 8 || batch > 4096) return false;
     if (cache_kind == kE4M3) return head_dim == 128;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
 }

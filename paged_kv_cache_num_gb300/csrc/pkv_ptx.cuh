@@ -123,6 +123,15 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
+// Transpose an 8x8 b16 matrix held one 32-bit register per lane in the
+// mma fragment layout (lane = 4*row + col/2).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Two e4m3 codes (low byte -> low half) to an f16x2 register (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two)
 {

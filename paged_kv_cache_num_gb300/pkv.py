@@ -187,6 +187,15 @@ class KVCache:
         return c
 
     def _struct(self) -> _Cache:
+        key = tuple((t.data_ptr(), t.dtype, t.shape, t.stride()) for t in self.tensors())
+        cached = self.__dict__.get("_cstruct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
+        s = self._build_struct()
+        self.__dict__["_cstruct"] = (key, s)
+        return s
+
+    def _build_struct(self) -> _Cache:
         s = _Cache()
         code = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "u3": U3}[self.kind]
         s.k_cache = _desc(self.k_cache, code)
@@ -250,9 +259,10 @@ def paged_decode(q, cache: KVCache, block_tables, context_lens, sm_scale: Option
     if out is None:
         out = torch.empty_like(q)
     cs = cache._struct()
-    need = decode_workspace_bytes(q, cache, block_tables, num_splits)
-    if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:
+        need = decode_workspace_bytes(q, cache, block_tables, num_splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
     ws_n = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().pkv_paged_decode(ctypes.byref(_desc(q)), ctypes.byref(cs),

@@ -48,7 +48,7 @@ def test_gqa_bf16_small(pkv, orc, splits):
     _check(w, out, ref)
 
 
-@pytest.mark.parametrize("G,BS,D", [(1, 16, 128), (2, 32, 64), (8, 16, 128), (16, 8, 64),
+@pytest.mark.parametrize("G,BS,D", [(1, 16, 128), (2, 32, 64), (8, 16, 128), (16, 8, 64), (16, 16, 128),
                                     (4, 64, 128), (3, 16, 64)])
 def test_group_block_dim_matrix(pkv, orc, G, BS, D):
     w = W.gqa_bf16(batch=3, ctx_lo=1, ctx_hi=9 * BS + 5, num_heads=2 * G, num_kv_heads=2,

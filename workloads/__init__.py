@@ -179,8 +179,10 @@ def gqa_bf16(device="cpu", batch=64, ctx_lo=512, ctx_hi=4096, num_heads=32, num_
     v_new = _randn((B, Hkv, D), g, device, dt)
     new_req = torch.arange(B, dtype=torch.int32, device=device)
     new_pos = (ctx - 1).to(torch.int32)
-    return Workload("gqa_bf16", dt, "bf16", B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
-                    k_new, v_new, k_cache0, v_cache0)
+    w = Workload("gqa_bf16", dt, "bf16", B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
+                 k_new, v_new, k_cache0, v_cache0)
+    w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
+    return w
 
 
 def mixed_append(device="cpu", n_prefill=8, n_decode=56, prefill_lo=128, prefill_hi=2048,
@@ -224,6 +226,8 @@ def mixed_append(device="cpu", n_prefill=8, n_decode=56, prefill_lo=128, prefill
     w = Workload("mixed_append", dt, "bf16", B, Hkv, Hkv, D, BS, P, ctx, bt, None, new_req,
                  new_pos, k_new, v_new, k_cache0, v_cache0)
     w.extra["n_real_tokens"] = n_real
+    w.extra["context"] = "prefill U{%d..%d} + decode U{%d..%d}" % (prefill_lo, prefill_hi, ctx_lo,
+                                                                   ctx_hi)
     return w
 
 
@@ -261,9 +265,11 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
     v_new = _randn((B, Hkv, D), g, device, dt)
     new_req = torch.arange(B, dtype=torch.int32, device=device)
     new_pos = (ctx - 1).to(torch.int32)
-    return Workload("fp8_long", dt, "e4m3", B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
-                    k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
-                    v_fill=v_fill, k_scale=k_scale.contiguous(), v_scale=v_scale.contiguous())
+    w = Workload("fp8_long", dt, "e4m3", B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
+                 k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
+                 v_fill=v_fill, k_scale=k_scale.contiguous(), v_scale=v_scale.contiguous())
+    w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
+    return w
 
 
 def u3_mha(device="cpu", batch=32, ctx_lo=1024, ctx_hi=8192, num_heads=32, head_dim=128,
@@ -287,9 +293,11 @@ def u3_mha(device="cpu", batch=32, ctx_lo=1024, ctx_hi=8192, num_heads=32, head_
     v_new = _randn((B, H, D), g, device, dt)
     new_req = torch.arange(B, dtype=torch.int32, device=device)
     new_pos = (ctx - 1).to(torch.int32)
-    return Workload("u3_mha", dt, "u3", B, H, H, D, BS, P, ctx, bt, q, new_req, new_pos,
-                    k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
-                    v_fill=v_fill)
+    w = Workload("u3_mha", dt, "u3", B, H, H, D, BS, P, ctx, bt, q, new_req, new_pos,
+                 k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
+                 v_fill=v_fill)
+    w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
+    return w
 
 
 def all_octets() -> torch.Tensor:
