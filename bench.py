@@ -40,6 +40,12 @@ import torch  # noqa: E402
 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
+# sources of the decode kernels; a recorded ncu traffic figure is only used
+# while these are unchanged
+DECODE_SOURCES = ("paged_kv_cache_num_gb300/csrc/decode_tma.cu",
+                  "paged_kv_cache_num_gb300/csrc/decode.cu",
+                  "paged_kv_cache_num_gb300/csrc/pkv_ptx.cuh",
+                  "paged_kv_cache_num_gb300/csrc/pkv_device.cuh")
 
 
 class L2Flush:
@@ -505,7 +511,7 @@ def main():
 
     # ---------------- roofline of the dominant operation (paged_decode)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
-    src = source_hash("paged_kv_cache_num_gb300/csrc/decode.cu")
+    src = source_hash(*DECODE_SOURCES)
     traffic = profile_traffic("paged_decode:" + args.workload, src)
     roofline = {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(dec_gbs / peak, 4), "traffic": traffic,

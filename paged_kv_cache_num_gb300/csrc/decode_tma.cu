@@ -50,16 +50,19 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 #define NEG_INF (-__int_as_float(0x7f800000))
 
 struct SmemLayout {
-    int tile_bytes, stage_bytes, bars_off, ok_off, prefix_off, nblk_off, total;
+    int tile_bytes, stage_bytes, f16_off, bars_off, ok_off, prefix_off, nblk_off, total;
 };
 
+// [stages x (K tile, V tile)] [f16 staging: nh x bs x head_dim halves, 3-bit
+// caches only] [mbarriers] [per-stage block ids] [prefix sums] [block counts]
 __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
-                                                  int batch)
+                                                  int batch, int f16_row_bytes = 0)
 {
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
     L.stage_bytes = 2 * L.tile_bytes;
-    L.bars_off = stages * L.stage_bytes;
+    L.f16_off = stages * L.stage_bytes;
+    L.bars_off = L.f16_off + nh * bs * f16_row_bytes;
     L.ok_off = L.bars_off + 2 * stages * 8;
     L.prefix_off = L.ok_off + stages * 4;
     L.nblk_off = L.prefix_off + (batch + 1) * 4;
@@ -110,17 +113,80 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
     return v;
 }
 
-// CK: cache kind (kF16 / kBF16 / kE4M3); D head_dim; BS block size.
+// ---------------------------------------------------------------- 3-bit
+// Lanes of a 96-bit group (lane i = bits 3i..3i+2) are converted two at a
+// time: pair p = (i, j) sits in one 32-bit window of the group at bits x and
+// 16 + y, so (window & mask) | 0x64006400 is the f16 pair
+// (1024 + 2^x v_i, 1024 + 2^y v_j) -- exact, one shift and one LOP3.  Every
+// x, y is >= 5, which keeps the 1024 offset within a factor ~9 of the value
+// term (the offset and the zero point are removed in fp32 afterwards).  The
+// 32 lanes are covered exactly once.
+struct U3Pair {
+    int i, j, x, y;
+};
+__host__ __device__ constexpr U3Pair u3_pair_info(int p)
+{
+    switch (p) {
+    case 0: return {0, 5, 6, 5};
+    case 1: return {1, 6, 6, 5};
+    case 2: return {2, 7, 6, 5};
+    case 3: return {3, 8, 6, 5};
+    case 4: return {4, 9, 6, 5};
+    case 5: return {10, 15, 6, 5};
+    case 6: return {11, 16, 6, 5};
+    case 7: return {12, 17, 6, 5};
+    case 8: return {13, 18, 6, 5};
+    case 9: return {14, 19, 6, 5};
+    case 10: return {20, 25, 6, 5};
+    case 11: return {21, 27, 5, 7};
+    case 12: return {22, 28, 5, 7};
+    case 13: return {23, 29, 5, 7};
+    case 14: return {24, 30, 5, 7};
+    default: return {26, 31, 6, 5};
+    }
+}
+// stored index s (mod 32) of a converted group -> lane and its 2^x factor:
+// s = 2p + e holds lane (e ? j : i) of pair p
+__constant__ uint8_t c_u3_lane[32] = {0,  5,  1,  6,  2,  7,  3,  8,  4,  9,  10, 15, 11, 16, 12, 17,
+                                      13, 18, 14, 19, 20, 25, 21, 27, 22, 28, 23, 29, 24, 30, 26, 31};
+__constant__ uint8_t c_u3_x[32] = {6, 5, 6, 5, 6, 5, 6, 5, 6, 5, 6, 5, 6, 5, 6, 5,
+                                   6, 5, 6, 5, 6, 5, 5, 7, 5, 7, 5, 7, 5, 7, 6, 5};
+
+// Pair p of the group held in words (w0, w1, w2); p is a constant after
+// unrolling, so the shift / funnel choice folds away.
+__device__ __forceinline__ uint32_t u3_pair(int p, uint32_t w0, uint32_t w1, uint32_t w2)
+{
+    const U3Pair pr = u3_pair_info(p);
+    const int sh = 3 * pr.i - pr.x;
+    uint32_t win;
+    if (sh < 0) {
+        win = w0 << (-sh);
+    } else {
+        const int w = sh >> 5, off = sh & 31;
+        const uint32_t lo = w == 0 ? w0 : (w == 1 ? w1 : w2);
+        if (off + 16 + pr.y + 3 <= 32) {
+            win = lo >> off;
+        } else {
+            const uint32_t hi = w == 0 ? w1 : w2;
+            win = __funnelshift_r(lo, hi, off);
+        }
+    }
+    const uint32_t mask = (7u << pr.x) | (7u << (16 + pr.y));
+    return (win & mask) | 0x64006400u;
+}
+
+// CK: cache kind (kF16 / kBF16 / kE4M3 / kU3); D head_dim; BS block size.
 // MMA operand type: bf16 for bf16 caches, f16 otherwise (fp8 codes convert
 // exactly to f16).
 template <int CK, int D, int BS>
 struct Tile {
     static constexpr bool kFp8 = CK == kE4M3;
+    static constexpr bool kIsU3 = CK == pkv::kU3;
     static constexpr bool kBF = CK == kBF16;
-    static constexpr int ES = kFp8 ? 1 : 2;
-    static constexpr int ROW = D * ES;              // bytes per token row
-    static constexpr int HALVES = ROW / 128;        // 128-byte swizzled sub-rows
-    static constexpr int NT = BS / 8;               // score n-tiles
+    static constexpr int ES = (kFp8 || kIsU3) ? 1 : 2;
+    static constexpr int ROW = kIsU3 ? 3 * D / 8 : D * ES;   // bytes per token row
+    static constexpr int HALVES = kIsU3 ? 1 : ROW / 128;     // 128-byte swizzled sub-rows
+    static constexpr int BOX0 = kIsU3 ? ROW : 128 / ES;      // TMA box inner extent (elements)
     static constexpr int KT = BS / 16;              // PV k-steps
     static constexpr int DT = D / 8;                // output n-tiles
     static constexpr int QK = D / 16;               // QK k-steps
@@ -137,10 +203,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nh = f.nh, B = p.batch, G = p.group, stages = f.stages;
-    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B);
+    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, T::kIsU3 ? 2 * D : 0);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
-    volatile int *stage_ok = reinterpret_cast<volatile int *>(smem + L.ok_off);
+    volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
     int *prefix = reinterpret_cast<int *>(smem + L.prefix_off);
     int *nblk = reinterpret_cast<int *>(smem + L.nblk_off);
 
@@ -230,19 +296,16 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         const uint32_t fb = bar_full + 8 * s;
                         const uint32_t kdst = sbase + s * L.stage_bytes;
                         const uint32_t vdst = kdst + L.tile_bytes;
+                        stage_pb[s] = pbk;
                         if (pbk >= 0) {
-                            stage_ok[s] = 1;
                             ptx::mbar_arrive_expect_tx(fb, uint32_t(L.stage_bytes));
 #pragma unroll
                             for (int h = 0; h < T::HALVES; ++h) {
                                 const int half_bytes = L.tile_bytes / T::HALVES;
-                                ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * (128 / T::ES), 0,
-                                                 hgk * nh, pbk);
-                                ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * (128 / T::ES), 0,
-                                                 hgk * nh, pbk);
+                                ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
                             }
                         } else {
-                            stage_ok[s] = 0;
                             ptx::mbar_arrive(fb);
                         }
                         ++issued;
@@ -284,6 +347,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
     float mult = 1.0f, vmul = 1.0f;
     int ctx_b = 0;
+    // 3-bit only: per head column, 1024 * sum(q') and sum(q' 2^x) of the QK
+    // operand, and the running sum of P' and of P' * zero of the PV operand
+    float c0h[2] = {0.0f, 0.0f}, q1h[2] = {0.0f, 0.0f}, b1[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
 
     auto start_segment = [&]() {
         const int kvh = hg * nh + warp;
@@ -293,7 +359,62 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         const bool hv = gid < G;  // this lane's B column (q head gid) exists
         const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
-        if constexpr (!T::kFp8) {
+        if constexpr (T::kIsU3) {
+            // q' = q * 2^-x (f16) in the pair order of the converted K rows:
+            // k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1) and pair
+            // 2kk+1 (k = 2tig+8, 2tig+9) of 96-bit group tig.
+            float qv[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (hv) u = *reinterpret_cast<const uint4 *>(qr + 32 * tig + 8 * c4);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float a, c;
+                    if (p.q_is_bf16) {
+                        a = __uint_as_float(w[e] << 16);
+                        c = __uint_as_float(w[e] & 0xffff0000u);
+                    } else {
+                        const float2 t2 = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                        a = t2.x;
+                        c = t2.y;
+                    }
+                    qv[8 * c4 + 2 * e] = a;
+                    qv[8 * c4 + 2 * e + 1] = c;
+                    amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c)));
+                }
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+            float qs = 1.0f;
+            while (amax * qs > 16384.0f) qs *= 0.5f;
+            float c0 = 0.0f, q1 = 0.0f;
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp) {
+                const U3Pair pr = u3_pair_info(pp);
+                float ra, rb;
+                const uint32_t w = pack_f16(qv[pr.i] * qs * (1.0f / float(1 << pr.x)),
+                                            qv[pr.j] * qs * (1.0f / float(1 << pr.y)), ra, rb);
+                qb[pp >> 1][pp & 1] = w;
+                c0 += ra + rb;
+                q1 += ra * float(1 << pr.x) + rb * float(1 << pr.y);
+            }
+            c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
+            c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
+            q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+            q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {       // values of head columns 2tig, 2tig+1
+                c0h[c] = 1024.0f * __shfl_sync(0xffffffffu, c0, 4 * (2 * tig + c));
+                q1h[c] = __shfl_sync(0xffffffffu, q1, 4 * (2 * tig + c));
+                b1[c] = 0.0f;
+                zs[c] = 0.0f;
+            }
+            mult = log2e_scale / qs;
+            vmul = 1.0f;
+        } else if constexpr (!T::kFp8) {
 #pragma unroll
             for (int kk = 0; kk < T::QK; ++kk) {
                 const int d = 16 * kk + 2 * tig;
@@ -348,8 +469,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
     // d held by this lane for accumulator tile t, row half r (0: gid, 1: gid+8)
     auto d_of = [&](int t, int r) -> int {
-        if constexpr (!T::kFp8) return 16 * t + 8 * r + gid;
-        else return 32 * (t >> 1) + 4 * gid + 2 * (t & 1) + r;
+        if constexpr (T::kIsU3) {
+            const int sidx = 16 * t + 8 * r + gid;           // stored (converted) index
+            return (sidx & ~31) + c_u3_lane[sidx & 31];
+        } else if constexpr (!T::kFp8) {
+            return 16 * t + 8 * r + gid;
+        } else {
+            return 32 * (t >> 1) + 4 * gid + 2 * (t & 1) + r;
+        }
     };
 
     auto finish_segment = [&](int64_t seg_end) {
@@ -365,6 +492,29 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             v += __shfl_xor_sync(0xffffffffu, v, 16);
             lt[c] = v;
         }
+        float bt[2] = {0.0f, 0.0f}, zt[2] = {0.0f, 0.0f};
+        if constexpr (T::kIsU3) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v = b1[c], z = zs[c];
+#pragma unroll
+                for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                    v += __shfl_xor_sync(0xffffffffu, v, o2);
+                    z += __shfl_xor_sync(0xffffffffu, z, o2);
+                }
+                bt[c] = 1024.0f * v;
+                zt[c] = z;
+            }
+        }
+        // accumulator entry (t, r, c) -> value of the segment's unnormalised output
+        auto oval = [&](int t, int r, int c) -> float {
+            if constexpr (T::kIsU3) {
+                const int sidx = 16 * t + 8 * r + gid;
+                return (o[t][2 * r + c] - bt[c]) * (1.0f / float(1 << c_u3_x[sidx & 31])) - zt[c];
+            } else {
+                return o[t][2 * r + c];
+            }
+        };
         const bool whole = seg_start == unit_first && seg_end == unit_last;
         const int64_t key = int64_t(blockIdx.x) + int64_t(hg) * B + b;
 #pragma unroll
@@ -379,7 +529,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 for (int t = 0; t < T::DT / 2; ++t)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const float v = o[t][2 * r + c] * inv;
+                        const float v = oval(t, r, c) * inv;
                         orow[d_of(t, r)] = p.q_is_bf16 ? f2h<kBF16>(v) : f2h<kF16>(v);
                     }
             } else {
@@ -392,7 +542,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
                 for (int t = 0; t < T::DT / 2; ++t)
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) acc[d_of(t, r)] = o[t][2 * r + c] * vmul;
+                    for (int r = 0; r < 2; ++r) acc[d_of(t, r)] = oval(t, r, c) * vmul;
             }
         }
     };
@@ -412,7 +562,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         // valid tokens of this block (only the last block of a sequence is partial)
         const int valid = min(BS, ctx_b - j * BS);
-        if (stage_ok[s]) {
+        const int spb = stage_pb[s];
+        if (spb >= 0 && !T::kIsU3) {
             const uint32_t ktile = sbase + s * L.stage_bytes + warp * BS * 128;
             const uint32_t vtile = ktile + L.tile_bytes;
             const int half_bytes = L.tile_bytes / T::HALVES;
@@ -554,6 +705,136 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 }
             }
         }
+        if constexpr (T::kIsU3) {
+            if (spb >= 0) {
+                const int kvh = hg * nh + warp;
+                const uint32_t kpk = sbase + s * L.stage_bytes + warp * BS * T::ROW;   // packed K rows
+                const uint32_t vpk = kpk + L.tile_bytes;                                 // packed V rows
+                const uint32_t vst = sbase + L.f16_off + warp * BS * 2 * D;              // f16 V staging
+                const bool partial = valid < BS;
+                // ---- V: packed rows -> f16 (1024 + 2^x v) staging tile, rows of
+                // 256 B, 16-byte chunks XOR-swizzled by (token & 7) inside each half
+#pragma unroll
+                for (int k = 0; k < BS * 4 / 32; ++k) {
+                    const int u = lane + 32 * k;
+                    const int t = u % BS, g = u / BS;
+                    const uint32_t a = vpk + t * T::ROW + 12 * g;
+                    const uint32_t w0 = ld_shared_u32(a), w1 = ld_shared_u32(a + 4), w2 = ld_shared_u32(a + 8);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = 4 * g + c;
+                        const uint32_t dst = vst + t * 256 + (((chunk & 8) | ((chunk & 7) ^ (t & 7))) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                     "r"(u3_pair(4 * c, w0, w1, w2)), "r"(u3_pair(4 * c + 1, w0, w1, w2)),
+                                     "r"(u3_pair(4 * c + 2, w0, w1, w2)), "r"(u3_pair(4 * c + 3, w0, w1, w2))
+                                     : "memory");
+                    }
+                }
+                // ---- metadata of this lane's score rows (tokens gid, gid+8 of each tile)
+                float sk[T::KT][2], zk[T::KT][2], sv[T::KT][2], zv[T::KT][2];
+#pragma unroll
+                for (int mt = 0; mt < T::KT; ++mt)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int tok = 16 * mt + gid + 8 * r;
+                        const int64_t mo = int64_t(spb) * p.m_blk + tok * p.m_slot + kvh * p.m_head;
+                        const int64_t zo = int64_t(spb) * p.z_blk + tok * p.z_slot + kvh * p.z_head;
+                        sk[mt][r] = __half2float(__ushort_as_half(__ldg(p.k_qs + mo)));
+                        sv[mt][r] = __half2float(__ushort_as_half(__ldg(p.v_qs + mo)));
+                        zk[mt][r] = float(__ldg(p.k_qz + zo));
+                        zv[mt][r] = float(__ldg(p.v_qz + zo));
+                    }
+                // ---- S^T = K Q'^T with K converted straight into A fragments:
+                // lane (gid, tig) takes group tig of token rows gid and gid+8
+                float sc[T::KT][4];
+#pragma unroll
+                for (int mt = 0; mt < T::KT; ++mt) {
+                    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
+                    const uint32_t a0 = kpk + (16 * mt + gid) * T::ROW + 12 * tig;
+                    const uint32_t a1 = a0 + 8 * T::ROW;
+                    const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
+                    const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
+#pragma unroll
+                    for (int kk = 0; kk < T::QK; ++kk) {
+                        uint32_t a[4];
+                        a[0] = u3_pair(2 * kk, x0, x1, x2);
+                        a[1] = u3_pair(2 * kk, y0, y1, y2);
+                        a[2] = u3_pair(2 * kk + 1, x0, x1, x2);
+                        a[3] = u3_pair(2 * kk + 1, y0, y1, y2);
+                        ptx::mma16816<false>(sc[mt], a, qb[kk][0], qb[kk][1]);
+                    }
+                }
+                // ---- scores: remove the 1024 offset and the zero point, apply
+                // the per-token scale, mask; online softmax per head column
+                float mx[2] = {NEG_INF, NEG_INF};
+#pragma unroll
+                for (int t = 0; t < T::KT; ++t)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = e >> 1, c = e & 1;
+                        float v = mult * sk[t][r] * (sc[t][e] - c0h[c] - zk[t][r] * q1h[c]);
+                        if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
+                        sc[t][e] = v;
+                        mx[c] = fmaxf(mx[c], v);
+                    }
+                float alpha[2];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+                    const float mn = fmaxf(m[c], mx[c]);
+                    alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
+                    m[c] = mn;
+                    l[c] *= alpha[c];
+                    b1[c] *= alpha[c];
+                    zs[c] *= alpha[c];
+                }
+                // P' = p * v_scale (0 for masked tokens) as the B operand of PV
+                uint32_t pbf[T::KT][2];
+#pragma unroll
+                for (int t = 0; t < T::KT; ++t)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
+                        const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
+                        const float p1 = exp2_approx(sc[t][2 * r + 1] - m[1]);
+                        l[0] += p0;
+                        l[1] += p1;
+                        float q0, q1;
+                        const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
+                        b1[0] += q0;
+                        b1[1] += q1;
+                        zs[0] += q0 * zv[t][r];
+                        zs[1] += q1 * zv[t][r];
+                        pbf[t][r] = ptx::movmatrix_trans(w);
+                    }
+                if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+                    for (int t = 0; t < T::DT / 2; ++t) {
+                        o[t][0] *= alpha[0];
+                        o[t][1] *= alpha[1];
+                        o[t][2] *= alpha[0];
+                        o[t][3] *= alpha[1];
+                    }
+                }
+                __syncwarp();          // staging tile complete
+                // ---- O^T += V'^T P'^T from the staging tile
+                const int mi = lane >> 3;
+#pragma unroll
+                for (int kt = 0; kt < T::KT; ++kt) {
+#pragma unroll
+                    for (int md = 0; md < T::DT / 2; ++md) {
+                        const int tok = 16 * kt + 8 * (mi >> 1) + (lane & 7);
+                        const int chunk = 2 * md + (mi & 1);
+                        uint32_t a[4];
+                        ptx::ldmatrix_x4_trans(vst + tok * 256 + (((chunk & 8) | ((chunk & 7) ^ (tok & 7))) << 4),
+                                               a[0], a[1], a[2], a[3]);
+                        ptx::mma16816<false>(o[md], a, pbf[kt][0], pbf[kt][1]);
+                    }
+                }
+            }
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
         // advance the walk; close the segment at a unit boundary
@@ -649,22 +930,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 4-D map over one cache: (row element, slot, kv head, block) with the
-// caller's strides; box = one 128-byte sub-row x block_size slots x nh heads.
+// caller's strides; box = one 128-byte swizzled sub-row (16-bit / fp8) or one
+// whole packed row (3-bit, no swizzle) x block_size slots x nh heads.
 bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, int P, int64_t c_slot,
               int64_t c_head, int64_t c_blk, int nh)
 {
     auto enc = encode_fn();
     if (!enc) return false;
-    const int es = ck == kE4M3 ? 1 : 2;
-    const CUtensorMapDataType dt = ck == kE4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                   : ck == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(BS), cuuint64_t(Hkv), cuuint64_t(P)};
+    const bool u3 = ck == kU3;
+    const int es = (ck == kE4M3 || u3) ? 1 : 2;
+    const CUtensorMapDataType dt = (ck == kE4M3 || u3) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : ck == kBF16        ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int row_elems = u3 ? 3 * D / 8 : D;
+    cuuint64_t dims[4] = {cuuint64_t(row_elems), cuuint64_t(BS), cuuint64_t(Hkv), cuuint64_t(P)};
     cuuint64_t strides[3] = {cuuint64_t(c_slot), cuuint64_t(c_head), cuuint64_t(c_blk)};
-    cuuint32_t box[4] = {cuuint32_t(128 / es), cuuint32_t(BS), cuuint32_t(nh), 1};
+    cuuint32_t box[4] = {cuuint32_t(u3 ? row_elems : 128 / es), cuuint32_t(BS), cuuint32_t(nh), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           u3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -695,7 +980,9 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
     switch (p.block_size) {
     case 16: return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
     case 32: return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
-    case 64: return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
+    case 64:
+        if constexpr (CK != kU3) return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
+        return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }
 }
@@ -707,6 +994,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
     if (group > 8 || batch > 4096) return false;
     if (cache_kind == kE4M3) return head_dim == 128;
+    if (cache_kind == kU3) return head_dim == 128 && block_size <= 32;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
 }
 
@@ -714,15 +1002,20 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
                int cache_kind, int sm_count, FastParams &f, size_t &workspace)
 {
+    const bool u3 = cache_kind == kU3;
     const int es = cache_kind == kE4M3 ? 1 : 2;
-    const int row = head_dim * es;
+    const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
+    const int f16_row = u3 ? 2 * head_dim : 0;         // per-warp V staging (3-bit)
     int nh = 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
     const int budget = 227 * 1024;
-    int stages = 4;
-    while (stages > 2 && smem_layout(nh, block_size, row, stages, batch).total > budget) --stages;
-    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch);
+    // ring depth: enough bytes in flight per SM, within the shared memory
+    int stages = 8;
+    while (stages > 2 && (stages * 2 * nh * block_size * row > 192 * 1024 ||
+                          smem_layout(nh, block_size, row, stages, batch, f16_row).total > budget))
+        --stages;
+    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, f16_row);
     if (L.total > budget) return false;
     const int n_hg = num_kv_heads / nh;
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
@@ -766,6 +1059,7 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
                   p.c_head, p.c_blk, f.nh))
         return cudaErrorInvalidValue;
     if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
+    if (cache_kind == kU3) return launch_fast_bs<kU3, 128>(p, f, mk, mv, s);
     if (cache_kind == kBF16)
         return p.head_dim == 128 ? launch_fast_bs<kBF16, 128>(p, f, mk, mv, s) : launch_fast_bs<kBF16, 64>(p, f, mk, mv, s);
     return p.head_dim == 128 ? launch_fast_bs<kF16, 128>(p, f, mk, mv, s) : launch_fast_bs<kF16, 64>(p, f, mk, mv, s);

@@ -355,8 +355,8 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
     const int sm = pkv::sm_count_current_device();
     dc.plan = pkv::DecodePlan{};
     if (num_splits == 0 && pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
-        // the fp8 path reads q rows 8 bytes at a time, the 16-bit path 4
-        const size_t qa = ci.kind == PKV_DTYPE_E4M3 ? 8 : 4;
+        // q rows are read 16 (3-bit), 8 (fp8) or 4 (16-bit) bytes at a time
+        const size_t qa = ci.kind == PKV_DTYPE_U3 ? 16 : (ci.kind == PKV_DTYPE_E4M3 ? 8 : 4);
         const bool q_ok = aligned(q->data, qa) && (p.q_b % qa) == 0 && (p.q_h % qa) == 0;
         pkv::FastParams f{};
         size_t ws = 0;

@@ -83,6 +83,45 @@ def test_u3_small(pkv, orc, splits):
     _check(w, out, PL.oracle_decode(w, orc, oc))
 
 
+@pytest.mark.parametrize("BS,H,Hkv", [(32, 8, 8), (16, 16, 4), (32, 12, 4)])
+def test_u3_block_and_group_variants(pkv, orc, BS, H, Hkv):
+    """3-bit cache with block 32, and grouped q heads over a 3-bit cache."""
+    w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=7 * BS + 3, num_heads=H, block_size=BS, seed=80 + BS + H)
+    if Hkv != H:   # regroup: keep Hkv kv heads, H q heads
+        w.num_kv_heads = Hkv
+        g = torch.Generator().manual_seed(81)
+        w.k_fill = w.k_fill[:, :Hkv].contiguous()
+        w.v_fill = w.v_fill[:, :Hkv].contiguous()
+        w.k_new = w.k_new[:, :Hkv].contiguous()
+        w.v_new = w.v_new[:, :Hkv].contiguous()
+    for splits in (0, 3):
+        cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+        oc = PL.oracle_caches(w, orc)
+        _check(w, out, PL.oracle_decode(w, orc, oc))
+
+
+def test_u3_poisoned_tail_metadata(pkv, orc):
+    """NaN scales and garbage codes in slots beyond the contexts of a 3-bit
+    cache leave the output finite and unchanged."""
+    w = W.u3_mha(batch=4, ctx_lo=3, ctx_hi=300, num_heads=8, seed=88)
+    live = torch.zeros((w.num_blocks, w.block_size), dtype=torch.bool)
+    for b in range(w.batch):
+        for t in range(int(w.context_lens[b])):
+            live[int(w.block_tables[b, t // w.block_size]), t % w.block_size] = True
+    dead = (~live).cuda()
+
+    def poison(cache):
+        for t in (cache.k_qscale, cache.v_qscale):
+            t[dead] = float("nan")
+        for t in (cache.k_cache, cache.v_cache):
+            t[dead] = 0xA5
+    for splits in (0, 2):
+        _, clean = PL.gpu_run(w, pkv, num_splits=splits)
+        _, dirty = PL.gpu_run(w, pkv, num_splits=splits, poison=poison)
+        assert torch.isfinite(dirty.float()).all()
+        assert torch.equal(clean, dirty)
+
+
 def test_u3_head_dim_64(pkv, orc):
     w = W.u3_mha(batch=3, ctx_lo=5, ctx_hi=300, num_heads=4, head_dim=64, seed=34)
     cache, out = PL.gpu_run(w, pkv)
