@@ -50,17 +50,19 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 #define NEG_INF (-__int_as_float(0x7f800000))
 
 struct SmemLayout {
-    int tile_bytes, stage_bytes, f16_off, bars_off, ok_off, prefix_off, nblk_off, total;
+    int tile_bytes, meta_bytes, stage_bytes, f16_off, bars_off, ok_off, prefix_off, nblk_off, total;
 };
 
-// [stages x (K tile, V tile)] [f16 staging: nh x bs x head_dim halves, 3-bit
-// caches only] [mbarriers] [per-stage block ids] [prefix sums] [block counts]
+// [stages x (K tile, V tile, 3-bit metadata of the whole block)] [f16
+// staging: nh x bs x head_dim halves, 3-bit caches only] [mbarriers]
+// [per-stage block ids] [prefix sums] [block counts]
 __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
-                                                  int batch, int f16_row_bytes = 0)
+                                                  int batch, int f16_row_bytes = 0, int meta_bytes = 0)
 {
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
-    L.stage_bytes = 2 * L.tile_bytes;
+    L.meta_bytes = meta_bytes;
+    L.stage_bytes = 2 * L.tile_bytes + meta_bytes;
     L.f16_off = stages * L.stage_bytes;
     L.bars_off = L.f16_off + nh * bs * f16_row_bytes;
     L.ok_off = L.bars_off + 2 * stages * 8;
@@ -203,7 +205,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nh = f.nh, B = p.batch, G = p.group, stages = f.stages;
-    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, T::kIsU3 ? 2 * D : 0);
+    // 3-bit metadata per stage: K scales, V scales (fp16), K zeros, V zeros
+    // (u8) of all num_kv_heads for the block's BS slots
+    const int meta_bytes = T::kIsU3 ? 6 * BS * p.num_kv_heads : 0;
+    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, T::kIsU3 ? 2 * D : 0, meta_bytes);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
     volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
@@ -304,6 +309,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                                 const int half_bytes = L.tile_bytes / T::HALVES;
                                 ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
                                 ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                            }
+                            if constexpr (T::kIsU3) {
+                                const int HB = BS * p.num_kv_heads;       // entries per block
+                                const uint32_t md = vdst + L.tile_bytes;
+                                ptx::bulk_load(md, p.k_qs + int64_t(pbk) * p.m_blk, 2 * HB, fb);
+                                ptx::bulk_load(md + 2 * HB, p.v_qs + int64_t(pbk) * p.m_blk, 2 * HB, fb);
+                                ptx::bulk_load(md + 4 * HB, p.k_qz + int64_t(pbk) * p.z_blk, HB, fb);
+                                ptx::bulk_load(md + 5 * HB, p.v_qz + int64_t(pbk) * p.z_blk, HB, fb);
                             }
                         } else {
                             ptx::mbar_arrive(fb);
@@ -730,25 +743,31 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                                      : "memory");
                     }
                 }
-                // ---- metadata of this lane's score rows (tokens gid, gid+8 of each tile)
+                // ---- metadata of this lane's score rows (tokens gid, gid+8 of
+                // each tile), staged with the block: [BS][num_kv_heads] arrays
+                const int HKV = p.num_kv_heads;
+                const unsigned char *meta = smem + (s * L.stage_bytes + 2 * L.tile_bytes);
+                const __half *mks = reinterpret_cast<const __half *>(meta);
+                const __half *mvs = mks + BS * HKV;
+                const uint8_t *mkz = meta + 4 * BS * HKV;
+                const uint8_t *mvz = mkz + BS * HKV;
                 float sk[T::KT][2], zk[T::KT][2], sv[T::KT][2], zv[T::KT][2];
 #pragma unroll
                 for (int mt = 0; mt < T::KT; ++mt)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int tok = 16 * mt + gid + 8 * r;
-                        const int64_t mo = int64_t(spb) * p.m_blk + tok * p.m_slot + kvh * p.m_head;
-                        const int64_t zo = int64_t(spb) * p.z_blk + tok * p.z_slot + kvh * p.z_head;
-                        sk[mt][r] = __half2float(__ushort_as_half(__ldg(p.k_qs + mo)));
-                        sv[mt][r] = __half2float(__ushort_as_half(__ldg(p.v_qs + mo)));
-                        zk[mt][r] = float(__ldg(p.k_qz + zo));
-                        zv[mt][r] = float(__ldg(p.v_qz + zo));
+                        const int e = (16 * mt + gid + 8 * r) * HKV + kvh;
+                        sk[mt][r] = __half2float(mks[e]);
+                        sv[mt][r] = __half2float(mvs[e]);
+                        zk[mt][r] = float(mkz[e]);
+                        zv[mt][r] = float(mvz[e]);
                     }
                 // ---- S^T = K Q'^T with K converted straight into A fragments:
                 // lane (gid, tig) takes group tig of token rows gid and gid+8
                 float sc[T::KT][4];
 #pragma unroll
                 for (int mt = 0; mt < T::KT; ++mt) {
+                    float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
                     sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
                     const uint32_t a0 = kpk + (16 * mt + gid) * T::ROW + 12 * tig;
                     const uint32_t a1 = a0 + 8 * T::ROW;
@@ -761,8 +780,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         a[1] = u3_pair(2 * kk, y0, y1, y2);
                         a[2] = u3_pair(2 * kk + 1, x0, x1, x2);
                         a[3] = u3_pair(2 * kk + 1, y0, y1, y2);
-                        ptx::mma16816<false>(sc[mt], a, qb[kk][0], qb[kk][1]);
+                        ptx::mma16816<false>((kk & 1) ? sx : sc[mt], a, qb[kk][0], qb[kk][1]);
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[mt][e] += sx[e];
                 }
                 // ---- scores: remove the 1024 offset and the zero point, apply
                 // the per-token scale, mask; online softmax per head column
@@ -1012,10 +1033,11 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const int budget = 227 * 1024;
     // ring depth: enough bytes in flight per SM, within the shared memory
     int stages = 8;
-    while (stages > 2 && (stages * 2 * nh * block_size * row > 192 * 1024 ||
-                          smem_layout(nh, block_size, row, stages, batch, f16_row).total > budget))
+    const int meta = u3 ? 6 * block_size * num_kv_heads : 0;
+    while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 ||
+                          smem_layout(nh, block_size, row, stages, batch, f16_row, meta).total > budget))
         --stages;
-    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, f16_row);
+    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, f16_row, u3 ? 6 * block_size * num_kv_heads : 0);
     if (L.total > budget) return false;
     const int n_hg = num_kv_heads / nh;
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
