@@ -72,6 +72,19 @@ def dist_env():
     return ws, rank, local
 
 
+def job_throughput(pg, bytes_local, ms_local, device):
+    """Whole-job throughput over all ranks: the bytes every rank processed
+    divided by the slowest rank's time (max over ranks).  Returns
+    (ms_max, GB/s).  ``pg`` is torch.distributed (any backend) or None."""
+    ms_t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    b_t = torch.tensor([float(bytes_local)], dtype=torch.float64, device=device)
+    if pg is not None:
+        pg.all_reduce(ms_t, op=pg.ReduceOp.MAX)
+        pg.all_reduce(b_t, op=pg.ReduceOp.SUM)
+    ms_max = float(ms_t.item())
+    return ms_max, float(b_t.item()) / (ms_max * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -182,15 +195,18 @@ def algorithmic_bytes(w, decode=True, append=True):
     return total
 
 
-def make_workload(name, device):
+def make_workload(name, device, rank=0):
+    """The named workload; rank r > 0 (a replica under torchrun) draws an
+    independent instance of the same recipe (seed + 1000 r)."""
+    seed = W.SEEDS[name] + 1000 * rank
     if name == "gqa_bf16":
-        return W.gqa_bf16(device=device)
+        return W.gqa_bf16(device=device, seed=seed)
     if name == "fp8_long":
-        return W.fp8_long(device=device)
+        return W.fp8_long(device=device, seed=seed)
     if name == "u3_mha":
-        return W.u3_mha(device=device)
+        return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
-        return W.mixed_append(device=device)
+        return W.mixed_append(device=device, seed=seed)
     if name == "tiny_fp16":
         return W.tiny(device=device)
     raise ValueError(name)
@@ -445,7 +461,7 @@ def main():
     flush = L2Flush(dev)
 
     # ---------------- main workload, device-timed
-    w = make_workload(args.workload, dev)
+    w = make_workload(args.workload, dev, rank)
     step_bytes = algorithmic_bytes(w)
     dec_bytes = algorithmic_bytes(w, append=False)
     app_bytes = algorithmic_bytes(w, decode=False)
@@ -467,12 +483,7 @@ def main():
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    ms = float(np.mean(tot))
-    ms_t = torch.tensor([ms], device=dev)
-    if pg:
-        pg.all_reduce(ms_t, op=pg.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = ws * step_bytes / (ms_max * 1e-3) / 1e9
+    ms_max, value = job_throughput(pg, step_bytes, float(np.mean(tot)), dev)
     dec_ms = float(np.mean(dec))
     app_ms = float(np.mean(app))
     assert int(st.err.item()) == 0, "device error flag %d" % int(st.err.item())
@@ -502,12 +513,7 @@ def main():
         s.synchronize()
         if i >= 3:
             e2e_t.append(time.perf_counter() - t0)
-    e2e_ms = 1e3 * float(np.mean(e2e_t))
-    e2e_val = step_bytes / (e2e_ms * 1e-3) / 1e9
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_val = ws * step_bytes / (float(t.item()) * 1e-3) / 1e9
+    e2e_ms, e2e_val = job_throughput(pg, step_bytes, 1e3 * float(np.mean(e2e_t)), dev)
 
     # ---------------- roofline of the dominant operation (paged_decode)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
@@ -540,7 +546,7 @@ def main():
     del st
     torch.cuda.empty_cache()
     for name in [x for x in args.extra.split(",") if x]:
-        wx = make_workload(name, dev)
+        wx = make_workload(name, dev, rank)
         sb = algorithmic_bytes(wx)
         db = algorithmic_bytes(wx, append=False)
         ab = algorithmic_bytes(wx, decode=False)

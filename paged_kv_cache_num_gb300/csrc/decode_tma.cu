@@ -252,6 +252,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (blockIdx.x == 0)
         for (int b = threadIdx.x; b <= B; b += blockDim.x) f.prefix[b] = prefix[b];
 
+    // the merge kernel may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t NBT = prefix[B];                  // blocks per head group
     const int64_t N = NBT * f.n_hg;
     const int64_t lo = int64_t(blockIdx.x) * N / gridDim.x;
@@ -878,12 +880,25 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 }
 
+// floor(a / n) for 0 <= a < 2^62, 0 < n < 2^31: a float estimate corrected
+// by exact integer comparisons (cheaper than a 64-bit division).
+__device__ __forceinline__ int64_t floordiv_i64(int64_t a, int64_t n)
+{
+    int64_t q = int64_t(__fdividef(float(a), float(n)));
+    while (q > 0 && q * n > a) --q;
+    while ((q + 1) * n <= a) ++q;
+    return q;
+}
+
 // Merge the partials of units split across CTAs (one warp per (sequence,
 // q head)); units held whole by one CTA were written by it, units with an
 // empty context get zeros.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f)
 {
+    // launched as a programmatic dependent of the decode kernel: wait until
+    // that grid has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= p.batch * p.num_heads) return;
@@ -902,12 +917,17 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f
     if (n > 0) {
         const int64_t S = f.grid;
         const int64_t first = int64_t(hg) * NBT + f.prefix[b];
-        const int64_t i0 = ((first + 1) * S - 1) / N;
-        const int64_t i1 = ((first + n) * S - 1) / N;
+        // CTA i streams [i*N/S, (i+1)*N/S): the owner of flat index x is
+        // floor(((x+1)*S - 1) / N)
+        const int64_t i0 = floordiv_i64((first + 1) * S - 1, N);
+        const int64_t i1 = floordiv_i64((first + n) * S - 1, N);
         if (i0 == i1) return;                         // written whole by CTA i0
         const int64_t unit = int64_t(hg) * p.batch + b;
-        // CTAs with an empty range (more CTAs than blocks) wrote nothing
-        auto empty_range = [&](int64_t i) { return (i * N) / S == ((i + 1) * N) / S; };
+        // with fewer blocks than CTAs some CTAs have an empty range and wrote
+        // nothing (never the case when N >= S)
+        auto empty_range = [&](int64_t i) {
+            return N < S && (i * N) / S == ((i + 1) * N) / S;
+        };
         float M = NEG_INF;
         for (int64_t i = i0; i <= i1; ++i)
             if (!empty_range(i)) M = fmaxf(M, f.part_ml[2 * ((i + unit) * nh * G + local)]);
@@ -990,8 +1010,17 @@ cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUte
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int rows = p.batch * p.num_heads;
-    merge_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(p, f);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<D>, p, f);
 }
 
 template <int CK, int D>
