@@ -599,9 +599,11 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         ptx::ldmatrix_x4(ktile + (chunk >> 3) * half_bytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4),
                                          a[0], a[1], a[2], a[3]);
                     } else {
-                        const int t0 = 16 * mt + gid, t1 = t0 + 8;
-                        const uint32_t w0 = ld_shared_u32(ktile + t0 * 128 + (((kk & 7) ^ (t0 & 7)) << 4) + 4 * tig);
-                        const uint32_t w1 = ld_shared_u32(ktile + t1 * 128 + (((kk & 7) ^ (t1 & 7)) << 4) + 4 * tig);
+                        // rows 16mt+gid and +8 share the swizzle phase gid: the
+                        // address is (row base | gid << 4) ^ (kk << 4)
+                        const uint32_t kb = (ktile + (16 * mt + gid) * 128 + 4 * tig) | (uint32_t(gid) << 4);
+                        const uint32_t w0 = ld_shared_u32(kb ^ uint32_t((kk & 7) << 4));
+                        const uint32_t w1 = ld_shared_u32((kb + 8 * 128) ^ uint32_t((kk & 7) << 4));
                         a[0] = f16x2_from_e4m3x2(w0);
                         a[1] = f16x2_from_e4m3x2(w1);
                         a[2] = f16x2_from_e4m3x2(w0 >> 16);
@@ -691,18 +693,22 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 } else {
                     const int t0 = 16 * kt + 2 * tig;
                     const int rows[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
+                    // row i's address for chunk 2q4 + (gid >> 2) is
+                    // (row base | ((gid >> 2) ^ (row & 7)) << 4) ^ (q4 << 5)
+                    uint32_t vb[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        vb[i] = (vtile + rows[i] * 128 + (gid & 3) * 4) | (uint32_t((gid >> 2) ^ (rows[i] & 7)) << 4);
 #pragma unroll
                     for (int q4 = 0; q4 < D / 32; ++q4) {
                         // bytes d = 32q4 + 4gid .. +3 of the four token rows;
                         // tile 2q4 takes bytes 0 (rows gid) and 1 (rows gid+8),
                         // tile 2q4+1 bytes 2 and 3
-                        const int chunk = 2 * q4 + (gid >> 2);
                         uint32_t w[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int tok = rows[i];
-                            w[i] = ld_shared_u32(vtile + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4) + (gid & 3) * 4);
-                            if (partial && tok >= valid) w[i] = 0u;
+                            w[i] = ld_shared_u32(vb[i] ^ uint32_t((q4 & 3) << 5));
+                            if (partial && rows[i] >= valid) w[i] = 0u;
                         }
 #pragma unroll
                         for (int hb = 0; hb < 2; ++hb) {

@@ -42,17 +42,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// try_wait suspends the thread until the phase completes or the hint (ns)
+// runs out, so a waiting warp does not spin on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n"
         ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         "selp.u32 %0, 1, 0, p;\n"
         "}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(100000u)
         : "memory");
     return ok != 0;
 }
@@ -65,7 +67,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     const uint64_t t0 = globaltimer();
     uint32_t n = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if ((++n & 255u) == 0 && globaltimer() - t0 > timeout_ns) return false;
+        if ((++n & 15u) == 0 && globaltimer() - t0 > timeout_ns) return false;
     }
     return true;
 }
