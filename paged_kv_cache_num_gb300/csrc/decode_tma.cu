@@ -50,21 +50,19 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 #define NEG_INF (-__int_as_float(0x7f800000))
 
 struct SmemLayout {
-    int tile_bytes, meta_bytes, stage_bytes, f16_off, bars_off, ok_off, prefix_off, nblk_off, total;
+    int tile_bytes, meta_bytes, stage_bytes, bars_off, ok_off, prefix_off, nblk_off, total;
 };
 
-// [stages x (K tile, V tile, 3-bit metadata of the whole block)] [f16
-// staging: nh x bs x head_dim halves, 3-bit caches only] [mbarriers]
-// [per-stage block ids] [prefix sums] [block counts]
+// [stages x (K tile, V tile, 3-bit metadata of the whole block)]
+// [mbarriers] [per-stage block ids] [prefix sums] [block counts]
 __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
-                                                  int batch, int f16_row_bytes = 0, int meta_bytes = 0)
+                                                  int batch, int meta_bytes = 0)
 {
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
     L.meta_bytes = meta_bytes;
     L.stage_bytes = 2 * L.tile_bytes + meta_bytes;
-    L.f16_off = stages * L.stage_bytes;
-    L.bars_off = L.f16_off + nh * bs * f16_row_bytes;
+    L.bars_off = stages * L.stage_bytes;
     L.ok_off = L.bars_off + 2 * stages * 8;
     L.prefix_off = L.ok_off + stages * 4;
     L.nblk_off = L.prefix_off + (batch + 1) * 4;
@@ -116,66 +114,68 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
 }
 
 // ---------------------------------------------------------------- 3-bit
-// Lanes of a 96-bit group (lane i = bits 3i..3i+2) are converted two at a
-// time: pair p = (i, j) sits in one 32-bit window of the group at bits x and
-// 16 + y, so (window & mask) | 0x64006400 is the f16 pair
-// (1024 + 2^x v_i, 1024 + 2^y v_j) -- exact, one shift and one LOP3.  Every
-// x, y is >= 5, which keeps the 1024 offset within a factor ~9 of the value
-// term (the offset and the zero point are removed in fp32 afterwards).  The
-// 32 lanes are covered exactly once.
-struct U3Pair {
-    int i, j, x, y;
+// A 3-bit code v placed at bit x <= 7 of an otherwise zero 16-bit half is
+// the f16 subnormal v * 2^(x - 24): exact, and never a NaN or an infinity
+// whatever the bits around it.  Products with normal f16 operands are exact
+// in the fp32 accumulators, so the factor 2^(x - 24) is folded into q' on
+// the K side and into the output on the V side, and no offset has to be
+// removed after the MMA.  One LOP3 (mask) makes a pair; the windows the
+// masks apply to are the costly part and are shared between pairs.
+//
+// K side: the A fragments of S^T = K Q'^T pair two codes of one token row.
+// A 96-bit group (32 codes, lane i at bits 3i..3i+2) is cut into seven
+// 32-bit windows -- its three words and four shifts -- and each window
+// gives up to three pairs, lane i at bit x and lane j at bit 16 + y.
+struct U3KPair {
+    int s, i, j, x, y;   // window = bits s .. s+31 of the group
 };
-__host__ __device__ constexpr U3Pair u3_pair_info(int p)
+__host__ __device__ constexpr U3KPair u3k_pair_info(int p)
 {
     switch (p) {
-    case 0: return {0, 5, 6, 5};
-    case 1: return {1, 6, 6, 5};
-    case 2: return {2, 7, 6, 5};
-    case 3: return {3, 8, 6, 5};
-    case 4: return {4, 9, 6, 5};
-    case 5: return {10, 15, 6, 5};
-    case 6: return {11, 16, 6, 5};
-    case 7: return {12, 17, 6, 5};
-    case 8: return {13, 18, 6, 5};
-    case 9: return {14, 19, 6, 5};
-    case 10: return {20, 25, 6, 5};
-    case 11: return {21, 27, 5, 7};
-    case 12: return {22, 28, 5, 7};
-    case 13: return {23, 29, 5, 7};
-    case 14: return {24, 30, 5, 7};
-    default: return {26, 31, 6, 5};
+    case 0: return {0, 0, 7, 0, 5};
+    case 1: return {0, 1, 6, 3, 2};
+    case 2: return {4, 2, 9, 2, 7};
+    case 3: return {4, 3, 8, 5, 4};
+    case 4: return {10, 4, 11, 2, 7};
+    case 5: return {10, 5, 10, 5, 4};
+    case 6: return {32, 12, 17, 4, 3};
+    case 7: return {32, 13, 18, 7, 6};
+    case 8: return {41, 14, 21, 1, 6};
+    case 9: return {41, 15, 20, 4, 3};
+    case 10: return {41, 16, 19, 7, 0};
+    case 11: return {64, 22, 27, 2, 1};
+    case 12: return {64, 23, 28, 5, 4};
+    case 13: return {71, 24, 31, 1, 6};
+    case 14: return {71, 25, 30, 4, 3};
+    default: return {71, 26, 29, 7, 0};
     }
 }
-// stored index s (mod 32) of a converted group -> lane and its 2^x factor:
-// s = 2p + e holds lane (e ? j : i) of pair p
-__constant__ uint8_t c_u3_lane[32] = {0,  5,  1,  6,  2,  7,  3,  8,  4,  9,  10, 15, 11, 16, 12, 17,
-                                      13, 18, 14, 19, 20, 25, 21, 27, 22, 28, 23, 29, 24, 30, 26, 31};
-__constant__ uint8_t c_u3_x[32] = {6, 5, 6, 5, 6, 5, 6, 5, 6, 5, 6, 5, 6, 5, 6, 5,
-                                   6, 5, 6, 5, 6, 5, 5, 7, 5, 7, 5, 7, 5, 7, 6, 5};
 
 // Pair p of the group held in words (w0, w1, w2); p is a constant after
-// unrolling, so the shift / funnel choice folds away.
-__device__ __forceinline__ uint32_t u3_pair(int p, uint32_t w0, uint32_t w1, uint32_t w2)
+// unrolling, so the window choice folds away (and equal windows are shared).
+__device__ __forceinline__ uint32_t u3k_pair(int p, uint32_t w0, uint32_t w1, uint32_t w2)
 {
-    const U3Pair pr = u3_pair_info(p);
-    const int sh = 3 * pr.i - pr.x;
+    const U3KPair pr = u3k_pair_info(p);
     uint32_t win;
-    if (sh < 0) {
-        win = w0 << (-sh);
-    } else {
-        const int w = sh >> 5, off = sh & 31;
-        const uint32_t lo = w == 0 ? w0 : (w == 1 ? w1 : w2);
-        if (off + 16 + pr.y + 3 <= 32) {
-            win = lo >> off;
-        } else {
-            const uint32_t hi = w == 0 ? w1 : w2;
-            win = __funnelshift_r(lo, hi, off);
-        }
-    }
-    const uint32_t mask = (7u << pr.x) | (7u << (16 + pr.y));
-    return (win & mask) | 0x64006400u;
+    if (pr.s == 0) win = w0;
+    else if (pr.s < 32) win = __funnelshift_r(w0, w1, pr.s);
+    else if (pr.s == 32) win = w1;
+    else if (pr.s < 64) win = __funnelshift_r(w1, w2, pr.s - 32);
+    else if (pr.s == 64) win = w2;
+    else win = w2 >> (pr.s - 64);
+    return win & ((7u << pr.x) | (7u << (16 + pr.y)));
 }
+
+// V side: the A fragments of O^T = V'^T P'^T pair one code of two tokens.
+// A lane owns the 16 codes of bytes 6g .. 6g+5 of a row (g = its group id);
+// code c of that slice lies in the 16-bit piece that starts at slice byte
+// u3v_win(c), at bit u3v_x(c) of it.  A byte permute puts the piece of
+// token A in the low half and that of token B in the high half.
+__host__ __device__ constexpr int u3v_win(int c)
+{
+    return c < 3 ? 0 : c < 6 ? 1 : c < 8 ? 2 : c < 11 ? 3 : c < 14 ? 4 : 5;
+}
+__host__ __device__ constexpr int u3v_x(int c) { return 3 * c - 8 * u3v_win(c); }
 
 // CK: cache kind (kF16 / kBF16 / kE4M3 / kU3); D head_dim; BS block size.
 // MMA operand type: bf16 for bf16 caches, f16 otherwise (fp8 codes convert
@@ -208,7 +208,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // 3-bit metadata per stage: K scales, V scales (fp16), K zeros, V zeros
     // (u8) of all num_kv_heads for the block's BS slots
     const int meta_bytes = T::kIsU3 ? 6 * BS * p.num_kv_heads : 0;
-    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, T::kIsU3 ? 2 * D : 0, meta_bytes);
+    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
     volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
@@ -362,9 +362,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
     float mult = 1.0f, vmul = 1.0f;
     int ctx_b = 0;
-    // 3-bit only: per head column, 1024 * sum(q') and sum(q' 2^x) of the QK
-    // operand, and the running sum of P' and of P' * zero of the PV operand
-    float c0h[2] = {0.0f, 0.0f}, q1h[2] = {0.0f, 0.0f}, b1[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
+    // 3-bit only: per head column, sum(q' 2^(x-24)) of the QK operand and
+    // the running sum of P' * zero of the PV operand
+    float q1h[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
 
     auto start_segment = [&]() {
         const int kvh = hg * nh + warp;
@@ -375,9 +375,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const bool hv = gid < G;  // this lane's B column (q head gid) exists
         const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
         if constexpr (T::kIsU3) {
-            // q' = q * 2^-x (f16) in the pair order of the converted K rows:
-            // k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1) and pair
-            // 2kk+1 (k = 2tig+8, 2tig+9) of 96-bit group tig.
+            // q' = q qs 2^(1-x) (f16, exact) in the pair order of the K
+            // fragments: k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1)
+            // and pair 2kk+1 (k = 2tig+8, 2tig+9) of 96-bit group tig, so that
+            // q' k' = qs 2^-23 q v for every code.
             float qv[32];
             float amax = 0.0f;
 #pragma unroll
@@ -405,29 +406,24 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
             float qs = 1.0f;
             while (amax * qs > 16384.0f) qs *= 0.5f;
-            float c0 = 0.0f, q1 = 0.0f;
+            float q1 = 0.0f;
 #pragma unroll
             for (int pp = 0; pp < 16; ++pp) {
-                const U3Pair pr = u3_pair_info(pp);
+                const U3KPair pr = u3k_pair_info(pp);
                 float ra, rb;
-                const uint32_t w = pack_f16(qv[pr.i] * qs * (1.0f / float(1 << pr.x)),
-                                            qv[pr.j] * qs * (1.0f / float(1 << pr.y)), ra, rb);
+                const uint32_t w = pack_f16(qv[pr.i] * qs * (2.0f / float(1 << pr.x)),
+                                            qv[pr.j] * qs * (2.0f / float(1 << pr.y)), ra, rb);
                 qb[pp >> 1][pp & 1] = w;
-                c0 += ra + rb;
-                q1 += ra * float(1 << pr.x) + rb * float(1 << pr.y);
+                q1 += ra * (float(1 << pr.x) * 0x1p-24f) + rb * (float(1 << pr.y) * 0x1p-24f);
             }
-            c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
-            c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
             q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
             q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {       // values of head columns 2tig, 2tig+1
-                c0h[c] = 1024.0f * __shfl_sync(0xffffffffu, c0, 4 * (2 * tig + c));
                 q1h[c] = __shfl_sync(0xffffffffu, q1, 4 * (2 * tig + c));
-                b1[c] = 0.0f;
                 zs[c] = 0.0f;
             }
-            mult = log2e_scale / qs;
+            mult = log2e_scale * 0x1p23f / qs;
             vmul = 1.0f;
         } else if constexpr (!T::kFp8) {
 #pragma unroll
@@ -485,8 +481,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // d held by this lane for accumulator tile t, row half r (0: gid, 1: gid+8)
     auto d_of = [&](int t, int r) -> int {
         if constexpr (T::kIsU3) {
-            const int sidx = 16 * t + 8 * r + gid;           // stored (converted) index
-            return (sidx & ~31) + c_u3_lane[sidx & 31];
+            return 16 * gid + 2 * t + r;                     // slice code 2t + r
         } else if constexpr (!T::kFp8) {
             return 16 * t + 8 * r + gid;
         } else {
@@ -507,25 +502,20 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             v += __shfl_xor_sync(0xffffffffu, v, 16);
             lt[c] = v;
         }
-        float bt[2] = {0.0f, 0.0f}, zt[2] = {0.0f, 0.0f};
+        float zt[2] = {0.0f, 0.0f};
         if constexpr (T::kIsU3) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float v = b1[c], z = zs[c];
+                float z = zs[c];
 #pragma unroll
-                for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                    v += __shfl_xor_sync(0xffffffffu, v, o2);
-                    z += __shfl_xor_sync(0xffffffffu, z, o2);
-                }
-                bt[c] = 1024.0f * v;
+                for (int o2 = 4; o2 < 32; o2 <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o2);
                 zt[c] = z;
             }
         }
         // accumulator entry (t, r, c) -> value of the segment's unnormalised output
         auto oval = [&](int t, int r, int c) -> float {
             if constexpr (T::kIsU3) {
-                const int sidx = 16 * t + 8 * r + gid;
-                return (o[t][2 * r + c] - bt[c]) * (1.0f / float(1 << c_u3_x[sidx & 31])) - zt[c];
+                return o[t][2 * r + c] * float(1 << (24 - u3v_x(2 * t + r))) - zt[c];
             } else {
                 return o[t][2 * r + c];
             }
@@ -731,26 +721,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int kvh = hg * nh + warp;
                 const uint32_t kpk = sbase + s * L.stage_bytes + warp * BS * T::ROW;   // packed K rows
                 const uint32_t vpk = kpk + L.tile_bytes;                                 // packed V rows
-                const uint32_t vst = sbase + L.f16_off + warp * BS * 2 * D;              // f16 V staging
                 const bool partial = valid < BS;
-                // ---- V: packed rows -> f16 (1024 + 2^x v) staging tile, rows of
-                // 256 B, 16-byte chunks XOR-swizzled by (token & 7) inside each half
-#pragma unroll
-                for (int k = 0; k < BS * 4 / 32; ++k) {
-                    const int u = lane + 32 * k;
-                    const int t = u % BS, g = u / BS;
-                    const uint32_t a = vpk + t * T::ROW + 12 * g;
-                    const uint32_t w0 = ld_shared_u32(a), w1 = ld_shared_u32(a + 4), w2 = ld_shared_u32(a + 8);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int chunk = 4 * g + c;
-                        const uint32_t dst = vst + t * 256 + (((chunk & 8) | ((chunk & 7) ^ (t & 7))) << 4);
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                                     "r"(u3_pair(4 * c, w0, w1, w2)), "r"(u3_pair(4 * c + 1, w0, w1, w2)),
-                                     "r"(u3_pair(4 * c + 2, w0, w1, w2)), "r"(u3_pair(4 * c + 3, w0, w1, w2))
-                                     : "memory");
-                    }
-                }
                 // ---- metadata of this lane's score rows (tokens gid, gid+8 of
                 // each tile), staged with the block: [BS][num_kv_heads] arrays
                 const int HKV = p.num_kv_heads;
@@ -784,24 +755,24 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < T::QK; ++kk) {
                         uint32_t a[4];
-                        a[0] = u3_pair(2 * kk, x0, x1, x2);
-                        a[1] = u3_pair(2 * kk, y0, y1, y2);
-                        a[2] = u3_pair(2 * kk + 1, x0, x1, x2);
-                        a[3] = u3_pair(2 * kk + 1, y0, y1, y2);
+                        a[0] = u3k_pair(2 * kk, x0, x1, x2);
+                        a[1] = u3k_pair(2 * kk, y0, y1, y2);
+                        a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
+                        a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
                         ptx::mma16816<false>((kk & 1) ? sx : sc[mt], a, qb[kk][0], qb[kk][1]);
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[mt][e] += sx[e];
                 }
-                // ---- scores: remove the 1024 offset and the zero point, apply
-                // the per-token scale, mask; online softmax per head column
+                // ---- scores: remove the zero point, apply the per-token
+                // scale, mask; online softmax per head column
                 float mx[2] = {NEG_INF, NEG_INF};
 #pragma unroll
                 for (int t = 0; t < T::KT; ++t)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = e >> 1, c = e & 1;
-                        float v = mult * sk[t][r] * (sc[t][e] - c0h[c] - zk[t][r] * q1h[c]);
+                        float v = mult * sk[t][r] * (sc[t][e] - zk[t][r] * q1h[c]);
                         if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
                         sc[t][e] = v;
                         mx[c] = fmaxf(mx[c], v);
@@ -816,7 +787,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
                     m[c] = mn;
                     l[c] *= alpha[c];
-                    b1[c] *= alpha[c];
                     zs[c] *= alpha[c];
                 }
                 // P' = p * v_scale (0 for masked tokens) as the B operand of PV
@@ -832,8 +802,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         l[1] += p1;
                         float q0, q1;
                         const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
-                        b1[0] += q0;
-                        b1[1] += q1;
                         zs[0] += q0 * zv[t][r];
                         zs[1] += q1 * zv[t][r];
                         pbf[t][r] = ptx::movmatrix_trans(w);
@@ -847,18 +815,42 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         o[t][3] *= alpha[1];
                     }
                 }
-                __syncwarp();          // staging tile complete
-                // ---- O^T += V'^T P'^T from the staging tile
-                const int mi = lane >> 3;
+                // ---- O^T += V'^T P'^T with V converted straight into A
+                // fragments: lane (gid, tig) owns codes 16gid .. 16gid+15 (row
+                // bytes 6gid .. 6gid+5) of tokens 2tig, 2tig+1 (k = 2tig, 2tig+1)
+                // and 2tig+8, 2tig+9; tile md holds codes 2md (row gid) and
+                // 2md+1 (row gid+8) of the slices.  X / Y are slice bytes 0-3 / 2-5.
+                const uint32_t vlane = vpk + ((6 * gid) & ~3);
+                const int sxy = 16 * (gid & 1);
 #pragma unroll
                 for (int kt = 0; kt < T::KT; ++kt) {
+                    uint32_t X[4], Y[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int tok = 16 * kt + 2 * tig + (i & 1) + 8 * (i >> 1);
+                        const uint32_t w0 = ld_shared_u32(vlane + tok * T::ROW);
+                        const uint32_t w1 = ld_shared_u32(vlane + tok * T::ROW + 4);
+                        X[i] = __funnelshift_r(w0, w1, sxy);
+                        Y[i] = __funnelshift_rc(w0, w1, sxy + 16);
+                    }
+                    uint32_t win[2][6];
+#pragma unroll
+                    for (int tp = 0; tp < 2; ++tp) {
+                        win[tp][0] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x5410u);
+                        win[tp][1] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x6521u);
+                        win[tp][2] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x7632u);
+                        win[tp][3] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x6521u);
+                        win[tp][4] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7632u);
+                        win[tp][5] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7733u);
+                    }
 #pragma unroll
                     for (int md = 0; md < T::DT / 2; ++md) {
-                        const int tok = 16 * kt + 8 * (mi >> 1) + (lane & 7);
-                        const int chunk = 2 * md + (mi & 1);
+                        constexpr uint32_t kMask3 = 0x00070007u;
                         uint32_t a[4];
-                        ptx::ldmatrix_x4_trans(vst + tok * 256 + (((chunk & 8) | ((chunk & 7) ^ (tok & 7))) << 4),
-                                               a[0], a[1], a[2], a[3]);
+                        a[0] = win[0][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
+                        a[1] = win[0][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
+                        a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
+                        a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
                         ptx::mma16816<false>(o[md], a, pbf[kt][0], pbf[kt][1]);
                     }
                 }
@@ -1061,7 +1053,6 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const bool u3 = cache_kind == kU3;
     const int es = cache_kind == kE4M3 ? 1 : 2;
     const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
-    const int f16_row = u3 ? 2 * head_dim : 0;         // per-warp V staging (3-bit)
     int nh = 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
@@ -1070,9 +1061,9 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     int stages = 8;
     const int meta = u3 ? 6 * block_size * num_kv_heads : 0;
     while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 ||
-                          smem_layout(nh, block_size, row, stages, batch, f16_row, meta).total > budget))
+                          smem_layout(nh, block_size, row, stages, batch, meta).total > budget))
         --stages;
-    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, f16_row, u3 ? 6 * block_size * num_kv_heads : 0);
+    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, meta);
     if (L.total > budget) return false;
     const int n_hg = num_kv_heads / nh;
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
