@@ -105,7 +105,13 @@ typedef struct pkv_tensor {
  *     code c means e4m3(c) * scale.
  *   k_qscale, v_qscale (F16) and k_qzero, v_qzero (U8), U3 only:
  *     [num_blocks, block_size, num_kv_heads]; a stored code u means
- *     (u - zero) * scale for its (slot, head) row.
+ *     (u - zero) * scale for its (slot, head) row.  Any strides are
+ *     accepted (the two scale arrays alike, the two zero arrays alike).
+ *     Decode reads them fastest head-major (slot stride 1, head stride
+ *     block_size: a [num_blocks, num_kv_heads, block_size] array seen through
+ *     a transposed view), where each CTA stages only its own heads' runs;
+ *     slot-major (head stride 1, slot stride num_kv_heads) also takes the
+ *     persistent kernel; other layouts take the general one.
  */
 typedef struct pkv_cache {
     pkv_tensor k_cache;

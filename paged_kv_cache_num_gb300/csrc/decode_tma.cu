@@ -194,8 +194,19 @@ struct Tile {
     static constexpr int QK = D / 16;               // QK k-steps
 };
 
+// 3-bit caches: CTAs of (at most) 4 kv heads, three per SM -- the consumers
+// are latency-bound on the unpacking and gain from more warps per SM, and
+// 3 x 5 warps keep at most 4 warps (128 registers each) per SM sub-partition.
+// The others: CTAs of up to 8 kv heads, one per SM.
+constexpr int kU3Heads = 4;
+constexpr int kU3CtasPerSm = 3;
+template <int CK>
+constexpr int kCtasPerSm = CK == kU3 ? kU3CtasPerSm : 1;
+template <int CK>
+constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
+
 template <int CK, int D, int BS>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(kMaxThreads<CK>, kCtasPerSm<CK>)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeParams p, FastParams f)
 {
@@ -206,8 +217,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nh = f.nh, B = p.batch, G = p.group, stages = f.stages;
     // 3-bit metadata per stage: K scales, V scales (fp16), K zeros, V zeros
-    // (u8) of all num_kv_heads for the block's BS slots
-    const int meta_bytes = T::kIsU3 ? 6 * BS * p.num_kv_heads : 0;
+    // (u8) for the block's BS slots, of the CTA's nh heads ([nh][BS] runs,
+    // head-major arrays) or of all num_kv_heads ([BS][num_kv_heads])
+    const int meta_bytes = T::kIsU3 ? 6 * BS * f.meta_heads : 0;
     const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
@@ -313,12 +325,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                                 ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
                             }
                             if constexpr (T::kIsU3) {
-                                const int HB = BS * p.num_kv_heads;       // entries per block
+                                const int HB = BS * f.meta_heads;         // entries per stage
+                                // head-major: the group's heads are one run at head hgk*nh
+                                const int64_t h0 = f.meta_heads == nh ? int64_t(hgk) * nh * BS : 0;
                                 const uint32_t md = vdst + L.tile_bytes;
-                                ptx::bulk_load(md, p.k_qs + int64_t(pbk) * p.m_blk, 2 * HB, fb);
-                                ptx::bulk_load(md + 2 * HB, p.v_qs + int64_t(pbk) * p.m_blk, 2 * HB, fb);
-                                ptx::bulk_load(md + 4 * HB, p.k_qz + int64_t(pbk) * p.z_blk, HB, fb);
-                                ptx::bulk_load(md + 5 * HB, p.v_qz + int64_t(pbk) * p.z_blk, HB, fb);
+                                ptx::bulk_load(md, p.k_qs + int64_t(pbk) * p.m_blk + h0, 2 * HB, fb);
+                                ptx::bulk_load(md + 2 * HB, p.v_qs + int64_t(pbk) * p.m_blk + h0, 2 * HB, fb);
+                                ptx::bulk_load(md + 4 * HB, p.k_qz + int64_t(pbk) * p.z_blk + h0, HB, fb);
+                                ptx::bulk_load(md + 5 * HB, p.v_qz + int64_t(pbk) * p.z_blk + h0, HB, fb);
                             }
                         } else {
                             ptx::mbar_arrive(fb);
@@ -723,19 +737,22 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const uint32_t vpk = kpk + L.tile_bytes;                                 // packed V rows
                 const bool partial = valid < BS;
                 // ---- metadata of this lane's score rows (tokens gid, gid+8 of
-                // each tile), staged with the block: [BS][num_kv_heads] arrays
-                const int HKV = p.num_kv_heads;
+                // each tile), staged with the block: [nh][BS] runs (head-major)
+                // or [BS][num_kv_heads] arrays
+                const int MH = f.meta_heads;
+                const bool hmaj = MH == nh;
+                const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? warp * BS : kvh;
                 const unsigned char *meta = smem + (s * L.stage_bytes + 2 * L.tile_bytes);
                 const __half *mks = reinterpret_cast<const __half *>(meta);
-                const __half *mvs = mks + BS * HKV;
-                const uint8_t *mkz = meta + 4 * BS * HKV;
-                const uint8_t *mvz = mkz + BS * HKV;
+                const __half *mvs = mks + BS * MH;
+                const uint8_t *mkz = meta + 4 * BS * MH;
+                const uint8_t *mvz = mkz + BS * MH;
                 float sk[T::KT][2], zk[T::KT][2], sv[T::KT][2], zv[T::KT][2];
 #pragma unroll
                 for (int mt = 0; mt < T::KT; ++mt)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int e = (16 * mt + gid + 8 * r) * HKV + kvh;
+                        const int e = (16 * mt + gid + 8 * r) * m_tok + m_h;
                         sk[mt][r] = __half2float(mks[e]);
                         sv[mt][r] = __half2float(mvs[e]);
                         zk[mt][r] = float(mkz[e]);
@@ -1048,19 +1065,24 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
 
 // Choose heads per CTA, stages and grid for the fast kernel.
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
-               int cache_kind, int sm_count, FastParams &f, size_t &workspace)
+               int cache_kind, bool meta_head_major, int sm_count, FastParams &f, size_t &workspace)
 {
     const bool u3 = cache_kind == kU3;
     const int es = cache_kind == kE4M3 ? 1 : 2;
     const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
-    int nh = 8;
+    int nh = u3 ? kU3Heads : 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
-    const int budget = 227 * 1024;
+    // 3-bit kernels are register-capped so that several CTAs share an SM; the
+    // shared memory (228 KB per SM, 1 KB of it reserved per CTA) and the
+    // bytes kept in flight are split between them
+    const int ctas_per_sm = u3 ? kU3CtasPerSm : 1;
+    const int budget = (228 * 1024) / ctas_per_sm - 1024;
     // ring depth: enough bytes in flight per SM, within the shared memory
     int stages = 8;
-    const int meta = u3 ? 6 * block_size * num_kv_heads : 0;
-    while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 ||
+    const int meta_heads = meta_head_major ? nh : num_kv_heads;
+    const int meta = u3 ? 6 * block_size * meta_heads : 0;
+    while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 / ctas_per_sm ||
                           smem_layout(nh, block_size, row, stages, batch, meta).total > budget))
         --stages;
     const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, meta);
@@ -1070,8 +1092,10 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     f.nh = nh;
     f.n_hg = n_hg;
     f.stages = stages;
-    f.grid = int(max_units < sm_count ? (max_units > 0 ? max_units : 1) : sm_count);
+    const int64_t slots = int64_t(sm_count) * ctas_per_sm;
+    f.grid = int(max_units < slots ? (max_units > 0 ? max_units : 1) : slots);
     f.smem_bytes = L.total;
+    f.meta_heads = meta_heads;
     const int group = num_heads / num_kv_heads;
     const int64_t rows = (int64_t(f.grid) + int64_t(n_hg) * batch) * nh * group;
     const size_t prefix_bytes = (size_t(batch + 1) * 4 + 255) / 256 * 256;

@@ -359,19 +359,23 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
         const size_t qa = ci.kind == PKV_DTYPE_U3 ? 16 : (ci.kind == PKV_DTYPE_E4M3 ? 8 : 4);
         const bool q_ok = aligned(q->data, qa) && (p.q_b % qa) == 0 && (p.q_h % qa) == 0;
         // 3-bit: each block's metadata must be one contiguous, 16-byte aligned
-        // [block_size][num_kv_heads] run per array (staged with bulk copies)
-        bool meta_ok = true;
+        // run per array (staged with bulk copies), either head-major
+        // [num_kv_heads][block_size] (a CTA copies its own heads) or
+        // slot-major [block_size][num_kv_heads] (a CTA copies all heads)
+        bool meta_ok = true, meta_hmaj = false;
         if (ci.kind == PKV_DTYPE_U3) {
             const int64_t hb = ci.block_size * ci.num_kv_heads;
-            meta_ok = p.m_head == 1 && p.m_slot == ci.num_kv_heads && p.z_head == 1 &&
-                      p.z_slot == ci.num_kv_heads && (p.m_blk * 2) % 16 == 0 && p.z_blk % 16 == 0 &&
-                      (hb % 16) == 0 && aligned(p.k_qs, 16) && aligned(p.v_qs, 16) && aligned(p.k_qz, 16) &&
-                      aligned(p.v_qz, 16);
+            meta_hmaj = p.m_slot == 1 && p.m_head == ci.block_size && p.z_slot == 1 && p.z_head == ci.block_size;
+            const bool smaj = p.m_head == 1 && p.m_slot == ci.num_kv_heads && p.z_head == 1 &&
+                              p.z_slot == ci.num_kv_heads;
+            meta_ok = (meta_hmaj || smaj) && (p.m_blk * 2) % 16 == 0 && p.z_blk % 16 == 0 && (hb % 16) == 0 &&
+                      (ci.block_size % 16) == 0 && aligned(p.k_qs, 16) && aligned(p.v_qs, 16) &&
+                      aligned(p.k_qz, 16) && aligned(p.v_qz, 16);
         }
         pkv::FastParams f{};
         size_t ws = 0;
         if (q_ok && meta_ok && pkv::plan_fast(p.batch, p.num_heads, p.num_kv_heads, p.head_dim, p.block_size, p.max_blocks,
-                                   ci.kind, sm, f, ws) &&
+                                   ci.kind, meta_hmaj, sm, f, ws) &&
             pkv::fast_maps_encodable(p, ci.kind, f.nh)) {
             dc.plan.kernel = 1;
             dc.plan.fast = f;

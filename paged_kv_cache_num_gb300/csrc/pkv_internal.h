@@ -99,6 +99,8 @@ struct FastParams {
     int stages;                 // shared-memory ring depth
     int grid;                   // persistent CTAs
     int smem_bytes;
+    int meta_heads;             // 3-bit: kv heads whose scale/zero runs a stage holds
+                                // (nh when the arrays are head-major, else all)
     int32_t *prefix;            // [B+1] blocks-per-sequence prefix sums (workspace)
     float *part_ml;             // [(grid + n_hg*B) * nh * G, 2]
     float *part_acc;            // [(grid + n_hg*B) * nh * G, D]
@@ -117,7 +119,8 @@ DecodePlan plan_decode_general(int batch, int num_heads, int num_kv_heads, int h
 
 bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch);
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-               int max_blocks, int cache_kind, int sm_count, FastParams &f, size_t &workspace);
+               int max_blocks, int cache_kind, bool meta_head_major, int sm_count, FastParams &f,
+               size_t &workspace);
 bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh);
 
 cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cudaStream_t s);

@@ -173,16 +173,24 @@ class KVCache:
         elif kind == "u3":
             k = torch.empty(shape + (3 * head_dim // 8,), dtype=torch.uint8, device=device)
             v = torch.empty_like(k)
-            c = KVCache(kind, k, v,
-                        k_qscale=torch.empty(shape, dtype=torch.float16, device=device),
-                        k_qzero=torch.empty(shape, dtype=torch.uint8, device=device),
-                        v_qscale=torch.empty(shape, dtype=torch.float16, device=device),
-                        v_qzero=torch.empty(shape, dtype=torch.uint8, device=device))
+            # scale / zero stored head-major ([num_blocks, num_kv_heads,
+            # block_size]) and seen through a [num_blocks, block_size,
+            # num_kv_heads] view: a decode CTA then stages only its own heads'
+            # runs of each block
+            meta = (num_blocks, num_kv_heads, block_size)
+
+            def mk(dt):
+                return torch.empty(meta, dtype=dt, device=device).permute(0, 2, 1)
+
+            c = KVCache(kind, k, v, k_qscale=mk(torch.float16), k_qzero=mk(torch.uint8),
+                        v_qscale=mk(torch.float16), v_qzero=mk(torch.uint8))
         else:
             raise ValueError(kind)
         if fill is not None:
             for t in (c.k_cache, c.v_cache, c.k_qscale, c.k_qzero, c.v_qscale, c.v_qzero):
                 if t is not None:
+                    if not t.is_contiguous():
+                        t = t.permute(0, 2, 1)
                     t.view(torch.uint8).fill_(fill)
         return c
 

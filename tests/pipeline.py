@@ -18,14 +18,20 @@ def src_code(w):
 
 # ---------------------------------------------------------------- GPU side
 
-def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, stream=None):
-    """Fill + append + decode on the GPU.  Returns (cache, out)."""
+def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, stream=None,
+            meta_slot_major=False):
+    """Fill + append + decode on the GPU.  Returns (cache, out).
+    meta_slot_major: store 3-bit scale/zero arrays contiguous [blocks, slots,
+    heads] instead of the allocator's head-major layout."""
     dev = "cuda"
     cache = pkv.KVCache.allocate(w.cache_kind, w.num_blocks, w.block_size, w.num_kv_heads,
                                  w.head_dim, device=dev,
                                  k_scale=None if w.k_scale is None else w.k_scale.to(dev),
                                  v_scale=None if w.v_scale is None else w.v_scale.to(dev),
                                  fill=0)
+    if meta_slot_major and w.cache_kind == "u3":
+        for name in ("k_qscale", "k_qzero", "v_qscale", "v_qzero"):
+            setattr(cache, name, torch.zeros_like(getattr(cache, name).contiguous()))
     if w.k_cache0 is not None:
         cache.k_cache.copy_(w.k_cache0.to(dev))
         cache.v_cache.copy_(w.v_cache0.to(dev))
@@ -59,7 +65,7 @@ def gpu_cache_host(cache):
     for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero"):
         t = getattr(cache, name)
         if t is not None:
-            t = t.cpu()
+            t = t.cpu().contiguous()
             d[name] = t.view(torch.int16).numpy().view(np.uint16) if t.element_size() == 2 \
                 else t.view(torch.uint8).numpy()
     return d

@@ -122,6 +122,20 @@ def test_u3_poisoned_tail_metadata(pkv, orc):
         assert torch.equal(clean, dirty)
 
 
+def test_u3_slot_major_metadata(pkv, orc):
+    """Scale / zero arrays stored slot-major (each CTA stages every head's
+    metadata) give the same output as the head-major default, and match the
+    oracle."""
+    w = W.u3_mha(batch=5, ctx_lo=3, ctx_hi=700, num_heads=16, seed=91)
+    c1, out_h = PL.gpu_run(w, pkv)
+    c2, out_s = PL.gpu_run(w, pkv, meta_slot_major=True)
+    assert c1.k_qscale.stride()[1:] == (1, w.block_size)
+    assert c2.k_qscale.is_contiguous()
+    assert torch.equal(out_h, out_s)
+    oc = PL.oracle_caches(w, orc)
+    _check(w, out_s, PL.oracle_decode(w, orc, oc))
+
+
 def test_u3_head_dim_64(pkv, orc):
     w = W.u3_mha(batch=3, ctx_lo=5, ctx_hi=300, num_heads=4, head_dim=64, seed=34)
     cache, out = PL.gpu_run(w, pkv)
