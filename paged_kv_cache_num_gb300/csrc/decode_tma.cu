@@ -1,4 +1,4 @@
-// decode_tma.cu -- the fast paged-decode path for 16-bit and fp8 caches:
+// decode_tma.cu -- the fast paged-decode path for 16-bit, fp8 and 3-bit caches:
 // a persistent, load-balanced kernel that streams whole physical blocks into
 // shared memory with TMA and runs both products of each block on tensor
 // cores, plus the merge kernel for sequences split across CTAs.
@@ -29,15 +29,17 @@
 // a ring of `stages` shared-memory stages guarded by full/empty mbarriers.
 // Each consumer warp computes, for its kv head and the G <= 8 query heads
 // that share it, with m16n8k16 mma.sync (block tokens on M, q heads on N):
-//   S^T = K Q^T (K from shared memory by ldmatrix, or fp8 bytes converted to
-//   f16 in registers), masking of tokens >= context_len, online softmax per
-//   q head in log2 units, O^T = O^T * alpha + V^T P^T (P^T moved from the
-//   score accumulators into operand layout by movmatrix; V^T by
-//   ldmatrix.trans or fp8 byte pairing + conversion).
+//   S^T = K Q^T (K from shared memory by ldmatrix, or fp8 / 3-bit codes
+//   converted to f16 in registers), masking of tokens >= context_len, online
+//   softmax per q head in log2 units, O^T = O^T * alpha + V^T P^T (P^T moved
+//   from the score accumulators into operand layout by movmatrix; V^T by
+//   ldmatrix.trans, or fp8 / 3-bit code pairing + conversion).  3-bit
+//   blocks also bring their per-token scale / zero runs with bulk copies.
 // Every wait is bounded (about 2 s of wall time) and raises
 // PKV_DEVERR_TIMEOUT instead of hanging.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pkv_device.cuh"
@@ -47,6 +49,7 @@ namespace pkv {
 namespace {
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
 #define NEG_INF (-__int_as_float(0x7f800000))
 
 struct SmemLayout {
@@ -205,12 +208,15 @@ constexpr int kCtasPerSm = CK == kU3 ? kU3CtasPerSm : 1;
 template <int CK>
 constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
 
-template <int CK, int D, int BS>
+// G1: one q head per kv head (multi-head attention) -- the consumers skip
+// the second head column of their C fragments, which never exists then.
+template <int CK, int D, int BS, bool G1 = false>
 __global__ void __launch_bounds__(kMaxThreads<CK>, kCtasPerSm<CK>)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeParams p, FastParams f)
 {
     using T = Tile<CK, D, BS>;
+    constexpr int NC = G1 ? 1 : 2;      // head columns (2tig, 2tig+1) that can exist
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -789,14 +795,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = e >> 1, c = e & 1;
+                        if (c >= NC) continue;
                         float v = mult * sk[t][r] * (sc[t][e] - zk[t][r] * q1h[c]);
                         if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
                         sc[t][e] = v;
                         mx[c] = fmaxf(mx[c], v);
                     }
-                float alpha[2];
+                float alpha[2] = {1.0f, 1.0f};
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < NC; ++c) {
                     mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
                     mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
                     mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
@@ -814,22 +821,24 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     for (int r = 0; r < 2; ++r) {
                         const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
                         const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
-                        const float p1 = exp2_approx(sc[t][2 * r + 1] - m[1]);
+                        const float p1 = NC > 1 ? exp2_approx(sc[t][2 * r + 1] - m[1]) : 0.0f;
                         l[0] += p0;
-                        l[1] += p1;
+                        if (NC > 1) l[1] += p1;
                         float q0, q1;
                         const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
                         zs[0] += q0 * zv[t][r];
-                        zs[1] += q1 * zv[t][r];
+                        if (NC > 1) zs[1] += q1 * zv[t][r];
                         pbf[t][r] = ptx::movmatrix_trans(w);
                     }
                 if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
                     for (int t = 0; t < T::DT / 2; ++t) {
                         o[t][0] *= alpha[0];
-                        o[t][1] *= alpha[1];
                         o[t][2] *= alpha[0];
-                        o[t][3] *= alpha[1];
+                        if (NC > 1) {
+                            o[t][1] *= alpha[1];
+                            o[t][3] *= alpha[1];
+                        }
                     }
                 }
                 // ---- O^T += V'^T P'^T with V converted straight into A
@@ -1010,19 +1019,24 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
     return r == CUDA_SUCCESS;
 }
 
-template <int CK, int D, int BS>
+template <int CK, int D, int BS, bool G1 = false>
 cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                           const CUtensorMap &mv, cudaStream_t s)
 {
-    auto kern = decode_tma_kernel<CK, D, BS>;
-    static int configured = 0;
-    if (configured < f.smem_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem_bytes);
+    auto kern = decode_tma_kernel<CK, D, BS, G1>;
+    // dynamic shared memory limit, raised once per device as needed
+    static std::atomic<int> configured[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (configured[dev].load(std::memory_order_relaxed) < f.smem_bytes) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem_bytes);
         if (e != cudaSuccess) return e;
-        configured = f.smem_bytes;
+        configured[dev].store(f.smem_bytes, std::memory_order_relaxed);
     }
     kern<<<f.grid, (f.nh + 1) * 32, f.smem_bytes, s>>>(mk, mv, p, f);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int rows = p.batch * p.num_heads;
     cudaLaunchConfig_t cfg = {};
@@ -1042,6 +1056,12 @@ template <int CK, int D>
 cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                            const CUtensorMap &mv, cudaStream_t s)
 {
+    if constexpr (CK == kU3) {      // MHA caches get the one-column consumers
+        if (p.group == 1) {
+            if (p.block_size == 16) return launch_fast_t<CK, D, 16, true>(p, f, mk, mv, s);
+            if (p.block_size == 32) return launch_fast_t<CK, D, 32, true>(p, f, mk, mv, s);
+        }
+    }
     switch (p.block_size) {
     case 16: return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
     case 32: return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
