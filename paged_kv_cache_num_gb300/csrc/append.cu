@@ -15,7 +15,8 @@
 // coalesced 16-byte loads and stores; the grid is a function of num_tokens
 // only (CUDA-graph safe).  The 3-bit kernel gives each warp one row: the
 // min / max are warp-shuffle reductions and the packing goes through shared
-// memory.
+// memory.  All are programmatic dependent launches, so the launch of each
+// overlaps the tail of the previous kernel in the stream.
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -41,6 +42,8 @@ __device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, i
 template <int CHUNK>
 __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParams p)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int chunks_per_row = p.head_dim * 2 / CHUNK;
     const int64_t per_token = int64_t(2) * p.num_kv_heads * chunks_per_row;
     const int64_t total = p.num_tokens * per_token;
@@ -70,6 +73,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
 template <int SRC, bool VEC>
 __global__ void __launch_bounds__(kAppendThreads) append_e4m3_kernel(AppendParams p)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int groups = p.head_dim / 8;
     const int64_t per_token = int64_t(2) * p.num_kv_heads * groups;
     const int64_t total = p.num_tokens * per_token;
@@ -122,6 +127,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_e4m3_kernel(AppendParam
 template <int SRC, int EPL>
 __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams p)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     constexpr int D = EPL * 32;
     constexpr int WARPS = kAppendThreads / 32;
     __shared__ uint8_t codes[WARPS][D];
@@ -185,6 +192,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
 
 __global__ void slot_mapping_kernel(SlotMapParams p)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < p.n;
          t += int64_t(gridDim.x) * blockDim.x) {
         const int32_t pos = p.pos[t * p.pos_stride];
@@ -219,31 +228,31 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
     if (cache_kind == kF16 || cache_kind == kBF16) {
         if (vec16) {
             const int64_t work = p.num_tokens * 2 * p.num_kv_heads * (p.head_dim * 2 / 16);
-            append_copy_kernel<16><<<grid_for(work, T), T, 0, s>>>(p);
+            return launch_pdl(append_copy_kernel<16>, grid_for(work, T), T, 0, s, p);
         } else {
             const int64_t work = p.num_tokens * 2 * p.num_kv_heads * p.head_dim;
-            append_copy_kernel<2><<<grid_for(work, T), T, 0, s>>>(p);
+            return launch_pdl(append_copy_kernel<2>, grid_for(work, T), T, 0, s, p);
         }
     } else if (cache_kind == kE4M3) {
         const int64_t work = p.num_tokens * 2 * p.num_kv_heads * (p.head_dim / 8);
         const int g = grid_for(work, T);
         if (p.src_kind == kBF16) {
-            if (vec16) append_e4m3_kernel<kBF16, true><<<g, T, 0, s>>>(p);
-            else append_e4m3_kernel<kBF16, false><<<g, T, 0, s>>>(p);
+            if (vec16) return launch_pdl(append_e4m3_kernel<kBF16, true>, g, T, 0, s, p);
+            else return launch_pdl(append_e4m3_kernel<kBF16, false>, g, T, 0, s, p);
         } else {
-            if (vec16) append_e4m3_kernel<kF16, true><<<g, T, 0, s>>>(p);
-            else append_e4m3_kernel<kF16, false><<<g, T, 0, s>>>(p);
+            if (vec16) return launch_pdl(append_e4m3_kernel<kF16, true>, g, T, 0, s, p);
+            else return launch_pdl(append_e4m3_kernel<kF16, false>, g, T, 0, s, p);
         }
     } else {  // kU3
         const int64_t rows = p.num_tokens * 2 * p.num_kv_heads;
         const int g = grid_for(rows * 32, T);
         const bool bf = p.src_kind == kBF16;
         if (p.head_dim == 128) {
-            if (bf) append_u3_kernel<kBF16, 4><<<g, T, 0, s>>>(p);
-            else append_u3_kernel<kF16, 4><<<g, T, 0, s>>>(p);
+            if (bf) return launch_pdl(append_u3_kernel<kBF16, 4>, g, T, 0, s, p);
+            else return launch_pdl(append_u3_kernel<kF16, 4>, g, T, 0, s, p);
         } else {
-            if (bf) append_u3_kernel<kBF16, 2><<<g, T, 0, s>>>(p);
-            else append_u3_kernel<kF16, 2><<<g, T, 0, s>>>(p);
+            if (bf) return launch_pdl(append_u3_kernel<kBF16, 2>, g, T, 0, s, p);
+            else return launch_pdl(append_u3_kernel<kF16, 2>, g, T, 0, s, p);
         }
     }
     return cudaGetLastError();
@@ -252,8 +261,7 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
 cudaError_t launch_slot_mapping(const SlotMapParams &p, cudaStream_t s)
 {
     if (p.n == 0) return cudaSuccess;
-    slot_mapping_kernel<<<grid_for(p.n, 256), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(slot_mapping_kernel, grid_for(p.n, 256), 256, 0, s, p);
 }
 
 }  // namespace pkv

@@ -232,6 +232,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
     int *prefix = reinterpret_cast<int *>(smem + L.prefix_off);
     int *nblk = reinterpret_cast<int *>(smem + L.nblk_off);
+    griddep_wait();                // the stream's previous kernel (an append) is done
 
     // ---- per-sequence block counts and their prefix sums
     const int cap = p.max_blocks << p.block_shift;
@@ -271,7 +272,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int b = threadIdx.x; b <= B; b += blockDim.x) f.prefix[b] = prefix[b];
 
     // the merge kernel may be scheduled now; it waits for this grid to finish
-    asm volatile("griddepcontrol.launch_dependents;");
+    griddep_launch_dependents();
     const int64_t NBT = prefix[B];                  // blocks per head group
     const int64_t N = NBT * f.n_hg;
     const int64_t lo = int64_t(blockIdx.x) * N / gridDim.x;
@@ -922,7 +923,7 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f
 {
     // launched as a programmatic dependent of the decode kernel: wait until
     // that grid has completed and its writes are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    griddep_wait();
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= p.batch * p.num_heads) return;
@@ -1035,21 +1036,10 @@ cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUte
         if (e != cudaSuccess) return e;
         configured[dev].store(f.smem_bytes, std::memory_order_relaxed);
     }
-    kern<<<f.grid, (f.nh + 1) * 32, f.smem_bytes, s>>>(mk, mv, p, f);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(f.grid), dim3((f.nh + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
     if (e != cudaSuccess) return e;
     const int rows = p.batch * p.num_heads;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((rows + 7) / 8);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel<D>, p, f);
+    return launch_pdl(merge_kernel<D>, dim3((rows + 7) / 8), dim3(256), 0, s, p, f);
 }
 
 template <int CK, int D>

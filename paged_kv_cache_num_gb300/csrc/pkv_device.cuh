@@ -10,6 +10,21 @@
 
 namespace pkv {
 
+// Programmatic dependent launch.  A kernel launched with
+// launch_pdl may start while the previous kernel of its stream still runs:
+// it must call griddep_wait() before touching any global memory that kernel
+// may write, and calls griddep_launch_dependents() once the next kernel may
+// be scheduled.  Both are no-ops for a normally launched kernel.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
 __device__ __forceinline__ void raise_err(int32_t *flag, int bits)
 {
     if (flag) atomicOr(flag, bits);

@@ -136,6 +136,25 @@ cudaError_t launch_copy_peak(const void *src, void *dst, size_t bytes, cudaStrea
 
 int sm_count_current_device();
 
+// Launch `kernel` on `s` with programmatic stream serialization: it may
+// begin while the stream's previous kernel finishes (see griddep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Record `msg` as this host thread's pkv_last_error() text; returns `code`.
 int set_last_error(int code, const char *msg);
 

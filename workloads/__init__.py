@@ -300,11 +300,11 @@ def u3_mha(device="cpu", batch=32, ctx_lo=1024, ctx_hi=8192, num_heads=32, head_
     return w
 
 
-def all_octets() -> torch.Tensor:
+def all_octets(device="cpu") -> torch.Tensor:
     """Every 24-bit octet state as 8 lane values, uint8 [2^24, 8]: state n
     has lane i = bits 3i..3i+2 of n (enumeration of the state space)."""
-    n = torch.arange(1 << 24, dtype=torch.int64)
-    lanes = torch.arange(8, dtype=torch.int64) * 3
+    n = torch.arange(1 << 24, dtype=torch.int64, device=device)
+    lanes = torch.arange(8, dtype=torch.int64, device=device) * 3
     return ((n[:, None] >> lanes[None, :]) & 7).to(torch.uint8)
 
 
