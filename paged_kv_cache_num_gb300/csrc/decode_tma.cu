@@ -918,6 +918,8 @@ __device__ __forceinline__ int64_t floordiv_i64(int64_t a, int64_t n)
 // Merge the partials of units split across CTAs (one warp per (sequence,
 // q head)); units held whole by one CTA were written by it, units with an
 // empty context get zeros.
+constexpr int kMergeBatch = 8;   // partials a row combines in one round trip
+
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f)
 {
@@ -948,26 +950,80 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f
         const int64_t i1 = floordiv_i64((first + n) * S - 1, N);
         if (i0 == i1) return;                         // written whole by CTA i0
         const int64_t unit = int64_t(hg) * p.batch + b;
+        const int64_t stride = int64_t(nh) * G;      // partial rows per CTA slot
         // with fewer blocks than CTAs some CTAs have an empty range and wrote
         // nothing (never the case when N >= S)
-        auto empty_range = [&](int64_t i) {
-            return N < S && (i * N) / S == ((i + 1) * N) / S;
-        };
-        float M = NEG_INF;
-        for (int64_t i = i0; i <= i1; ++i)
-            if (!empty_range(i)) M = fmaxf(M, f.part_ml[2 * ((i + unit) * nh * G + local)]);
-        float Lsum = 0.0f;
-        if (M != NEG_INF) {
-            for (int64_t i = i0; i <= i1; ++i) {
-                if (empty_range(i)) continue;
-                const int64_t row = (i + unit) * nh * G + local;
-                const float mi = f.part_ml[2 * row];
-                const float wgt = mi == NEG_INF ? 0.0f : exp2_approx(mi - M);
-                Lsum += f.part_ml[2 * row + 1] * wgt;
-                const float *pa = f.part_acc + row * D + EPL * lane;
+        auto live = [&](int64_t i) { return !(N < S && (i * N) / S == ((i + 1) * N) / S); };
+        const int64_t np = i1 - i0 + 1;               // partials (CTA slots) to combine
+        float M = NEG_INF, Lsum = 0.0f;
+        if (np <= kMergeBatch) {
+            // one round trip: lane k loads (m, l) of partial k while every
+            // lane loads its head_dim slice of all partials
+            float v[kMergeBatch][EPL];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] += pa[e] * wgt;
+            for (int k = 0; k < kMergeBatch; ++k) {
+                const bool ok = k < np && live(i0 + k);
+                const float *pa = f.part_acc + ((i0 + k + unit) * stride + local) * D + EPL * lane;
+                if constexpr (EPL == 4) {
+                    const float4 t = ok ? *reinterpret_cast<const float4 *>(pa) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[k][0] = t.x;
+                    v[k][1] = t.y;
+                    v[k][2] = t.z;
+                    v[k][3] = t.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) v[k][e] = ok ? pa[e] : 0.0f;
+                }
             }
+            float mi = NEG_INF, li = 0.0f;
+            if (lane < np && live(i0 + lane)) {
+                const int64_t row = (i0 + lane + unit) * stride + local;
+                mi = f.part_ml[2 * row];
+                li = f.part_ml[2 * row + 1];
+            }
+            M = mi;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float wgt = mi == NEG_INF ? 0.0f : exp2_approx(mi - M);
+            Lsum = li * wgt;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, wgt, k);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] += v[k][e] * wk;
+            }
+        } else {
+            // many partials (a long sequence over many CTAs): lanes over the
+            // partials for the maximum and the weights, then lanes over
+            // head_dim for the accumulation, 32 partials at a time
+            for (int64_t c = i0; c <= i1; c += 32) {
+                const int64_t i = c + lane;
+                if (i <= i1 && live(i)) M = fmaxf(M, f.part_ml[2 * ((i + unit) * stride + local)]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            for (int64_t c = i0; c <= i1; c += 32) {
+                const int64_t i = c + lane;
+                float wgt = 0.0f;
+                if (i <= i1 && live(i)) {
+                    const int64_t row = (i + unit) * stride + local;
+                    const float mi = f.part_ml[2 * row];
+                    wgt = mi == NEG_INF ? 0.0f : exp2_approx(mi - M);
+                    Lsum += f.part_ml[2 * row + 1] * wgt;
+                }
+                const int cnt = int(i1 - c + 1 < 32 ? i1 - c + 1 : 32);
+                for (int k = 0; k < cnt; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, wgt, k);
+                    if (wk == 0.0f) continue;       // uniform; also skips unwritten slots
+                    const float *pa = f.part_acc + ((c + k + unit) * stride + local) * D + EPL * lane;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc[e] += pa[e] * wk;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
         }
         const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
 #pragma unroll
