@@ -72,3 +72,28 @@ def test_walking_isolation_on_gpu(pkv, orc):
     assert np.array_equal(words.cpu().numpy().reshape(-1, 32), vals)
     assert np.array_equal(packed.cpu().numpy().reshape(-1, 3),
                           orc.pack3(vals.reshape(-1, 8)))
+
+
+@pytest.mark.parametrize("n,off", [(4099, 4), (4099, 0), (33, 8), (16, 12)])
+def test_unpack_alignments(pkv, orc, n, off):
+    """unpack3 from packed data at 16-byte aligned and merely 4-byte aligned
+    addresses (both kernels), with tails of every length mod 16."""
+    rng = np.random.default_rng(n + off)
+    packed_h = rng.integers(0, 256, size=(n * 3,), dtype=np.uint8)
+    buf = torch.zeros(n * 3 + 16, dtype=torch.uint8, device="cuda")
+    buf[off:off + n * 3] = torch.from_numpy(packed_h).cuda()
+    got = pkv.unpack3(buf[off:off + n * 3])
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy().reshape(-1, 8), orc.unpack3(packed_h.reshape(-1, 3)))
+
+
+@pytest.mark.parametrize("m,off", [(50001, 0), (50001, 4), (3, 0), (6, 8)])
+def test_unpack_words_ragged_and_unaligned(pkv, orc, m, off):
+    rng = np.random.default_rng(m + off)
+    W_ = rng.integers(0, 1 << 32, size=(m, 3), dtype=np.uint64).astype(np.uint32)
+    buf = torch.zeros(m * 3 + 4, dtype=torch.int32, device="cuda")
+    o = off // 4
+    buf[o:o + m * 3] = torch.from_numpy(W_.view(np.int32).reshape(-1).copy()).cuda()
+    got = pkv.unpack3_words(buf[o:o + m * 3])
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy().reshape(-1, 32), orc.unpack3_words(W_))
