@@ -579,11 +579,9 @@ def main():
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         dpack.copy_(hpack, non_blocking=True)
-        pkv.slot_mapping(dbuf["block_tables"], dbuf["new_req"], dbuf["new_pos"], w.block_size,
-                         out=st.slots, err_flag=st.err)
-        pkv.kv_append(dbuf["k_new"], dbuf["v_new"], st.slots, st.cache, err_flag=st.err)
-        pkv.paged_decode(dbuf["q"], st.cache, dbuf["block_tables"], dbuf["context_lens"],
-                         sm_scale=w.sm_scale, out=st.out, workspace=st.ws, err_flag=st.err)
+        pkv.decode_step(dbuf["k_new"], dbuf["v_new"], dbuf["new_req"], dbuf["new_pos"], dbuf["q"],
+                        st.cache, dbuf["block_tables"], dbuf["context_lens"], sm_scale=w.sm_scale,
+                        out=st.out, slots=st.slots, workspace=st.ws, err_flag=st.err)
         out_host.copy_(st.out, non_blocking=True)
         s.synchronize()
         if i >= 3:
@@ -674,8 +672,9 @@ def main():
                        "launch": "a device-timed step replays one CUDA graph (slot_mapping, "
                                  "kv_append, paged_decode; programmatic dependent launches); "
                                  "its append and decode parts are replayed alone for the "
-                                 "breakdown; e2e calls the C ABI eagerly with one packed "
-                                 "host-to-device copy of the step's inputs"},
+                                 "breakdown; e2e makes one eager pkv_decode_step call (slot "
+                                 "mapping, append, decode) after one packed host-to-device copy "
+                                 "of the step's inputs"},
             "pct_of_peak": round(100 * value / peak, 2),
             "decode_gbs": round(dec_gbs, 1), "decode_ms": round(dec_ms, 5),
             "append_tokens_per_s": round(n_real / (app_ms * 1e-3), 1),

@@ -235,6 +235,26 @@ int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tens
                      void *stream);
 
 /*
+ * pkv_decode_step -- one decode step of a serving loop in one call:
+ * pkv_slot_mapping of the step's tokens (block size from the cache), then
+ * pkv_kv_append of their K/V rows through that mapping, then
+ * pkv_paged_decode over every sequence ("Write Triton Kv Cache Append
+ * Kernel", reasoning step 9, followed by the decode of "10. Triton KV Cache
+ * and PagedAttention").  The arguments are those of the three calls, with
+ * the same meaning, layouts and rules; slot_mapping (I64 [num_tokens],
+ * caller-owned) receives the computed slots.  Every argument of all three
+ * is validated before the first launch, so an error status means nothing
+ * was enqueued.  The three launches are ordered on `stream` (the append and
+ * decode kernels start as programmatic dependents of the previous kernel).
+ * An addition of this library: it saves two host-side calls per step.
+ */
+int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *req,
+                    const pkv_tensor *pos, const pkv_tensor *slot_mapping, const pkv_tensor *q,
+                    const pkv_cache *cache, const pkv_tensor *block_tables, const pkv_tensor *context_lens,
+                    float sm_scale, const pkv_tensor *out, int num_splits, void *workspace,
+                    size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
  * pkv_paged_decode_noalloc -- pkv_paged_decode for callers that cannot
  * allocate device memory at call time: code being captured into a CUDA
  * graph, plugin or custom-op hooks of inference engines that may not

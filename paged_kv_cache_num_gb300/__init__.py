@@ -4,8 +4,10 @@ The compute lives in libpkv.so (CUDA kernels behind the C ABI of
 include/pkv.h); ``pkv`` is its ctypes binding.  Build with
 ``paged_kv_cache_num_gb300.build.build()``.
 """
-from .pkv import (KVCache, PkvError, copy_peak, decode_workspace_bytes, kv_append, lib,
-                  pack3, paged_decode, slot_mapping, unpack3, unpack3_words, version)
+from .pkv import (KVCache, PkvError, copy_peak, decode_step, decode_workspace_bytes, kv_append,
+                  lib, pack3, paged_decode, paged_decode_noalloc, slot_mapping, unpack3,
+                  unpack3_words, version)
 
-__all__ = ["KVCache", "PkvError", "copy_peak", "decode_workspace_bytes", "kv_append", "lib",
-           "pack3", "paged_decode", "slot_mapping", "unpack3", "unpack3_words", "version"]
+__all__ = ["KVCache", "PkvError", "copy_peak", "decode_step", "decode_workspace_bytes",
+           "kv_append", "lib", "pack3", "paged_decode", "paged_decode_noalloc", "slot_mapping",
+           "unpack3", "unpack3_words", "version"]

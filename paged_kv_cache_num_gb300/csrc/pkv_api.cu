@@ -171,8 +171,11 @@ const char *pkv_version(void) { return "pkv 0.1.0 (sm_103a)"; }
 int pkv_abi_version(void) { return PKV_ABI_VERSION; }
 const char *pkv_last_error(void) { return g_err; }
 
-int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, const pkv_tensor *pos,
-                     int block_size, const pkv_tensor *slot_mapping, int32_t *err_flag, void *stream)
+// Validation + launch parameters of each entry point, kept apart from the
+// launch so that pkv_decode_step can check all three before launching any.
+static int prep_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, const pkv_tensor *pos,
+                             int block_size, const pkv_tensor *slot_mapping, int32_t *err_flag,
+                             pkv::SlotMapParams &p)
 {
     TRY(check_tensor(block_tables, "block_tables", 2));
     TRY(check_tensor(req, "req", 1));
@@ -186,7 +189,7 @@ int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, cons
         return fail(PKV_ERR_SHAPE, "req, pos and slot_mapping lengths differ");
     if (slot_mapping->stride[0] != 1 && n > 1) return fail(PKV_ERR_LAYOUT, "slot_mapping must be contiguous");
     if (!is_pow2(block_size)) return fail(PKV_ERR_VALUE, "block_size must be a power of two");
-    pkv::SlotMapParams p{};
+    p = pkv::SlotMapParams{};
     p.bt = static_cast<const int32_t *>(block_tables->data);
     p.bt_b = block_tables->stride[0];
     p.bt_j = block_tables->stride[1];
@@ -200,11 +203,20 @@ int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, cons
     p.block_shift = log2i(block_size);
     p.slot_mapping = static_cast<int64_t *>(slot_mapping->data);
     p.err_flag = err_flag;
+    return PKV_OK;
+}
+
+int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, const pkv_tensor *pos,
+                     int block_size, const pkv_tensor *slot_mapping, int32_t *err_flag, void *stream)
+{
+    pkv::SlotMapParams p;
+    TRY(prep_slot_mapping(block_tables, req, pos, block_size, slot_mapping, err_flag, p));
     return launch_status(pkv::launch_slot_mapping(p, as_stream(stream)), "slot_mapping kernel");
 }
 
-int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *slot_mapping,
-                  const pkv_cache *cache, int32_t *err_flag, void *stream)
+static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *slot_mapping,
+                          const pkv_cache *cache, int32_t *err_flag, pkv::AppendParams &p, int &kind,
+                          bool &vec16)
 {
     TRY(check_tensor(k_new, "k_new", 3));
     TRY(check_tensor(v_new, "v_new", 3));
@@ -231,11 +243,11 @@ int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_te
     if (ci.kind == PKV_DTYPE_U3 && ci.head_dim != 64 && ci.head_dim != 128)
         return fail(PKV_ERR_UNSUPPORTED, "U3 append supports head_dim 64 and 128");
     const int64_t es = 2;
-    const bool vec16 = aligned(k_new->data, 16) && aligned(v_new->data, 16) &&
+    vec16 = aligned(k_new->data, 16) && aligned(v_new->data, 16) &&
                        (k_new->stride[0] * es) % 16 == 0 && (k_new->stride[1] * es) % 16 == 0 &&
                        (v_new->stride[0] * es) % 16 == 0 && (v_new->stride[1] * es) % 16 == 0 &&
                        (ci.head_dim * 2) % 16 == 0;
-    pkv::AppendParams p{};
+    p = pkv::AppendParams{};
     p.k_new = static_cast<const char *>(k_new->data);
     p.v_new = static_cast<const char *>(v_new->data);
     p.k_src_tok = k_new->stride[0] * es;
@@ -271,7 +283,18 @@ int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_te
     p.num_slots = ci.num_blocks * ci.block_size;
     p.src_kind = src;
     p.err_flag = err_flag;
-    return launch_status(pkv::launch_append(p, ci.kind, vec16, as_stream(stream)), "kv_append kernel");
+    kind = ci.kind;
+    return PKV_OK;
+}
+
+int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *slot_mapping,
+                  const pkv_cache *cache, int32_t *err_flag, void *stream)
+{
+    pkv::AppendParams p;
+    int kind = 0;
+    bool vec16 = false;
+    TRY(prep_kv_append(k_new, v_new, slot_mapping, cache, err_flag, p, kind, vec16));
+    return launch_status(pkv::launch_append(p, kind, vec16, as_stream(stream)), "kv_append kernel");
 }
 
 namespace {
@@ -401,11 +424,11 @@ int pkv_paged_decode_workspace(const pkv_tensor *q, const pkv_cache *cache, cons
     return ok();
 }
 
-int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
-                     const pkv_tensor *context_lens, float sm_scale, const pkv_tensor *out, int num_splits,
-                     void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream)
+static int prep_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
+                             const pkv_tensor *context_lens, float sm_scale, const pkv_tensor *out,
+                             int num_splits, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                             DecodeCheck &dc)
 {
-    DecodeCheck dc{};
     TRY(check_decode_common(q, cache, block_tables, num_splits, dc));
     TRY(check_tensor(context_lens, "context_lens", 1));
     TRY(check_tensor(out, "out", 3));
@@ -424,7 +447,7 @@ int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tens
                         pl.workspace_bytes);
         if (!aligned(workspace, 16)) return fail(PKV_ERR_LAYOUT, "workspace must be 16-byte aligned");
     }
-    pkv::DecodeParams p = dc.p;
+    pkv::DecodeParams &p = dc.p;
     p.context_lens = static_cast<const int32_t *>(context_lens->data);
     p.cl_stride = context_lens->stride[0];
     p.out = static_cast<char *>(out->data);
@@ -433,17 +456,57 @@ int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tens
     p.out_vec_ok = aligned(out->data, 16) && (p.o_b % 16) == 0 && (p.o_h % 16) == 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.err_flag = err_flag;
-    if (pl.kernel == 1)
-        return launch_status(pkv::launch_decode_fast(p, pl.fast, dc.ci.kind, workspace, workspace_bytes,
+    if (pl.kernel != 1) {
+        p.num_splits = pl.num_splits;
+        p.chunk_tokens = pl.chunk_tokens;
+        if (pl.num_splits > 1) {
+            p.part_acc = static_cast<float *>(workspace);
+            p.part_ml = p.part_acc + size_t(dc.batch) * dc.num_heads * pl.num_splits * dc.ci.head_dim;
+        }
+    }
+    return PKV_OK;
+}
+
+static int launch_paged_decode(const DecodeCheck &dc, int q_dtype, void *workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    if (dc.plan.kernel == 1)
+        return launch_status(pkv::launch_decode_fast(dc.p, dc.plan.fast, dc.ci.kind, workspace, workspace_bytes,
                                                      as_stream(stream)),
                              "paged_decode kernels");
-    p.num_splits = pl.num_splits;
-    p.chunk_tokens = pl.chunk_tokens;
-    if (pl.num_splits > 1) {
-        p.part_acc = static_cast<float *>(workspace);
-        p.part_ml = p.part_acc + size_t(dc.batch) * dc.num_heads * pl.num_splits * dc.ci.head_dim;
-    }
-    return launch_status(pkv::launch_decode(p, dc.ci.kind, q->dtype, as_stream(stream)), "paged_decode kernels");
+    return launch_status(pkv::launch_decode(dc.p, dc.ci.kind, q_dtype, as_stream(stream)), "paged_decode kernels");
+}
+
+int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
+                     const pkv_tensor *context_lens, float sm_scale, const pkv_tensor *out, int num_splits,
+                     void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream)
+{
+    DecodeCheck dc{};
+    TRY(prep_paged_decode(q, cache, block_tables, context_lens, sm_scale, out, num_splits, workspace,
+                          workspace_bytes, err_flag, dc));
+    return launch_paged_decode(dc, q->dtype, workspace, workspace_bytes, stream);
+}
+
+int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *req,
+                    const pkv_tensor *pos, const pkv_tensor *slot_mapping, const pkv_tensor *q,
+                    const pkv_cache *cache, const pkv_tensor *block_tables, const pkv_tensor *context_lens,
+                    float sm_scale, const pkv_tensor *out, int num_splits, void *workspace,
+                    size_t workspace_bytes, int32_t *err_flag, void *stream)
+{
+    CacheInfo ci{};
+    TRY(check_cache(cache, ci));
+    pkv::SlotMapParams sp;
+    TRY(prep_slot_mapping(block_tables, req, pos, int(ci.block_size), slot_mapping, err_flag, sp));
+    pkv::AppendParams ap;
+    int kind = 0;
+    bool vec16 = false;
+    TRY(prep_kv_append(k_new, v_new, slot_mapping, cache, err_flag, ap, kind, vec16));
+    DecodeCheck dc{};
+    TRY(prep_paged_decode(q, cache, block_tables, context_lens, sm_scale, out, num_splits, workspace,
+                          workspace_bytes, err_flag, dc));
+    TRY(launch_status(pkv::launch_slot_mapping(sp, as_stream(stream)), "slot_mapping kernel"));
+    TRY(launch_status(pkv::launch_append(ap, kind, vec16, as_stream(stream)), "kv_append kernel"));
+    return launch_paged_decode(dc, q->dtype, workspace, workspace_bytes, stream);
 }
 
 int pkv_pack3(const uint8_t *values, uint8_t *packed, int64_t n_octets, void *stream)

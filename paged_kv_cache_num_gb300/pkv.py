@@ -75,14 +75,16 @@ def lib():
                                            ctypes.c_size_t, P, P]
             L.pkv_paged_decode_noalloc.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP,
                                                    ctypes.c_int, P, P]
+            L.pkv_decode_step.argtypes = [TP, TP, TP, TP, TP, TP, CP, TP, TP, ctypes.c_float, TP,
+                                          ctypes.c_int, P, ctypes.c_size_t, P, P]
             L.pkv_noalloc_scratch_bytes.restype = ctypes.c_size_t
             L.pkv_pack3.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_unpack3.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_unpack3_words.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_copy_peak.argtypes = [P, P, ctypes.c_size_t, P]
             for fn in ("pkv_slot_mapping", "pkv_kv_append", "pkv_paged_decode_workspace",
-                       "pkv_paged_decode", "pkv_paged_decode_noalloc", "pkv_pack3", "pkv_unpack3", "pkv_unpack3_words",
-                       "pkv_copy_peak"):
+                       "pkv_paged_decode", "pkv_paged_decode_noalloc", "pkv_decode_step", "pkv_pack3",
+                       "pkv_unpack3", "pkv_unpack3_words", "pkv_copy_peak"):
                 getattr(L, fn).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -278,6 +280,35 @@ def paged_decode(q, cache: KVCache, block_tables, context_lens, sm_scale: Option
                                   ctypes.byref(_desc(context_lens)), float(sm_scale),
                                   ctypes.byref(_desc(out)), int(num_splits), ws_ptr, ws_n,
                                   _ptr(err_flag), _stream(stream)))
+    return out
+
+
+def decode_step(k_new, v_new, req, pos, q, cache: KVCache, block_tables, context_lens,
+                sm_scale: Optional[float] = None, out=None, slots=None, num_splits: int = 0,
+                workspace=None, err_flag=None, stream=None):
+    """slot_mapping + kv_append + paged_decode in one library call (see
+    pkv_decode_step in pkv.h); returns out.  `slots` (int64 [num_tokens])
+    receives the slot mapping."""
+    _need_cuda(k_new, v_new, req, pos, q, block_tables, context_lens, *cache.tensors())
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+    if out is None:
+        out = torch.empty_like(q)
+    if slots is None:
+        slots = torch.empty(req.shape[0], dtype=torch.int64, device=q.device)
+    cs = cache._struct()
+    if workspace is None:
+        need = decode_workspace_bytes(q, cache, block_tables, num_splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
+    ws_n = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step(ctypes.byref(_desc(k_new)), ctypes.byref(_desc(v_new)),
+                                 ctypes.byref(_desc(req)), ctypes.byref(_desc(pos)),
+                                 ctypes.byref(_desc(slots)), ctypes.byref(_desc(q)), ctypes.byref(cs),
+                                 ctypes.byref(_desc(block_tables)), ctypes.byref(_desc(context_lens)),
+                                 float(sm_scale), ctypes.byref(_desc(out)), int(num_splits), ws_ptr,
+                                 ws_n, _ptr(err_flag), _stream(stream)))
     return out
 
 

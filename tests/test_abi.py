@@ -27,7 +27,8 @@ def _declared_functions():
 def test_header_declares_expected_calls():
     names = _declared_functions()
     for n in ("pkv_kv_append", "pkv_paged_decode", "pkv_paged_decode_workspace", "pkv_pack3",
-              "pkv_unpack3", "pkv_unpack3_words", "pkv_slot_mapping", "pkv_last_error"):
+              "pkv_unpack3", "pkv_unpack3_words", "pkv_slot_mapping", "pkv_last_error",
+              "pkv_decode_step", "pkv_paged_decode_noalloc"):
         assert n in names
 
 
@@ -139,3 +140,31 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkv, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         pkv.lib()
+
+
+def test_decode_step_validates_everything_before_launching(lib):
+    """pkv_decode_step rejects a bad argument of any of its three parts (here
+    with fake device pointers: a launch would fault, so none may happen)."""
+    from paged_kv_cache_num_gb300 import pkv
+    B, Hq, H, D, T = 2, 4, 2, 64, 2
+    by = ctypes.byref
+    c = _cache(pkv.F16, H=H, D=D)
+    kn = _fake((T, H, D), pkv.F16)
+    req, pos = _fake((T,), pkv.I32), _fake((T,), pkv.I32)
+    sm = _fake((T,), pkv.I64)
+    q, out = _fake((B, Hq, D), pkv.F16), _fake((B, Hq, D), pkv.F16)
+    bt, cl = _fake((B, 5), pkv.I32), _fake((B,), pkv.I32)
+
+    def step(**kw):
+        a = dict(k=kn, v=kn, req=req, pos=pos, sm=sm, q=q, bt=bt, cl=cl, out=out)
+        a.update(kw)
+        return lib.pkv_decode_step(by(a["k"]), by(a["v"]), by(a["req"]), by(a["pos"]), by(a["sm"]),
+                                   by(a["q"]), by(c), by(a["bt"]), by(a["cl"]), ctypes.c_float(0.125),
+                                   by(a["out"]), 0, None, 0, None, None)
+    # slot-mapping part: wrong slot dtype; append part: slot count != tokens;
+    # decode part: out dtype, context_lens length
+    assert step(sm=_fake((T,), pkv.I32)) == -2
+    assert step(req=_fake((T + 1,), pkv.I32), pos=_fake((T + 1,), pkv.I32),
+                sm=_fake((T + 1,), pkv.I64)) == -3
+    assert step(out=_fake((B, Hq, D), pkv.BF16)) == -2
+    assert step(cl=_fake((B + 1,), pkv.I32)) == -3

@@ -292,3 +292,28 @@ def test_full_u3_mha_sampled(pkv, orc):
     pairs = _sample_pairs(w, seqs)
     ref = PL.oracle_decode(w, orc, oc, pairs=pairs)
     _check(w, out, ref, pairs)
+
+
+@pytest.mark.parametrize("maker", ["gqa", "u3"])
+def test_decode_step_equals_separate_calls(pkv, orc, maker):
+    """pkv_decode_step (slot mapping + append + decode in one call) gives the
+    same slots, cache bytes and output as the three calls."""
+    if maker == "gqa":
+        w = W.gqa_bf16(batch=6, ctx_lo=10, ctx_hi=400, seed=92)
+    else:
+        w = W.u3_mha(batch=5, ctx_lo=3, ctx_hi=500, num_heads=8, seed=93)
+    cache, out_sep = PL.gpu_run(w, pkv)               # fill, append, decode: three calls
+    before = PL.gpu_cache_host(cache)
+    dev = "cuda"
+    bt, req, pos = w.block_tables.to(dev), w.new_req.to(dev), w.new_pos.to(dev)
+    slots_sep = pkv.slot_mapping(bt, req, pos, w.block_size)
+    slots = torch.full_like(slots_sep, -7)
+    out = pkv.decode_step(w.k_new.to(dev), w.v_new.to(dev), req, pos, w.q.to(dev), cache, bt,
+                          w.context_lens.to(dev), sm_scale=w.sm_scale, slots=slots)
+    torch.cuda.synchronize()
+    assert torch.equal(slots, slots_sep)
+    after = PL.gpu_cache_host(cache)
+    for k in before:                                  # re-appending the same rows changes nothing
+        assert np.array_equal(before[k], after[k]), k
+    assert torch.equal(out, out_sep)
+    _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
