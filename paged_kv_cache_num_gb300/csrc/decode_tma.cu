@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include "pkv_device.cuh"
@@ -573,6 +574,162 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
     };
 
+    // 3-bit blocks: NB (1, or 2 for 16-token blocks) consecutive blocks of
+    // one sequence, held in stages s0 (and s1), as NB * KT tiles of 16
+    // tokens; `valid` counts the live tokens of all NB blocks (only the last
+    // block of a sequence can be partial).
+    auto u3_body = [&](auto nb_c, int s0, int s1, int valid) {
+        constexpr int NB = decltype(nb_c)::value;
+        constexpr int KTT = NB * T::KT;          // 16-token tiles of the NB blocks
+        const int kvh = hg * nh + warp;
+        const bool partial = valid < NB * BS;
+        // stage of tile t, and the tile's first row within its block
+        auto tile_stage = [&](int t) { return t < T::KT ? s0 : s1; };
+        auto tile_row = [&](int t) { return 16 * (t % T::KT); };
+        auto kpk = [&](int t) {                  // packed K rows of the tile (shared address)
+            return sbase + tile_stage(t) * L.stage_bytes + warp * BS * T::ROW + tile_row(t) * T::ROW;
+        };
+        // ---- metadata of this lane's score rows (tokens gid, gid+8 of
+        // each tile), staged with the block: [nh][BS] runs (head-major)
+        // or [BS][num_kv_heads] arrays
+        const int MH = f.meta_heads;
+        const bool hmaj = MH == nh;
+        const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? warp * BS : kvh;
+        float sk[KTT][2], zk[KTT][2], sv[KTT][2], zv[KTT][2];
+#pragma unroll
+        for (int mt = 0; mt < KTT; ++mt) {
+            const unsigned char *meta = smem + (tile_stage(mt) * L.stage_bytes + 2 * L.tile_bytes);
+            const __half *mks = reinterpret_cast<const __half *>(meta);
+            const __half *mvs = mks + BS * MH;
+            const uint8_t *mkz = meta + 4 * BS * MH;
+            const uint8_t *mvz = mkz + BS * MH;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int e = (tile_row(mt) + gid + 8 * r) * m_tok + m_h;
+                sk[mt][r] = __half2float(mks[e]);
+                sv[mt][r] = __half2float(mvs[e]);
+                zk[mt][r] = float(mkz[e]);
+                zv[mt][r] = float(mvz[e]);
+            }
+        }
+        // ---- S^T = K Q'^T with K converted straight into A fragments:
+        // lane (gid, tig) takes group tig of token rows gid and gid+8
+        float sc[KTT][4];
+#pragma unroll
+        for (int mt = 0; mt < KTT; ++mt) {
+            float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
+            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
+            const uint32_t a0 = kpk(mt) + gid * T::ROW + 12 * tig;
+            const uint32_t a1 = a0 + 8 * T::ROW;
+            const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
+            const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
+#pragma unroll
+            for (int kk = 0; kk < T::QK; ++kk) {
+                uint32_t a[4];
+                a[0] = u3k_pair(2 * kk, x0, x1, x2);
+                a[1] = u3k_pair(2 * kk, y0, y1, y2);
+                a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
+                a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
+                ptx::mma16816<false>((kk & 1) ? sx : sc[mt], a, qb[kk][0], qb[kk][1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][e] += sx[e];
+        }
+        // ---- scores: remove the zero point, apply the per-token
+        // scale, mask; online softmax per head column
+        float mx[2] = {NEG_INF, NEG_INF};
+#pragma unroll
+        for (int t = 0; t < KTT; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = e >> 1, c = e & 1;
+                if (c >= NC) continue;
+                float v = mult * sk[t][r] * (sc[t][e] - zk[t][r] * q1h[c]);
+                if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
+                sc[t][e] = v;
+                mx[c] = fmaxf(mx[c], v);
+            }
+        float alpha[2] = {1.0f, 1.0f};
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+            const float mn = fmaxf(m[c], mx[c]);
+            alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
+            m[c] = mn;
+            l[c] *= alpha[c];
+            zs[c] *= alpha[c];
+        }
+        // P' = p * v_scale (0 for masked tokens) as the B operand of PV
+        uint32_t pbf[KTT][2];
+#pragma unroll
+        for (int t = 0; t < KTT; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
+                const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
+                const float p1 = NC > 1 ? exp2_approx(sc[t][2 * r + 1] - m[1]) : 0.0f;
+                l[0] += p0;
+                if (NC > 1) l[1] += p1;
+                float q0, q1;
+                const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
+                zs[0] += q0 * zv[t][r];
+                if (NC > 1) zs[1] += q1 * zv[t][r];
+                pbf[t][r] = ptx::movmatrix_trans(w);
+            }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+            for (int t = 0; t < T::DT / 2; ++t) {
+                o[t][0] *= alpha[0];
+                o[t][2] *= alpha[0];
+                if (NC > 1) {
+                    o[t][1] *= alpha[1];
+                    o[t][3] *= alpha[1];
+                }
+            }
+        }
+        // ---- O^T += V'^T P'^T with V converted straight into A
+        // fragments: lane (gid, tig) owns codes 16gid .. 16gid+15 (row
+        // bytes 6gid .. 6gid+5) of tokens 2tig, 2tig+1 (k = 2tig, 2tig+1)
+        // and 2tig+8, 2tig+9; tile md holds codes 2md (row gid) and
+        // 2md+1 (row gid+8) of the slices.  X / Y are slice bytes 0-3 / 2-5.
+        const int sxy = 16 * (gid & 1);
+#pragma unroll
+        for (int kt = 0; kt < KTT; ++kt) {
+            const uint32_t vlane = kpk(kt) + L.tile_bytes + ((6 * gid) & ~3);   // packed V rows
+            uint32_t X[4], Y[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tok = 2 * tig + (i & 1) + 8 * (i >> 1);
+                const uint32_t w0 = ld_shared_u32(vlane + tok * T::ROW);
+                const uint32_t w1 = ld_shared_u32(vlane + tok * T::ROW + 4);
+                X[i] = __funnelshift_r(w0, w1, sxy);
+                Y[i] = __funnelshift_rc(w0, w1, sxy + 16);
+            }
+            uint32_t win[2][6];
+#pragma unroll
+            for (int tp = 0; tp < 2; ++tp) {
+                win[tp][0] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x5410u);
+                win[tp][1] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x6521u);
+                win[tp][2] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x7632u);
+                win[tp][3] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x6521u);
+                win[tp][4] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7632u);
+                win[tp][5] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7733u);
+            }
+#pragma unroll
+            for (int md = 0; md < T::DT / 2; ++md) {
+                constexpr uint32_t kMask3 = 0x00070007u;
+                uint32_t a[4];
+                a[0] = win[0][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
+                a[1] = win[0][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
+                a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
+                a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
+                ptx::mma16816<false>(o[md], a, pbf[kt][0], pbf[kt][1]);
+            }
+        }
+    };
+
     start_segment();
     int cs = 0;                  // stage of the current block
     uint32_t cphase = 0;         // parity of its fill round
@@ -738,149 +895,34 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             }
         }
         if constexpr (T::kIsU3) {
-            if (spb >= 0) {
-                const int kvh = hg * nh + warp;
-                const uint32_t kpk = sbase + s * L.stage_bytes + warp * BS * T::ROW;   // packed K rows
-                const uint32_t vpk = kpk + L.tile_bytes;                                 // packed V rows
-                const bool partial = valid < BS;
-                // ---- metadata of this lane's score rows (tokens gid, gid+8 of
-                // each tile), staged with the block: [nh][BS] runs (head-major)
-                // or [BS][num_kv_heads] arrays
-                const int MH = f.meta_heads;
-                const bool hmaj = MH == nh;
-                const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? warp * BS : kvh;
-                const unsigned char *meta = smem + (s * L.stage_bytes + 2 * L.tile_bytes);
-                const __half *mks = reinterpret_cast<const __half *>(meta);
-                const __half *mvs = mks + BS * MH;
-                const uint8_t *mkz = meta + 4 * BS * MH;
-                const uint8_t *mvz = mkz + BS * MH;
-                float sk[T::KT][2], zk[T::KT][2], sv[T::KT][2], zv[T::KT][2];
-#pragma unroll
-                for (int mt = 0; mt < T::KT; ++mt)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int e = (16 * mt + gid + 8 * r) * m_tok + m_h;
-                        sk[mt][r] = __half2float(mks[e]);
-                        sv[mt][r] = __half2float(mvs[e]);
-                        zk[mt][r] = float(mkz[e]);
-                        zv[mt][r] = float(mvz[e]);
-                    }
-                // ---- S^T = K Q'^T with K converted straight into A fragments:
-                // lane (gid, tig) takes group tig of token rows gid and gid+8
-                float sc[T::KT][4];
-#pragma unroll
-                for (int mt = 0; mt < T::KT; ++mt) {
-                    float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
-                    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
-                    const uint32_t a0 = kpk + (16 * mt + gid) * T::ROW + 12 * tig;
-                    const uint32_t a1 = a0 + 8 * T::ROW;
-                    const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
-                    const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
-#pragma unroll
-                    for (int kk = 0; kk < T::QK; ++kk) {
-                        uint32_t a[4];
-                        a[0] = u3k_pair(2 * kk, x0, x1, x2);
-                        a[1] = u3k_pair(2 * kk, y0, y1, y2);
-                        a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
-                        a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
-                        ptx::mma16816<false>((kk & 1) ? sx : sc[mt], a, qb[kk][0], qb[kk][1]);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[mt][e] += sx[e];
+            // 16-token blocks go two at a time when the next unit continues
+            // the sequence: the per-block softmax, barrier and walk work is
+            // then shared by 32 tokens
+            const bool pair = BS == 16 && x + 1 < hi && j + 1 < nblk[b];
+            if (pair) {
+                const int s1 = cs;
+                if (!ptx::mbar_wait_bounded(bar_full + 8 * s1, cphase, kTimeoutNs)) {
+                    raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
+                    return;
                 }
-                // ---- scores: remove the zero point, apply the per-token
-                // scale, mask; online softmax per head column
-                float mx[2] = {NEG_INF, NEG_INF};
-#pragma unroll
-                for (int t = 0; t < T::KT; ++t)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = e >> 1, c = e & 1;
-                        if (c >= NC) continue;
-                        float v = mult * sk[t][r] * (sc[t][e] - zk[t][r] * q1h[c]);
-                        if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
-                        sc[t][e] = v;
-                        mx[c] = fmaxf(mx[c], v);
-                    }
-                float alpha[2] = {1.0f, 1.0f};
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-                    const float mn = fmaxf(m[c], mx[c]);
-                    alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
-                    m[c] = mn;
-                    l[c] *= alpha[c];
-                    zs[c] *= alpha[c];
+                if (++cs == stages) {
+                    cs = 0;
+                    cphase ^= 1u;
                 }
-                // P' = p * v_scale (0 for masked tokens) as the B operand of PV
-                uint32_t pbf[T::KT][2];
-#pragma unroll
-                for (int t = 0; t < T::KT; ++t)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
-                        const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
-                        const float p1 = NC > 1 ? exp2_approx(sc[t][2 * r + 1] - m[1]) : 0.0f;
-                        l[0] += p0;
-                        if (NC > 1) l[1] += p1;
-                        float q0, q1;
-                        const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
-                        zs[0] += q0 * zv[t][r];
-                        if (NC > 1) zs[1] += q1 * zv[t][r];
-                        pbf[t][r] = ptx::movmatrix_trans(w);
-                    }
-                if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-                    for (int t = 0; t < T::DT / 2; ++t) {
-                        o[t][0] *= alpha[0];
-                        o[t][2] *= alpha[0];
-                        if (NC > 1) {
-                            o[t][1] *= alpha[1];
-                            o[t][3] *= alpha[1];
-                        }
-                    }
+                const int spb1 = stage_pb[s1];
+                const int valid1 = min(BS, ctx_b - (j + 1) * BS);
+                if (spb >= 0 && spb1 >= 0) {
+                    u3_body(std::integral_constant<int, 2>{}, s, s1, BS + valid1);
+                } else {
+                    if (spb >= 0) u3_body(std::integral_constant<int, 1>{}, s, s, valid);
+                    if (spb1 >= 0) u3_body(std::integral_constant<int, 1>{}, s1, s1, valid1);
                 }
-                // ---- O^T += V'^T P'^T with V converted straight into A
-                // fragments: lane (gid, tig) owns codes 16gid .. 16gid+15 (row
-                // bytes 6gid .. 6gid+5) of tokens 2tig, 2tig+1 (k = 2tig, 2tig+1)
-                // and 2tig+8, 2tig+9; tile md holds codes 2md (row gid) and
-                // 2md+1 (row gid+8) of the slices.  X / Y are slice bytes 0-3 / 2-5.
-                const uint32_t vlane = vpk + ((6 * gid) & ~3);
-                const int sxy = 16 * (gid & 1);
-#pragma unroll
-                for (int kt = 0; kt < T::KT; ++kt) {
-                    uint32_t X[4], Y[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int tok = 16 * kt + 2 * tig + (i & 1) + 8 * (i >> 1);
-                        const uint32_t w0 = ld_shared_u32(vlane + tok * T::ROW);
-                        const uint32_t w1 = ld_shared_u32(vlane + tok * T::ROW + 4);
-                        X[i] = __funnelshift_r(w0, w1, sxy);
-                        Y[i] = __funnelshift_rc(w0, w1, sxy + 16);
-                    }
-                    uint32_t win[2][6];
-#pragma unroll
-                    for (int tp = 0; tp < 2; ++tp) {
-                        win[tp][0] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x5410u);
-                        win[tp][1] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x6521u);
-                        win[tp][2] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x7632u);
-                        win[tp][3] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x6521u);
-                        win[tp][4] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7632u);
-                        win[tp][5] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7733u);
-                    }
-#pragma unroll
-                    for (int md = 0; md < T::DT / 2; ++md) {
-                        constexpr uint32_t kMask3 = 0x00070007u;
-                        uint32_t a[4];
-                        a[0] = win[0][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
-                        a[1] = win[0][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
-                        a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
-                        a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
-                        ptx::mma16816<false>(o[md], a, pbf[kt][0], pbf[kt][1]);
-                    }
-                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s1);
+                ++j;             // the pair's first block is never its sequence's last
+                ++x;
+            } else if (spb >= 0) {
+                u3_body(std::integral_constant<int, 1>{}, s, s, valid);
             }
         }
         __syncwarp();

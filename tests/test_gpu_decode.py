@@ -317,3 +317,25 @@ def test_decode_step_equals_separate_calls(pkv, orc, maker):
         assert np.array_equal(before[k], after[k]), k
     assert torch.equal(out, out_sep)
     _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
+
+
+def test_u3_bad_block_ids_in_pairs(pkv, orc):
+    """3-bit cache with 16-token blocks (which the persistent kernel takes two
+    at a time): block ids out of range at an even and at an odd position of a
+    sequence are skipped and flagged; the untouched sequences still match the
+    oracle, and the broken ones match the general kernel, which leaves out the
+    same blocks."""
+    w = W.u3_mha(batch=4, ctx_lo=100, ctx_hi=200, num_heads=8, seed=95)
+    w.block_tables[1, 2] = w.num_blocks + 5
+    w.block_tables[2, 5] = -1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, fast = PL.gpu_run(w, pkv, err_flag=err)
+    assert int(err.item()) & pkv.pkv.DEVERR_BLOCK_RANGE
+    _, general = PL.gpu_run(w, pkv, num_splits=1)
+    a, g = PL.out_f64(fast), PL.out_f64(general)
+    assert np.isfinite(a).all()
+    assert np.max(np.abs(a[1:3] - g[1:3])) <= PL.tolerance(w)
+    seqs = [0, 3]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    pairs = _sample_pairs(w, seqs)
+    _check(w, fast, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
