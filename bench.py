@@ -207,6 +207,8 @@ def make_workload(name, device, rank=0):
         return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
         return W.mixed_append(device=device, seed=seed)
+    if name == "mha_short":
+        return W.mha_short(device=device, seed=seed)
     if name == "tiny_fp16":
         return W.tiny(device=device)
     raise ValueError(name)
@@ -494,7 +496,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_bf16")
-    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append",
+    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)

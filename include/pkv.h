@@ -175,6 +175,13 @@ int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req,
  *                q_d = clamp(rint(x_d / s) + z, 0, 7), packed along head_dim;
  *                s == 0 stores z = 0 and all q = 0.  head_dim % 8 == 0.
  *                Rows must be finite.
+ *   block_size may be any positive number here (decode needs a power of two
+ *   <= 256): a contiguous per-request cache [batch, num_kv_heads,
+ *   max_seq_len, D] ("Write Triton Kv Cache Append Kernel", inputs item 1,
+ *   the contiguous layout with slot = req * max_seq_len + pos) is passed as
+ *   the view [batch, max_seq_len, num_kv_heads, D] with strides
+ *   (num_kv_heads * max_seq_len * D, D, max_seq_len * D, 1), i.e. one block
+ *   of max_seq_len slots per request.
  *   The grid depends only on num_tokens and num_kv_heads (graph safe).  A
  *   slot >= num_blocks * block_size is skipped and raises
  *   PKV_DEVERR_SLOT_RANGE.  Two tokens with the same slot race (undefined

@@ -33,8 +33,13 @@ __device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, i
         raise_err(p.err_flag, PKV_DEVERR_SLOT_RANGE);
         return false;
     }
-    blk = slot >> p.block_shift;
-    off = slot & ((int64_t(1) << p.block_shift) - 1);
+    if (p.block_shift >= 0) {
+        blk = slot >> p.block_shift;
+        off = slot & ((int64_t(1) << p.block_shift) - 1);
+    } else {                                    // e.g. one block per request of max_seq_len
+        blk = slot / p.block_size;
+        off = slot - blk * p.block_size;
+    }
     return true;
 }
 

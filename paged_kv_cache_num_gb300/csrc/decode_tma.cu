@@ -65,7 +65,13 @@ __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes,
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
     L.meta_bytes = meta_bytes;
-    L.stage_bytes = 2 * L.tile_bytes + meta_bytes;
+    // TMA writes each tile at a 1024-byte (128B-swizzled tiles) or 128-byte
+    // (unswizzled 3-bit tiles) aligned shared address, so stages are rounded
+    // up to 1024 bytes, or 128 when the stage holds 3-bit metadata.  (Tiles
+    // are multiples of 768 bytes (3-bit) or 2048 bytes (others) at block 16+,
+    // so only the 3-bit metadata can leave a stage unaligned.)
+    const int align = meta_bytes > 0 ? 128 : 1024;
+    L.stage_bytes = (2 * L.tile_bytes + meta_bytes + align - 1) / align * align;
     L.bars_off = stages * L.stage_bytes;
     L.ok_off = L.bars_off + 2 * stages * 8;
     L.prefix_off = L.ok_off + stages * 4;
@@ -325,7 +331,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         const uint32_t vdst = kdst + L.tile_bytes;
                         stage_pb[s] = pbk;
                         if (pbk >= 0) {
-                            ptx::mbar_arrive_expect_tx(fb, uint32_t(L.stage_bytes));
+                            ptx::mbar_arrive_expect_tx(fb, uint32_t(2 * L.tile_bytes + L.meta_bytes));
 #pragma unroll
                             for (int h = 0; h < T::HALVES; ++h) {
                                 const int half_bytes = L.tile_bytes / T::HALVES;

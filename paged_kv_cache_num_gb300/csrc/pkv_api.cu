@@ -79,7 +79,10 @@ struct CacheInfo {
 };
 
 // Validate a pkv_cache; head_dim comes from the row length and the dtype.
-int check_cache(const pkv_cache *c, CacheInfo &ci)
+// `any_block_size`: the append takes any block size (e.g. a contiguous
+// [batch, kv_heads, max_seq_len, D] cache seen as one block per request);
+// decode needs a power of two <= 256.
+int check_cache(const pkv_cache *c, CacheInfo &ci, bool any_block_size = false)
 {
     if (!c) return fail(PKV_ERR_NULL, "cache: descriptor is NULL");
     TRY(check_tensor(&c->k_cache, "k_cache", 4));
@@ -109,7 +112,7 @@ int check_cache(const pkv_cache *c, CacheInfo &ci)
     ci.head_dim = kind == PKV_DTYPE_U3 ? k.shape[3] * 8 / 3 : k.shape[3];
     if (kind == PKV_DTYPE_U3 && k.shape[3] * 8 != ci.head_dim * 3)
         return fail(PKV_ERR_SHAPE, "U3 cache row of %lld bytes is not 3*head_dim/8", (long long)k.shape[3]);
-    if (!is_pow2(ci.block_size) || ci.block_size > 256)
+    if (any_block_size ? ci.block_size < 1 : (!is_pow2(ci.block_size) || ci.block_size > 256))
         return fail(PKV_ERR_UNSUPPORTED, "block_size %lld must be a power of two <= 256",
                     (long long)ci.block_size);
     if (ci.num_blocks * ci.block_size > (int64_t(1) << 31))
@@ -222,7 +225,7 @@ static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, cons
     TRY(check_tensor(v_new, "v_new", 3));
     TRY(check_tensor(slot_mapping, "slot_mapping", 1));
     CacheInfo ci{};
-    TRY(check_cache(cache, ci));
+    TRY(check_cache(cache, ci, true));
     if (k_new->dtype != v_new->dtype) return fail(PKV_ERR_DTYPE, "k_new and v_new dtypes differ");
     const int src = k_new->dtype;
     if (src != PKV_DTYPE_F16 && src != PKV_DTYPE_BF16) return fail(PKV_ERR_DTYPE, "k_new must be F16 or BF16");
@@ -279,7 +282,8 @@ static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, cons
     p.num_tokens = T;
     p.num_kv_heads = int(ci.num_kv_heads);
     p.head_dim = int(ci.head_dim);
-    p.block_shift = log2i(ci.block_size);
+    p.block_shift = is_pow2(ci.block_size) ? log2i(ci.block_size) : -1;
+    p.block_size = ci.block_size;
     p.num_slots = ci.num_blocks * ci.block_size;
     p.src_kind = src;
     p.err_flag = err_flag;

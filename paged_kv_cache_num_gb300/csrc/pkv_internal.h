@@ -35,7 +35,8 @@ struct AppendParams {
     int64_t num_tokens;
     int num_kv_heads;
     int head_dim;
-    int block_shift;            // log2(block_size)
+    int block_shift;            // log2(block_size), or -1 when not a power of two
+    int64_t block_size;
     int64_t num_slots;          // num_blocks * block_size
     int src_kind;               // kF16 / kBF16
     int32_t *err_flag;

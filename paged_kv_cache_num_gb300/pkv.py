@@ -180,20 +180,15 @@ class KVCache:
             # num_kv_heads] view: a decode CTA then stages only its own heads'
             # runs of each block
             meta = (num_blocks, num_kv_heads, block_size)
-
-            def mk(dt):
-                return torch.empty(meta, dtype=dt, device=device).permute(0, 2, 1)
-
-            c = KVCache(kind, k, v, k_qscale=mk(torch.float16), k_qzero=mk(torch.uint8),
-                        v_qscale=mk(torch.float16), v_qzero=mk(torch.uint8))
+            phys = [torch.empty(meta, dtype=dt, device=device)
+                    for dt in (torch.float16, torch.uint8, torch.float16, torch.uint8)]
+            ks_, kz_, vs_, vz_ = (t.permute(0, 2, 1) for t in phys)
+            c = KVCache(kind, k, v, k_qscale=ks_, k_qzero=kz_, v_qscale=vs_, v_qzero=vz_)
         else:
             raise ValueError(kind)
         if fill is not None:
-            for t in (c.k_cache, c.v_cache, c.k_qscale, c.k_qzero, c.v_qscale, c.v_qzero):
-                if t is not None:
-                    if not t.is_contiguous():
-                        t = t.permute(0, 2, 1)
-                    t.view(torch.uint8).fill_(fill)
+            for t in [c.k_cache, c.v_cache] + (phys if kind == "u3" else []):
+                t.view(torch.uint8).fill_(fill)
         return c
 
     def _struct(self) -> _Cache:

@@ -84,11 +84,15 @@ def test_append_validation_errors(lib):
     # head count mismatch
     assert lib.pkv_kv_append(by(_fake((T, 3, D), pkv.F16)), by(_fake((T, 3, D), pkv.F16)),
                              by(sm), by(c), None, None) == -3
-    # block size not a power of two
+    # a block size that is not a power of two is fine for the append (a
+    # contiguous per-request cache) but not for decode; checked through the
+    # workspace query, which never launches (these pointers are fake)
     c2 = pkv._Cache()
     c2.k_cache = _fake((4, 12, H, D), pkv.F16)
     c2.v_cache = _fake((4, 12, H, D), pkv.F16)
-    assert lib.pkv_kv_append(by(kn), by(kn), by(sm), by(c2), None, None) == -5
+    q2, bt2 = _fake((2, H, D), pkv.F16), _fake((2, 4), pkv.I32)
+    n2 = ctypes.c_size_t(0)
+    assert lib.pkv_paged_decode_workspace(by(q2), by(c2), by(bt2), 0, by(n2)) == -5
     # e4m3 without scales
     c3 = _cache(pkv.E4M3)
     assert lib.pkv_kv_append(by(kn), by(kn), by(sm), by(c3), None, None) == -1

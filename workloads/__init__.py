@@ -32,6 +32,11 @@ Workloads (names used by the tests and the benchmark):
   u3_mha         batch 32, 32 heads (MHA), head_dim 128, block 16, fp16,
                  context U{1024..8192}; 3-bit packed cache filled by
                  appending N(0,1) rows, then 32 new tokens.
+  mha_short      the benchmark shape of "10. Triton KV Cache and
+                 PagedAttention": batch 32, 32 heads (MHA), head_dim 128,
+                 block 16, fp16, a 2048-block pool of N(0,1) K/V, context
+                 U{100..999}, blocks allocated one after another (sequence
+                 b's blocks follow sequence b-1's); 32 new tokens appended.
 
 Token lists are given as (request index, position) pairs; a position of -1
 marks a padding token.  The slot of a token is computed by the code under
@@ -46,7 +51,7 @@ from typing import Dict, Optional
 import torch
 
 SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44,
-         "fp8_long": 45, "u3_mha": 46}
+         "fp8_long": 45, "u3_mha": 46, "mha_short": 47}
 
 
 @dataclass
@@ -296,6 +301,35 @@ def u3_mha(device="cpu", batch=32, ctx_lo=1024, ctx_hi=8192, num_heads=32, head_
     w = Workload("u3_mha", dt, "u3", B, H, H, D, BS, P, ctx, bt, q, new_req, new_pos,
                  k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
                  v_fill=v_fill)
+    w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
+    return w
+
+
+def mha_short(device="cpu", batch=32, num_heads=32, head_dim=128, block_size=16, num_blocks=2048,
+              ctx_lo=100, ctx_hi=999, seed=None) -> Workload:
+    """MHA fp16 decode over a pool of random K/V with contiguously allocated
+    block tables (defaults: the page's benchmark shape)."""
+    g = _gen(SEEDS["mha_short"] if seed is None else seed, device)
+    dt = torch.float16
+    B, H, D, BS, P = batch, num_heads, head_dim, block_size, num_blocks
+    ctx = _randint(ctx_lo, ctx_hi, B, g, device).to(torch.int32)
+    nb = [_cdiv(int(c), BS) for c in ctx.tolist()]
+    if sum(nb) > P:
+        raise ValueError("pool of %d blocks holds fewer than the %d needed" % (P, sum(nb)))
+    MB = _cdiv(ctx_hi, BS)
+    bt = torch.zeros((B, MB), dtype=torch.int32, device=device)
+    off = 0
+    for b, n in enumerate(nb):
+        bt[b, :n] = torch.arange(off, off + n, dtype=torch.int32, device=device)
+        off += n
+    q = _randn((B, H, D), g, device, dt)
+    k0 = _randn((P, BS, H, D), g, device, dt)
+    v0 = _randn((P, BS, H, D), g, device, dt)
+    k_new = _randn((B, H, D), g, device, dt)
+    v_new = _randn((B, H, D), g, device, dt)
+    w = Workload("mha_short", dt, "f16", B, H, H, D, BS, P, ctx, bt, q,
+                 torch.arange(B, dtype=torch.int32, device=device), (ctx - 1).to(torch.int32),
+                 k_new, v_new, k_cache0=k0, v_cache0=v0)
     w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
     return w
 
