@@ -27,7 +27,7 @@ _lock = threading.Lock()
 _lib = None
 
 # dtype codes of the oracle's own interface
-F16, BF16, E4M3, U3 = 1, 2, 3, 4
+F16, BF16, E4M3, U3, E5M2 = 1, 2, 3, 4, 9
 
 
 def build(force: bool = False) -> str:
@@ -75,7 +75,8 @@ def _load():
         lib.pkvo_paged_decode.restype = i64
         lib.pkvo_max_threads.restype = i32
         for fn in ("pkvo_f32_to_e4m3_n", "pkvo_f32_to_f16_n", "pkvo_f16_to_f64_n",
-                   "pkvo_bf16_to_f64_n", "pkvo_e4m3_to_f64_n"):
+                   "pkvo_bf16_to_f64_n", "pkvo_e4m3_to_f64_n", "pkvo_f32_to_e5m2_n",
+                   "pkvo_e5m2_to_f64_n"):
             getattr(lib, fn).argtypes = [P, P, i64]
         _lib = lib
         return lib
@@ -121,6 +122,16 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
 def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
     """binary32 -> E4M3 code, RNE, saturating to +-448 (NaN -> 0x7F)."""
     return _conv("pkvo_f32_to_e4m3_n", x, np.float32, np.uint8)
+
+
+def e5m2_to_f64(codes: np.ndarray) -> np.ndarray:
+    """OCP E5M2 decode of each byte."""
+    return _conv("pkvo_e5m2_to_f64_n", codes, np.uint8, np.float64)
+
+
+def f32_to_e5m2(x: np.ndarray) -> np.ndarray:
+    """binary32 -> E5M2 code, RNE, saturating to +-57344 (NaN -> 0x7F)."""
+    return _conv("pkvo_f32_to_e5m2_n", x, np.float32, np.uint8)
 
 
 def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:

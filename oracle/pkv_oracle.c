@@ -30,6 +30,11 @@
  *   - e4m3 is the OCP "fn" variant (bias 7, max 448, no infinities,
  *     S.1111.111 = NaN); encoding rounds to nearest even and saturates finite
  *     overflow and infinities to +-448; every NaN encodes to 0x7F.
+ *   - e5m2 (the second fp8 cache format of "Write Triton Kv Cache Append
+ *     Kernel", inputs item 4) is the OCP E5M2 format (bias 15, 2 mantissa
+ *     bits, infinities and NaNs at exponent 31, max 57344); encoding rounds
+ *     to nearest even and saturates finite overflow and infinities to
+ *     +-57344, like e4m3; every NaN encodes to 0x7F.
  *   - 3-bit quantiser: s = fp16_rn((max-min)/7), z = clamp(rint(-min/s),0,7),
  *     q = clamp(rint(x/s)+z,0,7), all fp32; s == 0 gives z = 0, q = 0; an s
  *     that overflows fp16 saturates to 65504.  Element d of a head row sits at
@@ -54,6 +59,7 @@
 #define O_BF16 2
 #define O_E4M3 3
 #define O_U3 4
+#define O_E5M2 9
 
 /* ------------------------------------------------------------------------ */
 /* Scalar formats                                                           */
@@ -137,6 +143,50 @@ double pkvo_e4m3_to_f64(uint8_t c)
 }
 
 /* binary32 -> E4M3, round to nearest even, saturating to +-448. */
+/* OCP E5M2: S.EEEEE.MM, bias 15; E = 31 holds the infinities (M = 0) and
+ * NaNs; E = 0 the subnormals M/4 * 2^-14. */
+double pkvo_e5m2_to_f64(uint8_t c)
+{
+    int s = c >> 7, E = (c >> 2) & 0x1f, m = c & 3;
+    double v;
+    if (E == 31)
+        v = m ? NAN : INFINITY;
+    else if (E == 0)
+        v = ldexp((double)m, -16);
+    else
+        v = ldexp((double)(4 + m), E - 17);
+    return s ? -v : v;
+}
+
+/* Nearest even, finite overflow and infinities to +-57344 (S.11110.11), NaN
+ * to 0x7F: the value's binade sets the quantum (2^-16 in the subnormal
+ * range), the rounded multiple of it is re-encoded. */
+uint8_t pkvo_f32_to_e5m2(float f)
+{
+    uint8_t sign = signbit(f) ? 0x80 : 0;
+    if (isnan(f))
+        return 0x7f;
+    double a = fabs((double)f);
+    if (a >= 57344.0)
+        return sign | 0x7b;
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);
+    int ex = e - 1;                     /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -14)
+        ex = -14;
+    double quantum = ldexp(1.0, ex - 2);
+    double r = nearbyint(a / quantum) * quantum; /* a < 57344 => r <= 57344 */
+    if (r < ldexp(1.0, -14))
+        return sign | (uint8_t)(r / ldexp(1.0, -16));
+    int e2;
+    frexp(r, &e2);
+    int E = e2 - 1;
+    uint8_t mant = (uint8_t)(r / ldexp(1.0, E - 2) - 4.0);
+    return sign | (uint8_t)((E + 15) << 2) | mant;
+}
+
 uint8_t pkvo_f32_to_e4m3(float f)
 {
     uint8_t sign = signbit(f) ? 0x80 : 0;
@@ -335,15 +385,15 @@ int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int n
             if (cache_dtype == O_F16 || cache_dtype == O_BF16) {
                 memcpy((uint16_t *)k_cache + row * D, ks, (size_t)D * 2);
                 memcpy((uint16_t *)v_cache + row * D, vs, (size_t)D * 2);
-            } else if (cache_dtype == O_E4M3) {
+            } else if (cache_dtype == O_E4M3 || cache_dtype == O_E5M2) {
                 uint8_t *kd = (uint8_t *)k_cache + row * D;
                 uint8_t *vd = (uint8_t *)v_cache + row * D;
                 for (int d = 0; d < D; ++d) {
                     /* scale division in fp32, then the cast */
                     float xk = (float)elem16_to_f64(ks[d], src_dtype) / k_scale[h];
                     float xv = (float)elem16_to_f64(vs[d], src_dtype) / v_scale[h];
-                    kd[d] = pkvo_f32_to_e4m3(xk);
-                    vd[d] = pkvo_f32_to_e4m3(xv);
+                    kd[d] = cache_dtype == O_E4M3 ? pkvo_f32_to_e4m3(xk) : pkvo_f32_to_e5m2(xk);
+                    vd[d] = cache_dtype == O_E4M3 ? pkvo_f32_to_e4m3(xv) : pkvo_f32_to_e5m2(xv);
                 }
             } else { /* O_U3 */
                 int64_t rb = 3 * D / 8;
@@ -371,6 +421,8 @@ static double cache_elem(int cache_dtype, const void *cache, int64_t row, int D,
         return pkvo_bf16_to_f64(((const uint16_t *)cache)[row * D + d]);
     if (cache_dtype == O_E4M3)
         return pkvo_e4m3_to_f64(((const uint8_t *)cache)[row * D + d]) * scale_h;
+    if (cache_dtype == O_E5M2)
+        return pkvo_e5m2_to_f64(((const uint8_t *)cache)[row * D + d]) * scale_h;
     /* O_U3: bit 3d of the row's little-endian bit stream */
     const uint8_t *p = (const uint8_t *)cache + row * (int64_t)(3 * D / 8);
     uint8_t v[8];
@@ -508,4 +560,16 @@ void pkvo_e4m3_to_f64_n(const uint8_t *x, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = pkvo_e4m3_to_f64(x[i]);
+}
+
+void pkvo_f32_to_e5m2_n(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = pkvo_f32_to_e5m2(x[i]);
+}
+
+void pkvo_e5m2_to_f64_n(const uint8_t *x, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = pkvo_e5m2_to_f64(x[i]);
 }

@@ -58,6 +58,13 @@ def e4m3_dequant(codes: np.ndarray, scale_per_head: np.ndarray) -> np.ndarray:
     return (v * torch.from_numpy(scale_per_head.astype(np.float64))[:, None]).numpy()
 
 
+def e5m2_dequant(codes: np.ndarray, scale_per_head: np.ndarray) -> np.ndarray:
+    """[..., Hkv, D] e5m2 codes -> float64 values times the per-head scale
+    (torch's float8_e5m2 view as the decoder)."""
+    v = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e5m2).to(torch.float64)
+    return (v * torch.from_numpy(scale_per_head.astype(np.float64))[:, None]).numpy()
+
+
 def u3_dequant(packed: np.ndarray, qscale_bits: np.ndarray, qzero: np.ndarray, D: int):
     """[..., 3D/8] packed rows + fp16 scale bits + zero -> float64 (q-z)*s."""
     lead = packed.shape[:-1]

@@ -5,7 +5,7 @@ import numpy as np
 import torch
 
 import workloads as W
-from tests.refs import bitstream_unpack3, e4m3_dequant
+from tests.refs import bitstream_unpack3, e4m3_dequant, e5m2_dequant
 
 
 def _slots_closed_form(bt, req, pos, BS):
@@ -78,6 +78,36 @@ def test_scatter_out_of_range_slots_skipped(orc):
     kc, vc = W.bits16(k0).copy(), W.bits16(v0).copy()
     bad = orc.kv_append(orc.F16, orc.F16, W.bits16(kn), W.bits16(vn), slots, kc, vc)
     assert bad == 2
+
+
+def test_scatter_e5m2_matches_cast_and_step(orc):
+    """fp8 e5m2: codes equal torch's e5m2 cast of (x / scale) taken in fp32
+    (in range), out-of-range values saturate to +-57344, and the dequantised
+    cache is within half an e5m2 step of the source."""
+    P, BS, H, D, T, k0, v0, kn, vn, slots = _scatter_case(orc, torch.bfloat16, seed=3)
+    # head 2 of V gets a scale too small for its values: those saturate
+    kscale = np.array([1e-4, 2e-4, 3e-5], np.float32)
+    vscale = np.array([1.5e-4, 5e-5, 2e-5], np.float32)
+    kc = np.zeros((P, BS, H, D), np.uint8)
+    vc = np.zeros((P, BS, H, D), np.uint8)
+    orc.kv_append(orc.E5M2, orc.BF16, W.bits16(kn), W.bits16(vn), slots, kc, vc, kscale, vscale)
+    real = slots >= 0
+    for cache, src, sc in ((kc, kn, kscale), (vc, vn, vscale)):
+        x = src[torch.from_numpy(real)].float() / torch.from_numpy(sc)[None, :, None]
+        inr = (x.abs() < 57344).numpy()
+        ref = x.to(torch.float8_e5m2).view(torch.uint8).numpy()
+        got = cache.reshape(P * BS, H, D)[slots[real]]
+        assert np.array_equal(got[inr], ref[inr])
+        sat = np.where(x.numpy() > 0, 0x7B, 0xFB)
+        assert np.array_equal(got[~inr], sat[~inr])
+        inr_rows = inr.all(axis=(0, 2))
+        got, sc = got[:, inr_rows], sc[inr_rows]
+        deq = e5m2_dequant(got, sc)
+        xs = src[torch.from_numpy(real)].double().numpy()[:, inr_rows]
+        # half of the e5m2 spacing at each value: 2^(floor(log2|x/s|)-3) * s
+        mag = np.maximum(np.abs(xs) / sc[None, :, None], 2.0 ** -14)
+        half_step = 2.0 ** (np.floor(np.log2(mag)) - 3) * sc[None, :, None]
+        assert np.all(np.abs(deq - xs) <= half_step * (1 + 1e-6))
 
 
 def test_scatter_e4m3_matches_cast_and_step(orc):

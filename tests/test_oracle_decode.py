@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from tests.refs import e4m3_dequant, gather_attention, u3_dequant
+from tests.refs import e4m3_dequant, e5m2_dequant, gather_attention, u3_dequant
 
 
 def _decode16(orc, w, q=None, kc=None, vc=None, bt=None, ctx=None, pairs=None):
@@ -146,7 +146,7 @@ def _fill_quantised(orc, w, code):
     vn = np.concatenate([W.bits16(w.v_fill), W.bits16(w.v_new)])
     slots = orc.build_slot_mapping(w.block_tables.numpy(), req, pos, BS)
     c = {}
-    if code == orc.E4M3:
+    if code in (orc.E4M3, orc.E5M2):
         c["k"] = np.zeros((P, BS, H, D), np.uint8)
         c["v"] = np.zeros((P, BS, H, D), np.uint8)
         orc.kv_append(code, src_code, kn, vn, slots, c["k"], c["v"], w.k_scale.numpy(),
@@ -173,6 +173,20 @@ def test_fp8_decode_on_dequantised_cache(orc):
     assert bad == 0
     kd = e4m3_dequant(c["k"], w.k_scale.numpy())
     vd = e4m3_dequant(c["v"], w.v_scale.numpy())
+    ref = gather_attention(w.q, kd, vd, w.block_tables.numpy(), w.context_lens.numpy(),
+                           w.block_size, w.sm_scale)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def test_e5m2_decode_on_dequantised_cache(orc):
+    w = W.fp8_long(batch=3, ctx_lo=40, ctx_hi=150, calib_tokens=64, seed=16, fp8="e5m2")
+    c = _fill_quantised(orc, w, orc.E5M2)
+    out, bad = orc.paged_decode(orc.E5M2, orc.BF16, W.bits16(w.q), c["k"], c["v"],
+                                w.block_tables.numpy(), w.context_lens.numpy(), w.block_size,
+                                w.sm_scale, k_scale=w.k_scale.numpy(), v_scale=w.v_scale.numpy())
+    assert bad == 0
+    kd = e5m2_dequant(c["k"], w.k_scale.numpy())
+    vd = e5m2_dequant(c["v"], w.v_scale.numpy())
     ref = gather_attention(w.q, kd, vd, w.block_tables.numpy(), w.context_lens.numpy(),
                            w.block_size, w.sm_scale)
     assert np.max(np.abs(out - ref)) < 1e-12

@@ -92,3 +92,49 @@ def test_e4m3_ties_to_even(orc):
     # between 1.125 and 1.25 (0x3A): 1.1875 is a tie -> 1.25
     x = np.array([1.0625, 1.1875, 1.0625 + 2 ** -20, 2 ** -10, 3 * 2 ** -10], np.float32)
     assert orc.f32_to_e4m3(x).tolist() == [0x38, 0x3A, 0x39, 0x00, 0x02]
+
+
+# ---------------------------------------------------------------- OCP e5m2
+
+def test_e5m2_decode_table(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e5m2_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 6 and all(nan[c] for c in (0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF))
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # closed-form anchors: infinities, largest finite, one, smallest normal
+    # and subnormal
+    assert got[0x7C] == np.inf and got[0xFC] == -np.inf
+    assert got[0x7B] == 57344.0 and got[0xFB] == -57344.0
+    assert got[0x3C] == 1.0 and got[0x04] == 2.0 ** -14 and got[0x01] == 2.0 ** -16
+
+
+def test_e5m2_encode_matches_torch_in_range(orc):
+    x = _structured_f32_sample()
+    x = x[np.isfinite(x) & (np.abs(x) < 57344.0)]
+    got = orc.f32_to_e5m2(x)
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_e5m2_encode_saturates_and_nan(orc):
+    x = np.array([57344.0, 57344.5, 61440.0, 1e6, np.inf, -np.inf, -60000.0, np.nan, 0.0, -0.0],
+                 dtype=np.float32)
+    got = orc.f32_to_e5m2(x)
+    assert got.tolist() == [0x7B, 0x7B, 0x7B, 0x7B, 0x7B, 0xFB, 0xFB, 0x7F, 0x00, 0x80]
+
+
+def test_e5m2_roundtrip_codes(orc):
+    codes = np.array([c for c in range(256) if (c >> 2) & 0x1F != 31], dtype=np.uint8)
+    vals = orc.e5m2_to_f64(codes).astype(np.float32)
+    assert np.array_equal(orc.f32_to_e5m2(vals), codes)
+
+
+def test_e5m2_ties_to_even(orc):
+    # 1.125 lies half way between 1.0 (0x3C) and 1.25 (0x3D): even -> 1.0;
+    # 1.375 between 1.25 and 1.5 (0x3E): even -> 1.5; in the subnormal
+    # range 2^-17 ties to 0 and 3 * 2^-17 to 2 * 2^-16
+    x = np.array([1.125, 1.375, 1.125 + 2 ** -20, 2 ** -17, 3 * 2 ** -17], np.float32)
+    assert orc.f32_to_e5m2(x).tolist() == [0x3C, 0x3E, 0x3D, 0x00, 0x02]

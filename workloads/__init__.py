@@ -244,9 +244,11 @@ def _fill_lists(ctx_list, device):
 
 
 def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, num_kv_heads=8,
-             head_dim=128, block_size=32, calib_tokens=4096, seed=None) -> Workload:
-    """Long-context e4m3 cache with per-kv-head scales amax/448 (defaults:
-    the full-size case)."""
+             head_dim=128, block_size=32, calib_tokens=4096, seed=None,
+             fp8="e4m3") -> Workload:
+    """Long-context fp8 cache with per-kv-head scales amax / (the format's
+    largest finite value): 448 for e4m3 (defaults: the full-size case),
+    57344 for e5m2."""
     g = _gen(SEEDS["fp8_long"] if seed is None else seed, device)
     dt = torch.bfloat16
     B, Hq, Hkv, D, BS = batch, num_heads, num_kv_heads, head_dim, block_size
@@ -259,9 +261,10 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
     q = _randn((B, Hq, D), g, device, dt)
     k_cal = _randn((calib_tokens, Hkv, D), g, device, dt)
     v_cal = _randn((calib_tokens, Hkv, D), g, device, dt)
-    # calibration: per-kv-head amax / 448 in fp32
-    k_scale = k_cal.float().abs().amax(dim=(0, 2)) / 448.0
-    v_scale = v_cal.float().abs().amax(dim=(0, 2)) / 448.0
+    # calibration: per-kv-head amax / max-finite in fp32
+    fmax = {"e4m3": 448.0, "e5m2": 57344.0}[fp8]
+    k_scale = k_cal.float().abs().amax(dim=(0, 2)) / fmax
+    v_scale = v_cal.float().abs().amax(dim=(0, 2)) / fmax
     fill_req, fill_pos = _fill_lists(ctx_list, device)
     n_fill = int(fill_req.shape[0])
     k_fill = _randn((n_fill, Hkv, D), g, device, dt)
@@ -270,7 +273,7 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
     v_new = _randn((B, Hkv, D), g, device, dt)
     new_req = torch.arange(B, dtype=torch.int32, device=device)
     new_pos = (ctx - 1).to(torch.int32)
-    w = Workload("fp8_long", dt, "e4m3", B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
+    w = Workload("fp8_long", dt, fp8, B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
                  k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
                  v_fill=v_fill, k_scale=k_scale.contiguous(), v_scale=v_scale.contiguous())
     w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
