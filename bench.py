@@ -181,7 +181,7 @@ def algorithmic_bytes(w, decode=True, append=True):
     append: per real new token Hkv * (2 source rows + 2 cache rows + metadata)
             + its slot (8 B) and (request, position) (8 B)."""
     D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
-    row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "u3": 3 * D // 8}[w.cache_kind]
+    row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "u3": 3 * D // 8}[w.cache_kind]
     meta = 3 if w.cache_kind == "u3" else 0
     total = 0
     if decode and w.q is not None:
@@ -203,6 +203,8 @@ def make_workload(name, device, rank=0):
         return W.gqa_bf16(device=device, seed=seed)
     if name == "fp8_long":
         return W.fp8_long(device=device, seed=seed)
+    if name == "fp8_long_e5m2":
+        return W.fp8_long(device=device, seed=seed, fp8="e5m2")
     if name == "u3_mha":
         return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
@@ -415,7 +417,7 @@ class OracleArm:
     def _bytes(self):
         w = self.w
         D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
-        row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "u3": 3 * D // 8}[w.cache_kind]
+        row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "u3": 3 * D // 8}[w.cache_kind]
         meta = 3 if w.cache_kind == "u3" else 0
         req = w.new_req.numpy()
         sel = np.isin(req, self.seqs) & (w.new_pos.numpy() >= 0)
@@ -496,7 +498,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_bf16")
-    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short",
+    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)
@@ -661,7 +663,7 @@ def main():
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3", "u3": "u3"}[w.cache_kind],
+            "dtype": w.cache_kind,
             "data": "synthetic (seeded torch CUDA generator; N(0,1) K/V/q)",
             "config": {"workload": args.workload, "batch": w.batch, "num_heads": w.num_heads,
                        "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,

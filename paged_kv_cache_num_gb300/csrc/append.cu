@@ -74,9 +74,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
     }
 }
 
-// fp8 e4m3: one thread per 8 elements (16 source bytes -> 8 cache bytes).
-template <int SRC, bool VEC>
-__global__ void __launch_bounds__(kAppendThreads) append_e4m3_kernel(AppendParams p)
+// fp8 (e4m3 or e5m2): one thread per 8 elements (16 source bytes -> 8
+// cache bytes).
+template <int SRC, bool VEC, int FP8>
+__global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams p)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -115,7 +116,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_e4m3_kernel(AppendParam
             float2 x;
             x.x = __fdiv_rn(h2f<SRC>(e[2 * j]), scale);
             x.y = __fdiv_rn(h2f<SRC>(e[2 * j + 1]), scale);
-            const uint32_t two = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+            const uint32_t two =
+                __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, FP8 == kE4M3 ? __NV_E4M3 : __NV_E5M2);
             if (j & 1) packed[j >> 1] |= two << 16; else packed[j >> 1] = two;
         }
         if constexpr (VEC) {
@@ -238,15 +240,20 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
             const int64_t work = p.num_tokens * 2 * p.num_kv_heads * p.head_dim;
             return launch_pdl(append_copy_kernel<2>, grid_for(work, T), T, 0, s, p);
         }
-    } else if (cache_kind == kE4M3) {
+    } else if (is_fp8(cache_kind)) {
         const int64_t work = p.num_tokens * 2 * p.num_kv_heads * (p.head_dim / 8);
         const int g = grid_for(work, T);
+        const bool e4 = cache_kind == kE4M3;
         if (p.src_kind == kBF16) {
-            if (vec16) return launch_pdl(append_e4m3_kernel<kBF16, true>, g, T, 0, s, p);
-            else return launch_pdl(append_e4m3_kernel<kBF16, false>, g, T, 0, s, p);
+            if (vec16) return e4 ? launch_pdl(append_fp8_kernel<kBF16, true, kE4M3>, g, T, 0, s, p)
+                                 : launch_pdl(append_fp8_kernel<kBF16, true, kE5M2>, g, T, 0, s, p);
+            return e4 ? launch_pdl(append_fp8_kernel<kBF16, false, kE4M3>, g, T, 0, s, p)
+                      : launch_pdl(append_fp8_kernel<kBF16, false, kE5M2>, g, T, 0, s, p);
         } else {
-            if (vec16) return launch_pdl(append_e4m3_kernel<kF16, true>, g, T, 0, s, p);
-            else return launch_pdl(append_e4m3_kernel<kF16, false>, g, T, 0, s, p);
+            if (vec16) return e4 ? launch_pdl(append_fp8_kernel<kF16, true, kE4M3>, g, T, 0, s, p)
+                                 : launch_pdl(append_fp8_kernel<kF16, true, kE5M2>, g, T, 0, s, p);
+            return e4 ? launch_pdl(append_fp8_kernel<kF16, false, kE4M3>, g, T, 0, s, p)
+                      : launch_pdl(append_fp8_kernel<kF16, false, kE5M2>, g, T, 0, s, p);
         }
     } else {  // kU3
         const int64_t rows = p.num_tokens * 2 * p.num_kv_heads;

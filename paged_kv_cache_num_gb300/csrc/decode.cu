@@ -46,15 +46,15 @@ __device__ __forceinline__ void load_row(const char *row, int e0, float scale, f
             const uint32_t u = *reinterpret_cast<const uint32_t *>(r);
             x[0] = h2f<CK>(u & 0xffff); x[1] = h2f<CK>(u >> 16);
         }
-    } else if constexpr (CK == kE4M3) {
+    } else if constexpr (is_fp8(CK)) {
         const uint8_t *r = reinterpret_cast<const uint8_t *>(row) + e0;
         if constexpr (EPL == 4) {
             const uint32_t u = *reinterpret_cast<const uint32_t *>(r);
-            const float2 a = e4m3x2_to_float2(uint16_t(u & 0xffff));
-            const float2 b = e4m3x2_to_float2(uint16_t(u >> 16));
+            const float2 a = fp8x2_to_float2<CK>(uint16_t(u & 0xffff));
+            const float2 b = fp8x2_to_float2<CK>(uint16_t(u >> 16));
             x[0] = a.x * scale; x[1] = a.y * scale; x[2] = b.x * scale; x[3] = b.y * scale;
         } else {
-            const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t *>(r));
+            const float2 a = fp8x2_to_float2<CK>(*reinterpret_cast<const uint16_t *>(r));
             x[0] = a.x * scale; x[1] = a.y * scale;
         }
     } else {  // kU3: element d at bits 3d..3d+2 of the little-endian row
@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[g][e] = 0.0f;
     }
-    const float ks = (CK == kE4M3) ? p.k_scale[kvh] : 1.0f;
-    const float vs = (CK == kE4M3) ? p.v_scale[kvh] : 1.0f;
+    const float ks = is_fp8(CK) ? p.k_scale[kvh] : 1.0f;
+    const float vs = is_fp8(CK) ? p.v_scale[kvh] : 1.0f;
     const int bmask = (1 << p.block_shift) - 1;
 
     for (int t = t0 + warp; t < t1; t += kGenWarps) {
@@ -281,6 +281,7 @@ cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cud
         switch (cache_kind) {
         case kBF16: return launch_by_dim<kBF16, kBF16>(p, s);
         case kE4M3: return launch_by_dim<kBF16, kE4M3>(p, s);
+        case kE5M2: return launch_by_dim<kBF16, kE5M2>(p, s);
         case kU3: return launch_by_dim<kBF16, kU3>(p, s);
         default: return cudaErrorInvalidValue;
         }
@@ -288,6 +289,7 @@ cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cud
     switch (cache_kind) {
     case kF16: return launch_by_dim<kF16, kF16>(p, s);
     case kE4M3: return launch_by_dim<kF16, kE4M3>(p, s);
+    case kE5M2: return launch_by_dim<kF16, kE5M2>(p, s);
     case kU3: return launch_by_dim<kF16, kU3>(p, s);
     default: return cudaErrorInvalidValue;
     }

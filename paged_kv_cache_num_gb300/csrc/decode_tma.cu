@@ -109,10 +109,13 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float &rlo, flo
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two)
+// Two fp8 codes (the low 16 bits, low byte first) of cache kind CK -> an
+// f16x2 register (exact for both formats).
+template <int CK>
+__device__ __forceinline__ uint32_t f16x2_from_fp8x2(uint32_t two)
 {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu),
-                                                     __NV_E4M3);
+                                                     CK == kE4M3 ? __NV_E4M3 : __NV_E5M2);
     return uint32_t(h.x) | (uint32_t(h.y) << 16);
 }
 
@@ -187,12 +190,12 @@ __host__ __device__ constexpr int u3v_win(int c)
 }
 __host__ __device__ constexpr int u3v_x(int c) { return 3 * c - 8 * u3v_win(c); }
 
-// CK: cache kind (kF16 / kBF16 / kE4M3 / kU3); D head_dim; BS block size.
+// CK: cache kind (kF16 / kBF16 / kE4M3 / kE5M2 / kU3); D head_dim; BS block size.
 // MMA operand type: bf16 for bf16 caches, f16 otherwise (fp8 codes convert
 // exactly to f16).
 template <int CK, int D, int BS>
 struct Tile {
-    static constexpr bool kFp8 = CK == kE4M3;
+    static constexpr bool kFp8 = is_fp8(CK);
     static constexpr bool kIsU3 = CK == pkv::kU3;
     static constexpr bool kBF = CK == kBF16;
     static constexpr int ES = (kFp8 || kIsU3) ? 1 : 2;
@@ -778,10 +781,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         const uint32_t kb = (ktile + (16 * mt + gid) * 128 + 4 * tig) | (uint32_t(gid) << 4);
                         const uint32_t w0 = ld_shared_u32(kb ^ uint32_t((kk & 7) << 4));
                         const uint32_t w1 = ld_shared_u32((kb + 8 * 128) ^ uint32_t((kk & 7) << 4));
-                        a[0] = f16x2_from_e4m3x2(w0);
-                        a[1] = f16x2_from_e4m3x2(w1);
-                        a[2] = f16x2_from_e4m3x2(w0 >> 16);
-                        a[3] = f16x2_from_e4m3x2(w1 >> 16);
+                        a[0] = f16x2_from_fp8x2<CK>(w0);
+                        a[1] = f16x2_from_fp8x2<CK>(w1);
+                        a[2] = f16x2_from_fp8x2<CK>(w0 >> 16);
+                        a[3] = f16x2_from_fp8x2<CK>(w1 >> 16);
                     }
                     ptx::mma16816<T::kBF>(sc[mt], a, qb[kk][0], qb[kk][1]);
                 }
@@ -890,10 +893,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             const uint32_t x01 = ptx::prmt(w[0], w[1], sel);
                             const uint32_t x23 = ptx::prmt(w[2], w[3], sel);
                             uint32_t a[4];
-                            a[0] = f16x2_from_e4m3x2(x01);
-                            a[1] = f16x2_from_e4m3x2(x01 >> 16);
-                            a[2] = f16x2_from_e4m3x2(x23);
-                            a[3] = f16x2_from_e4m3x2(x23 >> 16);
+                            a[0] = f16x2_from_fp8x2<CK>(x01);
+                            a[1] = f16x2_from_fp8x2<CK>(x01 >> 16);
+                            a[2] = f16x2_from_fp8x2<CK>(x23);
+                            a[3] = f16x2_from_fp8x2<CK>(x23 >> 16);
                             ptx::mma16816<false>(o[2 * q4 + hb], a, pb[kt][0], pb[kt][1]);
                         }
                     }
@@ -1108,8 +1111,8 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
     auto enc = encode_fn();
     if (!enc) return false;
     const bool u3 = ck == kU3;
-    const int es = (ck == kE4M3 || u3) ? 1 : 2;
-    const CUtensorMapDataType dt = (ck == kE4M3 || u3) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+    const int es = (is_fp8(ck) || u3) ? 1 : 2;
+    const CUtensorMapDataType dt = (is_fp8(ck) || u3) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : ck == kBF16        ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int row_elems = u3 ? 3 * D / 8 : D;
@@ -1172,7 +1175,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
 {
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
     if (group > 8 || batch > 4096) return false;
-    if (cache_kind == kE4M3) return head_dim == 128;
+    if (is_fp8(cache_kind)) return head_dim == 128;
     if (cache_kind == kU3) return head_dim == 128 && block_size <= 32;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
 }
@@ -1182,7 +1185,7 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
                int cache_kind, bool meta_head_major, int sm_count, FastParams &f, size_t &workspace)
 {
     const bool u3 = cache_kind == kU3;
-    const int es = cache_kind == kE4M3 ? 1 : 2;
+    const int es = is_fp8(cache_kind) ? 1 : 2;
     const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
     int nh = u3 ? kU3Heads : 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
@@ -1245,6 +1248,7 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
                   p.c_head, p.c_blk, f.nh))
         return cudaErrorInvalidValue;
     if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
+    if (cache_kind == kE5M2) return launch_fast_bs<kE5M2, 128>(p, f, mk, mv, s);
     if (cache_kind == kU3) return launch_fast_bs<kU3, 128>(p, f, mk, mv, s);
     if (cache_kind == kBF16)
         return p.head_dim == 128 ? launch_fast_bs<kBF16, 128>(p, f, mk, mv, s) : launch_fast_bs<kBF16, 64>(p, f, mk, mv, s);

@@ -73,4 +73,13 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two)
     return __half22float2(__half2(h2));
 }
 
+// Two fp8 bytes of cache kind FP8 (kE4M3 / kE5M2) -> two floats (exact).
+template <int FP8>
+__device__ __forceinline__ float2 fp8x2_to_float2(uint16_t two)
+{
+    __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two),
+                                                FP8 == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+    return __half22float2(__half2(h2));
+}
+
 }  // namespace pkv

@@ -9,7 +9,10 @@
 
 namespace pkv {
 
-enum CacheKind : int { kF16 = 1, kBF16 = 2, kE4M3 = 3, kU3 = 4 };
+enum CacheKind : int { kF16 = 1, kBF16 = 2, kE4M3 = 3, kU3 = 4, kE5M2 = 9 };
+
+// fp8 cache kinds: one byte per element, a per-kv-head fp32 scale
+constexpr bool is_fp8(int ck) { return ck == kE4M3 || ck == kE5M2; }
 
 // ---------------------------------------------------------------- append
 struct AppendParams {

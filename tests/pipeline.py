@@ -9,7 +9,7 @@ import torch
 
 import workloads as W
 
-KIND_CODE_ORACLE = {"f16": 1, "bf16": 2, "e4m3": 3, "u3": 4}
+KIND_CODE_ORACLE = {"f16": 1, "bf16": 2, "e4m3": 3, "u3": 4, "e5m2": 9}
 
 
 def src_code(w):
@@ -83,7 +83,7 @@ def oracle_caches(w, orc, seqs=None):
     if kind in ("f16", "bf16"):
         c["k_cache"] = W.bits16(w.k_cache0).copy()
         c["v_cache"] = W.bits16(w.v_cache0).copy()
-    elif kind == "e4m3":
+    elif kind in ("e4m3", "e5m2"):
         c["k_cache"] = np.zeros((P, BS, H, D), np.uint8)
         c["v_cache"] = np.zeros((P, BS, H, D), np.uint8)
     else:

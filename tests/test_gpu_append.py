@@ -122,10 +122,12 @@ def test_idempotent_append(pkv):
         assert np.array_equal(before[k], after[k])
 
 
-@pytest.mark.parametrize("src", [torch.bfloat16, torch.float16])
-def test_e4m3_every_source_pattern(pkv, orc, src):
+@pytest.mark.parametrize("src,fp8", [(torch.bfloat16, "e4m3"), (torch.float16, "e4m3"),
+                                     (torch.bfloat16, "e5m2"), (torch.float16, "e5m2")])
+def test_fp8_every_source_pattern(pkv, orc, src, fp8):
     """All 2^16 source bit patterns (NaN, inf, subnormal, overflow included)
-    through the fp8 append for several scales: bit exact with the oracle."""
+    through the fp8 append (e4m3 and e5m2) for several scales: bit exact
+    with the oracle, which encodes from the formats' definitions."""
     H, D, BS = 4, 128, 16
     pats = torch.arange(1 << 16, dtype=torch.int32).to(torch.int16).view(src)
     T = (1 << 16) // D                        # 512 tokens, one head row each x 4 heads
@@ -134,7 +136,7 @@ def test_e4m3_every_source_pattern(pkv, orc, src):
     P = T // BS
     k_scale = torch.tensor([1.0, 1e-3, 37.5, 2.0 ** -20], dtype=torch.float32)
     v_scale = torch.tensor([0.5, 3e4, 1.0 / 3.0, 448.0], dtype=torch.float32)
-    cache = pkv.KVCache.allocate("e4m3", P, BS, H, D, k_scale=k_scale.cuda(),
+    cache = pkv.KVCache.allocate(fp8, P, BS, H, D, k_scale=k_scale.cuda(),
                                  v_scale=v_scale.cuda(), fill=0)
     slots = torch.randperm(P * BS, generator=torch.Generator().manual_seed(3))[:T]
     pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache)
@@ -142,8 +144,8 @@ def test_e4m3_every_source_pattern(pkv, orc, src):
     kc = np.zeros((P, BS, H, D), np.uint8)
     vc = np.zeros((P, BS, H, D), np.uint8)
     code = 1 if src == torch.float16 else 2
-    orc.kv_append(3, code, W.bits16(kn), W.bits16(vn), slots.numpy(), kc, vc, k_scale.numpy(),
-                  v_scale.numpy())
+    orc.kv_append(PL.KIND_CODE_ORACLE[fp8], code, W.bits16(kn), W.bits16(vn), slots.numpy(), kc, vc,
+                  k_scale.numpy(), v_scale.numpy())
     assert np.array_equal(cache.k_cache.cpu().numpy(), kc)
     assert np.array_equal(cache.v_cache.cpu().numpy(), vc)
 

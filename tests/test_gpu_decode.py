@@ -73,6 +73,19 @@ def test_fp8_small(pkv, orc, splits):
 
 
 @pytest.mark.parametrize("splits", [0, 1, 4])
+def test_e5m2_small(pkv, orc, splits):
+    """e5m2 cache: append bit exact, decode (fast path and split general
+    kernel) against the fp64 oracle on the oracle's own cache."""
+    w = W.fp8_long(batch=4, ctx_lo=20, ctx_hi=700, calib_tokens=64, seed=98, fp8="e5m2")
+    cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+    oc = PL.oracle_caches(w, orc)
+    gc = PL.gpu_cache_host(cache)
+    for k in oc:
+        assert np.array_equal(gc[k], oc[k]), k
+    _check(w, out, PL.oracle_decode(w, orc, oc))
+
+
+@pytest.mark.parametrize("splits", [0, 1, 4])
 def test_u3_small(pkv, orc, splits):
     w = W.u3_mha(batch=4, ctx_lo=20, ctx_hi=900, num_heads=8, seed=33)
     cache, out = PL.gpu_run(w, pkv, num_splits=splits)
@@ -285,6 +298,17 @@ def test_full_fp8_long_sampled(pkv, orc):
     pairs = _sample_pairs(w, seqs)
     ref = PL.oracle_decode(w, orc, oc, pairs=pairs)
     _check(w, out, ref, pairs)
+
+
+def test_full_fp8_long_e5m2_sampled(pkv, orc):
+    """The long-context shape with an e5m2 cache (scales amax/57344):
+    sampled sequences against the oracle."""
+    w = W.fp8_long(seed=W.SEEDS["fp8_long_e5m2"], fp8="e5m2")
+    cache, out = PL.gpu_run(w, pkv)
+    seqs = [0, 15]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    pairs = _sample_pairs(w, seqs, heads_per_seq=range(0, w.num_heads, 5))
+    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
 
 
 def test_full_u3_mha_sampled(pkv, orc):

@@ -51,7 +51,7 @@ from typing import Dict, Optional
 import torch
 
 SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44,
-         "fp8_long": 45, "u3_mha": 46, "mha_short": 47}
+         "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48}
 
 
 @dataclass
