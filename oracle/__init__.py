@@ -27,7 +27,7 @@ _lock = threading.Lock()
 _lib = None
 
 # dtype codes of the oracle's own interface
-F16, BF16, E4M3, U3, E5M2 = 1, 2, 3, 4, 9
+F16, BF16, E4M3, U3, E5M2, I8 = 1, 2, 3, 4, 9, 10
 
 
 def build(force: bool = False) -> str:
@@ -76,7 +76,7 @@ def _load():
         lib.pkvo_max_threads.restype = i32
         for fn in ("pkvo_f32_to_e4m3_n", "pkvo_f32_to_f16_n", "pkvo_f16_to_f64_n",
                    "pkvo_bf16_to_f64_n", "pkvo_e4m3_to_f64_n", "pkvo_f32_to_e5m2_n",
-                   "pkvo_e5m2_to_f64_n"):
+                   "pkvo_e5m2_to_f64_n", "pkvo_f32_to_i8_n"):
             getattr(lib, fn).argtypes = [P, P, i64]
         _lib = lib
         return lib
@@ -132,6 +132,12 @@ def e5m2_to_f64(codes: np.ndarray) -> np.ndarray:
 def f32_to_e5m2(x: np.ndarray) -> np.ndarray:
     """binary32 -> E5M2 code, RNE, saturating to +-57344 (NaN -> 0x7F)."""
     return _conv("pkvo_f32_to_e5m2_n", x, np.float32, np.uint8)
+
+
+def f32_to_i8(x: np.ndarray) -> np.ndarray:
+    """binary32 (already divided by the scale) -> int8 code: nearest, half to
+    even, saturated to +-127, NaN -> 0."""
+    return _conv("pkvo_f32_to_i8_n", x, np.float32, np.int8)
 
 
 def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:

@@ -35,6 +35,11 @@
  *     bits, infinities and NaNs at exponent 31, max 57344); encoding rounds
  *     to nearest even and saturates finite overflow and infinities to
  *     +-57344, like e4m3; every NaN encodes to 0x7F.
+ *   - int8 caches ("Write Triton Kv Cache Append Kernel", inputs item 4 and
+ *     reasoning step 6: (x / scale) cast to the cache dtype) store
+ *     clamp(rint(x / scale), -127, 127) with x / scale in fp32 and rint
+ *     rounding half to even (symmetric range); NaN stores 0; the stored code
+ *     c means c * scale.
  *   - 3-bit quantiser: s = fp16_rn((max-min)/7), z = clamp(rint(-min/s),0,7),
  *     q = clamp(rint(x/s)+z,0,7), all fp32; s == 0 gives z = 0, q = 0; an s
  *     that overflows fp16 saturates to 65504.  Element d of a head row sits at
@@ -60,6 +65,7 @@
 #define O_E4M3 3
 #define O_U3 4
 #define O_E5M2 9
+#define O_I8 10
 
 /* ------------------------------------------------------------------------ */
 /* Scalar formats                                                           */
@@ -185,6 +191,19 @@ uint8_t pkvo_f32_to_e5m2(float f)
     int E = e2 - 1;
     uint8_t mant = (uint8_t)(r / ldexp(1.0, E - 2) - 4.0);
     return sign | (uint8_t)((E + 15) << 2) | mant;
+}
+
+/* int8 code of x (already divided by the scale, in fp32): nearest integer,
+ * half to even, saturated to +-127; NaN -> 0. */
+int8_t pkvo_f32_to_i8(float f)
+{
+    if (isnan(f))
+        return 0;
+    if (f >= 127.0f)
+        return 127;
+    if (f <= -127.0f)
+        return -127;
+    return (int8_t)nearbyintf(f);
 }
 
 uint8_t pkvo_f32_to_e4m3(float f)
@@ -385,6 +404,15 @@ int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int n
             if (cache_dtype == O_F16 || cache_dtype == O_BF16) {
                 memcpy((uint16_t *)k_cache + row * D, ks, (size_t)D * 2);
                 memcpy((uint16_t *)v_cache + row * D, vs, (size_t)D * 2);
+            } else if (cache_dtype == O_I8) {
+                int8_t *kd = (int8_t *)k_cache + row * D;
+                int8_t *vd = (int8_t *)v_cache + row * D;
+                for (int d = 0; d < D; ++d) {
+                    float xk = (float)elem16_to_f64(ks[d], src_dtype) / k_scale[h];
+                    float xv = (float)elem16_to_f64(vs[d], src_dtype) / v_scale[h];
+                    kd[d] = pkvo_f32_to_i8(xk);
+                    vd[d] = pkvo_f32_to_i8(xv);
+                }
             } else if (cache_dtype == O_E4M3 || cache_dtype == O_E5M2) {
                 uint8_t *kd = (uint8_t *)k_cache + row * D;
                 uint8_t *vd = (uint8_t *)v_cache + row * D;
@@ -423,6 +451,8 @@ static double cache_elem(int cache_dtype, const void *cache, int64_t row, int D,
         return pkvo_e4m3_to_f64(((const uint8_t *)cache)[row * D + d]) * scale_h;
     if (cache_dtype == O_E5M2)
         return pkvo_e5m2_to_f64(((const uint8_t *)cache)[row * D + d]) * scale_h;
+    if (cache_dtype == O_I8)
+        return (double)((const int8_t *)cache)[row * D + d] * scale_h;
     /* O_U3: bit 3d of the row's little-endian bit stream */
     const uint8_t *p = (const uint8_t *)cache + row * (int64_t)(3 * D / 8);
     uint8_t v[8];
@@ -566,6 +596,12 @@ void pkvo_f32_to_e5m2_n(const float *x, uint8_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = pkvo_f32_to_e5m2(x[i]);
+}
+
+void pkvo_f32_to_i8_n(const float *x, int8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = pkvo_f32_to_i8(x[i]);
 }
 
 void pkvo_e5m2_to_f64_n(const uint8_t *x, double *out, int64_t n)

@@ -110,6 +110,31 @@ def test_scatter_e5m2_matches_cast_and_step(orc):
         assert np.all(np.abs(deq - xs) <= half_step * (1 + 1e-6))
 
 
+def test_scatter_i8_matches_round_and_step(orc):
+    """int8: codes equal torch's round-half-even of (x / scale) in fp32,
+    clamped to +-127, and the dequantised cache is within half a step
+    (the scale) of the source where it is in range."""
+    P, BS, H, D, T, k0, v0, kn, vn, slots = _scatter_case(orc, torch.bfloat16, seed=4)
+    kscale = np.array([0.02, 0.005, 0.03], np.float32)
+    vscale = np.array([0.025, 0.01, 0.004], np.float32)
+    kc = np.zeros((P, BS, H, D), np.int8)
+    vc = np.zeros((P, BS, H, D), np.int8)
+    orc.kv_append(orc.I8, orc.BF16, W.bits16(kn), W.bits16(vn), slots, kc, vc, kscale, vscale)
+    real = slots >= 0
+    for cache, src, sc in ((kc, kn, kscale), (vc, vn, vscale)):
+        x = src[torch.from_numpy(real)].float() / torch.from_numpy(sc)[None, :, None]
+        ref = x.round().clamp(-127, 127).to(torch.int8).numpy()
+        got = cache.reshape(P * BS, H, D)[slots[real]]
+        assert np.array_equal(got, ref)
+        inr = (x.abs() <= 127).numpy()
+        xs = src[torch.from_numpy(real)].double().numpy()
+        deq = got.astype(np.float64) * sc[None, :, None]
+        err = np.abs(deq - xs) / sc[None, :, None]
+        # half a step, plus the fp32 rounding of x / scale (<= 2^-24 * 127)
+        assert np.all(err[inr] <= 0.5 + 1e-5)
+        assert (~inr).any()              # some values saturate at these scales
+
+
 def test_scatter_e4m3_matches_cast_and_step(orc):
     """fp8: codes equal torch's e4m3 cast of (x / scale) taken in fp32 (in
     range), and the dequantised cache is within half a quantisation step of

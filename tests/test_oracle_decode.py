@@ -146,9 +146,10 @@ def _fill_quantised(orc, w, code):
     vn = np.concatenate([W.bits16(w.v_fill), W.bits16(w.v_new)])
     slots = orc.build_slot_mapping(w.block_tables.numpy(), req, pos, BS)
     c = {}
-    if code in (orc.E4M3, orc.E5M2):
-        c["k"] = np.zeros((P, BS, H, D), np.uint8)
-        c["v"] = np.zeros((P, BS, H, D), np.uint8)
+    if code in (orc.E4M3, orc.E5M2, orc.I8):
+        dt = np.int8 if code == orc.I8 else np.uint8
+        c["k"] = np.zeros((P, BS, H, D), dt)
+        c["v"] = np.zeros((P, BS, H, D), dt)
         orc.kv_append(code, src_code, kn, vn, slots, c["k"], c["v"], w.k_scale.numpy(),
                       w.v_scale.numpy())
     else:
@@ -187,6 +188,20 @@ def test_e5m2_decode_on_dequantised_cache(orc):
     assert bad == 0
     kd = e5m2_dequant(c["k"], w.k_scale.numpy())
     vd = e5m2_dequant(c["v"], w.v_scale.numpy())
+    ref = gather_attention(w.q, kd, vd, w.block_tables.numpy(), w.context_lens.numpy(),
+                           w.block_size, w.sm_scale)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def test_i8_decode_on_dequantised_cache(orc):
+    w = W.fp8_long(batch=3, ctx_lo=40, ctx_hi=150, calib_tokens=64, seed=17, fp8="i8")
+    c = _fill_quantised(orc, w, orc.I8)
+    out, bad = orc.paged_decode(orc.I8, orc.BF16, W.bits16(w.q), c["k"], c["v"],
+                                w.block_tables.numpy(), w.context_lens.numpy(), w.block_size,
+                                w.sm_scale, k_scale=w.k_scale.numpy(), v_scale=w.v_scale.numpy())
+    assert bad == 0
+    kd = c["k"].astype(np.float64) * w.k_scale.numpy().astype(np.float64)[:, None]
+    vd = c["v"].astype(np.float64) * w.v_scale.numpy().astype(np.float64)[:, None]
     ref = gather_attention(w.q, kd, vd, w.block_tables.numpy(), w.context_lens.numpy(),
                            w.block_size, w.sm_scale)
     assert np.max(np.abs(out - ref)) < 1e-12

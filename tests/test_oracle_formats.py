@@ -138,3 +138,28 @@ def test_e5m2_ties_to_even(orc):
     # range 2^-17 ties to 0 and 3 * 2^-17 to 2 * 2^-16
     x = np.array([1.125, 1.375, 1.125 + 2 ** -20, 2 ** -17, 3 * 2 ** -17], np.float32)
     assert orc.f32_to_e5m2(x).tolist() == [0x3C, 0x3E, 0x3D, 0x00, 0x02]
+
+
+# ---------------------------------------------------------------- int8 codes
+
+def test_i8_encode_matches_torch_round_and_clamp(orc):
+    x = _structured_f32_sample()
+    x = x[~np.isnan(x)]
+    got = orc.f32_to_i8(x)
+    ref = torch.from_numpy(x).round().clamp(-127, 127).to(torch.int8).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_i8_ties_saturation_nan(orc):
+    x = np.array([0.5, 1.5, 2.5, -0.5, -2.5, 126.5, -126.5, 127.0, 127.4, 1e9, np.inf, -np.inf,
+                  -200.0, np.nan, -0.0], np.float32)
+    assert orc.f32_to_i8(x).tolist() == [0, 2, 2, 0, -2, 126, -126, 127, 127, 127, 127, -127, -127,
+                                         0, 0]
+
+
+def test_i8_symmetric_and_exact_on_integers(orc):
+    x = _structured_f32_sample()
+    x = x[np.isfinite(x)]
+    assert np.array_equal(orc.f32_to_i8(-x), -orc.f32_to_i8(x))
+    ints = np.arange(-127, 128, dtype=np.float32)
+    assert np.array_equal(orc.f32_to_i8(ints), ints.astype(np.int8))

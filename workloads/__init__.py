@@ -51,7 +51,7 @@ from typing import Dict, Optional
 import torch
 
 SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44,
-         "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48}
+         "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48, "i8_long": 49}
 
 
 @dataclass
@@ -246,9 +246,9 @@ def _fill_lists(ctx_list, device):
 def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, num_kv_heads=8,
              head_dim=128, block_size=32, calib_tokens=4096, seed=None,
              fp8="e4m3") -> Workload:
-    """Long-context fp8 cache with per-kv-head scales amax / (the format's
-    largest finite value): 448 for e4m3 (defaults: the full-size case),
-    57344 for e5m2."""
+    """Long-context quantised cache with per-kv-head scales amax / (the
+    format's largest value): 448 for e4m3 (defaults: the full-size case),
+    57344 for e5m2, 127 for int8 ("i8")."""
     g = _gen(SEEDS["fp8_long"] if seed is None else seed, device)
     dt = torch.bfloat16
     B, Hq, Hkv, D, BS = batch, num_heads, num_kv_heads, head_dim, block_size
@@ -262,7 +262,7 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
     k_cal = _randn((calib_tokens, Hkv, D), g, device, dt)
     v_cal = _randn((calib_tokens, Hkv, D), g, device, dt)
     # calibration: per-kv-head amax / max-finite in fp32
-    fmax = {"e4m3": 448.0, "e5m2": 57344.0}[fp8]
+    fmax = {"e4m3": 448.0, "e5m2": 57344.0, "i8": 127.0}[fp8]
     k_scale = k_cal.float().abs().amax(dim=(0, 2)) / fmax
     v_scale = v_cal.float().abs().amax(dim=(0, 2)) / fmax
     fill_req, fill_pos = _fill_lists(ctx_list, device)
