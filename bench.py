@@ -181,7 +181,7 @@ def algorithmic_bytes(w, decode=True, append=True):
     append: per real new token Hkv * (2 source rows + 2 cache rows + metadata)
             + its slot (8 B) and (request, position) (8 B)."""
     D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
-    row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "u3": 3 * D // 8}[w.cache_kind]
+    row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "i8": D, "u3": 3 * D // 8}[w.cache_kind]
     meta = 3 if w.cache_kind == "u3" else 0
     total = 0
     if decode and w.q is not None:
@@ -205,6 +205,8 @@ def make_workload(name, device, rank=0):
         return W.fp8_long(device=device, seed=seed)
     if name == "fp8_long_e5m2":
         return W.fp8_long(device=device, seed=seed, fp8="e5m2")
+    if name == "i8_long":
+        return W.fp8_long(device=device, seed=seed, fp8="i8")
     if name == "u3_mha":
         return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
@@ -417,7 +419,7 @@ class OracleArm:
     def _bytes(self):
         w = self.w
         D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
-        row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "u3": 3 * D // 8}[w.cache_kind]
+        row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "i8": D, "u3": 3 * D // 8}[w.cache_kind]
         meta = 3 if w.cache_kind == "u3" else 0
         req = w.new_req.numpy()
         sel = np.isin(req, self.seqs) & (w.new_pos.numpy() >= 0)
@@ -498,7 +500,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_bf16")
-    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2",
+    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)

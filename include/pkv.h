@@ -52,7 +52,8 @@ enum {
     PKV_DTYPE_I32 = 6,
     PKV_DTYPE_I64 = 7,
     PKV_DTYPE_F32 = 8,
-    PKV_DTYPE_E5M2 = 9  /* OCP fp8 e5m2 (max 57344, with inf / NaN codes) */
+    PKV_DTYPE_E5M2 = 9, /* OCP fp8 e5m2 (max 57344, with inf / NaN codes) */
+    PKV_DTYPE_I8 = 10   /* int8 codes (scaled, symmetric range +-127) */
 };
 
 /* Host-side status codes. */
@@ -92,7 +93,7 @@ typedef struct pkv_tensor {
  * and PagedAttention", Step 1):
  *
  *   k_cache, v_cache : [num_blocks, block_size, num_kv_heads, row]
- *       F16 / BF16 / E4M3 / E5M2 : row = head_dim elements;
+ *       F16 / BF16 / E4M3 / E5M2 / I8 : row = head_dim elements;
  *       U3                : row = 3 * head_dim / 8 bytes; element d of a
  *                           head row is bits 3d..3d+2 of the row read as one
  *                           little-endian bit string, i.e. octet j holds
@@ -102,8 +103,8 @@ typedef struct pkv_tensor {
  *     aligned; the block stride must be a multiple of 16 bytes, and for
  *     F16/BF16/E4M3 also the slot and head strides.  K and V must have the
  *     same dtype, shape and strides.
- *   k_scale, v_scale : E4M3 and E5M2 only, device fp32 [num_kv_heads], > 0.
- *     A stored code c means fp8(c) * scale.
+ *   k_scale, v_scale : E4M3, E5M2 and I8 only, device fp32 [num_kv_heads],
+ *     > 0.  A stored code c means fp8(c) * scale, or c * scale for I8.
  *   k_qscale, v_qscale (F16) and k_qzero, v_qzero (U8), U3 only:
  *     [num_blocks, block_size, num_kv_heads]; a stored code u means
  *     (u - zero) * scale for its (slot, head) row.  Any strides are
@@ -172,6 +173,8 @@ int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req,
  *                NaN stores 0x7F.
  *     E5M2     : the same with e5m2_rn_satfinite (overflow and infinities
  *                to +-57344, NaN stores 0x7F).
+ *     I8       : code = clamp(rint(x / scale), -127, 127), x / scale in fp32,
+ *                rint rounding half to even; NaN stores 0.
  *     U3       : per (token, head) row, all in fp32 with IEEE rounding:
  *                s = fp16_rn((max - min) / 7) (65504 if that overflows),
  *                z = clamp(rint(-min / s), 0, 7),

@@ -17,6 +17,8 @@
 // min / max are warp-shuffle reductions and the packing goes through shared
 // memory.  All are programmatic dependent launches, so the launch of each
 // overlaps the tail of the previous kernel in the stream.
+#include <type_traits>
+
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -74,8 +76,25 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
     }
 }
 
-// fp8 (e4m3 or e5m2): one thread per 8 elements (16 source bytes -> 8
-// cache bytes).
+// Two values already divided by the scale -> two one-byte codes (low byte
+// first): fp8 satfinite casts, or int8 nearest-even saturated to +-127
+// (NaN -> 0).
+template <int Q8>
+__device__ __forceinline__ uint32_t q8x2_encode(float2 x)
+{
+    if constexpr (Q8 == kI8) {
+        auto one = [](float v) -> uint32_t {
+            int c = isnan(v) ? 0 : __float2int_rn(fminf(fmaxf(v, -127.0f), 127.0f));
+            return uint32_t(c) & 0xffu;
+        };
+        return one(x.x) | (one(x.y) << 8);
+    } else {
+        return __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, Q8 == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+    }
+}
+
+// One-byte codes (e4m3, e5m2, int8): one thread per 8 elements (16 source
+// bytes -> 8 cache bytes).
 template <int SRC, bool VEC, int FP8>
 __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams p)
 {
@@ -116,8 +135,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
             float2 x;
             x.x = __fdiv_rn(h2f<SRC>(e[2 * j]), scale);
             x.y = __fdiv_rn(h2f<SRC>(e[2 * j + 1]), scale);
-            const uint32_t two =
-                __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, FP8 == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+            const uint32_t two = q8x2_encode<FP8>(x);
             if (j & 1) packed[j >> 1] |= two << 16; else packed[j >> 1] = two;
         }
         if constexpr (VEC) {
@@ -240,21 +258,21 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
             const int64_t work = p.num_tokens * 2 * p.num_kv_heads * p.head_dim;
             return launch_pdl(append_copy_kernel<2>, grid_for(work, T), T, 0, s, p);
         }
-    } else if (is_fp8(cache_kind)) {
+    } else if (is_q8(cache_kind)) {
         const int64_t work = p.num_tokens * 2 * p.num_kv_heads * (p.head_dim / 8);
         const int g = grid_for(work, T);
-        const bool e4 = cache_kind == kE4M3;
-        if (p.src_kind == kBF16) {
-            if (vec16) return e4 ? launch_pdl(append_fp8_kernel<kBF16, true, kE4M3>, g, T, 0, s, p)
-                                 : launch_pdl(append_fp8_kernel<kBF16, true, kE5M2>, g, T, 0, s, p);
-            return e4 ? launch_pdl(append_fp8_kernel<kBF16, false, kE4M3>, g, T, 0, s, p)
-                      : launch_pdl(append_fp8_kernel<kBF16, false, kE5M2>, g, T, 0, s, p);
-        } else {
-            if (vec16) return e4 ? launch_pdl(append_fp8_kernel<kF16, true, kE4M3>, g, T, 0, s, p)
-                                 : launch_pdl(append_fp8_kernel<kF16, true, kE5M2>, g, T, 0, s, p);
-            return e4 ? launch_pdl(append_fp8_kernel<kF16, false, kE4M3>, g, T, 0, s, p)
-                      : launch_pdl(append_fp8_kernel<kF16, false, kE5M2>, g, T, 0, s, p);
-        }
+        auto go = [&](auto src_c, auto vec_c) -> cudaError_t {
+            constexpr int S = decltype(src_c)::value;
+            constexpr bool V = decltype(vec_c)::value;
+            if (cache_kind == kE4M3) return launch_pdl(append_fp8_kernel<S, V, kE4M3>, g, T, 0, s, p);
+            if (cache_kind == kE5M2) return launch_pdl(append_fp8_kernel<S, V, kE5M2>, g, T, 0, s, p);
+            return launch_pdl(append_fp8_kernel<S, V, kI8>, g, T, 0, s, p);
+        };
+        using BF = std::integral_constant<int, kBF16>;
+        using HF = std::integral_constant<int, kF16>;
+        if (p.src_kind == kBF16)
+            return vec16 ? go(BF{}, std::true_type{}) : go(BF{}, std::false_type{});
+        return vec16 ? go(HF{}, std::true_type{}) : go(HF{}, std::false_type{});
     } else {  // kU3
         const int64_t rows = p.num_tokens * 2 * p.num_kv_heads;
         const int g = grid_for(rows * 32, T);

@@ -46,7 +46,11 @@ __device__ __forceinline__ void load_row(const char *row, int e0, float scale, f
             const uint32_t u = *reinterpret_cast<const uint32_t *>(r);
             x[0] = h2f<CK>(u & 0xffff); x[1] = h2f<CK>(u >> 16);
         }
-    } else if constexpr (is_fp8(CK)) {
+    } else if constexpr (CK == kI8) {
+        const int8_t *r = reinterpret_cast<const int8_t *>(row) + e0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) x[e] = float(r[e]) * scale;
+    } else if constexpr (is_q8(CK)) {
         const uint8_t *r = reinterpret_cast<const uint8_t *>(row) + e0;
         if constexpr (EPL == 4) {
             const uint32_t u = *reinterpret_cast<const uint32_t *>(r);
@@ -120,8 +124,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[g][e] = 0.0f;
     }
-    const float ks = is_fp8(CK) ? p.k_scale[kvh] : 1.0f;
-    const float vs = is_fp8(CK) ? p.v_scale[kvh] : 1.0f;
+    const float ks = is_q8(CK) ? p.k_scale[kvh] : 1.0f;
+    const float vs = is_q8(CK) ? p.v_scale[kvh] : 1.0f;
     const int bmask = (1 << p.block_shift) - 1;
 
     for (int t = t0 + warp; t < t1; t += kGenWarps) {
@@ -282,6 +286,7 @@ cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cud
         case kBF16: return launch_by_dim<kBF16, kBF16>(p, s);
         case kE4M3: return launch_by_dim<kBF16, kE4M3>(p, s);
         case kE5M2: return launch_by_dim<kBF16, kE5M2>(p, s);
+        case kI8: return launch_by_dim<kBF16, kI8>(p, s);
         case kU3: return launch_by_dim<kBF16, kU3>(p, s);
         default: return cudaErrorInvalidValue;
         }
@@ -290,6 +295,7 @@ cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cud
     case kF16: return launch_by_dim<kF16, kF16>(p, s);
     case kE4M3: return launch_by_dim<kF16, kE4M3>(p, s);
     case kE5M2: return launch_by_dim<kF16, kE5M2>(p, s);
+    case kI8: return launch_by_dim<kF16, kI8>(p, s);
     case kU3: return launch_by_dim<kF16, kU3>(p, s);
     default: return cudaErrorInvalidValue;
     }

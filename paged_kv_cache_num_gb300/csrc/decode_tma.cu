@@ -109,15 +109,23 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float &rlo, flo
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Two fp8 codes (the low 16 bits, low byte first) of cache kind CK -> an
-// f16x2 register (exact for both formats).
+// Two one-byte codes (the low 16 bits, low byte first) of cache kind CK ->
+// an f16x2 register, exactly: fp8 through the hardware conversion; int8 c
+// as 1152 + c (a byte permute puts c next to the exponent of 1024 and an
+// XOR of the byte's top bit adds 128), the 1152 offset being removed in
+// fp32 after the MMA.
 template <int CK>
 __device__ __forceinline__ uint32_t f16x2_from_fp8x2(uint32_t two)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu),
-                                                     CK == kE4M3 ? __NV_E4M3 : __NV_E5M2);
-    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+    if constexpr (CK == kI8) {
+        return ptx::prmt(two, 0x64646464u, 0x4140u) ^ 0x00800080u;
+    } else {
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu),
+                                                         CK == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+        return uint32_t(h.x) | (uint32_t(h.y) << 16);
+    }
 }
+constexpr float kI8Bias = 1152.0f;
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
 {
@@ -195,7 +203,7 @@ __host__ __device__ constexpr int u3v_x(int c) { return 3 * c - 8 * u3v_win(c); 
 // exactly to f16).
 template <int CK, int D, int BS>
 struct Tile {
-    static constexpr bool kFp8 = is_fp8(CK);
+    static constexpr bool kFp8 = is_q8(CK);
     static constexpr bool kIsU3 = CK == pkv::kU3;
     static constexpr bool kBF = CK == kBF16;
     static constexpr int ES = (kFp8 || kIsU3) ? 1 : 2;
@@ -393,8 +401,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
     float mult = 1.0f, vmul = 1.0f;
     int ctx_b = 0;
-    // 3-bit only: per head column, sum(q' 2^(x-24)) of the QK operand and
-    // the running sum of P' * zero of the PV operand
+    // per head column: 3-bit, sum(q' 2^(x-24)) of the QK operand and the
+    // running sum of P' * zero of the PV operand; int8, 1152 sum(q') and the
+    // running sum of P' (the operands' 1152 offsets)
     float q1h[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
 
     auto start_segment = [&]() {
@@ -494,11 +503,21 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
             float qs = 1.0f;
             while (amax * qs > 16384.0f) qs *= 0.5f;
-            float d0, d1;
+            float d0, d1, d2, d3, c0 = 0.0f;
 #pragma unroll
             for (int kk = 0; kk < T::QK; ++kk) {
                 qb[kk][0] = pack_f16(f[kk][0] * qs, f[kk][1] * qs, d0, d1);
-                qb[kk][1] = pack_f16(f[kk][2] * qs, f[kk][3] * qs, d0, d1);
+                qb[kk][1] = pack_f16(f[kk][2] * qs, f[kk][3] * qs, d2, d3);
+                c0 += (d0 + d1) + (d2 + d3);
+            }
+            if constexpr (CK == kI8) {     // sum of q' over head_dim, per q head gid
+                c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
+                c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {   // head columns 2tig, 2tig+1
+                    q1h[c] = kI8Bias * __shfl_sync(0xffffffffu, c0, 4 * (2 * tig + c));
+                    zs[c] = 0.0f;
+                }
             }
             mult = log2e_scale * p.k_scale[kvh] / qs;
             vmul = p.v_scale[kvh];
@@ -534,19 +553,21 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             lt[c] = v;
         }
         float zt[2] = {0.0f, 0.0f};
-        if constexpr (T::kIsU3) {
+        if constexpr (T::kIsU3 || CK == kI8) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float z = zs[c];
 #pragma unroll
                 for (int o2 = 4; o2 < 32; o2 <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o2);
-                zt[c] = z;
+                zt[c] = CK == kI8 ? kI8Bias * z : z;
             }
         }
         // accumulator entry (t, r, c) -> value of the segment's unnormalised output
         auto oval = [&](int t, int r, int c) -> float {
             if constexpr (T::kIsU3) {
                 return o[t][2 * r + c] * float(1 << (24 - u3v_x(2 * t + r))) - zt[c];
+            } else if constexpr (CK == kI8) {
+                return o[t][2 * r + c] - zt[c];
             } else {
                 return o[t][2 * r + c];
             }
@@ -796,7 +817,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int t = 0; t < T::KT; ++t) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float v = sc[t][e] * mult;
+                    float v = (CK == kI8 ? sc[t][e] - q1h[e & 1] : sc[t][e]) * mult;
                     if (partial) {
                         const int tok = 16 * t + gid + 8 * (e >> 1);
                         v = tok < valid ? v : NEG_INF;
@@ -815,6 +836,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
                 m[c] = mn;
                 l[c] *= alpha[c];
+                if constexpr (CK == kI8) zs[c] *= alpha[c];
             }
             // P^T as the B operand of the PV product: pack each 8-token half
             // of a tile (rows = tokens, cols = heads) and transpose it in
@@ -830,6 +852,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     l[1] += p1;
                     float q0, q1;
                     const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0, p1, q0, q1);
+                    if constexpr (CK == kI8) {   // the PV operand's offset: sum of P' as rounded
+                        zs[0] += q0;
+                        zs[1] += q1;
+                    }
                     pb[t][r] = ptx::movmatrix_trans(w);
                 }
             }
@@ -1111,8 +1137,8 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
     auto enc = encode_fn();
     if (!enc) return false;
     const bool u3 = ck == kU3;
-    const int es = (is_fp8(ck) || u3) ? 1 : 2;
-    const CUtensorMapDataType dt = (is_fp8(ck) || u3) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+    const int es = (is_q8(ck) || u3) ? 1 : 2;
+    const CUtensorMapDataType dt = (is_q8(ck) || u3) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : ck == kBF16        ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int row_elems = u3 ? 3 * D / 8 : D;
@@ -1175,7 +1201,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
 {
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
     if (group > 8 || batch > 4096) return false;
-    if (is_fp8(cache_kind)) return head_dim == 128;
+    if (is_q8(cache_kind)) return head_dim == 128;
     if (cache_kind == kU3) return head_dim == 128 && block_size <= 32;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
 }
@@ -1185,7 +1211,7 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
                int cache_kind, bool meta_head_major, int sm_count, FastParams &f, size_t &workspace)
 {
     const bool u3 = cache_kind == kU3;
-    const int es = is_fp8(cache_kind) ? 1 : 2;
+    const int es = is_q8(cache_kind) ? 1 : 2;
     const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
     int nh = u3 ? kU3Heads : 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
@@ -1249,6 +1275,7 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
         return cudaErrorInvalidValue;
     if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
     if (cache_kind == kE5M2) return launch_fast_bs<kE5M2, 128>(p, f, mk, mv, s);
+    if (cache_kind == kI8) return launch_fast_bs<kI8, 128>(p, f, mk, mv, s);
     if (cache_kind == kU3) return launch_fast_bs<kU3, 128>(p, f, mk, mv, s);
     if (cache_kind == kBF16)
         return p.head_dim == 128 ? launch_fast_bs<kBF16, 128>(p, f, mk, mv, s) : launch_fast_bs<kBF16, 64>(p, f, mk, mv, s);

@@ -34,6 +34,7 @@ int elem_size(int dtype)
     case PKV_DTYPE_BF16: return 2;
     case PKV_DTYPE_E4M3:
     case PKV_DTYPE_E5M2:
+    case PKV_DTYPE_I8:
     case PKV_DTYPE_U3:
     case PKV_DTYPE_U8: return 1;
     case PKV_DTYPE_I32:
@@ -91,9 +92,8 @@ int check_cache(const pkv_cache *c, CacheInfo &ci, bool any_block_size = false)
     const pkv_tensor &k = c->k_cache, &v = c->v_cache;
     if (k.dtype != v.dtype) return fail(PKV_ERR_DTYPE, "k_cache and v_cache dtypes differ");
     const int kind = k.dtype;
-    if (kind != PKV_DTYPE_F16 && kind != PKV_DTYPE_BF16 && kind != PKV_DTYPE_E4M3 && kind != PKV_DTYPE_E5M2 &&
-        kind != PKV_DTYPE_U3)
-        return fail(PKV_ERR_DTYPE, "cache dtype %d is not F16, BF16, E4M3, E5M2 or U3", kind);
+    if (kind != PKV_DTYPE_F16 && kind != PKV_DTYPE_BF16 && !pkv::is_q8(kind) && kind != PKV_DTYPE_U3)
+        return fail(PKV_ERR_DTYPE, "cache dtype %d is not F16, BF16, E4M3, E5M2, I8 or U3", kind);
     for (int i = 0; i < 4; ++i) {
         if (k.shape[i] != v.shape[i]) return fail(PKV_ERR_SHAPE, "k_cache and v_cache shapes differ");
         if (k.stride[i] != v.stride[i]) return fail(PKV_ERR_LAYOUT, "k_cache and v_cache strides differ");
@@ -119,8 +119,8 @@ int check_cache(const pkv_cache *c, CacheInfo &ci, bool any_block_size = false)
                     (long long)ci.block_size);
     if (ci.num_blocks * ci.block_size > (int64_t(1) << 31))
         return fail(PKV_ERR_UNSUPPORTED, "pool of more than 2^31 slots");
-    if ((kind == PKV_DTYPE_E4M3 || kind == PKV_DTYPE_E5M2) && (!c->k_scale || !c->v_scale))
-        return fail(PKV_ERR_NULL, "fp8 cache needs k_scale and v_scale");
+    if (pkv::is_q8(kind) && (!c->k_scale || !c->v_scale))
+        return fail(PKV_ERR_NULL, "fp8 / int8 cache needs k_scale and v_scale");
     if (kind == PKV_DTYPE_U3) {
         TRY(check_tensor(&c->k_qscale, "k_qscale", 3));
         TRY(check_tensor(&c->k_qzero, "k_qzero", 3));
@@ -244,8 +244,8 @@ static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, cons
     if (k_new->stride[2] != 1 || v_new->stride[2] != 1) return fail(PKV_ERR_LAYOUT, "head_dim of k_new/v_new must be contiguous");
     if ((ci.kind == PKV_DTYPE_F16 || ci.kind == PKV_DTYPE_BF16) && ci.kind != src)
         return fail(PKV_ERR_DTYPE, "16-bit cache dtype must equal the source dtype");
-    if (pkv::is_fp8(ci.kind) && ci.head_dim % 8 != 0)
-        return fail(PKV_ERR_UNSUPPORTED, "fp8 append needs head_dim % 8 == 0");
+    if (pkv::is_q8(ci.kind) && ci.head_dim % 8 != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "fp8 / int8 append needs head_dim % 8 == 0");
     if (ci.kind == PKV_DTYPE_U3 && ci.head_dim != 64 && ci.head_dim != 128)
         return fail(PKV_ERR_UNSUPPORTED, "U3 append supports head_dim 64 and 128");
     const int64_t es = 2;
@@ -386,7 +386,7 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
     dc.plan = pkv::DecodePlan{};
     if (num_splits == 0 && pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
         // q rows are read 16 (3-bit), 8 (fp8) or 4 (16-bit) bytes at a time
-        const size_t qa = ci.kind == PKV_DTYPE_U3 ? 16 : (pkv::is_fp8(ci.kind) ? 8 : 4);
+        const size_t qa = ci.kind == PKV_DTYPE_U3 ? 16 : (pkv::is_q8(ci.kind) ? 8 : 4);
         const bool q_ok = aligned(q->data, qa) && (p.q_b % qa) == 0 && (p.q_h % qa) == 0;
         // 3-bit: each block's metadata must be one contiguous, 16-byte aligned
         // run per array (staged with bulk copies), either head-major

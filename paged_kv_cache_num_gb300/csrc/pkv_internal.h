@@ -9,10 +9,10 @@
 
 namespace pkv {
 
-enum CacheKind : int { kF16 = 1, kBF16 = 2, kE4M3 = 3, kU3 = 4, kE5M2 = 9 };
+enum CacheKind : int { kF16 = 1, kBF16 = 2, kE4M3 = 3, kU3 = 4, kE5M2 = 9, kI8 = 10 };
 
-// fp8 cache kinds: one byte per element, a per-kv-head fp32 scale
-constexpr bool is_fp8(int ck) { return ck == kE4M3 || ck == kE5M2; }
+// one-byte codes with a per-kv-head fp32 scale: fp8 e4m3 / e5m2 and int8
+constexpr bool is_q8(int ck) { return ck == kE4M3 || ck == kE5M2 || ck == kI8; }
 
 // ---------------------------------------------------------------- append
 struct AppendParams {

@@ -18,13 +18,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 
 # dtype codes (pkv.h)
-F16, BF16, E4M3, U3, U8, I32, I64, F32, E5M2 = 1, 2, 3, 4, 5, 6, 7, 8, 9
+F16, BF16, E4M3, U3, U8, I32, I64, F32, E5M2, I8 = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 # device error bits
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE, DEVERR_POS_RANGE, DEVERR_TIMEOUT = (
     1, 2, 4, 8, 16)
 
 _TORCH_CODES = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3,
-                torch.float8_e5m2: E5M2,
+                torch.float8_e5m2: E5M2, torch.int8: I8,
                 torch.uint8: U8, torch.int32: I32, torch.int64: I64, torch.float32: F32}
 
 
@@ -130,7 +130,7 @@ def _need_cuda(*ts):
 @dataclass
 class KVCache:
     """A paged KV cache [num_blocks, block_size, num_kv_heads, row] in device
-    memory.  kind: "f16", "bf16", "e4m3" / "e5m2" (+ per-kv-head fp32 scales) or "u3"
+    memory.  kind: "f16", "bf16", "e4m3" / "e5m2" / "i8" (+ per-kv-head fp32 scales) or "u3"
     (3-bit codes, row = 3*head_dim/8 bytes, + fp16 scale / uint8 zero per
     (slot, head))."""
     kind: str
@@ -169,8 +169,9 @@ class KVCache:
             k = torch.empty(shape + (head_dim,), dtype=dt, device=device)
             v = torch.empty_like(k)
             c = KVCache(kind, k, v)
-        elif kind in ("e4m3", "e5m2"):
-            k = torch.empty(shape + (head_dim,), dtype=torch.uint8, device=device)
+        elif kind in ("e4m3", "e5m2", "i8"):
+            k = torch.empty(shape + (head_dim,), dtype=torch.int8 if kind == "i8" else torch.uint8,
+                            device=device)
             v = torch.empty_like(k)
             c = KVCache(kind, k, v, k_scale=k_scale, v_scale=v_scale)
         elif kind == "u3":
@@ -203,12 +204,12 @@ class KVCache:
 
     def _build_struct(self) -> _Cache:
         s = _Cache()
-        code = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2, "u3": U3}[self.kind]
+        code = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2, "i8": I8, "u3": U3}[self.kind]
         s.k_cache = _desc(self.k_cache, code)
         s.v_cache = _desc(self.v_cache, code)
-        if self.kind in ("e4m3", "e5m2"):
+        if self.kind in ("e4m3", "e5m2", "i8"):
             if self.k_scale is None or self.v_scale is None:
-                raise ValueError("fp8 cache needs k_scale / v_scale")
+                raise ValueError("fp8 / int8 cache needs k_scale / v_scale")
             s.k_scale = self.k_scale.data_ptr()
             s.v_scale = self.v_scale.data_ptr()
         if self.kind == "u3":

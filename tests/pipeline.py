@@ -9,7 +9,7 @@ import torch
 
 import workloads as W
 
-KIND_CODE_ORACLE = {"f16": 1, "bf16": 2, "e4m3": 3, "u3": 4, "e5m2": 9}
+KIND_CODE_ORACLE = {"f16": 1, "bf16": 2, "e4m3": 3, "u3": 4, "e5m2": 9, "i8": 10}
 
 
 def src_code(w):
@@ -67,7 +67,7 @@ def gpu_cache_host(cache):
         if t is not None:
             t = t.cpu().contiguous()
             d[name] = t.view(torch.int16).numpy().view(np.uint16) if t.element_size() == 2 \
-                else t.view(torch.uint8).numpy()
+                else t.numpy() if t.dtype == torch.int8 else t.view(torch.uint8).numpy()
     return d
 
 
@@ -83,9 +83,10 @@ def oracle_caches(w, orc, seqs=None):
     if kind in ("f16", "bf16"):
         c["k_cache"] = W.bits16(w.k_cache0).copy()
         c["v_cache"] = W.bits16(w.v_cache0).copy()
-    elif kind in ("e4m3", "e5m2"):
-        c["k_cache"] = np.zeros((P, BS, H, D), np.uint8)
-        c["v_cache"] = np.zeros((P, BS, H, D), np.uint8)
+    elif kind in ("e4m3", "e5m2", "i8"):
+        dt = np.int8 if kind == "i8" else np.uint8
+        c["k_cache"] = np.zeros((P, BS, H, D), dt)
+        c["v_cache"] = np.zeros((P, BS, H, D), dt)
     else:
         c["k_cache"] = np.zeros((P, BS, H, 3 * D // 8), np.uint8)
         c["v_cache"] = np.zeros((P, BS, H, 3 * D // 8), np.uint8)

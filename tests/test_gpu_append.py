@@ -123,11 +123,12 @@ def test_idempotent_append(pkv):
 
 
 @pytest.mark.parametrize("src,fp8", [(torch.bfloat16, "e4m3"), (torch.float16, "e4m3"),
-                                     (torch.bfloat16, "e5m2"), (torch.float16, "e5m2")])
+                                     (torch.bfloat16, "e5m2"), (torch.float16, "e5m2"),
+                                     (torch.bfloat16, "i8"), (torch.float16, "i8")])
 def test_fp8_every_source_pattern(pkv, orc, src, fp8):
     """All 2^16 source bit patterns (NaN, inf, subnormal, overflow included)
-    through the fp8 append (e4m3 and e5m2) for several scales: bit exact
-    with the oracle, which encodes from the formats' definitions."""
+    through the one-byte appends (e4m3, e5m2, int8) for several scales: bit
+    exact with the oracle, which encodes from the formats' definitions."""
     H, D, BS = 4, 128, 16
     pats = torch.arange(1 << 16, dtype=torch.int32).to(torch.int16).view(src)
     T = (1 << 16) // D                        # 512 tokens, one head row each x 4 heads
@@ -141,8 +142,8 @@ def test_fp8_every_source_pattern(pkv, orc, src, fp8):
     slots = torch.randperm(P * BS, generator=torch.Generator().manual_seed(3))[:T]
     pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache)
     torch.cuda.synchronize()
-    kc = np.zeros((P, BS, H, D), np.uint8)
-    vc = np.zeros((P, BS, H, D), np.uint8)
+    kc = np.zeros((P, BS, H, D), np.int8 if fp8 == "i8" else np.uint8)
+    vc = np.zeros_like(kc)
     code = 1 if src == torch.float16 else 2
     orc.kv_append(PL.KIND_CODE_ORACLE[fp8], code, W.bits16(kn), W.bits16(vn), slots.numpy(), kc, vc,
                   k_scale.numpy(), v_scale.numpy())

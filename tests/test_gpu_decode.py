@@ -72,11 +72,12 @@ def test_fp8_small(pkv, orc, splits):
     _check(w, out, PL.oracle_decode(w, orc, oc))
 
 
+@pytest.mark.parametrize("kind", ["e5m2", "i8"])
 @pytest.mark.parametrize("splits", [0, 1, 4])
-def test_e5m2_small(pkv, orc, splits):
-    """e5m2 cache: append bit exact, decode (fast path and split general
-    kernel) against the fp64 oracle on the oracle's own cache."""
-    w = W.fp8_long(batch=4, ctx_lo=20, ctx_hi=700, calib_tokens=64, seed=98, fp8="e5m2")
+def test_e5m2_i8_small(pkv, orc, splits, kind):
+    """e5m2 and int8 caches: append bit exact, decode (fast path and split
+    general kernel) against the fp64 oracle on the oracle's own cache."""
+    w = W.fp8_long(batch=4, ctx_lo=20, ctx_hi=700, calib_tokens=64, seed=98, fp8=kind)
     cache, out = PL.gpu_run(w, pkv, num_splits=splits)
     oc = PL.oracle_caches(w, orc)
     gc = PL.gpu_cache_host(cache)
@@ -308,6 +309,17 @@ def test_full_fp8_long_e5m2_sampled(pkv, orc):
     seqs = [0, 15]
     oc = PL.oracle_caches(w, orc, seqs=seqs)
     pairs = _sample_pairs(w, seqs, heads_per_seq=range(0, w.num_heads, 5))
+    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+
+
+def test_full_i8_long_sampled(pkv, orc):
+    """The long-context shape with an int8 cache (scales amax/127): sampled
+    sequences against the oracle."""
+    w = W.fp8_long(seed=W.SEEDS["i8_long"], fp8="i8")
+    cache, out = PL.gpu_run(w, pkv)
+    seqs = [3, 12]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    pairs = _sample_pairs(w, seqs, heads_per_seq=range(1, w.num_heads, 5))
     _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
 
 
