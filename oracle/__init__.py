@@ -28,6 +28,8 @@ _lib = None
 
 # dtype codes of the oracle's own interface
 F16, BF16, E4M3, U3, E5M2, I8 = 1, 2, 3, 4, 9, 10
+# scale granularity of fp8 / int8 caches
+SCALE_PER_HEAD, SCALE_PER_BLOCK, SCALE_PER_TOKEN = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -73,6 +75,10 @@ def _load():
         lib.pkvo_paged_decode.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P, i64, P,
                                           i32, P, dbl, P, P, P, P, P, P, P, i64, P, i32]
         lib.pkvo_paged_decode.restype = i64
+        lib.pkvo_kv_append_scaled.argtypes = lib.pkvo_kv_append.argtypes + [i32, P, P, P, P]
+        lib.pkvo_kv_append_scaled.restype = i64
+        lib.pkvo_paged_decode_scaled.argtypes = lib.pkvo_paged_decode.argtypes + [i32, P, P]
+        lib.pkvo_paged_decode_scaled.restype = i64
         lib.pkvo_max_threads.restype = i32
         for fn in ("pkvo_f32_to_e4m3_n", "pkvo_f32_to_f16_n", "pkvo_f16_to_f64_n",
                    "pkvo_bf16_to_f64_n", "pkvo_e4m3_to_f64_n", "pkvo_f32_to_e5m2_n",
@@ -205,12 +211,16 @@ def build_slot_mapping(block_tables: np.ndarray, req: np.ndarray, pos: np.ndarra
 
 def kv_append(cache_dtype: int, src_dtype: int, k_new, v_new, slot_mapping, k_cache, v_cache,
               k_scale=None, v_scale=None, k_qscale=None, k_qzero=None, v_qscale=None,
-              v_qzero=None) -> int:
+              v_qzero=None, scale_mode: int = SCALE_PER_HEAD, k_new_scale=None, v_new_scale=None,
+              k_scales=None, v_scales=None) -> int:
     """Scatter new rows into the (host, contiguous) cache arrays in place.
 
     k_new/v_new: uint16 bits [T, Hkv, D]; caches: [P, BS, Hkv, row] uint16 or
-    uint8; 3-bit metadata: [P, BS, Hkv].  Returns the count of out-of-range
-    slots (skipped)."""
+    uint8; 3-bit metadata: [P, BS, Hkv].  fp8 / int8 scales: per head
+    (k_scale / v_scale [Hkv]), per block (k_scales / v_scales [P, Hkv]) or
+    per token (k_new_scale / v_new_scale [T, Hkv], stored into k_scales /
+    v_scales [P, BS, Hkv]).  Returns the count of out-of-range slots
+    (skipped)."""
     k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
     v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
@@ -220,16 +230,21 @@ def kv_append(cache_dtype: int, src_dtype: int, k_new, v_new, slot_mapping, k_ca
         assert a is None or a.flags["C_CONTIGUOUS"]
     ks = None if k_scale is None else np.ascontiguousarray(k_scale, dtype=np.float32)
     vs = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
-    return int(_load().pkvo_kv_append(
+    kns = None if k_new_scale is None else np.ascontiguousarray(k_new_scale, dtype=np.float32)
+    vns = None if v_new_scale is None else np.ascontiguousarray(v_new_scale, dtype=np.float32)
+    for a in (k_scales, v_scales):
+        assert a is None or (a.dtype == np.float32 and a.flags["C_CONTIGUOUS"])
+    return int(_load().pkvo_kv_append_scaled(
         cache_dtype, src_dtype, T, Hkv, D, _ptr(k_new), _ptr(v_new), _ptr(sm), P, BS,
         _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs), _ptr(k_qscale), _ptr(k_qzero),
-        _ptr(v_qscale), _ptr(v_qzero)))
+        _ptr(v_qscale), _ptr(v_qzero), int(scale_mode), _ptr(kns), _ptr(vns), _ptr(k_scales),
+        _ptr(v_scales)))
 
 
 def paged_decode(cache_dtype: int, q_dtype: int, q, k_cache, v_cache, block_tables,
                  context_lens, block_size: int, sm_scale: float, k_scale=None, v_scale=None,
                  k_qscale=None, k_qzero=None, v_qscale=None, v_qzero=None, pairs=None,
-                 nthreads: int = 1):
+                 nthreads: int = 1, scale_mode: int = SCALE_PER_HEAD, k_scales=None, v_scales=None):
     """fp64 paged attention decode.  q: uint16 bits [B, Hq, D].  Returns
     (out float64 [B, Hq, D], bad_rows).  With ``pairs`` (flattened b*Hq+h)
     only those rows are computed; the others are NaN."""
@@ -244,9 +259,12 @@ def paged_decode(cache_dtype: int, q_dtype: int, q, k_cache, v_cache, block_tabl
     vs = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
     for a in (k_cache, v_cache):
         assert a.flags["C_CONTIGUOUS"]
-    bad = _load().pkvo_paged_decode(
+    kss = None if k_scales is None else np.ascontiguousarray(k_scales, dtype=np.float32)
+    vss = None if v_scales is None else np.ascontiguousarray(v_scales, dtype=np.float32)
+    bad = _load().pkvo_paged_decode_scaled(
         cache_dtype, q_dtype, B, Hq, Hkv, D, block_size, _ptr(q), _ptr(k_cache), _ptr(v_cache),
         k_cache.shape[0], _ptr(bt), bt.shape[1], _ptr(cl), float(sm_scale), _ptr(ks), _ptr(vs),
         _ptr(k_qscale), _ptr(k_qzero), _ptr(v_qscale), _ptr(v_qzero), _ptr(pr),
-        0 if pr is None else pr.shape[0], _ptr(out), int(nthreads))
+        0 if pr is None else pr.shape[0], _ptr(out), int(nthreads), int(scale_mode), _ptr(kss),
+        _ptr(vss))
     return out, int(bad)

@@ -35,6 +35,13 @@
  *     bits, infinities and NaNs at exponent 31, max 57344); encoding rounds
  *     to nearest even and saturates finite overflow and infinities to
  *     +-57344, like e4m3; every NaN encodes to 0x7F.
+ *   - scale granularity of fp8 / int8 caches (inputs item 4: per tensor,
+ *     per token, per head or per block): a row's scale is the kv head's
+ *     (per head; per tensor is equal per-head scales), the physical block's
+ *     scale for that head ([num_blocks, num_kv_heads]), or the row's own
+ *     scale ([num_blocks, block_size, num_kv_heads], per token: the append
+ *     takes each new token's scale per kv head from the caller and stores it
+ *     at the token's slot).
  *   - int8 caches ("Write Triton Kv Cache Append Kernel", inputs item 4 and
  *     reasoning step 6: (x / scale) cast to the cache dtype) store
  *     clamp(rint(x / scale), -127, 127) with x / scale in fp32 and rint
@@ -379,12 +386,32 @@ void pkvo_build_slot_mapping(const int32_t *block_tables, int max_blocks, int bl
  * New K/V are contiguous [num_tokens, num_kv_heads, head_dim] 16-bit bits.
  * Tokens are applied in order (a duplicated slot keeps the last write).
  * Returns the number of tokens whose slot was out of range (skipped). */
-int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int num_kv_heads,
-                       int head_dim, const uint16_t *k_new, const uint16_t *v_new,
-                       const int64_t *slot_mapping, int64_t num_blocks, int block_size,
-                       void *k_cache, void *v_cache, const float *k_scale,
-                       const float *v_scale, uint16_t *k_qscale, uint8_t *k_qzero,
-                       uint16_t *v_qscale, uint8_t *v_qzero)
+/* Scale of cache row (blk, off, h) for fp8 / int8 caches, by granularity. */
+#define SCALE_PER_HEAD 0
+#define SCALE_PER_BLOCK 1
+#define SCALE_PER_TOKEN 2
+static double row_scale(int mode, const float *per_head, const float *arr, int64_t blk, int64_t off,
+                        int h, int num_kv_heads, int block_size)
+{
+    if (mode == SCALE_PER_BLOCK)
+        return arr[blk * num_kv_heads + h];
+    if (mode == SCALE_PER_TOKEN)
+        return arr[(blk * block_size + off) * num_kv_heads + h];
+    return per_head ? per_head[h] : 1.0;
+}
+
+/* The append with a scale granularity: per head (k_scale / v_scale),
+ * per block (k_scales / v_scales [num_blocks, Hkv], read), or per token
+ * (k_new_scale / v_new_scale [num_tokens, Hkv] given with the new rows and
+ * stored into k_scales / v_scales [num_blocks, block_size, Hkv]). */
+int64_t pkvo_kv_append_scaled(int cache_dtype, int src_dtype, int64_t num_tokens, int num_kv_heads,
+                              int head_dim, const uint16_t *k_new, const uint16_t *v_new,
+                              const int64_t *slot_mapping, int64_t num_blocks, int block_size,
+                              void *k_cache, void *v_cache, const float *k_scale,
+                              const float *v_scale, uint16_t *k_qscale, uint8_t *k_qzero,
+                              uint16_t *v_qscale, uint8_t *v_qzero, int scale_mode,
+                              const float *k_new_scale, const float *v_new_scale, float *k_scales,
+                              float *v_scales)
 {
     int64_t bad = 0;
     const int D = head_dim;
@@ -401,6 +428,20 @@ int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int n
             int64_t row = (blk * block_size + off) * num_kv_heads + h; /* row index */
             const uint16_t *ks = k_new + (t * num_kv_heads + h) * D;
             const uint16_t *vs = v_new + (t * num_kv_heads + h) * D;
+            float ksc = 1.0f, vsc = 1.0f;             /* the row's fp8 / int8 scales */
+            if (scale_mode == SCALE_PER_TOKEN && (cache_dtype == O_E4M3 || cache_dtype == O_E5M2 ||
+                                                  cache_dtype == O_I8)) {
+                ksc = k_new_scale[t * num_kv_heads + h];
+                vsc = v_new_scale[t * num_kv_heads + h];
+                k_scales[row] = ksc;
+                v_scales[row] = vsc;
+            } else if (scale_mode == SCALE_PER_BLOCK) {
+                ksc = k_scales[blk * num_kv_heads + h];
+                vsc = v_scales[blk * num_kv_heads + h];
+            } else if (k_scale) {
+                ksc = k_scale[h];
+                vsc = v_scale[h];
+            }
             if (cache_dtype == O_F16 || cache_dtype == O_BF16) {
                 memcpy((uint16_t *)k_cache + row * D, ks, (size_t)D * 2);
                 memcpy((uint16_t *)v_cache + row * D, vs, (size_t)D * 2);
@@ -408,8 +449,8 @@ int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int n
                 int8_t *kd = (int8_t *)k_cache + row * D;
                 int8_t *vd = (int8_t *)v_cache + row * D;
                 for (int d = 0; d < D; ++d) {
-                    float xk = (float)elem16_to_f64(ks[d], src_dtype) / k_scale[h];
-                    float xv = (float)elem16_to_f64(vs[d], src_dtype) / v_scale[h];
+                    float xk = (float)elem16_to_f64(ks[d], src_dtype) / ksc;
+                    float xv = (float)elem16_to_f64(vs[d], src_dtype) / vsc;
                     kd[d] = pkvo_f32_to_i8(xk);
                     vd[d] = pkvo_f32_to_i8(xv);
                 }
@@ -418,8 +459,8 @@ int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int n
                 uint8_t *vd = (uint8_t *)v_cache + row * D;
                 for (int d = 0; d < D; ++d) {
                     /* scale division in fp32, then the cast */
-                    float xk = (float)elem16_to_f64(ks[d], src_dtype) / k_scale[h];
-                    float xv = (float)elem16_to_f64(vs[d], src_dtype) / v_scale[h];
+                    float xk = (float)elem16_to_f64(ks[d], src_dtype) / ksc;
+                    float xv = (float)elem16_to_f64(vs[d], src_dtype) / vsc;
                     kd[d] = cache_dtype == O_E4M3 ? pkvo_f32_to_e4m3(xk) : pkvo_f32_to_e5m2(xk);
                     vd[d] = cache_dtype == O_E4M3 ? pkvo_f32_to_e4m3(xv) : pkvo_f32_to_e5m2(xv);
                 }
@@ -433,6 +474,19 @@ int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int n
         }
     }
     return bad;
+}
+
+int64_t pkvo_kv_append(int cache_dtype, int src_dtype, int64_t num_tokens, int num_kv_heads,
+                       int head_dim, const uint16_t *k_new, const uint16_t *v_new,
+                       const int64_t *slot_mapping, int64_t num_blocks, int block_size,
+                       void *k_cache, void *v_cache, const float *k_scale,
+                       const float *v_scale, uint16_t *k_qscale, uint8_t *k_qzero,
+                       uint16_t *v_qscale, uint8_t *v_qzero)
+{
+    return pkvo_kv_append_scaled(cache_dtype, src_dtype, num_tokens, num_kv_heads, head_dim, k_new,
+                                 v_new, slot_mapping, num_blocks, block_size, k_cache, v_cache,
+                                 k_scale, v_scale, k_qscale, k_qzero, v_qscale, v_qzero,
+                                 SCALE_PER_HEAD, NULL, NULL, NULL, NULL);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -466,14 +520,15 @@ static double cache_elem(int cache_dtype, const void *cache, int64_t row, int D,
  * b*num_heads + h rows to compute; other rows of `out` are left untouched.
  * Returns the number of rows that met an out-of-range block id or context
  * length (those rows are set to NaN). */
-int64_t pkvo_paged_decode(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, int D, int BS,
-                          const uint16_t *q, const void *k_cache, const void *v_cache,
-                          int64_t num_blocks, const int32_t *block_tables, int max_blocks,
-                          const int32_t *context_lens, double sm_scale, const float *k_scale,
-                          const float *v_scale, const uint16_t *k_qscale,
-                          const uint8_t *k_qzero, const uint16_t *v_qscale,
-                          const uint8_t *v_qzero, const int32_t *pairs, int64_t n_pairs,
-                          double *out, int nthreads)
+int64_t pkvo_paged_decode_scaled(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, int D, int BS,
+                                 const uint16_t *q, const void *k_cache, const void *v_cache,
+                                 int64_t num_blocks, const int32_t *block_tables, int max_blocks,
+                                 const int32_t *context_lens, double sm_scale, const float *k_scale,
+                                 const float *v_scale, const uint16_t *k_qscale,
+                                 const uint8_t *k_qzero, const uint16_t *v_qscale,
+                                 const uint8_t *v_qzero, const int32_t *pairs, int64_t n_pairs,
+                                 double *out, int nthreads, int scale_mode, const float *k_scales,
+                                 const float *v_scales)
 {
     int64_t n_rows = pairs ? n_pairs : (int64_t)B * Hq;
     int64_t bad = 0;
@@ -503,8 +558,6 @@ int64_t pkvo_paged_decode(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, 
         double qd[1024];
         for (int d = 0; d < D; ++d)
             qd[d] = elem16_to_f64(q[bh * D + d], q_dtype);
-        double ks = k_scale ? (double)k_scale[kvh] : 1.0;
-        double vs = v_scale ? (double)v_scale[kvh] : 1.0;
         /* pass 1: scores and their maximum */
         double *score = (double *)malloc(sizeof(double) * (size_t)ctx);
         double m = -INFINITY;
@@ -516,6 +569,7 @@ int64_t pkvo_paged_decode(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, 
                 break;
             }
             int64_t row = ((int64_t)pb * BS + t % BS) * Hkv + kvh;
+            double ks = row_scale(scale_mode, k_scale, k_scales, pb, t % BS, kvh, Hkv, BS);
             double acc = 0.0;
             for (int d = 0; d < D; ++d)
                 acc += qd[d] * cache_elem(cache_dtype, k_cache, row, D, d, ks, k_qscale, k_qzero);
@@ -537,6 +591,7 @@ int64_t pkvo_paged_decode(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, 
         for (int t = 0; t < ctx; ++t) {
             int32_t pb = block_tables[(int64_t)b * max_blocks + t / BS];
             int64_t row = ((int64_t)pb * BS + t % BS) * Hkv + kvh;
+            double vs = row_scale(scale_mode, v_scale, v_scales, pb, t % BS, kvh, Hkv, BS);
             double p = exp(score[t] - m);
             l += p;
             for (int d = 0; d < D; ++d)
@@ -547,6 +602,21 @@ int64_t pkvo_paged_decode(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, 
         free(score);
     }
     return bad;
+}
+
+int64_t pkvo_paged_decode(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, int D, int BS,
+                          const uint16_t *q, const void *k_cache, const void *v_cache,
+                          int64_t num_blocks, const int32_t *block_tables, int max_blocks,
+                          const int32_t *context_lens, double sm_scale, const float *k_scale,
+                          const float *v_scale, const uint16_t *k_qscale,
+                          const uint8_t *k_qzero, const uint16_t *v_qscale,
+                          const uint8_t *v_qzero, const int32_t *pairs, int64_t n_pairs,
+                          double *out, int nthreads)
+{
+    return pkvo_paged_decode_scaled(cache_dtype, q_dtype, B, Hq, Hkv, D, BS, q, k_cache, v_cache,
+                                    num_blocks, block_tables, max_blocks, context_lens, sm_scale,
+                                    k_scale, v_scale, k_qscale, k_qzero, v_qscale, v_qzero, pairs,
+                                    n_pairs, out, nthreads, SCALE_PER_HEAD, NULL, NULL);
 }
 
 int pkvo_max_threads(void)

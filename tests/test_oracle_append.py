@@ -2,6 +2,7 @@
 Cache Append Kernel": reasoning steps 5, 6 and 9; correctness requirements;
 output format item 4).  CPU only."""
 import numpy as np
+import pytest
 import torch
 
 import workloads as W
@@ -194,3 +195,55 @@ def test_scatter_u3_rows_and_metadata(orc):
     mask = np.ones(P * BS, bool)
     mask[slots[real]] = False
     assert not kc.reshape(P * BS, H, RB)[mask].any() and not ks.reshape(P * BS, H)[mask].any()
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "i8"])
+def test_scatter_per_token_and_per_block_scales(orc, kind):
+    """Scale granularities: per block, each row quantised with its block's
+    scale for its head; per token, with the scale given for that token and
+    head, which is stored at the token's slot.  Codes are checked against
+    the per-row cast / round of x / scale, and equal-valued block or token
+    scales reproduce the per-head cache exactly."""
+    P, BS, H, D, T, k0, v0, kn, vn, slots = _scatter_case(orc, torch.bfloat16, seed=5)
+    code = orc.E4M3 if kind == "e4m3" else orc.I8
+    dt = np.uint8 if kind == "e4m3" else np.int8
+    g = np.random.default_rng(6)
+    real = slots >= 0
+    rows = slots[real]                      # slot of each real token
+
+    def cast(x):                            # x: torch float32
+        if kind == "e4m3":
+            return x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        return x.round().clamp(-127, 127).to(torch.int8).numpy()
+
+    # per block
+    kb = (g.random((P, H)) * 0.02 + 0.002).astype(np.float32)
+    vb = (g.random((P, H)) * 0.02 + 0.002).astype(np.float32)
+    kc, vc = np.zeros((P, BS, H, D), dt), np.zeros((P, BS, H, D), dt)
+    orc.kv_append(code, orc.BF16, W.bits16(kn), W.bits16(vn), slots, kc, vc,
+                  scale_mode=orc.SCALE_PER_BLOCK, k_scales=kb, v_scales=vb)
+    for cache, src, sc in ((kc, kn, kb), (vc, vn, vb)):
+        x = src[torch.from_numpy(real)].float() / torch.from_numpy(sc[rows // BS])[:, :, None]
+        assert np.array_equal(cache.reshape(P * BS, H, D)[rows], cast(x))
+    # per token: scales given per new token, stored at its slot
+    kt = (g.random((T, H)) * 0.02 + 0.002).astype(np.float32)
+    vt = (g.random((T, H)) * 0.02 + 0.002).astype(np.float32)
+    ks_arr, vs_arr = np.zeros((P, BS, H), np.float32), np.zeros((P, BS, H), np.float32)
+    kc, vc = np.zeros((P, BS, H, D), dt), np.zeros((P, BS, H, D), dt)
+    orc.kv_append(code, orc.BF16, W.bits16(kn), W.bits16(vn), slots, kc, vc,
+                  scale_mode=orc.SCALE_PER_TOKEN, k_new_scale=kt, v_new_scale=vt,
+                  k_scales=ks_arr, v_scales=vs_arr)
+    assert np.array_equal(ks_arr.reshape(P * BS, H)[rows], kt[real])
+    assert np.array_equal(vs_arr.reshape(P * BS, H)[rows], vt[real])
+    for cache, src, sc in ((kc, kn, kt), (vc, vn, vt)):
+        x = src[torch.from_numpy(real)].float() / torch.from_numpy(sc[real])[:, :, None]
+        assert np.array_equal(cache.reshape(P * BS, H, D)[rows], cast(x))
+    # equal-valued granular scales == per-head scales
+    hs = np.array([0.01, 0.004, 0.02], np.float32)
+    ref_k, ref_v = np.zeros((P, BS, H, D), dt), np.zeros((P, BS, H, D), dt)
+    orc.kv_append(code, orc.BF16, W.bits16(kn), W.bits16(vn), slots, ref_k, ref_v, hs, hs)
+    kc, vc = np.zeros((P, BS, H, D), dt), np.zeros((P, BS, H, D), dt)
+    orc.kv_append(code, orc.BF16, W.bits16(kn), W.bits16(vn), slots, kc, vc,
+                  scale_mode=orc.SCALE_PER_BLOCK, k_scales=np.tile(hs, (P, 1)),
+                  v_scales=np.tile(hs, (P, 1)))
+    assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)

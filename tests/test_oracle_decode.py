@@ -241,3 +241,46 @@ def test_appended_token_is_attended_at_last_position(orc):
                            torch.from_numpy(vc.view(np.float16)), w.block_tables.numpy(),
                            w.context_lens.numpy(), w.block_size, w.sm_scale)
     assert np.max(np.abs(out - ref)) < 1e-12
+
+
+@pytest.mark.parametrize("mode", ["block", "token"])
+def test_granular_scale_decode_on_dequantised_cache(orc, mode):
+    """fp8 decode with per-block or per-token scales equals fp64 attention
+    on the cache dequantised independently with each row's own scale."""
+    w = W.fp8_long(batch=3, ctx_lo=40, ctx_hi=150, calib_tokens=64, seed=18)
+    P, BS, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+    g = np.random.default_rng(19)
+    req = np.concatenate([w.fill_req.numpy(), w.new_req.numpy()])
+    pos = np.concatenate([w.fill_pos.numpy(), w.new_pos.numpy()])
+    kn = np.concatenate([W.bits16(w.k_fill), W.bits16(w.k_new)])
+    vn = np.concatenate([W.bits16(w.v_fill), W.bits16(w.v_new)])
+    slots = orc.build_slot_mapping(w.block_tables.numpy(), req, pos, BS)
+    kc, vc = np.zeros((P, BS, H, D), np.uint8), np.zeros((P, BS, H, D), np.uint8)
+    if mode == "block":
+        ks = (g.random((P, H)) * 0.01 + 0.003).astype(np.float32)
+        vs = (g.random((P, H)) * 0.01 + 0.003).astype(np.float32)
+        orc.kv_append(orc.E4M3, orc.BF16, kn, vn, slots, kc, vc, scale_mode=orc.SCALE_PER_BLOCK,
+                      k_scales=ks, v_scales=vs)
+        krow = np.repeat(ks[:, None, :], BS, axis=1)          # [P, BS, H]
+        vrow = np.repeat(vs[:, None, :], BS, axis=1)
+        sm = orc.SCALE_PER_BLOCK
+    else:
+        T = len(slots)
+        ks = np.zeros((P, BS, H), np.float32)
+        vs = np.zeros((P, BS, H), np.float32)
+        kt = (g.random((T, H)) * 0.01 + 0.003).astype(np.float32)
+        vt = (g.random((T, H)) * 0.01 + 0.003).astype(np.float32)
+        orc.kv_append(orc.E4M3, orc.BF16, kn, vn, slots, kc, vc, scale_mode=orc.SCALE_PER_TOKEN,
+                      k_new_scale=kt, v_new_scale=vt, k_scales=ks, v_scales=vs)
+        krow, vrow = ks, vs
+        sm = orc.SCALE_PER_TOKEN
+    out, bad = orc.paged_decode(orc.E4M3, orc.BF16, W.bits16(w.q), kc, vc, w.block_tables.numpy(),
+                                w.context_lens.numpy(), BS, w.sm_scale, scale_mode=sm,
+                                k_scales=ks, v_scales=vs)
+    assert bad == 0
+    one = np.ones(H)
+    kd = e4m3_dequant(kc, one) * krow[..., None].astype(np.float64)
+    vd = e4m3_dequant(vc, one) * vrow[..., None].astype(np.float64)
+    ref = gather_attention(w.q, kd, vd, w.block_tables.numpy(), w.context_lens.numpy(), BS,
+                           w.sm_scale)
+    assert np.max(np.abs(out - ref)) < 1e-12
