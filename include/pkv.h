@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 /* Element types. */
 enum {
@@ -103,8 +103,10 @@ typedef struct pkv_tensor {
  *     aligned; the block stride must be a multiple of 16 bytes, and for
  *     F16/BF16/E4M3 also the slot and head strides.  K and V must have the
  *     same dtype, shape and strides.
- *   k_scale, v_scale : E4M3, E5M2 and I8 only, device fp32 [num_kv_heads],
- *     > 0.  A stored code c means fp8(c) * scale, or c * scale for I8.
+ *   k_scale, v_scale : E4M3, E5M2 and I8 with scale_mode PER_HEAD, device
+ *     fp32 [num_kv_heads], > 0.  A stored code c means fp8(c) * scale, or
+ *     c * scale for I8, with the scale of the row's granularity (see
+ *     PKV_SCALE_*).
  *   k_qscale, v_qscale (F16) and k_qzero, v_qzero (U8), U3 only:
  *     [num_blocks, block_size, num_kv_heads]; a stored code u means
  *     (u - zero) * scale for its (slot, head) row.  Any strides are
@@ -115,6 +117,17 @@ typedef struct pkv_tensor {
  *     slot-major (head stride 1, slot stride num_kv_heads) also takes the
  *     persistent kernel; other layouts take the general one.
  */
+/* Scale granularity of E4M3 / E5M2 / I8 caches ("Write Triton Kv Cache
+ * Append Kernel", inputs items 4 and 8: per tensor, per token, per head or
+ * per block; a per-tensor scale is a per-head scale equal for every head). */
+enum {
+    PKV_SCALE_PER_HEAD = 0,  /* k_scale / v_scale: fp32 [num_kv_heads] */
+    PKV_SCALE_PER_BLOCK = 1, /* k_scales / v_scales: F32 [num_blocks, num_kv_heads] */
+    PKV_SCALE_PER_TOKEN = 2  /* k_scales / v_scales: F32 [num_blocks, block_size,
+                                num_kv_heads], one per cached row; written by
+                                pkv_kv_append_scaled from the new tokens' scales */
+};
+
 typedef struct pkv_cache {
     pkv_tensor k_cache;
     pkv_tensor v_cache;
@@ -124,6 +137,12 @@ typedef struct pkv_cache {
     pkv_tensor k_qzero;
     pkv_tensor v_qscale;
     pkv_tensor v_qzero;
+    /* ABI 2: scale granularity of E4M3 / E5M2 / I8 caches (PKV_SCALE_*; 0 =
+     * per head, the ABI-1 behaviour) and the per-block / per-token scale
+     * arrays (any strides, the same for K and V; positive values). */
+    int32_t scale_mode;
+    pkv_tensor k_scales;
+    pkv_tensor v_scales;
 } pkv_cache;
 
 /* Library version string and ABI version. */
@@ -196,6 +215,21 @@ int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req,
 int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new,
                   const pkv_tensor *slot_mapping, const pkv_cache *cache, int32_t *err_flag,
                   void *stream);
+
+/*
+ * pkv_kv_append_scaled -- pkv_kv_append for caches with per-token scales
+ * (scale_mode PKV_SCALE_PER_TOKEN; "load the appropriate scalar first",
+ * reasoning step 6): each new row is divided by its own scale, and the
+ * scale is stored at the token's slot in cache->k_scales / v_scales for
+ * decode.
+ *   k_new_scale, v_new_scale : F32 [num_tokens, num_kv_heads], > 0, any
+ *                              strides; rows of padding tokens are not read.
+ * Everything else as pkv_kv_append (which rejects per-token caches).
+ */
+int pkv_kv_append_scaled(const pkv_tensor *k_new, const pkv_tensor *v_new,
+                         const pkv_tensor *k_new_scale, const pkv_tensor *v_new_scale,
+                         const pkv_tensor *slot_mapping, const pkv_cache *cache, int32_t *err_flag,
+                         void *stream);
 
 /*
  * pkv_paged_decode -- paged attention for one query token per sequence

@@ -5,9 +5,9 @@ include/pkv.h); ``pkv`` is its ctypes binding.  Build with
 ``paged_kv_cache_num_gb300.build.build()``.
 """
 from .pkv import (KVCache, PkvError, copy_peak, decode_step, decode_workspace_bytes, kv_append,
-                  lib, pack3, paged_decode, paged_decode_noalloc, slot_mapping, unpack3,
-                  unpack3_words, version)
+                  kv_append_scaled, lib, pack3, paged_decode, paged_decode_noalloc, slot_mapping,
+                  unpack3, unpack3_words, version)
 
 __all__ = ["KVCache", "PkvError", "copy_peak", "decode_step", "decode_workspace_bytes",
-           "kv_append", "lib", "pack3", "paged_decode", "paged_decode_noalloc", "slot_mapping",
+           "kv_append", "kv_append_scaled", "lib", "pack3", "paged_decode", "paged_decode_noalloc", "slot_mapping",
            "unpack3", "unpack3_words", "version"]

@@ -118,7 +118,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
                : p.k_new + t * p.k_src_tok + h * p.k_src_head) + 8 * c;
         uint8_t *dst = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
                                                    off * p.c_slot + h * p.c_head) + 8 * c;
-        const float scale = (kv ? p.v_scale : p.k_scale)[h];
+        float scale;
+        if (p.scale_mode == 0) {                // per kv head
+            scale = (kv ? p.v_scale : p.k_scale)[h];
+        } else if (p.scale_mode == 1) {         // the block's scale for this head
+            scale = (kv ? p.v_gs : p.k_gs)[blk * p.gs_blk + h * p.gs_head];
+        } else {                                // the token's own, kept at its slot
+            scale = (kv ? p.v_ns : p.k_ns)[t * p.ns_tok + h * p.ns_head];
+            if (c == 0) (kv ? p.v_gs : p.k_gs)[blk * p.gs_blk + off * p.gs_slot + h * p.gs_head] = scale;
+        }
         uint16_t e[8];
         if constexpr (VEC) {
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));

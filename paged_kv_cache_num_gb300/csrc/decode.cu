@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[g][e] = 0.0f;
     }
-    const float ks = is_q8(CK) ? p.k_scale[kvh] : 1.0f;
-    const float vs = is_q8(CK) ? p.v_scale[kvh] : 1.0f;
+    const float ks = is_q8(CK) && p.scale_mode == 0 ? p.k_scale[kvh] : 1.0f;
+    const float vs = is_q8(CK) && p.scale_mode == 0 ? p.v_scale[kvh] : 1.0f;
     const int bmask = (1 << p.block_shift) - 1;
 
     for (int t = t0 + warp; t < t1; t += kGenWarps) {
@@ -137,6 +137,12 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
         }
         const int64_t roff = pb * p.c_blk + off * p.c_slot + kvh * p.c_head;
         float kq = 1.0f, kz = 0.0f, vq = 1.0f, vz = 0.0f;
+        float kst = ks, vst = vs;             // the row's fp8 / int8 scales
+        if (is_q8(CK) && p.scale_mode != 0) {
+            const int64_t gi = pb * p.gs_blk + off * p.gs_slot + kvh * p.gs_head;
+            kst = p.k_gs[gi];
+            vst = p.v_gs[gi];
+        }
         if constexpr (CK == kU3) {
             kq = __half2float(__ushort_as_half(p.k_qs[pb * p.m_blk + off * p.m_slot + kvh * p.m_head]));
             vq = __half2float(__ushort_as_half(p.v_qs[pb * p.m_blk + off * p.m_slot + kvh * p.m_head]));
@@ -144,8 +150,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
             vz = float(p.v_qz[pb * p.z_blk + off * p.z_slot + kvh * p.z_head]);
         }
         float kx[EPL], vx[EPL];
-        load_row<CK, EPL>(p.k_cache + roff, EPL * lane, ks, kq, kz, kx);
-        load_row<CK, EPL>(p.v_cache + roff, EPL * lane, vs, vq, vz, vx);
+        load_row<CK, EPL>(p.k_cache + roff, EPL * lane, kst, kq, kz, kx);
+        load_row<CK, EPL>(p.v_cache + roff, EPL * lane, vst, vq, vz, vx);
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) {
             if (g < G) {

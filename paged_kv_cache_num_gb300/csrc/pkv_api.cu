@@ -78,6 +78,8 @@ int check_tensor(const pkv_tensor *t, const char *name, int ndim)
 struct CacheInfo {
     int kind;
     int64_t num_blocks, block_size, num_kv_heads, head_dim;
+    int scale_mode;                       // PKV_SCALE_* (fp8 / int8 caches)
+    int64_t gs_blk, gs_slot, gs_head;     // strides of the per-block / per-token scales
 };
 
 // Validate a pkv_cache; head_dim comes from the row length and the dtype.
@@ -119,8 +121,33 @@ int check_cache(const pkv_cache *c, CacheInfo &ci, bool any_block_size = false)
                     (long long)ci.block_size);
     if (ci.num_blocks * ci.block_size > (int64_t(1) << 31))
         return fail(PKV_ERR_UNSUPPORTED, "pool of more than 2^31 slots");
-    if (pkv::is_q8(kind) && (!c->k_scale || !c->v_scale))
+    ci.scale_mode = c->scale_mode;
+    if (c->scale_mode != PKV_SCALE_PER_HEAD && c->scale_mode != PKV_SCALE_PER_BLOCK &&
+        c->scale_mode != PKV_SCALE_PER_TOKEN)
+        return fail(PKV_ERR_VALUE, "scale_mode %d is not a PKV_SCALE_* value", c->scale_mode);
+    if (c->scale_mode != PKV_SCALE_PER_HEAD && !pkv::is_q8(kind))
+        return fail(PKV_ERR_UNSUPPORTED, "scale granularities apply to E4M3 / E5M2 / I8 caches");
+    if (pkv::is_q8(kind) && c->scale_mode == PKV_SCALE_PER_HEAD && (!c->k_scale || !c->v_scale))
         return fail(PKV_ERR_NULL, "fp8 / int8 cache needs k_scale and v_scale");
+    if (c->scale_mode != PKV_SCALE_PER_HEAD) {
+        const bool blk = c->scale_mode == PKV_SCALE_PER_BLOCK;
+        const int nd = blk ? 2 : 3;
+        TRY(check_tensor(&c->k_scales, "k_scales", nd));
+        TRY(check_tensor(&c->v_scales, "v_scales", nd));
+        if (c->k_scales.dtype != PKV_DTYPE_F32 || c->v_scales.dtype != PKV_DTYPE_F32)
+            return fail(PKV_ERR_DTYPE, "k_scales / v_scales must be F32");
+        const int64_t want[3] = {ci.num_blocks, blk ? ci.num_kv_heads : ci.block_size, ci.num_kv_heads};
+        for (int i = 0; i < nd; ++i) {
+            if (c->k_scales.shape[i] != want[i] || c->v_scales.shape[i] != want[i])
+                return fail(PKV_ERR_SHAPE, blk ? "per-block scales must be [num_blocks, num_kv_heads]"
+                                               : "per-token scales must be [num_blocks, block_size, num_kv_heads]");
+            if (c->k_scales.stride[i] != c->v_scales.stride[i])
+                return fail(PKV_ERR_LAYOUT, "k_scales and v_scales strides differ");
+        }
+        ci.gs_blk = c->k_scales.stride[0];
+        ci.gs_slot = blk ? 0 : c->k_scales.stride[1];
+        ci.gs_head = c->k_scales.stride[blk ? 1 : 2];
+    }
     if (kind == PKV_DTYPE_U3) {
         TRY(check_tensor(&c->k_qscale, "k_qscale", 3));
         TRY(check_tensor(&c->k_qzero, "k_qzero", 3));
@@ -221,7 +248,8 @@ int pkv_slot_mapping(const pkv_tensor *block_tables, const pkv_tensor *req, cons
 
 static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *slot_mapping,
                           const pkv_cache *cache, int32_t *err_flag, pkv::AppendParams &p, int &kind,
-                          bool &vec16)
+                          bool &vec16, const pkv_tensor *k_new_scale = nullptr,
+                          const pkv_tensor *v_new_scale = nullptr)
 {
     TRY(check_tensor(k_new, "k_new", 3));
     TRY(check_tensor(v_new, "v_new", 3));
@@ -270,6 +298,33 @@ static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, cons
     p.c_head = cache->k_cache.stride[2] * ces;
     p.k_scale = cache->k_scale;
     p.v_scale = cache->v_scale;
+    p.scale_mode = ci.scale_mode;
+    if (ci.scale_mode != PKV_SCALE_PER_HEAD) {
+        p.k_gs = static_cast<float *>(cache->k_scales.data);
+        p.v_gs = static_cast<float *>(cache->v_scales.data);
+        p.gs_blk = ci.gs_blk;
+        p.gs_slot = ci.gs_slot;
+        p.gs_head = ci.gs_head;
+    }
+    if (ci.scale_mode == PKV_SCALE_PER_TOKEN) {
+        if (!k_new_scale || !v_new_scale)
+            return fail(PKV_ERR_UNSUPPORTED, "a per-token-scale cache is appended with pkv_kv_append_scaled");
+        TRY(check_tensor(k_new_scale, "k_new_scale", 2));
+        TRY(check_tensor(v_new_scale, "v_new_scale", 2));
+        if (k_new_scale->dtype != PKV_DTYPE_F32 || v_new_scale->dtype != PKV_DTYPE_F32)
+            return fail(PKV_ERR_DTYPE, "k_new_scale / v_new_scale must be F32");
+        if (k_new_scale->shape[0] != T || v_new_scale->shape[0] != T ||
+            k_new_scale->shape[1] != ci.num_kv_heads || v_new_scale->shape[1] != ci.num_kv_heads)
+            return fail(PKV_ERR_SHAPE, "new-token scales must be [num_tokens, num_kv_heads]");
+        if (k_new_scale->stride[0] != v_new_scale->stride[0] || k_new_scale->stride[1] != v_new_scale->stride[1])
+            return fail(PKV_ERR_LAYOUT, "k_new_scale and v_new_scale strides differ");
+        p.k_ns = static_cast<const float *>(k_new_scale->data);
+        p.v_ns = static_cast<const float *>(v_new_scale->data);
+        p.ns_tok = k_new_scale->stride[0];
+        p.ns_head = k_new_scale->stride[1];
+    } else if (k_new_scale || v_new_scale) {
+        return fail(PKV_ERR_VALUE, "new-token scales given for a cache without per-token scales");
+    }
     if (ci.kind == PKV_DTYPE_U3) {
         p.k_qs = static_cast<uint16_t *>(cache->k_qscale.data);
         p.v_qs = static_cast<uint16_t *>(cache->v_qscale.data);
@@ -301,6 +356,20 @@ int pkv_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_te
     int kind = 0;
     bool vec16 = false;
     TRY(prep_kv_append(k_new, v_new, slot_mapping, cache, err_flag, p, kind, vec16));
+    return launch_status(pkv::launch_append(p, kind, vec16, as_stream(stream)), "kv_append kernel");
+}
+
+int pkv_kv_append_scaled(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *k_new_scale,
+                         const pkv_tensor *v_new_scale, const pkv_tensor *slot_mapping, const pkv_cache *cache,
+                         int32_t *err_flag, void *stream)
+{
+    if (!k_new_scale || !v_new_scale) return fail(PKV_ERR_NULL, "k_new_scale / v_new_scale are NULL");
+    if (!cache || cache->scale_mode != PKV_SCALE_PER_TOKEN)
+        return fail(PKV_ERR_VALUE, "pkv_kv_append_scaled needs a cache with scale_mode PKV_SCALE_PER_TOKEN");
+    pkv::AppendParams p;
+    int kind = 0;
+    bool vec16 = false;
+    TRY(prep_kv_append(k_new, v_new, slot_mapping, cache, err_flag, p, kind, vec16, k_new_scale, v_new_scale));
     return launch_status(pkv::launch_append(p, kind, vec16, as_stream(stream)), "kv_append kernel");
 }
 
@@ -356,6 +425,14 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
     p.c_head = cache->k_cache.stride[2] * ces;
     p.k_scale = cache->k_scale;
     p.v_scale = cache->v_scale;
+    p.scale_mode = ci.scale_mode;
+    if (ci.scale_mode != PKV_SCALE_PER_HEAD) {
+        p.k_gs = static_cast<const float *>(cache->k_scales.data);
+        p.v_gs = static_cast<const float *>(cache->v_scales.data);
+        p.gs_blk = ci.gs_blk;
+        p.gs_slot = ci.gs_slot;
+        p.gs_head = ci.gs_head;
+    }
     if (ci.kind == PKV_DTYPE_U3) {
         p.k_qs = static_cast<const uint16_t *>(cache->k_qscale.data);
         p.v_qs = static_cast<const uint16_t *>(cache->v_qscale.data);
@@ -384,7 +461,8 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
 
     const int sm = pkv::sm_count_current_device();
     dc.plan = pkv::DecodePlan{};
-    if (num_splits == 0 && pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
+    if (num_splits == 0 && ci.scale_mode == PKV_SCALE_PER_HEAD &&
+        pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
         // q rows are read 16 (3-bit), 8 (fp8) or 4 (16-bit) bytes at a time
         const size_t qa = ci.kind == PKV_DTYPE_U3 ? 16 : (pkv::is_q8(ci.kind) ? 8 : 4);
         const bool q_ok = aligned(q->data, qa) && (p.q_b % qa) == 0 && (p.q_h % qa) == 0;

@@ -25,9 +25,17 @@ struct AppendParams {
     char *k_cache;
     char *v_cache;
     int64_t c_blk, c_slot, c_head;  // byte strides of K and V caches (equal)
-    // fp8
+    // fp8 / int8 scales: per kv head, or (scale_mode 1 / 2) an array indexed
+    // blk * gs_blk + slot * gs_slot + head * gs_head (gs_slot = 0 per block)
     const float *k_scale;
     const float *v_scale;
+    int scale_mode;
+    float *k_gs;
+    float *v_gs;
+    int64_t gs_blk, gs_slot, gs_head;
+    const float *k_ns;          // per-token mode: the new tokens' scales
+    const float *v_ns;
+    int64_t ns_tok, ns_head;
     // 3-bit metadata (element strides, same for the four arrays)
     uint16_t *k_qs;
     uint8_t *k_qz;
@@ -71,6 +79,10 @@ struct DecodeParams {
     int64_t c_blk, c_slot, c_head;  // byte strides (K and V equal)
     const float *k_scale;
     const float *v_scale;
+    int scale_mode;             // 0 per kv head, 1 per block, 2 per token (see AppendParams)
+    const float *k_gs;
+    const float *v_gs;
+    int64_t gs_blk, gs_slot, gs_head;
     const uint16_t *k_qs;
     const uint8_t *k_qz;
     const uint16_t *v_qs;

@@ -44,7 +44,12 @@ class _Tensor(ctypes.Structure):
 class _Cache(ctypes.Structure):
     _fields_ = [("k_cache", _Tensor), ("v_cache", _Tensor), ("k_scale", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("k_qscale", _Tensor), ("k_qzero", _Tensor),
-                ("v_qscale", _Tensor), ("v_qzero", _Tensor)]
+                ("v_qscale", _Tensor), ("v_qzero", _Tensor), ("scale_mode", ctypes.c_int32),
+                ("k_scales", _Tensor), ("v_scales", _Tensor)]
+
+
+# scale granularity of fp8 / int8 caches (pkv.h PKV_SCALE_*)
+SCALE_MODES = {"head": 0, "block": 1, "token": 2}
 
 
 _lib = None
@@ -70,6 +75,7 @@ def lib():
             L.pkv_abi_version.restype = ctypes.c_int
             L.pkv_slot_mapping.argtypes = [TP, TP, TP, ctypes.c_int, TP, P, P]
             L.pkv_kv_append.argtypes = [TP, TP, TP, CP, P, P]
+            L.pkv_kv_append_scaled.argtypes = [TP, TP, TP, TP, TP, CP, P, P]
             L.pkv_paged_decode_workspace.argtypes = [TP, CP, TP, ctypes.c_int,
                                                      ctypes.POINTER(ctypes.c_size_t)]
             L.pkv_paged_decode.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP, ctypes.c_int, P,
@@ -83,7 +89,8 @@ def lib():
             L.pkv_unpack3.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_unpack3_words.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_copy_peak.argtypes = [P, P, ctypes.c_size_t, P]
-            for fn in ("pkv_slot_mapping", "pkv_kv_append", "pkv_paged_decode_workspace",
+            for fn in ("pkv_slot_mapping", "pkv_kv_append", "pkv_kv_append_scaled",
+                       "pkv_paged_decode_workspace",
                        "pkv_paged_decode", "pkv_paged_decode_noalloc", "pkv_decode_step", "pkv_pack3",
                        "pkv_unpack3", "pkv_unpack3_words", "pkv_copy_peak"):
                 getattr(L, fn).restype = ctypes.c_int
@@ -142,6 +149,12 @@ class KVCache:
     k_qzero: Optional[torch.Tensor] = None
     v_qscale: Optional[torch.Tensor] = None
     v_qzero: Optional[torch.Tensor] = None
+    # fp8 / int8 scale granularity: "head" (k_scale / v_scale [Hkv]), "block"
+    # (k_scales / v_scales fp32 [num_blocks, Hkv]) or "token" (fp32
+    # [num_blocks, block_size, Hkv], filled by kv_append_scaled)
+    scale_mode: str = "head"
+    k_scales: Optional[torch.Tensor] = None
+    v_scales: Optional[torch.Tensor] = None
 
     @property
     def num_blocks(self):
@@ -162,7 +175,12 @@ class KVCache:
 
     @staticmethod
     def allocate(kind: str, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
-                 device="cuda", k_scale=None, v_scale=None, fill=None) -> "KVCache":
+                 device="cuda", k_scale=None, v_scale=None, fill=None, scale_mode: str = "head",
+                 k_scales=None, v_scales=None) -> "KVCache":
+        """A cache of `kind`; fp8 / int8 caches take per-head scales (k_scale,
+        v_scale), per-block scales (scale_mode "block": k_scales / v_scales
+        [num_blocks, Hkv]) or per-token scales (scale_mode "token": arrays
+        allocated here, written by kv_append_scaled)."""
         shape = (num_blocks, block_size, num_kv_heads)
         if kind in ("f16", "bf16"):
             dt = torch.float16 if kind == "f16" else torch.bfloat16
@@ -173,7 +191,12 @@ class KVCache:
             k = torch.empty(shape + (head_dim,), dtype=torch.int8 if kind == "i8" else torch.uint8,
                             device=device)
             v = torch.empty_like(k)
-            c = KVCache(kind, k, v, k_scale=k_scale, v_scale=v_scale)
+            c = KVCache(kind, k, v, k_scale=k_scale, v_scale=v_scale, scale_mode=scale_mode)
+            if scale_mode == "block":
+                c.k_scales, c.v_scales = k_scales, v_scales
+            elif scale_mode == "token":
+                c.k_scales = torch.ones(shape, dtype=torch.float32, device=device)
+                c.v_scales = torch.ones(shape, dtype=torch.float32, device=device)
         elif kind == "u3":
             k = torch.empty(shape + (3 * head_dim // 8,), dtype=torch.uint8, device=device)
             v = torch.empty_like(k)
@@ -207,7 +230,7 @@ class KVCache:
         code = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2, "i8": I8, "u3": U3}[self.kind]
         s.k_cache = _desc(self.k_cache, code)
         s.v_cache = _desc(self.v_cache, code)
-        if self.kind in ("e4m3", "e5m2", "i8"):
+        if self.kind in ("e4m3", "e5m2", "i8") and self.scale_mode == "head":
             if self.k_scale is None or self.v_scale is None:
                 raise ValueError("fp8 / int8 cache needs k_scale / v_scale")
             s.k_scale = self.k_scale.data_ptr()
@@ -217,11 +240,16 @@ class KVCache:
             s.k_qzero = _desc(self.k_qzero, U8)
             s.v_qscale = _desc(self.v_qscale, F16)
             s.v_qzero = _desc(self.v_qzero, U8)
+        s.scale_mode = SCALE_MODES[self.scale_mode]
+        if self.scale_mode != "head":
+            s.k_scales = _desc(self.k_scales, F32)
+            s.v_scales = _desc(self.v_scales, F32)
         return s
 
     def tensors(self):
         return [t for t in (self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.k_qscale,
-                            self.k_qzero, self.v_qscale, self.v_qzero) if t is not None]
+                            self.k_qzero, self.v_qscale, self.v_qzero, self.k_scales,
+                            self.v_scales) if t is not None]
 
 
 def version() -> str:
@@ -246,6 +274,17 @@ def kv_append(k_new, v_new, slot_mapping, cache: KVCache, err_flag=None, stream=
     _check(lib().pkv_kv_append(ctypes.byref(_desc(k_new)), ctypes.byref(_desc(v_new)),
                                ctypes.byref(_desc(slot_mapping)), ctypes.byref(cs),
                                _ptr(err_flag), _stream(stream)))
+
+
+def kv_append_scaled(k_new, v_new, k_new_scale, v_new_scale, slot_mapping, cache: KVCache,
+                     err_flag=None, stream=None):
+    """kv_append for a cache with per-token scales: k_new_scale / v_new_scale
+    fp32 [num_tokens, Hkv] are divided out and stored at the tokens' slots."""
+    _need_cuda(k_new, v_new, k_new_scale, v_new_scale, slot_mapping, *cache.tensors())
+    _check(lib().pkv_kv_append_scaled(ctypes.byref(_desc(k_new)), ctypes.byref(_desc(v_new)),
+                                      ctypes.byref(_desc(k_new_scale)), ctypes.byref(_desc(v_new_scale)),
+                                      ctypes.byref(_desc(slot_mapping)), ctypes.byref(cache._struct()),
+                                      _ptr(err_flag), _stream(stream)))
 
 
 def decode_workspace_bytes(q, cache: KVCache, block_tables, num_splits: int = 0) -> int:

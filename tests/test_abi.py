@@ -28,7 +28,7 @@ def test_header_declares_expected_calls():
     names = _declared_functions()
     for n in ("pkv_kv_append", "pkv_paged_decode", "pkv_paged_decode_workspace", "pkv_pack3",
               "pkv_unpack3", "pkv_unpack3_words", "pkv_slot_mapping", "pkv_last_error",
-              "pkv_decode_step", "pkv_paged_decode_noalloc"):
+              "pkv_decode_step", "pkv_paged_decode_noalloc", "pkv_kv_append_scaled"):
         assert n in names
 
 
@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_version(lib):
     from paged_kv_cache_num_gb300 import pkv
     assert "sm_103a" in pkv.version()
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
 
 
 def _fake(shape, dtype, strides=None, ptr=0x10000):
