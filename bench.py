@@ -182,16 +182,22 @@ def algorithmic_bytes(w, decode=True, append=True):
             + its slot (8 B) and (request, position) (8 B)."""
     D, Hkv, BS = w.head_dim, w.num_kv_heads, w.block_size
     row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "i8": D, "u3": 3 * D // 8}[w.cache_kind]
-    meta = 3 if w.cache_kind == "u3" else 0
+    # per cached row and K/V: 3-bit scale + zero, or a per-token fp32 scale
+    meta = 3 if w.cache_kind == "u3" else (4 if w.scale_mode == "token" else 0)
     total = 0
     if decode and w.q is not None:
         ctx = w.context_lens.to(torch.int64).cpu()
+        nblk = int(((ctx + BS - 1) // BS).sum())
         total += int(ctx.sum()) * Hkv * 2 * (row + meta)
         total += 2 * w.q.numel() * 2                       # q in, out
-        total += int(((ctx + BS - 1) // BS).sum()) * 4 + w.batch * 4
+        total += nblk * 4 + w.batch * 4
+        if w.scale_mode == "block":                        # each block's K and V scales
+            total += nblk * Hkv * 2 * 4
     if append:
         n_real = int((w.new_pos >= 0).sum())
-        total += n_real * Hkv * 2 * (2 * D + row + meta) + n_real * 16
+        # a per-token scale is read with the row and written at its slot
+        meta_app = meta + (4 if w.scale_mode == "token" else 0)
+        total += n_real * Hkv * 2 * (2 * D + row + meta_app) + n_real * 16
     return total
 
 
@@ -207,6 +213,10 @@ def make_workload(name, device, rank=0):
         return W.fp8_long(device=device, seed=seed, fp8="e5m2")
     if name == "i8_long":
         return W.fp8_long(device=device, seed=seed, fp8="i8")
+    if name == "fp8_long_token_scales":
+        return W.fp8_long(device=device, seed=seed, scales="token")
+    if name == "fp8_long_block_scales":
+        return W.fp8_long(device=device, seed=seed, scales="block")
     if name == "u3_mha":
         return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
@@ -226,7 +236,9 @@ class Step:
         dev = w.new_req.device
         self.cache = pkv.KVCache.allocate(
             w.cache_kind, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, device=dev,
-            k_scale=w.k_scale, v_scale=w.v_scale, fill=0)
+            k_scale=w.k_scale, v_scale=w.v_scale, fill=0, scale_mode=w.scale_mode,
+            k_scales=w.k_block_scale, v_scales=w.v_block_scale)
+        self.tok = w.scale_mode == "token"
         if w.k_cache0 is not None:
             self.cache.k_cache.copy_(w.k_cache0)
             self.cache.v_cache.copy_(w.v_cache0)
@@ -237,9 +249,15 @@ class Step:
             for i in range(0, w.fill_req.shape[0], ch):
                 sm = pkv.slot_mapping(w.block_tables, w.fill_req[i:i + ch], w.fill_pos[i:i + ch],
                                       w.block_size, err_flag=self.err)
-                pkv.kv_append(w.k_fill[i:i + ch], w.v_fill[i:i + ch], sm, self.cache,
-                              err_flag=self.err)
+                if self.tok:
+                    pkv.kv_append_scaled(w.k_fill[i:i + ch], w.v_fill[i:i + ch],
+                                         w.k_fill_scale[i:i + ch], w.v_fill_scale[i:i + ch], sm,
+                                         self.cache, err_flag=self.err)
+                else:
+                    pkv.kv_append(w.k_fill[i:i + ch], w.v_fill[i:i + ch], sm, self.cache,
+                                  err_flag=self.err)
             w.k_fill = w.v_fill = w.fill_req = w.fill_pos = None
+            w.k_fill_scale = w.v_fill_scale = None
         self.slots = torch.empty(w.new_req.shape[0], dtype=torch.int64, device=dev)
         self.out = torch.empty_like(w.q) if w.q is not None else None
         self.ws = None
@@ -255,8 +273,13 @@ class Step:
         pkv.slot_mapping(w.block_tables, w.new_req if req is None else req,
                          w.new_pos if pos is None else pos, w.block_size, out=self.slots,
                          err_flag=self.err)
-        pkv.kv_append(w.k_new if k is None else k, w.v_new if v is None else v, self.slots,
-                      self.cache, err_flag=self.err)
+        if self.tok:
+            pkv.kv_append_scaled(w.k_new if k is None else k, w.v_new if v is None else v,
+                                 w.k_new_scale, w.v_new_scale, self.slots, self.cache,
+                                 err_flag=self.err)
+        else:
+            pkv.kv_append(w.k_new if k is None else k, w.v_new if v is None else v, self.slots,
+                          self.cache, err_flag=self.err)
 
     def decode(self, q=None):
         w = self.w
@@ -500,7 +523,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_bf16")
-    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long",
+    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long,"
+                                       "fp8_long_token_scales,fp8_long_block_scales",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)

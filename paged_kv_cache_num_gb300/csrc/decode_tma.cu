@@ -65,12 +65,12 @@ __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes,
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
     L.meta_bytes = meta_bytes;
-    // TMA writes each tile at a 1024-byte (128B-swizzled tiles) or 128-byte
-    // (unswizzled 3-bit tiles) aligned shared address, so stages are rounded
-    // up to 1024 bytes, or 128 when the stage holds 3-bit metadata.  (Tiles
-    // are multiples of 768 bytes (3-bit) or 2048 bytes (others) at block 16+,
-    // so only the 3-bit metadata can leave a stage unaligned.)
-    const int align = meta_bytes > 0 ? 128 : 1024;
+    // TMA writes each tile at a 1024-byte (128B-swizzled tiles: rows of 128
+    // or 256 bytes) or 128-byte (unswizzled 3-bit tiles) aligned shared
+    // address, so stages are rounded up to that.  (Tiles are multiples of 768
+    // bytes (3-bit) or 2048 bytes (others) at block 16+, so only the staged
+    // scales / metadata can leave a stage unaligned.)
+    const int align = row_bytes % 128 == 0 ? 1024 : 128;
     L.stage_bytes = (2 * L.tile_bytes + meta_bytes + align - 1) / align * align;
     L.bars_off = stages * L.stage_bytes;
     L.ok_off = L.bars_off + 2 * stages * 8;
@@ -228,7 +228,8 @@ constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
 
 // G1: one q head per kv head (multi-head attention) -- the consumers skip
 // the second head column of their C fragments, which never exists then.
-template <int CK, int D, int BS, bool G1 = false>
+// GSC: fp8 / int8 with per-block or per-token scales, staged per block.
+template <int CK, int D, int BS, bool G1 = false, bool GSC = false>
 __global__ void __launch_bounds__(kMaxThreads<CK>, kCtasPerSm<CK>)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeParams p, FastParams f)
@@ -242,8 +243,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int nh = f.nh, B = p.batch, G = p.group, stages = f.stages;
     // 3-bit metadata per stage: K scales, V scales (fp16), K zeros, V zeros
     // (u8) for the block's BS slots, of the CTA's nh heads ([nh][BS] runs,
-    // head-major arrays) or of all num_kv_heads ([BS][num_kv_heads])
-    const int meta_bytes = T::kIsU3 ? 6 * BS * f.meta_heads : 0;
+    // head-major arrays) or of all num_kv_heads ([BS][num_kv_heads]).
+    // fp8 / int8 with per-block or per-token scales: the K and V scales of
+    // the CTA's heads for the block, [nh] or [nh][BS] fp32 each.
+    const int GS = p.scale_mode == 2 ? BS : 1;        // staged scales per head
+    constexpr bool gscale = T::kFp8 && GSC;
+    const int meta_bytes = T::kIsU3 ? 6 * BS * f.meta_heads : (gscale ? 8 * nh * GS : 0);
     const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
@@ -348,6 +353,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                                 const int half_bytes = L.tile_bytes / T::HALVES;
                                 ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
                                 ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                            }
+                            if constexpr (gscale) {  // the heads' runs of the block's scales
+                                const int64_t g0 = int64_t(pbk) * p.gs_blk + int64_t(hgk) * nh * p.gs_head;
+                                const uint32_t md = vdst + L.tile_bytes;
+                                ptx::bulk_load(md, p.k_gs + g0, uint32_t(4 * nh * GS), fb);
+                                ptx::bulk_load(md + 4 * nh * GS, p.v_gs + g0, uint32_t(4 * nh * GS), fb);
                             }
                             if constexpr (T::kIsU3) {
                                 const int HB = BS * f.meta_heads;         // entries per stage
@@ -519,8 +530,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     zs[c] = 0.0f;
                 }
             }
-            mult = log2e_scale * p.k_scale[kvh] / qs;
-            vmul = p.v_scale[kvh];
+            // per-block / per-token scales are applied per row (scores and P')
+            mult = log2e_scale * (gscale ? 1.0f : p.k_scale[kvh]) / qs;
+            vmul = gscale ? 1.0f : p.v_scale[kvh];
         }
 #pragma unroll
         for (int t = 0; t < T::DT / 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
@@ -777,6 +789,13 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const int valid = min(BS, ctx_b - j * BS);
         const int spb = stage_pb[s];
         if (spb >= 0 && !T::kIsU3) {
+            // fp8 / int8 per-block or per-token scales of this warp's head,
+            // staged with the block: [nh][GS] K scales, then V scales
+            const float *gsk = reinterpret_cast<const float *>(smem + s * L.stage_bytes + 2 * L.tile_bytes) +
+                               warp * GS;
+            const float *gsv = gsk + nh * GS;
+            auto row_ks = [&](int tok) { return gsk[GS == 1 ? 0 : tok]; };
+            auto row_vs = [&](int tok) { return gsv[GS == 1 ? 0 : tok]; };
             const uint32_t ktile = sbase + s * L.stage_bytes + warp * BS * 128;
             const uint32_t vtile = ktile + L.tile_bytes;
             const int half_bytes = L.tile_bytes / T::HALVES;
@@ -818,6 +837,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float v = (CK == kI8 ? sc[t][e] - q1h[e & 1] : sc[t][e]) * mult;
+                    if (T::kFp8 && gscale) v *= row_ks(16 * t + gid + 8 * (e >> 1));
                     if (partial) {
                         const int tok = 16 * t + gid + 8 * (e >> 1);
                         v = tok < valid ? v : NEG_INF;
@@ -850,8 +870,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     const float p1 = exp2_approx(sc[t][2 * r + 1] - m[1]);
                     l[0] += p0;
                     l[1] += p1;
+                    // per-block / per-token V scales fold into P' = p * scale
+                    const float vsr = T::kFp8 && gscale ? row_vs(16 * t + gid + 8 * r) : 1.0f;
                     float q0, q1;
-                    const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0, p1, q0, q1);
+                    const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0 * vsr, p1 * vsr, q0, q1);
                     if constexpr (CK == kI8) {   // the PV operand's offset: sum of P' as rounded
                         zs[0] += q0;
                         zs[1] += q1;
@@ -1153,11 +1175,11 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
     return r == CUDA_SUCCESS;
 }
 
-template <int CK, int D, int BS, bool G1 = false>
+template <int CK, int D, int BS, bool G1 = false, bool GSC = false>
 cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                           const CUtensorMap &mv, cudaStream_t s)
 {
-    auto kern = decode_tma_kernel<CK, D, BS, G1>;
+    auto kern = decode_tma_kernel<CK, D, BS, G1, GSC>;
     // dynamic shared memory limit, raised once per device as needed
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
@@ -1185,6 +1207,16 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
             if (p.block_size == 32) return launch_fast_t<CK, D, 32, true>(p, f, mk, mv, s);
         }
     }
+    if constexpr (is_q8(CK)) {      // per-block / per-token scales staged with the tiles
+        if (p.scale_mode != 0) {
+            switch (p.block_size) {
+            case 16: return launch_fast_t<CK, D, 16, false, true>(p, f, mk, mv, s);
+            case 32: return launch_fast_t<CK, D, 32, false, true>(p, f, mk, mv, s);
+            case 64: return launch_fast_t<CK, D, 64, false, true>(p, f, mk, mv, s);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+    }
     switch (p.block_size) {
     case 16: return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
     case 32: return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
@@ -1208,7 +1240,8 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
 
 // Choose heads per CTA, stages and grid for the fast kernel.
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
-               int cache_kind, bool meta_head_major, int sm_count, FastParams &f, size_t &workspace)
+               int cache_kind, bool meta_head_major, int sm_count, FastParams &f, size_t &workspace,
+               int q8_scales_per_head)
 {
     const bool u3 = cache_kind == kU3;
     const int es = is_q8(cache_kind) ? 1 : 2;
@@ -1224,7 +1257,10 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // ring depth: enough bytes in flight per SM, within the shared memory
     int stages = 8;
     const int meta_heads = meta_head_major ? nh : num_kv_heads;
-    const int meta = u3 ? 6 * block_size * meta_heads : 0;
+    // staged fp8 / int8 granular scales: K and V runs of nh * q8_scales_per_head
+    // fp32, each a multiple of 16 bytes for the bulk copies
+    if (q8_scales_per_head > 0 && (4 * nh * q8_scales_per_head) % 16 != 0) return false;
+    const int meta = u3 ? 6 * block_size * meta_heads : 8 * nh * q8_scales_per_head;
     while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 / ctas_per_sm ||
                           smem_layout(nh, block_size, row, stages, batch, meta).total > budget))
         --stages;

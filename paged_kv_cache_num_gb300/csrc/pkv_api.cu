@@ -461,7 +461,22 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
 
     const int sm = pkv::sm_count_current_device();
     dc.plan = pkv::DecodePlan{};
-    if (num_splits == 0 && ci.scale_mode == PKV_SCALE_PER_HEAD &&
+    // fp8 / int8 granular scales take the persistent kernel when each CTA's
+    // heads' scales of a block are one 16-byte aligned run: per-block
+    // [num_blocks, Hkv] with head stride 1, per-token head-major
+    // ([num_blocks, Hkv, block_size] seen as [num_blocks, block_size, Hkv])
+    int q8_gs = 0;
+    bool gs_ok = ci.scale_mode == PKV_SCALE_PER_HEAD;
+    if (ci.scale_mode == PKV_SCALE_PER_BLOCK) {
+        q8_gs = 1;
+        gs_ok = ci.gs_head == 1 && (ci.gs_blk * 4) % 16 == 0;
+    } else if (ci.scale_mode == PKV_SCALE_PER_TOKEN) {
+        q8_gs = int(ci.block_size);
+        gs_ok = ci.gs_slot == 1 && ci.gs_head == ci.block_size && (ci.gs_blk * 4) % 16 == 0;
+    }
+    if (ci.scale_mode != PKV_SCALE_PER_HEAD)
+        gs_ok = gs_ok && aligned(p.k_gs, 16) && aligned(p.v_gs, 16);
+    if (num_splits == 0 && gs_ok &&
         pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
         // q rows are read 16 (3-bit), 8 (fp8) or 4 (16-bit) bytes at a time
         const size_t qa = ci.kind == PKV_DTYPE_U3 ? 16 : (pkv::is_q8(ci.kind) ? 8 : 4);
@@ -483,7 +498,7 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
         pkv::FastParams f{};
         size_t ws = 0;
         if (q_ok && meta_ok && pkv::plan_fast(p.batch, p.num_heads, p.num_kv_heads, p.head_dim, p.block_size, p.max_blocks,
-                                   ci.kind, meta_hmaj, sm, f, ws) &&
+                                   ci.kind, meta_hmaj, sm, f, ws, q8_gs) &&
             pkv::fast_maps_encodable(p, ci.kind, f.nh)) {
             dc.plan.kernel = 1;
             dc.plan.fast = f;

@@ -136,7 +136,7 @@ DecodePlan plan_decode_general(int batch, int num_heads, int num_kv_heads, int h
 bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch);
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
                int max_blocks, int cache_kind, bool meta_head_major, int sm_count, FastParams &f,
-               size_t &workspace);
+               size_t &workspace, int q8_scales_per_head = 0);
 bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh);
 
 cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cudaStream_t s);

@@ -195,8 +195,11 @@ class KVCache:
             if scale_mode == "block":
                 c.k_scales, c.v_scales = k_scales, v_scales
             elif scale_mode == "token":
-                c.k_scales = torch.ones(shape, dtype=torch.float32, device=device)
-                c.v_scales = torch.ones(shape, dtype=torch.float32, device=device)
+                # head-major storage behind a [num_blocks, block_size, Hkv] view,
+                # as the 3-bit metadata: a decode CTA stages its heads' runs
+                hm = (num_blocks, num_kv_heads, block_size)
+                c.k_scales = torch.ones(hm, dtype=torch.float32, device=device).permute(0, 2, 1)
+                c.v_scales = torch.ones(hm, dtype=torch.float32, device=device).permute(0, 2, 1)
         elif kind == "u3":
             k = torch.empty(shape + (3 * head_dim // 8,), dtype=torch.uint8, device=device)
             v = torch.empty_like(k)

@@ -28,7 +28,16 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
                                  w.head_dim, device=dev,
                                  k_scale=None if w.k_scale is None else w.k_scale.to(dev),
                                  v_scale=None if w.v_scale is None else w.v_scale.to(dev),
-                                 fill=0)
+                                 fill=0, scale_mode=w.scale_mode,
+                                 k_scales=None if w.k_block_scale is None else w.k_block_scale.to(dev),
+                                 v_scales=None if w.v_block_scale is None else w.v_block_scale.to(dev))
+    tok = w.scale_mode == "token"
+
+    def append(kn, vn, sm, ks=None, vs=None):
+        if tok:
+            pkv.kv_append_scaled(kn, vn, ks.to(dev), vs.to(dev), sm, cache, err_flag=err_flag)
+        else:
+            pkv.kv_append(kn, vn, sm, cache, err_flag=err_flag)
     if meta_slot_major and w.cache_kind == "u3":
         for name in ("k_qscale", "k_qzero", "v_qscale", "v_qzero"):
             setattr(cache, name, torch.zeros_like(getattr(cache, name).contiguous()))
@@ -44,11 +53,12 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
             req = w.fill_req[i:i + chunk].to(dev)
             pos = w.fill_pos[i:i + chunk].to(dev)
             sm = pkv.slot_mapping(bt, req, pos, w.block_size, err_flag=err_flag)
-            pkv.kv_append(w.k_fill[i:i + chunk].to(dev), w.v_fill[i:i + chunk].to(dev), sm,
-                          cache, err_flag=err_flag)
+            append(w.k_fill[i:i + chunk].to(dev), w.v_fill[i:i + chunk].to(dev), sm,
+                   w.k_fill_scale[i:i + chunk] if tok else None,
+                   w.v_fill_scale[i:i + chunk] if tok else None)
     sm = pkv.slot_mapping(bt, w.new_req.to(dev), w.new_pos.to(dev), w.block_size,
                           err_flag=err_flag)
-    pkv.kv_append(w.k_new.to(dev), w.v_new.to(dev), sm, cache, err_flag=err_flag)
+    append(w.k_new.to(dev), w.v_new.to(dev), sm, w.k_new_scale, w.v_new_scale)
     if poison is not None:
         poison(cache)
     out = None
@@ -62,12 +72,13 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
 def gpu_cache_host(cache):
     """Host numpy copies of every cache array (bit patterns)."""
     d = {}
-    for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero"):
+    for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero", "k_scales",
+                 "v_scales"):
         t = getattr(cache, name)
         if t is not None:
             t = t.cpu().contiguous()
             d[name] = t.view(torch.int16).numpy().view(np.uint16) if t.element_size() == 2 \
-                else t.numpy() if t.dtype == torch.int8 else t.view(torch.uint8).numpy()
+                else t.numpy() if t.dtype in (torch.int8, torch.float32) else t.view(torch.uint8).numpy()
     return d
 
 
@@ -95,12 +106,23 @@ def oracle_caches(w, orc, seqs=None):
         c["k_qzero"] = np.zeros((P, BS, H), np.uint8)
         c["v_qzero"] = np.zeros((P, BS, H), np.uint8)
     bt = w.block_tables.numpy()
+    mode = {"head": orc.SCALE_PER_HEAD, "block": orc.SCALE_PER_BLOCK,
+            "token": orc.SCALE_PER_TOKEN}[w.scale_mode]
+    if w.scale_mode == "block":
+        c["k_scales"] = w.k_block_scale.numpy().copy()
+        c["v_scales"] = w.v_block_scale.numpy().copy()
+    elif w.scale_mode == "token":
+        c["k_scales"] = np.ones((P, BS, H), np.float32)
+        c["v_scales"] = np.ones((P, BS, H), np.float32)
     rows = []
     if w.fill_req is not None:
-        rows.append((w.fill_req.numpy(), w.fill_pos.numpy(), w.k_fill, w.v_fill))
-    rows.append((w.new_req.numpy(), w.new_pos.numpy(), w.k_new, w.v_new))
+        rows.append((w.fill_req.numpy(), w.fill_pos.numpy(), w.k_fill, w.v_fill, w.k_fill_scale,
+                     w.v_fill_scale))
+    rows.append((w.new_req.numpy(), w.new_pos.numpy(), w.k_new, w.v_new, w.k_new_scale,
+                 w.v_new_scale))
     code = KIND_CODE_ORACLE[kind]
-    for req, pos, kn, vn in rows:
+    for req, pos, kn, vn, kts, vts in rows:
+        idx = None
         if seqs is not None:
             sel = np.isin(req, np.asarray(seqs)) & (pos >= 0)
             idx = np.nonzero(sel)[0]
@@ -108,12 +130,17 @@ def oracle_caches(w, orc, seqs=None):
             kb, vb = W.bits16(kn[torch.from_numpy(idx)]), W.bits16(vn[torch.from_numpy(idx)])
         else:
             kb, vb = W.bits16(kn), W.bits16(vn)
+        if kts is not None:
+            kts, vts = kts.numpy(), vts.numpy()
+            if idx is not None:
+                kts, vts = kts[idx], vts[idx]
         slots = orc.build_slot_mapping(bt, req, pos, BS)
         ks = None if w.k_scale is None else w.k_scale.numpy()
         vs = None if w.v_scale is None else w.v_scale.numpy()
         bad = orc.kv_append(code, src_code(w), kb, vb, slots, c["k_cache"], c["v_cache"], ks, vs,
                             c.get("k_qscale"), c.get("k_qzero"), c.get("v_qscale"),
-                            c.get("v_qzero"))
+                            c.get("v_qzero"), scale_mode=mode, k_new_scale=kts, v_new_scale=vts,
+                            k_scales=c.get("k_scales"), v_scales=c.get("v_scales"))
         assert bad == 0
     return c
 
@@ -127,7 +154,10 @@ def oracle_decode(w, orc, c, pairs=None, nthreads=None):
         k_scale=None if w.k_scale is None else w.k_scale.numpy(),
         v_scale=None if w.v_scale is None else w.v_scale.numpy(),
         k_qscale=c.get("k_qscale"), k_qzero=c.get("k_qzero"), v_qscale=c.get("v_qscale"),
-        v_qzero=c.get("v_qzero"), pairs=pairs, nthreads=nthreads)
+        v_qzero=c.get("v_qzero"), pairs=pairs, nthreads=nthreads,
+        scale_mode={"head": orc.SCALE_PER_HEAD, "block": orc.SCALE_PER_BLOCK,
+                    "token": orc.SCALE_PER_TOKEN}[w.scale_mode],
+        k_scales=c.get("k_scales"), v_scales=c.get("v_scales"))
     assert bad == 0
     return out
 

@@ -29,9 +29,12 @@ def _tokens(w):
     return req, pos, kn, vn
 
 
+@pytest.mark.parametrize("splits", [0, 2])
 @pytest.mark.parametrize("kind", ["e4m3", "i8"])
 @pytest.mark.parametrize("mode", ["block", "token"])
-def test_granular_scales_append_and_decode(pkv, orc, kind, mode):
+def test_granular_scales_append_and_decode(pkv, orc, kind, mode, splits):
+    """splits 0: the persistent kernel, which stages each block's scales
+    with the K/V tiles; splits 2: the general kernel."""
     w = W.fp8_long(batch=4, ctx_lo=30, ctx_hi=600, calib_tokens=64, seed=99, fp8=kind)
     P, BS, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
     fmax = 448.0 if kind == "e4m3" else 127.0
@@ -59,7 +62,7 @@ def test_granular_scales_append_and_decode(pkv, orc, kind, mode):
         pkv.kv_append_scaled(kn.to(dev), vn.to(dev), kt.to(dev), vt.to(dev), slots, cache,
                              err_flag=err)
     out = pkv.paged_decode(w.q.to(dev), cache, bt, w.context_lens.to(dev), sm_scale=w.sm_scale,
-                           err_flag=err)
+                           num_splits=splits, err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     # oracle
@@ -77,8 +80,8 @@ def test_granular_scales_append_and_decode(pkv, orc, kind, mode):
         orc.kv_append(code, orc.BF16, W.bits16(kn), W.bits16(vn), sl, kc, vc,
                       scale_mode=orc.SCALE_PER_TOKEN, k_new_scale=kt.numpy(),
                       v_new_scale=vt.numpy(), k_scales=ks_o, v_scales=vs_o)
-        assert np.array_equal(cache.k_scales.cpu().numpy(), ks_o)
-        assert np.array_equal(cache.v_scales.cpu().numpy(), vs_o)
+        assert np.array_equal(cache.k_scales.cpu().contiguous().numpy(), ks_o)
+        assert np.array_equal(cache.v_scales.cpu().contiguous().numpy(), vs_o)
         sm = orc.SCALE_PER_TOKEN
     assert np.array_equal(cache.k_cache.cpu().numpy(), kc)
     assert np.array_equal(cache.v_cache.cpu().numpy(), vc)
@@ -87,3 +90,45 @@ def test_granular_scales_append_and_decode(pkv, orc, kind, mode):
                                 k_scales=ks_o, v_scales=vs_o, nthreads=orc.max_threads())
     assert bad == 0
     _check(w, out, ref)
+
+
+def test_slot_major_token_scales_take_the_general_kernel(pkv, orc):
+    """Per-token scales stored slot-major (contiguous [num_blocks,
+    block_size, Hkv]) are not one run per head: decode runs the general
+    kernel and still matches the head-major (persistent kernel) result."""
+    w = W.fp8_long(batch=3, ctx_lo=30, ctx_hi=400, calib_tokens=64, seed=101)
+    P, BS, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+    g = torch.Generator().manual_seed(102)
+    req, pos, kn, vn = _tokens(w)
+    kt = (torch.rand((req.shape[0], H), generator=g) + 1) / 200
+    vt = (torch.rand((req.shape[0], H), generator=g) + 1) / 200
+    dev = "cuda"
+    bt = w.block_tables.to(dev)
+    outs = []
+    for slot_major in (False, True):
+        cache = pkv.KVCache.allocate("e4m3", P, BS, H, D, device=dev, fill=0, scale_mode="token")
+        if slot_major:
+            cache.k_scales = torch.ones((P, BS, H), dtype=torch.float32, device=dev)
+            cache.v_scales = torch.ones((P, BS, H), dtype=torch.float32, device=dev)
+        slots = pkv.slot_mapping(bt, req.to(dev), pos.to(dev), BS)
+        pkv.kv_append_scaled(kn.to(dev), vn.to(dev), kt.to(dev), vt.to(dev), slots, cache)
+        outs.append(pkv.paged_decode(w.q.to(dev), cache, bt, w.context_lens.to(dev),
+                                     sm_scale=w.sm_scale))
+    torch.cuda.synchronize()
+    a, b = PL.out_f64(outs[0]), PL.out_f64(outs[1])
+    assert np.max(np.abs(a - b)) <= PL.tolerance(w)
+
+
+@pytest.mark.parametrize("scales", ["token", "block"])
+def test_full_fp8_long_granular_sampled(pkv, orc, scales):
+    """The long-context shape with per-token (each row's amax / 448) or
+    per-block scales, through the persistent kernel: sampled sequences
+    against the oracle."""
+    name = "fp8_long_%s_scales" % scales
+    w = W.fp8_long(seed=W.SEEDS[name], scales=scales)
+    cache, out = PL.gpu_run(w, pkv)
+    seqs = [2, 9]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    from tests.test_gpu_decode import _sample_pairs
+    pairs = _sample_pairs(w, seqs, heads_per_seq=range(0, w.num_heads, 7))
+    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)

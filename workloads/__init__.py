@@ -51,7 +51,8 @@ from typing import Dict, Optional
 import torch
 
 SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44,
-         "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48, "i8_long": 49}
+         "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48, "i8_long": 49,
+         "fp8_long_token_scales": 50, "fp8_long_block_scales": 51}
 
 
 @dataclass
@@ -81,8 +82,18 @@ class Workload:
     fill_pos: Optional[torch.Tensor] = None
     k_fill: Optional[torch.Tensor] = None
     v_fill: Optional[torch.Tensor] = None
-    k_scale: Optional[torch.Tensor] = None   # fp32 [Hkv] (e4m3)
+    k_scale: Optional[torch.Tensor] = None   # fp32 [Hkv] (fp8 / int8, per-head scales)
     v_scale: Optional[torch.Tensor] = None
+    # fp8 / int8 scale granularity: "head" (k_scale / v_scale), "block"
+    # (k_block_scale / v_block_scale [P, Hkv]) or "token" (one scale per
+    # appended row: k_fill_scale [n_fill, Hkv], k_new_scale [T, Hkv], ...)
+    scale_mode: str = "head"
+    k_block_scale: Optional[torch.Tensor] = None
+    v_block_scale: Optional[torch.Tensor] = None
+    k_fill_scale: Optional[torch.Tensor] = None
+    v_fill_scale: Optional[torch.Tensor] = None
+    k_new_scale: Optional[torch.Tensor] = None
+    v_new_scale: Optional[torch.Tensor] = None
     extra: Dict[str, object] = field(default_factory=dict)
 
     @property
@@ -245,10 +256,12 @@ def _fill_lists(ctx_list, device):
 
 def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, num_kv_heads=8,
              head_dim=128, block_size=32, calib_tokens=4096, seed=None,
-             fp8="e4m3") -> Workload:
+             fp8="e4m3", scales="head") -> Workload:
     """Long-context quantised cache with per-kv-head scales amax / (the
     format's largest value): 448 for e4m3 (defaults: the full-size case),
-    57344 for e5m2, 127 for int8 ("i8")."""
+    57344 for e5m2, 127 for int8 ("i8").  scales="block": each block's scale
+    per head is the head's calibration scale times U[1, 1.5]; scales="token":
+    each appended row's own amax / max, a caller-side dynamic calibration."""
     g = _gen(SEEDS["fp8_long"] if seed is None else seed, device)
     dt = torch.bfloat16
     B, Hq, Hkv, D, BS = batch, num_heads, num_kv_heads, head_dim, block_size
@@ -276,6 +289,15 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
     w = Workload("fp8_long", dt, fp8, B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
                  k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
                  v_fill=v_fill, k_scale=k_scale.contiguous(), v_scale=v_scale.contiguous())
+    w.scale_mode = scales
+    if scales == "block":
+        w.k_block_scale = (k_scale[None, :] * (1 + 0.5 * torch.rand((P, Hkv), generator=g, device=device))).contiguous()
+        w.v_block_scale = (v_scale[None, :] * (1 + 0.5 * torch.rand((P, Hkv), generator=g, device=device))).contiguous()
+    elif scales == "token":
+        def row_scale(x):          # per (token, head) amax / max, never 0
+            return (x.float().abs().amax(dim=2) / fmax).clamp_min(2.0 ** -60).contiguous()
+        w.k_fill_scale, w.v_fill_scale = row_scale(k_fill), row_scale(v_fill)
+        w.k_new_scale, w.v_new_scale = row_scale(k_new), row_scale(v_new)
     w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
     return w
 
