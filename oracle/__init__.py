@@ -268,3 +268,38 @@ def paged_decode(cache_dtype: int, q_dtype: int, q, k_cache, v_cache, block_tabl
         0 if pr is None else pr.shape[0], _ptr(out), int(nthreads), int(scale_mode), _ptr(kss),
         _ptr(vss))
     return out, int(bad)
+
+
+# --------------------------------------------------------------------------
+# storage layouts
+# --------------------------------------------------------------------------
+
+def xvec_elems(elem_bytes: int) -> int:
+    """x of the x-vectorised layout: the elements of one 16-byte piece."""
+    return 16 // elem_bytes
+
+
+def to_xvec(cache: np.ndarray, x: int) -> np.ndarray:
+    """The older vLLM paged layout with a vectorised inner dimension
+    ("Write Triton Kv Cache Append Kernel", "Inputs the agent should gather
+    first" item 1): a cache [num_blocks, block_size, num_kv_heads, head_dim]
+    is stored as [num_blocks, num_kv_heads, head_dim // x, block_size, x],
+    i.e. head_dim is cut into pieces of x consecutive elements and, within a
+    block and head, piece c of every slot comes before piece c + 1 of any.
+    Element (b, s, h, d) lands at [b, h, d // x, s, d % x]."""
+    P, BS, H, D = cache.shape
+    assert D % x == 0
+    out = np.empty((P, H, D // x, BS, x), dtype=cache.dtype)
+    for c in range(D // x):
+        # piece c of every (block, slot, head) row, heads before slots
+        out[:, :, c, :, :] = cache[:, :, :, c * x:(c + 1) * x].transpose(0, 2, 1, 3)
+    return out
+
+
+def from_xvec(phys: np.ndarray) -> np.ndarray:
+    """Inverse of to_xvec: [P, Hkv, D // x, BS, x] -> [P, BS, Hkv, D]."""
+    P, H, C, BS, x = phys.shape
+    out = np.empty((P, BS, H, C * x), dtype=phys.dtype)
+    for c in range(C):
+        out[:, :, :, c * x:(c + 1) * x] = phys[:, :, c, :, :].transpose(0, 2, 1, 3)
+    return out
