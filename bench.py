@@ -43,6 +43,8 @@ L2_FLUSH_BYTES = 256 << 20
 # sources of the decode kernels; a recorded ncu traffic figure is only used
 # while these are unchanged
 DECODE_SOURCES = ("paged_kv_cache_num_gb300/csrc/decode_tma.cu",
+                  "paged_kv_cache_num_gb300/csrc/decode_tma_kernel.cuh",
+                  "paged_kv_cache_num_gb300/csrc/decode_tma_xv.cu",
                   "paged_kv_cache_num_gb300/csrc/decode.cu",
                   "paged_kv_cache_num_gb300/csrc/pkv_ptx.cuh",
                   "paged_kv_cache_num_gb300/csrc/pkv_device.cuh")
@@ -217,6 +219,10 @@ def make_workload(name, device, rank=0):
         return W.fp8_long(device=device, seed=seed, scales="token")
     if name == "fp8_long_block_scales":
         return W.fp8_long(device=device, seed=seed, scales="block")
+    if name == "gqa_bf16_xvec":
+        return W.gqa_bf16(device=device, seed=seed, layout="xvec")
+    if name == "fp8_long_xvec":
+        return W.fp8_long(device=device, seed=seed, layout="xvec")
     if name == "u3_mha":
         return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
@@ -237,11 +243,11 @@ class Step:
         self.cache = pkv.KVCache.allocate(
             w.cache_kind, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, device=dev,
             k_scale=w.k_scale, v_scale=w.v_scale, fill=0, scale_mode=w.scale_mode,
-            k_scales=w.k_block_scale, v_scales=w.v_block_scale)
+            k_scales=w.k_block_scale, v_scales=w.v_block_scale, layout=w.layout)
         self.tok = w.scale_mode == "token"
         if w.k_cache0 is not None:
-            self.cache.k_cache.copy_(w.k_cache0)
-            self.cache.v_cache.copy_(w.v_cache0)
+            self.cache.k_cache.copy_(W.storage(w.k_cache0, w.layout))
+            self.cache.v_cache.copy_(W.storage(w.v_cache0, w.layout))
             w.k_cache0 = w.v_cache0 = None      # release the staging copies
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         if w.fill_req is not None:            # context fill (setup, not timed)
@@ -524,7 +530,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_bf16")
     ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long,"
-                                       "fp8_long_token_scales,fp8_long_block_scales",
+                                       "fp8_long_token_scales,fp8_long_block_scales,gqa_bf16_xvec,"
+                                       "fp8_long_xvec",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 /* Element types. */
 enum {
@@ -143,6 +143,20 @@ typedef struct pkv_cache {
     int32_t scale_mode;
     pkv_tensor k_scales;
     pkv_tensor v_scales;
+    /* ABI 3: F16 / BF16 / E4M3 / E5M2 / I8 only -- stride, in elements,
+     * between consecutive pieces of x elements of a head row, x = 16 bytes /
+     * element size (8 for 16-bit, 16 for one-byte codes); 0 means x (the
+     * row is contiguous).  A non-zero value selects the x-vectorised layout
+     * of older vLLM ("Write Triton Kv Cache Append Kernel", "Inputs the
+     * agent should gather first" item 1):
+     *   storage [num_blocks, num_kv_heads, head_dim / x, block_size, x],
+     * described by k_cache / v_cache as [num_blocks, block_size,
+     * num_kv_heads, head_dim] with strides [Hkv*D*BS, x, D*BS, 1] and
+     * chunk_stride = block_size * x (element (b, s, h, d) at
+     * b*stride0 + s*stride1 + h*stride2 + (d/x)*chunk_stride + d%x).
+     * head_dim must be a multiple of x and chunk_stride a multiple of 16
+     * bytes.  Both caches use it. */
+    int64_t chunk_stride;
 } pkv_cache;
 
 /* Library version string and ABI version. */

@@ -67,11 +67,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
         const char *src = kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
                              : p.k_new + t * p.k_src_tok + h * p.k_src_head;
         char *dst = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot + h * p.c_head;
+        // the row's 16-byte pieces are c_chunk bytes apart (16 when contiguous)
         if constexpr (CHUNK == 16) {
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + c);
-            reinterpret_cast<uint4 *>(dst)[c] = v;
+            *reinterpret_cast<uint4 *>(dst + c * p.c_chunk) = v;
         } else {
-            reinterpret_cast<uint16_t *>(dst)[c] = reinterpret_cast<const uint16_t *>(src)[c];
+            *reinterpret_cast<uint16_t *>(dst + (c >> 3) * p.c_chunk + 2 * (c & 7)) =
+                reinterpret_cast<const uint16_t *>(src)[c];
         }
     }
 }
@@ -116,8 +118,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
         const uint16_t *src = reinterpret_cast<const uint16_t *>(
             kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
                : p.k_new + t * p.k_src_tok + h * p.k_src_head) + 8 * c;
+        // elements 8c .. 8c+7: half of the row's 16-byte piece c / 2
         uint8_t *dst = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
-                                                   off * p.c_slot + h * p.c_head) + 8 * c;
+                                                   off * p.c_slot + h * p.c_head + (c >> 1) * p.c_chunk) +
+                       8 * (c & 1);
         float scale;
         if (p.scale_mode == 0) {                // per kv head
             scale = (kv ? p.v_scale : p.k_scale)[h];

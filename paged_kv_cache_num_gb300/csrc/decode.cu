@@ -127,6 +127,16 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
     const float ks = is_q8(CK) && p.scale_mode == 0 ? p.k_scale[kvh] : 1.0f;
     const float vs = is_q8(CK) && p.scale_mode == 0 ? p.v_scale[kvh] : 1.0f;
     const int bmask = (1 << p.block_shift) - 1;
+    // this lane's EPL elements: packed 3-bit rows are addressed by element;
+    // the others lie inside one 16-byte piece of the row, the pieces being
+    // c_chunk bytes apart (x-vectorised layout) or adjacent
+    int64_t eoff = 0;
+    int e0 = EPL * lane;
+    if constexpr (CK != kU3) {
+        constexpr int ES = (CK == kF16 || CK == kBF16) ? 2 : 1;
+        eoff = int64_t((EPL * lane * ES) >> 4) * p.c_chunk + ((EPL * lane * ES) & 15);
+        e0 = 0;
+    }
 
     for (int t = t0 + warp; t < t1; t += kGenWarps) {
         const int j = t >> p.block_shift, off = t & bmask;
@@ -150,8 +160,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
             vz = float(p.v_qz[pb * p.z_blk + off * p.z_slot + kvh * p.z_head]);
         }
         float kx[EPL], vx[EPL];
-        load_row<CK, EPL>(p.k_cache + roff, EPL * lane, kst, kq, kz, kx);
-        load_row<CK, EPL>(p.v_cache + roff, EPL * lane, vst, vq, vz, vx);
+        load_row<CK, EPL>(p.k_cache + roff + eoff, e0, kst, kq, kz, kx);
+        load_row<CK, EPL>(p.v_cache + roff + eoff, e0, vst, vq, vz, vx);
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) {
             if (g < G) {

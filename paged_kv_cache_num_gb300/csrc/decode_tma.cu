@@ -1,1137 +1,10 @@
-// decode_tma.cu -- the fast paged-decode path for 16-bit, fp8 and 3-bit caches:
-// a persistent, load-balanced kernel that streams whole physical blocks into
-// shared memory with TMA and runs both products of each block on tensor
-// cores, plus the merge kernel for sequences split across CTAs.
-//
-// What it computes is "10. Triton KV Cache and PagedAttention", reference
-// code TODO 1-5 (block-table lookup, masked K/V tile, scores, online softmax,
-// V accumulation, final normalisation), with grouped-query heads
-// ("Write Triton Kv Cache Append Kernel", design rules) and a split of long
-// contexts whose partial (m, l, acc) triples are merged by log-sum-exp
-// rescaling.
-//
-// Work decomposition.  The unit of work is one physical block of one group
-// of `nh` kv heads.  All (head group, sequence, logical block) units are laid
-// out in one flat index space (head group major, then sequence, then block)
-// and CTA i of the persistent grid takes the contiguous range
-// [i*N/S, (i+1)*N/S): every CTA streams the same number of blocks, whatever
-// the mix of context lengths.  A CTA's range crosses sequence boundaries; each
-// maximal run of one (head group, sequence) inside it is a segment.  A segment
-// that covers its whole sequence writes the output directly; otherwise it
-// writes an fp32 partial in slot (CTA index + unit index), which is unique
-// because both grow along the flat order, and the merge kernel combines the
-// partials of the CTAs that cover the unit.
-//
-// CTA layout.  nh consumer warps (one per kv head of the group) and one
-// producer warp.  The producer resolves 32 block-table entries at a time
-// (one per lane) and issues, per block, TMA tensor copies of the K and V
-// tiles [nh heads][block_size tokens][head_dim] (128-byte swizzled rows) into
-// a ring of `stages` shared-memory stages guarded by full/empty mbarriers.
-// Each consumer warp computes, for its kv head and the G <= 8 query heads
-// that share it, with m16n8k16 mma.sync (block tokens on M, q heads on N):
-//   S^T = K Q^T (K from shared memory by ldmatrix, or fp8 / 3-bit codes
-//   converted to f16 in registers), masking of tokens >= context_len, online
-//   softmax per q head in log2 units, O^T = O^T * alpha + V^T P^T (P^T moved
-//   from the score accumulators into operand layout by movmatrix; V^T by
-//   ldmatrix.trans, or fp8 / 3-bit code pairing + conversion).  3-bit
-//   blocks also bring their per-token scale / zero runs with bulk copies.
-// Every wait is bounded (about 2 s of wall time) and raises
-// PKV_DEVERR_TIMEOUT instead of hanging.
-#include <cudaTypedefs.h>
-
-#include <atomic>
-#include <type_traits>
-#include <mutex>
-
-#include "pkv_device.cuh"
-#include "pkv_ptx.cuh"
+// decode_tma.cu -- host side of the persistent paged-decode path: tensor
+// maps, planning, and the launches of the flash-layout instances (the
+// x-vectorised ones are in decode_tma_xv.cu).
+#include "decode_tma_kernel.cuh"
 
 namespace pkv {
 namespace {
-
-constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr int kMaxDevices = 64;
-#define NEG_INF (-__int_as_float(0x7f800000))
-
-struct SmemLayout {
-    int tile_bytes, meta_bytes, stage_bytes, bars_off, ok_off, prefix_off, nblk_off, total;
-};
-
-// [stages x (K tile, V tile, 3-bit metadata of the whole block)]
-// [mbarriers] [per-stage block ids] [prefix sums] [block counts]
-__host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
-                                                  int batch, int meta_bytes = 0)
-{
-    SmemLayout L;
-    L.tile_bytes = nh * bs * row_bytes;
-    L.meta_bytes = meta_bytes;
-    // TMA writes each tile at a 1024-byte (128B-swizzled tiles: rows of 128
-    // or 256 bytes) or 128-byte (unswizzled 3-bit tiles) aligned shared
-    // address, so stages are rounded up to that.  (Tiles are multiples of 768
-    // bytes (3-bit) or 2048 bytes (others) at block 16+, so only the staged
-    // scales / metadata can leave a stage unaligned.)
-    const int align = row_bytes % 128 == 0 ? 1024 : 128;
-    L.stage_bytes = (2 * L.tile_bytes + meta_bytes + align - 1) / align * align;
-    L.bars_off = stages * L.stage_bytes;
-    L.ok_off = L.bars_off + 2 * stages * 8;
-    L.prefix_off = L.ok_off + stages * 4;
-    L.nblk_off = L.prefix_off + (batch + 1) * 4;
-    L.total = L.nblk_off + batch * 4 + 1024;   // + alignment slack
-    return L;
-}
-
-// largest b in [0, B) with prefix[b] <= r, for 0 <= r < prefix[B]
-__device__ __forceinline__ int find_seq(const int *prefix, int B, int r)
-{
-    int lo = 0, hi = B;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= r) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &rlo, float &rhi)
-{
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    const float2 r = __bfloat1622float2(v);
-    rlo = r.x;
-    rhi = r.y;
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float &rlo, float &rhi)
-{
-    const __half2 v = __floats2half2_rn(lo, hi);
-    const float2 r = __half22float2(v);
-    rlo = r.x;
-    rhi = r.y;
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-// Two one-byte codes (the low 16 bits, low byte first) of cache kind CK ->
-// an f16x2 register, exactly: fp8 through the hardware conversion; int8 c
-// as 1152 + c (a byte permute puts c next to the exponent of 1024 and an
-// XOR of the byte's top bit adds 128), the 1152 offset being removed in
-// fp32 after the MMA.
-template <int CK>
-__device__ __forceinline__ uint32_t f16x2_from_fp8x2(uint32_t two)
-{
-    if constexpr (CK == kI8) {
-        return ptx::prmt(two, 0x64646464u, 0x4140u) ^ 0x00800080u;
-    } else {
-        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu),
-                                                         CK == kE4M3 ? __NV_E4M3 : __NV_E5M2);
-        return uint32_t(h.x) | (uint32_t(h.y) << 16);
-    }
-}
-constexpr float kI8Bias = 1152.0f;
-
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
-// ---------------------------------------------------------------- 3-bit
-// A 3-bit code v placed at bit x <= 7 of an otherwise zero 16-bit half is
-// the f16 subnormal v * 2^(x - 24): exact, and never a NaN or an infinity
-// whatever the bits around it.  Products with normal f16 operands are exact
-// in the fp32 accumulators, so the factor 2^(x - 24) is folded into q' on
-// the K side and into the output on the V side, and no offset has to be
-// removed after the MMA.  One LOP3 (mask) makes a pair; the windows the
-// masks apply to are the costly part and are shared between pairs.
-//
-// K side: the A fragments of S^T = K Q'^T pair two codes of one token row.
-// A 96-bit group (32 codes, lane i at bits 3i..3i+2) is cut into seven
-// 32-bit windows -- its three words and four shifts -- and each window
-// gives up to three pairs, lane i at bit x and lane j at bit 16 + y.
-struct U3KPair {
-    int s, i, j, x, y;   // window = bits s .. s+31 of the group
-};
-__host__ __device__ constexpr U3KPair u3k_pair_info(int p)
-{
-    switch (p) {
-    case 0: return {0, 0, 7, 0, 5};
-    case 1: return {0, 1, 6, 3, 2};
-    case 2: return {4, 2, 9, 2, 7};
-    case 3: return {4, 3, 8, 5, 4};
-    case 4: return {10, 4, 11, 2, 7};
-    case 5: return {10, 5, 10, 5, 4};
-    case 6: return {32, 12, 17, 4, 3};
-    case 7: return {32, 13, 18, 7, 6};
-    case 8: return {41, 14, 21, 1, 6};
-    case 9: return {41, 15, 20, 4, 3};
-    case 10: return {41, 16, 19, 7, 0};
-    case 11: return {64, 22, 27, 2, 1};
-    case 12: return {64, 23, 28, 5, 4};
-    case 13: return {71, 24, 31, 1, 6};
-    case 14: return {71, 25, 30, 4, 3};
-    default: return {71, 26, 29, 7, 0};
-    }
-}
-
-// Pair p of the group held in words (w0, w1, w2); p is a constant after
-// unrolling, so the window choice folds away (and equal windows are shared).
-__device__ __forceinline__ uint32_t u3k_pair(int p, uint32_t w0, uint32_t w1, uint32_t w2)
-{
-    const U3KPair pr = u3k_pair_info(p);
-    uint32_t win;
-    if (pr.s == 0) win = w0;
-    else if (pr.s < 32) win = __funnelshift_r(w0, w1, pr.s);
-    else if (pr.s == 32) win = w1;
-    else if (pr.s < 64) win = __funnelshift_r(w1, w2, pr.s - 32);
-    else if (pr.s == 64) win = w2;
-    else win = w2 >> (pr.s - 64);
-    return win & ((7u << pr.x) | (7u << (16 + pr.y)));
-}
-
-// V side: the A fragments of O^T = V'^T P'^T pair one code of two tokens.
-// A lane owns the 16 codes of bytes 6g .. 6g+5 of a row (g = its group id);
-// code c of that slice lies in the 16-bit piece that starts at slice byte
-// u3v_win(c), at bit u3v_x(c) of it.  A byte permute puts the piece of
-// token A in the low half and that of token B in the high half.
-__host__ __device__ constexpr int u3v_win(int c)
-{
-    return c < 3 ? 0 : c < 6 ? 1 : c < 8 ? 2 : c < 11 ? 3 : c < 14 ? 4 : 5;
-}
-__host__ __device__ constexpr int u3v_x(int c) { return 3 * c - 8 * u3v_win(c); }
-
-// CK: cache kind (kF16 / kBF16 / kE4M3 / kE5M2 / kU3); D head_dim; BS block size.
-// MMA operand type: bf16 for bf16 caches, f16 otherwise (fp8 codes convert
-// exactly to f16).
-template <int CK, int D, int BS>
-struct Tile {
-    static constexpr bool kFp8 = is_q8(CK);
-    static constexpr bool kIsU3 = CK == pkv::kU3;
-    static constexpr bool kBF = CK == kBF16;
-    static constexpr int ES = (kFp8 || kIsU3) ? 1 : 2;
-    static constexpr int ROW = kIsU3 ? 3 * D / 8 : D * ES;   // bytes per token row
-    static constexpr int HALVES = kIsU3 ? 1 : ROW / 128;     // 128-byte swizzled sub-rows
-    static constexpr int BOX0 = kIsU3 ? ROW : 128 / ES;      // TMA box inner extent (elements)
-    static constexpr int KT = BS / 16;              // PV k-steps
-    static constexpr int DT = D / 8;                // output n-tiles
-    static constexpr int QK = D / 16;               // QK k-steps
-};
-
-// 3-bit caches: CTAs of (at most) 4 kv heads, three per SM -- the consumers
-// are latency-bound on the unpacking and gain from more warps per SM, and
-// 3 x 5 warps keep at most 4 warps (128 registers each) per SM sub-partition.
-// The others: CTAs of up to 8 kv heads, one per SM.
-constexpr int kU3Heads = 4;
-constexpr int kU3CtasPerSm = 3;
-template <int CK>
-constexpr int kCtasPerSm = CK == kU3 ? kU3CtasPerSm : 1;
-template <int CK>
-constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
-
-// G1: one q head per kv head (multi-head attention) -- the consumers skip
-// the second head column of their C fragments, which never exists then.
-// GSC: fp8 / int8 with per-block or per-token scales, staged per block.
-template <int CK, int D, int BS, bool G1 = false, bool GSC = false>
-__global__ void __launch_bounds__(kMaxThreads<CK>, kCtasPerSm<CK>)
-decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  DecodeParams p, FastParams f)
-{
-    using T = Tile<CK, D, BS>;
-    constexpr int NC = G1 ? 1 : 2;      // head columns (2tig, 2tig+1) that can exist
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nh = f.nh, B = p.batch, G = p.group, stages = f.stages;
-    // 3-bit metadata per stage: K scales, V scales (fp16), K zeros, V zeros
-    // (u8) for the block's BS slots, of the CTA's nh heads ([nh][BS] runs,
-    // head-major arrays) or of all num_kv_heads ([BS][num_kv_heads]).
-    // fp8 / int8 with per-block or per-token scales: the K and V scales of
-    // the CTA's heads for the block, [nh] or [nh][BS] fp32 each.
-    const int GS = p.scale_mode == 2 ? BS : 1;        // staged scales per head
-    constexpr bool gscale = T::kFp8 && GSC;
-    const int meta_bytes = T::kIsU3 ? 6 * BS * f.meta_heads : (gscale ? 8 * nh * GS : 0);
-    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes);
-    const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
-    volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
-    int *prefix = reinterpret_cast<int *>(smem + L.prefix_off);
-    int *nblk = reinterpret_cast<int *>(smem + L.nblk_off);
-    griddep_wait();                // the stream's previous kernel (an append) is done
-
-    // ---- per-sequence block counts and their prefix sums
-    const int cap = p.max_blocks << p.block_shift;
-    for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        int ctx = p.context_lens[b * p.cl_stride];
-        if (ctx < 0 || ctx > cap) {
-            if (blockIdx.x == 0) raise_err(p.err_flag, PKV_DEVERR_CONTEXT_RANGE);
-            ctx = ctx < 0 ? 0 : cap;
-        }
-        nblk[b] = (ctx + BS - 1) / BS;
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
-            ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, nh);
-        }
-        ptx::fence_mbar_init();
-    }
-    __syncthreads();
-    if (warp == 0) {               // exclusive scan, 32 sequences per step
-        int carry = 0;
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int v = (b0 + lane < B) ? nblk[b0 + lane] : 0;
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            if (b0 + lane < B) prefix[b0 + lane] = carry + incl - v;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) prefix[B] = carry;
-    }
-    __syncthreads();
-    if (blockIdx.x == 0)
-        for (int b = threadIdx.x; b <= B; b += blockDim.x) f.prefix[b] = prefix[b];
-
-    // the merge kernel may be scheduled now; it waits for this grid to finish
-    griddep_launch_dependents();
-    const int64_t NBT = prefix[B];                  // blocks per head group
-    const int64_t N = NBT * f.n_hg;
-    const int64_t lo = int64_t(blockIdx.x) * N / gridDim.x;
-    const int64_t hi = int64_t(blockIdx.x + 1) * N / gridDim.x;
-    if (lo >= hi) return;
-
-    // ======================================================== producer warp
-    if (warp == nh) {
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tmk);
-            ptx::prefetch_tmap(&tmv);
-        }
-        bool aborted = false;
-        int64_t issued = 0;
-        int ps = 0;              // next stage to fill
-        uint32_t pphase = 0;     // completed-round parity of that stage
-        for (int64_t base = lo; base < hi && !aborted; base += 32) {
-            const int64_t x = base + lane;
-            int pb = -1, hg = 0;
-            if (x < hi) {
-                hg = int(x / NBT);
-                const int r = int(x - int64_t(hg) * NBT);
-                const int b = find_seq(prefix, B, r);
-                const int j = r - prefix[b];
-                pb = p.block_tables[b * p.bt_b + j * p.bt_j];
-                if (pb < 0 || pb >= p.num_blocks) {
-                    raise_err(p.err_flag, PKV_DEVERR_BLOCK_RANGE);
-                    pb = -1;
-                }
-            }
-            const int n = int(hi - base < 32 ? hi - base : 32);
-            for (int k = 0; k < n; ++k) {
-                const int pbk = __shfl_sync(0xffffffffu, pb, k);
-                const int hgk = __shfl_sync(0xffffffffu, hg, k);
-                if (lane == 0 && !aborted) {
-                    const int s = ps;
-                    const bool reuse = issued >= stages;     // stage held a block before
-                    const uint32_t par = pphase ^ 1u;
-                    if (++ps == stages) {
-                        ps = 0;
-                        pphase ^= 1u;
-                    }
-                    if (reuse && !ptx::mbar_wait_bounded(bar_empty + 8 * s, par, kTimeoutNs)) {
-                        raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
-                        aborted = true;
-                    } else {
-                        const uint32_t fb = bar_full + 8 * s;
-                        const uint32_t kdst = sbase + s * L.stage_bytes;
-                        const uint32_t vdst = kdst + L.tile_bytes;
-                        stage_pb[s] = pbk;
-                        if (pbk >= 0) {
-                            ptx::mbar_arrive_expect_tx(fb, uint32_t(2 * L.tile_bytes + L.meta_bytes));
-#pragma unroll
-                            for (int h = 0; h < T::HALVES; ++h) {
-                                const int half_bytes = L.tile_bytes / T::HALVES;
-                                ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
-                                ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
-                            }
-                            if constexpr (gscale) {  // the heads' runs of the block's scales
-                                const int64_t g0 = int64_t(pbk) * p.gs_blk + int64_t(hgk) * nh * p.gs_head;
-                                const uint32_t md = vdst + L.tile_bytes;
-                                ptx::bulk_load(md, p.k_gs + g0, uint32_t(4 * nh * GS), fb);
-                                ptx::bulk_load(md + 4 * nh * GS, p.v_gs + g0, uint32_t(4 * nh * GS), fb);
-                            }
-                            if constexpr (T::kIsU3) {
-                                const int HB = BS * f.meta_heads;         // entries per stage
-                                // head-major: the group's heads are one run at head hgk*nh
-                                const int64_t h0 = f.meta_heads == nh ? int64_t(hgk) * nh * BS : 0;
-                                const uint32_t md = vdst + L.tile_bytes;
-                                ptx::bulk_load(md, p.k_qs + int64_t(pbk) * p.m_blk + h0, 2 * HB, fb);
-                                ptx::bulk_load(md + 2 * HB, p.v_qs + int64_t(pbk) * p.m_blk + h0, 2 * HB, fb);
-                                ptx::bulk_load(md + 4 * HB, p.k_qz + int64_t(pbk) * p.z_blk + h0, HB, fb);
-                                ptx::bulk_load(md + 5 * HB, p.v_qz + int64_t(pbk) * p.z_blk + h0, HB, fb);
-                            }
-                        } else {
-                            ptx::mbar_arrive(fb);
-                        }
-                        ++issued;
-                    }
-                }
-                aborted = __shfl_sync(0xffffffffu, aborted, 0);
-            }
-        }
-        // let the copies in flight land before this warp retires
-        if (lane == 0) {
-            for (int64_t it = issued > stages ? issued - stages : 0; it < issued; ++it)
-                ptx::mbar_wait_bounded(bar_full + 8 * int(it % stages), uint32_t((it / stages) & 1),
-                                       kTimeoutNs);   // once per CTA, off the hot loop
-        }
-        return;
-    }
-
-    // ======================================================== consumer warps
-    // Tokens on the MMA's M dimension, the group's q heads on N (G <= 8):
-    //   S^T[tok][head] = K[tok][:] . Q[head][:]        (A = K, B = Q^T)
-    //   O^T[d][head]  += V^T[d][tok] P^T[tok][head]     (A = V^T, B = P^T)
-    // A thread of the C fragments holds heads 2tig, 2tig+1 for tokens
-    // (or d) gid and gid+8 of each 16-row tile.
-    const int gid = lane >> 2, tig = lane & 3;
-    const float log2e_scale = p.scale_log2;
-    // walk state
-    int64_t x = lo;
-    int hg = int(x / NBT);
-    int b, j;
-    {
-        const int r = int(x - int64_t(hg) * NBT);
-        b = find_seq(prefix, B, r);
-        j = r - prefix[b];
-    }
-    int64_t seg_start = lo;
-
-    uint32_t qb[T::QK][2];        // B fragments of Q^T per k-step
-    float o[T::DT / 2][4];        // O^T accumulators: 16-d tiles x (heads 2tig, 2tig+1)
-    float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
-    float mult = 1.0f, vmul = 1.0f;
-    int ctx_b = 0;
-    // per head column: 3-bit, sum(q' 2^(x-24)) of the QK operand and the
-    // running sum of P' * zero of the PV operand; int8, 1152 sum(q') and the
-    // running sum of P' (the operands' 1152 offsets)
-    float q1h[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
-
-    auto start_segment = [&]() {
-        const int kvh = hg * nh + warp;
-        {
-            const int cb = p.context_lens[b * p.cl_stride];
-            ctx_b = cb < 0 ? 0 : (cb > cap ? cap : cb);
-        }
-        const bool hv = gid < G;  // this lane's B column (q head gid) exists
-        const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
-        if constexpr (T::kIsU3) {
-            // q' = q qs 2^(1-x) (f16, exact) in the pair order of the K
-            // fragments: k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1)
-            // and pair 2kk+1 (k = 2tig+8, 2tig+9) of 96-bit group tig, so that
-            // q' k' = qs 2^-23 q v for every code.
-            float qv[32];
-            float amax = 0.0f;
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (hv) u = *reinterpret_cast<const uint4 *>(qr + 32 * tig + 8 * c4);
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float a, c;
-                    if (p.q_is_bf16) {
-                        a = __uint_as_float(w[e] << 16);
-                        c = __uint_as_float(w[e] & 0xffff0000u);
-                    } else {
-                        const float2 t2 = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-                        a = t2.x;
-                        c = t2.y;
-                    }
-                    qv[8 * c4 + 2 * e] = a;
-                    qv[8 * c4 + 2 * e + 1] = c;
-                    amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c)));
-                }
-            }
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
-            float qs = 1.0f;
-            while (amax * qs > 16384.0f) qs *= 0.5f;
-            float q1 = 0.0f;
-#pragma unroll
-            for (int pp = 0; pp < 16; ++pp) {
-                const U3KPair pr = u3k_pair_info(pp);
-                float ra, rb;
-                const uint32_t w = pack_f16(qv[pr.i] * qs * (2.0f / float(1 << pr.x)),
-                                            qv[pr.j] * qs * (2.0f / float(1 << pr.y)), ra, rb);
-                qb[pp >> 1][pp & 1] = w;
-                q1 += ra * (float(1 << pr.x) * 0x1p-24f) + rb * (float(1 << pr.y) * 0x1p-24f);
-            }
-            q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
-            q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {       // values of head columns 2tig, 2tig+1
-                q1h[c] = __shfl_sync(0xffffffffu, q1, 4 * (2 * tig + c));
-                zs[c] = 0.0f;
-            }
-            mult = log2e_scale * 0x1p23f / qs;
-            vmul = 1.0f;
-        } else if constexpr (!T::kFp8) {
-#pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                const int d = 16 * kk + 2 * tig;
-                qb[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qr + d) : 0u;
-                qb[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qr + d + 8) : 0u;
-            }
-            mult = log2e_scale;
-            vmul = 1.0f;
-        } else {
-            // q (16-bit) -> f16 operands in the element order of the fp8 K
-            // fragments: k-step kk, lane tig holds d = 16kk + 4tig + {0,1}
-            // (k = 2tig, 2tig+1) and + {2,3} (k = 2tig+8, 2tig+9).  A
-            // power-of-two pre-scale keeps every element inside f16 range.
-            float f[T::QK][4];
-            float amax = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                uint2 u = make_uint2(0, 0);
-                if (hv) u = *reinterpret_cast<const uint2 *>(qr + 16 * kk + 4 * tig);
-                const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    if (p.q_is_bf16) {
-                        f[kk][2 * e] = __uint_as_float(w[e] << 16);
-                        f[kk][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                    } else {
-                        const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-                        f[kk][2 * e] = t.x;
-                        f[kk][2 * e + 1] = t.y;
-                    }
-                    amax = fmaxf(amax, fmaxf(fabsf(f[kk][2 * e]), fabsf(f[kk][2 * e + 1])));
-                }
-            }
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
-            float qs = 1.0f;
-            while (amax * qs > 16384.0f) qs *= 0.5f;
-            float d0, d1, d2, d3, c0 = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                qb[kk][0] = pack_f16(f[kk][0] * qs, f[kk][1] * qs, d0, d1);
-                qb[kk][1] = pack_f16(f[kk][2] * qs, f[kk][3] * qs, d2, d3);
-                c0 += (d0 + d1) + (d2 + d3);
-            }
-            if constexpr (CK == kI8) {     // sum of q' over head_dim, per q head gid
-                c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
-                c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {   // head columns 2tig, 2tig+1
-                    q1h[c] = kI8Bias * __shfl_sync(0xffffffffu, c0, 4 * (2 * tig + c));
-                    zs[c] = 0.0f;
-                }
-            }
-            // per-block / per-token scales are applied per row (scores and P')
-            mult = log2e_scale * (gscale ? 1.0f : p.k_scale[kvh]) / qs;
-            vmul = gscale ? 1.0f : p.v_scale[kvh];
-        }
-#pragma unroll
-        for (int t = 0; t < T::DT / 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
-        m[0] = m[1] = NEG_INF;
-        l[0] = l[1] = 0.0f;
-    };
-
-    // d held by this lane for accumulator tile t, row half r (0: gid, 1: gid+8)
-    auto d_of = [&](int t, int r) -> int {
-        if constexpr (T::kIsU3) {
-            return 16 * gid + 2 * t + r;                     // slice code 2t + r
-        } else if constexpr (!T::kFp8) {
-            return 16 * t + 8 * r + gid;
-        } else {
-            return 32 * (t >> 1) + 4 * gid + 2 * (t & 1) + r;
-        }
-    };
-
-    auto finish_segment = [&](int64_t seg_end) {
-        const int kvh = hg * nh + warp;
-        const int64_t unit_first = int64_t(hg) * NBT + prefix[b];
-        const int64_t unit_last = unit_first + nblk[b] - 1;
-        float lt[2];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {       // sum the partial sums over the 8 token rows (gid)
-            float v = l[c];
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
-            v += __shfl_xor_sync(0xffffffffu, v, 16);
-            lt[c] = v;
-        }
-        float zt[2] = {0.0f, 0.0f};
-        if constexpr (T::kIsU3 || CK == kI8) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float z = zs[c];
-#pragma unroll
-                for (int o2 = 4; o2 < 32; o2 <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o2);
-                zt[c] = CK == kI8 ? kI8Bias * z : z;
-            }
-        }
-        // accumulator entry (t, r, c) -> value of the segment's unnormalised output
-        auto oval = [&](int t, int r, int c) -> float {
-            if constexpr (T::kIsU3) {
-                return o[t][2 * r + c] * float(1 << (24 - u3v_x(2 * t + r))) - zt[c];
-            } else if constexpr (CK == kI8) {
-                return o[t][2 * r + c] - zt[c];
-            } else {
-                return o[t][2 * r + c];
-            }
-        };
-        const bool whole = seg_start == unit_first && seg_end == unit_last;
-        const int64_t key = int64_t(blockIdx.x) + int64_t(hg) * B + b;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int g = 2 * tig + c;
-            if (g >= G) continue;
-            const int h = kvh * G + g;
-            if (whole) {
-                const float inv = lt[c] > 0.0f ? vmul / lt[c] : 0.0f;
-                uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
-#pragma unroll
-                for (int t = 0; t < T::DT / 2; ++t)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const float v = oval(t, r, c) * inv;
-                        orow[d_of(t, r)] = p.q_is_bf16 ? f2h<kBF16>(v) : f2h<kF16>(v);
-                    }
-            } else {
-                const int64_t row = key * (int64_t(nh) * G) + int64_t(warp) * G + g;
-                float *acc = f.part_acc + row * D;
-                if (gid == 0) {
-                    f.part_ml[2 * row] = m[c];
-                    f.part_ml[2 * row + 1] = lt[c];
-                }
-#pragma unroll
-                for (int t = 0; t < T::DT / 2; ++t)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) acc[d_of(t, r)] = oval(t, r, c) * vmul;
-            }
-        }
-    };
-
-    // 3-bit blocks: NB (1, or 2 for 16-token blocks) consecutive blocks of
-    // one sequence, held in stages s0 (and s1), as NB * KT tiles of 16
-    // tokens; `valid` counts the live tokens of all NB blocks (only the last
-    // block of a sequence can be partial).
-    auto u3_body = [&](auto nb_c, int s0, int s1, int valid) {
-        constexpr int NB = decltype(nb_c)::value;
-        constexpr int KTT = NB * T::KT;          // 16-token tiles of the NB blocks
-        const int kvh = hg * nh + warp;
-        const bool partial = valid < NB * BS;
-        // stage of tile t, and the tile's first row within its block
-        auto tile_stage = [&](int t) { return t < T::KT ? s0 : s1; };
-        auto tile_row = [&](int t) { return 16 * (t % T::KT); };
-        auto kpk = [&](int t) {                  // packed K rows of the tile (shared address)
-            return sbase + tile_stage(t) * L.stage_bytes + warp * BS * T::ROW + tile_row(t) * T::ROW;
-        };
-        // ---- metadata of this lane's score rows (tokens gid, gid+8 of
-        // each tile), staged with the block: [nh][BS] runs (head-major)
-        // or [BS][num_kv_heads] arrays
-        const int MH = f.meta_heads;
-        const bool hmaj = MH == nh;
-        const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? warp * BS : kvh;
-        float sk[KTT][2], zk[KTT][2], sv[KTT][2], zv[KTT][2];
-#pragma unroll
-        for (int mt = 0; mt < KTT; ++mt) {
-            const unsigned char *meta = smem + (tile_stage(mt) * L.stage_bytes + 2 * L.tile_bytes);
-            const __half *mks = reinterpret_cast<const __half *>(meta);
-            const __half *mvs = mks + BS * MH;
-            const uint8_t *mkz = meta + 4 * BS * MH;
-            const uint8_t *mvz = mkz + BS * MH;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int e = (tile_row(mt) + gid + 8 * r) * m_tok + m_h;
-                sk[mt][r] = __half2float(mks[e]);
-                sv[mt][r] = __half2float(mvs[e]);
-                zk[mt][r] = float(mkz[e]);
-                zv[mt][r] = float(mvz[e]);
-            }
-        }
-        // ---- S^T = K Q'^T with K converted straight into A fragments:
-        // lane (gid, tig) takes group tig of token rows gid and gid+8
-        float sc[KTT][4];
-#pragma unroll
-        for (int mt = 0; mt < KTT; ++mt) {
-            float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
-            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
-            const uint32_t a0 = kpk(mt) + gid * T::ROW + 12 * tig;
-            const uint32_t a1 = a0 + 8 * T::ROW;
-            const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
-            const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
-#pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                uint32_t a[4];
-                a[0] = u3k_pair(2 * kk, x0, x1, x2);
-                a[1] = u3k_pair(2 * kk, y0, y1, y2);
-                a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
-                a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
-                ptx::mma16816<false>((kk & 1) ? sx : sc[mt], a, qb[kk][0], qb[kk][1]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[mt][e] += sx[e];
-        }
-        // ---- scores: remove the zero point, apply the per-token
-        // scale, mask; online softmax per head column
-        float mx[2] = {NEG_INF, NEG_INF};
-#pragma unroll
-        for (int t = 0; t < KTT; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e >> 1, c = e & 1;
-                if (c >= NC) continue;
-                float v = mult * sk[t][r] * (sc[t][e] - zk[t][r] * q1h[c]);
-                if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
-                sc[t][e] = v;
-                mx[c] = fmaxf(mx[c], v);
-            }
-        float alpha[2] = {1.0f, 1.0f};
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-            const float mn = fmaxf(m[c], mx[c]);
-            alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
-            m[c] = mn;
-            l[c] *= alpha[c];
-            zs[c] *= alpha[c];
-        }
-        // P' = p * v_scale (0 for masked tokens) as the B operand of PV
-        uint32_t pbf[KTT][2];
-#pragma unroll
-        for (int t = 0; t < KTT; ++t)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
-                const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
-                const float p1 = NC > 1 ? exp2_approx(sc[t][2 * r + 1] - m[1]) : 0.0f;
-                l[0] += p0;
-                if (NC > 1) l[1] += p1;
-                float q0, q1;
-                const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
-                zs[0] += q0 * zv[t][r];
-                if (NC > 1) zs[1] += q1 * zv[t][r];
-                pbf[t][r] = ptx::movmatrix_trans(w);
-            }
-        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-            for (int t = 0; t < T::DT / 2; ++t) {
-                o[t][0] *= alpha[0];
-                o[t][2] *= alpha[0];
-                if (NC > 1) {
-                    o[t][1] *= alpha[1];
-                    o[t][3] *= alpha[1];
-                }
-            }
-        }
-        // ---- O^T += V'^T P'^T with V converted straight into A
-        // fragments: lane (gid, tig) owns codes 16gid .. 16gid+15 (row
-        // bytes 6gid .. 6gid+5) of tokens 2tig, 2tig+1 (k = 2tig, 2tig+1)
-        // and 2tig+8, 2tig+9; tile md holds codes 2md (row gid) and
-        // 2md+1 (row gid+8) of the slices.  X / Y are slice bytes 0-3 / 2-5.
-        const int sxy = 16 * (gid & 1);
-#pragma unroll
-        for (int kt = 0; kt < KTT; ++kt) {
-            const uint32_t vlane = kpk(kt) + L.tile_bytes + ((6 * gid) & ~3);   // packed V rows
-            uint32_t X[4], Y[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = 2 * tig + (i & 1) + 8 * (i >> 1);
-                const uint32_t w0 = ld_shared_u32(vlane + tok * T::ROW);
-                const uint32_t w1 = ld_shared_u32(vlane + tok * T::ROW + 4);
-                X[i] = __funnelshift_r(w0, w1, sxy);
-                Y[i] = __funnelshift_rc(w0, w1, sxy + 16);
-            }
-            uint32_t win[2][6];
-#pragma unroll
-            for (int tp = 0; tp < 2; ++tp) {
-                win[tp][0] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x5410u);
-                win[tp][1] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x6521u);
-                win[tp][2] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x7632u);
-                win[tp][3] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x6521u);
-                win[tp][4] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7632u);
-                win[tp][5] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7733u);
-            }
-#pragma unroll
-            for (int md = 0; md < T::DT / 2; ++md) {
-                constexpr uint32_t kMask3 = 0x00070007u;
-                uint32_t a[4];
-                a[0] = win[0][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
-                a[1] = win[0][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
-                a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
-                a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
-                ptx::mma16816<false>(o[md], a, pbf[kt][0], pbf[kt][1]);
-            }
-        }
-    };
-
-    start_segment();
-    int cs = 0;                  // stage of the current block
-    uint32_t cphase = 0;         // parity of its fill round
-    for (; x < hi; ++x) {
-        const int s = cs;
-        if (!ptx::mbar_wait_bounded(bar_full + 8 * s, cphase, kTimeoutNs)) {
-            raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
-            return;
-        }
-        if (++cs == stages) {
-            cs = 0;
-            cphase ^= 1u;
-        }
-        // valid tokens of this block (only the last block of a sequence is partial)
-        const int valid = min(BS, ctx_b - j * BS);
-        const int spb = stage_pb[s];
-        if (spb >= 0 && !T::kIsU3) {
-            // fp8 / int8 per-block or per-token scales of this warp's head,
-            // staged with the block: [nh][GS] K scales, then V scales
-            const float *gsk = reinterpret_cast<const float *>(smem + s * L.stage_bytes + 2 * L.tile_bytes) +
-                               warp * GS;
-            const float *gsv = gsk + nh * GS;
-            auto row_ks = [&](int tok) { return gsk[GS == 1 ? 0 : tok]; };
-            auto row_vs = [&](int tok) { return gsv[GS == 1 ? 0 : tok]; };
-            const uint32_t ktile = sbase + s * L.stage_bytes + warp * BS * 128;
-            const uint32_t vtile = ktile + L.tile_bytes;
-            const int half_bytes = L.tile_bytes / T::HALVES;
-            const int mi = lane >> 3;    // ldmatrix: which 8x8 matrix this lane addresses
-            // ---------------- S^T = K Q^T
-            float sc[T::KT][4];
-#pragma unroll
-            for (int t = 0; t < T::KT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-#pragma unroll
-                for (int mt = 0; mt < T::KT; ++mt) {
-                    uint32_t a[4];
-                    if constexpr (!T::kFp8) {
-                        // matrices: (tok 0-7 | 8-15) x (d chunk 2kk | 2kk+1)
-                        const int tok = 16 * mt + 8 * (mi & 1) + (lane & 7);
-                        const int chunk = 2 * kk + (mi >> 1);
-                        ptx::ldmatrix_x4(ktile + (chunk >> 3) * half_bytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4),
-                                         a[0], a[1], a[2], a[3]);
-                    } else {
-                        // rows 16mt+gid and +8 share the swizzle phase gid: the
-                        // address is (row base | gid << 4) ^ (kk << 4)
-                        const uint32_t kb = (ktile + (16 * mt + gid) * 128 + 4 * tig) | (uint32_t(gid) << 4);
-                        const uint32_t w0 = ld_shared_u32(kb ^ uint32_t((kk & 7) << 4));
-                        const uint32_t w1 = ld_shared_u32((kb + 8 * 128) ^ uint32_t((kk & 7) << 4));
-                        a[0] = f16x2_from_fp8x2<CK>(w0);
-                        a[1] = f16x2_from_fp8x2<CK>(w1);
-                        a[2] = f16x2_from_fp8x2<CK>(w0 >> 16);
-                        a[3] = f16x2_from_fp8x2<CK>(w1 >> 16);
-                    }
-                    ptx::mma16816<T::kBF>(sc[mt], a, qb[kk][0], qb[kk][1]);
-                }
-            }
-            // ---------------- online softmax per q head (columns), log2 units
-            const bool partial = valid < BS;   // only a sequence's last block
-            float mx[2] = {NEG_INF, NEG_INF};
-#pragma unroll
-            for (int t = 0; t < T::KT; ++t) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = (CK == kI8 ? sc[t][e] - q1h[e & 1] : sc[t][e]) * mult;
-                    if (T::kFp8 && gscale) v *= row_ks(16 * t + gid + 8 * (e >> 1));
-                    if (partial) {
-                        const int tok = 16 * t + gid + 8 * (e >> 1);
-                        v = tok < valid ? v : NEG_INF;
-                    }
-                    sc[t][e] = v;
-                    mx[e & 1] = fmaxf(mx[e & 1], v);
-                }
-            }
-            float alpha[2];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-                const float mn = fmaxf(m[c], mx[c]);
-                alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
-                m[c] = mn;
-                l[c] *= alpha[c];
-                if constexpr (CK == kI8) zs[c] *= alpha[c];
-            }
-            // P^T as the B operand of the PV product: pack each 8-token half
-            // of a tile (rows = tokens, cols = heads) and transpose it in
-            // registers, giving lane (gid, tig) tokens 2tig, 2tig+1 of head gid.
-            uint32_t pb[T::KT][2];
-#pragma unroll
-            for (int t = 0; t < T::KT; ++t) {
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
-                    const float p1 = exp2_approx(sc[t][2 * r + 1] - m[1]);
-                    l[0] += p0;
-                    l[1] += p1;
-                    // per-block / per-token V scales fold into P' = p * scale
-                    const float vsr = T::kFp8 && gscale ? row_vs(16 * t + gid + 8 * r) : 1.0f;
-                    float q0, q1;
-                    const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0 * vsr, p1 * vsr, q0, q1);
-                    if constexpr (CK == kI8) {   // the PV operand's offset: sum of P' as rounded
-                        zs[0] += q0;
-                        zs[1] += q1;
-                    }
-                    pb[t][r] = ptx::movmatrix_trans(w);
-                }
-            }
-            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-                for (int t = 0; t < T::DT / 2; ++t) {
-                    o[t][0] *= alpha[0];
-                    o[t][1] *= alpha[1];
-                    o[t][2] *= alpha[0];
-                    o[t][3] *= alpha[1];
-                }
-            }
-            // ---------------- O^T += V^T P^T
-#pragma unroll
-            for (int kt = 0; kt < T::KT; ++kt) {
-                if constexpr (!T::kFp8) {
-                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (partial) {  // zero V of masked tokens (0 * NaN would poison O)
-                        const int t0 = 16 * kt + 2 * tig;
-                        mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-                        mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-                    }
-#pragma unroll
-                    for (int md = 0; md < T::DT / 2; ++md) {
-                        // matrices: (tok 0-7 | 8-15) x (d chunk 2md | 2md+1), transposed
-                        const int tok = 16 * kt + 8 * (mi >> 1) + (lane & 7);
-                        const int chunk = 2 * md + (mi & 1);
-                        uint32_t a[4];
-                        ptx::ldmatrix_x4_trans(vtile + (chunk >> 3) * half_bytes + tok * 128 +
-                                                   (((chunk & 7) ^ (tok & 7)) << 4),
-                                               a[0], a[1], a[2], a[3]);
-                        a[0] &= mlo;
-                        a[1] &= mlo;
-                        a[2] &= mhi;
-                        a[3] &= mhi;
-                        ptx::mma16816<T::kBF>(o[md], a, pb[kt][0], pb[kt][1]);
-                    }
-                } else {
-                    const int t0 = 16 * kt + 2 * tig;
-                    const int rows[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
-                    // row i's address for chunk 2q4 + (gid >> 2) is
-                    // (row base | ((gid >> 2) ^ (row & 7)) << 4) ^ (q4 << 5)
-                    uint32_t vb[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        vb[i] = (vtile + rows[i] * 128 + (gid & 3) * 4) | (uint32_t((gid >> 2) ^ (rows[i] & 7)) << 4);
-#pragma unroll
-                    for (int q4 = 0; q4 < D / 32; ++q4) {
-                        // bytes d = 32q4 + 4gid .. +3 of the four token rows;
-                        // tile 2q4 takes bytes 0 (rows gid) and 1 (rows gid+8),
-                        // tile 2q4+1 bytes 2 and 3
-                        uint32_t w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            w[i] = ld_shared_u32(vb[i] ^ uint32_t((q4 & 3) << 5));
-                            if (partial && rows[i] >= valid) w[i] = 0u;
-                        }
-#pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {
-                            const uint32_t sel = (2 * hb) | ((2 * hb + 4) << 4) | ((2 * hb + 1) << 8) | ((2 * hb + 5) << 12);
-                            const uint32_t x01 = ptx::prmt(w[0], w[1], sel);
-                            const uint32_t x23 = ptx::prmt(w[2], w[3], sel);
-                            uint32_t a[4];
-                            a[0] = f16x2_from_fp8x2<CK>(x01);
-                            a[1] = f16x2_from_fp8x2<CK>(x01 >> 16);
-                            a[2] = f16x2_from_fp8x2<CK>(x23);
-                            a[3] = f16x2_from_fp8x2<CK>(x23 >> 16);
-                            ptx::mma16816<false>(o[2 * q4 + hb], a, pb[kt][0], pb[kt][1]);
-                        }
-                    }
-                }
-            }
-        }
-        if constexpr (T::kIsU3) {
-            // 16-token blocks go two at a time when the next unit continues
-            // the sequence: the per-block softmax, barrier and walk work is
-            // then shared by 32 tokens
-            const bool pair = BS == 16 && x + 1 < hi && j + 1 < nblk[b];
-            if (pair) {
-                const int s1 = cs;
-                if (!ptx::mbar_wait_bounded(bar_full + 8 * s1, cphase, kTimeoutNs)) {
-                    raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
-                    return;
-                }
-                if (++cs == stages) {
-                    cs = 0;
-                    cphase ^= 1u;
-                }
-                const int spb1 = stage_pb[s1];
-                const int valid1 = min(BS, ctx_b - (j + 1) * BS);
-                if (spb >= 0 && spb1 >= 0) {
-                    u3_body(std::integral_constant<int, 2>{}, s, s1, BS + valid1);
-                } else {
-                    if (spb >= 0) u3_body(std::integral_constant<int, 1>{}, s, s, valid);
-                    if (spb1 >= 0) u3_body(std::integral_constant<int, 1>{}, s1, s1, valid1);
-                }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s1);
-                ++j;             // the pair's first block is never its sequence's last
-                ++x;
-            } else if (spb >= 0) {
-                u3_body(std::integral_constant<int, 1>{}, s, s, valid);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
-        // advance the walk; close the segment at a unit boundary
-        if (x + 1 < hi) {
-            if (++j == nblk[b]) {
-                finish_segment(x);
-                j = 0;
-                do {
-                    if (++b == B) {
-                        b = 0;
-                        ++hg;
-                    }
-                } while (nblk[b] == 0);
-                seg_start = x + 1;
-                start_segment();
-            }
-        } else {
-            finish_segment(x);
-        }
-    }
-}
-
-// floor(a / n) for 0 <= a < 2^62, 0 < n < 2^31: a float estimate corrected
-// by exact integer comparisons (cheaper than a 64-bit division).
-__device__ __forceinline__ int64_t floordiv_i64(int64_t a, int64_t n)
-{
-    int64_t q = int64_t(__fdividef(float(a), float(n)));
-    while (q > 0 && q * n > a) --q;
-    while ((q + 1) * n <= a) ++q;
-    return q;
-}
-
-// Merge the partials of units split across CTAs (one warp per (sequence,
-// q head)); units held whole by one CTA were written by it, units with an
-// empty context get zeros.
-constexpr int kMergeBatch = 8;   // partials a row combines in one round trip
-
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f)
-{
-    // launched as a programmatic dependent of the decode kernel: wait until
-    // that grid has completed and its writes are visible
-    griddep_wait();
-    const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (w >= p.batch * p.num_heads) return;
-    const int b = w / p.num_heads, h = w % p.num_heads;
-    const int G = p.group, nh = f.nh;
-    const int kvh = h / G, hg = kvh / nh;
-    const int local = h - hg * nh * G;
-    const int64_t NBT = f.prefix[p.batch];
-    const int64_t N = NBT * f.n_hg;
-    const int n = f.prefix[b + 1] - f.prefix[b];
-    constexpr int EPL = D / 32;
-    uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
-    float acc[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-    if (n > 0) {
-        const int64_t S = f.grid;
-        const int64_t first = int64_t(hg) * NBT + f.prefix[b];
-        // CTA i streams [i*N/S, (i+1)*N/S): the owner of flat index x is
-        // floor(((x+1)*S - 1) / N)
-        const int64_t i0 = floordiv_i64((first + 1) * S - 1, N);
-        const int64_t i1 = floordiv_i64((first + n) * S - 1, N);
-        if (i0 == i1) return;                         // written whole by CTA i0
-        const int64_t unit = int64_t(hg) * p.batch + b;
-        const int64_t stride = int64_t(nh) * G;      // partial rows per CTA slot
-        // with fewer blocks than CTAs some CTAs have an empty range and wrote
-        // nothing (never the case when N >= S)
-        auto live = [&](int64_t i) { return !(N < S && (i * N) / S == ((i + 1) * N) / S); };
-        const int64_t np = i1 - i0 + 1;               // partials (CTA slots) to combine
-        float M = NEG_INF, Lsum = 0.0f;
-        if (np <= kMergeBatch) {
-            // one round trip: lane k loads (m, l) of partial k while every
-            // lane loads its head_dim slice of all partials
-            float v[kMergeBatch][EPL];
-#pragma unroll
-            for (int k = 0; k < kMergeBatch; ++k) {
-                const bool ok = k < np && live(i0 + k);
-                const float *pa = f.part_acc + ((i0 + k + unit) * stride + local) * D + EPL * lane;
-                if constexpr (EPL == 4) {
-                    const float4 t = ok ? *reinterpret_cast<const float4 *>(pa) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[k][0] = t.x;
-                    v[k][1] = t.y;
-                    v[k][2] = t.z;
-                    v[k][3] = t.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) v[k][e] = ok ? pa[e] : 0.0f;
-                }
-            }
-            float mi = NEG_INF, li = 0.0f;
-            if (lane < np && live(i0 + lane)) {
-                const int64_t row = (i0 + lane + unit) * stride + local;
-                mi = f.part_ml[2 * row];
-                li = f.part_ml[2 * row + 1];
-            }
-            M = mi;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float wgt = mi == NEG_INF ? 0.0f : exp2_approx(mi - M);
-            Lsum = li * wgt;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-#pragma unroll
-            for (int k = 0; k < kMergeBatch; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, wgt, k);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] += v[k][e] * wk;
-            }
-        } else {
-            // many partials (a long sequence over many CTAs): lanes over the
-            // partials for the maximum and the weights, then lanes over
-            // head_dim for the accumulation, 32 partials at a time
-            for (int64_t c = i0; c <= i1; c += 32) {
-                const int64_t i = c + lane;
-                if (i <= i1 && live(i)) M = fmaxf(M, f.part_ml[2 * ((i + unit) * stride + local)]);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            for (int64_t c = i0; c <= i1; c += 32) {
-                const int64_t i = c + lane;
-                float wgt = 0.0f;
-                if (i <= i1 && live(i)) {
-                    const int64_t row = (i + unit) * stride + local;
-                    const float mi = f.part_ml[2 * row];
-                    wgt = mi == NEG_INF ? 0.0f : exp2_approx(mi - M);
-                    Lsum += f.part_ml[2 * row + 1] * wgt;
-                }
-                const int cnt = int(i1 - c + 1 < 32 ? i1 - c + 1 : 32);
-                for (int k = 0; k < cnt; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, wgt, k);
-                    if (wk == 0.0f) continue;       // uniform; also skips unwritten slots
-                    const float *pa = f.part_acc + ((c + k + unit) * stride + local) * D + EPL * lane;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc[e] += pa[e] * wk;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-        }
-        const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] *= inv;
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e)
-        orow[EPL * lane + e] = p.q_is_bf16 ? f2h<kBF16>(acc[e]) : f2h<kF16>(acc[e]);
-}
 
 // ---------------------------------------------------------------- host side
 
@@ -1153,8 +26,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // 4-D map over one cache: (row element, slot, kv head, block) with the
 // caller's strides; box = one 128-byte swizzled sub-row (16-bit / fp8) or one
 // whole packed row (3-bit, no swizzle) x block_size slots x nh heads.
+// x-vectorised caches (c_chunk != 16 bytes between a row's 16-byte pieces):
+// 5-D map (element in piece, slot, piece, kv head, block), box = the whole
+// [nh][head_dim/x][block_size][x] tile, no swizzle.
 bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, int P, int64_t c_slot,
-              int64_t c_head, int64_t c_blk, int nh)
+              int64_t c_head, int64_t c_blk, int64_t c_chunk, int nh)
 {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -1163,6 +39,17 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
     const CUtensorMapDataType dt = (is_q8(ck) || u3) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : ck == kBF16        ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (c_chunk != 16) {
+        if (u3) return false;
+        const int x = 16 / es;
+        cuuint64_t dims[5] = {cuuint64_t(x), cuuint64_t(BS), cuuint64_t(D / x), cuuint64_t(Hkv), cuuint64_t(P)};
+        cuuint64_t strides[4] = {cuuint64_t(c_slot), cuuint64_t(c_chunk), cuuint64_t(c_head), cuuint64_t(c_blk)};
+        cuuint32_t box[5] = {cuuint32_t(x), cuuint32_t(BS), cuuint32_t(D / x), cuuint32_t(nh), 1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        return enc(m, dt, 5, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     const int row_elems = u3 ? 3 * D / 8 : D;
     cuuint64_t dims[4] = {cuuint64_t(row_elems), cuuint64_t(BS), cuuint64_t(Hkv), cuuint64_t(P)};
     cuuint64_t strides[3] = {cuuint64_t(c_slot), cuuint64_t(c_head), cuuint64_t(c_blk)};
@@ -1173,28 +60,6 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
                            u3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-template <int CK, int D, int BS, bool G1 = false, bool GSC = false>
-cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
-                          const CUtensorMap &mv, cudaStream_t s)
-{
-    auto kern = decode_tma_kernel<CK, D, BS, G1, GSC>;
-    // dynamic shared memory limit, raised once per device as needed
-    static std::atomic<int> configured[kMaxDevices];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (configured[dev].load(std::memory_order_relaxed) < f.smem_bytes) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem_bytes);
-        if (e != cudaSuccess) return e;
-        configured[dev].store(f.smem_bytes, std::memory_order_relaxed);
-    }
-    e = launch_pdl(kern, dim3(f.grid), dim3((f.nh + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
-    if (e != cudaSuccess) return e;
-    const int rows = p.batch * p.num_heads;
-    return launch_pdl(merge_kernel<D>, dim3((rows + 7) / 8), dim3(256), 0, s, p, f);
 }
 
 template <int CK, int D>
@@ -1287,9 +152,9 @@ bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh)
 {
     CUtensorMap mk, mv;
     return make_map(&mk, p.k_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
-                    p.c_head, p.c_blk, nh) &&
+                    p.c_head, p.c_blk, p.c_chunk, nh) &&
            make_map(&mv, p.v_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
-                    p.c_head, p.c_blk, nh);
+                    p.c_head, p.c_blk, p.c_chunk, nh);
 }
 
 cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_kind, void *ws, size_t ws_bytes,
@@ -1305,10 +170,11 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
     f.part_acc = reinterpret_cast<float *>(c + prefix_bytes + ml_bytes);
     CUtensorMap mk, mv;
     if (!make_map(&mk, p.k_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
-                  p.c_head, p.c_blk, f.nh) ||
+                  p.c_head, p.c_blk, p.c_chunk, f.nh) ||
         !make_map(&mv, p.v_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
-                  p.c_head, p.c_blk, f.nh))
+                  p.c_head, p.c_blk, p.c_chunk, f.nh))
         return cudaErrorInvalidValue;
+    if (p.c_chunk != 16) return launch_decode_fast_xv(p, f, cache_kind, &mk, &mv, s);
     if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
     if (cache_kind == kE5M2) return launch_fast_bs<kE5M2, 128>(p, f, mk, mv, s);
     if (cache_kind == kI8) return launch_fast_bs<kI8, 128>(p, f, mk, mv, s);

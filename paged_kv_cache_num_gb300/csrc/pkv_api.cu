@@ -80,6 +80,7 @@ struct CacheInfo {
     int64_t num_blocks, block_size, num_kv_heads, head_dim;
     int scale_mode;                       // PKV_SCALE_* (fp8 / int8 caches)
     int64_t gs_blk, gs_slot, gs_head;     // strides of the per-block / per-token scales
+    int64_t c_chunk;                      // bytes between the 16-byte pieces of a row
 };
 
 // Validate a pkv_cache; head_dim comes from the row length and the dtype.
@@ -109,6 +110,16 @@ int check_cache(const pkv_cache *c, CacheInfo &ci, bool any_block_size = false)
             return fail(PKV_ERR_LAYOUT, "cache stride %d is not a multiple of 16 bytes", i);
     if (!aligned(k.data, 16) || !aligned(v.data, 16))
         return fail(PKV_ERR_LAYOUT, "cache base pointers must be 16-byte aligned");
+    ci.c_chunk = 16;
+    if (c->chunk_stride != 0) {     // x-vectorised rows: pieces of 16 bytes
+        if (kind == PKV_DTYPE_U3)
+            return fail(PKV_ERR_UNSUPPORTED, "chunk_stride does not apply to U3 caches");
+        if (c->chunk_stride < 0 || (c->chunk_stride * es) % 16 != 0)
+            return fail(PKV_ERR_LAYOUT, "chunk_stride must be a positive multiple of 16 bytes");
+        if ((k.shape[3] * es) % 16 != 0)
+            return fail(PKV_ERR_SHAPE, "head_dim must be a multiple of x = 16 bytes / element size");
+        ci.c_chunk = c->chunk_stride * es;
+    }
     ci.kind = kind;
     ci.num_blocks = k.shape[0];
     ci.block_size = k.shape[1];
@@ -296,6 +307,7 @@ static int prep_kv_append(const pkv_tensor *k_new, const pkv_tensor *v_new, cons
     p.c_blk = cache->k_cache.stride[0] * ces;
     p.c_slot = cache->k_cache.stride[1] * ces;
     p.c_head = cache->k_cache.stride[2] * ces;
+    p.c_chunk = ci.c_chunk;
     p.k_scale = cache->k_scale;
     p.v_scale = cache->v_scale;
     p.scale_mode = ci.scale_mode;
@@ -423,6 +435,7 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
     p.c_blk = cache->k_cache.stride[0] * ces;
     p.c_slot = cache->k_cache.stride[1] * ces;
     p.c_head = cache->k_cache.stride[2] * ces;
+    p.c_chunk = ci.c_chunk;
     p.k_scale = cache->k_scale;
     p.v_scale = cache->v_scale;
     p.scale_mode = ci.scale_mode;
@@ -476,6 +489,8 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
     }
     if (ci.scale_mode != PKV_SCALE_PER_HEAD)
         gs_ok = gs_ok && aligned(p.k_gs, 16) && aligned(p.v_gs, 16);
+    // x-vectorised caches: the persistent kernel with per-head scales
+    if (ci.c_chunk != 16 && ci.scale_mode != PKV_SCALE_PER_HEAD) gs_ok = false;
     if (num_splits == 0 && gs_ok &&
         pkv::fast_decode_supported(ci.kind, p.head_dim, p.block_size, p.group, p.batch)) {
         // q rows are read 16 (3-bit), 8 (fp8) or 4 (16-bit) bytes at a time

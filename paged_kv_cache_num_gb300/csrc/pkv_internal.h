@@ -25,6 +25,7 @@ struct AppendParams {
     char *k_cache;
     char *v_cache;
     int64_t c_blk, c_slot, c_head;  // byte strides of K and V caches (equal)
+    int64_t c_chunk;            // byte stride between the 16-byte pieces of a row (16: contiguous)
     // fp8 / int8 scales: per kv head, or (scale_mode 1 / 2) an array indexed
     // blk * gs_blk + slot * gs_slot + head * gs_head (gs_slot = 0 per block)
     const float *k_scale;
@@ -77,6 +78,7 @@ struct DecodeParams {
     const char *k_cache;
     const char *v_cache;
     int64_t c_blk, c_slot, c_head;  // byte strides (K and V equal)
+    int64_t c_chunk;            // byte stride between the 16-byte pieces of a row (16: contiguous)
     const float *k_scale;
     const float *v_scale;
     int scale_mode;             // 0 per kv head, 1 per block, 2 per token (see AppendParams)
@@ -138,6 +140,10 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
                int max_blocks, int cache_kind, bool meta_head_major, int sm_count, FastParams &f,
                size_t &workspace, int q8_scales_per_head = 0);
 bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh);
+// x-vectorised caches (c_chunk != 16): 16-bit or one-byte codes with
+// per-head scales, head_dim 128 (16-bit also 64), block size 16 / 32 / 64
+cudaError_t launch_decode_fast_xv(const DecodeParams &p, const FastParams &f, int cache_kind,
+                                  const void *tmk, const void *tmv, cudaStream_t s);
 
 cudaError_t launch_decode(const DecodeParams &p, int cache_kind, int q_kind, cudaStream_t s);
 cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_kind, void *ws,

@@ -45,7 +45,7 @@ class _Cache(ctypes.Structure):
     _fields_ = [("k_cache", _Tensor), ("v_cache", _Tensor), ("k_scale", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("k_qscale", _Tensor), ("k_qzero", _Tensor),
                 ("v_qscale", _Tensor), ("v_qzero", _Tensor), ("scale_mode", ctypes.c_int32),
-                ("k_scales", _Tensor), ("v_scales", _Tensor)]
+                ("k_scales", _Tensor), ("v_scales", _Tensor), ("chunk_stride", ctypes.c_int64)]
 
 
 # scale granularity of fp8 / int8 caches (pkv.h PKV_SCALE_*)
@@ -118,6 +118,20 @@ def _desc(t: Optional[torch.Tensor], code: Optional[int] = None) -> _Tensor:
     return d
 
 
+def _xvec_desc(t: torch.Tensor, code: int) -> _Tensor:
+    if t.dim() != 5 or t.stride(4) != 1:
+        raise ValueError("an xvec cache is [num_blocks, Hkv, head_dim // x, block_size, x], x contiguous")
+    d = _Tensor()
+    d.data = t.data_ptr() if t.numel() > 0 else 0
+    d.dtype = code
+    d.ndim = 4
+    P, H, C, BS, x = t.shape
+    for i, (n, st) in enumerate(((P, t.stride(0)), (BS, t.stride(3)), (H, t.stride(1)), (C * x, 1))):
+        d.shape[i] = n
+        d.stride[i] = st
+    return d
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -139,7 +153,9 @@ class KVCache:
     """A paged KV cache [num_blocks, block_size, num_kv_heads, row] in device
     memory.  kind: "f16", "bf16", "e4m3" / "e5m2" / "i8" (+ per-kv-head fp32 scales) or "u3"
     (3-bit codes, row = 3*head_dim/8 bytes, + fp16 scale / uint8 zero per
-    (slot, head))."""
+    (slot, head)).  layout "xvec" (16-bit and one-byte kinds): k_cache /
+    v_cache are stored [num_blocks, num_kv_heads, head_dim // x, block_size,
+    x] with x = 16 bytes / element size."""
     kind: str
     k_cache: torch.Tensor
     v_cache: torch.Tensor
@@ -155,6 +171,7 @@ class KVCache:
     scale_mode: str = "head"
     k_scales: Optional[torch.Tensor] = None
     v_scales: Optional[torch.Tensor] = None
+    layout: str = "flash"
 
     @property
     def num_blocks(self):
@@ -162,26 +179,53 @@ class KVCache:
 
     @property
     def block_size(self):
-        return self.k_cache.shape[1]
+        return self.k_cache.shape[3 if self.layout == "xvec" else 1]
 
     @property
     def num_kv_heads(self):
-        return self.k_cache.shape[2]
+        return self.k_cache.shape[1 if self.layout == "xvec" else 2]
 
     @property
     def head_dim(self):
+        if self.layout == "xvec":
+            return self.k_cache.shape[2] * self.k_cache.shape[4]
         r = self.k_cache.shape[3]
         return r * 8 // 3 if self.kind == "u3" else r
 
     @staticmethod
     def allocate(kind: str, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
                  device="cuda", k_scale=None, v_scale=None, fill=None, scale_mode: str = "head",
-                 k_scales=None, v_scales=None) -> "KVCache":
+                 k_scales=None, v_scales=None, layout: str = "flash") -> "KVCache":
         """A cache of `kind`; fp8 / int8 caches take per-head scales (k_scale,
         v_scale), per-block scales (scale_mode "block": k_scales / v_scales
         [num_blocks, Hkv]) or per-token scales (scale_mode "token": arrays
-        allocated here, written by kv_append_scaled)."""
+        allocated here, written by kv_append_scaled).  layout "xvec": the
+        x-vectorised storage [num_blocks, Hkv, head_dim // x, block_size, x]."""
         shape = (num_blocks, block_size, num_kv_heads)
+        if layout == "xvec":
+            if kind not in ("f16", "bf16", "e4m3", "e5m2", "i8"):
+                raise ValueError("layout xvec applies to 16-bit and one-byte caches")
+            dt = {"f16": torch.float16, "bf16": torch.bfloat16, "i8": torch.int8}.get(kind, torch.uint8)
+            x = 16 // torch.empty((), dtype=dt).element_size()
+            if head_dim % x:
+                raise ValueError("head_dim must be a multiple of x = %d" % x)
+            k = torch.empty((num_blocks, num_kv_heads, head_dim // x, block_size, x), dtype=dt,
+                            device=device)
+            v = torch.empty_like(k)
+            c = KVCache(kind, k, v, k_scale=k_scale, v_scale=v_scale, scale_mode=scale_mode,
+                        layout="xvec")
+            if scale_mode == "block":
+                c.k_scales, c.v_scales = k_scales, v_scales
+            elif scale_mode == "token":
+                hm = (num_blocks, num_kv_heads, block_size)
+                c.k_scales = torch.ones(hm, dtype=torch.float32, device=device).permute(0, 2, 1)
+                c.v_scales = torch.ones(hm, dtype=torch.float32, device=device).permute(0, 2, 1)
+            if fill is not None:
+                for t in (k, v):
+                    t.view(torch.uint8).fill_(fill)
+            return c
+        elif layout != "flash":
+            raise ValueError(layout)
         if kind in ("f16", "bf16"):
             dt = torch.float16 if kind == "f16" else torch.bfloat16
             k = torch.empty(shape + (head_dim,), dtype=dt, device=device)
@@ -231,8 +275,14 @@ class KVCache:
     def _build_struct(self) -> _Cache:
         s = _Cache()
         code = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2, "i8": I8, "u3": U3}[self.kind]
-        s.k_cache = _desc(self.k_cache, code)
-        s.v_cache = _desc(self.v_cache, code)
+        if self.layout == "xvec":
+            # [P, Hkv, D/x, BS, x] described as [P, BS, Hkv, D] + the piece stride
+            s.k_cache = _xvec_desc(self.k_cache, code)
+            s.v_cache = _xvec_desc(self.v_cache, code)
+            s.chunk_stride = self.k_cache.stride(2)
+        else:
+            s.k_cache = _desc(self.k_cache, code)
+            s.v_cache = _desc(self.v_cache, code)
         if self.kind in ("e4m3", "e5m2", "i8") and self.scale_mode == "head":
             if self.k_scale is None or self.v_scale is None:
                 raise ValueError("fp8 / int8 cache needs k_scale / v_scale")

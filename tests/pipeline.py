@@ -30,7 +30,8 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
                                  v_scale=None if w.v_scale is None else w.v_scale.to(dev),
                                  fill=0, scale_mode=w.scale_mode,
                                  k_scales=None if w.k_block_scale is None else w.k_block_scale.to(dev),
-                                 v_scales=None if w.v_block_scale is None else w.v_block_scale.to(dev))
+                                 v_scales=None if w.v_block_scale is None else w.v_block_scale.to(dev),
+                                 layout=w.layout)
     tok = w.scale_mode == "token"
 
     def append(kn, vn, sm, ks=None, vs=None):
@@ -42,8 +43,8 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
         for name in ("k_qscale", "k_qzero", "v_qscale", "v_qzero"):
             setattr(cache, name, torch.zeros_like(getattr(cache, name).contiguous()))
     if w.k_cache0 is not None:
-        cache.k_cache.copy_(w.k_cache0.to(dev))
-        cache.v_cache.copy_(w.v_cache0.to(dev))
+        cache.k_cache.copy_(W.storage(w.k_cache0, w.layout).to(dev))
+        cache.v_cache.copy_(W.storage(w.v_cache0, w.layout).to(dev))
     bt = w.block_tables.to(dev)
     if err_flag is None:
         err_flag = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -70,7 +71,7 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
 
 
 def gpu_cache_host(cache):
-    """Host numpy copies of every cache array (bit patterns)."""
+    """Host numpy copies of every cache array (bit patterns), as stored."""
     d = {}
     for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero", "k_scales",
                  "v_scales"):

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_version(lib):
     from paged_kv_cache_num_gb300 import pkv
     assert "sm_103a" in pkv.version()
-    assert lib.pkv_abi_version() == 2
+    assert lib.pkv_abi_version() == 3
 
 
 def _fake(shape, dtype, strides=None, ptr=0x10000):
@@ -129,6 +129,39 @@ def test_decode_validation_errors(lib):
     outb = _fake((B, Hq, D), pkv.BF16)
     assert lib.pkv_paged_decode(by(q), by(c), by(bt), by(cl), ctypes.c_float(0.125), by(outb), 1,
                                 None, 0, None, None) == -2
+
+
+def test_xvec_cache_validation(lib):
+    """chunk_stride (the x-vectorised layout) is checked before any launch:
+    workspace queries only, the pointers being fake."""
+    from paged_kv_cache_num_gb300 import pkv
+    B, Hq, H, D, P, BS = 2, 4, 2, 64, 4, 16
+    q, bt = _fake((B, Hq, D), pkv.F16), _fake((B, 5), pkv.I32)
+    by = ctypes.byref
+    n = ctypes.c_size_t(0)
+    x = 8
+    strides = (H * D * BS, x, D * BS, 1)      # [P, Hkv, D/x, BS, x] seen as [P, BS, Hkv, D]
+    c = pkv._Cache()
+    c.k_cache = _fake((P, BS, H, D), pkv.F16, strides)
+    c.v_cache = _fake((P, BS, H, D), pkv.F16, strides, ptr=0x20000)
+    c.chunk_stride = BS * x
+    assert lib.pkv_paged_decode_workspace(by(q), by(c), by(bt), 0, by(n)) == 0
+    c.chunk_stride = 4                         # 8 bytes: not a multiple of 16
+    assert lib.pkv_paged_decode_workspace(by(q), by(c), by(bt), 0, by(n)) == -4
+    c.chunk_stride = -BS * x
+    assert lib.pkv_paged_decode_workspace(by(q), by(c), by(bt), 0, by(n)) == -4
+    cu = _cache(pkv.U3, H=H, D=128)
+    cu.chunk_stride = 16
+    q128 = _fake((B, Hq, 128), pkv.F16)
+    assert lib.pkv_paged_decode_workspace(by(q128), by(cu), by(bt), 0, by(n)) == -5
+    # one-byte codes: x = 16 elements, head_dim 72 is not a multiple of it
+    c8 = pkv._Cache()
+    c8.k_cache = _fake((P, BS, H, 72), pkv.E4M3, (H * 72 * BS, 16, 72 * BS, 1))
+    c8.v_cache = _fake((P, BS, H, 72), pkv.E4M3, (H * 72 * BS, 16, 72 * BS, 1), ptr=0x20000)
+    c8.k_scale = c8.v_scale = 0x30000
+    c8.chunk_stride = BS * 16
+    q72 = _fake((B, Hq, 72), pkv.F16)
+    assert lib.pkv_paged_decode_workspace(by(q72), by(c8), by(bt), 0, by(n)) == -3
 
 
 def test_pack_validation(lib):

@@ -52,7 +52,8 @@ import torch
 
 SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44,
          "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48, "i8_long": 49,
-         "fp8_long_token_scales": 50, "fp8_long_block_scales": 51}
+         "fp8_long_token_scales": 50, "fp8_long_block_scales": 51,
+         "gqa_bf16_xvec": 43, "fp8_long_xvec": 45}
 
 
 @dataclass
@@ -95,6 +96,9 @@ class Workload:
     k_new_scale: Optional[torch.Tensor] = None
     v_new_scale: Optional[torch.Tensor] = None
     extra: Dict[str, object] = field(default_factory=dict)
+    # cache storage: "flash" [P, BS, Hkv, D] or "xvec" [P, Hkv, D // x, BS, x]
+    # (the same logical contents; only where each element is stored differs)
+    layout: str = "flash"
 
     @property
     def group(self) -> int:
@@ -178,8 +182,9 @@ def tiny(literal: bool = False, device="cpu") -> Workload:
 
 
 def gqa_bf16(device="cpu", batch=64, ctx_lo=512, ctx_hi=4096, num_heads=32, num_kv_heads=8,
-             head_dim=128, block_size=16, seed=None) -> Workload:
-    """Llama-3-8B-like GQA decode step, bf16 (defaults: the full-size case)."""
+             head_dim=128, block_size=16, seed=None, layout="flash") -> Workload:
+    """Llama-3-8B-like GQA decode step, bf16 (defaults: the full-size case).
+    layout="xvec": the same data stored x-vectorised."""
     g = _gen(SEEDS["gqa_bf16"] if seed is None else seed, device)
     dt = torch.bfloat16
     B, Hq, Hkv, D, BS = batch, num_heads, num_kv_heads, head_dim, block_size
@@ -198,6 +203,7 @@ def gqa_bf16(device="cpu", batch=64, ctx_lo=512, ctx_hi=4096, num_heads=32, num_
     w = Workload("gqa_bf16", dt, "bf16", B, Hq, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
                  k_new, v_new, k_cache0, v_cache0)
     w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
+    w.layout = layout
     return w
 
 
@@ -256,7 +262,7 @@ def _fill_lists(ctx_list, device):
 
 def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, num_kv_heads=8,
              head_dim=128, block_size=32, calib_tokens=4096, seed=None,
-             fp8="e4m3", scales="head") -> Workload:
+             fp8="e4m3", scales="head", layout="flash") -> Workload:
     """Long-context quantised cache with per-kv-head scales amax / (the
     format's largest value): 448 for e4m3 (defaults: the full-size case),
     57344 for e5m2, 127 for int8 ("i8").  scales="block": each block's scale
@@ -299,6 +305,7 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
         w.k_fill_scale, w.v_fill_scale = row_scale(k_fill), row_scale(v_fill)
         w.k_new_scale, w.v_new_scale = row_scale(k_new), row_scale(v_new)
     w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
+    w.layout = layout
     return w
 
 
@@ -365,6 +372,17 @@ def all_octets(device="cpu") -> torch.Tensor:
     n = torch.arange(1 << 24, dtype=torch.int64, device=device)
     lanes = torch.arange(8, dtype=torch.int64, device=device) * 3
     return ((n[:, None] >> lanes[None, :]) & 7).to(torch.uint8)
+
+
+def storage(t: torch.Tensor, layout: str) -> torch.Tensor:
+    """A logical [P, BS, Hkv, D] cache tensor arranged for the given storage
+    layout: itself ("flash") or [P, Hkv, D // x, BS, x] ("xvec", x = 16 bytes
+    / element size)."""
+    if layout == "flash":
+        return t
+    P, BS, H, D = t.shape
+    x = 16 // t.element_size()
+    return t.reshape(P, BS, H, D // x, x).permute(0, 2, 3, 1, 4).contiguous()
 
 
 def bits16(t: torch.Tensor):
