@@ -174,7 +174,12 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
         !make_map(&mv, p.v_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
                   p.c_head, p.c_blk, p.c_chunk, f.nh))
         return cudaErrorInvalidValue;
-    if (p.c_chunk != 16) return launch_decode_fast_xv(p, f, cache_kind, &mk, &mv, s);
+    if (p.c_chunk != 16) {
+        const int64_t es = is_q8(cache_kind) ? 1 : 2;
+        f.xv_bulk = p.c_slot == 16 && p.c_chunk == 16 * int64_t(p.block_size) &&
+                    p.c_head == int64_t(p.block_size) * p.head_dim * es;
+        return launch_decode_fast_xv(p, f, cache_kind, &mk, &mv, s);
+    }
     if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
     if (cache_kind == kE5M2) return launch_fast_bs<kE5M2, 128>(p, f, mk, mv, s);
     if (cache_kind == kI8) return launch_fast_bs<kI8, 128>(p, f, mk, mv, s);

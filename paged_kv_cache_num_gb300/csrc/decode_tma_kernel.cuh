@@ -31,7 +31,9 @@
 // x-vectorised caches ([blocks][kv heads][head_dim/x][block_size][x], x
 // elements = 16 bytes) arrive as stored, [nh][head_dim/x][block_size][16 B]:
 // the eight rows an ldmatrix phase reads are then 128 consecutive bytes, so
-// they need no swizzle.
+// they need no swizzle.  When the nh heads' tiles of a block are one
+// contiguous run (the packed layout), each is staged by a single 1-D bulk
+// copy instead of a tensor copy made of 16-byte rows.
 // Each consumer warp computes, for its kv head and the G <= 8 query heads
 // that share it, with m16n8k16 mma.sync (block tokens on M, q heads on N):
 //   S^T = K Q^T (K from shared memory by ldmatrix, or fp8 / 3-bit codes
@@ -354,9 +356,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         stage_pb[s] = pbk;
                         if (pbk >= 0) {
                             ptx::mbar_arrive_expect_tx(fb, uint32_t(2 * L.tile_bytes + L.meta_bytes));
-                            if constexpr (XV) {   // (x, slot, piece, head, block) boxes
-                                ptx::tma_load_5d(kdst, &tmk, fb, 0, 0, 0, hgk * nh, pbk);
-                                ptx::tma_load_5d(vdst, &tmv, fb, 0, 0, 0, hgk * nh, pbk);
+                            if constexpr (XV) {
+                                if (f.xv_bulk) {   // the heads' tiles: one run each of K and V
+                                    const int64_t off = int64_t(pbk) * p.c_blk + int64_t(hgk) * nh * p.c_head;
+                                    ptx::bulk_load(kdst, p.k_cache + off, uint32_t(L.tile_bytes), fb);
+                                    ptx::bulk_load(vdst, p.v_cache + off, uint32_t(L.tile_bytes), fb);
+                                } else {           // (x, slot, piece, head, block) boxes
+                                    ptx::tma_load_5d(kdst, &tmk, fb, 0, 0, 0, hgk * nh, pbk);
+                                    ptx::tma_load_5d(vdst, &tmv, fb, 0, 0, 0, hgk * nh, pbk);
+                                }
                             } else {
 #pragma unroll
                                 for (int h = 0; h < T::HALVES; ++h) {

@@ -119,6 +119,8 @@ struct FastParams {
     int smem_bytes;
     int meta_heads;             // 3-bit: kv heads whose scale/zero runs a stage holds
                                 // (nh when the arrays are head-major, else all)
+    int xv_bulk;                // x-vectorised cache whose nh head tiles of a block are
+                                // one contiguous run: staged by 1-D bulk copies
     int32_t *prefix;            // [B+1] blocks-per-sequence prefix sums (workspace)
     float *part_ml;             // [(grid + n_hg*B) * nh * G, 2]
     float *part_acc;            // [(grid + n_hg*B) * nh * G, D]

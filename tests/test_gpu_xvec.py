@@ -133,3 +133,40 @@ def test_full_fp8_long_xvec_sampled(pkv, orc):
     oc = PL.oracle_caches(w, orc, seqs=seqs)
     pairs = _sample_pairs(w, seqs)
     _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+def test_xvec_padded_pieces(pkv, orc, kind):
+    """Pieces further apart than block_size * 16 bytes (slots padded): the
+    persistent kernel then stages tiles with 5-D tensor copies instead of one
+    bulk copy per head group; append and decode match the oracle."""
+    if kind == "bf16":
+        w = W.gqa_bf16(batch=4, ctx_lo=1, ctx_hi=900, seed=250, layout="xvec")
+    else:
+        w = W.fp8_long(batch=3, ctx_lo=50, ctx_hi=900, calib_tokens=64, seed=251, layout="xvec")
+    P, BS, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+    x = _x(kind)
+    dt = torch.bfloat16 if kind == "bf16" else torch.uint8
+    pad_k = torch.zeros((P, H, D // x, BS + 16, x), dtype=dt, device="cuda")
+    pad_v = torch.zeros_like(pad_k)
+    cache = pkv.KVCache(w.cache_kind, pad_k[:, :, :, :BS], pad_v[:, :, :, :BS],
+                        k_scale=None if w.k_scale is None else w.k_scale.cuda(),
+                        v_scale=None if w.v_scale is None else w.v_scale.cuda(), layout="xvec")
+    if w.k_cache0 is not None:
+        cache.k_cache.copy_(W.storage(w.k_cache0, "xvec").cuda())
+        cache.v_cache.copy_(W.storage(w.v_cache0, "xvec").cuda())
+    bt = w.block_tables.cuda()
+    if w.fill_req is not None:
+        sm = pkv.slot_mapping(bt, w.fill_req.cuda(), w.fill_pos.cuda(), BS)
+        pkv.kv_append(w.k_fill.cuda(), w.v_fill.cuda(), sm, cache)
+    sm = pkv.slot_mapping(bt, w.new_req.cuda(), w.new_pos.cuda(), BS)
+    pkv.kv_append(w.k_new.cuda(), w.v_new.cuda(), sm, cache)
+    out = pkv.paged_decode(w.q.cuda(), cache, bt, w.context_lens.cuda(), sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    oc = PL.oracle_caches(w, orc)
+    _same_storage(w, orc, cache, oc)
+    _check(w, out, PL.oracle_decode(w, orc, oc))
+    # the padding slots were never written
+    assert not pad_k[:, :, :, BS:].view(torch.uint8).any()
+    _, packed = PL.gpu_run(w, pkv)
+    assert torch.equal(out.cpu().view(torch.int16), packed.cpu().view(torch.int16))
