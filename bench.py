@@ -271,7 +271,7 @@ class Step:
         if w.q is not None:
             n = pkv.decode_workspace_bytes(w.q, self.cache, w.block_tables)
             self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
-            self.launches += 2 if n > 0 else 1
+            self.launches += pkv.decode_launches(w.q, self.cache, w.block_tables)
         torch.cuda.synchronize()
 
     def append(self, req=None, pos=None, k=None, v=None):
@@ -690,6 +690,21 @@ def main():
         nb, sec = arm.step()
         cpu = {"value": round(nb / sec / 1e9, 4), "unit": "GB/s", "cores": arm.nthreads,
                "kind": "oracle", "sample": arm.describe(sec)}
+        # the same sample on one host core
+        arm.nthreads = 1
+        nb1, sec1 = arm.step()
+        cpu["single_thread"] = {"value": round(nb1 / sec1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "sample": arm.describe(sec1)}
+        # the oracle's 2^24-octet pack + unpack (one thread), beside the pages' CPU time
+        vals = W.all_octets("cpu").numpy().reshape(-1, 8)
+        t0 = time.perf_counter()
+        packed = orc.pack3(vals)
+        back = orc.unpack3(packed)
+        t_or = time.perf_counter() - t0
+        if "pack3_2^24" in extra:
+            extra["pack3_2^24"]["oracle_pack_unpack_s"] = round(t_or, 3)
+            extra["pack3_2^24"]["oracle_roundtrip_ok"] = bool(np.array_equal(back, vals))
+        del vals, packed, back
 
     if rank == 0:
         line = {

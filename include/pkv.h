@@ -7,8 +7,8 @@
  *     fp32 scales) or to 3-bit affine codes packed 8 values per 3 bytes;
  *   - paged_decode: one-query-token attention over that pool, indirected by
  *     block tables, with grouped-query heads, online softmax, a split over
- *     the context merged by a separate reduce kernel, and the fp8 / 3-bit
- *     dequantisation done in registers;
+ *     the context merged by log-sum-exp rescaling, and the fp8 / int8 /
+ *     3-bit dequantisation done in registers;
  *   - pack3 / unpack3: the bit-exact 3-bit packing on its own.
  *
  * Conventions shared by every call
@@ -252,7 +252,8 @@ int pkv_kv_append_scaled(const pkv_tensor *k_new, const pkv_tensor *v_new,
  * Kv Cache Append Kernel", design rules: replication happens in the
  * attention kernel by index arithmetic) and a split of each context into
  * chunks whose partial (max, sum, accumulator) triples a second kernel
- * merges by log-sum-exp rescaling.
+ * merges by log-sum-exp rescaling (pkv_paged_decode_launches tells how
+ * many kernels a call launches).
  *
  *   q            : F16 or BF16 [batch, num_heads, head_dim], head_dim
  *                  contiguous, 16-byte aligned rows.
@@ -272,6 +273,7 @@ int pkv_kv_append_scaled(const pkv_tensor *k_new, const pkv_tensor *v_new,
  *                  pkv_paged_decode_workspace for the same arguments (may be
  *                  NULL when that size is 0); its contents need no
  *                  initialisation and are dead after the call's kernels.
+ *                  Calls whose kernels may overlap must not share one.
  *
  *   Grouped-query mapping: q head h reads kv head h / (num_heads /
  *   num_kv_heads).  Output = softmax(sm_scale * q . K^T) V over the first
@@ -289,6 +291,11 @@ int pkv_kv_append_scaled(const pkv_tensor *k_new, const pkv_tensor *v_new,
  */
 int pkv_paged_decode_workspace(const pkv_tensor *q, const pkv_cache *cache,
                                const pkv_tensor *block_tables, int num_splits, size_t *bytes);
+
+/* Kernel launches a pkv_paged_decode call with these arguments makes (1 or
+ * 2), written to *launches; validation as pkv_paged_decode_workspace. */
+int pkv_paged_decode_launches(const pkv_tensor *q, const pkv_cache *cache,
+                              const pkv_tensor *block_tables, int num_splits, int32_t *launches);
 
 int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
                      const pkv_tensor *context_lens, float sm_scale, const pkv_tensor *out,

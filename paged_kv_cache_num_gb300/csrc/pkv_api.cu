@@ -539,6 +539,17 @@ int pkv_paged_decode_workspace(const pkv_tensor *q, const pkv_cache *cache, cons
     return ok();
 }
 
+int pkv_paged_decode_launches(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
+                              int num_splits, int32_t *launches)
+{
+    if (!launches) return fail(PKV_ERR_NULL, "launches is NULL");
+    DecodeCheck dc{};
+    TRY(check_decode_common(q, cache, block_tables, num_splits, dc));
+    // persistent path: decode + merge; general path: decode (+ reduce when split)
+    *launches = dc.plan.kernel == 1 ? 2 : (dc.plan.num_splits > 1 ? 2 : 1);
+    return ok();
+}
+
 static int prep_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tensor *block_tables,
                              const pkv_tensor *context_lens, float sm_scale, const pkv_tensor *out,
                              int num_splits, void *workspace, size_t workspace_bytes, int32_t *err_flag,

@@ -78,6 +78,8 @@ def lib():
             L.pkv_kv_append_scaled.argtypes = [TP, TP, TP, TP, TP, CP, P, P]
             L.pkv_paged_decode_workspace.argtypes = [TP, CP, TP, ctypes.c_int,
                                                      ctypes.POINTER(ctypes.c_size_t)]
+            L.pkv_paged_decode_launches.argtypes = [TP, CP, TP, ctypes.c_int,
+                                                    ctypes.POINTER(ctypes.c_int32)]
             L.pkv_paged_decode.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP, ctypes.c_int, P,
                                            ctypes.c_size_t, P, P]
             L.pkv_paged_decode_noalloc.argtypes = [TP, CP, TP, TP, ctypes.c_float, TP,
@@ -90,7 +92,7 @@ def lib():
             L.pkv_unpack3_words.argtypes = [P, P, ctypes.c_int64, P]
             L.pkv_copy_peak.argtypes = [P, P, ctypes.c_size_t, P]
             for fn in ("pkv_slot_mapping", "pkv_kv_append", "pkv_kv_append_scaled",
-                       "pkv_paged_decode_workspace",
+                       "pkv_paged_decode_workspace", "pkv_paged_decode_launches",
                        "pkv_paged_decode", "pkv_paged_decode_noalloc", "pkv_decode_step", "pkv_pack3",
                        "pkv_unpack3", "pkv_unpack3_words", "pkv_copy_peak"):
                 getattr(L, fn).restype = ctypes.c_int
@@ -346,6 +348,15 @@ def decode_workspace_bytes(q, cache: KVCache, block_tables, num_splits: int = 0)
     _check(lib().pkv_paged_decode_workspace(ctypes.byref(_desc(q)), ctypes.byref(cs),
                                             ctypes.byref(_desc(block_tables)), int(num_splits),
                                             ctypes.byref(n)))
+    return int(n.value)
+
+
+def decode_launches(q, cache: KVCache, block_tables, num_splits: int = 0) -> int:
+    """Kernel launches one paged_decode call with these arguments makes."""
+    n = ctypes.c_int32(0)
+    _check(lib().pkv_paged_decode_launches(ctypes.byref(_desc(q)), ctypes.byref(cache._struct()),
+                                           ctypes.byref(_desc(block_tables)), int(num_splits),
+                                           ctypes.byref(n)))
     return int(n.value)
 
 

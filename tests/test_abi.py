@@ -28,7 +28,8 @@ def test_header_declares_expected_calls():
     names = _declared_functions()
     for n in ("pkv_kv_append", "pkv_paged_decode", "pkv_paged_decode_workspace", "pkv_pack3",
               "pkv_unpack3", "pkv_unpack3_words", "pkv_slot_mapping", "pkv_last_error",
-              "pkv_decode_step", "pkv_paged_decode_noalloc", "pkv_kv_append_scaled"):
+              "pkv_decode_step", "pkv_paged_decode_noalloc", "pkv_kv_append_scaled",
+              "pkv_paged_decode_launches"):
         assert n in names
 
 
@@ -119,6 +120,10 @@ def test_decode_validation_errors(lib):
     c96 = _cache(pkv.F16, D=96)
     q96 = _fake((B, Hq, 96), pkv.F16)
     assert lib.pkv_paged_decode_workspace(by(q96), by(c96), by(bt), 0, by(n)) == -5
+    nl = ctypes.c_int32(0)
+    assert lib.pkv_paged_decode_launches(by(q), by(c), by(bt), 1, by(nl)) == 0 and nl.value == 1
+    assert lib.pkv_paged_decode_launches(by(q), by(c), by(bt), 4, by(nl)) == 0 and nl.value == 2
+    assert lib.pkv_paged_decode_launches(by(q3), by(c), by(bt), 0, by(nl)) == -3
     # explicit split needs workspace
     assert lib.pkv_paged_decode_workspace(by(q), by(c), by(bt), 4, by(n)) == 0
     assert n.value > 0
