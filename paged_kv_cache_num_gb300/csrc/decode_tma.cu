@@ -142,9 +142,8 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     f.meta_heads = meta_heads;
     const int group = num_heads / num_kv_heads;
     const int64_t rows = (int64_t(f.grid) + int64_t(n_hg) * batch) * nh * group;
-    const size_t prefix_bytes = (size_t(batch + 1) * 4 + 255) / 256 * 256;
     const size_t ml_bytes = (size_t(rows) * 2 * 4 + 255) / 256 * 256;
-    workspace = prefix_bytes + ml_bytes + size_t(rows) * head_dim * 4;
+    workspace = ml_bytes + size_t(rows) * head_dim * 4;
     return true;
 }
 
@@ -162,12 +161,10 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
 {
     const int64_t rows = (int64_t(f.grid) + int64_t(f.n_hg) * p.batch) * f.nh * p.group;
     char *c = static_cast<char *>(ws);
-    const size_t prefix_bytes = (size_t(p.batch + 1) * 4 + 255) / 256 * 256;
     const size_t ml_bytes = (size_t(rows) * 2 * 4 + 255) / 256 * 256;
     (void)ws_bytes;
-    f.prefix = reinterpret_cast<int32_t *>(c);
-    f.part_ml = reinterpret_cast<float *>(c + prefix_bytes);
-    f.part_acc = reinterpret_cast<float *>(c + prefix_bytes + ml_bytes);
+    f.part_ml = reinterpret_cast<float *>(c);
+    f.part_acc = reinterpret_cast<float *>(c + ml_bytes);
     CUtensorMap mk, mv;
     if (!make_map(&mk, p.k_cache, cache_kind, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.c_slot,
                   p.c_head, p.c_blk, p.c_chunk, f.nh) ||

@@ -299,8 +299,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (lane == 0) prefix[B] = carry;
     }
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int b = threadIdx.x; b <= B; b += blockDim.x) f.prefix[b] = prefix[b];
 
     // the merge kernel may be scheduled now; it waits for this grid to finish
     griddep_launch_dependents();
@@ -316,6 +314,11 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             ptx::prefetch_tmap(&tmk);
             ptx::prefetch_tmap(&tmv);
         }
+        // flash-layout 16-bit / one-byte tiles are streamed with an L2
+        // evict-first policy (each is read once); measured neutral to
+        // slightly worse for 3-bit and x-vectorised tiles, which keep the
+        // default policy
+        const uint64_t once = ptx::policy_evict_first();
         bool aborted = false;
         int64_t issued = 0;
         int ps = 0;              // next stage to fill
@@ -369,8 +372,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
                                 for (int h = 0; h < T::HALVES; ++h) {
                                     const int half_bytes = L.tile_bytes / T::HALVES;
-                                    ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
-                                    ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                    if constexpr (T::kIsU3) {
+                                        ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                        ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                    } else {
+                                        ptx::tma_load_4d_hint(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0,
+                                                              hgk * nh, pbk, once);
+                                        ptx::tma_load_4d_hint(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0,
+                                                              hgk * nh, pbk, once);
+                                    }
                                 }
                             }
                             if constexpr (gscale) {  // the heads' runs of the block's scales
@@ -1058,24 +1068,66 @@ __device__ __forceinline__ int64_t floordiv_i64(int64_t a, int64_t n)
 // Merge the partials of units split across CTAs (one warp per (sequence,
 // q head)); units held whole by one CTA were written by it, units with an
 // empty context get zeros.
-constexpr int kMergeBatch = 8;   // partials a row combines in one round trip
+constexpr int kMergeBatch = 16;  // partials a row combines in one round trip
+// 4 warps a CTA: small enough in registers to sit beside a decode CTA on its
+// SM, where it computes its prologue before the decode grid completes
+constexpr int kMergeWarps = 4;
 
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f)
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeParams p, FastParams f)
 {
-    // launched as a programmatic dependent of the decode kernel: wait until
-    // that grid has completed and its writes are visible
+    // Blocks per sequence and their prefix sums, from context_lens (an input
+    // of the call, clamped as the decode kernel clamps it): computed while
+    // the decode kernel still runs, this kernel being its programmatic
+    // dependent, so that only the partials are read after the wait.
+    extern __shared__ int sprefix[];            // [batch + 1]
+    __shared__ int wsum[kMergeWarps];
+    const int B = p.batch, tid = threadIdx.x, lane = tid & 31;
+    {
+        const int cap = p.max_blocks << p.block_shift;
+        const int per = (B + 32 * kMergeWarps - 1) / (32 * kMergeWarps);
+        const int lo = min(B, tid * per), hi = min(B, lo + per);
+        int sum = 0;
+        for (int b = lo; b < hi; ++b) {
+            int ctx = p.context_lens[b * p.cl_stride];
+            ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+            const int nb = (ctx + p.block_size - 1) >> p.block_shift;
+            sprefix[b] = nb;
+            sum += nb;
+        }
+        int incl = sum;             // block-wide exclusive scan of the sums
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) wsum[tid >> 5] = incl;
+        __syncthreads();
+        int run = incl - sum, total = 0;
+#pragma unroll
+        for (int w4 = 0; w4 < kMergeWarps; ++w4) {
+            if (w4 < (tid >> 5)) run += wsum[w4];
+            total += wsum[w4];
+        }
+        for (int b = lo; b < hi; ++b) {
+            const int c = sprefix[b];
+            sprefix[b] = run;
+            run += c;
+        }
+        if (tid == 0) sprefix[B] = total;
+        __syncthreads();
+    }
+    // wait until the decode grid has completed and its writes are visible
     griddep_wait();
-    const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (w >= p.batch * p.num_heads) return;
+    const int w = blockIdx.x * kMergeWarps + (tid >> 5);
+    if (w >= B * p.num_heads) return;
     const int b = w / p.num_heads, h = w % p.num_heads;
     const int G = p.group, nh = f.nh;
     const int kvh = h / G, hg = kvh / nh;
     const int local = h - hg * nh * G;
-    const int64_t NBT = f.prefix[p.batch];
+    const int64_t NBT = sprefix[B];
     const int64_t N = NBT * f.n_hg;
-    const int n = f.prefix[b + 1] - f.prefix[b];
+    const int n = sprefix[b + 1] - sprefix[b];
     constexpr int EPL = D / 32;
     uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
     float acc[EPL];
@@ -1083,7 +1135,7 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p, FastParams f
     for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
     if (n > 0) {
         const int64_t S = f.grid;
-        const int64_t first = int64_t(hg) * NBT + f.prefix[b];
+        const int64_t first = int64_t(hg) * NBT + sprefix[b];
         // CTA i streams [i*N/S, (i+1)*N/S): the owner of flat index x is
         // floor(((x+1)*S - 1) / N)
         const int64_t i0 = floordiv_i64((first + 1) * S - 1, N);
@@ -1193,7 +1245,8 @@ cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUte
     e = launch_pdl(kern, dim3(f.grid), dim3((f.nh + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
     if (e != cudaSuccess) return e;
     const int rows = p.batch * p.num_heads;
-    return launch_pdl(merge_kernel<D>, dim3((rows + 7) / 8), dim3(256), 0, s, p, f);
+    return launch_pdl(merge_kernel<D>, dim3((rows + kMergeWarps - 1) / kMergeWarps), dim3(32 * kMergeWarps),
+                      size_t(p.batch + 1) * 4, s, p, f);
 }
 
 }  // namespace

@@ -121,7 +121,6 @@ struct FastParams {
                                 // (nh when the arrays are head-major, else all)
     int xv_bulk;                // x-vectorised cache whose nh head tiles of a block are
                                 // one contiguous run: staged by 1-D bulk copies
-    int32_t *prefix;            // [B+1] blocks-per-sequence prefix sums (workspace)
     float *part_ml;             // [(grid + n_hg*B) * nh * G, 2]
     float *part_acc;            // [(grid + n_hg*B) * nh * G, D]
 };
