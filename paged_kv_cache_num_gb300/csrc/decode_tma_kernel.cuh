@@ -436,6 +436,19 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     int64_t seg_start = lo;
 
+    // one-byte codes in 128-byte swizzled rows: 16-byte chunk c of row r sits
+    // at r * 128 + ((c ^ r) & 7) * 16.  The rows a lane reads have a fixed
+    // r & 7 (gid for K; 2tig or 2tig + 1 for V), so the chunk offsets are
+    // per-lane constants, computed once: K chunk kk, V chunk 2q4 + (gid >> 2)
+    // of the even / odd token rows
+    uint32_t kswz[8], vswz[2][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) kswz[c] = uint32_t((c ^ gid) & 7) << 4;
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+            vswz[a][q4] = uint32_t(((2 * q4 + (gid >> 2)) ^ ((2 * tig + a) & 7)) & 7) << 4;
     uint32_t qb[T::QK][2];        // B fragments of Q^T per k-step
     float o[T::DT / 2][4];        // O^T accumulators: 16-d tiles x (heads 2tig, 2tig+1)
     float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
@@ -855,12 +868,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             const uint32_t kb = ktile + (kk * BS + 16 * mt + gid) * 16 + 4 * tig;
                             w0 = ld_shared_u32(kb);
                             w1 = ld_shared_u32(kb + 8 * 16);
-                        } else {
-                            // rows 16mt+gid and +8 share the swizzle phase gid: the
-                            // address is (row base | gid << 4) ^ (kk << 4)
-                            const uint32_t kb = (ktile + (16 * mt + gid) * 128 + 4 * tig) | (uint32_t(gid) << 4);
-                            w0 = ld_shared_u32(kb ^ uint32_t((kk & 7) << 4));
-                            w1 = ld_shared_u32((kb + 8 * 128) ^ uint32_t((kk & 7) << 4));
+                        } else {   // chunk kk of rows 16mt+gid and +8 (both r & 7 = gid)
+                            const uint32_t kb = ktile + gid * 128 + 4 * tig + kswz[kk & 7] + mt * 2048;
+                            w0 = ld_shared_u32(kb);
+                            w1 = ld_shared_u32(kb + 8 * 128);
                         }
                         a[0] = f16x2_from_fp8x2<CK>(w0);
                         a[1] = f16x2_from_fp8x2<CK>(w1);
@@ -970,9 +981,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     for (int i = 0; i < 4; ++i) {
                         if constexpr (XV)   // piece 2q4 + (gid >> 2) of row i
                             vb[i] = vtile + ((gid >> 2) * BS + rows[i]) * 16 + (gid & 3) * 4;
-                        else   // (row base | ((gid >> 2) ^ (row & 7)) << 4) ^ (q4 << 5)
-                            vb[i] = (vtile + rows[i] * 128 + (gid & 3) * 4) |
-                                    (uint32_t((gid >> 2) ^ (rows[i] & 7)) << 4);
+                        else                // row i; its chunk offset is vswz[i & 1][q4]
+                            vb[i] = vtile + rows[i] * 128 + (gid & 3) * 4;
                     }
 #pragma unroll
                     for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -982,7 +992,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         uint32_t w[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            w[i] = ld_shared_u32(XV ? vb[i] + q4 * 2 * BS * 16 : vb[i] ^ uint32_t((q4 & 3) << 5));
+                            w[i] = ld_shared_u32(XV ? vb[i] + q4 * 2 * BS * 16 : vb[i] + vswz[i & 1][q4 & 3]);
                             if (partial && rows[i] >= valid) w[i] = 0u;
                         }
 #pragma unroll
