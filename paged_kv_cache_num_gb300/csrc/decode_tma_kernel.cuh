@@ -116,22 +116,31 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float &rlo, flo
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Two one-byte codes (the low 16 bits, low byte first) of cache kind CK ->
-// an f16x2 register, exactly: fp8 through the hardware conversion; int8 c
-// as 1152 + c (a byte permute puts c next to the exponent of 1024 and an
-// XOR of the byte's top bit adds 128), the 1152 offset being removed in
-// fp32 after the MMA.
-template <int CK>
-__device__ __forceinline__ uint32_t f16x2_from_fp8x2(uint32_t two)
+// Two one-byte codes of cache kind CK, bytes 2HI and 2HI+1 of w (low byte
+// first) -> an f16x2 register, exactly: fp8 through cvt.rn.f16x2 on the
+// 16-bit half of the register (no shift); int8 c as 1152 + c (a byte
+// permute puts c next to the exponent of 1024 and an XOR of the byte's top
+// bit adds 128), the 1152 offset being removed in fp32 after the MMA.
+template <int CK, int HI>
+__device__ __forceinline__ uint32_t f16x2_from_q8(uint32_t w)
 {
+    uint32_t r;
     if constexpr (CK == kI8) {
-        return ptx::prmt(two, 0x64646464u, 0x4140u) ^ 0x00800080u;
+        r = ptx::prmt(w, 0x64646464u, HI ? 0x4342u : 0x4140u) ^ 0x00800080u;
+    } else if constexpr (CK == kE4M3) {
+        if constexpr (HI)
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(r) : "r"(w));
+        else
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, l;\n}" : "=r"(r) : "r"(w));
     } else {
-        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu),
-                                                         CK == kE4M3 ? __NV_E4M3 : __NV_E5M2);
-        return uint32_t(h.x) | (uint32_t(h.y) << 16);
+        if constexpr (HI)
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e5m2x2 %0, h;\n}" : "=r"(r) : "r"(w));
+        else
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e5m2x2 %0, l;\n}" : "=r"(r) : "r"(w));
     }
+    return r;
 }
+
 constexpr float kI8Bias = 1152.0f;
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a)
@@ -873,10 +882,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             w0 = ld_shared_u32(kb);
                             w1 = ld_shared_u32(kb + 8 * 128);
                         }
-                        a[0] = f16x2_from_fp8x2<CK>(w0);
-                        a[1] = f16x2_from_fp8x2<CK>(w1);
-                        a[2] = f16x2_from_fp8x2<CK>(w0 >> 16);
-                        a[3] = f16x2_from_fp8x2<CK>(w1 >> 16);
+                        a[0] = f16x2_from_q8<CK, 0>(w0);
+                        a[1] = f16x2_from_q8<CK, 0>(w1);
+                        a[2] = f16x2_from_q8<CK, 1>(w0);
+                        a[3] = f16x2_from_q8<CK, 1>(w1);
                     }
                     ptx::mma16816<T::kBF>(sc[mt], a, qb[kk][0], qb[kk][1]);
                 }
@@ -1002,10 +1011,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             const uint32_t x01 = ptx::prmt(w[0], w[1], sel);
                             const uint32_t x23 = ptx::prmt(w[2], w[3], sel);
                             uint32_t a[4];
-                            a[0] = f16x2_from_fp8x2<CK>(x01);
-                            a[1] = f16x2_from_fp8x2<CK>(x01 >> 16);
-                            a[2] = f16x2_from_fp8x2<CK>(x23);
-                            a[3] = f16x2_from_fp8x2<CK>(x23 >> 16);
+                            a[0] = f16x2_from_q8<CK, 0>(x01);
+                            a[1] = f16x2_from_q8<CK, 1>(x01);
+                            a[2] = f16x2_from_q8<CK, 0>(x23);
+                            a[3] = f16x2_from_q8<CK, 1>(x23);
                             ptx::mma16816<false>(o[2 * q4 + hb], a, pb[kt][0], pb[kt][1]);
                         }
                     }
