@@ -54,11 +54,11 @@ __device__ __forceinline__ void load_row(const char *row, int e0, float scale, f
         const uint8_t *r = reinterpret_cast<const uint8_t *>(row) + e0;
         if constexpr (EPL == 4) {
             const uint32_t u = *reinterpret_cast<const uint32_t *>(r);
-            const float2 a = fp8x2_to_float2<CK>(uint16_t(u & 0xffff));
-            const float2 b = fp8x2_to_float2<CK>(uint16_t(u >> 16));
+            const float2 a = fp8x2_to_float2<CK, 0>(u);
+            const float2 b = fp8x2_to_float2<CK, 1>(u);
             x[0] = a.x * scale; x[1] = a.y * scale; x[2] = b.x * scale; x[3] = b.y * scale;
         } else {
-            const float2 a = fp8x2_to_float2<CK>(*reinterpret_cast<const uint16_t *>(r));
+            const float2 a = fp8x2_to_float2<CK, 0>(uint32_t(*reinterpret_cast<const uint16_t *>(r)));
             x[0] = a.x * scale; x[1] = a.y * scale;
         }
     } else {  // kU3: element d at bits 3d..3d+2 of the little-endian row

@@ -59,27 +59,25 @@ template <> __device__ __forceinline__ uint16_t f2h<kBF16>(float v)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// e4m3 byte -> float (exact), through the hardware fp8 -> f16 conversion.
-__device__ __forceinline__ float e4m3_to_float(uint8_t c)
+// Two fp8 codes of cache kind FP8 (kE4M3 / kE5M2), bytes 2HI and 2HI+1 of w
+// (low byte first) -> two floats, exactly: cvt.rn.f16x2 on the 16-bit half
+// of the register, then the f16 -> f32 widening.
+template <int FP8, int HI>
+__device__ __forceinline__ float2 fp8x2_to_float2(uint32_t w)
 {
-    __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
-    return __half2float(__half(h));
-}
-
-// Two e4m3 bytes (low byte first) -> two floats.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two)
-{
-    __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-    return __half22float2(__half2(h2));
-}
-
-// Two fp8 bytes of cache kind FP8 (kE4M3 / kE5M2) -> two floats (exact).
-template <int FP8>
-__device__ __forceinline__ float2 fp8x2_to_float2(uint16_t two)
-{
-    __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two),
-                                                FP8 == kE4M3 ? __NV_E4M3 : __NV_E5M2);
-    return __half22float2(__half2(h2));
+    uint32_t h;
+    if constexpr (FP8 == kE4M3) {
+        if constexpr (HI)
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(h) : "r"(w));
+        else
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, l;\n}" : "=r"(h) : "r"(w));
+    } else {
+        if constexpr (HI)
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e5m2x2 %0, h;\n}" : "=r"(h) : "r"(w));
+        else
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e5m2x2 %0, l;\n}" : "=r"(h) : "r"(w));
+    }
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
 }  // namespace pkv
