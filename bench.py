@@ -313,8 +313,9 @@ class Step:
             self.decode()
         with torch.cuda.graph(self.g_app):
             self.append()
-        with torch.cuda.graph(self.g_dec):
-            self.decode()
+        if self.w.q is not None:          # append-only workloads have no decode part
+            with torch.cuda.graph(self.g_dec):
+                self.decode()
         torch.cuda.synchronize()
 
     def replay_step(self):

@@ -10,12 +10,13 @@
 // the cast (step 6).  The 3-bit store follows the "triton-3bit-kv-cache-
 // kernel" README section 1.A octet layout.
 //
-// GB300 mapping: the copy and fp8 kernels give each thread one 16-byte
-// chunk of a row, so a warp covers two 256-byte bf16 rows with fully
-// coalesced 16-byte loads and stores; the grid is a function of num_tokens
-// only (CUDA-graph safe).  The 3-bit kernel gives each warp one row: the
-// min / max are warp-shuffle reductions and the packing goes through shared
-// memory.  All are programmatic dependent launches, so the launch of each
+// GB300 mapping: the copy and fp8 kernels give each (token, K|V) to one
+// warp whose lanes take the token's 16-byte pieces across its kv heads (one
+// slot lookup per warp, 32-bit index arithmetic, four 16-byte loads in
+// flight per lane, fully coalesced loads and stores); the grid is a
+// function of num_tokens only (CUDA-graph safe).  The 3-bit kernel gives
+// each warp one row: the min / max are warp-shuffle reductions and the
+// packing goes through shared memory.  All are programmatic dependent launches, so the launch of each
 // overlaps the tail of the previous kernel in the stream.
 #include <type_traits>
 
@@ -45,35 +46,62 @@ __device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, i
     return true;
 }
 
-// 16-bit copy: one thread per CHUNK-byte piece of one K or V row.
-template <int CHUNK>
+// Work items of the copy and one-byte append kernels: a (token, K|V) row
+// split into parts of 32 * U pieces, one warp per item.  U = 4 (four loads
+// in flight per lane) for large batches, U = 1 for small ones, which then
+// spread over more warps.
+__host__ __device__ inline int append_parts(int per, int U) { return (per + 32 * U - 1) / (32 * U); }
+
+// 16-bit copy: one warp per (token, K|V, part), its lanes over the part's
+// (kv head, CHUNK-byte piece) pieces.  The slot is resolved once per warp;
+// the index arithmetic is 32-bit.
+template <int CHUNK, int U>
 __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParams p)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int chunks_per_row = p.head_dim * 2 / CHUNK;
-    const int64_t per_token = int64_t(2) * p.num_kv_heads * chunks_per_row;
-    const int64_t total = p.num_tokens * per_token;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = i / per_token;
-        int r = int(i - t * per_token);
-        const int c = r % chunks_per_row;
-        r /= chunks_per_row;
-        const int h = r % p.num_kv_heads;
-        const int kv = r / p.num_kv_heads;       // 0 = K, 1 = V
+    using V = std::conditional_t<CHUNK == 16, uint4, uint16_t>;
+    const int lane = threadIdx.x & 31;
+    const int cph = p.head_dim * 2 / CHUNK;        // pieces per head row
+    const int per = p.num_kv_heads * cph;          // pieces per (token, K|V)
+    const int parts = append_parts(per, U);
+    const int64_t items = p.num_tokens * 2 * parts;
+    const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t item = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; item < items; item += wstep) {
+        const int64_t row = item / parts;
+        const int part = int(item - row * parts);
+        const int64_t t = row >> 1;
+        const int kv = int(row & 1);
         int64_t blk, off;
-        if (!resolve_slot(p, t, blk, off)) continue;
-        const char *src = kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
-                             : p.k_new + t * p.k_src_tok + h * p.k_src_head;
-        char *dst = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot + h * p.c_head;
-        // the row's 16-byte pieces are c_chunk bytes apart (16 when contiguous)
-        if constexpr (CHUNK == 16) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + c);
-            *reinterpret_cast<uint4 *>(dst + c * p.c_chunk) = v;
-        } else {
-            *reinterpret_cast<uint16_t *>(dst + (c >> 3) * p.c_chunk + 2 * (c & 7)) =
-                reinterpret_cast<const uint16_t *>(src)[c];
+        if (!resolve_slot(p, t, blk, off)) continue;   // warp-uniform
+        const char *src = kv ? p.v_new + t * p.v_src_tok : p.k_new + t * p.k_src_tok;
+        const int64_t src_head = kv ? p.v_src_head : p.k_src_head;
+        char *dst = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot;
+        {
+            const int i0 = part * 32 * U + lane;
+            constexpr int kU = U;
+            V v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + 32 * u;
+                if (i < per) {
+                    const int h = i / cph, c = i - h * cph;
+                    v[u] = __ldg(reinterpret_cast<const V *>(src + h * src_head) + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + 32 * u;
+                if (i < per) {
+                    const int h = i / cph, c = i - h * cph;
+                    // the row's 16-byte pieces are c_chunk bytes apart (16 when contiguous)
+                    char *d = dst + h * p.c_head;
+                    if constexpr (CHUNK == 16)
+                        *reinterpret_cast<uint4 *>(d + c * p.c_chunk) = v[u];
+                    else
+                        *reinterpret_cast<uint16_t *>(d + (c >> 3) * p.c_chunk + 2 * (c & 7)) = v[u];
+                }
+            }
         }
     }
 }
@@ -95,66 +123,83 @@ __device__ __forceinline__ uint32_t q8x2_encode(float2 x)
     }
 }
 
-// One-byte codes (e4m3, e5m2, int8): one thread per 8 elements (16 source
-// bytes -> 8 cache bytes).
-template <int SRC, bool VEC, int FP8>
+// One-byte codes (e4m3, e5m2, int8): one warp per (token, K|V, part), its
+// lanes over the part's (kv head, 8-element group) pieces (16 source bytes
+// -> 8 cache bytes each).
+template <int SRC, bool VEC, int FP8, int U>
 __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams p)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int groups = p.head_dim / 8;
-    const int64_t per_token = int64_t(2) * p.num_kv_heads * groups;
-    const int64_t total = p.num_tokens * per_token;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = i / per_token;
-        int r = int(i - t * per_token);
-        const int c = r % groups;
-        r /= groups;
-        const int h = r % p.num_kv_heads;
-        const int kv = r / p.num_kv_heads;
+    constexpr int kU = U;
+    const int lane = threadIdx.x & 31;
+    const int groups = p.head_dim / 8;             // pieces per head row
+    const int per = p.num_kv_heads * groups;       // pieces per (token, K|V)
+    const int parts = append_parts(per, U);
+    const int64_t items = p.num_tokens * 2 * parts;
+    const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t item = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; item < items; item += wstep) {
+        const int64_t row = item / parts;
+        const int part = int(item - row * parts);
+        const int64_t t = row >> 1;
+        const int kv = int(row & 1);
         int64_t blk, off;
-        if (!resolve_slot(p, t, blk, off)) continue;
-        const uint16_t *src = reinterpret_cast<const uint16_t *>(
-            kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
-               : p.k_new + t * p.k_src_tok + h * p.k_src_head) + 8 * c;
-        // elements 8c .. 8c+7: half of the row's 16-byte piece c / 2
-        uint8_t *dst = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
-                                                   off * p.c_slot + h * p.c_head + (c >> 1) * p.c_chunk) +
-                       8 * (c & 1);
-        float scale;
-        if (p.scale_mode == 0) {                // per kv head
-            scale = (kv ? p.v_scale : p.k_scale)[h];
-        } else if (p.scale_mode == 1) {         // the block's scale for this head
-            scale = (kv ? p.v_gs : p.k_gs)[blk * p.gs_blk + h * p.gs_head];
-        } else {                                // the token's own, kept at its slot
-            scale = (kv ? p.v_ns : p.k_ns)[t * p.ns_tok + h * p.ns_head];
-            if (c == 0) (kv ? p.v_gs : p.k_gs)[blk * p.gs_blk + off * p.gs_slot + h * p.gs_head] = scale;
-        }
-        uint16_t e[8];
-        if constexpr (VEC) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
-            e[0] = v.x & 0xffff; e[1] = v.x >> 16; e[2] = v.y & 0xffff; e[3] = v.y >> 16;
-            e[4] = v.z & 0xffff; e[5] = v.z >> 16; e[6] = v.w & 0xffff; e[7] = v.w >> 16;
-        } else {
+        if (!resolve_slot(p, t, blk, off)) continue;   // warp-uniform
+        const char *src_row = kv ? p.v_new + t * p.v_src_tok : p.k_new + t * p.k_src_tok;
+        const int64_t src_head = kv ? p.v_src_head : p.k_src_head;
+        char *dst_row = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot;
+        {
+            const int i0 = part * 32 * U + lane;
+            uint16_t e[kU][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = src[j];
-        }
-        uint32_t packed[2];
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + 32 * u;
+                if (i >= per) continue;
+                const int h = i / groups, c = i - h * groups;
+                const uint16_t *src = reinterpret_cast<const uint16_t *>(src_row + h * src_head) + 8 * c;
+                if constexpr (VEC) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+                    e[u][0] = v.x & 0xffff; e[u][1] = v.x >> 16; e[u][2] = v.y & 0xffff; e[u][3] = v.y >> 16;
+                    e[u][4] = v.z & 0xffff; e[u][5] = v.z >> 16; e[u][6] = v.w & 0xffff; e[u][7] = v.w >> 16;
+                } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            // scale division in fp32 (IEEE round to nearest), then the cast
-            float2 x;
-            x.x = __fdiv_rn(h2f<SRC>(e[2 * j]), scale);
-            x.y = __fdiv_rn(h2f<SRC>(e[2 * j + 1]), scale);
-            const uint32_t two = q8x2_encode<FP8>(x);
-            if (j & 1) packed[j >> 1] |= two << 16; else packed[j >> 1] = two;
-        }
-        if constexpr (VEC) {
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-        } else {
+                    for (int j = 0; j < 8; ++j) e[u][j] = src[j];
+                }
+            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = uint8_t(packed[j >> 2] >> (8 * (j & 3)));
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + 32 * u;
+                if (i >= per) continue;
+                const int h = i / groups, c = i - h * groups;
+                // elements 8c .. 8c+7: half of the row's 16-byte piece c / 2
+                uint8_t *dst = reinterpret_cast<uint8_t *>(dst_row + h * p.c_head + (c >> 1) * p.c_chunk) +
+                               8 * (c & 1);
+                float scale;
+                if (p.scale_mode == 0) {                // per kv head
+                    scale = (kv ? p.v_scale : p.k_scale)[h];
+                } else if (p.scale_mode == 1) {         // the block's scale for this head
+                    scale = (kv ? p.v_gs : p.k_gs)[blk * p.gs_blk + h * p.gs_head];
+                } else {                                // the token's own, kept at its slot
+                    scale = (kv ? p.v_ns : p.k_ns)[t * p.ns_tok + h * p.ns_head];
+                    if (c == 0) (kv ? p.v_gs : p.k_gs)[blk * p.gs_blk + off * p.gs_slot + h * p.gs_head] = scale;
+                }
+                uint32_t packed[2];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // scale division in fp32 (IEEE round to nearest), then the cast
+                    float2 x;
+                    x.x = __fdiv_rn(h2f<SRC>(e[u][2 * j]), scale);
+                    x.y = __fdiv_rn(h2f<SRC>(e[u][2 * j + 1]), scale);
+                    const uint32_t two = q8x2_encode<FP8>(x);
+                    if (j & 1) packed[j >> 1] |= two << 16; else packed[j >> 1] = two;
+                }
+                if constexpr (VEC) {
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[j] = uint8_t(packed[j >> 2] >> (8 * (j & 3)));
+                }
+            }
         }
     }
 }
@@ -262,29 +307,41 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
 {
     if (p.num_tokens == 0) return cudaSuccess;
     const int T = kAppendThreads;
+    // one warp per (token, K|V, part): four pieces per lane when that still
+    // gives every SM several warps, else one (more, shorter warps)
+    auto small = [&](int per) {
+        return p.num_tokens * 2 * append_parts(per, 4) < int64_t(sm_count_current_device()) * 8;
+    };
+    auto grid = [&](int per, int U) { return grid_for(p.num_tokens * 2 * append_parts(per, U) * 32, T); };
     if (cache_kind == kF16 || cache_kind == kBF16) {
-        if (vec16) {
-            const int64_t work = p.num_tokens * 2 * p.num_kv_heads * (p.head_dim * 2 / 16);
-            return launch_pdl(append_copy_kernel<16>, grid_for(work, T), T, 0, s, p);
-        } else {
-            const int64_t work = p.num_tokens * 2 * p.num_kv_heads * p.head_dim;
-            return launch_pdl(append_copy_kernel<2>, grid_for(work, T), T, 0, s, p);
-        }
+        const int per = p.num_kv_heads * (vec16 ? p.head_dim * 2 / 16 : p.head_dim);
+        const bool one = small(per);
+        const int g = grid(per, one ? 1 : 4);
+        if (vec16) return one ? launch_pdl(append_copy_kernel<16, 1>, g, T, 0, s, p)
+                              : launch_pdl(append_copy_kernel<16, 4>, g, T, 0, s, p);
+        return one ? launch_pdl(append_copy_kernel<2, 1>, g, T, 0, s, p)
+                   : launch_pdl(append_copy_kernel<2, 4>, g, T, 0, s, p);
     } else if (is_q8(cache_kind)) {
-        const int64_t work = p.num_tokens * 2 * p.num_kv_heads * (p.head_dim / 8);
-        const int g = grid_for(work, T);
-        auto go = [&](auto src_c, auto vec_c) -> cudaError_t {
+        const int per = p.num_kv_heads * (p.head_dim / 8);
+        const bool one = small(per);
+        const int g = grid(per, one ? 1 : 4);
+        auto go = [&](auto src_c, auto vec_c, auto u_c) -> cudaError_t {
             constexpr int S = decltype(src_c)::value;
             constexpr bool V = decltype(vec_c)::value;
-            if (cache_kind == kE4M3) return launch_pdl(append_fp8_kernel<S, V, kE4M3>, g, T, 0, s, p);
-            if (cache_kind == kE5M2) return launch_pdl(append_fp8_kernel<S, V, kE5M2>, g, T, 0, s, p);
-            return launch_pdl(append_fp8_kernel<S, V, kI8>, g, T, 0, s, p);
+            constexpr int U = decltype(u_c)::value;
+            if (cache_kind == kE4M3) return launch_pdl(append_fp8_kernel<S, V, kE4M3, U>, g, T, 0, s, p);
+            if (cache_kind == kE5M2) return launch_pdl(append_fp8_kernel<S, V, kE5M2, U>, g, T, 0, s, p);
+            return launch_pdl(append_fp8_kernel<S, V, kI8, U>, g, T, 0, s, p);
+        };
+        auto go_u = [&](auto src_c, auto vec_c) -> cudaError_t {
+            return one ? go(src_c, vec_c, std::integral_constant<int, 1>{})
+                       : go(src_c, vec_c, std::integral_constant<int, 4>{});
         };
         using BF = std::integral_constant<int, kBF16>;
         using HF = std::integral_constant<int, kF16>;
         if (p.src_kind == kBF16)
-            return vec16 ? go(BF{}, std::true_type{}) : go(BF{}, std::false_type{});
-        return vec16 ? go(HF{}, std::true_type{}) : go(HF{}, std::false_type{});
+            return vec16 ? go_u(BF{}, std::true_type{}) : go_u(BF{}, std::false_type{});
+        return vec16 ? go_u(HF{}, std::true_type{}) : go_u(HF{}, std::false_type{});
     } else {  // kU3
         const int64_t rows = p.num_tokens * 2 * p.num_kv_heads;
         const int g = grid_for(rows * 32, T);
