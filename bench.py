@@ -267,7 +267,8 @@ class Step:
         self.slots = torch.empty(w.new_req.shape[0], dtype=torch.int64, device=dev)
         self.out = torch.empty_like(w.q) if w.q is not None else None
         self.ws = None
-        self.launches = 2
+        self.fused = w.q is not None and not self.tok
+        self.launches = 1 if self.fused else 2     # (slot computation +) append
         if w.q is not None:
             n = pkv.decode_workspace_bytes(w.q, self.cache, w.block_tables)
             self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
@@ -296,21 +297,30 @@ class Step:
                               workspace=self.ws, err_flag=self.err)
 
     def run(self):
-        self.append()
-        self.decode()
+        """One whole step through the public API: pkv_decode_step (slot
+        computation fused into the append kernel, then decode) where it
+        applies, else the separate calls (append-only workloads, per-token
+        scales, which need pkv_kv_append_scaled)."""
+        w = self.w
+        if self.fused:
+            self.pkv.decode_step(w.k_new, w.v_new, w.new_req, w.new_pos, w.q, self.cache,
+                                 w.block_tables, w.context_lens, sm_scale=w.sm_scale, out=self.out,
+                                 slots=self.slots, workspace=self.ws, err_flag=self.err)
+        else:
+            self.append()
+            self.decode()
 
     def capture(self):
-        """Record the step's launches (slot_mapping + kv_append + decode) as
-        one CUDA graph, and its append and decode parts as two more; replays
-        run the same kernels on the same buffers without the Python / ctypes
-        launch overhead."""
+        """Record the step's launches (see run) as one CUDA graph, and its
+        append (slot_mapping + kv_append) and decode parts as two more;
+        replays run the same kernels on the same buffers without the Python /
+        ctypes launch overhead."""
         self.run()                             # warm: function attributes, maps
         torch.cuda.synchronize()
         self.g_step = torch.cuda.CUDAGraph()
         self.g_app, self.g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_step):
-            self.append()
-            self.decode()
+            self.run()
         with torch.cuda.graph(self.g_app):
             self.append()
         if self.w.q is not None:          # append-only workloads have no decode part
@@ -743,10 +753,12 @@ def main():
                        "l2": "inputs larger than L2, and flushed between steps outside the "
                              "timed events (256 MiB write, then a 512 MiB read that drains "
                              "its write-back)",
-                       "launch": "a device-timed step replays one CUDA graph (slot_mapping, "
-                                 "kv_append, paged_decode; programmatic dependent launches); "
-                                 "its append and decode parts are replayed alone for the "
-                                 "breakdown; e2e replays one graph of [one packed "
+                       "launch": "a device-timed step replays one CUDA graph of one "
+                                 "pkv_decode_step call (append kernel with the slot "
+                                 "computation fused, decode, merge; programmatic dependent "
+                                 "launches); its append (pkv_slot_mapping + pkv_kv_append) and "
+                                 "decode parts are replayed alone for the breakdown; e2e "
+                                 "replays one graph of [one packed "
                                  "host-to-device copy of the step's inputs, pkv_decode_step "
                                  "(slot mapping, append, decode), the device-to-host copy of "
                                  "out] per step (e2e_eager: the same calls made eagerly)"},

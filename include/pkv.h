@@ -312,9 +312,11 @@ int pkv_paged_decode(const pkv_tensor *q, const pkv_cache *cache, const pkv_tens
  * the same meaning, layouts and rules; slot_mapping (I64 [num_tokens],
  * caller-owned) receives the computed slots.  Every argument of all three
  * is validated before the first launch, so an error status means nothing
- * was enqueued.  The three launches are ordered on `stream` (the append and
- * decode kernels start as programmatic dependents of the previous kernel).
- * An addition of this library: it saves two host-side calls per step.
+ * was enqueued.  The slot computation runs inside the append kernel (same
+ * rule and error bits as pkv_slot_mapping; the slots are still written to
+ * slot_mapping), then the decode kernels follow on `stream` as programmatic
+ * dependents.  An addition of this library: it saves two host-side calls
+ * and one kernel launch per step.
  */
 int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_tensor *req,
                     const pkv_tensor *pos, const pkv_tensor *slot_mapping, const pkv_tensor *q,

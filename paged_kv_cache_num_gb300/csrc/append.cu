@@ -27,10 +27,38 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 
-__device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, int64_t &blk,
-                                             int64_t &off)
+// slot of token t from its (request, position) through the block table:
+// blk = block_tables[req][pos >> log2(BS)], slot = blk * BS + (pos & (BS-1));
+// -1 for pos < 0 (padding), and for positions outside the table (raising
+// PKV_DEVERR_POS_RANGE)
+__device__ __forceinline__ int64_t slot_from_position(const SlotMapParams &p, int64_t t)
 {
-    const int64_t slot = p.slot_mapping[t * p.slot_stride];
+    const int32_t pos = p.pos[t * p.pos_stride];
+    const int32_t req = p.req[t * p.req_stride];
+    int64_t slot = -1;
+    if (pos >= 0) {
+        const int32_t logical = pos >> p.block_shift;
+        if (logical >= p.max_blocks || req < 0 || req >= p.batch) {
+            raise_err(p.err_flag, PKV_DEVERR_POS_RANGE);
+        } else {
+            const int64_t blk = p.bt[req * p.bt_b + logical * p.bt_j];
+            slot = (blk << p.block_shift) + (pos & ((1 << p.block_shift) - 1));
+        }
+    }
+    return slot;
+}
+
+// `first`: this caller writes the token's computed slot out (from_pos)
+__device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, int64_t &blk,
+                                             int64_t &off, bool first = false)
+{
+    int64_t slot;
+    if (p.from_pos) {
+        slot = slot_from_position(p.pos_map, t);
+        if (first) p.pos_map.slot_mapping[t] = slot;
+    } else {
+        slot = p.slot_mapping[t * p.slot_stride];
+    }
     if (slot < 0) return false;                 // padding token: nothing to read or write
     if (slot >= p.num_slots) {
         raise_err(p.err_flag, PKV_DEVERR_SLOT_RANGE);
@@ -73,7 +101,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
         const int64_t t = row >> 1;
         const int kv = int(row & 1);
         int64_t blk, off;
-        if (!resolve_slot(p, t, blk, off)) continue;   // warp-uniform
+        if (!resolve_slot(p, t, blk, off, kv == 0 && part == 0 && lane == 0)) continue;   // warp-uniform
         const char *src = kv ? p.v_new + t * p.v_src_tok : p.k_new + t * p.k_src_tok;
         const int64_t src_head = kv ? p.v_src_head : p.k_src_head;
         char *dst = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot;
@@ -144,7 +172,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
         const int64_t t = row >> 1;
         const int kv = int(row & 1);
         int64_t blk, off;
-        if (!resolve_slot(p, t, blk, off)) continue;   // warp-uniform
+        if (!resolve_slot(p, t, blk, off, kv == 0 && part == 0 && lane == 0)) continue;   // warp-uniform
         const char *src_row = kv ? p.v_new + t * p.v_src_tok : p.k_new + t * p.k_src_tok;
         const int64_t src_head = kv ? p.v_src_head : p.k_src_head;
         char *dst_row = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot;
@@ -222,7 +250,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
         const int r = int(row - t * 2 * p.num_kv_heads);
         const int h = r >> 1, kv = r & 1;
         int64_t blk, off;
-        if (!resolve_slot(p, t, blk, off)) continue;   // warp-uniform
+        if (!resolve_slot(p, t, blk, off, r == 0 && lane == 0)) continue;   // warp-uniform
         const uint16_t *src = reinterpret_cast<const uint16_t *>(
             kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
                : p.k_new + t * p.k_src_tok + h * p.k_src_head) + EPL * lane;
@@ -277,21 +305,8 @@ __global__ void slot_mapping_kernel(SlotMapParams p)
     griddep_wait();
     griddep_launch_dependents();
     for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < p.n;
-         t += int64_t(gridDim.x) * blockDim.x) {
-        const int32_t pos = p.pos[t * p.pos_stride];
-        const int32_t req = p.req[t * p.req_stride];
-        int64_t slot = -1;
-        if (pos >= 0) {
-            const int32_t logical = pos >> p.block_shift;
-            if (logical >= p.max_blocks || req < 0 || req >= p.batch) {
-                raise_err(p.err_flag, PKV_DEVERR_POS_RANGE);
-            } else {
-                const int64_t blk = p.bt[req * p.bt_b + logical * p.bt_j];
-                slot = (blk << p.block_shift) + (pos & ((1 << p.block_shift) - 1));
-            }
-        }
-        p.slot_mapping[t] = slot;
-    }
+         t += int64_t(gridDim.x) * blockDim.x)
+        p.slot_mapping[t] = slot_from_position(p, t);
 }
 
 int grid_for(int64_t work, int threads)

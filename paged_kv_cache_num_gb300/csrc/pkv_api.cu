@@ -630,7 +630,10 @@ int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_
     DecodeCheck dc{};
     TRY(prep_paged_decode(q, cache, block_tables, context_lens, sm_scale, out, num_splits, workspace,
                           workspace_bytes, err_flag, dc));
-    TRY(launch_status(pkv::launch_slot_mapping(sp, as_stream(stream)), "slot_mapping kernel"));
+    // the append kernel computes each token's slot itself (the slot_mapping
+    // kernel's rule) and writes it to slot_mapping: one launch fewer
+    ap.from_pos = 1;
+    ap.pos_map = sp;
     TRY(launch_status(pkv::launch_append(ap, kind, vec16, as_stream(stream)), "kv_append kernel"));
     return launch_paged_decode(dc, q->dtype, workspace, workspace_bytes, stream);
 }

@@ -15,6 +15,19 @@ enum CacheKind : int { kF16 = 1, kBF16 = 2, kE4M3 = 3, kU3 = 4, kE5M2 = 9, kI8 =
 constexpr bool is_q8(int ck) { return ck == kE4M3 || ck == kE5M2 || ck == kI8; }
 
 // ---------------------------------------------------------------- append
+struct SlotMapParams {
+    const int32_t *bt;
+    int64_t bt_b, bt_j;
+    int batch, max_blocks;
+    const int32_t *req;
+    int64_t req_stride;
+    const int32_t *pos;
+    int64_t pos_stride;
+    int64_t n;
+    int block_shift;
+    int64_t *slot_mapping;
+    int32_t *err_flag;
+};
 struct AppendParams {
     const char *k_new;          // source rows (bytes)
     const char *v_new;
@@ -52,23 +65,15 @@ struct AppendParams {
     int64_t num_slots;          // num_blocks * block_size
     int src_kind;               // kF16 / kBF16
     int32_t *err_flag;
+    // from_pos: slots are computed from (request, position) through the block
+    // table (the slot_mapping kernel's rule, fused into the append) and
+    // written to pos_map.slot_mapping; slot_mapping above is then unused
+    int from_pos;
+    SlotMapParams pos_map;
 };
 
 cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cudaStream_t s);
 
-struct SlotMapParams {
-    const int32_t *bt;
-    int64_t bt_b, bt_j;
-    int batch, max_blocks;
-    const int32_t *req;
-    int64_t req_stride;
-    const int32_t *pos;
-    int64_t pos_stride;
-    int64_t n;
-    int block_shift;
-    int64_t *slot_mapping;
-    int32_t *err_flag;
-};
 cudaError_t launch_slot_mapping(const SlotMapParams &p, cudaStream_t s);
 
 // ---------------------------------------------------------------- decode

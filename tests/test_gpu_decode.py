@@ -358,6 +358,43 @@ def test_decode_step_equals_separate_calls(pkv, orc, maker):
     _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
 
 
+@pytest.mark.parametrize("kind", ["e4m3", "bf16"])
+def test_decode_step_padding_and_bad_positions(pkv, orc, kind):
+    """decode_step computes the slots inside its append kernel: padding
+    tokens (pos -1, NaN rows) and a position beyond the block table give slot
+    -1, write nothing and (the latter) raise PKV_DEVERR_POS_RANGE, exactly as
+    pkv_slot_mapping does; the cache and the output match the separate calls."""
+    if kind == "e4m3":
+        w = W.fp8_long(batch=3, ctx_lo=40, ctx_hi=300, calib_tokens=64, seed=270)
+    else:
+        w = W.gqa_bf16(batch=3, ctx_lo=40, ctx_hi=300, seed=271)
+    cache, out_sep = PL.gpu_run(w, pkv)
+    before = PL.gpu_cache_host(cache)
+    dev = "cuda"
+    B = w.batch
+    n_bad = 5
+    req = torch.cat([w.new_req, torch.tensor([0, 1, 2, 0, 1], dtype=torch.int32)])
+    pos = torch.cat([w.new_pos, torch.tensor([-1, -1, w.max_blocks * w.block_size + 3, -1, -1],
+                                             dtype=torch.int32)])
+    nan = torch.full((n_bad,) + tuple(w.k_new.shape[1:]), float("nan"), dtype=w.k_new.dtype)
+    kn, vn = torch.cat([w.k_new, nan]).to(dev), torch.cat([w.v_new, nan]).to(dev)
+    bt, req, pos = w.block_tables.to(dev), req.to(dev), pos.to(dev)
+    err_sep = torch.zeros(1, dtype=torch.int32, device=dev)
+    slots_sep = pkv.slot_mapping(bt, req, pos, w.block_size, err_flag=err_sep)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    slots = torch.full_like(slots_sep, -7)
+    out = pkv.decode_step(kn, vn, req, pos, w.q.to(dev), cache, bt, w.context_lens.to(dev),
+                          sm_scale=w.sm_scale, slots=slots, err_flag=err)
+    torch.cuda.synchronize()
+    assert torch.equal(slots, slots_sep)
+    assert int(slots[-n_bad:].max()) == -1
+    assert int(err.item()) == int(err_sep.item()) == pkv.pkv.DEVERR_POS_RANGE
+    after = PL.gpu_cache_host(cache)
+    for k in before:
+        assert np.array_equal(before[k], after[k]), k
+    assert torch.equal(out, out_sep)
+
+
 def test_u3_bad_block_ids_in_pairs(pkv, orc):
     """3-bit cache with 16-token blocks (which the persistent kernel takes two
     at a time): block ids out of range at an even and at an odd position of a
