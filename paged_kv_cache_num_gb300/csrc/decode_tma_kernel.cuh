@@ -272,7 +272,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
     int *prefix = reinterpret_cast<int *>(smem + L.prefix_off);
     int *nblk = reinterpret_cast<int *>(smem + L.nblk_off);
-    griddep_wait();                // the stream's previous kernel (an append) is done
+    // the stream's previous kernel is done (with early_inputs: only before
+    // the producer's first cache copy, see below)
+    if (!p.early_inputs) griddep_wait();
 
     // ---- per-sequence block counts and their prefix sums
     const int cap = p.max_blocks << p.block_shift;
@@ -322,6 +324,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (lane == 0) {
             ptx::prefetch_tmap(&tmk);
             ptx::prefetch_tmap(&tmv);
+            // every copy (tiles, 3-bit metadata, granular scales) reads what
+            // the previous kernel (the append) may have written
+            if (p.early_inputs) griddep_wait();
         }
         // flash-layout 16-bit / one-byte tiles are streamed with an L2
         // evict-first policy (each is read once); measured neutral to

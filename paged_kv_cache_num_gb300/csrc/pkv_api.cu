@@ -634,6 +634,9 @@ int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_
     // kernel's rule) and writes it to slot_mapping: one launch fewer
     ap.from_pos = 1;
     ap.pos_map = sp;
+    // the append writes only the cache and slot_mapping, so the decode may
+    // read its inputs while the append still runs
+    dc.p.early_inputs = 1;
     TRY(launch_status(pkv::launch_append(ap, kind, vec16, as_stream(stream)), "kv_append kernel"));
     return launch_paged_decode(dc, q->dtype, workspace, workspace_bytes, stream);
 }

@@ -113,6 +113,11 @@ struct DecodeParams {
     int q_is_bf16;
     int out_vec_ok;             // out rows 16-byte aligned (vector stores allowed)
     int32_t *err_flag;
+    // the stream's previous kernel writes only the cache (the append of
+    // pkv_decode_step): the persistent kernel then reads its inputs (q,
+    // context_lens, block_tables) and writes out before its dependency wait,
+    // which only the cache copies come after
+    int early_inputs;
 };
 
 // Persistent TMA kernel (16-bit and fp8 caches).
