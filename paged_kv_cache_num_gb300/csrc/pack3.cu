@@ -11,7 +11,9 @@
 //
 // GB300 mapping: each thread handles 4 octets (32 value bytes <-> 12 packed
 // bytes) so both sides move with aligned 16-byte / 4-byte vector accesses;
-// the kernels are pure HBM streams.
+// the unpacking kernels exchange halves between lanes so that each store
+// instruction of a warp is one contiguous 512-byte run.  The kernels are
+// pure HBM streams.
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -75,25 +77,47 @@ __global__ void __launch_bounds__(kThreads) pack3_kernel(const uint8_t *__restri
     }
 }
 
+// A warp unpacks 32 consecutive 4-octet quads (384 packed bytes -> 1 KB of
+// values): lane l unpacks quad l, then the two store instructions write
+// 16-byte units l and 32 + l of the warp's kilobyte, the halves moved
+// between lanes by shuffles, so that every store instruction is one
+// contiguous 512-byte run.
 __global__ void __launch_bounds__(kThreads) unpack3_kernel(const uint8_t *__restrict__ packed,
                                                            uint8_t *__restrict__ values, int64_t n)
 {
     const int64_t n4 = n / 4;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(packed + 12 * i);
-        const uint32_t a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
-        const uint32_t w0 = a & 0xffffffu;
-        const uint32_t w1 = (a >> 24) | ((b & 0xffffu) << 8);
-        const uint32_t w2 = (b >> 16) | ((c & 0xffu) << 16);
-        const uint32_t w3 = c >> 8;
-        uint4 x, y;
-        unpack_octet(w0, x.x, x.y);
-        unpack_octet(w1, x.z, x.w);
-        unpack_octet(w2, y.x, y.y);
-        unpack_octet(w3, y.z, y.w);
-        reinterpret_cast<uint4 *>(values)[2 * i] = x;
-        reinterpret_cast<uint4 *>(values)[2 * i + 1] = y;
+    const int lane = threadIdx.x & 31;
+    const int64_t chunks = (n4 + 31) / 32;
+    const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t wc = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; wc < chunks; wc += wstep) {
+        const int64_t i = wc * 32 + lane;
+        uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
+        if (i < n4) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(packed + 12 * i);
+            const uint32_t a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
+            const uint32_t w0 = a & 0xffffffu;
+            const uint32_t w1 = (a >> 24) | ((b & 0xffffu) << 8);
+            const uint32_t w2 = (b >> 16) | ((c & 0xffu) << 16);
+            const uint32_t w3 = c >> 8;
+            unpack_octet(w0, x.x, x.y);
+            unpack_octet(w1, x.z, x.w);
+            unpack_octet(w2, y.x, y.y);
+            unpack_octet(w3, y.z, y.w);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            // unit 32k + lane = half (lane & 1) of quad 16k + (lane >> 1)
+            const int srcl = 16 * k + (lane >> 1);
+            // every lane takes part in both shuffles, then keeps its half
+            const bool hi = lane & 1;
+            const uint32_t a0 = __shfl_sync(0xffffffffu, x.x, srcl), b0 = __shfl_sync(0xffffffffu, y.x, srcl);
+            const uint32_t a1 = __shfl_sync(0xffffffffu, x.y, srcl), b1 = __shfl_sync(0xffffffffu, y.y, srcl);
+            const uint32_t a2 = __shfl_sync(0xffffffffu, x.z, srcl), b2 = __shfl_sync(0xffffffffu, y.z, srcl);
+            const uint32_t a3 = __shfl_sync(0xffffffffu, x.w, srcl), b3 = __shfl_sync(0xffffffffu, y.w, srcl);
+            const uint4 o = hi ? make_uint4(b0, b1, b2, b3) : make_uint4(a0, a1, a2, a3);
+            const int64_t q = wc * 32 + srcl;
+            if (q < n4) reinterpret_cast<uint4 *>(values)[2 * (wc * 32) + 32 * k + lane] = o;
+        }
     }
     const int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (t < n - 4 * n4) {
@@ -109,29 +133,48 @@ __global__ void __launch_bounds__(kThreads) unpack3_kernel(const uint8_t *__rest
     }
 }
 
-// One thread per 96-bit group: lane i = (W[w] >> s | W[w+1] << (32-s)) & 7
-// with w = 3i/32, s = 3i%32, the second term only for s > 29.
+// One 96-bit group per lane: lane i = (W[w] >> s | W[w+1] << (32-s)) & 7
+// with w = 3i/32, s = 3i%32, the second term only for s > 29.  A warp takes
+// 32 consecutive groups and writes their kilobyte of values with two
+// contiguous store instructions (halves exchanged by shuffles, as in
+// unpack3_kernel).
 __global__ void __launch_bounds__(kThreads) unpack3_words_kernel(
     const uint32_t *__restrict__ words, uint8_t *__restrict__ values, int64_t m)
 {
-    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < m;
-         g += int64_t(gridDim.x) * blockDim.x) {
-        uint32_t W[3];
-        W[0] = __ldg(words + 3 * g);
-        W[1] = __ldg(words + 3 * g + 1);
-        W[2] = __ldg(words + 3 * g + 2);
-        uint32_t out[8];
+    const int lane = threadIdx.x & 31;
+    const int64_t chunks = (m + 31) / 32;
+    const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t wc = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; wc < chunks; wc += wstep) {
+        const int64_t g = wc * 32 + lane;
+        uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (g < m) {
+            uint32_t W[3];
+            W[0] = __ldg(words + 3 * g);
+            W[1] = __ldg(words + 3 * g + 1);
+            W[2] = __ldg(words + 3 * g + 2);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int w = (3 * i) >> 5, s = (3 * i) & 31;
-            uint32_t v = W[w] >> s;
-            if (s > 29) v |= W[w + 1] << (32 - s);   // compile-time lanes 10, 21
-            v &= 7u;
-            if ((i & 3) == 0) out[i >> 2] = v; else out[i >> 2] |= v << (8 * (i & 3));
+            for (int i = 0; i < 32; ++i) {
+                const int w = (3 * i) >> 5, s = (3 * i) & 31;
+                uint32_t v = W[w] >> s;
+                if (s > 29) v |= W[w + 1] << (32 - s);   // compile-time lanes 10, 21
+                v &= 7u;
+                if ((i & 3) == 0) out[i >> 2] = v; else out[i >> 2] |= v << (8 * (i & 3));
+            }
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(values + 32 * g);
-        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            // unit 32k + lane = half (lane & 1) of group 16k + (lane >> 1)
+            const int srcl = 16 * k + (lane >> 1);
+            const bool hi = lane & 1;
+            uint32_t a[4], b[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // every lane takes part in both shuffles
+                a[j] = __shfl_sync(0xffffffffu, out[j], srcl);
+                b[j] = __shfl_sync(0xffffffffu, out[4 + j], srcl);
+            }
+            const uint4 o = hi ? make_uint4(b[0], b[1], b[2], b[3]) : make_uint4(a[0], a[1], a[2], a[3]);
+            if (wc * 32 + srcl < m) reinterpret_cast<uint4 *>(values)[2 * (wc * 32) + 32 * k + lane] = o;
+        }
     }
 }
 
