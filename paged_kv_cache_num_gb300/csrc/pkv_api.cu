@@ -635,8 +635,10 @@ int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_
     ap.from_pos = 1;
     ap.pos_map = sp;
     // the append writes only the cache and slot_mapping, so the decode may
-    // read its inputs while the append still runs
-    dc.p.early_inputs = 1;
+    // read its inputs while the append still runs -- only when the append
+    // kernel is launched (it then waits for the stream's earlier kernels
+    // before letting the decode start); with no tokens there is none
+    dc.p.early_inputs = ap.num_tokens > 0 ? 1 : 0;
     TRY(launch_status(pkv::launch_append(ap, kind, vec16, as_stream(stream)), "kv_append kernel"));
     return launch_paged_decode(dc, q->dtype, workspace, workspace_bytes, stream);
 }

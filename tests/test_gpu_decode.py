@@ -395,6 +395,26 @@ def test_decode_step_padding_and_bad_positions(pkv, orc, kind):
     assert torch.equal(out, out_sep)
 
 
+def test_decode_step_without_new_tokens(pkv):
+    """A step with no new tokens launches no append; its decode then waits
+    for the stream's earlier work as a plain paged_decode does, and gives the
+    same output (also right after another step's kernels on the stream)."""
+    w = W.gqa_bf16(batch=5, ctx_lo=30, ctx_hi=900, seed=272)
+    cache, out_sep = PL.gpu_run(w, pkv)
+    dev = "cuda"
+    bt, cl, q = w.block_tables.to(dev), w.context_lens.to(dev), w.q.to(dev)
+    e16 = torch.empty((0,) + tuple(w.k_new.shape[1:]), dtype=w.k_new.dtype, device=dev)
+    ei = torch.empty(0, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    for _ in range(3):
+        pkv.decode_step(w.k_new.to(dev), w.v_new.to(dev), w.new_req.to(dev), w.new_pos.to(dev), q,
+                        cache, bt, cl, sm_scale=w.sm_scale, out=out)
+        pkv.decode_step(e16, e16, ei, ei, q, cache, bt, cl, sm_scale=w.sm_scale, out=out,
+                        slots=torch.empty(0, dtype=torch.int64, device=dev))
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_sep)
+
+
 def test_u3_bad_block_ids_in_pairs(pkv, orc):
     """3-bit cache with 16-token blocks (which the persistent kernel takes two
     at a time): block ids out of range at an even and at an odd position of a
