@@ -97,7 +97,8 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
 bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch)
 {
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
-    if (group > 8 || batch > 4096) return false;
+    // groups of up to 16 q heads: two consumer warps per kv head above 8
+    if (group > (cache_kind == kU3 ? 8 : 16) || batch > 4096) return false;
     if (is_q8(cache_kind)) return head_dim == 128;
     if (cache_kind == kU3) return head_dim == 128 && block_size <= 32;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
@@ -111,7 +112,11 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const bool u3 = cache_kind == kU3;
     const int es = is_q8(cache_kind) ? 1 : 2;
     const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
-    int nh = u3 ? kU3Heads : 8;
+    const int group = num_heads / num_kv_heads;
+    // consumer warps per kv head: 2 for groups above 8 q heads (8 each);
+    // the CTA keeps at most 8 consumer warps
+    const int wsh = group > 8 ? 1 : 0;
+    int nh = u3 ? kU3Heads : (8 >> wsh);
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
     // 3-bit kernels are register-capped so that several CTAs share an SM; the
@@ -134,13 +139,13 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const int n_hg = num_kv_heads / nh;
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
     f.nh = nh;
+    f.wsh = wsh;
     f.n_hg = n_hg;
     f.stages = stages;
     const int64_t slots = int64_t(sm_count) * ctas_per_sm;
     f.grid = int(max_units < slots ? (max_units > 0 ? max_units : 1) : slots);
     f.smem_bytes = L.total;
     f.meta_heads = meta_heads;
-    const int group = num_heads / num_kv_heads;
     const int64_t rows = (int64_t(f.grid) + int64_t(n_hg) * batch) * nh * group;
     const size_t ml_bytes = (size_t(rows) * 2 * 4 + 255) / 256 * 256;
     workspace = ml_bytes + size_t(rows) * head_dim * 4;

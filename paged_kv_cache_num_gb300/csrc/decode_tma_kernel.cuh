@@ -289,7 +289,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, nh);
+            ptx::mbar_init(bar_empty + 8 * s, nh << f.wsh);   // one arrival per consumer warp
         }
         ptx::fence_mbar_init();
     }
@@ -320,7 +320,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (lo >= hi) return;
 
     // ======================================================== producer warp
-    if (warp == nh) {
+    if (warp == (nh << f.wsh)) {
         if (lane == 0) {
             ptx::prefetch_tmap(&tmk);
             ptx::prefetch_tmap(&tmv);
@@ -432,7 +432,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 
     // ======================================================== consumer warps
-    // Tokens on the MMA's M dimension, the group's q heads on N (G <= 8):
+    // Consumer warp w serves kv head kvl = w >> wsh of the CTA's group and,
+    // of its G q heads, the 8 (or fewer) from qh0 = 8 (w & (2^wsh - 1)):
+    // with groups of up to 8 q heads one warp per kv head, with up to 16
+    // two warps reading the same K / V tiles.
+    const int kvl = warp >> f.wsh;
+    const int qh0 = 8 * (warp & ((1 << f.wsh) - 1));
+    const int GW = min(8, G - qh0);           // q heads (head columns) of this warp
+    // Tokens on the MMA's M dimension, this warp's q heads on N (<= 8):
     //   S^T[tok][head] = K[tok][:] . Q[head][:]        (A = K, B = Q^T)
     //   O^T[d][head]  += V^T[d][tok] P^T[tok][head]     (A = V^T, B = P^T)
     // A thread of the C fragments holds heads 2tig, 2tig+1 for tokens
@@ -474,13 +481,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     float q1h[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
 
     auto start_segment = [&]() {
-        const int kvh = hg * nh + warp;
+        const int kvh = hg * nh + kvl;
         {
             const int cb = p.context_lens[b * p.cl_stride];
             ctx_b = cb < 0 ? 0 : (cb > cap ? cap : cb);
         }
-        const bool hv = gid < G;  // this lane's B column (q head gid) exists
-        const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + gid) * p.q_h);
+        const bool hv = gid < GW;  // this lane's B column (q head qh0 + gid) exists
+        const uint16_t *qr =
+            reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + qh0 + gid) * p.q_h);
         if constexpr (T::kIsU3) {
             // q' = q qs 2^(1-x) (f16, exact) in the pair order of the K
             // fragments: k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1)
@@ -608,7 +616,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     };
 
     auto finish_segment = [&](int64_t seg_end) {
-        const int kvh = hg * nh + warp;
+        const int kvh = hg * nh + kvl;
         const int64_t unit_first = int64_t(hg) * NBT + prefix[b];
         const int64_t unit_last = unit_first + nblk[b] - 1;
         float lt[2];
@@ -645,8 +653,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int g = 2 * tig + c;
-            if (g >= G) continue;
-            const int h = kvh * G + g;
+            if (g >= GW) continue;
+            const int h = kvh * G + qh0 + g;
             if (whole) {
                 const float inv = lt[c] > 0.0f ? vmul / lt[c] : 0.0f;
                 uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
@@ -658,7 +666,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         orow[d_of(t, r)] = p.q_is_bf16 ? f2h<kBF16>(v) : f2h<kF16>(v);
                     }
             } else {
-                const int64_t row = key * (int64_t(nh) * G) + int64_t(warp) * G + g;
+                const int64_t row = key * (int64_t(nh) * G) + int64_t(kvl) * G + qh0 + g;
                 float *acc = f.part_acc + row * D;
                 if (gid == 0) {
                     f.part_ml[2 * row] = m[c];
@@ -679,20 +687,20 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     auto u3_body = [&](auto nb_c, int s0, int s1, int valid) {
         constexpr int NB = decltype(nb_c)::value;
         constexpr int KTT = NB * T::KT;          // 16-token tiles of the NB blocks
-        const int kvh = hg * nh + warp;
+        const int kvh = hg * nh + kvl;
         const bool partial = valid < NB * BS;
         // stage of tile t, and the tile's first row within its block
         auto tile_stage = [&](int t) { return t < T::KT ? s0 : s1; };
         auto tile_row = [&](int t) { return 16 * (t % T::KT); };
         auto kpk = [&](int t) {                  // packed K rows of the tile (shared address)
-            return sbase + tile_stage(t) * L.stage_bytes + warp * BS * T::ROW + tile_row(t) * T::ROW;
+            return sbase + tile_stage(t) * L.stage_bytes + kvl * BS * T::ROW + tile_row(t) * T::ROW;
         };
         // ---- metadata of this lane's score rows (tokens gid, gid+8 of
         // each tile), staged with the block: [nh][BS] runs (head-major)
         // or [BS][num_kv_heads] arrays
         const int MH = f.meta_heads;
         const bool hmaj = MH == nh;
-        const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? warp * BS : kvh;
+        const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? kvl * BS : kvh;
         float sk[KTT][2], zk[KTT][2], sv[KTT][2], zv[KTT][2];
 #pragma unroll
         for (int mt = 0; mt < KTT; ++mt) {
@@ -848,14 +856,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             // fp8 / int8 per-block or per-token scales of this warp's head,
             // staged with the block: [nh][GS] K scales, then V scales
             const float *gsk = reinterpret_cast<const float *>(smem + s * L.stage_bytes + 2 * L.tile_bytes) +
-                               warp * GS;
+                               kvl * GS;
             const float *gsv = gsk + nh * GS;
             auto row_ks = [&](int tok) { return gsk[GS == 1 ? 0 : tok]; };
             auto row_vs = [&](int tok) { return gsv[GS == 1 ? 0 : tok]; };
             // this warp's head: rows of 128-byte sub-rows per half, or (XV)
             // one [head_dim/x][BS][16 B] run; piece c of token t at
             // (c * BS + t) * 16
-            const uint32_t ktile = sbase + s * L.stage_bytes + warp * BS * (XV ? T::ROW : 128);
+            const uint32_t ktile = sbase + s * L.stage_bytes + kvl * BS * (XV ? T::ROW : 128);
             const uint32_t vtile = ktile + L.tile_bytes;
             const int half_bytes = L.tile_bytes / T::HALVES;
             const int mi = lane >> 3;    // ldmatrix: which 8x8 matrix this lane addresses
@@ -1266,7 +1274,7 @@ cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUte
         if (e != cudaSuccess) return e;
         configured[dev].store(f.smem_bytes, std::memory_order_relaxed);
     }
-    e = launch_pdl(kern, dim3(f.grid), dim3((f.nh + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
+    e = launch_pdl(kern, dim3(f.grid), dim3(((f.nh << f.wsh) + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
     if (e != cudaSuccess) return e;
     const int rows = p.batch * p.num_heads;
     return launch_pdl(merge_kernel<D>, dim3((rows + kMergeWarps - 1) / kMergeWarps), dim3(32 * kMergeWarps),

@@ -122,7 +122,9 @@ struct DecodeParams {
 
 // Persistent TMA kernel (16-bit and fp8 caches).
 struct FastParams {
-    int nh;                     // kv heads per CTA (consumer warps)
+    int nh;                     // kv heads per CTA
+    int wsh;                    // log2(consumer warps per kv head): 1 when the group has
+                                // more than 8 q heads (each warp takes 8 of them)
     int n_hg;                   // head groups = num_kv_heads / nh
     int stages;                 // shared-memory ring depth
     int grid;                   // persistent CTAs

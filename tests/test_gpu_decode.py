@@ -435,3 +435,50 @@ def test_u3_bad_block_ids_in_pairs(pkv, orc):
     oc = PL.oracle_caches(w, orc, seqs=seqs)
     pairs = _sample_pairs(w, seqs)
     _check(w, fast, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+
+
+@pytest.mark.parametrize("kind,G,layout", [("bf16", 16, "flash"), ("bf16", 12, "flash"), ("f16", 16, "flash"),
+                                           ("bf16", 16, "xvec"), ("e4m3", 16, "flash"), ("i8", 12, "flash"),
+                                           ("e4m3", 16, "xvec")])
+def test_large_groups_two_warps_per_kv_head(pkv, orc, kind, G, layout):
+    """Groups of 9..16 q heads per kv head (Llama-3.1-405B: 128 q / 8 kv):
+    the persistent kernel gives each kv head two consumer warps, one per 8 q
+    heads (the second with G - 8 of them); parity with the oracle, on the
+    persistent kernel (no explicit split) and the general one."""
+    Hkv = 4
+    if kind in ("bf16", "f16"):
+        w = W.gqa_bf16(batch=5, ctx_lo=1, ctx_hi=1500, num_heads=G * Hkv, num_kv_heads=Hkv,
+                       seed=280 + G, layout=layout)
+        if kind == "f16":
+            w.dtype = torch.float16
+            w.cache_kind = "f16"
+            for name in ("q", "k_cache0", "v_cache0", "k_new", "v_new"):
+                setattr(w, name, getattr(w, name).to(torch.float16))
+    else:
+        w = W.fp8_long(batch=3, ctx_lo=20, ctx_hi=1200, num_heads=G * Hkv, num_kv_heads=Hkv,
+                       calib_tokens=64, seed=290 + G, fp8=kind, layout=layout)
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    for splits in (0, 2):
+        cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+        if splits == 0:
+            assert pkv.decode_launches(w.q.cuda(), cache, w.block_tables.cuda()) == 2  # persistent
+        _check(w, out, ref)
+
+
+def test_large_group_token_scales(pkv, orc):
+    """Group 16 with per-token fp8 scales staged with the blocks."""
+    w = W.fp8_long(batch=3, ctx_lo=20, ctx_hi=900, num_heads=64, num_kv_heads=4, calib_tokens=64,
+                   seed=299, scales="token")
+    _, out = PL.gpu_run(w, pkv)
+    _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
+
+
+def test_full_405b_like_fp8_sampled(pkv, orc):
+    """Llama-3.1-405B-like long-context e4m3 step: batch 8, 128 q / 8 kv
+    heads (group 16), contexts 16K..32K; sampled sequences, all heads."""
+    w = W.fp8_long(batch=8, num_heads=128, seed=298)
+    _, out = PL.gpu_run(w, pkv)
+    seqs = [1, 6]
+    oc = PL.oracle_caches(w, orc, seqs=seqs)
+    pairs = _sample_pairs(w, seqs)
+    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
