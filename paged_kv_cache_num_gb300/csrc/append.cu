@@ -18,9 +18,11 @@
 // each warp one row: the min / max are warp-shuffle reductions and the
 // packing goes through shared memory.  All are programmatic dependent launches, so the launch of each
 // overlaps the tail of the previous kernel in the stream.
+#include <algorithm>
 #include <type_traits>
 
 #include "pkv_device.cuh"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
@@ -48,17 +50,22 @@ __device__ __forceinline__ int64_t slot_from_position(const SlotMapParams &p, in
     return slot;
 }
 
-// `first`: this caller writes the token's computed slot out (from_pos)
-__device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, int64_t &blk,
-                                             int64_t &off, bool first = false)
+// the slot of token t; `first`: this caller writes a computed slot out
+// (from_pos)
+__device__ __forceinline__ int64_t fetch_slot(const AppendParams &p, int64_t t, bool first)
 {
-    int64_t slot;
     if (p.from_pos) {
-        slot = slot_from_position(p.pos_map, t);
+        const int64_t slot = slot_from_position(p.pos_map, t);
         if (first) p.pos_map.slot_mapping[t] = slot;
-    } else {
-        slot = p.slot_mapping[t * p.slot_stride];
+        return slot;
     }
+    return p.slot_mapping[t * p.slot_stride];
+}
+
+// (block, offset) of a slot; false for a padding token (slot < 0) and for a
+// slot outside the pool (raising PKV_DEVERR_SLOT_RANGE)
+__device__ __forceinline__ bool place_slot(const AppendParams &p, int64_t slot, int64_t &blk, int64_t &off)
+{
     if (slot < 0) return false;                 // padding token: nothing to read or write
     if (slot >= p.num_slots) {
         raise_err(p.err_flag, PKV_DEVERR_SLOT_RANGE);
@@ -72,6 +79,13 @@ __device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, i
         off = slot - blk * p.block_size;
     }
     return true;
+}
+
+// `first`: this caller writes the token's computed slot out (from_pos)
+__device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, int64_t &blk,
+                                             int64_t &off, bool first = false)
+{
+    return place_slot(p, fetch_slot(p, t, first), blk, off);
 }
 
 // Work items of the copy and one-byte append kernels: a (token, K|V) row
@@ -131,6 +145,87 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
                 }
             }
         }
+    }
+}
+
+// 16-bit rows whose kv heads are contiguous in the source and in the cache
+// (the flash layout): each (token, K|V) row is one run of Hkv * head_dim
+// elements on both sides and moves with two TMA bulk copies, global ->
+// shared -> global, without passing through registers.  One thread per CTA
+// issues them through a ring of kBulkSlots shared-memory rows: the load of
+// row k is issued kBulkLag rows ahead of its store, and a slot is reloaded
+// only once the store issued from it has read it.  The warp's lanes fetch
+// the slots of the next 32 rows at once.  Every wait is bounded.
+constexpr int kBulkSlots = 8;
+constexpr int64_t kBulkMinTokens = 1024;   // below this the warp kernel is as fast
+constexpr int kBulkLag = 4;
+constexpr uint64_t kBulkTimeoutNs = 2000000000ull;
+
+__global__ void __launch_bounds__(32) append_bulk_kernel(AppendParams p)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    extern __shared__ __align__(128) unsigned char bulk_buf[];
+    __shared__ __align__(8) uint64_t bars[kBulkSlots];
+    __shared__ char *dsts[kBulkSlots];
+    const int lane = threadIdx.x;
+    const uint32_t row_bytes = uint32_t(p.num_kv_heads) * uint32_t(p.head_dim) * 2u;
+    const uint32_t buf = ptx::smem_u32(bulk_buf);
+    const uint32_t bar0 = ptx::smem_u32(bars);
+    if (lane == 0) {
+        for (int i = 0; i < kBulkSlots; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    const int64_t rows = p.num_tokens * 2;
+    const int64_t n = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t k = 0;                  // rows of this CTA with a copy issued (lane 0)
+    bool aborted = false;
+    // store of the row in ring position j (its load issued earlier)
+    auto store = [&](int64_t j) {
+        const int sl = int(j % kBulkSlots);
+        if (!ptx::mbar_wait_bounded(bar0 + 8 * sl, uint32_t((j / kBulkSlots) & 1), kBulkTimeoutNs)) {
+            raise_err(p.err_flag, PKV_DEVERR_TIMEOUT);
+            aborted = true;
+            return;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::bulk_store(dsts[sl], buf + sl * row_bytes, row_bytes);
+        ptx::bulk_commit();
+    };
+    for (int64_t i0 = 0; i0 < n; i0 += 32) {
+        int64_t mine = -1;          // lane l: the slot of this CTA's row i0 + l
+        if (i0 + lane < n) {
+            const int64_t r = blockIdx.x + (i0 + lane) * gridDim.x;
+            mine = fetch_slot(p, r >> 1, (r & 1) == 0);
+        }
+        for (int jj = 0; jj < 32 && i0 + jj < n; ++jj) {
+            const int64_t slot = __shfl_sync(0xffffffffu, mine, jj);
+            if (lane != 0 || aborted) continue;
+            int64_t blk, off;
+            if (!place_slot(p, slot, blk, off)) continue;      // padding / out of range
+            const int64_t r = blockIdx.x + (i0 + jj) * gridDim.x;
+            const int64_t t = r >> 1;
+            const int kv = int(r & 1);
+            const int sl = int(k % kBulkSlots);
+            // the store issued from this slot kBulkSlots rows ago has read it:
+            // stores of rows <= k - kBulkLag - 1 are committed, at most
+            // kBulkSlots - kBulkLag - 1 of them may still be reading
+            if (k >= kBulkSlots) ptx::bulk_wait_read<kBulkSlots - kBulkLag - 1>();
+            dsts[sl] = (kv ? p.v_cache : p.k_cache) + blk * p.c_blk + off * p.c_slot;
+            const char *src = kv ? p.v_new + t * p.v_src_tok : p.k_new + t * p.k_src_tok;
+            ptx::mbar_arrive_expect_tx(bar0 + 8 * sl, row_bytes);
+            ptx::bulk_load(buf + sl * row_bytes, src, row_bytes, bar0 + 8 * sl);
+            if (k >= kBulkLag) store(k - kBulkLag);
+            ++k;
+        }
+    }
+    if (lane == 0) {
+        for (int64_t j = k > kBulkLag ? k - kBulkLag : 0; j < k && !aborted; ++j) store(j);
+        // copies still in flight (an aborted wait) land before the CTA exits
+        for (int64_t j = k > kBulkLag ? k - kBulkLag : 0; aborted && j < k; ++j)
+            ptx::mbar_wait_bounded(bar0 + 8 * int(j % kBulkSlots), uint32_t((j / kBulkSlots) & 1), kBulkTimeoutNs);
+        ptx::bulk_wait_all();
     }
 }
 
@@ -329,6 +424,14 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
     };
     auto grid = [&](int per, int U) { return grid_for(p.num_tokens * 2 * append_parts(per, U) * 32, T); };
     if (cache_kind == kF16 || cache_kind == kBF16) {
+        // large batches with contiguous head rows on both sides: TMA bulk copies
+        const int64_t row_bytes = int64_t(p.num_kv_heads) * p.head_dim * 2;
+        if (vec16 && p.num_tokens >= kBulkMinTokens && p.k_src_head == p.head_dim * 2 &&
+            p.v_src_head == p.head_dim * 2 && p.c_head == p.head_dim * 2 && p.c_chunk == 16 &&
+            row_bytes % 16 == 0 && kBulkSlots * row_bytes <= 48 * 1024) {
+            const int g = int(std::min<int64_t>(p.num_tokens * 2, int64_t(sm_count_current_device()) * 8));
+            return launch_pdl(append_bulk_kernel, g, 32, size_t(kBulkSlots * row_bytes), s, p);
+        }
         const int per = p.num_kv_heads * (vec16 ? p.head_dim * 2 / 16 : p.head_dim);
         const bool one = small(per);
         const int g = grid(per, one ? 1 : 4);

@@ -110,6 +110,40 @@ def test_out_of_range_slot_is_skipped_and_flagged(pkv):
     assert torch.all(flat[5] == 1) and int((flat != 0).sum()) == H * D
 
 
+@pytest.mark.parametrize("Hkv,T", [(8, 1500), (2, 4096), (16, 1024)])
+def test_bulk_copy_path_large_batch(pkv, orc, Hkv, T):
+    """Batches of >= 1024 tokens whose head rows are contiguous take the
+    TMA bulk-copy append (global -> shared -> global per (token, K|V) row):
+    bit exact over the whole pool, with padding tokens and slots out of the
+    pool skipped (and flagged), at several row sizes and ring wrap-arounds."""
+    D, BS = 128, 16
+    g = torch.Generator().manual_seed(300 + Hkv)
+    P = (T + 200) // BS + 8
+    perm = torch.randperm(P * BS, generator=g)[:T].to(torch.int64)
+    slots = perm.clone()
+    slots[::7] = -1                                   # padding tokens
+    slots[3] = P * BS + 11                            # out of the pool
+    kn = torch.randn((T, Hkv, D), generator=g).to(torch.bfloat16)
+    vn = torch.randn((T, Hkv, D), generator=g).to(torch.bfloat16)
+    kn[slots < 0] = float("nan")
+    vn[slots < 0] = float("nan")
+    k0 = torch.randint(0, 256, (P * BS * Hkv * D * 2,), generator=g, dtype=torch.uint8)
+    v0 = torch.randint(0, 256, (P * BS * Hkv * D * 2,), generator=g, dtype=torch.uint8)
+    cache = pkv.KVCache.allocate("bf16", P, BS, Hkv, D)
+    cache.k_cache.view(torch.uint8).view(-1).copy_(k0.cuda())
+    cache.v_cache.view(torch.uint8).view(-1).copy_(v0.cuda())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pkv.pkv.DEVERR_SLOT_RANGE
+    ok_ = k0.view(torch.int16).numpy().view(np.uint16).reshape(P, BS, Hkv, D).copy()
+    ov_ = v0.view(torch.int16).numpy().view(np.uint16).reshape(P, BS, Hkv, D).copy()
+    bad = orc.kv_append(2, 2, W.bits16(kn), W.bits16(vn), slots.numpy(), ok_, ov_)
+    assert bad == 1
+    got = PL.gpu_cache_host(cache)
+    assert np.array_equal(got["k_cache"], ok_) and np.array_equal(got["v_cache"], ov_)
+
+
 def test_idempotent_append(pkv):
     w = W.tiny()
     cache, _ = PL.gpu_run(w, pkv, decode=False)
