@@ -14,12 +14,37 @@
 // the unpacking kernels exchange halves between lanes so that each store
 // instruction of a warp is one contiguous 512-byte run.  The kernels are
 // pure HBM streams.
+#include <atomic>
+
 #include "pkv_device.cuh"
 
 namespace pkv {
 namespace {
 
 constexpr int kThreads = 256;
+
+// Blocks of kernel K (kThreads threads each, no dynamic shared memory) that
+// one SM holds at once, at least 1; queried once per device.  The
+// grid-stride kernels below size their grids to SMs x this, one wave:
+// blocks beyond it would start only after a first wave had finished its
+// share.
+template <auto K>
+int resident_blocks()
+{
+    constexpr int kDevices = 64;
+    static std::atomic<int> cache[kDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 1;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, kThreads, 0) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();     // not left pending for the launch's own check
+            n = 1;
+        }
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
 
 __device__ __forceinline__ uint32_t pack_octet(uint32_t lo4, uint32_t hi4)
 {
@@ -77,11 +102,48 @@ __global__ void __launch_bounds__(kThreads) pack3_kernel(const uint8_t *__restri
     }
 }
 
-// A warp unpacks 32 consecutive 4-octet quads (384 packed bytes -> 1 KB of
-// values): lane l unpacks quad l, then the two store instructions write
-// 16-byte units l and 32 + l of the warp's kilobyte, the halves moved
-// between lanes by shuffles, so that every store instruction is one
-// contiguous 512-byte run.
+// Quad (4 octets, 12 packed bytes) i of the input as 32 value bytes: x holds
+// octets 0-1, y octets 2-3 (zeros past the end).
+__device__ __forceinline__ void unpack_quad(const uint8_t *__restrict__ packed, int64_t i, int64_t n4, uint4 &x,
+                                            uint4 &y)
+{
+    x = make_uint4(0, 0, 0, 0);
+    y = make_uint4(0, 0, 0, 0);
+    if (i < n4) {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(packed + 12 * i);
+        const uint32_t a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
+        unpack_octet(a & 0xffffffu, x.x, x.y);
+        unpack_octet((a >> 24) | ((b & 0xffffu) << 8), x.z, x.w);
+        unpack_octet((b >> 16) | ((c & 0xffu) << 16), y.x, y.y);
+        unpack_octet(c >> 8, y.z, y.w);
+    }
+}
+
+// The warp's 32 units (x, y: 32 value bytes each, unit `lane` in lane
+// `lane`) of chunk wc, written as 16-byte pieces 32k + lane of the chunk's
+// kilobyte: piece 32k + lane is half (lane & 1) of unit 16k + (lane >> 1),
+// moved between lanes by shuffles, so that each store instruction is one
+// contiguous 512-byte run.  Every lane takes part in both shuffles, then
+// keeps its half.
+__device__ __forceinline__ void store_chunk(uint8_t *__restrict__ values, int64_t wc, int64_t units, int lane,
+                                            const uint4 &x, const uint4 &y)
+{
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int srcl = 16 * k + (lane >> 1);
+        const bool hi = lane & 1;
+        const uint32_t a0 = __shfl_sync(0xffffffffu, x.x, srcl), b0 = __shfl_sync(0xffffffffu, y.x, srcl);
+        const uint32_t a1 = __shfl_sync(0xffffffffu, x.y, srcl), b1 = __shfl_sync(0xffffffffu, y.y, srcl);
+        const uint32_t a2 = __shfl_sync(0xffffffffu, x.z, srcl), b2 = __shfl_sync(0xffffffffu, y.z, srcl);
+        const uint32_t a3 = __shfl_sync(0xffffffffu, x.w, srcl), b3 = __shfl_sync(0xffffffffu, y.w, srcl);
+        const uint4 o = hi ? make_uint4(b0, b1, b2, b3) : make_uint4(a0, a1, a2, a3);
+        if (wc * 32 + srcl < units) reinterpret_cast<uint4 *>(values)[2 * (wc * 32) + 32 * k + lane] = o;
+    }
+}
+
+// A warp unpacks chunks of 32 consecutive 4-octet quads (384 packed bytes ->
+// 1 KB of values), lane l quad l; two chunks per pass, both loads issued
+// before either is unpacked, so that each warp keeps two reads in flight.
 __global__ void __launch_bounds__(kThreads) unpack3_kernel(const uint8_t *__restrict__ packed,
                                                            uint8_t *__restrict__ values, int64_t n)
 {
@@ -89,35 +151,13 @@ __global__ void __launch_bounds__(kThreads) unpack3_kernel(const uint8_t *__rest
     const int lane = threadIdx.x & 31;
     const int64_t chunks = (n4 + 31) / 32;
     const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t wc = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; wc < chunks; wc += wstep) {
-        const int64_t i = wc * 32 + lane;
-        uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
-        if (i < n4) {
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(packed + 12 * i);
-            const uint32_t a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
-            const uint32_t w0 = a & 0xffffffu;
-            const uint32_t w1 = (a >> 24) | ((b & 0xffffu) << 8);
-            const uint32_t w2 = (b >> 16) | ((c & 0xffu) << 16);
-            const uint32_t w3 = c >> 8;
-            unpack_octet(w0, x.x, x.y);
-            unpack_octet(w1, x.z, x.w);
-            unpack_octet(w2, y.x, y.y);
-            unpack_octet(w3, y.z, y.w);
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            // unit 32k + lane = half (lane & 1) of quad 16k + (lane >> 1)
-            const int srcl = 16 * k + (lane >> 1);
-            // every lane takes part in both shuffles, then keeps its half
-            const bool hi = lane & 1;
-            const uint32_t a0 = __shfl_sync(0xffffffffu, x.x, srcl), b0 = __shfl_sync(0xffffffffu, y.x, srcl);
-            const uint32_t a1 = __shfl_sync(0xffffffffu, x.y, srcl), b1 = __shfl_sync(0xffffffffu, y.y, srcl);
-            const uint32_t a2 = __shfl_sync(0xffffffffu, x.z, srcl), b2 = __shfl_sync(0xffffffffu, y.z, srcl);
-            const uint32_t a3 = __shfl_sync(0xffffffffu, x.w, srcl), b3 = __shfl_sync(0xffffffffu, y.w, srcl);
-            const uint4 o = hi ? make_uint4(b0, b1, b2, b3) : make_uint4(a0, a1, a2, a3);
-            const int64_t q = wc * 32 + srcl;
-            if (q < n4) reinterpret_cast<uint4 *>(values)[2 * (wc * 32) + 32 * k + lane] = o;
-        }
+    for (int64_t wc = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; wc < chunks; wc += 2 * wstep) {
+        const int64_t wc2 = wc + wstep;
+        uint4 x0, y0, x1, y1;
+        unpack_quad(packed, wc * 32 + lane, n4, x0, y0);
+        unpack_quad(packed, wc2 * 32 + lane, n4, x1, y1);
+        store_chunk(values, wc, n4, lane, x0, y0);
+        if (wc2 < chunks) store_chunk(values, wc2, n4, lane, x1, y1);
     }
     const int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (t < n - 4 * n4) {
@@ -133,48 +173,46 @@ __global__ void __launch_bounds__(kThreads) unpack3_kernel(const uint8_t *__rest
     }
 }
 
-// One 96-bit group per lane: lane i = (W[w] >> s | W[w+1] << (32-s)) & 7
-// with w = 3i/32, s = 3i%32, the second term only for s > 29.  A warp takes
-// 32 consecutive groups and writes their kilobyte of values with two
-// contiguous store instructions (halves exchanged by shuffles, as in
-// unpack3_kernel).
+// 96-bit group g as 32 value bytes: lane i = (W[w] >> s | W[w+1] << (32-s))
+// & 7 with w = 3i/32, s = 3i%32, the second term only for s > 29 (zeros past
+// the end).
+__device__ __forceinline__ void unpack_group(const uint32_t *__restrict__ words, int64_t g, int64_t m, uint4 &x,
+                                             uint4 &y)
+{
+    uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (g < m) {
+        uint32_t W[3];
+        W[0] = __ldg(words + 3 * g);
+        W[1] = __ldg(words + 3 * g + 1);
+        W[2] = __ldg(words + 3 * g + 2);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int w = (3 * i) >> 5, s = (3 * i) & 31;
+            uint32_t v = W[w] >> s;
+            if (s > 29) v |= W[w + 1] << (32 - s);   // compile-time lanes 10, 21
+            v &= 7u;
+            if ((i & 3) == 0) out[i >> 2] = v; else out[i >> 2] |= v << (8 * (i & 3));
+        }
+    }
+    x = make_uint4(out[0], out[1], out[2], out[3]);
+    y = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+// One 96-bit group per lane, chunks of 32 consecutive groups (a kilobyte of
+// values) per warp, two chunks per pass as in unpack3_kernel.
 __global__ void __launch_bounds__(kThreads) unpack3_words_kernel(
     const uint32_t *__restrict__ words, uint8_t *__restrict__ values, int64_t m)
 {
     const int lane = threadIdx.x & 31;
     const int64_t chunks = (m + 31) / 32;
     const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t wc = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; wc < chunks; wc += wstep) {
-        const int64_t g = wc * 32 + lane;
-        uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (g < m) {
-            uint32_t W[3];
-            W[0] = __ldg(words + 3 * g);
-            W[1] = __ldg(words + 3 * g + 1);
-            W[2] = __ldg(words + 3 * g + 2);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int w = (3 * i) >> 5, s = (3 * i) & 31;
-                uint32_t v = W[w] >> s;
-                if (s > 29) v |= W[w + 1] << (32 - s);   // compile-time lanes 10, 21
-                v &= 7u;
-                if ((i & 3) == 0) out[i >> 2] = v; else out[i >> 2] |= v << (8 * (i & 3));
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            // unit 32k + lane = half (lane & 1) of group 16k + (lane >> 1)
-            const int srcl = 16 * k + (lane >> 1);
-            const bool hi = lane & 1;
-            uint32_t a[4], b[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {   // every lane takes part in both shuffles
-                a[j] = __shfl_sync(0xffffffffu, out[j], srcl);
-                b[j] = __shfl_sync(0xffffffffu, out[4 + j], srcl);
-            }
-            const uint4 o = hi ? make_uint4(b[0], b[1], b[2], b[3]) : make_uint4(a[0], a[1], a[2], a[3]);
-            if (wc * 32 + srcl < m) reinterpret_cast<uint4 *>(values)[2 * (wc * 32) + 32 * k + lane] = o;
-        }
+    for (int64_t wc = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; wc < chunks; wc += 2 * wstep) {
+        const int64_t wc2 = wc + wstep;
+        uint4 x0, y0, x1, y1;
+        unpack_group(words, wc * 32 + lane, m, x0, y0);
+        unpack_group(words, wc2 * 32 + lane, m, x1, y1);
+        store_chunk(values, wc, m, lane, x0, y0);
+        if (wc2 < chunks) store_chunk(values, wc2, m, lane, x1, y1);
     }
 }
 
@@ -196,10 +234,12 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const uint4 *__restrict_
     for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
+// blocks for `work` threads of kernel K, at most one resident wave
+template <auto K>
 int grid_for(int64_t work)
 {
     const int64_t blocks = (work + kThreads - 1) / kThreads;
-    const int64_t cap = int64_t(sm_count_current_device()) * 8;
+    const int64_t cap = int64_t(sm_count_current_device()) * resident_blocks<K>();
     return int(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
@@ -208,14 +248,14 @@ int grid_for(int64_t work)
 cudaError_t launch_pack3(const uint8_t *values, uint8_t *packed, int64_t n, cudaStream_t s)
 {
     if (n == 0) return cudaSuccess;
-    pack3_kernel<<<grid_for(n / 4 + 4), kThreads, 0, s>>>(values, packed, n);
+    pack3_kernel<<<grid_for<pack3_kernel>(n / 4 + 4), kThreads, 0, s>>>(values, packed, n);
     return cudaGetLastError();
 }
 
 cudaError_t launch_unpack3(const uint8_t *packed, uint8_t *values, int64_t n, cudaStream_t s)
 {
     if (n == 0) return cudaSuccess;
-    unpack3_kernel<<<grid_for(n / 4 + 4), kThreads, 0, s>>>(packed, values, n);
+    unpack3_kernel<<<grid_for<unpack3_kernel>(n / 4 + 4), kThreads, 0, s>>>(packed, values, n);
     return cudaGetLastError();
 }
 
@@ -223,7 +263,7 @@ cudaError_t launch_unpack3_words(const uint32_t *words, uint8_t *values, int64_t
                                  cudaStream_t s)
 {
     if (m == 0) return cudaSuccess;
-    unpack3_words_kernel<<<grid_for(m), kThreads, 0, s>>>(words, values, m);
+    unpack3_words_kernel<<<grid_for<unpack3_words_kernel>(m), kThreads, 0, s>>>(words, values, m);
     return cudaGetLastError();
 }
 
@@ -231,7 +271,7 @@ cudaError_t launch_copy_peak(const void *src, void *dst, size_t bytes, cudaStrea
 {
     const int64_t n16 = int64_t(bytes / 16);
     if (n16 == 0) return cudaSuccess;
-    const int blocks = sm_count_current_device() * 8;
+    const int blocks = sm_count_current_device() * resident_blocks<copy_kernel>();
     copy_kernel<<<blocks, kThreads, 0, s>>>(reinterpret_cast<const uint4 *>(src),
                                             reinterpret_cast<uint4 *>(dst), n16);
     return cudaGetLastError();

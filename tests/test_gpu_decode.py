@@ -395,6 +395,101 @@ def test_decode_step_padding_and_bad_positions(pkv, orc, kind):
     assert torch.equal(out, out_sep)
 
 
+def test_decode_step_prefill_sized_batch(pkv, orc):
+    """A step whose append is prefill-sized (>= 1024 tokens, contiguous head
+    rows) runs the bulk-copy append with the slots computed inside it: same
+    slots, cache bytes (whole pool) and output as the separate calls."""
+    w = W.mixed_append(n_prefill=4, n_decode=12, prefill_lo=300, prefill_hi=600, ctx_lo=100,
+                       ctx_hi=900, block_size=16, seed=273)
+    assert int((w.new_pos >= 0).sum()) >= 1024
+    g = torch.Generator().manual_seed(274)
+    w.num_heads = 4 * w.num_kv_heads
+    w.q = torch.randn((w.batch, w.num_heads, w.head_dim), generator=g).to(w.dtype)
+    # finite older rows for the decode requests (the pool is random bytes otherwise)
+    w.k_cache0 = torch.randn(tuple(w.k_cache0.shape), generator=g).to(w.dtype)
+    w.v_cache0 = torch.randn(tuple(w.v_cache0.shape), generator=g).to(w.dtype)
+    dev = "cuda"
+    cache_a, out_a = PL.gpu_run(w, pkv)                       # slot_mapping + append + decode
+    cache_b = pkv.KVCache.allocate("bf16", w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    cache_b.k_cache.copy_(w.k_cache0.to(dev))
+    cache_b.v_cache.copy_(w.v_cache0.to(dev))
+    bt, req, pos = w.block_tables.to(dev), w.new_req.to(dev), w.new_pos.to(dev)
+    slots = torch.full((req.shape[0],), -7, dtype=torch.int64, device=dev)
+    out_b = pkv.decode_step(w.k_new.to(dev), w.v_new.to(dev), req, pos, w.q.to(dev), cache_b, bt,
+                            w.context_lens.to(dev), sm_scale=w.sm_scale, slots=slots)
+    torch.cuda.synchronize()
+    assert torch.equal(slots, pkv.slot_mapping(bt, req, pos, w.block_size))
+    a, b = PL.gpu_cache_host(cache_a), PL.gpu_cache_host(cache_b)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    assert torch.equal(out_a, out_b)
+    oc = PL.oracle_caches(w, orc)
+    assert np.array_equal(b["k_cache"], oc["k_cache"]) and np.array_equal(b["v_cache"], oc["v_cache"])
+    _check(w, out_b, PL.oracle_decode(w, orc, oc))
+
+
+class _Top:
+    """The blocks [off, num_blocks) of a cache, under the attribute names
+    PL.gpu_cache_host reads."""
+    def __init__(self, cache, off):
+        for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero", "k_scales",
+                     "v_scales"):
+            t = getattr(cache, name, None)
+            setattr(self, name, None if t is None else t[off:])
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "u3"])
+def test_pool_beyond_4gib(pkv, orc, kind):
+    """A pool whose K and V caches pass 4 GiB each, the sequences' blocks at
+    its top (every byte offset above 2^32): the appends write the same bytes
+    and both decode kernels give the same outputs, bit for bit, as on a pool
+    of just those blocks."""
+    if kind == "bf16":
+        w = W.gqa_bf16(batch=3, ctx_lo=40, ctx_hi=300, seed=275)
+    elif kind == "e4m3":
+        w = W.fp8_long(batch=3, ctx_lo=40, ctx_hi=300, calib_tokens=64, seed=276)
+    else:
+        w = W.u3_mha(batch=3, ctx_lo=3, ctx_hi=500, num_heads=8, seed=277)
+    dev = "cuda"
+    small, out0 = PL.gpu_run(w, pkv)
+    _, out3 = PL.gpu_run(w, pkv, num_splits=3)
+    ref = PL.gpu_cache_host(small)
+    del small
+    row = {"bf16": 2 * w.head_dim, "e4m3": w.head_dim, "u3": 3 * w.head_dim // 8}[kind]
+    block_bytes = w.block_size * w.num_kv_heads * row
+    off = (1 << 32) // block_bytes + 17
+    cache = pkv.KVCache.allocate(w.cache_kind, w.num_blocks + off, w.block_size, w.num_kv_heads,
+                                 w.head_dim, device=dev,
+                                 k_scale=None if w.k_scale is None else w.k_scale.to(dev),
+                                 v_scale=None if w.v_scale is None else w.v_scale.to(dev))
+    assert cache.k_cache[off:].data_ptr() - cache.k_cache.data_ptr() > (1 << 32)
+    top = _Top(cache, off)
+    for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero"):
+        if getattr(top, name) is not None:     # as the small run's pool started (fill 0)
+            getattr(top, name).zero_()
+    if w.k_cache0 is not None:
+        top.k_cache.copy_(w.k_cache0.to(dev))
+        top.v_cache.copy_(w.v_cache0.to(dev))
+    bt = (w.block_tables + off).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if w.fill_req is not None:
+        sm = pkv.slot_mapping(bt, w.fill_req.to(dev), w.fill_pos.to(dev), w.block_size, err_flag=err)
+        pkv.kv_append(w.k_fill.to(dev), w.v_fill.to(dev), sm, cache, err_flag=err)
+    sm = pkv.slot_mapping(bt, w.new_req.to(dev), w.new_pos.to(dev), w.block_size, err_flag=err)
+    pkv.kv_append(w.k_new.to(dev), w.v_new.to(dev), sm, cache, err_flag=err)
+    outs = [pkv.paged_decode(w.q.to(dev), cache, bt, w.context_lens.to(dev), sm_scale=w.sm_scale,
+                             num_splits=ns, err_flag=err) for ns in (0, 3)]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = PL.gpu_cache_host(top)
+    for k in ref:
+        assert np.array_equal(ref[k], got[k]), k
+    assert torch.equal(outs[0], out0) and torch.equal(outs[1], out3)
+    del cache, top
+    torch.cuda.empty_cache()
+    _check(w, outs[0], PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
+
+
 def test_decode_step_without_new_tokens(pkv):
     """A step with no new tokens launches no append; its decode then waits
     for the stream's earlier work as a plain paged_decode does, and gives the
