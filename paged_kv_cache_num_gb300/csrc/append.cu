@@ -88,6 +88,31 @@ __device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, i
     return place_slot(p, fetch_slot(p, t, first), blk, off);
 }
 
+// A grid-stride walk over items i = major * n + minor (0 <= minor < n)
+// that keeps (major, minor) current by additions: one 64-bit division per
+// warp at the start, none per item (a 64-bit division by a runtime value
+// costs about a hundred instructions).
+struct Walk2 {
+    int64_t major, step_major;
+    int minor, step_minor, n;
+    __device__ __forceinline__ Walk2(int64_t first, int64_t step, int n_) : n(n_)
+    {
+        major = first / n;
+        minor = int(first - major * n);
+        step_major = step / n;
+        step_minor = int(step - step_major * n);
+    }
+    __device__ __forceinline__ void next()
+    {
+        major += step_major;
+        minor += step_minor;
+        if (minor >= n) {
+            minor -= n;
+            ++major;
+        }
+    }
+};
+
 // Work items of the copy and one-byte append kernels: a (token, K|V) row
 // split into parts of 32 * U pieces, one warp per item.  U = 4 (four loads
 // in flight per lane) for large batches, U = 1 for small ones, which then
@@ -107,11 +132,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_copy_kernel(AppendParam
     const int cph = p.head_dim * 2 / CHUNK;        // pieces per head row
     const int per = p.num_kv_heads * cph;          // pieces per (token, K|V)
     const int parts = append_parts(per, U);
-    const int64_t items = p.num_tokens * 2 * parts;
     const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t item = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; item < items; item += wstep) {
-        const int64_t row = item / parts;
-        const int part = int(item - row * parts);
+    for (Walk2 w((blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5, wstep, parts);
+         w.major < p.num_tokens * 2; w.next()) {
+        const int64_t row = w.major;          // (token, K|V)
+        const int part = w.minor;
         const int64_t t = row >> 1;
         const int kv = int(row & 1);
         int64_t blk, off;
@@ -257,13 +282,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
     constexpr int kU = U;
     const int lane = threadIdx.x & 31;
     const int groups = p.head_dim / 8;             // pieces per head row
+    const int gsh = (groups & (groups - 1)) == 0 ? __ffs(groups) - 1 : -1;   // log2(groups), if a power of 2
     const int per = p.num_kv_heads * groups;       // pieces per (token, K|V)
     const int parts = append_parts(per, U);
-    const int64_t items = p.num_tokens * 2 * parts;
     const int64_t wstep = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t item = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; item < items; item += wstep) {
-        const int64_t row = item / parts;
-        const int part = int(item - row * parts);
+    for (Walk2 w((blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5, wstep, parts);
+         w.major < p.num_tokens * 2; w.next()) {
+        const int64_t row = w.major;          // (token, K|V)
+        const int part = w.minor;
         const int64_t t = row >> 1;
         const int kv = int(row & 1);
         int64_t blk, off;
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
             for (int u = 0; u < kU; ++u) {
                 const int i = i0 + 32 * u;
                 if (i >= per) continue;
-                const int h = i / groups, c = i - h * groups;
+                const int h = gsh >= 0 ? i >> gsh : i / groups, c = i - h * groups;
                 const uint16_t *src = reinterpret_cast<const uint16_t *>(src_row + h * src_head) + 8 * c;
                 if constexpr (VEC) {
                     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
@@ -293,7 +319,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
             for (int u = 0; u < kU; ++u) {
                 const int i = i0 + 32 * u;
                 if (i >= per) continue;
-                const int h = i / groups, c = i - h * groups;
+                const int h = gsh >= 0 ? i >> gsh : i / groups, c = i - h * groups;
                 // elements 8c .. 8c+7: half of the row's 16-byte piece c / 2
                 uint8_t *dst = reinterpret_cast<uint8_t *>(dst_row + h * p.c_head + (c >> 1) * p.c_chunk) +
                                8 * (c & 1);
@@ -327,71 +353,111 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
     }
 }
 
-// 3-bit affine quantise + pack: one warp per (token, head, K|V) row.
-// Each lane holds head_dim / 32 consecutive elements.
+// 3-bit affine quantise + pack: eight lanes per (token, head, K|V) row,
+// four rows per warp.  Each lane holds EPL = head_dim / 8 consecutive
+// elements; a row's min / max are three-step shuffle reductions among its
+// eight lanes, which then each derive the row's scale and zero point (IEEE
+// divisions, as the codes).  A lane's codes make EPL / 8 fields of 24 bits
+// (8 codes each; code d sits at bit 3d of the packed row), and four
+// consecutive fields -- 96 bits -- fill one 12-byte run, assembled by the
+// first lane holding a field of it from the others' (warp shuffles).
 template <int SRC, int EPL>
 __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams p)
 {
     griddep_wait();
     griddep_launch_dependents();
-    constexpr int D = EPL * 32;
     constexpr int WARPS = kAppendThreads / 32;
-    __shared__ uint8_t codes[WARPS][D];
+    constexpr int NF = EPL / 8;          // 24-bit fields per lane (1 or 2)
+    constexpr int LR = 4 / NF;           // lanes per 12-byte run (4 or 2)
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int64_t rows = p.num_tokens * p.num_kv_heads * 2;
-    for (int64_t row = blockIdx.x * int64_t(WARPS) + wid; row < rows;
-         row += int64_t(gridDim.x) * WARPS) {
-        const int64_t t = row / (2 * p.num_kv_heads);
-        const int r = int(row - t * 2 * p.num_kv_heads);
+    const int grp = lane >> 3, sub = lane & 7;   // the warp's row, the lane within it
+    Walk2 w((blockIdx.x * int64_t(WARPS) + wid) * 4 + grp, int64_t(gridDim.x) * WARPS * 4, 2 * p.num_kv_heads);
+    while (__any_sync(0xffffffffu, w.major < p.num_tokens)) {
+        const int64_t t = w.major;
+        const int r = w.minor;               // (kv head, K|V)
         const int h = r >> 1, kv = r & 1;
-        int64_t blk, off;
-        if (!resolve_slot(p, t, blk, off, r == 0 && lane == 0)) continue;   // warp-uniform
-        const uint16_t *src = reinterpret_cast<const uint16_t *>(
-            kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
-               : p.k_new + t * p.k_src_tok + h * p.k_src_head) + EPL * lane;
+        int64_t blk = 0, off = 0;
+        const bool live = t < p.num_tokens && resolve_slot(p, t, blk, off, r == 0 && sub == 0);
         float x[EPL];
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) x[j] = h2f<SRC>(src[j]);
+        for (int j = 0; j < EPL; ++j) x[j] = 0.0f;
+        if (live) {
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(
+                kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
+                   : p.k_new + t * p.k_src_tok + h * p.k_src_head) + EPL * sub;
+            if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {       // 16-byte vector loads
+#pragma unroll
+                for (int v = 0; v < EPL / 8; ++v) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+                    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        x[8 * v + 2 * k] = h2f<SRC>(uint16_t(ww[k]));
+                        x[8 * v + 2 * k + 1] = h2f<SRC>(uint16_t(ww[k] >> 16));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) x[j] = h2f<SRC>(src[j]);
+            }
+        }
         float mn = x[0], mx = x[0];
 #pragma unroll
         for (int j = 1; j < EPL; ++j) { mn = fminf(mn, x[j]); mx = fmaxf(mx, x[j]); }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
+        for (int o = 1; o < 8; o <<= 1) {     // within the row's eight lanes
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
         // s = fp16_rn((max - min) / 7), saturated to the largest finite fp16
-        const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 7.0f);
-        uint16_t sbits = __half_as_ushort(__float2half_rn(s32));
+        uint16_t sbits = __half_as_ushort(__float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 7.0f)));
         if ((sbits & 0x7fff) == 0x7c00) sbits = 0x7bff;
         const float s = __half2float(__ushort_as_half(sbits));
         float z = 0.0f;
         if (s != 0.0f) z = fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.0f), 7.0f);
+        // fields: codes q_j at bits 3j (small integers, exact in fp32)
+        uint32_t f[NF];
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-            float q = 0.0f;
-            if (s != 0.0f) q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(x[j], s)), z), 0.0f), 7.0f);
-            codes[wid][EPL * lane + j] = uint8_t(q);
-        }
-        __syncwarp();
-        uint8_t *dst = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
-                                                   off * p.c_slot + h * p.c_head);
-        if (lane < D / 8) {            // one octet (8 codes -> 3 bytes) per lane
-            const uint8_t *v = &codes[wid][8 * lane];
-            uint32_t w24 = 0;
+        for (int fi = 0; fi < NF; ++fi) {
+            float fv = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w24 |= uint32_t(v[i] & 7) << (3 * i);
-            dst[3 * lane + 0] = uint8_t(w24);
-            dst[3 * lane + 1] = uint8_t(w24 >> 8);
-            dst[3 * lane + 2] = uint8_t(w24 >> 16);
+            for (int j = 7; j >= 0; --j) {
+                float q = 0.0f;
+                if (s != 0.0f) q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(x[8 * fi + j], s)), z), 0.0f), 7.0f);
+                fv = fmaf(fv, 8.0f, q);
+            }
+            f[fi] = uint32_t(fv);
         }
-        if (lane == 0) {
+        // the run's four fields, in order, gathered by its first lane
+        uint32_t F[4];
+#pragma unroll
+        for (int k = 0; k < LR; ++k)
+#pragma unroll
+            for (int fi = 0; fi < NF; ++fi) F[NF * k + fi] = __shfl_sync(0xffffffffu, f[fi], lane + k);
+        if (live && sub % LR == 0) {
+            const uint32_t w0 = F[0] | (F[1] << 24);
+            const uint32_t w1 = (F[1] >> 8) | (F[2] << 16);
+            const uint32_t w2 = (F[2] >> 16) | (F[3] << 8);
+            uint8_t *dst = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
+                                                       off * p.c_slot + h * p.c_head) + 12 * (sub / LR);
+            if ((reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+                uint32_t *d32 = reinterpret_cast<uint32_t *>(dst);
+                d32[0] = w0;
+                d32[1] = w1;
+                d32[2] = w2;
+            } else {                    // rows at strides that are not multiples of 4 bytes
+                const uint32_t run[3] = {w0, w1, w2};
+#pragma unroll
+                for (int b = 0; b < 12; ++b) dst[b] = uint8_t(run[b >> 2] >> (8 * (b & 3)));
+            }
+        }
+        if (live && sub == 0) {
             uint16_t *qs = kv ? p.v_qs : p.k_qs;
             uint8_t *qz = kv ? p.v_qz : p.k_qz;
             qs[blk * p.m_blk + off * p.m_slot + h * p.m_head] = sbits;
             qz[blk * p.z_blk + off * p.z_slot + h * p.z_head] = uint8_t(z);
         }
-        __syncwarp();
+        w.next();
     }
 }
 
@@ -462,14 +528,14 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
         return vec16 ? go_u(HF{}, std::true_type{}) : go_u(HF{}, std::false_type{});
     } else {  // kU3
         const int64_t rows = p.num_tokens * 2 * p.num_kv_heads;
-        const int g = grid_for(rows * 32, T);
+        const int g = grid_for(rows * 8, T);       // eight lanes per row
         const bool bf = p.src_kind == kBF16;
         if (p.head_dim == 128) {
-            if (bf) return launch_pdl(append_u3_kernel<kBF16, 4>, g, T, 0, s, p);
-            else return launch_pdl(append_u3_kernel<kF16, 4>, g, T, 0, s, p);
+            if (bf) return launch_pdl(append_u3_kernel<kBF16, 16>, g, T, 0, s, p);
+            else return launch_pdl(append_u3_kernel<kF16, 16>, g, T, 0, s, p);
         } else {
-            if (bf) return launch_pdl(append_u3_kernel<kBF16, 2>, g, T, 0, s, p);
-            else return launch_pdl(append_u3_kernel<kF16, 2>, g, T, 0, s, p);
+            if (bf) return launch_pdl(append_u3_kernel<kBF16, 8>, g, T, 0, s, p);
+            else return launch_pdl(append_u3_kernel<kF16, 8>, g, T, 0, s, p);
         }
     }
     return cudaGetLastError();

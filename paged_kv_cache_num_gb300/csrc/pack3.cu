@@ -11,6 +11,8 @@
 //
 // GB300 mapping: each thread handles 4 octets (32 value bytes <-> 12 packed
 // bytes) so both sides move with aligned 16-byte / 4-byte vector accesses;
+// the unpacking moves four codes at a time from their 3-bit to their byte
+// positions in two halving steps (spread4), a few ALU operations each;
 // the unpacking kernels exchange halves between lanes so that each store
 // instruction of a warp is one contiguous 512-byte run.  The kernels are
 // pure HBM streams.
@@ -46,6 +48,16 @@ int resident_blocks()
     return n;
 }
 
+// Four codes at bits 0-11 (code i at bit 3i) -> bytes 0-3, in two halving
+// steps instead of one shift and mask per code: codes 0-1 and 2-3 first
+// move apart as 6-bit pairs to bits 0-5 and 16-21, then each pair opens
+// out into its two bytes.  u < 2^12.
+__device__ __forceinline__ uint32_t spread4(uint32_t u)
+{
+    const uint32_t t = (u | (u << 10)) & 0x003F003Fu;
+    return (t | (t << 5)) & 0x07070707u;
+}
+
 __device__ __forceinline__ uint32_t pack_octet(uint32_t lo4, uint32_t hi4)
 {
     // lo4 / hi4 hold lanes 0-3 / 4-7 as bytes; keep 3 bits of each
@@ -58,15 +70,11 @@ __device__ __forceinline__ uint32_t pack_octet(uint32_t lo4, uint32_t hi4)
     return w;  // 24 significant bits
 }
 
+// w24 < 2^24
 __device__ __forceinline__ void unpack_octet(uint32_t w24, uint32_t &lo4, uint32_t &hi4)
 {
-    lo4 = 0;
-    hi4 = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        lo4 |= ((w24 >> (3 * i)) & 7u) << (8 * i);
-        hi4 |= ((w24 >> (3 * (i + 4))) & 7u) << (8 * i);
-    }
+    lo4 = spread4(w24 & 0xFFFu);
+    hi4 = spread4(w24 >> 12);
 }
 
 // 4 octets per thread: 32 value bytes (two 16-byte loads) -> 12 bytes.
@@ -102,6 +110,25 @@ __global__ void __launch_bounds__(kThreads) pack3_kernel(const uint8_t *__restri
     }
 }
 
+// 96 packed bits w0 | w1 << 32 | w2 << 64 as 32 value bytes: code i (bit
+// 3i) lies in 12-bit field i/4 at bit 3(i%4), and each field spreads into
+// 4 bytes.  Fields 2 and 5 span two words -- they hold codes 10 and 21, the
+// two codes whose high bits come from the next word -- and are cut with
+// funnel shifts.  Four octets (12 bytes, octet j = bits 24j..24j+23) and a
+// 96-bit group of three little-endian words are the same bits, so both
+// unpacking kernels use this.
+__device__ __forceinline__ void unpack96(uint32_t w0, uint32_t w1, uint32_t w2, uint4 &x, uint4 &y)
+{
+    x.x = spread4(w0 & 0xFFFu);
+    x.y = spread4((w0 >> 12) & 0xFFFu);
+    x.z = spread4(__funnelshift_r(w0, w1, 24) & 0xFFFu);
+    x.w = spread4((w1 >> 4) & 0xFFFu);
+    y.x = spread4((w1 >> 16) & 0xFFFu);
+    y.y = spread4(__funnelshift_r(w1, w2, 28) & 0xFFFu);
+    y.z = spread4((w2 >> 8) & 0xFFFu);
+    y.w = spread4(w2 >> 20);
+}
+
 // Quad (4 octets, 12 packed bytes) i of the input as 32 value bytes: x holds
 // octets 0-1, y octets 2-3 (zeros past the end).
 __device__ __forceinline__ void unpack_quad(const uint8_t *__restrict__ packed, int64_t i, int64_t n4, uint4 &x,
@@ -111,11 +138,7 @@ __device__ __forceinline__ void unpack_quad(const uint8_t *__restrict__ packed, 
     y = make_uint4(0, 0, 0, 0);
     if (i < n4) {
         const uint32_t *src = reinterpret_cast<const uint32_t *>(packed + 12 * i);
-        const uint32_t a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
-        unpack_octet(a & 0xffffffu, x.x, x.y);
-        unpack_octet((a >> 24) | ((b & 0xffffu) << 8), x.z, x.w);
-        unpack_octet((b >> 16) | ((c & 0xffu) << 16), y.x, y.y);
-        unpack_octet(c >> 8, y.z, y.w);
+        unpack96(__ldg(src), __ldg(src + 1), __ldg(src + 2), x, y);
     }
 }
 
@@ -173,29 +196,14 @@ __global__ void __launch_bounds__(kThreads) unpack3_kernel(const uint8_t *__rest
     }
 }
 
-// 96-bit group g as 32 value bytes: lane i = (W[w] >> s | W[w+1] << (32-s))
-// & 7 with w = 3i/32, s = 3i%32, the second term only for s > 29 (zeros past
-// the end).
+// 96-bit group g as 32 value bytes, lane i = bits 3i..3i+2 of the group
+// (zeros past the end).
 __device__ __forceinline__ void unpack_group(const uint32_t *__restrict__ words, int64_t g, int64_t m, uint4 &x,
                                              uint4 &y)
 {
-    uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (g < m) {
-        uint32_t W[3];
-        W[0] = __ldg(words + 3 * g);
-        W[1] = __ldg(words + 3 * g + 1);
-        W[2] = __ldg(words + 3 * g + 2);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int w = (3 * i) >> 5, s = (3 * i) & 31;
-            uint32_t v = W[w] >> s;
-            if (s > 29) v |= W[w + 1] << (32 - s);   // compile-time lanes 10, 21
-            v &= 7u;
-            if ((i & 3) == 0) out[i >> 2] = v; else out[i >> 2] |= v << (8 * (i & 3));
-        }
-    }
-    x = make_uint4(out[0], out[1], out[2], out[3]);
-    y = make_uint4(out[4], out[5], out[6], out[7]);
+    x = make_uint4(0, 0, 0, 0);
+    y = make_uint4(0, 0, 0, 0);
+    if (g < m) unpack96(__ldg(words + 3 * g), __ldg(words + 3 * g + 1), __ldg(words + 3 * g + 2), x, y);
 }
 
 // One 96-bit group per lane, chunks of 32 consecutive groups (a kilobyte of

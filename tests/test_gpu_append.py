@@ -207,3 +207,43 @@ def test_u3_append_bit_exact(pkv, orc, D, src):
     orc.kv_append(4, code, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
                   None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
     _assert_pools_equal(PL.gpu_cache_host(cache), c)
+
+
+@pytest.mark.parametrize("src", [torch.float16, torch.bfloat16])
+def test_u3_append_ties_zeros_extremes(pkv, orc, src):
+    """3-bit rows whose quotients x / scale are exact half-integers (ties,
+    rounded to even), rows of zeros with a few nonzero values, rows whose
+    range overflows fp32 or fp16, and rows of tiny values: the kernel's
+    division shortcut must fall back to the division wherever it could
+    change a code, so the pool stays bit-exact with the oracle."""
+    H, D, BS, P = 2, 128, 16, 16
+    g = torch.Generator().manual_seed(278)
+    big = 60000.0 if src == torch.float16 else 3.0e38
+    rows = []
+    ramp = torch.arange(-7, 8, dtype=torch.float32) * 0.125           # x / 0.25 = k / 2
+    rows.append(ramp.repeat(D // 15 + 1)[:D])
+    rows.append(torch.cat([ramp, ramp.flip(0)]).repeat(D // 30 + 1)[:D] * 4.0)
+    z = torch.zeros(D)
+    z[[3, 50]] = torch.tensor([0.75, -1.5])
+    rows.append(z)
+    e = torch.randn(D, generator=g)
+    e[[0, 1]] = torch.tensor([big, -big])
+    rows.append(e)
+    rows.append(torch.randn(D, generator=g) * 1e-6)
+    rows.append(torch.randn(D, generator=g) * 2.0 ** -30)
+    R = torch.stack(rows)                                              # [6, D]
+    T = 48
+    kn = R[torch.arange(T * H) % R.shape[0]].reshape(T, H, D).to(src)
+    vn = R[(torch.arange(T * H) + 3) % R.shape[0]].reshape(T, H, D).neg().to(src)
+    slots = torch.randperm(P * BS, generator=g)[:T]
+    cache = pkv.KVCache.allocate("u3", P, BS, H, D, fill=0)
+    pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache)
+    torch.cuda.synchronize()
+    RB = 3 * D // 8
+    c = {"k_cache": np.zeros((P, BS, H, RB), np.uint8), "v_cache": np.zeros((P, BS, H, RB), np.uint8),
+         "k_qscale": np.zeros((P, BS, H), np.uint16), "v_qscale": np.zeros((P, BS, H), np.uint16),
+         "k_qzero": np.zeros((P, BS, H), np.uint8), "v_qzero": np.zeros((P, BS, H), np.uint8)}
+    code = 1 if src == torch.float16 else 2
+    orc.kv_append(4, code, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
+                  None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
+    _assert_pools_equal(PL.gpu_cache_host(cache), c)
