@@ -89,18 +89,21 @@ __device__ __forceinline__ bool resolve_slot(const AppendParams &p, int64_t t, i
 }
 
 // A grid-stride walk over items i = major * n + minor (0 <= minor < n)
-// that keeps (major, minor) current by additions: one 64-bit division per
+// that keeps (major, minor) current by additions: two 32-bit divisions per
 // warp at the start, none per item (a 64-bit division by a runtime value
-// costs about a hundred instructions).
+// costs about a hundred instructions).  The first item and the stride are
+// warp counts of grids capped at a few thousand blocks, far below 2^32.
 struct Walk2 {
     int64_t major, step_major;
     int minor, step_minor, n;
     __device__ __forceinline__ Walk2(int64_t first, int64_t step, int n_) : n(n_)
     {
-        major = first / n;
-        minor = int(first - major * n);
-        step_major = step / n;
-        step_minor = int(step - step_major * n);
+        const uint32_t f = uint32_t(first), s = uint32_t(step), un = uint32_t(n_);
+        const uint32_t fq = f / un, sq = s / un;
+        major = fq;
+        minor = int(f - fq * un);
+        step_major = sq;
+        step_minor = int(s - sq * un);
     }
     __device__ __forceinline__ void next()
     {

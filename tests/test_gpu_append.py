@@ -247,3 +247,49 @@ def test_u3_append_ties_zeros_extremes(pkv, orc, src):
     orc.kv_append(4, code, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
                   None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
     _assert_pools_equal(PL.gpu_cache_host(cache), c)
+
+
+def test_u3_append_unaligned_rows_and_sources(pkv, orc):
+    """3-bit rows at a head stride of 49 bytes (rows start at any byte: the
+    kernel stores their 12-byte runs byte by byte) from sources that start
+    one element past a 16-byte boundary (scalar loads): the same codes and
+    metadata as the oracle, and the padding byte after each row untouched."""
+    H, D, BS, P, T = 3, 128, 16, 12, 100
+    RB = 3 * D // 8
+    g = torch.Generator().manual_seed(279)
+    kn = torch.randn((T, H, D), generator=g).to(torch.float16)
+    vn = (torch.randn((T, H, D), generator=g) * 7).to(torch.float16)
+    slots = torch.randperm(P * BS, generator=g)[:T]
+    dev = "cuda"
+    kbuf = torch.empty(T * H * D + 1, dtype=torch.float16, device=dev)
+    vbuf = torch.empty_like(kbuf)
+    ksrc, vsrc = kbuf[1:].view(T, H, D), vbuf[1:].view(T, H, D)
+    ksrc.copy_(kn.to(dev))
+    vsrc.copy_(vn.to(dev))
+    ref = pkv.KVCache.allocate("u3", P, BS, H, D, fill=0)
+    wide_k = torch.full((P, BS, H, RB + 1), 0xA5, dtype=torch.uint8, device=dev)
+    wide_v = torch.full_like(wide_k, 0x5A)
+    cache = pkv.KVCache("u3", wide_k[..., :RB], wide_v[..., :RB], k_qscale=ref.k_qscale.clone(),
+                        k_qzero=ref.k_qzero.clone(), v_qscale=ref.v_qscale.clone(),
+                        v_qzero=ref.v_qzero.clone())
+    assert cache.k_cache.stride(2) == RB + 1
+    pkv.kv_append(ksrc, vsrc, slots.to(dev), cache)
+    torch.cuda.synchronize()
+    c = {"k_cache": np.zeros((P, BS, H, RB), np.uint8), "v_cache": np.zeros((P, BS, H, RB), np.uint8),
+         "k_qscale": np.zeros((P, BS, H), np.uint16), "v_qscale": np.zeros((P, BS, H), np.uint16),
+         "k_qzero": np.zeros((P, BS, H), np.uint8), "v_qzero": np.zeros((P, BS, H), np.uint8)}
+    orc.kv_append(4, 1, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
+                  None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
+    written = np.zeros((P * BS,), bool)
+    written[slots.numpy()] = True
+    written = written.reshape(P, BS)
+    got = PL.gpu_cache_host(cache)
+    for name in ("k_cache", "v_cache"):
+        fill = 0xA5 if name == "k_cache" else 0x5A
+        exp = np.where(written[:, :, None, None], c[name], np.uint8(fill))
+        assert np.array_equal(got[name], exp), name
+    for name in ("k_qscale", "v_qscale", "k_qzero", "v_qzero"):
+        assert np.array_equal(got[name], c[name]), name
+    pad_k = wide_k[..., RB].cpu().numpy()
+    pad_v = wide_v[..., RB].cpu().numpy()
+    assert (pad_k == 0xA5).all() and (pad_v == 0x5A).all()
