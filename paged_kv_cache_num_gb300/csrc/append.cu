@@ -15,9 +15,13 @@
 // slot lookup per warp, 32-bit index arithmetic, four 16-byte loads in
 // flight per lane, fully coalesced loads and stores); the grid is a
 // function of num_tokens only (CUDA-graph safe).  The 3-bit kernel gives
-// each warp one row: the min / max are warp-shuffle reductions and the
-// packing goes through shared memory.  All are programmatic dependent launches, so the launch of each
-// overlaps the tail of the previous kernel in the stream.
+// each row eight lanes (four rows per warp): the min / max are shuffle
+// reductions among them and the packed 12-byte runs are assembled by
+// shuffles.  Work items are walked by additions, without a 64-bit division
+// per item.  Large batches with contiguous head rows move by TMA bulk
+// copies instead (append_bulk_kernel).  All are programmatic dependent
+// launches, so the launch of each overlaps the tail of the previous kernel
+// in the stream.
 #include <algorithm>
 #include <type_traits>
 
