@@ -130,7 +130,10 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // staged fp8 / int8 granular scales: K and V runs of nh * q8_scales_per_head
     // fp32, each a multiple of 16 bytes for the bulk copies
     if (q8_scales_per_head > 0 && (4 * nh * q8_scales_per_head) % 16 != 0) return false;
-    const int meta = u3 ? 6 * block_size * meta_heads : 8 * nh * q8_scales_per_head;
+    // 3-bit: the staged scale / zero runs plus room for their fp32
+    // conversion (16 bytes per (head, slot)); fp8 / int8: the staged
+    // granular scales
+    const int meta = u3 ? 6 * block_size * meta_heads + 16 * nh * block_size : 8 * nh * q8_scales_per_head;
     while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 / ctas_per_sm ||
                           smem_layout(nh, block_size, row, stages, batch, meta).total > budget))
         --stages;

@@ -64,7 +64,8 @@ struct SmemLayout {
     int tile_bytes, meta_bytes, stage_bytes, bars_off, ok_off, prefix_off, nblk_off, total;
 };
 
-// [stages x (K tile, V tile, 3-bit metadata of the whole block)]
+// [stages x (K tile, V tile, 3-bit metadata of the whole block + its fp32
+// conversion)]
 // [mbarriers] [per-stage block ids] [prefix sums] [block counts]
 __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
                                                   int batch, int meta_bytes = 0)
@@ -265,7 +266,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // the CTA's heads for the block, [nh] or [nh][BS] fp32 each.
     const int GS = p.scale_mode == 2 ? BS : 1;        // staged scales per head
     constexpr bool gscale = T::kFp8 && GSC;
-    const int meta_bytes = T::kIsU3 ? 6 * BS * f.meta_heads : (gscale ? 8 * nh * GS : 0);
+    // 3-bit: the raw metadata as staged (copied), then room for its fp32
+    // conversion (sk, zk, sv, zv per (head, slot), written by the consumers)
+    const int raw_meta = T::kIsU3 ? 6 * BS * f.meta_heads : (gscale ? 8 * nh * GS : 0);
+    const int meta_bytes = raw_meta + (T::kIsU3 ? 16 * nh * BS : 0);
     const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
@@ -372,7 +376,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         const uint32_t vdst = kdst + L.tile_bytes;
                         stage_pb[s] = pbk;
                         if (pbk >= 0) {
-                            ptx::mbar_arrive_expect_tx(fb, uint32_t(2 * L.tile_bytes + L.meta_bytes));
+                            ptx::mbar_arrive_expect_tx(fb, uint32_t(2 * L.tile_bytes + raw_meta));
                             if constexpr (XV) {
                                 if (f.xv_bulk) {   // the heads' tiles: one run each of K and V
                                     const int64_t off = int64_t(pbk) * p.c_blk + int64_t(hgk) * nh * p.c_head;
@@ -695,27 +699,41 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         auto kpk = [&](int t) {                  // packed K rows of the tile (shared address)
             return sbase + tile_stage(t) * L.stage_bytes + kvl * BS * T::ROW + tile_row(t) * T::ROW;
         };
-        // ---- metadata of this lane's score rows (tokens gid, gid+8 of
-        // each tile), staged with the block: [nh][BS] runs (head-major)
-        // or [BS][num_kv_heads] arrays
+        // ---- metadata: lane l converts token l of the NB blocks (this
+        // warp's head) to fp32 (sk, zk, sv, zv) in the stage's conversion
+        // area -- one token per lane instead of four 16- / 8-bit loads and
+        // conversions per score row in every lane -- and each lane then reads
+        // its score rows (tokens gid, gid+8 of each tile) with one 16-byte
+        // load each.  Staged as [nh][BS] runs (head-major) or [BS][num_kv_heads]
+        // arrays.
         const int MH = f.meta_heads;
         const bool hmaj = MH == nh;
-        const int m_tok = hmaj ? 1 : MH, m_h = hmaj ? kvl * BS : kvh;
+        auto conv_area = [&](int st) {
+            return reinterpret_cast<float4 *>(smem + (st * L.stage_bytes + 2 * L.tile_bytes + raw_meta));
+        };
+        if (lane < NB * BS) {
+            const int st = lane < BS ? s0 : s1, slot = lane & (BS - 1);
+            const unsigned char *raw = smem + (st * L.stage_bytes + 2 * L.tile_bytes);
+            const __half *mks = reinterpret_cast<const __half *>(raw);
+            const __half *mvs = mks + BS * MH;
+            const uint8_t *mkz = raw + 4 * BS * MH;
+            const uint8_t *mvz = mkz + BS * MH;
+            const int i = hmaj ? kvl * BS + slot : slot * MH + kvh;
+            conv_area(st)[kvl * BS + slot] =
+                make_float4(__half2float(mks[i]), float(mkz[i]), __half2float(mvs[i]), float(mvz[i]));
+        }
+        __syncwarp();
         float sk[KTT][2], zk[KTT][2], sv[KTT][2], zv[KTT][2];
 #pragma unroll
         for (int mt = 0; mt < KTT; ++mt) {
-            const unsigned char *meta = smem + (tile_stage(mt) * L.stage_bytes + 2 * L.tile_bytes);
-            const __half *mks = reinterpret_cast<const __half *>(meta);
-            const __half *mvs = mks + BS * MH;
-            const uint8_t *mkz = meta + 4 * BS * MH;
-            const uint8_t *mvz = mkz + BS * MH;
+            const float4 *cv = conv_area(tile_stage(mt));
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int e = (tile_row(mt) + gid + 8 * r) * m_tok + m_h;
-                sk[mt][r] = __half2float(mks[e]);
-                sv[mt][r] = __half2float(mvs[e]);
-                zk[mt][r] = float(mkz[e]);
-                zv[mt][r] = float(mvz[e]);
+                const float4 m4 = cv[kvl * BS + tile_row(mt) + gid + 8 * r];
+                sk[mt][r] = m4.x;
+                zk[mt][r] = m4.y;
+                sv[mt][r] = m4.z;
+                zv[mt][r] = m4.w;
             }
         }
         // ---- S^T = K Q'^T with K converted straight into A fragments:
