@@ -293,3 +293,50 @@ def test_u3_append_unaligned_rows_and_sources(pkv, orc):
     pad_k = wide_k[..., RB].cpu().numpy()
     pad_v = wide_v[..., RB].cpu().numpy()
     assert (pad_k == 0xA5).all() and (pad_v == 0x5A).all()
+
+
+@pytest.mark.parametrize("kind,H", [("bf16", 16), ("e4m3", 16), ("u3", 4)])
+def test_append_many_items_several_passes(pkv, orc, kind, H):
+    """Batches large enough that every warp of the grid walks several work
+    items, with more than one part (or row) per token: a strided 16-bit
+    source (the warp kernel, not the bulk path), 16 kv heads for e4m3 (two
+    parts per token row), 4 heads for 3-bit (four rows per warp spanning
+    tokens). The whole pool stays bit-exact with the oracle, padding and
+    skipped slots included."""
+    D, BS = 128, 16
+    T = 12000
+    P = (T + 600) // BS + 1
+    g = torch.Generator().manual_seed(280 + H)
+    src_dt = torch.bfloat16
+    # [T, H, 3, D]: K and V heads interleaved with a third row, so a token's
+    # heads are not one contiguous run and the 16-bit append takes the warp
+    # kernel rather than the bulk copies
+    fused = torch.randn((T, H, 3, D), generator=g).to(src_dt)
+    kn, vn = fused[:, :, 1], fused[:, :, 2]
+    slots = torch.randperm(P * BS, generator=g)[:T]
+    slots[::97] = -1                                               # padding tokens
+    dev = "cuda"
+    if kind == "e4m3":
+        ks = (torch.rand(H, generator=g) * 0.02 + 0.005).float()
+        vs = (torch.rand(H, generator=g) * 0.02 + 0.005).float()
+        cache = pkv.KVCache.allocate(kind, P, BS, H, D, k_scale=ks.to(dev), v_scale=vs.to(dev), fill=0)
+    else:
+        ks = vs = None
+        cache = pkv.KVCache.allocate(kind, P, BS, H, D, fill=0)
+    fd = fused.to(dev)
+    pkv.kv_append(fd[:, :, 1], fd[:, :, 2], slots.to(dev), cache)
+    torch.cuda.synchronize()
+    if kind == "u3":
+        RB = 3 * D // 8
+        c = {"k_cache": np.zeros((P, BS, H, RB), np.uint8), "v_cache": np.zeros((P, BS, H, RB), np.uint8),
+             "k_qscale": np.zeros((P, BS, H), np.uint16), "v_qscale": np.zeros((P, BS, H), np.uint16),
+             "k_qzero": np.zeros((P, BS, H), np.uint8), "v_qzero": np.zeros((P, BS, H), np.uint8)}
+        orc.kv_append(4, 2, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
+                      None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
+    else:
+        dt = np.uint16 if kind == "bf16" else np.uint8
+        c = {"k_cache": np.zeros((P, BS, H, D), dt), "v_cache": np.zeros((P, BS, H, D), dt)}
+        orc.kv_append(PL.KIND_CODE_ORACLE[kind], 2, W.bits16(kn), W.bits16(vn), slots.numpy(),
+                      c["k_cache"], c["v_cache"], None if ks is None else ks.numpy(),
+                      None if vs is None else vs.numpy())
+    _assert_pools_equal(PL.gpu_cache_host(cache), c)
