@@ -118,10 +118,13 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float &rlo, flo
 }
 
 // Two one-byte codes of cache kind CK, bytes 2HI and 2HI+1 of w (low byte
-// first) -> an f16x2 register, exactly: fp8 through cvt.rn.f16x2 on the
-// 16-bit half of the register (no shift); int8 c as 1152 + c (a byte
-// permute puts c next to the exponent of 1024 and an XOR of the byte's top
-// bit adds 128), the 1152 offset being removed in fp32 after the MMA.
+// first) -> an f16x2 register, exactly: e4m3 through cvt.rn.f16x2 on the
+// 16-bit half of the register (no shift); e5m2 by a byte permute alone (an
+// e5m2 code -- sign, 5 exponent bits with the f16 bias, 2 mantissa bits --
+// is the high byte of the f16 of the same value, subnormals, infinities and
+// NaN included); int8 c as 1152 + c (a byte permute puts c next to the
+// exponent of 1024 and an XOR of the byte's top bit adds 128), the 1152
+// offset being removed in fp32 after the MMA.
 template <int CK, int HI>
 __device__ __forceinline__ uint32_t f16x2_from_q8(uint32_t w)
 {
@@ -134,10 +137,7 @@ __device__ __forceinline__ uint32_t f16x2_from_q8(uint32_t w)
         else
             asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, l;\n}" : "=r"(r) : "r"(w));
     } else {
-        if constexpr (HI)
-            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e5m2x2 %0, h;\n}" : "=r"(r) : "r"(w));
-        else
-            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e5m2x2 %0, l;\n}" : "=r"(r) : "r"(w));
+        r = ptx::prmt(w, 0u, HI ? 0x3424u : 0x1404u);   // codes to the high bytes, zero low bytes
     }
     return r;
 }
