@@ -72,3 +72,26 @@ def u3_dequant(packed: np.ndarray, qscale_bits: np.ndarray, qzero: np.ndarray, D
     s = np.ascontiguousarray(qscale_bits).view(np.float16).astype(np.float64).reshape(-1, 1)
     z = qzero.astype(np.float64).reshape(-1, 1)
     return ((q - z) * s).reshape(*lead, D)
+
+
+def load_u3_ties(path=None):
+    """Rows of tests/golden/u3_ties.txt -> list of (name, s_bits, z, x [16]
+    fp16, q [16] uint8)."""
+    import os
+    if path is None:
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "u3_ties.txt")
+    rows = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, meta, xs, qs = (p.strip() for p in line.split("|"))
+            s_hex, z = meta.split()
+            x = np.array([float(v) for v in xs.split()], dtype=np.float64)
+            x16 = x.astype(np.float16)
+            assert np.array_equal(x16.astype(np.float64), x), name   # every x exact in fp16
+            q = np.array([int(v) for v in qs.split()], dtype=np.uint8)
+            assert x.shape == q.shape, name
+            rows.append((name, int(s_hex, 16), int(z), x16, q))
+    return rows

@@ -249,6 +249,43 @@ def test_u3_append_ties_zeros_extremes(pkv, orc, src):
     _assert_pools_equal(PL.gpu_cache_host(cache), c)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_u3_append_hand_worked_ties(pkv, D):
+    """The hand-worked rows of tests/golden/u3_ties.txt (tie quotients in the
+    zero point and the codes, fp16 scale ties both ways, clamped codes,
+    constant rows), tiled along head_dim, appended by the GPU: its scale
+    bits, zero points and unpacked codes equal the hand-worked values
+    directly, with no oracle in between."""
+    from tests.refs import bitstream_unpack3, load_u3_ties
+    rows = load_u3_ties()
+    R = np.stack([np.tile(r[3], D // 16) for r in rows])              # [n, D] fp16
+    H, BS = 2, 16
+    n = R.shape[0]
+    T = n                                                              # token t: K row t, V row n-1-t
+    P = (T + BS - 1) // BS + 1
+    kn = torch.from_numpy(R.astype(np.float32)).reshape(T, 1, D).expand(T, H, D).to(torch.float16)
+    vn = torch.from_numpy(R[::-1].astype(np.float32).copy()).reshape(T, 1, D).expand(T, H, D).to(torch.float16)
+    slots = torch.arange(T, dtype=torch.int64) + BS                    # skip block 0
+    cache = pkv.KVCache.allocate("u3", P, BS, H, D, fill=0)
+    pkv.kv_append(kn.contiguous().cuda(), vn.contiguous().cuda(), slots.cuda(), cache)
+    torch.cuda.synchronize()
+    got = PL.gpu_cache_host(cache)
+    RB = 3 * D // 8
+    for part, order in (("k", range(n)), ("v", range(n - 1, -1, -1))):
+        packed = got[part + "_cache"].reshape(P * BS, H, RB)
+        sc = got[part + "_qscale"].reshape(P * BS, H)
+        zr = got[part + "_qzero"].reshape(P * BS, H)
+        for t, ri in enumerate(order):
+            name, s_exp, z_exp, _, q_exp = rows[ri]
+            for h in range(H):
+                slot = BS + t
+                assert int(sc[slot, h]) == s_exp, (part, name, h)
+                assert int(zr[slot, h]) == z_exp, (part, name, h)
+                q = bitstream_unpack3(packed[slot, h][None, :], D)[0]
+                assert np.array_equal(q, np.tile(q_exp, D // 16)), (part, name, h)
+    assert not got["k_cache"][0].any() and not got["v_cache"][0].any()  # block 0 untouched
+
+
 def test_u3_append_unaligned_rows_and_sources(pkv, orc):
     """3-bit rows at a head stride of 49 bytes (rows start at any byte: the
     kernel stores their 12-byte runs byte by byte) from sources that start

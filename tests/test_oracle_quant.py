@@ -105,3 +105,24 @@ def test_bf16_source(orc):
     q = bitstream_unpack3(packed, 128)
     deq = (q - z[:, None].astype(np.int64)) * s.view(np.float16).astype(np.float64)[:, None]
     assert np.all(np.abs(deq - xh) <= 1.5 * s.view(np.float16).astype(np.float64)[:, None])
+
+
+def test_hand_worked_ties(orc):
+    """Hand-worked rows (tests/golden/u3_ties.txt) whose quotients -min/s and
+    x/s are exact half-integers, whose fp16 scale rounding meets a tie in
+    both directions, and whose codes and zero points clamp: the oracle's
+    scale bits, zero point and every code equal the hand-worked values.
+    A quantiser that rounds ties away from zero, up, or toward zero fails
+    here.  Each row is also tiled to D = 64 and D = 128 (min, max and so
+    scale and zero unchanged; codes tiled)."""
+    from tests.refs import load_u3_ties
+    rows = load_u3_ties()
+    assert len(rows) >= 10
+    for D in (16, 64, 128):
+        x = np.stack([np.tile(r[3], D // 16) for r in rows])
+        q, _, z = _quant(orc, x)
+        s_bits = orc.u3_quantize_pack(x.view(np.uint16), orc.F16)[1]
+        for i, (name, s_exp, z_exp, _, q_exp) in enumerate(rows):
+            assert int(s_bits[i]) == s_exp, (name, D, hex(int(s_bits[i])))
+            assert int(z[i]) == z_exp, (name, D)
+            assert np.array_equal(q[i], np.tile(q_exp, D // 16)), (name, D, q[i][:16])
