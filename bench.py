@@ -2,11 +2,19 @@
 
 One step = one pass of the path over one batch: build the slot mapping of
 the step's new tokens, append them to the paged cache (kv_append), then run
-paged_decode over every sequence.  The default workload is the GQA bf16
-decode step (batch 64, 32 q / 8 kv heads, head_dim 128, block 16, contexts
-U{512..4096}); the long-context fp8, 3-bit MHA and mixed prefill+decode
-append workloads are measured in the same run and reported under
-"workloads".
+paged_decode over every sequence.  The default workload is the
+long-context fp8 decode step (batch 16, 64 q / 8 kv heads, head_dim 128,
+block 32, contexts U{16384..32768}, e4m3 cache with per-kv-head scales, bf16
+q); the GQA bf16, 3-bit MHA, mixed prefill+decode append and the other
+workloads are measured in the same run and reported under "workloads", each
+with its own roofline block.
+
+Every decode workload's timed step is checked: after the timed replays the
+step graph runs once more, its output and the cache it leaves are copied to
+the host, and the oracle (the CPU-baseline leg) re-applies the step's append
+to a copy of that cache (bit-exact: nothing may change) and decodes every
+(sequence, head) over it; the largest absolute error against the stated
+tolerance is reported under "parity".
 
 value = algorithmic bytes of the step / device time of the step (GB/s), with
 the inputs resident in HBM and L2 flushed between steps (a 256 MiB write
@@ -23,6 +31,7 @@ the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -420,6 +429,121 @@ def time_steps(step, steps, warmup, flush, parts=True):
     return tot, app, dec
 
 
+# ---------------------------------------------------------------- configs
+
+def workload_config(w, name, ws):
+    """The workload a bench line measures (both arms print this)."""
+    return {"workload": name, "batch": w.batch, "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "context": w.extra.get("context"),
+            "cache_dtype": w.cache_kind, "q_dtype": str(w.dtype).replace("torch.", ""),
+            "scale_mode": w.scale_mode, "layout": w.layout,
+            "new_tokens": int((w.new_pos >= 0).sum()),
+            "parallelism": "replicas" if ws > 1 else "single"}
+
+
+def decode_roofline(name, dec_bytes, dec_ms, peak, peak_src):
+    gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = profile_traffic("paged_decode:" + name, source_hash(*DECODE_SOURCES))
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "traffic": traffic,
+            "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
+            "measured" else "fallback 6.8 TB/s",
+            "kernel": "paged_decode (decode kernel + split-K merge, one C-ABI call)",
+            "algorithmic_bytes_per_launch": dec_bytes}
+
+
+# ---------------------------------------------------------------- timed-output check
+
+def cache_host_logical(cache, layout):
+    """Host copies of the cache arrays in the logical [P, BS, Hkv, ...] order
+    (x-vectorised storage rearranged back), as numpy bit patterns."""
+    d = {}
+    for name in ("k_cache", "v_cache", "k_qscale", "k_qzero", "v_qscale", "v_qzero", "k_scales",
+                 "v_scales"):
+        t = getattr(cache, name)
+        if t is None:
+            continue
+        if name in ("k_cache", "v_cache") and layout == "xvec":
+            P, H, Dx, BS, x = t.shape
+            t = t.permute(0, 3, 1, 2, 4).reshape(P, BS, H, Dx * x)
+        t = t.cpu().contiguous()
+        if t.element_size() == 2:
+            d[name] = t.view(torch.int16).numpy().view(np.uint16)
+        elif t.dtype in (torch.int8, torch.float32):
+            d[name] = t.numpy()
+        else:
+            d[name] = t.view(torch.uint8).numpy()
+    return d
+
+
+def snapshot_timed_step(st):
+    """Replay the timed step graph once more (out poisoned with NaN first)
+    and copy its inputs, its output and the cache it leaves to the host.
+    Uses no oracle."""
+    w = st.w
+    st.out.fill_(float("nan"))
+    st.replay_step()
+    torch.cuda.synchronize()
+    assert int(st.err.item()) == 0, "device error flag %d" % int(st.err.item())
+
+    def h(t):
+        return None if t is None else t.cpu()
+    hw = dataclasses.replace(
+        w, context_lens=h(w.context_lens), block_tables=h(w.block_tables), q=h(w.q),
+        new_req=h(w.new_req), new_pos=h(w.new_pos), k_new=h(w.k_new), v_new=h(w.v_new),
+        k_scale=h(w.k_scale), v_scale=h(w.v_scale), k_block_scale=h(w.k_block_scale),
+        v_block_scale=h(w.v_block_scale), k_new_scale=h(w.k_new_scale),
+        v_new_scale=h(w.v_new_scale), k_cache0=None, v_cache0=None, fill_req=None,
+        fill_pos=None, k_fill=None, v_fill=None, k_fill_scale=None, v_fill_scale=None)
+    return hw, cache_host_logical(st.cache, w.layout), st.out.cpu()
+
+
+def check_timed_step(snap, orc, nthreads=None, seqs=None):
+    """The oracle leg's check of a timed step (snapshot_timed_step):
+    the oracle re-applies the step's append (its own slot mapping and
+    quantisation) to a copy of the GPU's cache, which must leave every byte
+    unchanged, and decodes every (sequence, head) over the GPU's cache; the
+    largest absolute error of the GPU's output against it is compared with
+    the stated tolerance (4e-3 fp16 outputs, 2e-2 bf16)."""
+    from tests import pipeline as PL
+    hw, c, out = snap
+    t0 = time.perf_counter()
+    c2 = {k: v.copy() for k, v in c.items()}
+    mode = {"head": orc.SCALE_PER_HEAD, "block": orc.SCALE_PER_BLOCK,
+            "token": orc.SCALE_PER_TOKEN}[hw.scale_mode]
+    req, pos = hw.new_req.numpy(), hw.new_pos.numpy()
+    slots = orc.build_slot_mapping(hw.block_tables.numpy(), req, pos, hw.block_size)
+    bad = orc.kv_append(PL.KIND_CODE_ORACLE[hw.cache_kind], PL.src_code(hw), W.bits16(hw.k_new),
+                        W.bits16(hw.v_new), slots, c2["k_cache"], c2["v_cache"],
+                        None if hw.k_scale is None else hw.k_scale.numpy(),
+                        None if hw.v_scale is None else hw.v_scale.numpy(), c2.get("k_qscale"),
+                        c2.get("k_qzero"), c2.get("v_qscale"), c2.get("v_qzero"),
+                        scale_mode=mode,
+                        k_new_scale=None if hw.k_new_scale is None else hw.k_new_scale.numpy(),
+                        v_new_scale=None if hw.v_new_scale is None else hw.v_new_scale.numpy(),
+                        k_scales=c2.get("k_scales"), v_scales=c2.get("v_scales"))
+    append_exact = bad == 0 and all(np.array_equal(c[k], c2[k]) for k in c)
+    del c2
+    Hq = hw.num_heads
+    if seqs is None:
+        seqs = list(range(hw.batch))
+    pairs = np.concatenate([np.arange(b * Hq, (b + 1) * Hq) for b in seqs]).astype(np.int32)
+    ref = PL.oracle_decode(hw, orc, c, pairs=pairs, nthreads=nthreads)[seqs]
+    got = out.to(torch.float64).numpy()[seqs]
+    finite = bool(np.isfinite(got).all())
+    max_abs = float(np.abs(got - ref).max()) if finite else float("inf")
+    tol = PL.tolerance(hw)
+    return {"rows": int(got.shape[0] * got.shape[1]), "of_rows": hw.batch * Hq,
+            "max_abs": max_abs, "tolerance": tol,
+            "ok": bool(finite and max_abs <= tol and append_exact),
+            "append_bit_exact": bool(append_exact), "oracle_s": round(time.perf_counter() - t0, 2),
+            "what": "%s of the timed step's output vs the fp64 oracle over the cache the "
+                    "step left; the step's appended rows re-applied by the oracle change no "
+                    "byte" % ("every (sequence, head)" if len(seqs) == hw.batch else
+                             "every head of sequences %s" % seqs)}
+
+
 # ---------------------------------------------------------------- oracle arms
 
 class OracleArm:
@@ -525,7 +649,8 @@ def run_reference(args, ws, rank):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "device": "host cores"},
+            "config": workload_config(w, args.workload, ws),
+            "device": "host cores",
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -543,8 +668,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gqa_bf16")
-    ap.add_argument("--extra", default="fp8_long,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long,"
+    ap.add_argument("--workload", default="fp8_long")
+    ap.add_argument("--extra", default="gqa_bf16,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long,"
                                        "fp8_long_token_scales,fp8_long_block_scales,gqa_bf16_xvec,"
                                        "fp8_long_xvec,fp8_long_g16,gqa_bf16_g16",
                     help="other workloads measured in the same run ('' for none)")
@@ -601,6 +726,8 @@ def main():
     dec_ms = float(np.mean(dec))
     app_ms = float(np.mean(app))
     assert int(st.err.item()) == 0, "device error flag %d" % int(st.err.item())
+    check_oracle = rank == 0 and not args.no_cpu_baseline
+    snap = snapshot_timed_step(st) if check_oracle and w.q is not None else None
 
     # ---------------- e2e through the public API with host buffers
     # the step's inputs packed into one pinned host buffer (256-byte aligned
@@ -663,14 +790,7 @@ def main():
 
     # ---------------- roofline of the dominant operation (paged_decode)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
-    src = source_hash(*DECODE_SOURCES)
-    traffic = profile_traffic("paged_decode:" + args.workload, src)
-    roofline = {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
-                "measured" else "fallback 6.8 TB/s",
-                "kernel": "paged_decode (decode kernel + split-K merge, one C-ABI call)",
-                "algorithmic_bytes_per_launch": dec_bytes}
+    roofline = decode_roofline(args.workload, dec_bytes, dec_ms, peak, peak_src)
 
     # copy-kernel yardstick (1 GiB each way)
     a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -707,7 +827,15 @@ def main():
             g = db / (float(np.mean(dd)) * 1e-3) / 1e9
             e.update({"decode_ms": round(float(np.mean(dd)), 4), "decode_gbs": round(g, 1),
                       "decode_frac_of_peak": round(g / peak, 4),
-                      "decode_algorithmic_bytes": db})
+                      "decode_algorithmic_bytes": db,
+                      "roofline": decode_roofline(name, db, float(np.mean(dd)), peak, peak_src)})
+            if check_oracle:
+                import oracle as orc
+                orc.build()
+                # the first and the last sequence, all heads (the headline
+                # workload's check covers every sequence)
+                e["parity"] = check_timed_step(snapshot_timed_step(sx), orc,
+                                               seqs=sorted({0, wx.batch - 1}))
         extra[name] = e
         del sx, wx
         torch.cuda.empty_cache()
@@ -717,20 +845,22 @@ def main():
         torch.cuda.empty_cache()
 
     # ---------------- CPU oracle on a bounded sample
-    cpu = None
+    cpu = parity = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle as orc
         orc.build()
         wh = make_workload(args.workload, "cpu")
-        arm = OracleArm(wh, orc, budget_s=15.0)
+        arm = OracleArm(wh, orc, budget_s=10.0)
         nb, sec = arm.step()
         cpu = {"value": round(nb / sec / 1e9, 4), "unit": "GB/s", "cores": arm.nthreads,
                "kind": "oracle", "sample": arm.describe(sec)}
-        # the same sample on one host core
-        arm.nthreads = 1
+        del arm
+        # a smaller sample of the same workload on one host core
+        arm = OracleArm(wh, orc, budget_s=4.0, nthreads=1)
         nb1, sec1 = arm.step()
         cpu["single_thread"] = {"value": round(nb1 / sec1 / 1e9, 4), "unit": "GB/s", "cores": 1,
                                 "sample": arm.describe(sec1)}
+        del arm, wh
         # the oracle's 2^24-octet pack + unpack (one thread), beside the pages' CPU time
         vals = W.all_octets("cpu").numpy().reshape(-1, 8)
         t0 = time.perf_counter()
@@ -741,6 +871,10 @@ def main():
             extra["pack3_2^24"]["oracle_pack_unpack_s"] = round(t_or, 3)
             extra["pack3_2^24"]["oracle_roundtrip_ok"] = bool(np.array_equal(back, vals))
         del vals, packed, back
+        # the timed step's own output and cache, checked by the oracle
+        if snap is not None:
+            parity = check_timed_step(snap, orc)
+            del snap
 
     if rank == 0:
         line = {
@@ -749,12 +883,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.cache_kind,
             "data": "synthetic (seeded torch CUDA generator; N(0,1) K/V/q)",
-            "config": {"workload": args.workload, "batch": w.batch, "num_heads": w.num_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                       "block_size": w.block_size, "context": w.extra.get("context"),
-                       "cache_dtype": w.cache_kind,
-                       "new_tokens": n_real, "parallelism": "replicas" if ws > 1 else "single",
-                       "l2": "inputs larger than L2, and flushed between steps outside the "
+            "config": workload_config(w, args.workload, ws),
+            "timing": {"l2": "inputs larger than L2, and flushed between steps outside the "
                              "timed events (256 MiB write, then a 512 MiB read that drains "
                              "its write-back)",
                        "launch": "a device-timed step replays one CUDA graph of one "
@@ -784,6 +914,7 @@ def main():
                           "how": "the same calls made eagerly from Python each step"},
             "gpu_launches": launches_per_step * args.steps,
             "cpu_baseline": cpu,
+            "parity": parity,
             "workloads": extra,
             "timed_wall_s": round(wall, 3),
         }

@@ -326,22 +326,30 @@ int pkv_decode_step(const pkv_tensor *k_new, const pkv_tensor *v_new, const pkv_
 
 /*
  * pkv_paged_decode_noalloc -- pkv_paged_decode for callers that cannot
- * allocate device memory at call time: code being captured into a CUDA
- * graph, plugin or custom-op hooks of inference engines that may not
- * allocate while enqueueing, and serving loops that cannot afford the
- * device-wide synchronisation of cudaMalloc.  The pages have no
- * counterpart; it is an addition of this library.
+ * allocate device memory at call time: plugin or custom-op hooks of
+ * inference engines that may not allocate while enqueueing, runtimes whose
+ * device memory all belongs to their own pool allocator, and serving loops
+ * that cannot afford the device-wide synchronisation of cudaMalloc.  The
+ * pages have no counterpart; it is an addition of this library.
  *
  * Same arguments and result as pkv_paged_decode without the workspace: the
  * split-K scratch is a fixed array inside the library
- * (pkv_noalloc_scratch_bytes(), 8 MiB), reserved on every GPU that loads
- * the library until the process exits.  Nothing is allocated, by the call
- * or by anything it calls.
- *   - A problem whose scratch need (pkv_paged_decode_workspace) exceeds the
- *     array is rejected with PKV_ERR_WORKSPACE before any launch.
+ * (pkv_noalloc_scratch_bytes(), 8 MiB), reserved on a GPU when the CUDA
+ * runtime loads the library's device code there (with lazy module loading,
+ * the CUDA default, at the first use of the library on that GPU -- at the
+ * latest, the first call of this function) and held until the process
+ * exits.  The call itself allocates nothing and calls nothing that does.
+ *   - num_splits 0: the automatic plan when its scratch fits the array,
+ *     else the largest explicit split count (16 down to 1) that fits; one
+ *     split needs no scratch, so num_splits 0 always finds a plan.
+ *   - An explicit num_splits whose scratch need (pkv_paged_decode_workspace)
+ *     exceeds the array is rejected with PKV_ERR_WORKSPACE before any
+ *     launch.  num_splits 1 needs no scratch.
  *   - The first call on a device looks the array's device address up with
  *     cudaGetSymbolAddress (once per device, with that device current);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is
+ *     cached per device ordinal: only the device's primary context (the
+ *     runtime API's) is supported, and not across a cudaDeviceReset.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls whose kernels overlap
  *     on the GPU (different streams, or concurrent host threads) race on
@@ -358,8 +366,10 @@ int pkv_paged_decode_noalloc(const pkv_tensor *q, const pkv_cache *cache,
  * pkv_pack3 / pkv_unpack3 -- 8 x uint3 <-> 3 bytes per octet
  * ("triton-3bit-kv-cache-kernel" README, section 1.A, packing and
  * explicit unpacking formulas).
- *   values : U8 [n_octets * 8], contiguous; only the low 3 bits are used.
- *   packed : U8 [n_octets * 3], contiguous.
+ *   values : U8 [n_octets * 8], contiguous, 16-byte aligned; only the low
+ *            3 bits are used.
+ *   packed : U8 [n_octets * 3], contiguous, 4-byte aligned.
+ *   A misaligned pointer is rejected with PKV_ERR_LAYOUT.
  *   Bit exact: packing the lanes v_i of octet state n = sum v_i * 8^i gives
  *   the three little-endian bytes of n.
  */
@@ -372,7 +382,8 @@ int pkv_unpack3(const uint8_t *packed, uint8_t *values, int64_t n_octets, void *
  * word 3i/32, shift 3i%32; lanes 10 and 21 straddle words).
  *   words  : device uint32 [n_groups * 3], 4-byte aligned.  The same bytes
  *            as 4 packed octets read as little-endian words.
- *   values : U8 [n_groups * 32].
+ *   values : U8 [n_groups * 32], 16-byte aligned.
+ *   A misaligned pointer is rejected with PKV_ERR_LAYOUT.
  */
 int pkv_unpack3_words(const uint32_t *words, uint8_t *values, int64_t n_groups, void *stream);
 

@@ -3,19 +3,22 @@
 // that cannot allocate device memory at call time.
 //
 // Who needs it: code that enqueues work where cudaMalloc is not allowed or
-// not affordable -- inside a region being captured into a CUDA graph (an
-// allocation is not a capturable operation), inside plugin / custom-op
-// hooks of inference engines that hand the op only its inputs and outputs
-// and forbid allocation while enqueueing, and latency-critical serving loops
-// where cudaMalloc's implicit device-wide synchronisation would stall every
-// other stream.  Such callers cannot provide the workspace that
-// pkv_paged_decode asks for, so this entry point brings its own.
+// not affordable -- plugin / custom-op hooks of inference engines that hand
+// the op only its inputs and outputs and forbid allocation while
+// enqueueing, runtimes whose memory is owned by their own pool allocator,
+// and latency-critical serving loops where cudaMalloc's implicit
+// device-wide synchronisation would stall every other stream.  Such callers
+// cannot provide the workspace that pkv_paged_decode asks for, so this entry
+// point brings its own.
 //
 // The scratch is one file-scope __device__ array of kNoAllocScratchBytes.
-// Every GPU that loads the library reserves it until the process exits.
-// Host code must not hand the array's name to a kernel (on the host it is
-// only a stand-in symbol), so the device address is looked up with
-// cudaGetSymbolAddress once per device and cached.
+// Every GPU that loads the library's device code reserves it until the
+// process exits.  Host code must not hand the array's name to a kernel (on
+// the host it is only a stand-in symbol), so the device address is looked
+// up with cudaGetSymbolAddress once per device and cached.  The cache is
+// keyed by device ordinal and so assumes the device's primary context (the
+// one the runtime API uses) for the life of the process: after a
+// cudaDeviceReset the cached address is stale.
 #include <cstdio>
 #include <mutex>
 
@@ -66,12 +69,26 @@ int pkv_paged_decode_noalloc(const pkv_tensor *q, const pkv_cache *cache,
     size_t need = 0;
     int rc = pkv_paged_decode_workspace(q, cache, block_tables, num_splits, &need);
     if (rc != PKV_OK) return rc;
+    if (need > kNoAllocScratchBytes && num_splits == 0) {
+        // The automatic plan does not fit: take the largest explicit split
+        // count that does.  One split needs no scratch at all, so this
+        // always ends with a plan.
+        for (int s = 16; s >= 1; --s) {
+            rc = pkv_paged_decode_workspace(q, cache, block_tables, s, &need);
+            if (rc != PKV_OK) return rc;
+            if (need <= kNoAllocScratchBytes) {
+                num_splits = s;
+                break;
+            }
+        }
+    }
     if (need > kNoAllocScratchBytes) {
         // Report through the same per-thread message as every other call.
         snprintf(g_msg, sizeof(g_msg),
-                 "paged_decode_noalloc: this problem needs %zu bytes of scratch, more than the "
-                 "library's fixed %zu-byte array; use pkv_paged_decode with a workspace",
-                 need, kNoAllocScratchBytes);
+                 "paged_decode_noalloc: num_splits %d needs %zu bytes of scratch, more than the "
+                 "library's fixed %zu-byte array; pass num_splits 0 (a plan that fits) or 1 "
+                 "(no scratch)",
+                 num_splits, need, kNoAllocScratchBytes);
         return pkv::set_last_error(PKV_ERR_WORKSPACE, g_msg);
     }
     void *scratch = nullptr;

@@ -19,10 +19,13 @@ def src_code(w):
 # ---------------------------------------------------------------- GPU side
 
 def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, stream=None,
-            meta_slot_major=False):
+            meta_slot_major=False, via_step=False):
     """Fill + append + decode on the GPU.  Returns (cache, out).
     meta_slot_major: store 3-bit scale/zero arrays contiguous [blocks, slots,
-    heads] instead of the allocator's head-major layout."""
+    heads] instead of the allocator's head-major layout.
+    via_step: the step's tokens go through pkv_decode_step (slot computation
+    fused into the append, decode reading its inputs before the append
+    completes), the path the benchmark times, instead of the three calls."""
     dev = "cuda"
     cache = pkv.KVCache.allocate(w.cache_kind, w.num_blocks, w.block_size, w.num_kv_heads,
                                  w.head_dim, device=dev,
@@ -57,6 +60,13 @@ def gpu_run(w, pkv, num_splits=0, decode=True, err_flag=None, poison=None, strea
             append(w.k_fill[i:i + chunk].to(dev), w.v_fill[i:i + chunk].to(dev), sm,
                    w.k_fill_scale[i:i + chunk] if tok else None,
                    w.v_fill_scale[i:i + chunk] if tok else None)
+    if via_step:
+        assert not tok and poison is None and decode and w.q is not None
+        out = pkv.decode_step(w.k_new.to(dev), w.v_new.to(dev), w.new_req.to(dev),
+                              w.new_pos.to(dev), w.q.to(dev), cache, bt, w.context_lens.to(dev),
+                              sm_scale=w.sm_scale, num_splits=num_splits, err_flag=err_flag)
+        torch.cuda.synchronize()
+        return cache, out
     sm = pkv.slot_mapping(bt, w.new_req.to(dev), w.new_pos.to(dev), w.block_size,
                           err_flag=err_flag)
     append(w.k_new.to(dev), w.v_new.to(dev), sm, w.k_new_scale, w.v_new_scale)

@@ -1,7 +1,8 @@
 """GPU parity of paged_decode with the fp64 oracle (max-abs 4e-3 for fp16
 outputs, 2e-2 for bf16 outputs), for 16-bit, fp8 and 3-bit caches, with and
 without the split-K merge, on small cases that span several blocks and a
-ragged tail, on the full-size workloads (sampled rows), and on the edge
+ragged tail, on the full-size workloads (every row, through the three
+calls and through pkv_decode_step), and on the edge
 cases: empty and one-token contexts, poisoned slots beyond the context,
 permuted blocks, out-of-range table data."""
 import numpy as np
@@ -272,65 +273,53 @@ def _sample_pairs(w, seqs, heads_per_seq=None):
     return np.array(pairs, np.int32)
 
 
+def _full_size(w, pkv, orc, paths=("calls", "step")):
+    """A full-size workload through the GPU along each path (the three calls;
+    pkv_decode_step, the benchmark's path), the oracle once: every cache
+    byte of the whole pool and every (sequence, head) output row compared."""
+    oc = PL.oracle_caches(w, orc)
+    ref = PL.oracle_decode(w, orc, oc)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    worst = 0.0
+    for path in paths:
+        cache, out = PL.gpu_run(w, pkv, err_flag=err, via_step=path == "step")
+        assert int(err.item()) == 0, path
+        gc = PL.gpu_cache_host(cache)
+        for k, arr in oc.items():
+            if w.layout == "xvec" and k in ("k_cache", "v_cache"):
+                arr = orc.to_xvec(arr, 16 // arr.dtype.itemsize)   # storage order
+            assert np.array_equal(gc[k], arr), (path, k)
+        del cache, gc
+        worst = max(worst, _check(w, out, ref))
+    return worst
+
+
 def test_full_gqa_bf16(pkv, orc):
-    """Full-size GQA bf16 workload (batch 64, contexts 512..4096): every
-    output row against the oracle."""
-    w = W.gqa_bf16()
-    _, out = PL.gpu_run(w, pkv)
-    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
-    _check(w, out, ref)
+    """Full-size GQA bf16 workload (batch 64, contexts 512..4096)."""
+    _full_size(W.gqa_bf16(), pkv, orc)
 
 
-def test_full_fp8_long_sampled(pkv, orc):
-    """Full-size long-context fp8 workload: sampled sequences, all their
-    heads; the oracle fills only those sequences' rows."""
-    w = W.fp8_long()
-    cache, out = PL.gpu_run(w, pkv)
-    seqs = [0, 7, 15]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    gc = PL.gpu_cache_host(cache)
-    for b in seqs:
-        n = int(w.context_lens[b])
-        blocks = w.block_tables[b, :(n + w.block_size - 1) // w.block_size].long().numpy()
-        for k in ("k_cache", "v_cache"):
-            flat_g = gc[k][blocks].reshape(-1, w.num_kv_heads, w.head_dim)[:n]
-            flat_o = oc[k][blocks].reshape(-1, w.num_kv_heads, w.head_dim)[:n]
-            assert np.array_equal(flat_g, flat_o)
-    pairs = _sample_pairs(w, seqs)
-    ref = PL.oracle_decode(w, orc, oc, pairs=pairs)
-    _check(w, out, ref, pairs)
+def test_full_fp8_long(pkv, orc):
+    """Full-size long-context fp8 workload (batch 16, 64 q / 8 kv heads,
+    contexts 16K..32K, e4m3 with per-head scales): the benchmark's
+    headline workload."""
+    _full_size(W.fp8_long(), pkv, orc)
 
 
-def test_full_fp8_long_e5m2_sampled(pkv, orc):
-    """The long-context shape with an e5m2 cache (scales amax/57344):
-    sampled sequences against the oracle."""
-    w = W.fp8_long(seed=W.SEEDS["fp8_long_e5m2"], fp8="e5m2")
-    cache, out = PL.gpu_run(w, pkv)
-    seqs = [0, 15]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs, heads_per_seq=range(0, w.num_heads, 5))
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+def test_full_fp8_long_e5m2(pkv, orc):
+    """The long-context shape with an e5m2 cache (scales amax/57344)."""
+    _full_size(W.fp8_long(seed=W.SEEDS["fp8_long_e5m2"], fp8="e5m2"), pkv, orc, paths=("step",))
 
 
-def test_full_i8_long_sampled(pkv, orc):
-    """The long-context shape with an int8 cache (scales amax/127): sampled
-    sequences against the oracle."""
-    w = W.fp8_long(seed=W.SEEDS["i8_long"], fp8="i8")
-    cache, out = PL.gpu_run(w, pkv)
-    seqs = [3, 12]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs, heads_per_seq=range(1, w.num_heads, 5))
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+def test_full_i8_long(pkv, orc):
+    """The long-context shape with an int8 cache (scales amax/127)."""
+    _full_size(W.fp8_long(seed=W.SEEDS["i8_long"], fp8="i8"), pkv, orc, paths=("step",))
 
 
-def test_full_u3_mha_sampled(pkv, orc):
-    w = W.u3_mha()
-    cache, out = PL.gpu_run(w, pkv)
-    seqs = [0, 13, 31]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs)
-    ref = PL.oracle_decode(w, orc, oc, pairs=pairs)
-    _check(w, out, ref, pairs)
+def test_full_u3_mha(pkv, orc):
+    """Full-size 3-bit MHA workload (batch 32, 32 heads, contexts
+    1024..8192)."""
+    _full_size(W.u3_mha(), pkv, orc)
 
 
 @pytest.mark.parametrize("maker", ["gqa", "u3"])
@@ -568,12 +557,14 @@ def test_large_group_token_scales(pkv, orc):
     _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
 
 
-def test_full_405b_like_fp8_sampled(pkv, orc):
+def test_full_405b_like_fp8(pkv, orc):
     """Llama-3.1-405B-like long-context e4m3 step: batch 8, 128 q / 8 kv
-    heads (group 16), contexts 16K..32K; sampled sequences, all heads."""
-    w = W.fp8_long(batch=8, num_heads=128, seed=298)
-    _, out = PL.gpu_run(w, pkv)
-    seqs = [1, 6]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs)
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+    heads (group 16), contexts 16K..32K."""
+    _full_size(W.fp8_long(batch=8, num_heads=128, seed=298), pkv, orc, paths=("step",))
+
+
+def test_full_fp8_long_g16(pkv, orc):
+    """The benchmark's group-16 long-context workload (batch 16, 128 q / 8
+    kv heads, e4m3)."""
+    _full_size(W.fp8_long(seed=W.SEEDS["fp8_long_g16"], num_heads=128), pkv, orc,
+               paths=("step",))

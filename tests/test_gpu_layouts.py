@@ -127,12 +127,9 @@ def test_mha_short_small(pkv, orc):
         _check(w, out, PL.oracle_decode(w, orc, PL.oracle_caches(w, orc)))
 
 
-def test_full_mha_short_sampled(pkv, orc):
+def test_full_mha_short(pkv, orc):
     """The page's benchmark shape at full size (batch 32, 32 heads, a
-    2048-block pool, contexts 100..999): sampled sequences, all heads."""
-    w = W.mha_short()
-    _, out = PL.gpu_run(w, pkv)
-    seqs = [0, 11, 31]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs)
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+    2048-block pool, contexts 100..999): every cache byte and every output
+    row, through the three calls and through pkv_decode_step."""
+    from tests.test_gpu_decode import _full_size
+    _full_size(W.mha_short(), pkv, orc)

@@ -120,15 +120,12 @@ def test_slot_major_token_scales_take_the_general_kernel(pkv, orc):
 
 
 @pytest.mark.parametrize("scales", ["token", "block"])
-def test_full_fp8_long_granular_sampled(pkv, orc, scales):
+def test_full_fp8_long_granular(pkv, orc, scales):
     """The long-context shape with per-token (each row's amax / 448) or
-    per-block scales, through the persistent kernel: sampled sequences
-    against the oracle."""
+    per-block scales, through the persistent kernel: every cache byte and
+    every output row against the oracle (per-token scales through the
+    separate calls, which carry them; per-block through pkv_decode_step)."""
+    from tests.test_gpu_decode import _full_size
     name = "fp8_long_%s_scales" % scales
     w = W.fp8_long(seed=W.SEEDS[name], scales=scales)
-    cache, out = PL.gpu_run(w, pkv)
-    seqs = [2, 9]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    from tests.test_gpu_decode import _sample_pairs
-    pairs = _sample_pairs(w, seqs, heads_per_seq=range(0, w.num_heads, 7))
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+    _full_size(w, pkv, orc, paths=("calls",) if scales == "token" else ("step",))

@@ -113,26 +113,19 @@ def test_xvec_matches_flash_layout_bitwise(pkv, kind):
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 
-def test_full_gqa_bf16_xvec_sampled(pkv, orc):
+def test_full_gqa_bf16_xvec(pkv, orc):
     """Full-size Llama-3-8B-like GQA step (batch 64, contexts 512..4096) in
-    the x-vectorised layout, sampled sequences against the oracle."""
-    w = W.gqa_bf16(layout="xvec")
-    _, out = PL.gpu_run(w, pkv)
-    seqs = [0, 17, 63]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs)
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+    the x-vectorised layout: every stored byte (storage order) and every
+    output row against the oracle."""
+    from tests.test_gpu_decode import _full_size
+    _full_size(W.gqa_bf16(layout="xvec"), pkv, orc, paths=("step",))
 
 
-def test_full_fp8_long_xvec_sampled(pkv, orc):
+def test_full_fp8_long_xvec(pkv, orc):
     """Full-size long-context e4m3 step (batch 16, contexts 16K..32K) in the
-    x-vectorised layout, sampled sequences against the oracle."""
-    w = W.fp8_long(layout="xvec")
-    _, out = PL.gpu_run(w, pkv)
-    seqs = [3, 12]
-    oc = PL.oracle_caches(w, orc, seqs=seqs)
-    pairs = _sample_pairs(w, seqs)
-    _check(w, out, PL.oracle_decode(w, orc, oc, pairs=pairs), pairs)
+    x-vectorised layout: every stored byte and every output row."""
+    from tests.test_gpu_decode import _full_size
+    _full_size(W.fp8_long(layout="xvec"), pkv, orc, paths=("step",))
 
 
 @pytest.mark.parametrize("kind", ["bf16", "e4m3"])

@@ -1,13 +1,15 @@
 """pkv_paged_decode_noalloc: the decode entry point for callers that cannot
-allocate device memory while they enqueue work (code under CUDA-graph
-capture, engine plugins that may not allocate during enqueue, serving loops
-that cannot pay cudaMalloc's device-wide synchronisation).  Its split-K
-scratch is a fixed array inside the library instead of a caller workspace.
+allocate device memory while they enqueue work (engine plugins that may not
+allocate during enqueue, runtimes whose device memory belongs to their own
+pool allocator, serving loops that cannot pay cudaMalloc's device-wide
+synchronisation).  Its split-K scratch is a fixed array inside the library
+instead of a caller workspace.
 
 Called through the C ABI, its output must match pkv_paged_decode's (which
-gets a workspace from the caller) within the decode tolerance, on two calls
-in a row with different inputs, so the second call runs over the first
-call's leftovers in the shared array.  This file sorts last so that a run
+gets a workspace from the caller) within the decode tolerance -- and, as
+both run the same plan and the same deterministic kernels, bit for bit --
+on two calls in a row with different inputs, so the second call runs over
+the first call's leftovers in the shared array.  This file sorts last so that a run
 stopping at the first failure has run every other test first; it also
 passes on its own in a fresh process."""
 import ctypes
@@ -58,11 +60,30 @@ def test_noalloc_matches_workspace_decode_twice(pkv, num_splits):
         assert int(err.item()) == 0
         d = np.max(np.abs(PL.out_f64(out) - PL.out_f64(ref)))
         assert d <= PL.tolerance(w), d
+        assert torch.equal(out, ref)
+
+
+def test_noalloc_auto_plan_falls_back_to_a_plan_that_fits(pkv):
+    """With num_splits 0 and a batch whose automatic plan needs more scratch
+    than the fixed array, the call takes the largest split count that fits
+    (at worst one split, no scratch) instead of failing; its output matches
+    the workspace decode's within the tolerance, on two calls in a row."""
+    for seed in (73, 74):
+        w = W.gqa_bf16(batch=512, ctx_lo=16, ctx_hi=200, seed=seed)
+        cache, ref = PL.gpu_run(w, pkv, num_splits=0)
+        need = pkv.decode_workspace_bytes(w.q.cuda(), cache, w.block_tables.cuda(), 0)
+        assert need > pkv.lib().pkv_noalloc_scratch_bytes()
+        out, err = _noalloc_c_abi(pkv, w.q.cuda(), cache, w.block_tables.cuda(),
+                                  w.context_lens.cuda(), w.sm_scale, 0)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        d = np.max(np.abs(PL.out_f64(out) - PL.out_f64(ref)))
+        assert d <= PL.tolerance(w), d
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(pkv):
-    """A problem needing more scratch than the fixed array gets
-    PKV_ERR_WORKSPACE and a message, before anything is launched."""
+    """An explicit split count needing more scratch than the fixed array
+    gets PKV_ERR_WORKSPACE and a message, before anything is launched."""
     m = pkv.pkv
     B, Hq, Hkv, D = 64, 64, 8, 128
     q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda")
