@@ -66,18 +66,26 @@ template <int CK, int D>
 cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                            const CUtensorMap &mv, cudaStream_t s)
 {
-    if constexpr (CK == kU3) {      // MHA caches get the one-column consumers
+    if constexpr (CK == kU3) {      // MHA caches: f.hpw kv heads per consumer warp
         if (p.group == 1) {
-            if (p.block_size == 16) return launch_fast_t<CK, D, 16, true>(p, f, mk, mv, s);
-            if (p.block_size == 32) return launch_fast_t<CK, D, 32, true>(p, f, mk, mv, s);
+            if (p.block_size == 16) {
+                if (f.hpw == 4) return launch_fast_t<CK, D, 16, 4>(p, f, mk, mv, s);
+                if (f.hpw == 2) return launch_fast_t<CK, D, 16, 2>(p, f, mk, mv, s);
+                return launch_fast_t<CK, D, 16, 1>(p, f, mk, mv, s);
+            }
+            if (p.block_size == 32) {
+                if (f.hpw == 4) return launch_fast_t<CK, D, 32, 4>(p, f, mk, mv, s);
+                if (f.hpw == 2) return launch_fast_t<CK, D, 32, 2>(p, f, mk, mv, s);
+                return launch_fast_t<CK, D, 32, 1>(p, f, mk, mv, s);
+            }
         }
     }
     if constexpr (is_q8(CK)) {      // per-block / per-token scales staged with the tiles
         if (p.scale_mode != 0) {
             switch (p.block_size) {
-            case 16: return launch_fast_t<CK, D, 16, false, true>(p, f, mk, mv, s);
-            case 32: return launch_fast_t<CK, D, 32, false, true>(p, f, mk, mv, s);
-            case 64: return launch_fast_t<CK, D, 64, false, true>(p, f, mk, mv, s);
+            case 16: return launch_fast_t<CK, D, 16, 0, true>(p, f, mk, mv, s);
+            case 32: return launch_fast_t<CK, D, 32, 0, true>(p, f, mk, mv, s);
+            case 64: return launch_fast_t<CK, D, 64, 0, true>(p, f, mk, mv, s);
             default: return cudaErrorInvalidValue;
             }
         }
@@ -116,13 +124,18 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // consumer warps per kv head: 2 for groups above 8 q heads (8 each);
     // the CTA keeps at most 8 consumer warps
     const int wsh = group > 8 ? 1 : 0;
-    int nh = u3 ? kU3Heads : (8 >> wsh);
+    // 3-bit multi-head caches: up to 4 kv heads per consumer warp (a power
+    // of two dividing num_kv_heads)
+    int hpw = 1;
+    if (u3 && group == 1) hpw = num_kv_heads % 4 == 0 ? 4 : (num_kv_heads % 2 == 0 ? 2 : 1);
+    int nh = u3 ? (hpw > 1 ? kU3MhaHeads : kU3Heads) : (8 >> wsh);
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
+    while (nh % hpw != 0) hpw >>= 1;
     // 3-bit kernels are register-capped so that several CTAs share an SM; the
     // shared memory (228 KB per SM, 1 KB of it reserved per CTA) and the
     // bytes kept in flight are split between them
-    const int ctas_per_sm = u3 ? kU3CtasPerSm : 1;
+    const int ctas_per_sm = u3 ? (hpw > 1 ? kU3MhaCtasPerSm : kU3CtasPerSm) : 1;
     const int budget = (228 * 1024) / ctas_per_sm - 1024;
     // ring depth: enough bytes in flight per SM, within the shared memory
     int stages = 8;
@@ -143,12 +156,15 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
     f.nh = nh;
     f.wsh = wsh;
+    f.hpw = hpw;
+    f.ncons = hpw > 1 ? nh / hpw : nh << wsh;
     f.n_hg = n_hg;
     f.stages = stages;
     const int64_t slots = int64_t(sm_count) * ctas_per_sm;
     f.grid = int(max_units < slots ? (max_units > 0 ? max_units : 1) : slots);
     f.smem_bytes = L.total;
     f.meta_heads = meta_heads;
+    f.meta_hmaj = meta_head_major ? 1 : 0;
     const int64_t rows = (int64_t(f.grid) + int64_t(n_hg) * batch) * nh * group;
     const size_t ml_bytes = (size_t(rows) * 2 * 4 + 255) / 256 * 256;
     workspace = ml_bytes + size_t(rows) * head_dim * 4;

@@ -238,22 +238,35 @@ struct Tile {
 // The others: CTAs of up to 8 kv heads, one per SM.
 constexpr int kU3Heads = 4;
 constexpr int kU3CtasPerSm = 3;
-template <int CK>
-constexpr int kCtasPerSm = CK == kU3 ? kU3CtasPerSm : 1;
+// 3-bit multi-head caches with several kv heads per consumer warp: CTAs of
+// (at most) 16 kv heads -- four consumer warps of four heads, 12 KB tensor
+// copies -- two per SM.
+constexpr int kU3MhaHeads = 16;
+constexpr int kU3MhaCtasPerSm = 2;
+template <int CK, int U3H>
+constexpr int kCtasPerSm = CK == kU3 ? (U3H >= 2 ? kU3MhaCtasPerSm : kU3CtasPerSm) : 1;
 template <int CK>
 constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
 
-// G1: one q head per kv head (multi-head attention) -- the consumers skip
-// the second head column of their C fragments, which never exists then.
+// U3H: 3-bit multi-head caches (one q head per kv head).  0: grouped q
+// heads (the head columns of a warp are the q heads of one kv head).  1: one
+// kv head per consumer warp, whose second head column never exists.  2 or 4:
+// HPW = U3H kv heads per consumer warp, column j of the C fragments being
+// kv head j of the warp -- K of head j runs through its own MMAs (the other
+// columns of those products are dropped), V through block-diagonal MMAs whose
+// k range is split between the heads, so that one set of O accumulators,
+// one softmax and one walk of the ring serve HPW heads.
 // GSC: fp8 / int8 with per-block or per-token scales, staged per block.
 // XV: x-vectorised cache layout (16-bit and one-byte codes).
-template <int CK, int D, int BS, bool G1 = false, bool GSC = false, bool XV = false>
-__global__ void __launch_bounds__(kMaxThreads<CK>, kCtasPerSm<CK>)
+template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false>
+__global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H>))
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeParams p, FastParams f)
 {
     using T = Tile<CK, D, BS>;
-    constexpr int NC = G1 ? 1 : 2;      // head columns (2tig, 2tig+1) that can exist
+    constexpr int NC = U3H == 1 ? 1 : 2;   // head columns (2tig, 2tig+1) that can exist
+    constexpr int HPW = U3H >= 2 ? U3H : 1;  // kv heads per consumer warp
+    static_assert(HPW == 1 || (T::kIsU3 && (HPW == 2 || HPW == 4)), "heads per warp");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -293,7 +306,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, nh << f.wsh);   // one arrival per consumer warp
+            ptx::mbar_init(bar_empty + 8 * s, f.ncons);   // one arrival per consumer warp
         }
         ptx::fence_mbar_init();
     }
@@ -324,7 +337,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (lo >= hi) return;
 
     // ======================================================== producer warp
-    if (warp == (nh << f.wsh)) {
+    if (warp == f.ncons) {
         if (lane == 0) {
             ptx::prefetch_tmap(&tmk);
             ptx::prefetch_tmap(&tmv);
@@ -410,7 +423,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             if constexpr (T::kIsU3) {
                                 const int HB = BS * f.meta_heads;         // entries per stage
                                 // head-major: the group's heads are one run at head hgk*nh
-                                const int64_t h0 = f.meta_heads == nh ? int64_t(hgk) * nh * BS : 0;
+                                const int64_t h0 = f.meta_hmaj ? int64_t(hgk) * nh * BS : 0;
                                 const uint32_t md = vdst + L.tile_bytes;
                                 ptx::bulk_load(md, p.k_qs + int64_t(pbk) * p.m_blk + h0, 2 * HB, fb);
                                 ptx::bulk_load(md + 2 * HB, p.v_qs + int64_t(pbk) * p.m_blk + h0, 2 * HB, fb);
@@ -439,10 +452,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // Consumer warp w serves kv head kvl = w >> wsh of the CTA's group and,
     // of its G q heads, the 8 (or fewer) from qh0 = 8 (w & (2^wsh - 1)):
     // with groups of up to 8 q heads one warp per kv head, with up to 16
-    // two warps reading the same K / V tiles.
-    const int kvl = warp >> f.wsh;
-    const int qh0 = 8 * (warp & ((1 << f.wsh) - 1));
-    const int GW = min(8, G - qh0);           // q heads (head columns) of this warp
+    // two warps reading the same K / V tiles.  With HPW > 1 (3-bit,
+    // multi-head) warp w serves kv heads kvl .. kvl + HPW - 1, kvl = HPW w,
+    // head column j being kv head kvl + j.
+    const int kvl = HPW > 1 ? HPW * warp : warp >> f.wsh;
+    const int qh0 = HPW > 1 ? 0 : 8 * (warp & ((1 << f.wsh) - 1));
+    const int GW = HPW > 1 ? HPW : min(8, G - qh0);   // head columns of this warp
     // Tokens on the MMA's M dimension, this warp's q heads on N (<= 8):
     //   S^T[tok][head] = K[tok][:] . Q[head][:]        (A = K, B = Q^T)
     //   O^T[d][head]  += V^T[d][tok] P^T[tok][head]     (A = V^T, B = P^T)
@@ -491,8 +506,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             ctx_b = cb < 0 ? 0 : (cb > cap ? cap : cb);
         }
         const bool hv = gid < GW;  // this lane's B column (q head qh0 + gid) exists
-        const uint16_t *qr =
-            reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (kvh * G + qh0 + gid) * p.q_h);
+        // column gid: q head qh0 + gid of kv head kvh, or (HPW > 1) the q
+        // head of kv head kvh + gid
+        const int qhead = HPW > 1 ? (kvh + gid) * G : kvh * G + qh0 + gid;
+        const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + qhead * p.q_h);
         if constexpr (T::kIsU3) {
             // q' = q qs 2^(1-x) (f16, exact) in the pair order of the K
             // fragments: k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1)
@@ -620,7 +637,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     };
 
     auto finish_segment = [&](int64_t seg_end) {
-        const int kvh = hg * nh + kvl;
         const int64_t unit_first = int64_t(hg) * NBT + prefix[b];
         const int64_t unit_last = unit_first + nblk[b] - 1;
         float lt[2];
@@ -658,7 +674,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int c = 0; c < 2; ++c) {
             const int g = 2 * tig + c;
             if (g >= GW) continue;
-            const int h = kvh * G + qh0 + g;
+            // q head of column g, within the head group and overall
+            const int local = HPW > 1 ? (kvl + g) * G : kvl * G + qh0 + g;
+            const int h = hg * nh * G + local;
             if (whole) {
                 const float inv = lt[c] > 0.0f ? vmul / lt[c] : 0.0f;
                 uint16_t *orow = reinterpret_cast<uint16_t *>(p.out + b * p.o_b + h * p.o_h);
@@ -670,7 +688,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         orow[d_of(t, r)] = p.q_is_bf16 ? f2h<kBF16>(v) : f2h<kF16>(v);
                     }
             } else {
-                const int64_t row = key * (int64_t(nh) * G) + int64_t(kvl) * G + qh0 + g;
+                const int64_t row = key * (int64_t(nh) * G) + local;
                 float *acc = f.part_acc + row * D;
                 if (gid == 0) {
                     f.part_ml[2 * row] = m[c];
@@ -687,77 +705,93 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // 3-bit blocks: NB (1, or 2 for 16-token blocks) consecutive blocks of
     // one sequence, held in stages s0 (and s1), as NB * KT tiles of 16
     // tokens; `valid` counts the live tokens of all NB blocks (only the last
-    // block of a sequence can be partial).
+    // block of a sequence can be partial).  The warp serves HPW kv heads
+    // (kvl ..): with HPW = 1 its head columns are q heads of kv head kvl,
+    // with HPW > 1 column j is kv head kvl + j.
     auto u3_body = [&](auto nb_c, int s0, int s1, int valid) {
         constexpr int NB = decltype(nb_c)::value;
         constexpr int KTT = NB * T::KT;          // 16-token tiles of the NB blocks
+        constexpr int NT = NB * BS;              // tokens of the NB blocks
         const int kvh = hg * nh + kvl;
-        const bool partial = valid < NB * BS;
+        const bool partial = valid < NT;
         // stage of tile t, and the tile's first row within its block
         auto tile_stage = [&](int t) { return t < T::KT ? s0 : s1; };
         auto tile_row = [&](int t) { return 16 * (t % T::KT); };
-        auto kpk = [&](int t) {                  // packed K rows of the tile (shared address)
-            return sbase + tile_stage(t) * L.stage_bytes + kvl * BS * T::ROW + tile_row(t) * T::ROW;
+        // packed K rows of tile t of the warp's head hh (shared address)
+        auto kpk = [&](int t, int hh) {
+            return sbase + tile_stage(t) * L.stage_bytes + (kvl + hh) * BS * T::ROW + tile_row(t) * T::ROW;
         };
-        // ---- metadata: lane l converts token l of the NB blocks (this
-        // warp's head) to fp32 (sk, zk, sv, zv) in the stage's conversion
-        // area -- one token per lane instead of four 16- / 8-bit loads and
-        // conversions per score row in every lane -- and each lane then reads
-        // its score rows (tokens gid, gid+8 of each tile) with one 16-byte
-        // load each.  Staged as [nh][BS] runs (head-major) or [BS][num_kv_heads]
-        // arrays.
+        // ---- metadata: the warp converts each (head, token) of its HPW
+        // heads and the NB blocks to fp32 (sk, zk, sv, zv) in the stage's
+        // conversion area -- one entry per lane and step instead of four 16-
+        // / 8-bit loads and conversions per score row in every lane -- and
+        // each lane then reads its score rows' entries.  Staged as [nh][BS]
+        // runs (head-major) or [BS][num_kv_heads] arrays.
         const int MH = f.meta_heads;
-        const bool hmaj = MH == nh;
+        const bool hmaj = f.meta_hmaj != 0;
         auto conv_area = [&](int st) {
             return reinterpret_cast<float4 *>(smem + (st * L.stage_bytes + 2 * L.tile_bytes + raw_meta));
         };
-        if (lane < NB * BS) {
-            const int st = lane < BS ? s0 : s1, slot = lane & (BS - 1);
-            const unsigned char *raw = smem + (st * L.stage_bytes + 2 * L.tile_bytes);
-            const __half *mks = reinterpret_cast<const __half *>(raw);
-            const __half *mvs = mks + BS * MH;
-            const uint8_t *mkz = raw + 4 * BS * MH;
-            const uint8_t *mvz = mkz + BS * MH;
-            const int i = hmaj ? kvl * BS + slot : slot * MH + kvh;
-            conv_area(st)[kvl * BS + slot] =
-                make_float4(__half2float(mks[i]), float(mkz[i]), __half2float(mvs[i]), float(mvz[i]));
-        }
-        __syncwarp();
-        float sk[KTT][2], zk[KTT][2], sv[KTT][2], zv[KTT][2];
 #pragma unroll
-        for (int mt = 0; mt < KTT; ++mt) {
-            const float4 *cv = conv_area(tile_stage(mt));
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float4 m4 = cv[kvl * BS + tile_row(mt) + gid + 8 * r];
-                sk[mt][r] = m4.x;
-                zk[mt][r] = m4.y;
-                sv[mt][r] = m4.z;
-                zv[mt][r] = m4.w;
+        for (int i0 = 0; i0 < HPW * NT; i0 += 32) {
+            const int i = i0 + lane;
+            if (i < HPW * NT) {
+                const int hh = i / NT, tk = i % NT;
+                const int st = tk < BS ? s0 : s1, slot = tk & (BS - 1);
+                const unsigned char *raw = smem + (st * L.stage_bytes + 2 * L.tile_bytes);
+                const __half *mks = reinterpret_cast<const __half *>(raw);
+                const __half *mvs = mks + BS * MH;
+                const uint8_t *mkz = raw + 4 * BS * MH;
+                const uint8_t *mvz = mkz + BS * MH;
+                const int k = hmaj ? (kvl + hh) * BS + slot : slot * MH + kvh + hh;
+                conv_area(st)[(kvl + hh) * BS + slot] =
+                    make_float4(__half2float(mks[k]), float(mkz[k]), __half2float(mvs[k]), float(mvz[k]));
             }
         }
+        __syncwarp();
+        // conversion entry of score row (tile t, row half r) and head column c
+        auto meta_of = [&](int t, int r, int c) -> const float4 * {
+            // HPW 4: lanes tig 0, 1 hold columns 0-3; lanes tig 2, 3 hold
+            // none and read an in-range entry
+            const int hc = HPW == 1 ? 0 : (HPW == 2 ? c : ((2 * tig + c) & 3));
+            return conv_area(tile_stage(t)) + (kvl + hc) * BS + tile_row(t) + gid + 8 * r;
+        };
         // ---- S^T = K Q'^T with K converted straight into A fragments:
-        // lane (gid, tig) takes group tig of token rows gid and gid+8
+        // lane (gid, tig) takes group tig of token rows gid and gid+8.  With
+        // HPW > 1 each head's product keeps only its own column: heads 2i
+        // and 2i+1 fill columns (0, 1) of lanes tig = i.
         float sc[KTT][4];
 #pragma unroll
         for (int mt = 0; mt < KTT; ++mt) {
-            float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
-            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
-            const uint32_t a0 = kpk(mt) + gid * T::ROW + 12 * tig;
-            const uint32_t a1 = a0 + 8 * T::ROW;
-            const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
-            const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
+            float colp[HPW > 1 ? HPW / 2 : 1][4];
 #pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                uint32_t a[4];
-                a[0] = u3k_pair(2 * kk, x0, x1, x2);
-                a[1] = u3k_pair(2 * kk, y0, y1, y2);
-                a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
-                a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
-                ptx::mma16816<false>((kk & 1) ? sx : sc[mt], a, qb[kk][0], qb[kk][1]);
+            for (int hh = 0; hh < HPW; ++hh) {
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
+                const uint32_t a0 = kpk(mt, hh) + gid * T::ROW + 12 * tig;
+                const uint32_t a1 = a0 + 8 * T::ROW;
+                const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
+                const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
+#pragma unroll
+                for (int kk = 0; kk < T::QK; ++kk) {
+                    uint32_t a[4];
+                    a[0] = u3k_pair(2 * kk, x0, x1, x2);
+                    a[1] = u3k_pair(2 * kk, y0, y1, y2);
+                    a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
+                    a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
+                    ptx::mma16816<false>((kk & 1) ? sx : acc, a, qb[kk][0], qb[kk][1]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (HPW == 1)
+                        colp[0][e] = acc[e] + sx[e];
+                    else if ((e & 1) == (hh & 1))
+                        colp[hh >> 1][e] = acc[e] + sx[e];
+                }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[mt][e] += sx[e];
+            for (int e = 0; e < 4; ++e)
+                sc[mt][e] = HPW == 4 ? (tig == 0 ? colp[0][e] : colp[HPW > 2 ? 1 : 0][e]) : colp[0][e];
         }
         // ---- scores: remove the zero point, apply the per-token
         // scale, mask; online softmax per head column
@@ -768,7 +802,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int e = 0; e < 4; ++e) {
                 const int r = e >> 1, c = e & 1;
                 if (c >= NC) continue;
-                float v = mult * sk[t][r] * (sc[t][e] - zk[t][r] * q1h[c]);
+                const float2 kz = *reinterpret_cast<const float2 *>(meta_of(t, r, c));   // (sk, zk)
+                float v = mult * kz.x * (sc[t][e] - kz.y * q1h[c]);
                 if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
                 sc[t][e] = v;
                 mx[c] = fmaxf(mx[c], v);
@@ -785,22 +820,26 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             l[c] *= alpha[c];
             zs[c] *= alpha[c];
         }
-        // P' = p * v_scale (0 for masked tokens) as the B operand of PV
-        uint32_t pbf[KTT][2];
+        // P' = p * v_scale (0 for masked tokens), transposed by movmatrix:
+        // pt[t][r] gives lane (gid, tig) the P' of tokens 8r + 2tig, +1 of
+        // tile t in head column gid
+        uint32_t pt[KTT][2];
 #pragma unroll
         for (int t = 0; t < KTT; ++t)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
+                const float2 vz0 = *reinterpret_cast<const float2 *>(&meta_of(t, r, 0)->z);   // (sv, zv)
+                const float2 vz1 = HPW > 1 ? *reinterpret_cast<const float2 *>(&meta_of(t, r, 1)->z) : vz0;
                 const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
                 const float p1 = NC > 1 ? exp2_approx(sc[t][2 * r + 1] - m[1]) : 0.0f;
                 l[0] += p0;
                 if (NC > 1) l[1] += p1;
                 float q0, q1;
-                const uint32_t w = pack_f16(ok ? p0 * sv[t][r] : 0.0f, ok ? p1 * sv[t][r] : 0.0f, q0, q1);
-                zs[0] += q0 * zv[t][r];
-                if (NC > 1) zs[1] += q1 * zv[t][r];
-                pbf[t][r] = ptx::movmatrix_trans(w);
+                const uint32_t w = pack_f16(ok ? p0 * vz0.x : 0.0f, ok ? p1 * vz1.x : 0.0f, q0, q1);
+                zs[0] += q0 * vz0.y;
+                if (NC > 1) zs[1] += q1 * vz1.y;
+                pt[t][r] = ptx::movmatrix_trans(w);
             }
         if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
@@ -813,43 +852,66 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 }
             }
         }
-        // ---- O^T += V'^T P'^T with V converted straight into A
-        // fragments: lane (gid, tig) owns codes 16gid .. 16gid+15 (row
-        // bytes 6gid .. 6gid+5) of tokens 2tig, 2tig+1 (k = 2tig, 2tig+1)
-        // and 2tig+8, 2tig+9; tile md holds codes 2md (row gid) and
-        // 2md+1 (row gid+8) of the slices.  X / Y are slice bytes 0-3 / 2-5.
+        // ---- O^T += V'^T P'^T with V converted straight into A fragments:
+        // lane (gid, tig) owns codes 16gid .. 16gid+15 (row bytes 6gid ..
+        // 6gid+5) of two token rows ra0, ra0+1 of head ha (k = 2tig, 2tig+1)
+        // and two rows rb0, rb0+1 of head hb (k = 2tig+8, 2tig+9); tile md
+        // holds codes 2md (row gid) and 2md+1 (row gid+8) of the slices.
+        // X / Y are slice bytes 0-3 / 2-5.  One pass per 16 tokens (HPW 1:
+        // one head, tokens 2tig.. and 2tig+8..), else block-diagonal passes
+        // in which the k range is split between heads: HPW 2, pass r: k < 8
+        // head 0, k >= 8 head 1, tokens 8r + 2tig, +1; HPW 4, pass (r, j):
+        // quarter i of k (4 tokens) is head (i ^ j) for i < 2, 2 + ((i-2) ^ j)
+        // above, tokens 8r + 2tig, +1.  The B operand of a pass is pt[t][r]
+        // kept only in the columns of the heads it pairs with each k.
         const int sxy = 16 * (gid & 1);
+        constexpr int NP = HPW == 1 ? 1 : HPW;   // passes per 16-token tile
 #pragma unroll
         for (int kt = 0; kt < KTT; ++kt) {
-            const uint32_t vlane = kpk(kt) + L.tile_bytes + ((6 * gid) & ~3);   // packed V rows
-            uint32_t X[4], Y[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = 2 * tig + (i & 1) + 8 * (i >> 1);
-                const uint32_t w0 = ld_shared_u32(vlane + tok * T::ROW);
-                const uint32_t w1 = ld_shared_u32(vlane + tok * T::ROW + 4);
-                X[i] = __funnelshift_r(w0, w1, sxy);
-                Y[i] = __funnelshift_rc(w0, w1, sxy + 16);
-            }
-            uint32_t win[2][6];
+            for (int ps = 0; ps < NP; ++ps) {
+                const int r = HPW == 4 ? (ps >> 1) : ps;
+                const int j = HPW == 4 ? (ps & 1) : 0;
+                int ha = 0, hb = 0, ra0 = 2 * tig, rb0 = 2 * tig + 8;
+                uint32_t b0 = pt[kt][0], b1 = pt[kt][1];
+                if constexpr (HPW > 1) {
+                    ha = HPW == 2 ? 0 : ((tig >> 1) ^ j);
+                    hb = HPW == 2 ? 1 : 2 + ((tig >> 1) ^ j);
+                    ra0 = rb0 = 8 * r + 2 * tig;
+                    b0 = gid == ha ? pt[kt][r] : 0u;
+                    b1 = gid == hb ? pt[kt][r] : 0u;
+                }
+                const uint32_t va = kpk(kt, ha) + L.tile_bytes + ((6 * gid) & ~3);   // packed V rows
+                const uint32_t vb = kpk(kt, hb) + L.tile_bytes + ((6 * gid) & ~3);
+                uint32_t X[4], Y[4];
 #pragma unroll
-            for (int tp = 0; tp < 2; ++tp) {
-                win[tp][0] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x5410u);
-                win[tp][1] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x6521u);
-                win[tp][2] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x7632u);
-                win[tp][3] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x6521u);
-                win[tp][4] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7632u);
-                win[tp][5] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7733u);
-            }
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t ra = (i < 2 ? va + ra0 * T::ROW : vb + rb0 * T::ROW) + (i & 1) * T::ROW;
+                    const uint32_t w0 = ld_shared_u32(ra);
+                    const uint32_t w1 = ld_shared_u32(ra + 4);
+                    X[i] = __funnelshift_r(w0, w1, sxy);
+                    Y[i] = __funnelshift_rc(w0, w1, sxy + 16);
+                }
+                uint32_t win[2][6];
 #pragma unroll
-            for (int md = 0; md < T::DT / 2; ++md) {
-                constexpr uint32_t kMask3 = 0x00070007u;
-                uint32_t a[4];
-                a[0] = win[0][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
-                a[1] = win[0][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
-                a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
-                a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
-                ptx::mma16816<false>(o[md], a, pbf[kt][0], pbf[kt][1]);
+                for (int tp = 0; tp < 2; ++tp) {
+                    win[tp][0] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x5410u);
+                    win[tp][1] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x6521u);
+                    win[tp][2] = ptx::prmt(X[2 * tp], X[2 * tp + 1], 0x7632u);
+                    win[tp][3] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x6521u);
+                    win[tp][4] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7632u);
+                    win[tp][5] = ptx::prmt(Y[2 * tp], Y[2 * tp + 1], 0x7733u);
+                }
+#pragma unroll
+                for (int md = 0; md < T::DT / 2; ++md) {
+                    constexpr uint32_t kMask3 = 0x00070007u;
+                    uint32_t a[4];
+                    a[0] = win[0][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
+                    a[1] = win[0][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
+                    a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
+                    a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
+                    ptx::mma16816<false>(o[md], a, b0, b1);
+                }
             }
         }
     };
@@ -1053,10 +1115,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             }
         }
         if constexpr (T::kIsU3) {
-            // 16-token blocks go two at a time when the next unit continues
-            // the sequence: the per-block softmax, barrier and walk work is
-            // then shared by 32 tokens
-            const bool pair = BS == 16 && x + 1 < hi && j + 1 < nblk[b];
+            // 16-token blocks of one kv head per warp go two at a time when
+            // the next unit continues the sequence: the per-block softmax,
+            // barrier and walk work is then shared by 32 tokens (warps of
+            // several heads share it between their heads instead, and keep
+            // one block per step so that more of the ring is in flight)
+            const bool pair = BS == 16 && HPW == 1 && x + 1 < hi && j + 1 < nblk[b];
             if (pair) {
                 const int s1 = cs;
                 if (!ptx::mbar_wait_bounded(bar_full + 8 * s1, cphase, kTimeoutNs)) {
@@ -1276,11 +1340,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeParams p,
         orow[EPL * lane + e] = p.q_is_bf16 ? f2h<kBF16>(acc[e]) : f2h<kF16>(acc[e]);
 }
 
-template <int CK, int D, int BS, bool G1 = false, bool GSC = false, bool XV = false>
+template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false>
 cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                           const CUtensorMap &mv, cudaStream_t s)
 {
-    auto kern = decode_tma_kernel<CK, D, BS, G1, GSC, XV>;
+    auto kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV>;
     // dynamic shared memory limit, raised once per device as needed
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
@@ -1292,7 +1356,7 @@ cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUte
         if (e != cudaSuccess) return e;
         configured[dev].store(f.smem_bytes, std::memory_order_relaxed);
     }
-    e = launch_pdl(kern, dim3(f.grid), dim3(((f.nh << f.wsh) + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
+    e = launch_pdl(kern, dim3(f.grid), dim3((f.ncons + 1) * 32), f.smem_bytes, s, mk, mv, p, f);
     if (e != cudaSuccess) return e;
     const int rows = p.batch * p.num_heads;
     return launch_pdl(merge_kernel<D>, dim3((rows + kMergeWarps - 1) / kMergeWarps), dim3(32 * kMergeWarps),

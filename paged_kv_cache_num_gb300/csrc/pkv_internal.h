@@ -131,8 +131,13 @@ struct FastParams {
     int smem_bytes;
     int meta_heads;             // 3-bit: kv heads whose scale/zero runs a stage holds
                                 // (nh when the arrays are head-major, else all)
+    int meta_hmaj;              // 3-bit: 1 when the scale/zero arrays are head-major
+                                // ([blocks][kv heads][slots]), 0 when slot-major
     int xv_bulk;                // x-vectorised cache whose nh head tiles of a block are
                                 // one contiguous run: staged by 1-D bulk copies
+    int hpw;                    // 3-bit multi-head caches: kv heads per consumer warp
+                                // (1, 2 or 4); 1 otherwise
+    int ncons;                  // consumer warps per CTA
     float *part_ml;             // [(grid + n_hg*B) * nh * G, 2]
     float *part_acc;            // [(grid + n_hg*B) * nh * G, D]
 };
