@@ -115,7 +115,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
 // Choose heads per CTA, stages and grid for the fast kernel.
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
                int cache_kind, bool meta_head_major, int sm_count, FastParams &f, size_t &workspace,
-               int q8_scales_per_head)
+               int q8_scales_per_head, int u3_tiles)
 {
     const bool u3 = cache_kind == kU3;
     const int es = is_q8(cache_kind) ? 1 : 2;
@@ -143,21 +143,29 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // staged fp8 / int8 granular scales: K and V runs of nh * q8_scales_per_head
     // fp32, each a multiple of 16 bytes for the bulk copies
     if (q8_scales_per_head > 0 && (4 * nh * q8_scales_per_head) % 16 != 0) return false;
-    // 3-bit: the staged scale / zero runs plus room for their fp32
-    // conversion (16 bytes per (head, slot)); fp8 / int8: the staged
+    // 3-bit: the staged scale / zero runs, and (outside the ring) each
+    // consumer warp's fp32 conversion of them; fp8 / int8: the staged
     // granular scales
-    const int meta = u3 ? 6 * block_size * meta_heads + 16 * nh * block_size : 8 * nh * q8_scales_per_head;
-    while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > 192 * 1024 / ctas_per_sm ||
-                          smem_layout(nh, block_size, row, stages, batch, meta).total > budget))
+    const int meta = u3 ? 6 * block_size * meta_heads : 8 * nh * q8_scales_per_head;
+    const int ncons = hpw > 1 ? nh / hpw : nh << wsh;
+    const int conv = u3 ? ncons * u3_conv_bytes_per_warp(hpw, block_size) : 0;
+    // bytes a CTA keeps in its ring: at most 192 KB per SM, except for the
+    // 3-bit multi-head CTAs, which hold one block per step and use what the
+    // shared memory allows
+    const int ring_cap = u3 && hpw > 1 ? budget : 192 * 1024 / ctas_per_sm;
+    if (!u3) u3_tiles = 0;
+    while (stages > 2 && (stages * (2 * nh * block_size * row + meta) > ring_cap ||
+                          smem_layout(nh, block_size, row, stages, batch, meta, conv).total > budget))
         --stages;
-    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, meta);
+    const SmemLayout L = smem_layout(nh, block_size, row, stages, batch, meta, conv);
     if (L.total > budget) return false;
     const int n_hg = num_kv_heads / nh;
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
     f.nh = nh;
     f.wsh = wsh;
     f.hpw = hpw;
-    f.ncons = hpw > 1 ? nh / hpw : nh << wsh;
+    f.ncons = ncons;
+    f.u3_tiles = u3_tiles;
     f.n_hg = n_hg;
     f.stages = stages;
     const int64_t slots = int64_t(sm_count) * ctas_per_sm;

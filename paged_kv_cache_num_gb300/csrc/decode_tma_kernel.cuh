@@ -61,14 +61,14 @@ constexpr int kMaxDevices = 64;
 #define NEG_INF (-__int_as_float(0x7f800000))
 
 struct SmemLayout {
-    int tile_bytes, meta_bytes, stage_bytes, bars_off, ok_off, prefix_off, nblk_off, total;
+    int tile_bytes, meta_bytes, stage_bytes, conv_off, bars_off, ok_off, prefix_off, nblk_off, total;
 };
 
-// [stages x (K tile, V tile, 3-bit metadata of the whole block + its fp32
-// conversion)]
+// [stages x (K tile, V tile, staged scales / 3-bit metadata of the block)]
+// [3-bit: each consumer warp's fp32 conversion of its heads' metadata]
 // [mbarriers] [per-stage block ids] [prefix sums] [block counts]
 __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes, int stages,
-                                                  int batch, int meta_bytes = 0)
+                                                  int batch, int meta_bytes = 0, int conv_bytes = 0)
 {
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
@@ -80,7 +80,8 @@ __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes,
     // scales / metadata can leave a stage unaligned.)
     const int align = row_bytes % 128 == 0 ? 1024 : 128;
     L.stage_bytes = (2 * L.tile_bytes + meta_bytes + align - 1) / align * align;
-    L.bars_off = stages * L.stage_bytes;
+    L.conv_off = stages * L.stage_bytes;
+    L.bars_off = L.conv_off + (conv_bytes + 15) / 16 * 16;
     L.ok_off = L.bars_off + 2 * stages * 8;
     L.prefix_off = L.ok_off + stages * 4;
     L.nblk_off = L.prefix_off + (batch + 1) * 4;
@@ -248,6 +249,12 @@ constexpr int kCtasPerSm = CK == kU3 ? (U3H >= 2 ? kU3MhaCtasPerSm : kU3CtasPerS
 template <int CK>
 constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
 
+// fp32 conversion area of a 3-bit consumer warp: (sk, zk, sv, zv) per
+// (head, token) of the HPW heads and the tokens of one step (two 16-token
+// blocks when one-head warps pair them)
+__host__ __device__ constexpr int u3_conv_tokens(int hpw, int bs) { return hpw == 1 && bs == 16 ? 32 : bs; }
+__host__ __device__ constexpr int u3_conv_bytes_per_warp(int hpw, int bs) { return 16 * hpw * u3_conv_tokens(hpw, bs); }
+
 // U3H: 3-bit multi-head caches (one q head per kv head).  0: grouped q
 // heads (the head columns of a warp are the q heads of one kv head).  1: one
 // kv head per consumer warp, whose second head column never exists.  2 or 4:
@@ -279,11 +286,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // the CTA's heads for the block, [nh] or [nh][BS] fp32 each.
     const int GS = p.scale_mode == 2 ? BS : 1;        // staged scales per head
     constexpr bool gscale = T::kFp8 && GSC;
-    // 3-bit: the raw metadata as staged (copied), then room for its fp32
-    // conversion (sk, zk, sv, zv per (head, slot), written by the consumers)
+    // 3-bit: the raw metadata as staged (copied); its fp32 conversion
+    // (sk, zk, sv, zv per (head, token), written and read by each consumer
+    // warp for its own heads) sits after the ring
     const int raw_meta = T::kIsU3 ? 6 * BS * f.meta_heads : (gscale ? 8 * nh * GS : 0);
-    const int meta_bytes = raw_meta + (T::kIsU3 ? 16 * nh * BS : 0);
-    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes);
+    const int meta_bytes = raw_meta;
+    const int conv_bytes = T::kIsU3 ? f.ncons * u3_conv_bytes_per_warp(HPW, BS) : 0;
+    const SmemLayout L = smem_layout(nh, BS, T::ROW, stages, B, meta_bytes, conv_bytes);
+    // bytes the copies of one stage bring (tiles + staged scales / metadata)
+    const uint32_t stage_tx = uint32_t(2 * L.tile_bytes + raw_meta);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar_full = sbase + L.bars_off, bar_empty = bar_full + 8 * stages;
     volatile int *stage_pb = reinterpret_cast<volatile int *>(smem + L.ok_off);   // block id or -1
@@ -389,7 +400,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         const uint32_t vdst = kdst + L.tile_bytes;
                         stage_pb[s] = pbk;
                         if (pbk >= 0) {
-                            ptx::mbar_arrive_expect_tx(fb, uint32_t(2 * L.tile_bytes + raw_meta));
+                            ptx::mbar_arrive_expect_tx(fb, stage_tx);
                             if constexpr (XV) {
                                 if (f.xv_bulk) {   // the heads' tiles: one run each of K and V
                                     const int64_t off = int64_t(pbk) * p.c_blk + int64_t(hgk) * nh * p.c_head;
@@ -404,8 +415,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                                 for (int h = 0; h < T::HALVES; ++h) {
                                     const int half_bytes = L.tile_bytes / T::HALVES;
                                     if constexpr (T::kIsU3) {
-                                        ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
-                                        ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                        if (f.u3_tiles == 1) {
+                                            // the nh heads' tiles are one run
+                                            const int64_t off = int64_t(pbk) * p.c_blk + int64_t(hgk) * nh * p.c_head;
+                                            ptx::bulk_load(kdst, p.k_cache + off, uint32_t(L.tile_bytes), fb);
+                                            ptx::bulk_load(vdst, p.v_cache + off, uint32_t(L.tile_bytes), fb);
+                                        } else {
+                                            ptx::tma_load_4d(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                            ptx::tma_load_4d(vdst + h * half_bytes, &tmv, fb, h * T::BOX0, 0, hgk * nh, pbk);
+                                        }
                                     } else {
                                         ptx::tma_load_4d_hint(kdst + h * half_bytes, &tmk, fb, h * T::BOX0, 0,
                                                               hgk * nh, pbk, once);
@@ -714,12 +732,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         constexpr int NT = NB * BS;              // tokens of the NB blocks
         const int kvh = hg * nh + kvl;
         const bool partial = valid < NT;
+        // shared-memory strides of the staged rows ([head][slot][row]):
+        // between heads and between slots
+        constexpr int hs = BS * T::ROW, ts = T::ROW;
         // stage of tile t, and the tile's first row within its block
         auto tile_stage = [&](int t) { return t < T::KT ? s0 : s1; };
         auto tile_row = [&](int t) { return 16 * (t % T::KT); };
         // packed K rows of tile t of the warp's head hh (shared address)
         auto kpk = [&](int t, int hh) {
-            return sbase + tile_stage(t) * L.stage_bytes + (kvl + hh) * BS * T::ROW + tile_row(t) * T::ROW;
+            return sbase + tile_stage(t) * L.stage_bytes + (kvl + hh) * hs + tile_row(t) * ts;
         };
         // ---- metadata: the warp converts each (head, token) of its HPW
         // heads and the NB blocks to fp32 (sk, zk, sv, zv) in the stage's
@@ -729,9 +750,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         // runs (head-major) or [BS][num_kv_heads] arrays.
         const int MH = f.meta_heads;
         const bool hmaj = f.meta_hmaj != 0;
-        auto conv_area = [&](int st) {
-            return reinterpret_cast<float4 *>(smem + (st * L.stage_bytes + 2 * L.tile_bytes + raw_meta));
-        };
+        // this warp's conversion area: entry (head hh, token tk of the NB
+        // blocks) at hh * NTM + tk
+        constexpr int NTM = u3_conv_tokens(HPW, BS);
+        static_assert(NT <= NTM, "conversion area");
+        float4 *cw = reinterpret_cast<float4 *>(smem + L.conv_off) + warp * HPW * NTM;
+        __syncwarp();    // the previous step's reads of the area are done
 #pragma unroll
         for (int i0 = 0; i0 < HPW * NT; i0 += 32) {
             const int i = i0 + lane;
@@ -744,7 +768,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const uint8_t *mkz = raw + 4 * BS * MH;
                 const uint8_t *mvz = mkz + BS * MH;
                 const int k = hmaj ? (kvl + hh) * BS + slot : slot * MH + kvh + hh;
-                conv_area(st)[(kvl + hh) * BS + slot] =
+                cw[hh * NTM + tk] =
                     make_float4(__half2float(mks[k]), float(mkz[k]), __half2float(mvs[k]), float(mvz[k]));
             }
         }
@@ -754,7 +778,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             // HPW 4: lanes tig 0, 1 hold columns 0-3; lanes tig 2, 3 hold
             // none and read an in-range entry
             const int hc = HPW == 1 ? 0 : (HPW == 2 ? c : ((2 * tig + c) & 3));
-            return conv_area(tile_stage(t)) + (kvl + hc) * BS + tile_row(t) + gid + 8 * r;
+            return cw + hc * NTM + 16 * t + gid + 8 * r;
         };
         // ---- S^T = K Q'^T with K converted straight into A fragments:
         // lane (gid, tig) takes group tig of token rows gid and gid+8.  With
@@ -768,8 +792,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int hh = 0; hh < HPW; ++hh) {
                 float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
-                const uint32_t a0 = kpk(mt, hh) + gid * T::ROW + 12 * tig;
-                const uint32_t a1 = a0 + 8 * T::ROW;
+                const uint32_t a0 = kpk(mt, hh) + gid * ts + 12 * tig;
+                const uint32_t a1 = a0 + 8 * ts;
                 const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
                 const uint32_t y0 = ld_shared_u32(a1), y1 = ld_shared_u32(a1 + 4), y2 = ld_shared_u32(a1 + 8);
 #pragma unroll
@@ -886,7 +910,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 uint32_t X[4], Y[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint32_t ra = (i < 2 ? va + ra0 * T::ROW : vb + rb0 * T::ROW) + (i & 1) * T::ROW;
+                    const uint32_t ra = (i < 2 ? va + ra0 * ts : vb + rb0 * ts) + (i & 1) * ts;
                     const uint32_t w0 = ld_shared_u32(ra);
                     const uint32_t w1 = ld_shared_u32(ra + 4);
                     X[i] = __funnelshift_r(w0, w1, sxy);
@@ -1134,7 +1158,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int spb1 = stage_pb[s1];
                 const int valid1 = min(BS, ctx_b - (j + 1) * BS);
                 if (spb >= 0 && spb1 >= 0) {
-                    u3_body(std::integral_constant<int, 2>{}, s, s1, BS + valid1);
+                    // (only one-head warps pair blocks, of 16 tokens)
+                    u3_body(std::integral_constant<int, HPW == 1 && BS == 16 ? 2 : 1>{}, s, s1, BS + valid1);
                 } else {
                     if (spb >= 0) u3_body(std::integral_constant<int, 1>{}, s, s, valid);
                     if (spb1 >= 0) u3_body(std::integral_constant<int, 1>{}, s1, s1, valid1);

@@ -510,10 +510,18 @@ int check_decode_common(const pkv_tensor *q, const pkv_cache *cache, const pkv_t
                       (ci.block_size % 16) == 0 && aligned(p.k_qs, 16) && aligned(p.v_qs, 16) &&
                       aligned(p.k_qz, 16) && aligned(p.v_qz, 16);
         }
+        // 3-bit K / V tiles by one bulk copy each where the CTA's heads'
+        // tiles are one run ([block][head][slot][row], the dual-stacked
+        // layout); else 4-D tensor copies
+        int u3_tiles = 0;
+        if (ci.kind == PKV_DTYPE_U3 && aligned(p.k_cache, 16) && aligned(p.v_cache, 16) && p.c_blk % 16 == 0) {
+            const int64_t row = 3 * int64_t(p.head_dim) / 8;
+            if (p.c_slot == row && p.c_head == row * p.block_size) u3_tiles = 1;
+        }
         pkv::FastParams f{};
         size_t ws = 0;
         if (q_ok && meta_ok && pkv::plan_fast(p.batch, p.num_heads, p.num_kv_heads, p.head_dim, p.block_size, p.max_blocks,
-                                   ci.kind, meta_hmaj, sm, f, ws, q8_gs) &&
+                                   ci.kind, meta_hmaj, sm, f, ws, q8_gs, u3_tiles) &&
             pkv::fast_maps_encodable(p, ci.kind, f.nh)) {
             dc.plan.kernel = 1;
             dc.plan.fast = f;

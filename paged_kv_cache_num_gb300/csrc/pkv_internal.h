@@ -138,6 +138,9 @@ struct FastParams {
     int hpw;                    // 3-bit multi-head caches: kv heads per consumer warp
                                 // (1, 2 or 4); 1 otherwise
     int ncons;                  // consumer warps per CTA
+    int u3_tiles;               // 3-bit K / V tiles ([head][slot][row] in shared
+                                // memory): 0 by 4-D tensor copies; 1 by one bulk
+                                // copy per tile (heads stored [block][head][slot][row])
     float *part_ml;             // [(grid + n_hg*B) * nh * G, 2]
     float *part_acc;            // [(grid + n_hg*B) * nh * G, D]
 };
@@ -156,7 +159,7 @@ DecodePlan plan_decode_general(int batch, int num_heads, int num_kv_heads, int h
 bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch);
 bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
                int max_blocks, int cache_kind, bool meta_head_major, int sm_count, FastParams &f,
-               size_t &workspace, int q8_scales_per_head = 0);
+               size_t &workspace, int q8_scales_per_head = 0, int u3_tiles = 0);
 bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh);
 // x-vectorised caches (c_chunk != 16): 16-bit or one-byte codes with
 // per-head scales, head_dim 128 (16-bit also 64), block size 16 / 32 / 64
