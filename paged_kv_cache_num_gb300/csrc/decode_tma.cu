@@ -83,16 +83,26 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
     if constexpr (is_q8(CK)) {      // per-block / per-token scales staged with the tiles
         if (p.scale_mode != 0) {
             switch (p.block_size) {
-            case 16: return launch_fast_t<CK, D, 16, 0, true>(p, f, mk, mv, s);
-            case 32: return launch_fast_t<CK, D, 32, 0, true>(p, f, mk, mv, s);
+            case 16:
+                return f.ng == 2 ? launch_fast_t<CK, D, 16, 0, true, false, 2>(p, f, mk, mv, s)
+                                 : launch_fast_t<CK, D, 16, 0, true>(p, f, mk, mv, s);
+            case 32:
+                return f.ng == 2 ? launch_fast_t<CK, D, 32, 0, true, false, 2>(p, f, mk, mv, s)
+                                 : launch_fast_t<CK, D, 32, 0, true>(p, f, mk, mv, s);
             case 64: return launch_fast_t<CK, D, 64, 0, true>(p, f, mk, mv, s);
             default: return cudaErrorInvalidValue;
             }
         }
     }
     switch (p.block_size) {
-    case 16: return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
-    case 32: return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
+    case 16:
+        if constexpr (CK != kU3)
+            if (f.ng == 2) return launch_fast_t<CK, D, 16, 0, false, false, 2>(p, f, mk, mv, s);
+        return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
+    case 32:
+        if constexpr (CK != kU3)
+            if (f.ng == 2) return launch_fast_t<CK, D, 32, 0, false, false, 2>(p, f, mk, mv, s);
+        return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
     case 64:
         if constexpr (CK != kU3) return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
         return cudaErrorInvalidValue;
@@ -105,8 +115,10 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
 bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int group, int batch)
 {
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
-    // groups of up to 16 q heads: two consumer warps per kv head above 8
+    // groups of up to 16 q heads (two groups of head columns per consumer
+    // warp above 8, for blocks of up to 32 slots)
     if (group > (cache_kind == kU3 ? 8 : 16) || batch > 4096) return false;
+    if (group > 8 && block_size > 32) return false;
     if (is_q8(cache_kind)) return head_dim == 128;
     if (cache_kind == kU3) return head_dim == 128 && block_size <= 32;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
@@ -121,14 +133,14 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const int es = is_q8(cache_kind) ? 1 : 2;
     const int row = u3 ? 3 * head_dim / 8 : head_dim * es;
     const int group = num_heads / num_kv_heads;
-    // consumer warps per kv head: 2 for groups above 8 q heads (8 each);
-    // the CTA keeps at most 8 consumer warps
-    const int wsh = group > 8 ? 1 : 0;
+    // one consumer warp per kv head (at most 8 per CTA), with two groups of
+    // 8 head columns for groups above 8 q heads
+    const int ng = !u3 && group > 8 ? 2 : 1;
     // 3-bit multi-head caches: up to 4 kv heads per consumer warp (a power
     // of two dividing num_kv_heads)
     int hpw = 1;
     if (u3 && group == 1) hpw = num_kv_heads % 4 == 0 ? 4 : (num_kv_heads % 2 == 0 ? 2 : 1);
-    int nh = u3 ? (hpw > 1 ? kU3MhaHeads : kU3Heads) : (8 >> wsh);
+    int nh = u3 ? (hpw > 1 ? kU3MhaHeads : kU3Heads) : 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
     while (nh % hpw != 0) hpw >>= 1;
@@ -147,7 +159,7 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // consumer warp's fp32 conversion of them; fp8 / int8: the staged
     // granular scales
     const int meta = u3 ? 6 * block_size * meta_heads : 8 * nh * q8_scales_per_head;
-    const int ncons = hpw > 1 ? nh / hpw : nh << wsh;
+    const int ncons = hpw > 1 ? nh / hpw : nh;
     const int conv = u3 ? ncons * u3_conv_bytes_per_warp(hpw, block_size) : 0;
     // bytes a CTA keeps in its ring: at most 192 KB per SM, except for the
     // 3-bit multi-head CTAs, which hold one block per step and use what the
@@ -162,7 +174,7 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const int n_hg = num_kv_heads / nh;
     const int64_t max_units = int64_t(n_hg) * batch * max_blocks;
     f.nh = nh;
-    f.wsh = wsh;
+    f.ng = ng;
     f.hpw = hpw;
     f.ncons = ncons;
     f.u3_tiles = u3_tiles;

@@ -265,7 +265,11 @@ __host__ __device__ constexpr int u3_conv_bytes_per_warp(int hpw, int bs) { retu
 // one softmax and one walk of the ring serve HPW heads.
 // GSC: fp8 / int8 with per-block or per-token scales, staged per block.
 // XV: x-vectorised cache layout (16-bit and one-byte codes).
-template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false>
+// NG: head-column groups per consumer warp (16-bit and one-byte caches).
+// With NG = 2 a warp serves the up to 16 q heads of its kv head as two
+// groups of 8 columns: every K / V fragment, loaded and converted once,
+// feeds one MMA per group.
+template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
 __global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H>))
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeParams p, FastParams f)
@@ -274,6 +278,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     constexpr int NC = U3H == 1 ? 1 : 2;   // head columns (2tig, 2tig+1) that can exist
     constexpr int HPW = U3H >= 2 ? U3H : 1;  // kv heads per consumer warp
     static_assert(HPW == 1 || (T::kIsU3 && (HPW == 2 || HPW == 4)), "heads per warp");
+    static_assert(NG == 1 || (NG == 2 && !T::kIsU3 && BS <= 32), "head-column groups");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -467,15 +472,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 
     // ======================================================== consumer warps
-    // Consumer warp w serves kv head kvl = w >> wsh of the CTA's group and,
-    // of its G q heads, the 8 (or fewer) from qh0 = 8 (w & (2^wsh - 1)):
-    // with groups of up to 8 q heads one warp per kv head, with up to 16
-    // two warps reading the same K / V tiles.  With HPW > 1 (3-bit,
-    // multi-head) warp w serves kv heads kvl .. kvl + HPW - 1, kvl = HPW w,
-    // head column j being kv head kvl + j.
-    const int kvl = HPW > 1 ? HPW * warp : warp >> f.wsh;
-    const int qh0 = HPW > 1 ? 0 : 8 * (warp & ((1 << f.wsh) - 1));
-    const int GW = HPW > 1 ? HPW : min(8, G - qh0);   // head columns of this warp
+    // Consumer warp w serves kv head kvl = w of the CTA's group and its G q
+    // heads: head column n of group g (NG groups of 8) is q head 8g + n.
+    // With HPW > 1 (3-bit, multi-head) warp w serves kv heads kvl .. kvl +
+    // HPW - 1, kvl = HPW w, head column j being kv head kvl + j.
+    const int kvl = HPW > 1 ? HPW * warp : warp;
+    const int GW = HPW > 1 ? HPW : min(8 * NG, G);   // head columns of this warp
     // Tokens on the MMA's M dimension, this warp's q heads on N (<= 8):
     //   S^T[tok][head] = K[tok][:] . Q[head][:]        (A = K, B = Q^T)
     //   O^T[d][head]  += V^T[d][tok] P^T[tok][head]     (A = V^T, B = P^T)
@@ -516,6 +518,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // running sum of P' * zero of the PV operand; int8, 1152 sum(q') and the
     // running sum of P' (the operands' 1152 offsets)
     float q1h[2] = {0.0f, 0.0f}, zs[2] = {0.0f, 0.0f};
+    // the same for the second group of head columns (NG = 2)
+    constexpr int NG1 = NG > 1 ? 1 : 0;
+    uint32_t qb1[NG1 ? T::QK : 1][2];
+    float o1[NG1 ? T::DT / 2 : 1][4];
+    float m1[2], l1[2];
+    float q1h1[2] = {0.0f, 0.0f}, zs1[2] = {0.0f, 0.0f};
 
     auto start_segment = [&]() {
         const int kvh = hg * nh + kvl;
@@ -523,11 +531,13 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const int cb = p.context_lens[b * p.cl_stride];
             ctx_b = cb < 0 ? 0 : (cb > cap ? cap : cb);
         }
-        const bool hv = gid < GW;  // this lane's B column (q head qh0 + gid) exists
-        // column gid: q head qh0 + gid of kv head kvh, or (HPW > 1) the q
-        // head of kv head kvh + gid
-        const int qhead = HPW > 1 ? (kvh + gid) * G : kvh * G + qh0 + gid;
+        const bool hv = gid < GW;  // this lane's B column (q head gid) exists
+        const bool hv1 = NG1 && 8 + gid < GW;   // ... and that of the second group
+        // column gid: q head gid of kv head kvh, or (HPW > 1) the q head of
+        // kv head kvh + gid; second group: q head 8 + gid
+        const int qhead = HPW > 1 ? (kvh + gid) * G : kvh * G + gid;
         const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + qhead * p.q_h);
+        const uint16_t *qr1 = reinterpret_cast<const uint16_t *>(p.q + b * p.q_b + (qhead + 8) * p.q_h);
         if constexpr (T::kIsU3) {
             // q' = q qs 2^(1-x) (f16, exact) in the pair order of the K
             // fragments: k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1)
@@ -585,6 +595,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int d = 16 * kk + 2 * tig;
                 qb[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qr + d) : 0u;
                 qb[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qr + d + 8) : 0u;
+                if constexpr (NG1) {
+                    qb1[kk][0] = hv1 ? *reinterpret_cast<const uint32_t *>(qr1 + d) : 0u;
+                    qb1[kk][1] = hv1 ? *reinterpret_cast<const uint32_t *>(qr1 + d + 8) : 0u;
+                }
             }
             mult = log2e_scale;
             vmul = 1.0f;
@@ -593,44 +607,50 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             // fragments: k-step kk, lane tig holds d = 16kk + 4tig + {0,1}
             // (k = 2tig, 2tig+1) and + {2,3} (k = 2tig+8, 2tig+9).  A
             // power-of-two pre-scale keeps every element inside f16 range.
-            float f[T::QK][4];
+            float f[NG][T::QK][4];
             float amax = 0.0f;
 #pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                uint2 u = make_uint2(0, 0);
-                if (hv) u = *reinterpret_cast<const uint2 *>(qr + 16 * kk + 4 * tig);
-                const uint32_t w[2] = {u.x, u.y};
+            for (int g = 0; g < NG; ++g)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    if (p.q_is_bf16) {
-                        f[kk][2 * e] = __uint_as_float(w[e] << 16);
-                        f[kk][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                    } else {
-                        const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-                        f[kk][2 * e] = t.x;
-                        f[kk][2 * e + 1] = t.y;
+                for (int kk = 0; kk < T::QK; ++kk) {
+                    uint2 u = make_uint2(0, 0);
+                    if (g == 0 ? hv : hv1) u = *reinterpret_cast<const uint2 *>((g == 0 ? qr : qr1) + 16 * kk + 4 * tig);
+                    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (p.q_is_bf16) {
+                            f[g][kk][2 * e] = __uint_as_float(w[e] << 16);
+                            f[g][kk][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+                        } else {
+                            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                            f[g][kk][2 * e] = t.x;
+                            f[g][kk][2 * e + 1] = t.y;
+                        }
+                        amax = fmaxf(amax, fmaxf(fabsf(f[g][kk][2 * e]), fabsf(f[g][kk][2 * e + 1])));
                     }
-                    amax = fmaxf(amax, fmaxf(fabsf(f[kk][2 * e]), fabsf(f[kk][2 * e + 1])));
                 }
-            }
 #pragma unroll
             for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
             float qs = 1.0f;
             while (amax * qs > 16384.0f) qs *= 0.5f;
-            float d0, d1, d2, d3, c0 = 0.0f;
 #pragma unroll
-            for (int kk = 0; kk < T::QK; ++kk) {
-                qb[kk][0] = pack_f16(f[kk][0] * qs, f[kk][1] * qs, d0, d1);
-                qb[kk][1] = pack_f16(f[kk][2] * qs, f[kk][3] * qs, d2, d3);
-                c0 += (d0 + d1) + (d2 + d3);
-            }
-            if constexpr (CK == kI8) {     // sum of q' over head_dim, per q head gid
-                c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
-                c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
+            for (int g = 0; g < NG; ++g) {
+                float d0, d1, d2, d3, c0 = 0.0f;
+                uint32_t (*qg)[2] = g == 0 ? qb : qb1;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {   // head columns 2tig, 2tig+1
-                    q1h[c] = kI8Bias * __shfl_sync(0xffffffffu, c0, 4 * (2 * tig + c));
-                    zs[c] = 0.0f;
+                for (int kk = 0; kk < T::QK; ++kk) {
+                    qg[kk][0] = pack_f16(f[g][kk][0] * qs, f[g][kk][1] * qs, d0, d1);
+                    qg[kk][1] = pack_f16(f[g][kk][2] * qs, f[g][kk][3] * qs, d2, d3);
+                    c0 += (d0 + d1) + (d2 + d3);
+                }
+                if constexpr (CK == kI8) {     // sum of q' over head_dim, per q head gid
+                    c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
+                    c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {   // head columns 2tig, 2tig+1
+                        (g == 0 ? q1h : q1h1)[c] = kI8Bias * __shfl_sync(0xffffffffu, c0, 4 * (2 * tig + c));
+                        (g == 0 ? zs : zs1)[c] = 0.0f;
+                    }
                 }
             }
             // per-block / per-token scales are applied per row (scores and P')
@@ -641,6 +661,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int t = 0; t < T::DT / 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
         m[0] = m[1] = NEG_INF;
         l[0] = l[1] = 0.0f;
+        if constexpr (NG1) {
+#pragma unroll
+            for (int t = 0; t < T::DT / 2; ++t) o1[t][0] = o1[t][1] = o1[t][2] = o1[t][3] = 0.0f;
+            m1[0] = m1[1] = NEG_INF;
+            l1[0] = l1[1] = 0.0f;
+        }
     };
 
     // d held by this lane for accumulator tile t, row half r (0: gid, 1: gid+8)
@@ -654,13 +680,17 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
     };
 
-    auto finish_segment = [&](int64_t seg_end) {
+    // Write the segment's result of one group of head columns (accumulators
+    // og, running max mg, sums lg, P' * zero / P' sums zsg), columns
+    // 8 g0 + 2tig + c.
+    auto finish_group = [&](int64_t seg_end, int g0, float (*og)[4], const float *mg, const float *lg,
+                            const float *zsg) {
         const int64_t unit_first = int64_t(hg) * NBT + prefix[b];
         const int64_t unit_last = unit_first + nblk[b] - 1;
         float lt[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {       // sum the partial sums over the 8 token rows (gid)
-            float v = l[c];
+            float v = lg[c];
             v += __shfl_xor_sync(0xffffffffu, v, 4);
             v += __shfl_xor_sync(0xffffffffu, v, 8);
             v += __shfl_xor_sync(0xffffffffu, v, 16);
@@ -670,7 +700,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if constexpr (T::kIsU3 || CK == kI8) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float z = zs[c];
+                float z = zsg[c];
 #pragma unroll
                 for (int o2 = 4; o2 < 32; o2 <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o2);
                 zt[c] = CK == kI8 ? kI8Bias * z : z;
@@ -679,21 +709,21 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         // accumulator entry (t, r, c) -> value of the segment's unnormalised output
         auto oval = [&](int t, int r, int c) -> float {
             if constexpr (T::kIsU3) {
-                return o[t][2 * r + c] * float(1 << (24 - u3v_x(2 * t + r))) - zt[c];
+                return og[t][2 * r + c] * float(1 << (24 - u3v_x(2 * t + r))) - zt[c];
             } else if constexpr (CK == kI8) {
-                return o[t][2 * r + c] - zt[c];
+                return og[t][2 * r + c] - zt[c];
             } else {
-                return o[t][2 * r + c];
+                return og[t][2 * r + c];
             }
         };
         const bool whole = seg_start == unit_first && seg_end == unit_last;
         const int64_t key = int64_t(blockIdx.x) + int64_t(hg) * B + b;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int g = 2 * tig + c;
+            const int g = 8 * g0 + 2 * tig + c;
             if (g >= GW) continue;
             // q head of column g, within the head group and overall
-            const int local = HPW > 1 ? (kvl + g) * G : kvl * G + qh0 + g;
+            const int local = HPW > 1 ? (kvl + g) * G : kvl * G + g;
             const int h = hg * nh * G + local;
             if (whole) {
                 const float inv = lt[c] > 0.0f ? vmul / lt[c] : 0.0f;
@@ -709,7 +739,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int64_t row = key * (int64_t(nh) * G) + local;
                 float *acc = f.part_acc + row * D;
                 if (gid == 0) {
-                    f.part_ml[2 * row] = m[c];
+                    f.part_ml[2 * row] = mg[c];
                     f.part_ml[2 * row + 1] = lt[c];
                 }
 #pragma unroll
@@ -718,6 +748,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     for (int r = 0; r < 2; ++r) acc[d_of(t, r)] = oval(t, r, c) * vmul;
             }
         }
+    };
+    auto finish_segment = [&](int64_t seg_end) {
+        finish_group(seg_end, 0, o, m, l, zs);
+        if constexpr (NG1) finish_group(seg_end, 1, o1, m1, l1, zs1);
     };
 
     // 3-bit blocks: NB (1, or 2 for 16-token blocks) consecutive blocks of
@@ -972,9 +1006,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const int half_bytes = L.tile_bytes / T::HALVES;
             const int mi = lane >> 3;    // ldmatrix: which 8x8 matrix this lane addresses
             // ---------------- S^T = K Q^T
-            float sc[T::KT][4];
+            float sc[T::KT][4], sc1[NG1 ? T::KT : 1][4];
 #pragma unroll
-            for (int t = 0; t < T::KT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.0f;
+            for (int t = 0; t < T::KT; ++t) {
+                sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.0f;
+                if constexpr (NG1) sc1[t][0] = sc1[t][1] = sc1[t][2] = sc1[t][3] = 0.0f;
+            }
 #pragma unroll
             for (int kk = 0; kk < T::QK; ++kk) {
 #pragma unroll
@@ -1005,69 +1042,77 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         a[3] = f16x2_from_q8<CK, 1>(w1);
                     }
                     ptx::mma16816<T::kBF>(sc[mt], a, qb[kk][0], qb[kk][1]);
+                    if constexpr (NG1) ptx::mma16816<T::kBF>(sc1[mt], a, qb1[kk][0], qb1[kk][1]);
                 }
             }
             // ---------------- online softmax per q head (columns), log2 units
             const bool partial = valid < BS;   // only a sequence's last block
-            float mx[2] = {NEG_INF, NEG_INF};
+            // one group of head columns: scores scg, running max mg / sums lg,
+            // int8 offsets zsg / q1g, accumulators og; P^T as the B operand of
+            // the PV product in pbg: each 8-token half of a tile (rows =
+            // tokens, cols = heads) packed and transposed in registers, giving
+            // lane (gid, tig) tokens 2tig, 2tig+1 of head gid
+            auto softmax_group = [&](float (*scg)[4], float *mg, float *lg, float *zsg, const float *q1g,
+                                     uint32_t (*pbg)[2], float (*og)[4]) {
+                float mx[2] = {NEG_INF, NEG_INF};
 #pragma unroll
-            for (int t = 0; t < T::KT; ++t) {
+                for (int t = 0; t < T::KT; ++t) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = (CK == kI8 ? sc[t][e] - q1h[e & 1] : sc[t][e]) * mult;
-                    if (T::kFp8 && gscale) v *= row_ks(16 * t + gid + 8 * (e >> 1));
-                    if (partial) {
-                        const int tok = 16 * t + gid + 8 * (e >> 1);
-                        v = tok < valid ? v : NEG_INF;
+                    for (int e = 0; e < 4; ++e) {
+                        float v = (CK == kI8 ? scg[t][e] - q1g[e & 1] : scg[t][e]) * mult;
+                        if (T::kFp8 && gscale) v *= row_ks(16 * t + gid + 8 * (e >> 1));
+                        if (partial) {
+                            const int tok = 16 * t + gid + 8 * (e >> 1);
+                            v = tok < valid ? v : NEG_INF;
+                        }
+                        scg[t][e] = v;
+                        mx[e & 1] = fmaxf(mx[e & 1], v);
                     }
-                    sc[t][e] = v;
-                    mx[e & 1] = fmaxf(mx[e & 1], v);
                 }
-            }
-            float alpha[2];
+                float alpha[2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-                const float mn = fmaxf(m[c], mx[c]);
-                alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
-                m[c] = mn;
-                l[c] *= alpha[c];
-                if constexpr (CK == kI8) zs[c] *= alpha[c];
-            }
-            // P^T as the B operand of the PV product: pack each 8-token half
-            // of a tile (rows = tokens, cols = heads) and transpose it in
-            // registers, giving lane (gid, tig) tokens 2tig, 2tig+1 of head gid.
-            uint32_t pb[T::KT][2];
+                for (int c = 0; c < 2; ++c) {
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+                    const float mn = fmaxf(mg[c], mx[c]);
+                    alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(mg[c] - mn);
+                    mg[c] = mn;
+                    lg[c] *= alpha[c];
+                    if constexpr (CK == kI8) zsg[c] *= alpha[c];
+                }
 #pragma unroll
-            for (int t = 0; t < T::KT; ++t) {
+                for (int t = 0; t < T::KT; ++t) {
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
-                    const float p1 = exp2_approx(sc[t][2 * r + 1] - m[1]);
-                    l[0] += p0;
-                    l[1] += p1;
-                    // per-block / per-token V scales fold into P' = p * scale
-                    const float vsr = T::kFp8 && gscale ? row_vs(16 * t + gid + 8 * r) : 1.0f;
-                    float q0, q1;
-                    const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0 * vsr, p1 * vsr, q0, q1);
-                    if constexpr (CK == kI8) {   // the PV operand's offset: sum of P' as rounded
-                        zs[0] += q0;
-                        zs[1] += q1;
+                    for (int r = 0; r < 2; ++r) {
+                        const float p0 = exp2_approx(scg[t][2 * r] - mg[0]);
+                        const float p1 = exp2_approx(scg[t][2 * r + 1] - mg[1]);
+                        lg[0] += p0;
+                        lg[1] += p1;
+                        // per-block / per-token V scales fold into P' = p * scale
+                        const float vsr = T::kFp8 && gscale ? row_vs(16 * t + gid + 8 * r) : 1.0f;
+                        float q0, q1;
+                        const uint32_t w = T::kBF ? pack_bf16(p0, p1, q0, q1) : pack_f16(p0 * vsr, p1 * vsr, q0, q1);
+                        if constexpr (CK == kI8) {   // the PV operand's offset: sum of P' as rounded
+                            zsg[0] += q0;
+                            zsg[1] += q1;
+                        }
+                        pbg[t][r] = ptx::movmatrix_trans(w);
                     }
-                    pb[t][r] = ptx::movmatrix_trans(w);
                 }
-            }
-            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+                if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
-                for (int t = 0; t < T::DT / 2; ++t) {
-                    o[t][0] *= alpha[0];
-                    o[t][1] *= alpha[1];
-                    o[t][2] *= alpha[0];
-                    o[t][3] *= alpha[1];
+                    for (int t = 0; t < T::DT / 2; ++t) {
+                        og[t][0] *= alpha[0];
+                        og[t][1] *= alpha[1];
+                        og[t][2] *= alpha[0];
+                        og[t][3] *= alpha[1];
+                    }
                 }
-            }
+            };
+            uint32_t pb[T::KT][2], pb1[NG1 ? T::KT : 1][2];
+            softmax_group(sc, m, l, zs, q1h, pb, o);
+            if constexpr (NG1) softmax_group(sc1, m1, l1, zs1, q1h1, pb1, o1);
             // ---------------- O^T += V^T P^T
 #pragma unroll
             for (int kt = 0; kt < T::KT; ++kt) {
@@ -1093,6 +1138,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         a[2] &= mhi;
                         a[3] &= mhi;
                         ptx::mma16816<T::kBF>(o[md], a, pb[kt][0], pb[kt][1]);
+                        if constexpr (NG1) ptx::mma16816<T::kBF>(o1[md], a, pb1[kt][0], pb1[kt][1]);
                     }
                 } else {
                     const int t0 = 16 * kt + 2 * tig;
@@ -1133,6 +1179,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             a[2] = f16x2_from_q8<CK, 0>(x23);
                             a[3] = f16x2_from_q8<CK, 1>(x23);
                             ptx::mma16816<false>(o[2 * q4 + hb], a, pb[kt][0], pb[kt][1]);
+                            if constexpr (NG1) ptx::mma16816<false>(o1[2 * q4 + hb], a, pb1[kt][0], pb1[kt][1]);
                         }
                     }
                 }
@@ -1365,11 +1412,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeParams p,
         orow[EPL * lane + e] = p.q_is_bf16 ? f2h<kBF16>(acc[e]) : f2h<kF16>(acc[e]);
 }
 
-template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false>
+template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
 cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                           const CUtensorMap &mv, cudaStream_t s)
 {
-    auto kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV>;
+    auto kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV, NG>;
     // dynamic shared memory limit, raised once per device as needed
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;

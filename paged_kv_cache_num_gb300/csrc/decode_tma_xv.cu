@@ -12,8 +12,12 @@ cudaError_t launch_xv_bs(const DecodeParams &p, const FastParams &f, const CUten
                          const CUtensorMap &mv, cudaStream_t s)
 {
     switch (p.block_size) {
-    case 16: return launch_fast_t<CK, D, 16, 0, false, true>(p, f, mk, mv, s);
-    case 32: return launch_fast_t<CK, D, 32, 0, false, true>(p, f, mk, mv, s);
+    case 16:
+        return f.ng == 2 ? launch_fast_t<CK, D, 16, 0, false, true, 2>(p, f, mk, mv, s)
+                         : launch_fast_t<CK, D, 16, 0, false, true>(p, f, mk, mv, s);
+    case 32:
+        return f.ng == 2 ? launch_fast_t<CK, D, 32, 0, false, true, 2>(p, f, mk, mv, s)
+                         : launch_fast_t<CK, D, 32, 0, false, true>(p, f, mk, mv, s);
     case 64: return launch_fast_t<CK, D, 64, 0, false, true>(p, f, mk, mv, s);
     default: return cudaErrorInvalidValue;
     }

@@ -123,8 +123,8 @@ struct DecodeParams {
 // Persistent TMA kernel (16-bit and fp8 caches).
 struct FastParams {
     int nh;                     // kv heads per CTA
-    int wsh;                    // log2(consumer warps per kv head): 1 when the group has
-                                // more than 8 q heads (each warp takes 8 of them)
+    int ng;                     // head-column groups of 8 per consumer warp: 2 when the
+                                // group has more than 8 q heads (16-bit / one-byte codes)
     int n_hg;                   // head groups = num_kv_heads / nh
     int stages;                 // shared-memory ring depth
     int grid;                   // persistent CTAs
