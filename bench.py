@@ -212,6 +212,16 @@ def algorithmic_bytes(w, decode=True, append=True):
     return total
 
 
+def fill_row_bytes(w):
+    """Algorithmic bytes of one token of a context-fill append (slots given):
+    its K and V source rows read, its cache rows (and 3-bit scale / zero)
+    written, its slot read."""
+    D, Hkv = w.head_dim, w.num_kv_heads
+    row = {"f16": 2 * D, "bf16": 2 * D, "e4m3": D, "e5m2": D, "i8": D, "u3": 3 * D // 8}[w.cache_kind]
+    meta = 3 if w.cache_kind == "u3" else 0
+    return Hkv * 2 * (2 * D + row + meta) + 8
+
+
 def make_workload(name, device, rank=0):
     """The named workload; rank r > 0 (a replica under torchrun) draws an
     independent instance of the same recipe (seed + 1000 r)."""
@@ -263,8 +273,10 @@ class Step:
             self.cache.v_cache.copy_(W.storage(w.v_cache0, w.layout))
             w.k_cache0 = w.v_cache0 = None      # release the staging copies
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.fill = None
         if w.fill_req is not None:            # context fill (setup, not timed)
             ch = 1 << 18
+            first = None
             for i in range(0, w.fill_req.shape[0], ch):
                 sm = pkv.slot_mapping(w.block_tables, w.fill_req[i:i + ch], w.fill_pos[i:i + ch],
                                       w.block_size, err_flag=self.err)
@@ -272,9 +284,27 @@ class Step:
                     pkv.kv_append_scaled(w.k_fill[i:i + ch], w.v_fill[i:i + ch],
                                          w.k_fill_scale[i:i + ch], w.v_fill_scale[i:i + ch], sm,
                                          self.cache, err_flag=self.err)
+                elif first is None:
+                    first = (w.k_fill[i:i + ch], w.v_fill[i:i + ch], sm)
+                    pkv.kv_append(*first, self.cache, err_flag=self.err)
                 else:
                     pkv.kv_append(w.k_fill[i:i + ch], w.v_fill[i:i + ch], sm, self.cache,
                                   err_flag=self.err)
+            if first is not None:
+                # the first chunk's append again (it writes the same bytes),
+                # timed alone: a prefill-sized quantising append
+                ts = []
+                for _ in range(3):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    pkv.kv_append(*first, self.cache, err_flag=self.err)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                n = int(first[2].shape[0])
+                self.fill = {"tokens": n, "ms": min(ts),
+                             "bytes": n * fill_row_bytes(w)}
+                del first
             w.k_fill = w.v_fill = w.fill_req = w.fill_pos = None
             w.k_fill_scale = w.v_fill_scale = None
         self.slots = torch.empty(w.new_req.shape[0], dtype=torch.int64, device=dev)
@@ -703,6 +733,12 @@ def main():
     app_bytes = algorithmic_bytes(w, decode=False)
     n_real = int((w.new_pos >= 0).sum())
     st = Step(w, pkv)
+    fill = None
+    if st.fill is not None:
+        fg = st.fill["bytes"] / (st.fill["ms"] * 1e-3) / 1e9
+        fill = {"tokens": st.fill["tokens"], "ms": round(st.fill["ms"], 4), "gbs": round(fg, 1),
+                "frac_of_peak": round(fg / peak, 4),
+                "what": "one context-fill append launch (slots given), CUDA events, best of 3"}
     st.capture()
     for _ in range(args.warmup):
         flush.zero_()
@@ -836,6 +872,12 @@ def main():
                 # workload's check covers every sequence)
                 e["parity"] = check_timed_step(snapshot_timed_step(sx), orc,
                                                seqs=sorted({0, wx.batch - 1}))
+        if sx.fill is not None:
+            fg = sx.fill["bytes"] / (sx.fill["ms"] * 1e-3) / 1e9
+            e["fill_append"] = {"tokens": sx.fill["tokens"], "ms": round(sx.fill["ms"], 4),
+                                "gbs": round(fg, 1), "frac_of_peak": round(fg / peak, 4),
+                                "what": "one context-fill append launch (slots given), "
+                                        "CUDA events, best of 3"}
         extra[name] = e
         del sx, wx
         torch.cuda.empty_cache()
@@ -900,6 +942,7 @@ def main():
             "decode_gbs": round(dec_gbs, 1), "decode_ms": round(dec_ms, 5),
             "append_tokens_per_s": round(n_real / (app_ms * 1e-3), 1),
             "append_ms": round(app_ms, 5),
+            "fill_append": fill,
             "step_algorithmic_bytes": step_bytes,
             "roofline": roofline,
             "copy_kernel_gbs": round(copy_gbs, 1),

@@ -422,15 +422,28 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
         const float s = __half2float(__ushort_as_half(sbits));
         float z = 0.0f;
         if (s != 0.0f) z = fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.0f), 7.0f);
-        // fields: codes q_j at bits 3j (small integers, exact in fp32)
+        // fields: codes q_j at bits 3j (small integers, exact in fp32).
+        // q = clamp(rint(fl(x / s)) + z, 0, 7) without a division per code:
+        // with r = RN(1/s), y1 = RN(x r) and the exact residual e = x - y1 s
+        // (one FMA), y = RN(y1 + e r) is RN(x / s) up to an error far below
+        // half an ulp (Markstein's refinement), so y equals x / s whenever
+        // x / s is an fp32 value -- in particular at every half-integer, where
+        // rint then rounds to even as on fl(x / s).  Off the half-integers
+        // the two roundings agree too: x and s are 16-bit floats, so an x / s
+        // in the codes' range (|x / s| < 2^10) that is not a half-integer
+        // lies at least 2^-13 away from one, far beyond the difference
+        // between y and fl(x / s).
         uint32_t f[NF];
+        const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
 #pragma unroll
         for (int fi = 0; fi < NF; ++fi) {
             float fv = 0.0f;
 #pragma unroll
             for (int j = 7; j >= 0; --j) {
-                float q = 0.0f;
-                if (s != 0.0f) q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(x[8 * fi + j], s)), z), 0.0f), 7.0f);
+                const float xv = x[8 * fi + j];
+                const float y1 = __fmul_rn(xv, rs);
+                const float y = __fmaf_rn(__fmaf_rn(-y1, s, xv), rs, y1);
+                const float q = s != 0.0f ? fminf(fmaxf(__fadd_rn(rintf(y), z), 0.0f), 7.0f) : 0.0f;
                 fv = fmaf(fv, 8.0f, q);
             }
             f[fi] = uint32_t(fv);

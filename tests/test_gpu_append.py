@@ -286,6 +286,54 @@ def test_u3_append_hand_worked_ties(pkv, D):
     assert not got["k_cache"][0].any() and not got["v_cache"][0].any()  # block 0 untouched
 
 
+@pytest.mark.parametrize("src", [torch.float16, torch.bfloat16])
+def test_u3_append_every_source_pattern_in_range(pkv, orc, src):
+    """Every finite fp16 (or bf16) value x between a row's minimum -3s and
+    maximum 4s, for scales s from 2^-20 to 2^12 (at most 8 significant bits,
+    so that -3s and 4s are exact and the row's scale is s, zero point 3):
+    the 3-bit append's codes, scales and zero points equal the oracle's
+    (division, then round half to even) bit for bit.  This covers every
+    quotient x / s the codes can take at these scales, the exact
+    half-integer ties included."""
+    D, H, BS = 128, 2, 16
+    g = torch.Generator().manual_seed(281)
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    allv = bits.view(src).to(torch.float64)
+    allv = allv[torch.isfinite(allv)]
+    rows = []
+    for s in (2.0 ** -20, 3 * 2.0 ** -14, 0.0078125 * 5, 0.25, 1.0, 1.5, 7.0, 100.0, 255.0 / 64, 2.0 ** 12):
+        sv = torch.tensor(s, dtype=torch.float64)
+        if any(float((k * sv).to(src).double()) != k * s for k in (1, 3, 4)):
+            continue                    # anchors not exact in this source type
+        vals = allv[(allv >= -3 * s) & (allv <= 4 * s)]
+        vals = vals[torch.randperm(vals.numel(), generator=g)]
+        n = (vals.numel() + D - 3) // (D - 2)
+        pad = n * (D - 2) - vals.numel()
+        vals = torch.cat([vals, vals[:pad]]).reshape(n, D - 2)
+        anchors = torch.tensor([-3 * s, 4 * s], dtype=torch.float64).expand(n, 2)
+        rows.append(torch.cat([anchors, vals], 1))
+    R = torch.cat(rows).to(src)                                   # [n_rows, D]
+    T = (R.shape[0] + 2 * H - 1) // (2 * H)
+    R = torch.cat([R, R[:T * 2 * H - R.shape[0]]])
+    kn = R[:T * H].reshape(T, H, D)
+    vn = R[T * H:].reshape(T, H, D)
+    P = (T + BS - 1) // BS + 1
+    slots = torch.randperm(P * BS, generator=g)[:T]
+    cache = pkv.KVCache.allocate("u3", P, BS, H, D, fill=0)
+    pkv.kv_append(kn.cuda(), vn.cuda(), slots.cuda(), cache)
+    torch.cuda.synchronize()
+    RB = 3 * D // 8
+    c = {"k_cache": np.zeros((P, BS, H, RB), np.uint8), "v_cache": np.zeros((P, BS, H, RB), np.uint8),
+         "k_qscale": np.zeros((P, BS, H), np.uint16), "v_qscale": np.zeros((P, BS, H), np.uint16),
+         "k_qzero": np.zeros((P, BS, H), np.uint8), "v_qzero": np.zeros((P, BS, H), np.uint8)}
+    code = 1 if src == torch.float16 else 2
+    orc.kv_append(4, code, W.bits16(kn), W.bits16(vn), slots.numpy(), c["k_cache"], c["v_cache"],
+                  None, None, c["k_qscale"], c["k_qzero"], c["v_qscale"], c["v_qzero"])
+    got = PL.gpu_cache_host(cache)
+    assert np.all(c["k_qzero"][slots.numpy() // BS, slots.numpy() % BS] == 3)
+    _assert_pools_equal(got, c)
+
+
 def test_u3_append_unaligned_rows_and_sources(pkv, orc):
     """3-bit rows at a head stride of 49 bytes (rows start at any byte: the
     kernel stores their 12-byte runs byte by byte) from sources that start
