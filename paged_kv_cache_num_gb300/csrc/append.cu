@@ -360,25 +360,42 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendParams
     }
 }
 
-// 3-bit affine quantise + pack: eight lanes per (token, head, K|V) row,
-// four rows per warp.  Each lane holds EPL = head_dim / 8 consecutive
-// elements; a row's min / max are three-step shuffle reductions among its
-// eight lanes, which then each derive the row's scale and zero point (IEEE
-// divisions, as the codes).  A lane's codes make EPL / 8 fields of 24 bits
-// (8 codes each; code d sits at bit 3d of the packed row), and four
-// consecutive fields -- 96 bits -- fill one 12-byte run, assembled by the
-// first lane holding a field of it from the others' (warp shuffles).
-template <int SRC, int EPL>
+// RN(x / s) for 16-bit float x and fp16 s > 0, through the correctly
+// rounded reciprocal rs = RN(1 / s): with y1 = RN(x rs) and the exact
+// residual e = x - y1 s (one FMA), RN(y1 + e rs) is within far less than
+// half an ulp of x / s (Markstein's refinement), so it equals x / s
+// wherever x / s is an fp32 value -- at every half-integer in particular.
+// Off the half-integers rint of it is rint(fl(x / s)) in the codes' range:
+// x and s have at most 11 significant bits, so an x / s with |x / s| < 2^10
+// that is not a half-integer lies at least 2^-13 away from one.
+__device__ __forceinline__ float u3_quotient(float x, float s, float rs)
+{
+    const float y1 = __fmul_rn(x, rs);
+    return __fmaf_rn(__fmaf_rn(-y1, s, x), rs, y1);
+}
+
+// 3-bit affine quantise + pack: LPR = 4 lanes per (token, head, K|V) row,
+// eight rows per warp.  Each lane holds EPL = head_dim / 4 consecutive
+// elements; a row's min / max are two-step shuffle reductions among its
+// lanes, which then each derive the row's scale (one IEEE division) and
+// zero point.  A lane's codes make EPL / 8 fields of 24 bits (8 codes each;
+// code d sits at bit 3d of the packed row); four consecutive fields -- 96
+// bits -- fill one 12-byte run, which is a lane's own at head_dim 128 and
+// is gathered from two lanes by shuffles at head_dim 64.
+template <int SRC, int EPL, int LPR>
 __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams p)
 {
     griddep_wait();
     griddep_launch_dependents();
+    constexpr int RPW = 32 / LPR;        // rows per warp
     constexpr int WARPS = kAppendThreads / 32;
-    constexpr int NF = EPL / 8;          // 24-bit fields per lane (1 or 2)
-    constexpr int LR = 4 / NF;           // lanes per 12-byte run (4 or 2)
+    constexpr int NF = EPL / 8;          // 24-bit fields per lane
+    constexpr int LR = NF >= 4 ? 1 : 4 / NF;   // lanes per 12-byte run
+    constexpr int RUNS = NF >= 4 ? NF / 4 : 1;  // runs a storing lane writes
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int grp = lane >> 3, sub = lane & 7;   // the warp's row, the lane within it
-    Walk2 w((blockIdx.x * int64_t(WARPS) + wid) * 4 + grp, int64_t(gridDim.x) * WARPS * 4, 2 * p.num_kv_heads);
+    const int grp = lane / LPR, sub = lane % LPR;   // the warp's row, the lane within it
+    Walk2 w((blockIdx.x * int64_t(WARPS) + wid) * RPW + grp, int64_t(gridDim.x) * WARPS * RPW,
+            2 * p.num_kv_heads);
     while (__any_sync(0xffffffffu, w.major < p.num_tokens)) {
         const int64_t t = w.major;
         const int r = w.minor;               // (kv head, K|V)
@@ -412,7 +429,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
 #pragma unroll
         for (int j = 1; j < EPL; ++j) { mn = fminf(mn, x[j]); mx = fmaxf(mx, x[j]); }
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {     // within the row's eight lanes
+        for (int o = 1; o < LPR; o <<= 1) {   // within the row's lanes
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
@@ -420,55 +437,53 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
         uint16_t sbits = __half_as_ushort(__float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 7.0f)));
         if ((sbits & 0x7fff) == 0x7c00) sbits = 0x7bff;
         const float s = __half2float(__ushort_as_half(sbits));
-        float z = 0.0f;
-        if (s != 0.0f) z = fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.0f), 7.0f);
-        // fields: codes q_j at bits 3j (small integers, exact in fp32).
-        // q = clamp(rint(fl(x / s)) + z, 0, 7) without a division per code:
-        // with r = RN(1/s), y1 = RN(x r) and the exact residual e = x - y1 s
-        // (one FMA), y = RN(y1 + e r) is RN(x / s) up to an error far below
-        // half an ulp (Markstein's refinement), so y equals x / s whenever
-        // x / s is an fp32 value -- in particular at every half-integer, where
-        // rint then rounds to even as on fl(x / s).  Off the half-integers
-        // the two roundings agree too: x and s are 16-bit floats, so an x / s
-        // in the codes' range (|x / s| < 2^10) that is not a half-integer
-        // lies at least 2^-13 away from one, far beyond the difference
-        // between y and fl(x / s).
-        uint32_t f[NF];
         const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
+        // z = clamp(rint(fl(-min / s)), 0, 7); -min is one of the row's
+        // 16-bit values, so u3_quotient gives the same rint
+        float z = 0.0f;
+        if (s != 0.0f) z = fminf(fmaxf(rintf(u3_quotient(-mn, s, rs)), 0.0f), 7.0f);
+        // fields: codes q_j = clamp(rint(fl(x_j / s)) + z, 0, 7) at bits 3j
+        // (small integers, exact in fp32)
+        uint32_t f[NF];
 #pragma unroll
         for (int fi = 0; fi < NF; ++fi) {
             float fv = 0.0f;
 #pragma unroll
             for (int j = 7; j >= 0; --j) {
-                const float xv = x[8 * fi + j];
-                const float y1 = __fmul_rn(xv, rs);
-                const float y = __fmaf_rn(__fmaf_rn(-y1, s, xv), rs, y1);
-                const float q = s != 0.0f ? fminf(fmaxf(__fadd_rn(rintf(y), z), 0.0f), 7.0f) : 0.0f;
+                const float q = s != 0.0f
+                    ? fminf(fmaxf(__fadd_rn(rintf(u3_quotient(x[8 * fi + j], s, rs)), z), 0.0f), 7.0f)
+                    : 0.0f;
                 fv = fmaf(fv, 8.0f, q);
             }
             f[fi] = uint32_t(fv);
         }
-        // the run's four fields, in order, gathered by its first lane
-        uint32_t F[4];
+        // each run's four fields, in order (gathered by its first lane when
+        // a lane holds fewer than four)
+        uint32_t F[RUNS][4];
 #pragma unroll
-        for (int k = 0; k < LR; ++k)
+        for (int ru = 0; ru < RUNS; ++ru)
 #pragma unroll
-            for (int fi = 0; fi < NF; ++fi) F[NF * k + fi] = __shfl_sync(0xffffffffu, f[fi], lane + k);
+            for (int k = 0; k < 4; ++k)
+                F[ru][k] = LR == 1 ? f[4 * ru + k] : __shfl_sync(0xffffffffu, f[k % NF], lane + k / NF);
         if (live && sub % LR == 0) {
-            const uint32_t w0 = F[0] | (F[1] << 24);
-            const uint32_t w1 = (F[1] >> 8) | (F[2] << 16);
-            const uint32_t w2 = (F[2] >> 16) | (F[3] << 8);
-            uint8_t *dst = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
-                                                       off * p.c_slot + h * p.c_head) + 12 * (sub / LR);
-            if ((reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
-                uint32_t *d32 = reinterpret_cast<uint32_t *>(dst);
-                d32[0] = w0;
-                d32[1] = w1;
-                d32[2] = w2;
-            } else {                    // rows at strides that are not multiples of 4 bytes
-                const uint32_t run[3] = {w0, w1, w2};
+            uint8_t *row = reinterpret_cast<uint8_t *>((kv ? p.v_cache : p.k_cache) + blk * p.c_blk +
+                                                       off * p.c_slot + h * p.c_head);
 #pragma unroll
-                for (int b = 0; b < 12; ++b) dst[b] = uint8_t(run[b >> 2] >> (8 * (b & 3)));
+            for (int ru = 0; ru < RUNS; ++ru) {
+                const uint32_t w0 = F[ru][0] | (F[ru][1] << 24);
+                const uint32_t w1 = (F[ru][1] >> 8) | (F[ru][2] << 16);
+                const uint32_t w2 = (F[ru][2] >> 16) | (F[ru][3] << 8);
+                uint8_t *dst = row + 12 * (RUNS * sub / LR + ru);
+                if ((reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+                    uint32_t *d32 = reinterpret_cast<uint32_t *>(dst);
+                    d32[0] = w0;
+                    d32[1] = w1;
+                    d32[2] = w2;
+                } else {                // rows at strides that are not multiples of 4 bytes
+                    const uint32_t run[3] = {w0, w1, w2};
+#pragma unroll
+                    for (int b = 0; b < 12; ++b) dst[b] = uint8_t(run[b >> 2] >> (8 * (b & 3)));
+                }
             }
         }
         if (live && sub == 0) {
@@ -548,14 +563,15 @@ cudaError_t launch_append(const AppendParams &p, int cache_kind, bool vec16, cud
         return vec16 ? go_u(HF{}, std::true_type{}) : go_u(HF{}, std::false_type{});
     } else {  // kU3
         const int64_t rows = p.num_tokens * 2 * p.num_kv_heads;
-        const int g = grid_for(rows * 8, T);       // eight lanes per row
+        constexpr int LPR = 4;                      // lanes per row (two: slower)
+        const int g = grid_for(rows * LPR, T);
         const bool bf = p.src_kind == kBF16;
         if (p.head_dim == 128) {
-            if (bf) return launch_pdl(append_u3_kernel<kBF16, 16>, g, T, 0, s, p);
-            else return launch_pdl(append_u3_kernel<kF16, 16>, g, T, 0, s, p);
+            if (bf) return launch_pdl(append_u3_kernel<kBF16, 128 / LPR, LPR>, g, T, 0, s, p);
+            else return launch_pdl(append_u3_kernel<kF16, 128 / LPR, LPR>, g, T, 0, s, p);
         } else {
-            if (bf) return launch_pdl(append_u3_kernel<kBF16, 8>, g, T, 0, s, p);
-            else return launch_pdl(append_u3_kernel<kF16, 8>, g, T, 0, s, p);
+            if (bf) return launch_pdl(append_u3_kernel<kBF16, 64 / LPR, LPR>, g, T, 0, s, p);
+            else return launch_pdl(append_u3_kernel<kF16, 64 / LPR, LPR>, g, T, 0, s, p);
         }
     }
     return cudaGetLastError();
