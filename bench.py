@@ -791,9 +791,14 @@ def main():
 
     def e2e_once():
         dpack.copy_(hpack, non_blocking=True)
-        pkv.decode_step(dbuf["k_new"], dbuf["v_new"], dbuf["new_req"], dbuf["new_pos"], dbuf["q"],
-                        st.cache, dbuf["block_tables"], dbuf["context_lens"], sm_scale=w.sm_scale,
-                        out=st.out, slots=st.slots, workspace=st.ws, err_flag=st.err)
+        if st.fused:
+            pkv.decode_step(dbuf["k_new"], dbuf["v_new"], dbuf["new_req"], dbuf["new_pos"],
+                            dbuf["q"], st.cache, dbuf["block_tables"], dbuf["context_lens"],
+                            sm_scale=w.sm_scale, out=st.out, slots=st.slots, workspace=st.ws,
+                            err_flag=st.err)
+        else:       # per-token scales: the separate calls (see Step.run)
+            st.append(dbuf["new_req"], dbuf["new_pos"], dbuf["k_new"], dbuf["v_new"])
+            st.decode(dbuf["q"])
         out_host.copy_(st.out, non_blocking=True)
 
     def e2e_times(run):
