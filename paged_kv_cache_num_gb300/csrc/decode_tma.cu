@@ -78,6 +78,11 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
                 if (f.hpw == 2) return launch_fast_t<CK, D, 32, 2>(p, f, mk, mv, s);
                 return launch_fast_t<CK, D, 32, 1>(p, f, mk, mv, s);
             }
+            if (p.block_size == 64) {
+                if (f.hpw == 4) return launch_fast_t<CK, D, 64, 4>(p, f, mk, mv, s);
+                if (f.hpw == 2) return launch_fast_t<CK, D, 64, 2>(p, f, mk, mv, s);
+                return launch_fast_t<CK, D, 64, 1>(p, f, mk, mv, s);
+            }
         }
     }
     if constexpr (is_q8(CK)) {      // per-block / per-token scales staged with the tiles
@@ -103,9 +108,7 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
         if constexpr (CK != kU3)
             if (f.ng == 2) return launch_fast_t<CK, D, 32, 0, false, false, 2>(p, f, mk, mv, s);
         return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
-    case 64:
-        if constexpr (CK != kU3) return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
-        return cudaErrorInvalidValue;
+    case 64: return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -120,7 +123,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
     if (group > (cache_kind == kU3 ? 8 : 16) || batch > 4096) return false;
     if (group > 8 && block_size > 32) return false;
     if (is_q8(cache_kind)) return head_dim == 128;
-    if (cache_kind == kU3) return head_dim == 128 && block_size <= 32;
+    if (cache_kind == kU3) return head_dim == 128;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
 }
 

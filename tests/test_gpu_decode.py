@@ -99,11 +99,14 @@ def test_u3_small(pkv, orc, splits):
 
 
 @pytest.mark.parametrize("BS,H,Hkv", [(32, 8, 8), (16, 16, 4), (32, 12, 4), (16, 4, 2), (16, 12, 6),
-                                      (32, 6, 6), (16, 3, 1)])
+                                      (32, 6, 6), (16, 3, 1), (64, 8, 8), (64, 6, 6), (64, 3, 3),
+                                      (64, 16, 4)])
 def test_u3_block_and_group_variants(pkv, orc, BS, H, Hkv):
-    """3-bit cache with block 32, and grouped q heads over a 3-bit cache,
-    including kv-head counts not divisible by the 4-head CTA (2- and 1-head
-    CTAs, whose ring stages must still start on TMA-aligned addresses)."""
+    """3-bit cache with blocks of 32 and 64 slots, and grouped q heads over a
+    3-bit cache, including kv-head counts not divisible by the 4-head CTA
+    (2- and 1-head CTAs, whose ring stages must still start on TMA-aligned
+    addresses) and multi-head caches with 4, 2 and 1 kv heads per consumer
+    warp."""
     w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=7 * BS + 3, num_heads=H, block_size=BS, seed=80 + BS + H)
     if Hkv != H:   # regroup: keep Hkv kv heads, H q heads
         w.num_kv_heads = Hkv
