@@ -260,8 +260,8 @@ def make_workload(name, device, rank=0):
 class Step:
     """Device-resident state of one workload and its step."""
 
-    def __init__(self, w, pkv):
-        self.w, self.pkv = w, pkv
+    def __init__(self, w, pkv, num_splits=0):
+        self.w, self.pkv, self.num_splits = w, pkv, num_splits
         dev = w.new_req.device
         self.cache = pkv.KVCache.allocate(
             w.cache_kind, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, device=dev,
@@ -313,9 +313,9 @@ class Step:
         self.fused = w.q is not None and not self.tok
         self.launches = 1 if self.fused else 2     # (slot computation +) append
         if w.q is not None:
-            n = pkv.decode_workspace_bytes(w.q, self.cache, w.block_tables)
+            n = pkv.decode_workspace_bytes(w.q, self.cache, w.block_tables, num_splits)
             self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
-            self.launches += pkv.decode_launches(w.q, self.cache, w.block_tables)
+            self.launches += pkv.decode_launches(w.q, self.cache, w.block_tables, num_splits)
         torch.cuda.synchronize()
 
     def append(self, req=None, pos=None, k=None, v=None):
@@ -337,7 +337,7 @@ class Step:
             return
         self.pkv.paged_decode(w.q if q is None else q, self.cache, w.block_tables,
                               w.context_lens, sm_scale=w.sm_scale, out=self.out,
-                              workspace=self.ws, err_flag=self.err)
+                              num_splits=self.num_splits, workspace=self.ws, err_flag=self.err)
 
     def run(self):
         """One whole step through the public API: pkv_decode_step (slot
@@ -348,7 +348,8 @@ class Step:
         if self.fused:
             self.pkv.decode_step(w.k_new, w.v_new, w.new_req, w.new_pos, w.q, self.cache,
                                  w.block_tables, w.context_lens, sm_scale=w.sm_scale, out=self.out,
-                                 slots=self.slots, workspace=self.ws, err_flag=self.err)
+                                 slots=self.slots, num_splits=self.num_splits, workspace=self.ws,
+                                 err_flag=self.err)
         else:
             self.append()
             self.decode()
@@ -706,6 +707,9 @@ def main():
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="explicit split count for every decode call (> 0 selects the general "
+                         "kernel; 0: the automatic plan)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -732,7 +736,7 @@ def main():
     dec_bytes = algorithmic_bytes(w, append=False)
     app_bytes = algorithmic_bytes(w, decode=False)
     n_real = int((w.new_pos >= 0).sum())
-    st = Step(w, pkv)
+    st = Step(w, pkv, args.num_splits)
     fill = None
     if st.fill is not None:
         fg = st.fill["bytes"] / (st.fill["ms"] * 1e-3) / 1e9
@@ -794,8 +798,8 @@ def main():
         if st.fused:
             pkv.decode_step(dbuf["k_new"], dbuf["v_new"], dbuf["new_req"], dbuf["new_pos"],
                             dbuf["q"], st.cache, dbuf["block_tables"], dbuf["context_lens"],
-                            sm_scale=w.sm_scale, out=st.out, slots=st.slots, workspace=st.ws,
-                            err_flag=st.err)
+                            sm_scale=w.sm_scale, out=st.out, slots=st.slots,
+                            num_splits=st.num_splits, workspace=st.ws, err_flag=st.err)
         else:       # per-token scales: the separate calls (see Step.run)
             st.append(dbuf["new_req"], dbuf["new_pos"], dbuf["k_new"], dbuf["v_new"])
             st.decode(dbuf["q"])
@@ -858,7 +862,7 @@ def main():
         db = algorithmic_bytes(wx, append=False)
         ab = algorithmic_bytes(wx, decode=False)
         nr = int((wx.new_pos >= 0).sum())
-        sx = Step(wx, pkv)
+        sx = Step(wx, pkv, args.num_splits)
         tt, aa, dd = time_steps(sx, args.extra_steps, max(3, args.warmup // 4), flush)
         assert int(sx.err.item()) == 0, name
         e = {"step_ms": round(float(np.mean(tt)), 4),
@@ -931,7 +935,7 @@ def main():
             "dtype": w.cache_kind,
             "data": "synthetic (seeded torch CUDA generator; N(0,1) K/V/q)",
             "config": workload_config(w, args.workload, ws),
-            "timing": {"l2": "inputs larger than L2, and flushed between steps outside the "
+            "timing": {"num_splits": args.num_splits, "l2": "inputs larger than L2, and flushed between steps outside the "
                              "timed events (256 MiB write, then a 512 MiB read that drains "
                              "its write-back)",
                        "launch": "a device-timed step replays one CUDA graph of one "

@@ -16,11 +16,11 @@
 // sm_scale * log2(e)) so every exponential is one ex2 instruction.
 //
 // This file holds the general kernel: one CTA of 4 warps per (chunk, kv head,
-// sequence); each warp walks every 4th token of the chunk with its lanes
-// splitting head_dim, and keeps its own online-softmax state for all q heads
-// of the group; the four states are merged through shared memory.  It serves
-// every cache dtype, head_dim 64/128, any block size and any group size up to
-// 16.
+// sequence); each warp walks steps of a few consecutive tokens of the chunk
+// (every 4th step) with its lanes splitting head_dim, and keeps its own
+// online-softmax state for all q heads of the group; the four states are
+// merged through shared memory.  It serves every cache dtype, head_dim
+// 64/128, any block size and any group size up to 16.
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -138,48 +138,134 @@ __global__ void __launch_bounds__(kGenThreads) decode_general_kernel(DecodeParam
         e0 = 0;
     }
 
-    for (int t = t0 + warp; t < t1; t += kGenWarps) {
-        const int j = t >> p.block_shift, off = t & bmask;
-        const int pb = p.block_tables[b * p.bt_b + j * p.bt_j];
-        if (pb < 0 || pb >= p.num_blocks) {
-            if (lane == 0) raise_err(p.err_flag, PKV_DEVERR_BLOCK_RANGE);
-            continue;
+    // Each warp takes TC consecutive tokens per step (steps strided over the
+    // CTA's warps).  Its lanes hold partial dot products for every (q head,
+    // token) pair of the step, NV = GMAX * TC values; a transposing butterfly
+    // (each xor step swaps half of the values with the partner lane) leaves
+    // lane L with the full score of pair index L >> RS, replicated over
+    // 2^RS lanes, for NV - 1 shuffles instead of 5 per pair.  The softmax
+    // update is then one exponential per lane, and the pairs' P values are
+    // broadcast for the V accumulation.
+    constexpr int TC = GMAX >= 16 ? 2 : 4;                       // tokens per step
+    constexpr int NV = GMAX * TC;                                // (head, token) pairs
+    constexpr int LNV = NV == 32 ? 5 : (NV == 16 ? 4 : (NV == 8 ? 3 : 2));   // log2 NV
+    constexpr int RS = 5 - LNV;                                  // replication bits
+    const int my_pair = lane >> RS;                              // this lane's pair
+    const int my_g = my_pair / TC;                               // its head
+    float lsum = 0.0f;                                           // sum of P of the lane's pair slot
+    for (int tb = t0 + warp * TC; tb < t1; tb += kGenWarps * TC) {
+        float part[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) part[i] = 0.0f;
+        float vx[TC][EPL];
+        bool live[TC];
+#pragma unroll
+        for (int tt = 0; tt < TC; ++tt) {
+            const int t = tb + tt;
+            live[tt] = false;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) vx[tt][e] = 0.0f;
+            if (t >= t1) continue;
+            const int j = t >> p.block_shift, off = t & bmask;
+            const int pb = p.block_tables[b * p.bt_b + j * p.bt_j];
+            if (pb < 0 || pb >= p.num_blocks) {
+                if (lane == 0) raise_err(p.err_flag, PKV_DEVERR_BLOCK_RANGE);
+                continue;
+            }
+            live[tt] = true;
+            const int64_t roff = pb * p.c_blk + off * p.c_slot + kvh * p.c_head;
+            float kq = 1.0f, kz = 0.0f, vq = 1.0f, vz = 0.0f;
+            float kst = ks, vst = vs;             // the row's fp8 / int8 scales
+            if (is_q8(CK) && p.scale_mode != 0) {
+                const int64_t gi = pb * p.gs_blk + off * p.gs_slot + kvh * p.gs_head;
+                kst = p.k_gs[gi];
+                vst = p.v_gs[gi];
+            }
+            if constexpr (CK == kU3) {
+                kq = __half2float(__ushort_as_half(p.k_qs[pb * p.m_blk + off * p.m_slot + kvh * p.m_head]));
+                vq = __half2float(__ushort_as_half(p.v_qs[pb * p.m_blk + off * p.m_slot + kvh * p.m_head]));
+                kz = float(p.k_qz[pb * p.z_blk + off * p.z_slot + kvh * p.z_head]);
+                vz = float(p.v_qz[pb * p.z_blk + off * p.z_slot + kvh * p.z_head]);
+            }
+            float kx[EPL];
+            load_row<CK, EPL>(p.k_cache + roff + eoff, e0, kst, kq, kz, kx);
+            load_row<CK, EPL>(p.v_cache + roff + eoff, e0, vst, vq, vz, vx[tt]);
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                float sp = 0.0f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) sp = fmaf(q[g][e], kx[e], sp);
+                part[g * TC + tt] = sp;
+            }
         }
-        const int64_t roff = pb * p.c_blk + off * p.c_slot + kvh * p.c_head;
-        float kq = 1.0f, kz = 0.0f, vq = 1.0f, vz = 0.0f;
-        float kst = ks, vst = vs;             // the row's fp8 / int8 scales
-        if (is_q8(CK) && p.scale_mode != 0) {
-            const int64_t gi = pb * p.gs_blk + off * p.gs_slot + kvh * p.gs_head;
-            kst = p.k_gs[gi];
-            vst = p.v_gs[gi];
+        // transposing reduction: after the halving steps lane L holds the sum
+        // of pair L >> RS over the lanes that share its top LNV bits; the
+        // remaining steps sum over those
+#pragma unroll
+        for (int st = 0; st < 5; ++st) {
+            const int o = 16 >> st;
+            const int n = NV >> st;                 // values still held
+            if (n > 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < n / 2; ++i) {
+                    const float send = up ? part[i] : part[i + n / 2];
+                    const float keep = up ? part[i + n / 2] : part[i];
+                    part[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            } else {
+                part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
+            }
         }
-        if constexpr (CK == kU3) {
-            kq = __half2float(__ushort_as_half(p.k_qs[pb * p.m_blk + off * p.m_slot + kvh * p.m_head]));
-            vq = __half2float(__ushort_as_half(p.v_qs[pb * p.m_blk + off * p.m_slot + kvh * p.m_head]));
-            kz = float(p.k_qz[pb * p.z_blk + off * p.z_slot + kvh * p.z_head]);
-            vz = float(p.v_qz[pb * p.z_blk + off * p.z_slot + kvh * p.z_head]);
+        // this lane's pair: head my_g, token my_pair % TC
+        const int my_t = my_pair % TC;
+        float sc = part[0];
+        {
+            bool lv = false;
+#pragma unroll
+            for (int tt = 0; tt < TC; ++tt) lv = tt == my_t ? live[tt] : lv;
+            if (!lv || my_g >= G) sc = kNegInf;   // masked token, or no such head
         }
-        float kx[EPL], vx[EPL];
-        load_row<CK, EPL>(p.k_cache + roff + eoff, e0, kst, kq, kz, kx);
-        load_row<CK, EPL>(p.v_cache + roff + eoff, e0, vst, vq, vz, vx);
+        // chunk max per head over its TC lanes, then to every lane
+        float cm = sc;
+#pragma unroll
+        for (int o = 1 << RS; o < (TC << RS); o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        float alpha[GMAX];
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            const float cmg = __shfl_sync(0xffffffffu, cm, (g * TC) << RS);
+            const float mn = fmaxf(m[g], cmg);
+            alpha[g] = mn == kNegInf ? 1.0f : exp2_approx(m[g] - mn);
+            m[g] = mn;
+        }
+        float mine_m = 0.0f, mine_a = 1.0f;
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g)
+            if (g == my_g) { mine_m = m[g]; mine_a = alpha[g]; }
+        const float pe = sc == kNegInf ? 0.0f : exp2_approx(sc - mine_m);
+        lsum = lsum * mine_a + pe;
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) {
             if (g < G) {
-                float s = 0.0f;
+                float pg[TC];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) s = fmaf(q[g][e], kx[e], s);
+                for (int tt = 0; tt < TC; ++tt) pg[tt] = __shfl_sync(0xffffffffu, pe, (g * TC + tt) << RS);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                const float mn = fmaxf(m[g], s);
-                const float alpha = exp2_approx(m[g] - mn);
-                const float pe = exp2_approx(s - mn);
-                l[g] = l[g] * alpha + pe;
+                for (int e = 0; e < EPL; ++e) {
+                    float a = acc[g][e] * alpha[g];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pe, vx[e], acc[g][e] * alpha);
-                m[g] = mn;
+                    for (int tt = 0; tt < TC; ++tt) a = fmaf(pg[tt], vx[tt][e], a);
+                    acc[g][e] = a;
+                }
             }
         }
     }
+    // the running sums: the lanes of one head hold its token slots (each
+    // replicated over 2^RS lanes, which are not summed)
+#pragma unroll
+    for (int o = 1 << RS; o < (TC << RS); o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+#pragma unroll
+    for (int g = 0; g < GMAX; ++g) l[g] = __shfl_sync(0xffffffffu, lsum, (g * TC) << RS);
 
     // merge the four warps' states
     __shared__ float s_m[kGenWarps][GMAX], s_l[kGenWarps][GMAX];
