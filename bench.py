@@ -49,12 +49,11 @@ import torch  # noqa: E402
 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
-# sources of the decode kernels; a recorded ncu traffic figure is only used
-# while these are unchanged
+# sources of the persistent decode kernel (the automatic plan's); a recorded
+# ncu traffic figure is only used while these are unchanged
 DECODE_SOURCES = ("paged_kv_cache_num_gb300/csrc/decode_tma.cu",
                   "paged_kv_cache_num_gb300/csrc/decode_tma_kernel.cuh",
                   "paged_kv_cache_num_gb300/csrc/decode_tma_xv.cu",
-                  "paged_kv_cache_num_gb300/csrc/decode.cu",
                   "paged_kv_cache_num_gb300/csrc/pkv_ptx.cuh",
                   "paged_kv_cache_num_gb300/csrc/pkv_device.cuh")
 
@@ -473,9 +472,11 @@ def workload_config(w, name, ws):
             "parallelism": "replicas" if ws > 1 else "single"}
 
 
-def decode_roofline(name, dec_bytes, dec_ms, peak, peak_src):
+def decode_roofline(name, dec_bytes, dec_ms, peak, peak_src, num_splits=0):
     gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = profile_traffic("paged_decode:" + name, source_hash(*DECODE_SOURCES))
+    # recorded traffic is the persistent kernel's (the automatic plan)
+    traffic = (profile_traffic("paged_decode:" + name, source_hash(*DECODE_SOURCES))
+               if num_splits == 0 else None)
     return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(gbs / peak, 4), "traffic": traffic,
             "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
@@ -835,7 +836,7 @@ def main():
 
     # ---------------- roofline of the dominant operation (paged_decode)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
-    roofline = decode_roofline(args.workload, dec_bytes, dec_ms, peak, peak_src)
+    roofline = decode_roofline(args.workload, dec_bytes, dec_ms, peak, peak_src, args.num_splits)
 
     # copy-kernel yardstick (1 GiB each way)
     a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -873,7 +874,8 @@ def main():
             e.update({"decode_ms": round(float(np.mean(dd)), 4), "decode_gbs": round(g, 1),
                       "decode_frac_of_peak": round(g / peak, 4),
                       "decode_algorithmic_bytes": db,
-                      "roofline": decode_roofline(name, db, float(np.mean(dd)), peak, peak_src)})
+                      "roofline": decode_roofline(name, db, float(np.mean(dd)), peak, peak_src,
+                                                  args.num_splits)})
             if check_oracle:
                 import oracle as orc
                 orc.build()
