@@ -245,6 +245,8 @@ def make_workload(name, device, rank=0):
         return W.fp8_long(device=device, seed=seed, num_heads=128)
     if name == "gqa_bf16_g16":
         return W.gqa_bf16(device=device, seed=seed, num_heads=128)
+    if name == "fp8_long_d64":
+        return W.fp8_long(device=device, seed=seed, head_dim=64)
     if name == "u3_mha":
         return W.u3_mha(device=device, seed=seed)
     if name == "mixed_append":
@@ -703,7 +705,7 @@ def main():
     ap.add_argument("--workload", default="fp8_long")
     ap.add_argument("--extra", default="gqa_bf16,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long,"
                                        "fp8_long_token_scales,fp8_long_block_scales,gqa_bf16_xvec,"
-                                       "fp8_long_xvec,fp8_long_g16,gqa_bf16_g16",
+                                       "fp8_long_xvec,fp8_long_g16,gqa_bf16_g16,fp8_long_d64",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)

@@ -51,66 +51,19 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
     const int row_elems = u3 ? 3 * D / 8 : D;
+    // 16-bit and one-byte rows: 128-byte swizzled sub-rows, or one 64-byte
+    // row with the 64-byte swizzle (one-byte codes at head_dim 64)
+    const int sub_bytes = D * es >= 128 ? 128 : D * es;
     cuuint64_t dims[4] = {cuuint64_t(row_elems), cuuint64_t(BS), cuuint64_t(Hkv), cuuint64_t(P)};
     cuuint64_t strides[3] = {cuuint64_t(c_slot), cuuint64_t(c_head), cuuint64_t(c_blk)};
-    cuuint32_t box[4] = {cuuint32_t(u3 ? row_elems : 128 / es), cuuint32_t(BS), cuuint32_t(nh), 1};
+    cuuint32_t box[4] = {cuuint32_t(u3 ? row_elems : sub_bytes / es), cuuint32_t(BS), cuuint32_t(nh), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapSwizzle sw = u3 ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                     : (sub_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     const CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           u3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-template <int CK, int D>
-cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
-                           const CUtensorMap &mv, cudaStream_t s)
-{
-    if constexpr (CK == kU3) {      // MHA caches: f.hpw kv heads per consumer warp
-        if (p.group == 1) {
-            if (p.block_size == 16) {
-                if (f.hpw == 4) return launch_fast_t<CK, D, 16, 4>(p, f, mk, mv, s);
-                if (f.hpw == 2) return launch_fast_t<CK, D, 16, 2>(p, f, mk, mv, s);
-                return launch_fast_t<CK, D, 16, 1>(p, f, mk, mv, s);
-            }
-            if (p.block_size == 32) {
-                if (f.hpw == 4) return launch_fast_t<CK, D, 32, 4>(p, f, mk, mv, s);
-                if (f.hpw == 2) return launch_fast_t<CK, D, 32, 2>(p, f, mk, mv, s);
-                return launch_fast_t<CK, D, 32, 1>(p, f, mk, mv, s);
-            }
-            if (p.block_size == 64) {
-                if (f.hpw == 4) return launch_fast_t<CK, D, 64, 4>(p, f, mk, mv, s);
-                if (f.hpw == 2) return launch_fast_t<CK, D, 64, 2>(p, f, mk, mv, s);
-                return launch_fast_t<CK, D, 64, 1>(p, f, mk, mv, s);
-            }
-        }
-    }
-    if constexpr (is_q8(CK)) {      // per-block / per-token scales staged with the tiles
-        if (p.scale_mode != 0) {
-            switch (p.block_size) {
-            case 16:
-                return f.ng == 2 ? launch_fast_t<CK, D, 16, 0, true, false, 2>(p, f, mk, mv, s)
-                                 : launch_fast_t<CK, D, 16, 0, true>(p, f, mk, mv, s);
-            case 32:
-                return f.ng == 2 ? launch_fast_t<CK, D, 32, 0, true, false, 2>(p, f, mk, mv, s)
-                                 : launch_fast_t<CK, D, 32, 0, true>(p, f, mk, mv, s);
-            case 64: return launch_fast_t<CK, D, 64, 0, true>(p, f, mk, mv, s);
-            default: return cudaErrorInvalidValue;
-            }
-        }
-    }
-    switch (p.block_size) {
-    case 16:
-        if constexpr (CK != kU3)
-            if (f.ng == 2) return launch_fast_t<CK, D, 16, 0, false, false, 2>(p, f, mk, mv, s);
-        return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
-    case 32:
-        if constexpr (CK != kU3)
-            if (f.ng == 2) return launch_fast_t<CK, D, 32, 0, false, false, 2>(p, f, mk, mv, s);
-        return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
-    case 64: return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
-    default: return cudaErrorInvalidValue;
-    }
 }
 
 }  // namespace
@@ -122,7 +75,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
     // warp above 8, for blocks of up to 32 slots)
     if (group > (cache_kind == kU3 ? 8 : 16) || batch > 4096) return false;
     if (group > 8 && block_size > 32) return false;
-    if (is_q8(cache_kind)) return head_dim == 128;
+    if (is_q8(cache_kind)) return head_dim == 128 || head_dim == 64;
     if (cache_kind == kU3) return head_dim == 128;
     return (cache_kind == kF16 || cache_kind == kBF16) && (head_dim == 64 || head_dim == 128);
 }
@@ -224,6 +177,7 @@ cudaError_t launch_decode_fast(const DecodeParams &p, FastParams f, int cache_ki
                     p.c_head == int64_t(p.block_size) * p.head_dim * es;
         return launch_decode_fast_xv(p, f, cache_kind, &mk, &mv, s);
     }
+    if (is_q8(cache_kind) && p.head_dim == 64) return launch_decode_fast_q8_d64(p, f, cache_kind, &mk, &mv, s);
     if (cache_kind == kE4M3) return launch_fast_bs<kE4M3, 128>(p, f, mk, mv, s);
     if (cache_kind == kE5M2) return launch_fast_bs<kE5M2, 128>(p, f, mk, mv, s);
     if (cache_kind == kI8) return launch_fast_bs<kI8, 128>(p, f, mk, mv, s);

@@ -73,12 +73,12 @@ __host__ __device__ inline SmemLayout smem_layout(int nh, int bs, int row_bytes,
     SmemLayout L;
     L.tile_bytes = nh * bs * row_bytes;
     L.meta_bytes = meta_bytes;
-    // TMA writes each tile at a 1024-byte (128B-swizzled tiles: rows of 128
+    // TMA writes each tile at a 1024-byte (swizzled tiles: rows of 64, 128
     // or 256 bytes) or 128-byte (unswizzled 3-bit tiles) aligned shared
     // address, so stages are rounded up to that.  (Tiles are multiples of 768
     // bytes (3-bit) or 2048 bytes (others) at block 16+, so only the staged
     // scales / metadata can leave a stage unaligned.)
-    const int align = row_bytes % 128 == 0 ? 1024 : 128;
+    const int align = row_bytes % 64 == 0 ? 1024 : 128;
     L.stage_bytes = (2 * L.tile_bytes + meta_bytes + align - 1) / align * align;
     L.conv_off = stages * L.stage_bytes;
     L.bars_off = L.conv_off + (conv_bytes + 15) / 16 * 16;
@@ -226,8 +226,11 @@ struct Tile {
     static constexpr bool kBF = CK == kBF16;
     static constexpr int ES = (kFp8 || kIsU3) ? 1 : 2;
     static constexpr int ROW = kIsU3 ? 3 * D / 8 : D * ES;   // bytes per token row
-    static constexpr int HALVES = kIsU3 ? 1 : ROW / 128;     // 128-byte swizzled sub-rows
-    static constexpr int BOX0 = kIsU3 ? ROW : 128 / ES;      // TMA box inner extent (elements)
+    // swizzled sub-rows: 128 bytes (128-byte swizzle), or the whole 64-byte
+    // row of one-byte codes at head_dim 64 (64-byte swizzle)
+    static constexpr int SROW = kIsU3 ? ROW : (ROW >= 128 ? 128 : ROW);
+    static constexpr int HALVES = kIsU3 ? 1 : ROW / SROW;    // sub-rows per row
+    static constexpr int BOX0 = kIsU3 ? ROW : SROW / ES;     // TMA box inner extent (elements)
     static constexpr int KT = BS / 16;              // PV k-steps
     static constexpr int DT = D / 8;                // output n-tiles
     static constexpr int QK = D / 16;               // QK k-steps
@@ -497,18 +500,21 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     int64_t seg_start = lo;
 
     // one-byte codes in 128-byte swizzled rows: 16-byte chunk c of row r sits
-    // at r * 128 + ((c ^ r) & 7) * 16.  The rows a lane reads have a fixed
-    // r & 7 (gid for K; 2tig or 2tig + 1 for V), so the chunk offsets are
-    // per-lane constants, computed once: K chunk kk, V chunk 2q4 + (gid >> 2)
-    // of the even / odd token rows
+    // at r * 128 + ((c ^ r) & 7) * 16; in 64-byte swizzled rows (head_dim 64)
+    // at r * 64 + ((c ^ (r >> 1)) & 3) * 16.  The rows a lane reads have a
+    // fixed r & 7 (gid for K; 2tig or 2tig + 1 for V), so the chunk offsets
+    // are per-lane constants, computed once: K chunk kk, V chunk
+    // 2q4 + (gid >> 2) of the even / odd token rows
     uint32_t kswz[8], vswz[2][4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) kswz[c] = uint32_t((c ^ gid) & 7) << 4;
+    for (int c = 0; c < 8; ++c)
+        kswz[c] = T::SROW == 128 ? uint32_t((c ^ gid) & 7) << 4 : uint32_t((c ^ (gid >> 1)) & 3) << 4;
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-            vswz[a][q4] = uint32_t(((2 * q4 + (gid >> 2)) ^ ((2 * tig + a) & 7)) & 7) << 4;
+            vswz[a][q4] = T::SROW == 128 ? uint32_t(((2 * q4 + (gid >> 2)) ^ ((2 * tig + a) & 7)) & 7) << 4
+                                         : uint32_t(((2 * q4 + (gid >> 2)) ^ tig) & 3) << 4;
     uint32_t qb[T::QK][2];        // B fragments of Q^T per k-step
     float o[T::DT / 2][4];        // O^T accumulators: 16-d tiles x (heads 2tig, 2tig+1)
     float m[2], l[2];             // running max / partial sum for heads 2tig, 2tig+1
@@ -998,10 +1004,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const float *gsv = gsk + nh * GS;
             auto row_ks = [&](int tok) { return gsk[GS == 1 ? 0 : tok]; };
             auto row_vs = [&](int tok) { return gsv[GS == 1 ? 0 : tok]; };
-            // this warp's head: rows of 128-byte sub-rows per half, or (XV)
+            // this warp's head: rows of swizzled sub-rows per half, or (XV)
             // one [head_dim/x][BS][16 B] run; piece c of token t at
             // (c * BS + t) * 16
-            const uint32_t ktile = sbase + s * L.stage_bytes + kvl * BS * (XV ? T::ROW : 128);
+            const uint32_t ktile = sbase + s * L.stage_bytes + kvl * BS * (XV ? T::ROW : T::SROW);
             const uint32_t vtile = ktile + L.tile_bytes;
             const int half_bytes = L.tile_bytes / T::HALVES;
             const int mi = lane >> 3;    // ldmatrix: which 8x8 matrix this lane addresses
@@ -1032,9 +1038,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             w0 = ld_shared_u32(kb);
                             w1 = ld_shared_u32(kb + 8 * 16);
                         } else {   // chunk kk of rows 16mt+gid and +8 (both r & 7 = gid)
-                            const uint32_t kb = ktile + gid * 128 + 4 * tig + kswz[kk & 7] + mt * 2048;
+                            const uint32_t kb = ktile + gid * T::SROW + 4 * tig + kswz[kk & (T::SROW / 16 - 1)] +
+                                                mt * 16 * T::SROW;
                             w0 = ld_shared_u32(kb);
-                            w1 = ld_shared_u32(kb + 8 * 128);
+                            w1 = ld_shared_u32(kb + 8 * T::SROW);
                         }
                         a[0] = f16x2_from_q8<CK, 0>(w0);
                         a[1] = f16x2_from_q8<CK, 0>(w1);
@@ -1154,7 +1161,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         if constexpr (XV)   // piece 2q4 + (gid >> 2) of row i
                             vb[i] = vtile + ((gid >> 2) * BS + rows[i]) * 16 + (gid & 3) * 4;
                         else                // row i; its chunk offset is vswz[i & 1][q4]
-                            vb[i] = vtile + rows[i] * 128 + (gid & 3) * 4;
+                            vb[i] = vtile + rows[i] * T::SROW + (gid & 3) * 4;
                     }
 #pragma unroll
                     for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -1433,6 +1440,59 @@ cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUte
     const int rows = p.batch * p.num_heads;
     return launch_pdl(merge_kernel<D>, dim3((rows + kMergeWarps - 1) / kMergeWarps), dim3(32 * kMergeWarps),
                       size_t(p.batch + 1) * 4, s, p, f);
+}
+
+// The instances of one cache kind and head_dim: block size, 3-bit kv heads
+// per consumer warp, staged granular scales and head-column groups.
+template <int CK, int D>
+cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
+                           const CUtensorMap &mv, cudaStream_t s)
+{
+    if constexpr (CK == kU3) {      // MHA caches: f.hpw kv heads per consumer warp
+        if (p.group == 1) {
+            if (p.block_size == 16) {
+                if (f.hpw == 4) return launch_fast_t<CK, D, 16, 4>(p, f, mk, mv, s);
+                if (f.hpw == 2) return launch_fast_t<CK, D, 16, 2>(p, f, mk, mv, s);
+                return launch_fast_t<CK, D, 16, 1>(p, f, mk, mv, s);
+            }
+            if (p.block_size == 32) {
+                if (f.hpw == 4) return launch_fast_t<CK, D, 32, 4>(p, f, mk, mv, s);
+                if (f.hpw == 2) return launch_fast_t<CK, D, 32, 2>(p, f, mk, mv, s);
+                return launch_fast_t<CK, D, 32, 1>(p, f, mk, mv, s);
+            }
+            if (p.block_size == 64) {
+                if (f.hpw == 4) return launch_fast_t<CK, D, 64, 4>(p, f, mk, mv, s);
+                if (f.hpw == 2) return launch_fast_t<CK, D, 64, 2>(p, f, mk, mv, s);
+                return launch_fast_t<CK, D, 64, 1>(p, f, mk, mv, s);
+            }
+        }
+    }
+    if constexpr (is_q8(CK)) {      // per-block / per-token scales staged with the tiles
+        if (p.scale_mode != 0) {
+            switch (p.block_size) {
+            case 16:
+                return f.ng == 2 ? launch_fast_t<CK, D, 16, 0, true, false, 2>(p, f, mk, mv, s)
+                                 : launch_fast_t<CK, D, 16, 0, true>(p, f, mk, mv, s);
+            case 32:
+                return f.ng == 2 ? launch_fast_t<CK, D, 32, 0, true, false, 2>(p, f, mk, mv, s)
+                                 : launch_fast_t<CK, D, 32, 0, true>(p, f, mk, mv, s);
+            case 64: return launch_fast_t<CK, D, 64, 0, true>(p, f, mk, mv, s);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+    }
+    switch (p.block_size) {
+    case 16:
+        if constexpr (CK != kU3)
+            if (f.ng == 2) return launch_fast_t<CK, D, 16, 0, false, false, 2>(p, f, mk, mv, s);
+        return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
+    case 32:
+        if constexpr (CK != kU3)
+            if (f.ng == 2) return launch_fast_t<CK, D, 32, 0, false, false, 2>(p, f, mk, mv, s);
+        return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
+    case 64: return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace

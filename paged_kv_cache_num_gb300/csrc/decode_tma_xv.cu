@@ -1,7 +1,7 @@
 // decode_tma_xv.cu -- the persistent paged-decode kernel instantiated for
 // x-vectorised caches ([num_blocks][num_kv_heads][head_dim/x][block_size][x],
-// x = 16 bytes / element size): 16-bit (head_dim 64 / 128) and one-byte codes
-// with per-kv-head scales (head_dim 128), block sizes 16, 32 and 64.
+// x = 16 bytes / element size): 16-bit and one-byte codes (one-byte with
+// per-kv-head scales), head_dim 64 / 128, block sizes 16, 32 and 64.
 #include "decode_tma_kernel.cuh"
 
 namespace pkv {
@@ -32,9 +32,12 @@ cudaError_t launch_decode_fast_xv(const DecodeParams &p, const FastParams &f, in
     const CUtensorMap &mv = *static_cast<const CUtensorMap *>(tmv);
     if (p.scale_mode != 0) return cudaErrorInvalidValue;
     switch (cache_kind) {
-    case kE4M3: return launch_xv_bs<kE4M3, 128>(p, f, mk, mv, s);
-    case kE5M2: return launch_xv_bs<kE5M2, 128>(p, f, mk, mv, s);
-    case kI8: return launch_xv_bs<kI8, 128>(p, f, mk, mv, s);
+    case kE4M3:
+        return p.head_dim == 128 ? launch_xv_bs<kE4M3, 128>(p, f, mk, mv, s) : launch_xv_bs<kE4M3, 64>(p, f, mk, mv, s);
+    case kE5M2:
+        return p.head_dim == 128 ? launch_xv_bs<kE5M2, 128>(p, f, mk, mv, s) : launch_xv_bs<kE5M2, 64>(p, f, mk, mv, s);
+    case kI8:
+        return p.head_dim == 128 ? launch_xv_bs<kI8, 128>(p, f, mk, mv, s) : launch_xv_bs<kI8, 64>(p, f, mk, mv, s);
     case kBF16:
         return p.head_dim == 128 ? launch_xv_bs<kBF16, 128>(p, f, mk, mv, s) : launch_xv_bs<kBF16, 64>(p, f, mk, mv, s);
     case kF16:

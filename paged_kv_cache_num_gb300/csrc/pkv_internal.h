@@ -163,6 +163,9 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
 bool fast_maps_encodable(const DecodeParams &p, int cache_kind, int nh);
 // x-vectorised caches (c_chunk != 16): 16-bit or one-byte codes with
 // per-head scales, head_dim 128 (16-bit also 64), block size 16 / 32 / 64
+// one-byte codes at head_dim 64 (decode_tma_d64.cu)
+cudaError_t launch_decode_fast_q8_d64(const DecodeParams &p, const FastParams &f, int cache_kind,
+                                      const void *tmk, const void *tmv, cudaStream_t s);
 cudaError_t launch_decode_fast_xv(const DecodeParams &p, const FastParams &f, int cache_kind,
                                   const void *tmk, const void *tmv, cudaStream_t s);
 

@@ -121,6 +121,34 @@ def test_u3_block_and_group_variants(pkv, orc, BS, H, Hkv):
         _check(w, out, PL.oracle_decode(w, orc, oc))
 
 
+@pytest.mark.parametrize("fp8,scales,G,BS,layout", [
+    ("e4m3", "head", 8, 32, "flash"), ("e5m2", "head", 4, 16, "flash"), ("i8", "head", 1, 64, "flash"),
+    ("e4m3", "block", 8, 16, "flash"), ("e4m3", "token", 4, 32, "flash"), ("i8", "token", 2, 16, "flash"),
+    ("e4m3", "head", 16, 32, "flash"), ("e5m2", "head", 12, 16, "flash"),
+    ("e4m3", "head", 8, 32, "xvec"), ("i8", "head", 4, 16, "xvec")])
+def test_one_byte_head_dim_64(pkv, orc, fp8, scales, G, BS, layout):
+    """One-byte caches at head_dim 64 on the persistent kernel (64-byte rows
+    with the 64-byte swizzle; x-vectorised tiles as stored): e4m3, e5m2 and
+    int8 with per-head, per-block and per-token scales, groups of 1 to 16 q
+    heads, blocks of 16, 32 and 64 slots; against the oracle, through the
+    persistent kernel and the general one."""
+    Hkv = 4
+    w = W.fp8_long(batch=3, ctx_lo=5, ctx_hi=9 * BS + 7, num_heads=G * Hkv, num_kv_heads=Hkv,
+                   head_dim=64, block_size=BS, calib_tokens=64, seed=300 + G + BS, fp8=fp8,
+                   scales=scales, layout=layout)
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    for splits in (0, 2):
+        cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+        _check(w, out, ref)
+        if splits == 0:
+            gc = PL.gpu_cache_host(cache)
+            oc = PL.oracle_caches(w, orc)
+            for k, arr in oc.items():
+                if layout == "xvec" and k in ("k_cache", "v_cache"):
+                    arr = orc.to_xvec(arr, 16)
+                assert np.array_equal(gc[k], arr), k
+
+
 def test_u3_poisoned_tail_metadata(pkv, orc):
     """NaN scales and garbage codes in slots beyond the contexts of a 3-bit
     cache leave the output finite and unchanged."""

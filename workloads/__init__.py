@@ -54,7 +54,7 @@ SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44
          "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48, "i8_long": 49,
          "fp8_long_token_scales": 50, "fp8_long_block_scales": 51,
          "gqa_bf16_xvec": 43, "fp8_long_xvec": 45, "fp8_long_g16": 52,
-         "gqa_bf16_g16": 53}
+         "gqa_bf16_g16": 53, "fp8_long_d64": 54}
 
 
 @dataclass
