@@ -73,7 +73,7 @@ bool fast_decode_supported(int cache_kind, int head_dim, int block_size, int gro
     if (block_size != 16 && block_size != 32 && block_size != 64) return false;
     // groups of up to 16 q heads (two groups of head columns per consumer
     // warp above 8, for blocks of up to 32 slots)
-    if (group > (cache_kind == kU3 ? 8 : 16) || batch > 4096) return false;
+    if (group > 16 || batch > 4096) return false;
     if (group > 8 && block_size > 32) return false;
     if (is_q8(cache_kind)) return head_dim == 128 || head_dim == 64;
     if (cache_kind == kU3) return head_dim == 128;
@@ -91,7 +91,7 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     const int group = num_heads / num_kv_heads;
     // one consumer warp per kv head (at most 8 per CTA), with two groups of
     // 8 head columns for groups above 8 q heads
-    const int ng = !u3 && group > 8 ? 2 : 1;
+    const int ng = group > 8 ? 2 : 1;
     // 3-bit multi-head caches: up to 4 kv heads per consumer warp (a power
     // of two dividing num_kv_heads)
     int hpw = 1;
@@ -103,7 +103,7 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // 3-bit kernels are register-capped so that several CTAs share an SM; the
     // shared memory (228 KB per SM, 1 KB of it reserved per CTA) and the
     // bytes kept in flight are split between them
-    const int ctas_per_sm = u3 ? (hpw > 1 ? kU3MhaCtasPerSm : kU3CtasPerSm) : 1;
+    const int ctas_per_sm = u3 ? u3_ctas_per_sm(hpw, ng) : 1;
     const int budget = (228 * 1024) / ctas_per_sm - 1024;
     // ring depth: enough bytes in flight per SM, within the shared memory
     int stages = 8;

@@ -247,8 +247,14 @@ constexpr int kU3CtasPerSm = 3;
 // copies -- two per SM.
 constexpr int kU3MhaHeads = 16;
 constexpr int kU3MhaCtasPerSm = 2;
-template <int CK, int U3H>
-constexpr int kCtasPerSm = CK == kU3 ? (U3H >= 2 ? kU3MhaCtasPerSm : kU3CtasPerSm) : 1;
+// 3-bit CTAs per SM by kv heads per consumer warp and head-column groups
+// (two groups of 8 q heads hold twice the accumulators: two CTAs per SM)
+__host__ __device__ constexpr int u3_ctas_per_sm(int hpw, int ng)
+{
+    return hpw > 1 ? kU3MhaCtasPerSm : (ng == 2 ? 2 : kU3CtasPerSm);
+}
+template <int CK, int U3H, int NG>
+constexpr int kCtasPerSm = CK == kU3 ? u3_ctas_per_sm(U3H >= 2 ? U3H : 1, NG) : 1;
 template <int CK>
 constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
 
@@ -268,20 +274,19 @@ __host__ __device__ constexpr int u3_conv_bytes_per_warp(int hpw, int bs) { retu
 // one softmax and one walk of the ring serve HPW heads.
 // GSC: fp8 / int8 with per-block or per-token scales, staged per block.
 // XV: x-vectorised cache layout (16-bit and one-byte codes).
-// NG: head-column groups per consumer warp (16-bit and one-byte caches).
-// With NG = 2 a warp serves the up to 16 q heads of its kv head as two
-// groups of 8 columns: every K / V fragment, loaded and converted once,
-// feeds one MMA per group.
-template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
-__global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H>))
-decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  DecodeParams p, FastParams f)
+// NG: head-column groups per consumer warp (grouped q heads).  With NG = 2
+// a warp serves the up to 16 q heads of its kv head as two groups of 8
+// columns: every K / V fragment, loaded and converted once, feeds one MMA
+// per group.
+template <int CK, int D, int BS, int U3H, bool GSC, bool XV, int NG>
+__device__ __forceinline__ void decode_tma_body(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                                const DecodeParams &p, const FastParams &f)
 {
     using T = Tile<CK, D, BS>;
     constexpr int NC = U3H == 1 ? 1 : 2;   // head columns (2tig, 2tig+1) that can exist
     constexpr int HPW = U3H >= 2 ? U3H : 1;  // kv heads per consumer warp
     static_assert(HPW == 1 || (T::kIsU3 && (HPW == 2 || HPW == 4)), "heads per warp");
-    static_assert(NG == 1 || (NG == 2 && !T::kIsU3 && BS <= 32), "head-column groups");
+    static_assert(NG == 1 || (NG == 2 && U3H == 0 && BS <= 32), "head-column groups");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -548,50 +553,68 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             // q' = q qs 2^(1-x) (f16, exact) in the pair order of the K
             // fragments: k-step kk, lane tig holds pair 2kk (k = 2tig, 2tig+1)
             // and pair 2kk+1 (k = 2tig+8, 2tig+9) of 96-bit group tig, so that
-            // q' k' = qs 2^-23 q v for every code.
-            float qv[32];
-            float amax = 0.0f;
+            // q' k' = qs 2^-23 q v for every code.  One power-of-two qs
+            // serves all the warp's head columns (both groups).
+            auto load_q = [&](const uint16_t *qrow, bool has, float (&qv)[32]) -> float {
+                float amax = 0.0f;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (hv) u = *reinterpret_cast<const uint4 *>(qr + 32 * tig + 8 * c4);
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint4 u = make_uint4(0, 0, 0, 0);
+                    if (has) u = *reinterpret_cast<const uint4 *>(qrow + 32 * tig + 8 * c4);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float a, c;
-                    if (p.q_is_bf16) {
-                        a = __uint_as_float(w[e] << 16);
-                        c = __uint_as_float(w[e] & 0xffff0000u);
-                    } else {
-                        const float2 t2 = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-                        a = t2.x;
-                        c = t2.y;
+                    for (int e = 0; e < 4; ++e) {
+                        float a, c;
+                        if (p.q_is_bf16) {
+                            a = __uint_as_float(w[e] << 16);
+                            c = __uint_as_float(w[e] & 0xffff0000u);
+                        } else {
+                            const float2 t2 = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                            a = t2.x;
+                            c = t2.y;
+                        }
+                        qv[8 * c4 + 2 * e] = a;
+                        qv[8 * c4 + 2 * e + 1] = c;
+                        amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c)));
                     }
-                    qv[8 * c4 + 2 * e] = a;
-                    qv[8 * c4 + 2 * e + 1] = c;
-                    amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c)));
                 }
+                return amax;
+            };
+            float qv[32];
+            float amax = load_q(qr, hv, qv);
+            if constexpr (NG1) {
+                float qv1[32];
+                amax = fmaxf(amax, load_q(qr1, hv1, qv1));
             }
 #pragma unroll
             for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
             float qs = 1.0f;
             while (amax * qs > 16384.0f) qs *= 0.5f;
-            float q1 = 0.0f;
+            // the fragments of one group and, per head column 2tig + c, the
+            // sum of q' 2^(x-24) over head_dim
+            auto convert_q = [&](const float (&qv)[32], uint32_t (*qbg)[2], float *q1g) {
+                float q1 = 0.0f;
 #pragma unroll
-            for (int pp = 0; pp < 16; ++pp) {
-                const U3KPair pr = u3k_pair_info(pp);
-                float ra, rb;
-                const uint32_t w = pack_f16(qv[pr.i] * qs * (2.0f / float(1 << pr.x)),
-                                            qv[pr.j] * qs * (2.0f / float(1 << pr.y)), ra, rb);
-                qb[pp >> 1][pp & 1] = w;
-                q1 += ra * (float(1 << pr.x) * 0x1p-24f) + rb * (float(1 << pr.y) * 0x1p-24f);
-            }
-            q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
-            q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+                for (int pp = 0; pp < 16; ++pp) {
+                    const U3KPair pr = u3k_pair_info(pp);
+                    float ra, rb;
+                    const uint32_t w = pack_f16(qv[pr.i] * qs * (2.0f / float(1 << pr.x)),
+                                                qv[pr.j] * qs * (2.0f / float(1 << pr.y)), ra, rb);
+                    qbg[pp >> 1][pp & 1] = w;
+                    q1 += ra * (float(1 << pr.x) * 0x1p-24f) + rb * (float(1 << pr.y) * 0x1p-24f);
+                }
+                q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+                q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {       // values of head columns 2tig, 2tig+1
-                q1h[c] = __shfl_sync(0xffffffffu, q1, 4 * (2 * tig + c));
-                zs[c] = 0.0f;
+                for (int c = 0; c < 2; ++c) q1g[c] = __shfl_sync(0xffffffffu, q1, 4 * (2 * tig + c));
+            };
+            convert_q(qv, qb, q1h);
+            zs[0] = zs[1] = 0.0f;
+            if constexpr (NG1) {
+                float qv1[32];
+                load_q(qr1, hv1, qv1);     // (read again: fewer live registers)
+                convert_q(qv1, qb1, q1h1);
+                zs1[0] = zs1[1] = 0.0f;
             }
             mult = log2e_scale * 0x1p23f / qs;
             vmul = 1.0f;
@@ -825,6 +848,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         // HPW > 1 each head's product keeps only its own column: heads 2i
         // and 2i+1 fill columns (0, 1) of lanes tig = i.
         float sc[KTT][4];
+        [[maybe_unused]] float sc1[NG1 ? KTT : 1][4];
 #pragma unroll
         for (int mt = 0; mt < KTT; ++mt) {
             float colp[HPW > 1 ? HPW / 2 : 1][4];
@@ -832,6 +856,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int hh = 0; hh < HPW; ++hh) {
                 float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 float sx[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // second chain (odd k-steps)
+                [[maybe_unused]] float acc1[NG1 ? 4 : 1] = {}, sx1[NG1 ? 4 : 1] = {};   // second group
                 const uint32_t a0 = kpk(mt, hh) + gid * ts + 12 * tig;
                 const uint32_t a1 = a0 + 8 * ts;
                 const uint32_t x0 = ld_shared_u32(a0), x1 = ld_shared_u32(a0 + 4), x2 = ld_shared_u32(a0 + 8);
@@ -844,9 +869,11 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     a[2] = u3k_pair(2 * kk + 1, x0, x1, x2);
                     a[3] = u3k_pair(2 * kk + 1, y0, y1, y2);
                     ptx::mma16816<false>((kk & 1) ? sx : acc, a, qb[kk][0], qb[kk][1]);
+                    if constexpr (NG1) ptx::mma16816<false>((kk & 1) ? sx1 : acc1, a, qb1[kk][0], qb1[kk][1]);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
+                    if constexpr (NG1) sc1[mt][e] = acc1[e] + sx1[e];
                     if (HPW == 1)
                         colp[0][e] = acc[e] + sx[e];
                     else if ((e & 1) == (hh & 1))
@@ -858,64 +885,72 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 sc[mt][e] = HPW == 4 ? (tig == 0 ? colp[0][e] : colp[HPW > 2 ? 1 : 0][e]) : colp[0][e];
         }
         // ---- scores: remove the zero point, apply the per-token
-        // scale, mask; online softmax per head column
-        float mx[2] = {NEG_INF, NEG_INF};
+        // scale, mask; online softmax per head column.  One group of head
+        // columns: scores scg, running max mg / sums lg / P' * zero sums zsg,
+        // q' sums q1g, accumulators og; P'^T (B operand of the PV product)
+        // in ptg: pt[t][r] gives lane (gid, tig) the P' of tokens 8r + 2tig,
+        // +1 of tile t in head column gid
+        auto u3_softmax = [&](float (*scg)[4], float *mg, float *lg, float *zsg, const float *q1g,
+                              uint32_t (*ptg)[2], float (*og)[4]) {
+            float mx[2] = {NEG_INF, NEG_INF};
 #pragma unroll
-        for (int t = 0; t < KTT; ++t)
+            for (int t = 0; t < KTT; ++t)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e >> 1, c = e & 1;
-                if (c >= NC) continue;
-                const float2 kz = *reinterpret_cast<const float2 *>(meta_of(t, r, c));   // (sk, zk)
-                float v = mult * kz.x * (sc[t][e] - kz.y * q1h[c]);
-                if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
-                sc[t][e] = v;
-                mx[c] = fmaxf(mx[c], v);
+                for (int e = 0; e < 4; ++e) {
+                    const int r = e >> 1, c = e & 1;
+                    if (c >= NC) continue;
+                    const float2 kz = *reinterpret_cast<const float2 *>(meta_of(t, r, c));   // (sk, zk)
+                    float v = mult * kz.x * (scg[t][e] - kz.y * q1g[c]);
+                    if (partial) v = (16 * t + gid + 8 * r) < valid ? v : NEG_INF;
+                    scg[t][e] = v;
+                    mx[c] = fmaxf(mx[c], v);
+                }
+            float alpha[2] = {1.0f, 1.0f};
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+                const float mn = fmaxf(mg[c], mx[c]);
+                alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(mg[c] - mn);
+                mg[c] = mn;
+                lg[c] *= alpha[c];
+                zsg[c] *= alpha[c];
             }
-        float alpha[2] = {1.0f, 1.0f};
+            // P' = p * v_scale (0 for masked tokens), transposed by movmatrix
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-            mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-            const float mn = fmaxf(m[c], mx[c]);
-            alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(m[c] - mn);
-            m[c] = mn;
-            l[c] *= alpha[c];
-            zs[c] *= alpha[c];
-        }
-        // P' = p * v_scale (0 for masked tokens), transposed by movmatrix:
-        // pt[t][r] gives lane (gid, tig) the P' of tokens 8r + 2tig, +1 of
-        // tile t in head column gid
-        uint32_t pt[KTT][2];
+            for (int t = 0; t < KTT; ++t)
 #pragma unroll
-        for (int t = 0; t < KTT; ++t)
+                for (int r = 0; r < 2; ++r) {
+                    const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
+                    const float2 vz0 = *reinterpret_cast<const float2 *>(&meta_of(t, r, 0)->z);   // (sv, zv)
+                    const float2 vz1 = HPW > 1 ? *reinterpret_cast<const float2 *>(&meta_of(t, r, 1)->z) : vz0;
+                    const float p0 = exp2_approx(scg[t][2 * r] - mg[0]);
+                    const float p1 = NC > 1 ? exp2_approx(scg[t][2 * r + 1] - mg[1]) : 0.0f;
+                    lg[0] += p0;
+                    if (NC > 1) lg[1] += p1;
+                    float q0, q1;
+                    const uint32_t w = pack_f16(ok ? p0 * vz0.x : 0.0f, ok ? p1 * vz1.x : 0.0f, q0, q1);
+                    zsg[0] += q0 * vz0.y;
+                    if (NC > 1) zsg[1] += q1 * vz1.y;
+                    ptg[t][r] = ptx::movmatrix_trans(w);
+                }
+            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const bool ok = !partial || (16 * t + gid + 8 * r) < valid;
-                const float2 vz0 = *reinterpret_cast<const float2 *>(&meta_of(t, r, 0)->z);   // (sv, zv)
-                const float2 vz1 = HPW > 1 ? *reinterpret_cast<const float2 *>(&meta_of(t, r, 1)->z) : vz0;
-                const float p0 = exp2_approx(sc[t][2 * r] - m[0]);
-                const float p1 = NC > 1 ? exp2_approx(sc[t][2 * r + 1] - m[1]) : 0.0f;
-                l[0] += p0;
-                if (NC > 1) l[1] += p1;
-                float q0, q1;
-                const uint32_t w = pack_f16(ok ? p0 * vz0.x : 0.0f, ok ? p1 * vz1.x : 0.0f, q0, q1);
-                zs[0] += q0 * vz0.y;
-                if (NC > 1) zs[1] += q1 * vz1.y;
-                pt[t][r] = ptx::movmatrix_trans(w);
-            }
-        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-            for (int t = 0; t < T::DT / 2; ++t) {
-                o[t][0] *= alpha[0];
-                o[t][2] *= alpha[0];
-                if (NC > 1) {
-                    o[t][1] *= alpha[1];
-                    o[t][3] *= alpha[1];
+                for (int t = 0; t < T::DT / 2; ++t) {
+                    og[t][0] *= alpha[0];
+                    og[t][2] *= alpha[0];
+                    if (NC > 1) {
+                        og[t][1] *= alpha[1];
+                        og[t][3] *= alpha[1];
+                    }
                 }
             }
-        }
+        };
+        uint32_t pt[KTT][2];
+        [[maybe_unused]] uint32_t pt1[NG1 ? KTT : 1][2];
+        u3_softmax(sc, m, l, zs, q1h, pt, o);
+        if constexpr (NG1) u3_softmax(sc1, m1, l1, zs1, q1h1, pt1, o1);
         // ---- O^T += V'^T P'^T with V converted straight into A fragments:
         // lane (gid, tig) owns codes 16gid .. 16gid+15 (row bytes 6gid ..
         // 6gid+5) of two token rows ra0, ra0+1 of head ha (k = 2tig, 2tig+1)
@@ -934,8 +969,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int kt = 0; kt < KTT; ++kt) {
 #pragma unroll
             for (int ps = 0; ps < NP; ++ps) {
-                const int r = HPW == 4 ? (ps >> 1) : ps;
-                const int j = HPW == 4 ? (ps & 1) : 0;
+                [[maybe_unused]] const int r = HPW == 4 ? (ps >> 1) : ps;
+                [[maybe_unused]] const int j = HPW == 4 ? (ps & 1) : 0;
                 int ha = 0, hb = 0, ra0 = 2 * tig, rb0 = 2 * tig + 8;
                 uint32_t b0 = pt[kt][0], b1 = pt[kt][1];
                 if constexpr (HPW > 1) {
@@ -975,6 +1010,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     a[2] = win[1][u3v_win(2 * md)] & (kMask3 << u3v_x(2 * md));
                     a[3] = win[1][u3v_win(2 * md + 1)] & (kMask3 << u3v_x(2 * md + 1));
                     ptx::mma16816<false>(o[md], a, b0, b1);
+                    if constexpr (NG1) ptx::mma16816<false>(o1[md], a, pt1[kt][0], pt1[kt][1]);
                 }
             }
         }
@@ -1198,7 +1234,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             // barrier and walk work is then shared by 32 tokens (warps of
             // several heads share it between their heads instead, and keep
             // one block per step so that more of the ring is in flight)
-            const bool pair = BS == 16 && HPW == 1 && x + 1 < hi && j + 1 < nblk[b];
+            const bool pair = BS == 16 && HPW == 1 && NG == 1 && x + 1 < hi && j + 1 < nblk[b];
             if (pair) {
                 const int s1 = cs;
                 if (!ptx::mbar_wait_bounded(bar_full + 8 * s1, cphase, kTimeoutNs)) {
@@ -1213,7 +1249,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int valid1 = min(BS, ctx_b - (j + 1) * BS);
                 if (spb >= 0 && spb1 >= 0) {
                     // (only one-head warps pair blocks, of 16 tokens)
-                    u3_body(std::integral_constant<int, HPW == 1 && BS == 16 ? 2 : 1>{}, s, s1, BS + valid1);
+                    u3_body(std::integral_constant<int, HPW == 1 && BS == 16 && NG == 1 ? 2 : 1>{}, s, s1, BS + valid1);
                 } else {
                     if (spb >= 0) u3_body(std::integral_constant<int, 1>{}, s, s, valid);
                     if (spb1 >= 0) u3_body(std::integral_constant<int, 1>{}, s1, s1, valid1);
@@ -1246,6 +1282,26 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             finish_segment(x);
         }
     }
+}
+
+template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
+__global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H, NG>))
+decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  DecodeParams p, FastParams f)
+{
+    decode_tma_body<CK, D, BS, U3H, GSC, XV, NG>(tmk, tmv, p, f);
+}
+
+// 3-bit caches with two groups of head columns: twice the accumulators, two
+// CTAs per SM under a hard register cap (__maxnreg__; a launch bound makes
+// the compiler settle far lower and spill)
+constexpr int kU3GroupRegs = 200;   // 65536 / (2 CTAs x 160 threads), in units of 8
+template <int D, int BS>
+__global__ void __maxnreg__(kU3GroupRegs)
+decode_tma_u3g_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                      DecodeParams p, FastParams f)
+{
+    decode_tma_body<kU3, D, BS, 0, false, false, 2>(tmk, tmv, p, f);
 }
 
 // floor(a / n) for 0 <= a < 2^62, 0 < n < 2^31: a float estimate corrected
@@ -1423,7 +1479,9 @@ template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false,
 cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                           const CUtensorMap &mv, cudaStream_t s)
 {
-    auto kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV, NG>;
+    void (*kern)(CUtensorMap, CUtensorMap, DecodeParams, FastParams);
+    if constexpr (CK == kU3 && NG == 2) kern = decode_tma_u3g_kernel<D, BS>;
+    else kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV, NG>;
     // dynamic shared memory limit, raised once per device as needed
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
@@ -1483,12 +1541,10 @@ cudaError_t launch_fast_bs(const DecodeParams &p, const FastParams &f, const CUt
     }
     switch (p.block_size) {
     case 16:
-        if constexpr (CK != kU3)
-            if (f.ng == 2) return launch_fast_t<CK, D, 16, 0, false, false, 2>(p, f, mk, mv, s);
+        if (f.ng == 2) return launch_fast_t<CK, D, 16, 0, false, false, 2>(p, f, mk, mv, s);
         return launch_fast_t<CK, D, 16>(p, f, mk, mv, s);
     case 32:
-        if constexpr (CK != kU3)
-            if (f.ng == 2) return launch_fast_t<CK, D, 32, 0, false, false, 2>(p, f, mk, mv, s);
+        if (f.ng == 2) return launch_fast_t<CK, D, 32, 0, false, false, 2>(p, f, mk, mv, s);
         return launch_fast_t<CK, D, 32>(p, f, mk, mv, s);
     case 64: return launch_fast_t<CK, D, 64>(p, f, mk, mv, s);
     default: return cudaErrorInvalidValue;

@@ -555,11 +555,12 @@ def test_u3_bad_block_ids_in_pairs(pkv, orc):
 @pytest.mark.parametrize("kind,G,layout", [("bf16", 16, "flash"), ("bf16", 12, "flash"), ("f16", 16, "flash"),
                                            ("bf16", 16, "xvec"), ("e4m3", 16, "flash"), ("i8", 12, "flash"),
                                            ("e4m3", 16, "xvec")])
-def test_large_groups_two_warps_per_kv_head(pkv, orc, kind, G, layout):
+def test_large_groups_two_column_groups(pkv, orc, kind, G, layout):
     """Groups of 9..16 q heads per kv head (Llama-3.1-405B: 128 q / 8 kv):
-    the persistent kernel gives each kv head two consumer warps, one per 8 q
-    heads (the second with G - 8 of them); parity with the oracle, on the
-    persistent kernel (no explicit split) and the general one."""
+    the persistent kernel's warp of a kv head serves them as two groups of
+    8 head columns (the second with G - 8 of them), each K / V fragment
+    feeding one MMA per group; parity with the oracle, on the persistent
+    kernel (no explicit split) and the general one."""
     Hkv = 4
     if kind in ("bf16", "f16"):
         w = W.gqa_bf16(batch=5, ctx_lo=1, ctx_hi=1500, num_heads=G * Hkv, num_kv_heads=Hkv,
@@ -577,6 +578,30 @@ def test_large_groups_two_warps_per_kv_head(pkv, orc, kind, G, layout):
         cache, out = PL.gpu_run(w, pkv, num_splits=splits)
         if splits == 0:
             assert pkv.decode_launches(w.q.cuda(), cache, w.block_tables.cuda()) == 2  # persistent
+        _check(w, out, ref)
+
+
+@pytest.mark.parametrize("BS,G,Hkv", [(16, 16, 4), (32, 16, 2), (16, 12, 2), (32, 9, 3), (16, 10, 1)])
+def test_u3_large_groups(pkv, orc, BS, G, Hkv):
+    """3-bit caches with groups of 9..16 q heads per kv head: two groups of
+    head columns per consumer warp, the codes of each K / V fragment
+    unpacked once for both; blocks of 16 and 32 slots, 1 to 4 kv heads;
+    parity with the oracle on the persistent kernel and the general one, and
+    the cache as written bit-exact."""
+    H = G * Hkv
+    w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=9 * BS + 5, num_heads=Hkv, block_size=BS, seed=400 + G + BS)
+    g = torch.Generator().manual_seed(401 + G)
+    w.num_heads = H
+    w.q = torch.randn(w.batch, H, w.head_dim, generator=g).to(w.dtype)
+    oc = PL.oracle_caches(w, orc)
+    ref = PL.oracle_decode(w, orc, oc)
+    for splits in (0, 3):
+        cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+        if splits == 0:
+            assert pkv.decode_launches(w.q.cuda(), cache, w.block_tables.cuda()) == 2  # persistent
+            gc = PL.gpu_cache_host(cache)
+            for k in oc:
+                assert np.array_equal(gc[k], oc[k]), k
         _check(w, out, ref)
 
 
