@@ -249,6 +249,9 @@ def make_workload(name, device, rank=0):
         return W.fp8_long(device=device, seed=seed, head_dim=64)
     if name == "u3_mha":
         return W.u3_mha(device=device, seed=seed)
+    if name in ("u3_g16", "u3_g8"):
+        return W.u3_mha(device=device, seed=seed, batch=16, ctx_lo=8192, ctx_hi=32768,
+                        num_heads=128 if name == "u3_g16" else 64, num_kv_heads=8)
     if name == "mixed_append":
         return W.mixed_append(device=device, seed=seed)
     if name == "mha_short":
@@ -705,7 +708,7 @@ def main():
     ap.add_argument("--workload", default="fp8_long")
     ap.add_argument("--extra", default="gqa_bf16,u3_mha,mixed_append,mha_short,fp8_long_e5m2,i8_long,"
                                        "fp8_long_token_scales,fp8_long_block_scales,gqa_bf16_xvec,"
-                                       "fp8_long_xvec,fp8_long_g16,gqa_bf16_g16,fp8_long_d64",
+                                       "fp8_long_xvec,fp8_long_g16,gqa_bf16_g16,fp8_long_d64,u3_g8,u3_g16",
                     help="other workloads measured in the same run ('' for none)")
     ap.add_argument("--extra-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=300)

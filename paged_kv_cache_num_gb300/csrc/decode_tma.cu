@@ -60,9 +60,13 @@ bool make_map(CUtensorMap *m, const void *base, int ck, int D, int BS, int Hkv, 
     cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapSwizzle sw = u3 ? CU_TENSOR_MAP_SWIZZLE_NONE
                                      : (sub_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    // 3-bit boxes read runs of nh * 48-byte rows that neighbouring head
+    // groups (other CTAs, at other times) continue: no L2 promotion, which
+    // would fetch up to 256 bytes around each run and read the cache
+    // again for the next group
+    const CUtensorMapL2promotion l2p = u3 ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     const CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2p, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -278,9 +278,10 @@ __host__ __device__ constexpr int u3_conv_bytes_per_warp(int hpw, int bs) { retu
 // a warp serves the up to 16 q heads of its kv head as two groups of 8
 // columns: every K / V fragment, loaded and converted once, feeds one MMA
 // per group.
-template <int CK, int D, int BS, int U3H, bool GSC, bool XV, int NG>
-__device__ __forceinline__ void decode_tma_body(const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                                const DecodeParams &p, const FastParams &f)
+template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
+__global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H, NG>))
+decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  DecodeParams p, FastParams f)
 {
     using T = Tile<CK, D, BS>;
     constexpr int NC = U3H == 1 ? 1 : 2;   // head columns (2tig, 2tig+1) that can exist
@@ -1284,26 +1285,6 @@ __device__ __forceinline__ void decode_tma_body(const CUtensorMap &tmk, const CU
     }
 }
 
-template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
-__global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H, NG>))
-decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  DecodeParams p, FastParams f)
-{
-    decode_tma_body<CK, D, BS, U3H, GSC, XV, NG>(tmk, tmv, p, f);
-}
-
-// 3-bit caches with two groups of head columns: twice the accumulators, two
-// CTAs per SM under a hard register cap (__maxnreg__; a launch bound makes
-// the compiler settle far lower and spill)
-constexpr int kU3GroupRegs = 200;   // 65536 / (2 CTAs x 160 threads), in units of 8
-template <int D, int BS>
-__global__ void __maxnreg__(kU3GroupRegs)
-decode_tma_u3g_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                      DecodeParams p, FastParams f)
-{
-    decode_tma_body<kU3, D, BS, 0, false, false, 2>(tmk, tmv, p, f);
-}
-
 // floor(a / n) for 0 <= a < 2^62, 0 < n < 2^31: a float estimate corrected
 // by exact integer comparisons (cheaper than a 64-bit division).
 __device__ __forceinline__ int64_t floordiv_i64(int64_t a, int64_t n)
@@ -1479,9 +1460,7 @@ template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false,
 cudaError_t launch_fast_t(const DecodeParams &p, const FastParams &f, const CUtensorMap &mk,
                           const CUtensorMap &mv, cudaStream_t s)
 {
-    void (*kern)(CUtensorMap, CUtensorMap, DecodeParams, FastParams);
-    if constexpr (CK == kU3 && NG == 2) kern = decode_tma_u3g_kernel<D, BS>;
-    else kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV, NG>;
+    auto kern = decode_tma_kernel<CK, D, BS, U3H, GSC, XV, NG>;
     // dynamic shared memory limit, raised once per device as needed
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;

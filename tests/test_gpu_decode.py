@@ -347,6 +347,13 @@ def test_full_i8_long(pkv, orc):
     _full_size(W.fp8_long(seed=W.SEEDS["i8_long"], fp8="i8"), pkv, orc, paths=("step",))
 
 
+def test_full_u3_g16(pkv, orc):
+    """Full-size grouped 3-bit step (batch 16, 128 q / 8 kv heads, contexts
+    U{8192..32768}, blocks of 16): every row and the whole pool."""
+    _full_size(W.u3_mha(batch=16, ctx_lo=8192, ctx_hi=32768, num_heads=128, num_kv_heads=8,
+                        seed=W.SEEDS["u3_g16"]), pkv, orc)
+
+
 def test_full_u3_mha(pkv, orc):
     """Full-size 3-bit MHA workload (batch 32, 32 heads, contexts
     1024..8192)."""
@@ -588,11 +595,8 @@ def test_u3_large_groups(pkv, orc, BS, G, Hkv):
     unpacked once for both; blocks of 16 and 32 slots, 1 to 4 kv heads;
     parity with the oracle on the persistent kernel and the general one, and
     the cache as written bit-exact."""
-    H = G * Hkv
-    w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=9 * BS + 5, num_heads=Hkv, block_size=BS, seed=400 + G + BS)
-    g = torch.Generator().manual_seed(401 + G)
-    w.num_heads = H
-    w.q = torch.randn(w.batch, H, w.head_dim, generator=g).to(w.dtype)
+    w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=9 * BS + 5, num_heads=G * Hkv, num_kv_heads=Hkv, block_size=BS,
+                 seed=400 + G + BS)
     oc = PL.oracle_caches(w, orc)
     ref = PL.oracle_decode(w, orc, oc)
     for splits in (0, 3):

@@ -54,7 +54,7 @@ SEEDS = {"tiny_fp16": 42, "tiny_literal": 42, "gqa_bf16": 43, "mixed_append": 44
          "fp8_long": 45, "u3_mha": 46, "mha_short": 47, "fp8_long_e5m2": 48, "i8_long": 49,
          "fp8_long_token_scales": 50, "fp8_long_block_scales": 51,
          "gqa_bf16_xvec": 43, "fp8_long_xvec": 45, "fp8_long_g16": 52,
-         "gqa_bf16_g16": 53, "fp8_long_d64": 54}
+         "gqa_bf16_g16": 53, "fp8_long_d64": 54, "u3_g16": 55, "u3_g8": 56}
 
 
 @dataclass
@@ -311,11 +311,13 @@ def fp8_long(device="cpu", batch=16, ctx_lo=16384, ctx_hi=32768, num_heads=64, n
 
 
 def u3_mha(device="cpu", batch=32, ctx_lo=1024, ctx_hi=8192, num_heads=32, head_dim=128,
-           block_size=16, seed=None) -> Workload:
-    """3-bit packed MHA cache, fp16 (defaults: the full-size case)."""
+           block_size=16, seed=None, num_kv_heads=None) -> Workload:
+    """3-bit packed cache, fp16: MHA (defaults: the full-size case), or
+    grouped q heads with num_kv_heads < num_heads."""
     g = _gen(SEEDS["u3_mha"] if seed is None else seed, device)
     dt = torch.float16
     B, H, D, BS = batch, num_heads, head_dim, block_size
+    Hkv = H if num_kv_heads is None else num_kv_heads
     ctx = _randint(ctx_lo, ctx_hi, B, g, device).to(torch.int32)
     ctx_list = ctx.tolist()
     nb = [_cdiv(int(c), BS) for c in ctx_list]
@@ -325,13 +327,13 @@ def u3_mha(device="cpu", batch=32, ctx_lo=1024, ctx_hi=8192, num_heads=32, head_
     q = _randn((B, H, D), g, device, dt)
     fill_req, fill_pos = _fill_lists(ctx_list, device)
     n_fill = int(fill_req.shape[0])
-    k_fill = _randn((n_fill, H, D), g, device, dt)
-    v_fill = _randn((n_fill, H, D), g, device, dt)
-    k_new = _randn((B, H, D), g, device, dt)
-    v_new = _randn((B, H, D), g, device, dt)
+    k_fill = _randn((n_fill, Hkv, D), g, device, dt)
+    v_fill = _randn((n_fill, Hkv, D), g, device, dt)
+    k_new = _randn((B, Hkv, D), g, device, dt)
+    v_new = _randn((B, Hkv, D), g, device, dt)
     new_req = torch.arange(B, dtype=torch.int32, device=device)
     new_pos = (ctx - 1).to(torch.int32)
-    w = Workload("u3_mha", dt, "u3", B, H, H, D, BS, P, ctx, bt, q, new_req, new_pos,
+    w = Workload("u3_mha" if Hkv == H else "u3_gqa", dt, "u3", B, H, Hkv, D, BS, P, ctx, bt, q, new_req, new_pos,
                  k_new, v_new, fill_req=fill_req, fill_pos=fill_pos, k_fill=k_fill,
                  v_fill=v_fill)
     w.extra["context"] = "U{%d..%d}" % (ctx_lo, ctx_hi)
