@@ -374,6 +374,25 @@ __device__ __forceinline__ float u3_quotient(float x, float s, float rs)
     return __fmaf_rn(__fmaf_rn(-y1, s, x), rs, y1);
 }
 
+// min / max of two pairs of 16-bit floats (non-NaN operand wins, as fminf /
+// fmaxf); exact, the values being 16-bit floats
+template <int SRC>
+__device__ __forceinline__ uint32_t min2_16(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    if constexpr (SRC == kBF16) asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else asm("min.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <int SRC>
+__device__ __forceinline__ uint32_t max2_16(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    if constexpr (SRC == kBF16) asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // 3-bit affine quantise + pack: LPR = 4 lanes per (token, head, K|V) row,
 // eight rows per warp.  Each lane holds EPL = head_dim / 4 consecutive
 // elements; a row's min / max are two-step shuffle reductions among its
@@ -402,9 +421,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
         const int h = r >> 1, kv = r & 1;
         int64_t blk = 0, off = 0;
         const bool live = t < p.num_tokens && resolve_slot(p, t, blk, off, r == 0 && sub == 0);
-        float x[EPL];
+        // the lane's EPL source values as pairs of 16-bit floats
+        uint32_t wv[EPL / 2];
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) x[j] = 0.0f;
+        for (int j = 0; j < EPL / 2; ++j) wv[j] = 0u;
         if (live) {
             const uint16_t *src = reinterpret_cast<const uint16_t *>(
                 kv ? p.v_new + t * p.v_src_tok + h * p.v_src_head
@@ -413,21 +433,31 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
 #pragma unroll
                 for (int v = 0; v < EPL / 8; ++v) {
                     const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-                    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        x[8 * v + 2 * k] = h2f<SRC>(uint16_t(ww[k]));
-                        x[8 * v + 2 * k + 1] = h2f<SRC>(uint16_t(ww[k] >> 16));
-                    }
+                    wv[4 * v] = u.x;
+                    wv[4 * v + 1] = u.y;
+                    wv[4 * v + 2] = u.z;
+                    wv[4 * v + 3] = u.w;
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < EPL; ++j) x[j] = h2f<SRC>(src[j]);
+                for (int j = 0; j < EPL / 2; ++j) wv[j] = uint32_t(src[2 * j]) | (uint32_t(src[2 * j + 1]) << 16);
             }
         }
-        float mn = x[0], mx = x[0];
+        float x[EPL];
 #pragma unroll
-        for (int j = 1; j < EPL; ++j) { mn = fminf(mn, x[j]); mx = fmaxf(mx, x[j]); }
+        for (int j = 0; j < EPL / 2; ++j) {
+            x[2 * j] = h2f<SRC>(uint16_t(wv[j]));
+            x[2 * j + 1] = h2f<SRC>(uint16_t(wv[j] >> 16));
+        }
+        // the lane's min / max: pairwise in 16 bits, then its two halves
+        uint32_t mn2 = wv[0], mx2 = wv[0];
+#pragma unroll
+        for (int j = 1; j < EPL / 2; ++j) {
+            mn2 = min2_16<SRC>(mn2, wv[j]);
+            mx2 = max2_16<SRC>(mx2, wv[j]);
+        }
+        float mn = fminf(h2f<SRC>(uint16_t(mn2)), h2f<SRC>(uint16_t(mn2 >> 16)));
+        float mx = fmaxf(h2f<SRC>(uint16_t(mx2)), h2f<SRC>(uint16_t(mx2 >> 16)));
 #pragma unroll
         for (int o = 1; o < LPR; o <<= 1) {   // within the row's lanes
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -443,16 +473,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_u3_kernel(AppendParams 
         float z = 0.0f;
         if (s != 0.0f) z = fminf(fmaxf(rintf(u3_quotient(-mn, s, rs)), 0.0f), 7.0f);
         // fields: codes q_j = clamp(rint(fl(x_j / s)) + z, 0, 7) at bits 3j
-        // (small integers, exact in fp32)
+        // (small integers, exact in fp32).  A constant row (s = 0: every x_j
+        // equal and finite) has rs = 0 and z = 0, so its quotients are 0 and
+        // its codes 0 without a test per element.
         uint32_t f[NF];
 #pragma unroll
         for (int fi = 0; fi < NF; ++fi) {
             float fv = 0.0f;
 #pragma unroll
             for (int j = 7; j >= 0; --j) {
-                const float q = s != 0.0f
-                    ? fminf(fmaxf(__fadd_rn(rintf(u3_quotient(x[8 * fi + j], s, rs)), z), 0.0f), 7.0f)
-                    : 0.0f;
+                const float q = fminf(fmaxf(__fadd_rn(rintf(u3_quotient(x[8 * fi + j], s, rs)), z), 0.0f), 7.0f);
                 fv = fmaf(fv, 8.0f, q);
             }
             f[fi] = uint32_t(fv);
