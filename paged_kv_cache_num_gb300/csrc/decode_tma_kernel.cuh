@@ -906,17 +906,22 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     scg[t][e] = v;
                     mx[c] = fmaxf(mx[c], v);
                 }
+            // (a block that raises no running max skips the reductions and
+            // the rescale, as in the other caches' softmax)
             float alpha[2] = {1.0f, 1.0f};
+            const bool raise = __any_sync(0xffffffffu, mx[0] > mg[0] || (NC > 1 && mx[1] > mg[1]));
+            if (raise) {
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-                const float mn = fmaxf(mg[c], mx[c]);
-                alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(mg[c] - mn);
-                mg[c] = mn;
-                lg[c] *= alpha[c];
-                zsg[c] *= alpha[c];
+                for (int c = 0; c < NC; ++c) {
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+                    const float mn = fmaxf(mg[c], mx[c]);
+                    alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(mg[c] - mn);
+                    mg[c] = mn;
+                    lg[c] *= alpha[c];
+                    zsg[c] *= alpha[c];
+                }
             }
             // P' = p * v_scale (0 for masked tokens), transposed by movmatrix
 #pragma unroll
@@ -936,7 +941,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     if (NC > 1) zsg[1] += q1 * vz1.y;
                     ptg[t][r] = ptx::movmatrix_trans(w);
                 }
-            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+            if (raise && __any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
                 for (int t = 0; t < T::DT / 2; ++t) {
                     og[t][0] *= alpha[0];
@@ -1113,17 +1118,24 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         mx[e & 1] = fmaxf(mx[e & 1], v);
                     }
                 }
-                float alpha[2];
+                // A block none of whose scores passes the running max leaves
+                // it (and the sums) as they are: the warp then skips the
+                // reductions and the rescale.  (The first block of a segment
+                // always raises it from -inf.)
+                float alpha[2] = {1.0f, 1.0f};
+                const bool raise = __any_sync(0xffffffffu, mx[0] > mg[0] || mx[1] > mg[1]);
+                if (raise) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-                    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-                    const float mn = fmaxf(mg[c], mx[c]);
-                    alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(mg[c] - mn);
-                    mg[c] = mn;
-                    lg[c] *= alpha[c];
-                    if constexpr (CK == kI8) zsg[c] *= alpha[c];
+                    for (int c = 0; c < 2; ++c) {
+                        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+                        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+                        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+                        const float mn = fmaxf(mg[c], mx[c]);
+                        alpha[c] = mn == NEG_INF ? 1.0f : exp2_approx(mg[c] - mn);
+                        mg[c] = mn;
+                        lg[c] *= alpha[c];
+                        if constexpr (CK == kI8) zsg[c] *= alpha[c];
+                    }
                 }
 #pragma unroll
                 for (int t = 0; t < T::KT; ++t) {
@@ -1144,7 +1156,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         pbg[t][r] = ptx::movmatrix_trans(w);
                     }
                 }
-                if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+                if (raise && __any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
                     for (int t = 0; t < T::DT / 2; ++t) {
                         og[t][0] *= alpha[0];
