@@ -628,3 +628,27 @@ def test_full_fp8_long_g16(pkv, orc):
     kv heads, e4m3)."""
     _full_size(W.fp8_long(seed=W.SEEDS["fp8_long_g16"], num_heads=128), pkv, orc,
                paths=("step",))
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "i8", "u3", "u3_g4"])
+@pytest.mark.parametrize("sm_scale", [-0.0883883476, 0.0, 0.75])
+def test_softmax_scale_sign_zero_and_sharp(pkv, orc, kind, sm_scale):
+    """The softmax scale at its edges: negative (the softmax of -q.k), zero
+    (uniform weights: each output row is the mean of its V rows) and large
+    (a sharp softmax whose logits span hundreds of log2 units), on the
+    persistent kernel and the general one, 16-bit, one-byte and 3-bit
+    caches; against the oracle at the same scale."""
+    if kind == "bf16":
+        w = W.gqa_bf16(batch=3, ctx_lo=1, ctx_hi=300, num_heads=8, num_kv_heads=2, seed=500)
+    elif kind in ("e4m3", "i8"):
+        w = W.fp8_long(batch=3, ctx_lo=5, ctx_hi=400, num_heads=16, num_kv_heads=2, calib_tokens=64,
+                       seed=501, fp8=kind)
+    elif kind == "u3":
+        w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=300, num_heads=8, seed=502)
+    else:
+        w = W.u3_mha(batch=3, ctx_lo=1, ctx_hi=300, num_heads=8, num_kv_heads=2, seed=503)
+    w.sm_scale = sm_scale
+    ref = PL.oracle_decode(w, orc, PL.oracle_caches(w, orc))
+    for splits in (0, 2):
+        cache, out = PL.gpu_run(w, pkv, num_splits=splits)
+        _check(w, out, ref)

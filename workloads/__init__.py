@@ -111,8 +111,13 @@ class Workload:
 
     @property
     def sm_scale(self) -> float:
-        # 1/sqrt(head_dim), rounded to fp32 (the value both sides receive)
-        return float(torch.tensor(1.0 / math.sqrt(self.head_dim), dtype=torch.float32))
+        # 1/sqrt(head_dim) unless set, rounded to fp32 (the value both sides receive)
+        v = self.extra.get("sm_scale", 1.0 / math.sqrt(self.head_dim))
+        return float(torch.tensor(v, dtype=torch.float32))
+
+    @sm_scale.setter
+    def sm_scale(self, v: float) -> None:
+        self.extra["sm_scale"] = float(v)
 
 
 def _gen(seed: int, device) -> torch.Generator:
