@@ -100,14 +100,14 @@ bool plan_fast(int batch, int num_heads, int num_kv_heads, int head_dim, int blo
     // of two dividing num_kv_heads)
     int hpw = 1;
     if (u3 && group == 1) hpw = num_kv_heads % 4 == 0 ? 4 : (num_kv_heads % 2 == 0 ? 2 : 1);
-    int nh = u3 ? (hpw > 1 ? kU3MhaHeads : kU3Heads) : 8;
+    int nh = u3 ? (hpw > 1 ? u3_mha_max_heads(hpw) : kU3Heads) : 8;
     while (nh > 1 && (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536)) nh >>= 1;
     if (num_kv_heads % nh != 0 || 2 * nh * block_size * row > 65536) return false;
     while (nh % hpw != 0) hpw >>= 1;
     // 3-bit kernels are register-capped so that several CTAs share an SM; the
     // shared memory (228 KB per SM, 1 KB of it reserved per CTA) and the
     // bytes kept in flight are split between them
-    const int ctas_per_sm = u3 ? u3_ctas_per_sm(hpw, ng) : 1;
+    const int ctas_per_sm = u3 ? u3_ctas_per_sm(hpw, ng, hpw > 1 ? nh / hpw : nh) : 1;
     const int budget = (228 * 1024) / ctas_per_sm - 1024;
     // ring depth: enough bytes in flight per SM, within the shared memory
     int stages = 8;

@@ -242,21 +242,24 @@ struct Tile {
 // The others: CTAs of up to 8 kv heads, one per SM.
 constexpr int kU3Heads = 4;
 constexpr int kU3CtasPerSm = 3;
-// 3-bit multi-head caches with several kv heads per consumer warp: CTAs of
-// (at most) 16 kv heads -- four consumer warps of four heads, 12 KB tensor
-// copies -- two per SM.
-constexpr int kU3MhaHeads = 16;
-constexpr int kU3MhaCtasPerSm = 2;
-// 3-bit CTAs per SM by kv heads per consumer warp and head-column groups
-// (two groups of 8 q heads hold twice the accumulators: two CTAs per SM)
-__host__ __device__ constexpr int u3_ctas_per_sm(int hpw, int ng)
+// 3-bit multi-head caches with HPW kv heads per consumer warp: CTAs of up to
+// 8 HPW kv heads -- eight consumer warps and a producer, one per SM, whose
+// per-block copies are then whole runs of the block's heads (with fewer
+// heads, four consumer warps or fewer: two CTAs per SM).  Their register
+// cap is that of nine warps (three per SM sub-partition: 168).
+__host__ __device__ constexpr int u3_mha_max_heads(int hpw) { return 8 * hpw; }
+// 3-bit CTAs per SM by kv heads per consumer warp, head-column groups and
+// consumer warps (two groups of 8 q heads hold twice the accumulators: two
+// CTAs per SM)
+__host__ __device__ constexpr int u3_ctas_per_sm(int hpw, int ng, int ncons)
 {
-    return hpw > 1 ? kU3MhaCtasPerSm : (ng == 2 ? 2 : kU3CtasPerSm);
+    return hpw > 1 ? (ncons <= 4 ? 2 : 1) : (ng == 2 ? 2 : kU3CtasPerSm);
 }
+// launch bounds: threads per CTA and CTAs per SM the register cap is set for
 template <int CK, int U3H, int NG>
-constexpr int kCtasPerSm = CK == kU3 ? u3_ctas_per_sm(U3H >= 2 ? U3H : 1, NG) : 1;
-template <int CK>
-constexpr int kMaxThreads = CK == kU3 ? 32 * (kU3Heads + 1) : 288;
+constexpr int kCtasPerSm = CK == kU3 && U3H < 2 ? u3_ctas_per_sm(1, NG, kU3Heads) : 1;
+template <int CK, int U3H>
+constexpr int kMaxThreads = CK == kU3 && U3H < 2 ? 32 * (kU3Heads + 1) : 288;
 
 // fp32 conversion area of a 3-bit consumer warp: (sk, zk, sv, zv) per
 // (head, token) of the HPW heads and the tokens of one step (two 16-token
@@ -279,7 +282,7 @@ __host__ __device__ constexpr int u3_conv_bytes_per_warp(int hpw, int bs) { retu
 // columns: every K / V fragment, loaded and converted once, feeds one MMA
 // per group.
 template <int CK, int D, int BS, int U3H = 0, bool GSC = false, bool XV = false, int NG = 1>
-__global__ void __launch_bounds__(kMaxThreads<CK>, (kCtasPerSm<CK, U3H, NG>))
+__global__ void __launch_bounds__((kMaxThreads<CK, U3H>), (kCtasPerSm<CK, U3H, NG>))
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeParams p, FastParams f)
 {
