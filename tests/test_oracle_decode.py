@@ -284,3 +284,30 @@ def test_granular_scale_decode_on_dequantised_cache(orc, mode):
     ref = gather_attention(w.q, kd, vd, w.block_tables.numpy(), w.context_lens.numpy(), BS,
                            w.sm_scale)
     assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def test_scale_edges_zero_and_negative(orc):
+    """sm_scale 0: uniform weights, each row the mean of its V rows;
+    sm_scale -s: the same as +s on the negated query (softmax of -q.k),
+    which is how a negative scale must be read.  Both against the gather
+    reference at the same scale."""
+    w = W.gqa_bf16(batch=3, ctx_lo=1, ctx_hi=70, seed=12, num_heads=4, num_kv_heads=2, head_dim=64)
+    v = _as_f64(W.bits16(w.v_cache0), torch.bfloat16)
+    w.sm_scale = 0.0
+    out0 = _decode16(orc, w)
+    for b in range(3):
+        n = int(w.context_lens[b])
+        rows = [v[int(w.block_tables[b, t // w.block_size]), t % w.block_size] for t in range(n)]
+        mean = np.mean(np.stack(rows), axis=0)
+        for h in range(4):
+            assert np.allclose(out0[b, h], mean[h // 2], rtol=0, atol=1e-12)
+    s = 0.125
+    w.sm_scale = -s
+    neg = _decode16(orc, w)
+    w.sm_scale = s
+    flipped = _decode16(orc, w, q=W.bits16(w.q) ^ np.uint16(0x8000))
+    assert np.max(np.abs(neg - flipped)) < 1e-12
+    w.sm_scale = -s
+    ref = gather_attention(w.q, w.k_cache0, w.v_cache0, w.block_tables.numpy(),
+                           w.context_lens.numpy(), w.block_size, w.sm_scale)
+    assert np.max(np.abs(neg - ref)) < 1e-12
