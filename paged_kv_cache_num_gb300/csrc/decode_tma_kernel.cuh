@@ -823,6 +823,29 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         static_assert(NT <= NTM, "conversion area");
         float4 *cw = reinterpret_cast<float4 *>(smem + L.conv_off) + warp * HPW * NTM;
         __syncwarp();    // the previous step's reads of the area are done
+        if (HPW > 1 && hmaj) {
+            // head-major runs of multi-head warps: a lane takes two
+            // consecutive tokens of one head (an even slot, both in one
+            // stage), loading their two scales and two zeros of K and of V
+            // at once
+            constexpr int NP2 = HPW * NT / 2;
+#pragma unroll
+            for (int i0 = 0; i0 < NP2; i0 += 32) {
+                const int i = i0 + lane;
+                if (i < NP2) {
+                    const int hh = i / (NT / 2), tk = 2 * (i % (NT / 2));
+                    const int st = tk < BS ? s0 : s1, slot = tk & (BS - 1);
+                    const unsigned char *raw = smem + (st * L.stage_bytes + 2 * L.tile_bytes);
+                    const int k = (kvl + hh) * BS + slot;
+                    const float2 ks = __half22float2(*reinterpret_cast<const __half2 *>(raw + 2 * k));
+                    const float2 vs = __half22float2(*reinterpret_cast<const __half2 *>(raw + 2 * BS * MH + 2 * k));
+                    const uint32_t kz = *reinterpret_cast<const uint16_t *>(raw + 4 * BS * MH + k);
+                    const uint32_t vz = *reinterpret_cast<const uint16_t *>(raw + 5 * BS * MH + k);
+                    cw[hh * NTM + tk] = make_float4(ks.x, float(kz & 0xffu), vs.x, float(vz & 0xffu));
+                    cw[hh * NTM + tk + 1] = make_float4(ks.y, float(kz >> 8), vs.y, float(vz >> 8));
+                }
+            }
+        } else {
 #pragma unroll
         for (int i0 = 0; i0 < HPW * NT; i0 += 32) {
             const int i = i0 + lane;
@@ -838,6 +861,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 cw[hh * NTM + tk] =
                     make_float4(__half2float(mks[k]), float(mkz[k]), __half2float(mvs[k]), float(mvz[k]));
             }
+        }
         }
         __syncwarp();
         // conversion entry of score row (tile t, row half r) and head column c
